@@ -1,0 +1,149 @@
+"""float64 CPU oracle of one RACE attention layer -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the smoke check and the CPU-baseline leg of the benchmark may import this
+package. It shares no code with the GPU library and the GPU library never calls it.
+
+Sources: "RACE Attention" slides (paper Algorithm 1, frames "Soft corner assignments make
+hashing differentiable", "Each bucket stores mass and a weighted value sum", "Normalize after
+combining the tables"; paper Algorithm 2, frame "Causality is a prefix update of the same
+statistics") and the reading notes, sections 2.4-2.6.  The C source states every step.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+_i64 = ctypes.c_int64
+_dp = ctypes.POINTER(ctypes.c_double)
+_vp = ctypes.c_void_p
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.race_oracle_max_p.restype = ctypes.c_int
+        L.race_oracle_features.argtypes = [_i64, _i64, _vp, _vp, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_double, ctypes.c_int, _vp, _vp]
+        L.race_oracle_readout_given_phi.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
+                                                    _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp]
+        L.race_oracle_forward.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                          ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
+        L.race_oracle_backward.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                           _vp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                           ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _vp, _vp,
+                                           ctypes.c_int]
+        for f in ("race_oracle_features", "race_oracle_readout_given_phi", "race_oracle_forward",
+                  "race_oracle_backward"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _tokens(a):
+    """Token tensor as (contiguous array, element code). bf16 arrives as uint16 bit patterns."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float64:
+        return a, 0
+    if a.dtype == np.float32:
+        return a, 1
+    if a.dtype == np.uint16:
+        return a, 2
+    raise TypeError("oracle token tensors must be float64, float32 or bf16 bits (uint16)")
+
+
+def _check(status, what):
+    if status != 0:
+        raise ValueError("%s failed with status %d" % (what, status))
+
+
+def features(X, W, beta, normalize=True):
+    """Bucket probabilities of rows X [M, d] for W [L, P, d]: returns (phi [M, L, R], u [M, L, P])."""
+    X = _f64(X)
+    W = _f64(W)
+    M, d = X.shape
+    L, P, _ = W.shape
+    R = 1 << P
+    phi = np.empty((M, L, R))
+    u = np.empty((M, L, P))
+    _check(lib().race_oracle_features(M, d, _ptr(X), _ptr(W), L, P, float(beta), int(normalize),
+                                      _ptr(phi), _ptr(u)), "features")
+    return phi, u
+
+
+def readout_given_phi(phiK, V, phiQ, causal=False):
+    """Sketch + global-ratio read-out with bucket probabilities given directly.
+
+    phiK [L, N, R], V [N, dv], phiQ [L, M, R]. Returns (O [M, dv], mass [L, R], content [L, R, dv]).
+    """
+    phiK, V, phiQ = _f64(phiK), _f64(V), _f64(phiQ)
+    L, N, R = phiK.shape
+    M = phiQ.shape[1]
+    dv = V.shape[1]
+    O = np.empty((M, dv))
+    mass = np.empty((L, R))
+    content = np.empty((L, R, dv))
+    _check(lib().race_oracle_readout_given_phi(N, M, dv, L, R, _ptr(phiK), _ptr(V), _ptr(phiQ),
+                                               int(causal), _ptr(O), _ptr(mass), _ptr(content)),
+           "readout_given_phi")
+    return O, mass, content
+
+
+def _rows(rows):
+    if rows is None:
+        return None, 0
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    return r, r.size
+
+
+def forward(Q, K, V, W, beta, causal, normalize=True, rows=None, want_sketch=False, nthreads=0):
+    """O for Q, K, V [B, H, N, d] (float64/float32/bf16-bits). rows: sorted token rows to output."""
+    Q, e = _tokens(Q)
+    K, e2 = _tokens(K)
+    V, e3 = _tokens(V)
+    assert e == e2 == e3 and Q.shape == K.shape == V.shape
+    W = _f64(W)
+    B, H, N, d = Q.shape
+    L, P, _ = W.shape
+    r, nr = _rows(rows)
+    nout = nr if r is not None else N
+    O = np.empty((B, H, nout, d))
+    sk = np.empty((B, H, L << P, d + 1)) if (want_sketch and not causal) else None
+    _check(lib().race_oracle_forward(B, H, N, d, e, _ptr(Q), _ptr(K), _ptr(V), _ptr(W), L, P,
+                                     float(beta), int(causal), int(normalize), _ptr(r), nr,
+                                     _ptr(O), _ptr(sk), int(nthreads)), "forward")
+    return (O, sk) if want_sketch else O
+
+
+def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0):
+    """(dQ, dK, dV) for the output O and its cotangent dO; rows as in `forward`."""
+    Q, e = _tokens(Q)
+    K, _ = _tokens(K)
+    V, _ = _tokens(V)
+    dO, e4 = _tokens(dO)
+    assert e == e4
+    W = _f64(W)
+    B, H, N, d = Q.shape
+    L, P, _ = W.shape
+    r, nr = _rows(rows)
+    nout = nr if r is not None else N
+    dQ = np.empty((B, H, nout, d))
+    dK = np.empty((B, H, nout, d))
+    dV = np.empty((B, H, nout, d))
+    _check(lib().race_oracle_backward(B, H, N, d, e, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(W),
+                                      L, P, float(beta), int(causal), int(normalize), _ptr(r), nr,
+                                      _ptr(dQ), _ptr(dK), _ptr(dV), int(nthreads)), "backward")
+    return dQ, dK, dV
