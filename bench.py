@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of one RACE attention layer, forward + backward, on GB300.
+
+A step is one forward and one backward pass (every kernel of the path) over one synthetic batch
+of the named workload, through the library's C ABI.  Inputs are resident in HBM when the timed
+region starts; every input tensor is larger than L2 for the default workload, so no flush is
+needed between steps.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle on the host cores (a bounded token prefix of the
+same workload per step) and prints the same line with "impl": "reference".
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RACE attn fwd+bwd tokens/sec at 1 GB300 (H=4,d=128); achieved HBM GB/s vs peak"
+DEFAULT_WORKLOAD = "c5_bf16_causal_12m"
+SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+# Compulsory HBM bytes per (token, head) of each kernel, as (multiples of d * elem_bytes,
+# extra bytes): the token tensors it must read or write once, plus per-token float32 scalars.
+KERNEL_BYTES = {
+    "sketch_keys": (2, 0),        # reads K, V
+    "sketch_grad": (2, 8),        # reads Q, dO and {1/den, dO.O}
+    "readout": (2, 0),            # reads Q, writes O
+    "bwd_query": (3, 8),          # reads Q, dO; writes dQ and {1/den, dO.O}
+    "bwd_key": (4, 0),            # reads K, V; writes dK, dV
+    "causal_fwd": (4, 0),         # reads Q, K, V; writes O
+    "causal_bwd_q": (5, 8),       # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
+    "causal_bwd_kv": (6, 8),      # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ------------------------------------------------------------------ host oracle timing
+
+def oracle_sample_rate(w, target_s, cap_tokens=None):
+    """Time the float64 oracle (forward + backward) on a token prefix of workload w sized to take
+    about target_s seconds; returns (tokens/s, threads used, description)."""
+    import torch
+
+    import oracle
+    from linear_lsh_sketch_gb300.workloads import as_oracle_array, make_inputs
+
+    threads = min(os.cpu_count() or 1, w.B * w.H)
+
+    def run(n):
+        ws = w.scaled(N=n)
+        inp = make_inputs(ws, seed=0, device="cpu")
+        a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V", "dO")}
+        W = inp["W"].double().numpy()
+        t0 = time.perf_counter()
+        oracle.forward(a["Q"], a["K"], a["V"], W, w.beta, w.causal, nthreads=threads)
+        oracle.backward(a["Q"], a["K"], a["V"], a["dO"], W, w.beta, w.causal, nthreads=threads)
+        return time.perf_counter() - t0
+
+    n = min(w.N, 2048)
+    dt = run(n)
+    while dt < 0.5 and n < w.N:
+        n = min(w.N, n * 4)
+        dt = run(n)
+    n_target = int(n * target_s / max(dt, 1e-6))
+    n_final = max(1, min(w.N, n_target, cap_tokens or w.N))
+    if n_final != n:
+        dt = run(n_final)
+        n = n_final
+    rate = w.B * n / dt
+    desc = ("first %d of %d tokens of each of the B*H=%d (batch, head) sequences, forward + backward, "
+            "float64, %.1f s" % (n, w.N, w.B * w.H, dt))
+    return rate, threads, desc, n, dt
+
+
+def run_reference(args, w):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return
+    import oracle
+    from linear_lsh_sketch_gb300.workloads import as_oracle_array, make_inputs
+
+    threads = min(os.cpu_count() or 1, w.B * w.H)
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    _, _, _, n, _ = oracle_sample_rate(w, per_step)
+    ws = w.scaled(N=n)
+    inp = make_inputs(ws, seed=0, device="cpu")
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V", "dO")}
+    W = inp["W"].double().numpy()
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(a["Q"], a["K"], a["V"], W, w.beta, w.causal, nthreads=threads)
+        oracle.backward(a["Q"], a["K"], a["V"], a["dO"], W, w.beta, w.causal, nthreads=threads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = w.B * n * len(times) / total
+    sample = ("first %d of %d tokens of each of the B*H=%d sequences per step (float64 oracle, "
+              "forward + backward)" % (n, w.N, w.B * w.H))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def workload_config(w):
+    return {"workload": w.describe(), "name": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "P": w.P,
+            "L": w.L, "R": w.R, "beta": w.beta, "causal": w.causal, "io_dtype": w.dtype,
+            "accumulate": "f32", "l2": "every input tensor (%.1f GB) is larger than L2; no flush"
+            % (w.B * w.H * w.N * w.d * w.elem_bytes / 1e9)}
+
+
+class ClockSampler:
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, "--query-gpu=" + ",".join(SMI_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(SMI_FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import linear_lsh_sketch_gb300 as race
+    from linear_lsh_sketch_gb300.workloads import make_inputs
+
+    rank, world, local = env_rank()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    race.load_library()
+    hbm_peak, tc_peak, peak_kind = load_peaks()
+
+    # host baseline first (rank 0 only), before the GPU is busy
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, desc, _, _ = oracle_sample_rate(w, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    inp = make_inputs(w, seed=rank, device=dev)
+    Q, K, V, dO, W = inp["Q"], inp["K"], inp["V"], inp["dO"], inp["W"]
+    shape = race.make_shape(w.B, w.H, w.N, w.d, w.torch_dtype)
+    state = torch.empty(race.race_attn_state_bytes(shape, w.L, w.P, w.causal), dtype=torch.uint8, device=dev)
+    ws_bytes = max(race.race_attn_workspace_bytes(shape, w.L, w.P, w.causal, b) for b in (0, 1))
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    O, dQ, dK, dV = (torch.empty_like(Q) for _ in range(4))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        race.race_attn_fwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, O=O, state=state, workspace=workspace)
+        race.race_attn_bwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, dO, O=O, dQ=dQ, dK=dK, dV=dV, state=state,
+                           workspace=workspace)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    uuid = torch.cuda.get_device_properties(dev).uuid
+    uuid = "GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid)
+    race.race_attn_profile_reset()
+    race.race_attn_profile(True)
+    n0 = race.race_attn_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    launches = race.race_attn_launch_count() - n0
+    race.race_attn_profile(False)
+    prof = race.race_attn_profile_read()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    tokens = w.B * w.N
+    value = world * tokens / (ms / 1000.0)
+
+    # dominant kernel and its roofline
+    roof = None
+    if prof:
+        name, (nl, tot) = max(prof.items(), key=lambda kv: kv[1][1])
+        per_launch_ms = tot / max(nl, 1)
+        mult, extra = KERNEL_BYTES.get(name, (0, 0))
+        alg = (mult * w.d * w.elem_bytes + extra) * w.B * w.H * w.N
+        achieved = alg / (per_launch_ms / 1000.0) / 1e9
+        roof = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "peak_kind": peak_kind + " (copy bandwidth)",
+                "algorithmic_bytes_per_launch": alg, "ms_per_launch": per_launch_ms,
+                "traffic": traffic_for(name, w)}
+    kernels = {k: {"launches": v[0], "ms_total": v[1], "share": v[1] / max(1e-9, sum(x[1] for x in prof.values()))}
+               for k, v in prof.items()}
+    step_bytes = 12 * w.d * w.elem_bytes * w.B * w.H * w.N
+    clocks = clk.summary()
+
+    e2e = None
+    if rank == 0 and not args.no_e2e:
+        e2e = measure_e2e(args, w, race, inp, state, workspace)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": workload_config(w), "clocks": clocks, "roofline": roof,
+            "step_hbm": {"algorithmic_bytes": step_bytes, "achieved_gbs": step_bytes / (ms / 1000.0) / 1e9,
+                         "frac": step_bytes / (ms / 1000.0) / 1e9 / hbm_peak,
+                         "note": "12 * d * elem_bytes per (token, head): fwd reads Q,K,V writes O; "
+                                 "bwd reads Q,K,V,O,dO writes dQ,dK,dV"},
+            "kernels": kernels, "gpu_launches": launches, "cpu_baseline": cpu, "e2e": e2e,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def traffic_for(name, w):
+    """Measured DRAM bytes per launch from the committed ncu summary, if it covers this kernel
+    and workload with the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except Exception:
+        return None
+    ent = table.get(name)
+    if not ent or ent.get("workload") != w.name:
+        return None
+    if ent.get("sources_sha") != sources_sha():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def sources_sha():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_lsh_sketch_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measure_e2e(args, w, race, inp, state, workspace):
+    """Same metric end to end through the public API: per step, pinned host -> device copies of
+    Q, K, V, dO, forward + backward, and device -> host copies of O, dQ, dK, dV."""
+    import torch
+
+    dev = inp["Q"].device
+    try:
+        host_in = {k: torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True) for k in ("Q", "K", "V", "dO")}
+        host_out = [torch.empty(inp["Q"].shape, dtype=inp["Q"].dtype, pin_memory=True) for _ in range(4)]
+    except Exception as exc:  # pinned memory unavailable
+        return {"value": None, "unit": "tokens/s", "error": "pinned allocation failed: %s" % exc}
+    for k in host_in:
+        host_in[k].copy_(inp[k])
+    dev_in = {k: torch.empty_like(inp[k]) for k in ("Q", "K", "V", "dO")}
+    W = inp["W"]
+    outs = [torch.empty_like(inp["Q"]) for _ in range(4)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        race.race_attn_fwd(dev_in["Q"], dev_in["K"], dev_in["V"], W, w.beta, w.L, w.P, w.causal, O=outs[0],
+                           state=state, workspace=workspace)
+        race.race_attn_bwd(dev_in["Q"], dev_in["K"], dev_in["V"], W, w.beta, w.L, w.P, w.causal, dev_in["dO"],
+                           O=outs[0], dQ=outs[1], dK=outs[2], dV=outs[3], state=state, workspace=workspace)
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    steps = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = inp["Q"].numel() * inp["Q"].element_size()
+    return {"value": w.B * w.N / (ms / 1000.0), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
+    from linear_lsh_sketch_gb300.workloads import CONFIGS
+    w = CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

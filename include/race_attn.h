@@ -1,0 +1,121 @@
+/*
+ * race_attn.h -- C ABI of the GB300 (sm_103a) RACE attention library, librace_attn.so.
+ *
+ * RACE attention ("RACE Attention" slides, arXiv:2510.04008v5; frames "Soft corner assignments
+ * make hashing differentiable", "Each bucket stores mass and a weighted value sum", "Normalize
+ * after combining the tables", "Causality is a prefix update of the same statistics"; reading
+ * notes sections 2.4-2.6).  For each of L tables with Gaussian hyperplanes W^(l) (P x d):
+ *
+ *     xhat = x / |x|                                  (each Q and K row; a zero row stays zero)
+ *     u^(l)(x) = tanh(W^(l) xhat)                     (P numbers)
+ *     phi^(l)_r(x) = softmax_r(beta * u^(l)(x) . v_r) (R = 2^P corners v_r of {-1,+1}^P,
+ *                                                      v_{r,t} = +1 iff bit t of r is set)
+ *     A^(l) = Phi_K^(l)T V   (R x d, bucket content),   B^(l) = Phi_K^(l)T 1   (R, bucket mass)
+ *     O_i = sum_l phi^(l)(Q_i) A^(l) / sum_l phi^(l)(Q_i) B^(l)
+ *
+ * The causal variant (paper Algorithm 2) replaces A and B by inclusive prefix sums: key t is
+ * added to the sketch before query t reads it.
+ *
+ * Conventions shared by every entry point
+ *  - Token tensors Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d], contiguous, d innermost, of
+ *    element type `shape->dtype` (float32 or bfloat16), on the current CUDA device, 16-byte
+ *    aligned.  Outputs are rounded to nearest-even from float32 arithmetic.
+ *  - W is float32 [L, P, d] on the device, shared by Q and K, by all tables' rows, and by all
+ *    (b, h).  beta is a finite scalar >= 0.
+ *  - Limits: N >= 1; B * H <= 65535; d a multiple of 8 in [8, 128]; 1 <= P <= 8; 1 <= L <= 16;
+ *    L * 2^P <= 256.
+ *  - The caller owns every buffer, including `workspace` (size from race_attn_workspace_bytes)
+ *    and `state` (size from race_attn_state_bytes).  The library allocates no device memory.
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *    stream) and the calls return without synchronising.  Calls that share a workspace must
+ *    not overlap on the device.
+ *  - Results are deterministic: the same inputs give bitwise identical outputs (fixed-order
+ *    reductions, no floating-point atomics).
+ *  - Return value: RACE_OK (0) or a negative race_status.  Argument checks happen before any
+ *    launch; on an error nothing has been enqueued unless the status is RACE_ERR_CUDA.
+ */
+#ifndef RACE_ATTN_H
+#define RACE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { RACE_F32 = 0, RACE_BF16 = 1 } race_dtype;
+
+typedef enum {
+    RACE_OK = 0,
+    RACE_ERR_INVALID_ARG = -1, /* null pointer, shape or parameter outside the limits above   */
+    RACE_ERR_UNSUPPORTED = -2, /* valid arguments this build has no kernel for               */
+    RACE_ERR_WORKSPACE = -3,   /* workspace_bytes smaller than race_attn_workspace_bytes()   */
+    RACE_ERR_CUDA = -4,        /* a CUDA launch or runtime call failed                        */
+    RACE_ERR_ALIGN = -5        /* a tensor pointer is not 16-byte aligned                     */
+} race_status;
+
+/* Token-tensor shape and element type. */
+typedef struct {
+    int64_t B, H, N, d;
+    int32_t dtype; /* race_dtype */
+} race_shape;
+
+/*
+ * Bytes of scratch memory race_attn_fwd (is_bwd = 0) or race_attn_bwd (is_bwd = 1) needs for
+ * this problem.  Returns 0 if the arguments are invalid.  Pure host function.
+ */
+size_t race_attn_workspace_bytes(const race_shape *shape, int L, int P, int causal, int is_bwd);
+
+/*
+ * Bytes of the optional saved-sketch buffer `state`: non-causal, the final [A | B] per (b, h)
+ * as float32 [B, H, L*2^P, d+1] (columns 0..d-1 = A, column d = B); causal, the sketch at the
+ * start of each of the library's sequence segments, float32 [B, H, nseg, L*2^P, d+1], where
+ * nseg is a function of the shape only.  Returns 0 if the arguments are invalid.
+ */
+size_t race_attn_state_bytes(const race_shape *shape, int L, int P, int causal);
+
+/*
+ * Forward pass: O = RACE attention of (Q, K, V) with hyperplanes W and sharpness beta.
+ * state: NULL, or a buffer of race_attn_state_bytes() that receives the saved sketch for a
+ * later race_attn_bwd call with the same inputs.
+ */
+int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const void *V,
+                  const float *W, float beta, int L, int P, int causal, void *O, void *state,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward pass: given the output cotangent dO, writes dQ, dK, dV (all [B, H, N, d]).
+ * O: the forward output.  It may be NULL: the kernels recompute what they need of O
+ * (dO . O per row) from the sketch, which is cheaper than reading it.
+ * state: NULL (the sketch is recomputed from K and V), or the buffer a race_attn_fwd call
+ * with the same Q, K, V, W, beta, L, P and causal filled in.
+ * Gradients with respect to W and beta are not produced.
+ */
+int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const void *V,
+                  const float *W, float beta, int L, int P, int causal, const void *O,
+                  const void *dO, void *dQ, void *dK, void *dV, const void *state,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static description of a status code. */
+const char *race_attn_strerror(int status);
+
+/*
+ * Instrumentation (host-side, process-wide; off by default).
+ * race_attn_launch_count: number of kernels this library has launched so far.
+ * race_attn_profile(1) makes every later launch record a CUDA event pair on its stream;
+ * race_attn_profile_read(i, ...) synchronises on the recorded events and reports, for kernel
+ * name i (0 <= i < count returned), its launches and summed device milliseconds.  Returns the
+ * number of distinct kernel names seen, or -1 if i is out of range.  race_attn_profile(0)
+ * stops recording; race_attn_profile_reset() clears the table.  Not thread-safe.
+ */
+uint64_t race_attn_launch_count(void);
+int race_attn_profile(int enable);
+int race_attn_profile_read(int i, const char **name, int64_t *launches, double *total_ms);
+void race_attn_profile_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RACE_ATTN_H */

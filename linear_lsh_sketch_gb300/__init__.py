@@ -1,0 +1,202 @@
+"""Python binding of librace_attn.so, the GB300 (sm_103a) RACE attention library.
+
+Argument marshalling only: every step of the computation runs in the library's CUDA kernels.
+The function names are those of the C ABI in include/race_attn.h, which states the contract of
+each call.  PyTorch supplies device memory and the current stream; tensors are passed by
+pointer.  There is no fallback: if the compiled library is missing, importing it raises.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "RaceAttnError", "race_attn_fwd", "race_attn_bwd", "race_attn_workspace_bytes",
+    "race_attn_state_bytes", "race_attn_strerror", "race_attn_launch_count", "race_attn_profile",
+    "race_attn_profile_read", "race_attn_profile_reset", "library_path", "load_library",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "librace_attn.so")
+
+RACE_F32, RACE_BF16 = 0, 1
+_DTYPES = {torch.float32: RACE_F32, torch.bfloat16: RACE_BF16}
+
+_lib = None
+
+
+class RaceAttnError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, race_attn_strerror(status), status))
+
+
+class race_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("d", ctypes.c_int64), ("dtype", ctypes.c_int32)]
+
+
+def load_library():
+    """Load librace_attn.so (built in-tree by __graft_entry__.build / build.py); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise ImportError("librace_attn.so is not built (expected at %s); run "
+                          "`python -m linear_lsh_sketch_gb300.build`" % library_path)
+    L = ctypes.CDLL(library_path)
+    vp, sz, i, f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+    shp = ctypes.POINTER(race_shape)
+    L.race_attn_workspace_bytes.argtypes = [shp, i, i, i, i]
+    L.race_attn_workspace_bytes.restype = sz
+    L.race_attn_state_bytes.argtypes = [shp, i, i, i]
+    L.race_attn_state_bytes.restype = sz
+    L.race_attn_fwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, sz, vp]
+    L.race_attn_fwd.restype = i
+    L.race_attn_bwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.race_attn_bwd.restype = i
+    L.race_attn_strerror.argtypes = [i]
+    L.race_attn_strerror.restype = ctypes.c_char_p
+    L.race_attn_launch_count.argtypes = []
+    L.race_attn_launch_count.restype = ctypes.c_uint64
+    L.race_attn_profile.argtypes = [i]
+    L.race_attn_profile.restype = i
+    L.race_attn_profile_read.argtypes = [i, ctypes.POINTER(ctypes.c_char_p),
+                                         ctypes.POINTER(ctypes.c_int64),
+                                         ctypes.POINTER(ctypes.c_double)]
+    L.race_attn_profile_read.restype = i
+    L.race_attn_profile_reset.argtypes = []
+    L.race_attn_profile_reset.restype = None
+    _lib = L
+    return L
+
+
+def make_shape(B, H, N, d, dtype):
+    code = _DTYPES.get(dtype, dtype) if not isinstance(dtype, int) else dtype
+    return race_shape(int(B), int(H), int(N), int(d), int(code))
+
+
+def _shape_of(Q):
+    if Q.dim() != 4:
+        raise ValueError("token tensors must be [B, H, N, d]")
+    if Q.dtype not in _DTYPES:
+        raise TypeError("token tensors must be float32 or bfloat16")
+    B, H, N, d = Q.shape
+    return make_shape(B, H, N, d, Q.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_like(name, t, ref):
+    if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
+        raise ValueError("%s must match Q in shape, dtype and device" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def race_attn_workspace_bytes(shape, L, P, causal, is_bwd):
+    return load_library().race_attn_workspace_bytes(ctypes.byref(shape), int(L), int(P), int(causal),
+                                                    int(is_bwd))
+
+
+def race_attn_state_bytes(shape, L, P, causal):
+    return load_library().race_attn_state_bytes(ctypes.byref(shape), int(L), int(P), int(causal))
+
+
+def race_attn_strerror(status):
+    return load_library().race_attn_strerror(int(status)).decode()
+
+
+def race_attn_launch_count():
+    return int(load_library().race_attn_launch_count())
+
+
+def race_attn_profile(enable):
+    return load_library().race_attn_profile(int(bool(enable)))
+
+
+def race_attn_profile_reset():
+    load_library().race_attn_profile_reset()
+
+
+def race_attn_profile_read():
+    """{kernel name: (launches, total device ms)} for the launches recorded since the last reset."""
+    L = load_library()
+    out = {}
+    name = ctypes.c_char_p()
+    n_l = ctypes.c_int64()
+    ms = ctypes.c_double()
+    n = L.race_attn_profile_read(0, ctypes.byref(name), ctypes.byref(n_l), ctypes.byref(ms))
+    for i in range(max(n, 0)):
+        L.race_attn_profile_read(i, ctypes.byref(name), ctypes.byref(n_l), ctypes.byref(ms))
+        out[name.value.decode()] = (int(n_l.value), float(ms.value))
+    return out
+
+
+def _bytes_buffer(nbytes, device, given):
+    if given is not None:
+        return given
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def race_attn_fwd(Q, K, V, W, beta, L, P, causal, O=None, state=None, workspace=None, stream=None):
+    """O = RACE attention of Q, K, V ([B, H, N, d], float32 or bfloat16, CUDA); W float32 [L, P, d].
+
+    O, state and workspace are allocated with torch when not given.  Returns O.
+    """
+    shape = _shape_of(Q)
+    _check_like("K", K, Q)
+    _check_like("V", V, Q)
+    _check_like("Q", Q, Q)
+    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
+        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
+    if O is None:
+        O = torch.empty_like(Q)
+    _check_like("O", O, Q)
+    ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 0)
+    if ws_bytes == 0:
+        raise RaceAttnError(-1, "race_attn_fwd")
+    workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
+    rc = load_library().race_attn_fwd(
+        ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
+        int(causal), _ptr(O), _ptr(state), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    if rc != 0:
+        raise RaceAttnError(rc, "race_attn_fwd")
+    return O
+
+
+def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, dV=None, state=None,
+                  workspace=None, stream=None):
+    """(dQ, dK, dV) of RACE attention for the output cotangent dO; allocates what is not given."""
+    shape = _shape_of(Q)
+    for n, t in (("K", K), ("V", V), ("dO", dO), ("Q", Q)):
+        _check_like(n, t, Q)
+    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
+        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(Q) if dK is None else dK
+    dV = torch.empty_like(Q) if dV is None else dV
+    for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        _check_like(n, t, Q)
+    ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 1)
+    if ws_bytes == 0:
+        raise RaceAttnError(-1, "race_attn_bwd")
+    workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
+    rc = load_library().race_attn_bwd(
+        ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
+        int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(state), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != 0:
+        raise RaceAttnError(rc, "race_attn_bwd")
+    return dQ, dK, dV

@@ -1,0 +1,356 @@
+// race_api.cu -- the C ABI of librace_attn.so: argument checks, work planning, workspace
+// carving and kernel dispatch.  Declarations and the contract of each entry point are in
+// include/race_attn.h.
+#include <cmath>
+#include <string>
+#include <type_traits>
+#include <vector>
+
+#include "race_attn.h"
+#include "race_launch.h"
+
+namespace race {
+
+// ------------------------------------------------------------------ instrumentation
+
+namespace {
+
+struct ProfEntry {
+    std::string name;
+    int64_t launches = 0;
+    double ms = 0.0;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending;
+};
+
+uint64_t g_launches = 0;
+bool g_profiling = false;
+std::vector<ProfEntry> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+cudaEvent_t g_open_start = nullptr;
+
+cudaEvent_t take_event()
+{
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+ProfEntry &entry(const char *name)
+{
+    for (auto &p : g_prof)
+        if (p.name == name) return p;
+    g_prof.push_back(ProfEntry{});
+    g_prof.back().name = name;
+    return g_prof.back();
+}
+
+void drain()
+{
+    for (auto &p : g_prof) {
+        for (auto &ev : p.pending) {
+            float ms = 0.f;
+            if (cudaEventSynchronize(ev.second) == cudaSuccess &&
+                cudaEventElapsedTime(&ms, ev.first, ev.second) == cudaSuccess) {
+                p.ms += ms;
+                p.launches += 1;
+            }
+            g_event_pool.push_back(ev.first);
+            g_event_pool.push_back(ev.second);
+        }
+        p.pending.clear();
+    }
+}
+
+}  // namespace
+
+void prof_before(const char *, cudaStream_t st)
+{
+    ++g_launches;
+    if (!g_profiling) return;
+    g_open_start = take_event();
+    if (g_open_start) cudaEventRecord(g_open_start, st);
+}
+
+void prof_after(const char *name, cudaStream_t st)
+{
+    if (!g_profiling || !g_open_start) return;
+    cudaEvent_t e1 = take_event();
+    if (!e1) return;
+    cudaEventRecord(e1, st);
+    entry(name).pending.emplace_back(g_open_start, e1);
+    g_open_start = nullptr;
+}
+
+// ------------------------------------------------------------------ planning
+
+namespace {
+
+constexpr int kSMs = 152;
+constexpr size_t kMaxSmem = 227 * 1024;
+
+struct Plan {
+    Dims D{};
+    bool causal = false, bf16 = false;
+    int nsplit = 1;        // token ranges (non-causal) or segments (causal) per (b, h)
+    int64_t seg_len = 0;   // tokens per range, a multiple of the token tile
+    size_t E = 0;          // floats per sketch: LR * (d + 1)
+    size_t off_part = 0, off_sk = 0, off_gpart = 0, off_gsk = 0, off_aux = 0;
+    size_t ws_fwd = 0, ws_bwd = 0, state = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
+{
+    if (!s) return RACE_ERR_INVALID_ARG;
+    if (s->B < 1 || s->H < 1 || s->N < 1) return RACE_ERR_INVALID_ARG;  // B * H <= 65535 below
+    if (s->d < 8 || s->d > kMaxD || s->d % 8 != 0) return RACE_ERR_INVALID_ARG;
+    if (P < 1 || P > kMaxP || L < 1 || L > kMaxL) return RACE_ERR_INVALID_ARG;
+    if ((L << P) > kMaxLR) return RACE_ERR_INVALID_ARG;
+    if (s->dtype != RACE_F32 && s->dtype != RACE_BF16) return RACE_ERR_INVALID_ARG;
+    if (s->B > 65535 || s->H > 65535 || s->B * s->H > 65535 || s->N > ((int64_t)1 << 40) / (s->B * s->H))
+        return RACE_ERR_INVALID_ARG;
+    Dims &D = pl.D;
+    D.BH = s->B * s->H;
+    D.N = s->N;
+    D.d = (int)s->d;
+    D.L = L;
+    D.P = P;
+    D.R = 1 << P;
+    D.LR = L << P;
+    D.LP = L * P;
+    D.dv = D.d + 1;
+    D.beta = 0.f;
+    pl.causal = causal != 0;
+    pl.bf16 = s->dtype == RACE_BF16;
+    pl.E = (size_t)D.LR * D.dv;
+
+    const int TT = 64;  // segment granule: a multiple of every kernel's token tile
+    const int64_t ntiles = ceil_div(D.N, TT);
+    int64_t want;
+    if (!pl.causal) {
+        const int64_t chunks = ceil_div(D.LR, 64);
+        want = ceil_div(4 * kSMs, chunks * D.BH);
+    } else {
+        want = ceil_div(2 * kSMs, D.BH);
+    }
+    want = std::max<int64_t>(1, std::min(want, ntiles));
+    pl.seg_len = ceil_div(ceil_div(D.N, want), TT) * TT;
+    pl.nsplit = (int)ceil_div(D.N, pl.seg_len);
+
+    const size_t sk_one = pl.E * sizeof(float);
+    const size_t per_split = (size_t)D.BH * pl.nsplit * sk_one;
+    const size_t per_bh = (size_t)D.BH * sk_one;
+    pl.off_part = 0;
+    pl.off_sk = align256(pl.off_part + per_split);
+    const size_t sk_bytes = pl.causal ? per_split : per_bh;
+    pl.ws_fwd = align256(pl.off_sk + sk_bytes);
+    pl.off_gpart = pl.ws_fwd;
+    pl.off_gsk = align256(pl.off_gpart + per_split);
+    pl.off_aux = align256(pl.off_gsk + sk_bytes);
+    pl.ws_bwd = align256(pl.off_aux + (size_t)D.BH * D.N * sizeof(float2));
+    pl.state = sk_bytes;
+
+    // every kernel of the chosen path must fit in shared memory
+    if (pl.causal) {
+        if (generic_smem_bytes(D, GenericKernel::CausalBwd) > kMaxSmem ||
+            generic_smem_bytes(D, GenericKernel::CausalFwd) > kMaxSmem)
+            return RACE_ERR_UNSUPPORTED;
+    } else {
+        if (generic_smem_bytes(D, GenericKernel::QueryBwd) > kMaxSmem ||
+            generic_smem_bytes(D, GenericKernel::KeyBwd) > kMaxSmem ||
+            generic_smem_bytes(D, GenericKernel::Readout) > kMaxSmem)
+            return RACE_ERR_UNSUPPORTED;
+    }
+    if (generic_smem_bytes(D, GenericKernel::Sketch) > kMaxSmem) return RACE_ERR_UNSUPPORTED;
+    return RACE_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+int check_beta(float beta) { return (std::isfinite(beta) && beta >= 0.f) ? RACE_OK : RACE_ERR_INVALID_ARG; }
+
+#define RACE_TRY(expr)                                   \
+    do {                                                 \
+        cudaError_t e_ = (expr);                         \
+        if (e_ != cudaSuccess) return RACE_ERR_CUDA;     \
+    } while (0)
+
+template <typename T>
+bool use_tc(const Plan &pl)
+{
+    if (!std::is_same<T, bf16_t>::value) return false;
+    return pl.causal && causal_tc_supported(pl.D);
+}
+
+template <typename T>
+int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float *W, T *O, float *state,
+                 char *ws, cudaStream_t st)
+{
+    const Dims &D = pl.D;
+    float *part = (float *)(ws + pl.off_part);
+    float *S = state ? state : (float *)(ws + pl.off_sk);
+    if constexpr (std::is_same<T, bf16_t>::value) {
+        if (use_tc<T>(pl)) {
+            RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, st));
+            RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
+            RACE_TRY(launch_causal_tc_fwd(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, st));
+            return RACE_OK;
+        }
+    }
+    RACE_TRY(launch_sketch<T>(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, 0, st));
+    if (!pl.causal) {
+        RACE_TRY(launch_combine(D, part, S, pl.nsplit, 0, st));
+        RACE_TRY(launch_readout<T>(D, Q, W, S, O, st));
+    } else {
+        RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
+        RACE_TRY(launch_causal_fwd<T>(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, st));
+    }
+    return RACE_OK;
+}
+
+template <typename T>
+int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float *W, const T *dO, T *dQ, T *dK,
+                  T *dV, const float *state, char *ws, cudaStream_t st)
+{
+    const Dims &D = pl.D;
+    float *part = (float *)(ws + pl.off_part);
+    float *gpart = (float *)(ws + pl.off_gpart);
+    float *gsk = (float *)(ws + pl.off_gsk);
+    float2 *aux = (float2 *)(ws + pl.off_aux);
+    const float *S = state;
+    if (!S) {
+        float *Sw = (float *)(ws + pl.off_sk);
+        RACE_TRY(launch_sketch<T>(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, 0, st));
+        RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, pl.causal ? 1 : 0, st));
+        S = Sw;
+    }
+    if (!pl.causal) {
+        RACE_TRY(launch_bwd_query<T>(D, Q, dO, W, S, dQ, aux, st));
+        RACE_TRY(launch_sketch<T>(D, Q, dO, aux, W, pl.seg_len, pl.nsplit, gpart, 1, st));
+        RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 0, st));
+        RACE_TRY(launch_bwd_key<T>(D, K, V, W, gsk, dK, dV, st));
+    } else {
+        RACE_TRY(launch_causal_bwd_q<T>(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, st));
+        RACE_TRY(launch_sketch<T>(D, Q, dO, aux, W, pl.seg_len, pl.nsplit, gpart, 1, st));
+        RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
+        RACE_TRY(launch_causal_bwd_kv<T>(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, st));
+    }
+    return RACE_OK;
+}
+
+}  // namespace
+}  // namespace race
+
+using namespace race;
+
+extern "C" {
+
+size_t race_attn_workspace_bytes(const race_shape *shape, int L, int P, int causal, int is_bwd)
+{
+    Plan pl;
+    if (make_plan(shape, L, P, causal, pl) != RACE_OK) return 0;
+    return is_bwd ? pl.ws_bwd : pl.ws_fwd;
+}
+
+size_t race_attn_state_bytes(const race_shape *shape, int L, int P, int causal)
+{
+    Plan pl;
+    if (make_plan(shape, L, P, causal, pl) != RACE_OK) return 0;
+    return pl.state;
+}
+
+int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const void *V, const float *W, float beta,
+                  int L, int P, int causal, void *O, void *state, void *workspace, size_t workspace_bytes,
+                  void *stream)
+{
+    Plan pl;
+    int rc = make_plan(shape, L, P, causal, pl);
+    if (rc != RACE_OK) return rc;
+    if ((rc = check_beta(beta)) != RACE_OK) return rc;
+    if (!Q || !K || !V || !W || !O || !workspace) return RACE_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(W) || !aligned16(O) ||
+        !aligned16(workspace) || (state && !aligned16(state)))
+        return RACE_ERR_ALIGN;
+    if (workspace_bytes < pl.ws_fwd) return RACE_ERR_WORKSPACE;
+    pl.D.beta = beta;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (pl.bf16)
+        return forward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
+                                           (const __nv_bfloat16 *)V, W, (__nv_bfloat16 *)O, (float *)state,
+                                           (char *)workspace, st);
+    return forward_impl<float>(pl, (const float *)Q, (const float *)K, (const float *)V, W, (float *)O,
+                               (float *)state, (char *)workspace, st);
+}
+
+int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const void *V, const float *W, float beta,
+                  int L, int P, int causal, const void *O, const void *dO, void *dQ, void *dK, void *dV,
+                  const void *state, void *workspace, size_t workspace_bytes, void *stream)
+{
+    (void)O;
+    Plan pl;
+    int rc = make_plan(shape, L, P, causal, pl);
+    if (rc != RACE_OK) return rc;
+    if ((rc = check_beta(beta)) != RACE_OK) return rc;
+    if (!Q || !K || !V || !W || !dO || !dQ || !dK || !dV || !workspace) return RACE_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(W) || !aligned16(dO) || !aligned16(dQ) ||
+        !aligned16(dK) || !aligned16(dV) || !aligned16(workspace) || (state && !aligned16(state)))
+        return RACE_ERR_ALIGN;
+    if (workspace_bytes < pl.ws_bwd) return RACE_ERR_WORKSPACE;
+    pl.D.beta = beta;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (pl.bf16)
+        return backward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
+                                            (const __nv_bfloat16 *)V, W, (const __nv_bfloat16 *)dO,
+                                            (__nv_bfloat16 *)dQ, (__nv_bfloat16 *)dK, (__nv_bfloat16 *)dV,
+                                            (const float *)state, (char *)workspace, st);
+    return backward_impl<float>(pl, (const float *)Q, (const float *)K, (const float *)V, W, (const float *)dO,
+                                (float *)dQ, (float *)dK, (float *)dV, (const float *)state, (char *)workspace, st);
+}
+
+const char *race_attn_strerror(int status)
+{
+    switch (status) {
+        case RACE_OK: return "ok";
+        case RACE_ERR_INVALID_ARG: return "invalid argument";
+        case RACE_ERR_UNSUPPORTED: return "unsupported problem size for this build";
+        case RACE_ERR_WORKSPACE: return "workspace too small";
+        case RACE_ERR_CUDA: return "CUDA launch or runtime error";
+        case RACE_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+        default: return "unknown status";
+    }
+}
+
+uint64_t race_attn_launch_count(void) { return g_launches; }
+
+int race_attn_profile(int enable)
+{
+    g_profiling = enable != 0;
+    return RACE_OK;
+}
+
+int race_attn_profile_read(int i, const char **name, int64_t *launches, double *total_ms)
+{
+    drain();
+    const int n = (int)g_prof.size();
+    if (i < 0 || i >= n) return i == 0 && n == 0 ? 0 : -1;
+    if (name) *name = g_prof[i].name.c_str();
+    if (launches) *launches = g_prof[i].launches;
+    if (total_ms) *total_ms = g_prof[i].ms;
+    return n;
+}
+
+void race_attn_profile_reset(void)
+{
+    drain();
+    g_prof.clear();
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// race_common.cuh -- types shared by the RACE attention kernels and their host launchers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace race {
+
+using bf16_t = __nv_bfloat16;
+
+constexpr int kMaxP = 8;     // hyperplanes per table
+constexpr int kMaxL = 16;    // tables
+constexpr int kMaxLR = 256;  // L * 2^P, the width of the concatenated bucket-feature vector
+constexpr int kMaxD = 128;   // head dimension
+
+// Problem dimensions as the kernels see them.  dv = d + 1: a sketch row holds the d content
+// columns (A = Phi_K^T V) followed by the mass column (B = Phi_K^T 1).
+struct Dims {
+    int64_t BH;  // B * H independent (batch, head) problems
+    int64_t N;   // tokens per problem
+    int d, L, P, R, LR, LP, dv;
+    float beta;
+};
+
+__device__ __forceinline__ float ld_f(const float *p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_f(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void st_f(float *p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_f(__nv_bfloat16 *p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+// Bump allocator for dynamic shared memory layouts, usable on host (to size the launch) and
+// device (to find the regions); every region starts on a 16-byte boundary.
+struct SmemLayout {
+    int used = 0;  // in floats
+    __host__ __device__ int take(int nfloats) {
+        int at = used;
+        used += (nfloats + 3) & ~3;
+        return at;
+    }
+    __host__ __device__ size_t bytes() const { return (size_t)used * sizeof(float); }
+};
+
+}  // namespace race

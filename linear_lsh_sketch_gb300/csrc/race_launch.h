@@ -1,0 +1,62 @@
+// race_launch.h -- host-side launchers of the RACE attention kernels (internal to the library).
+#pragma once
+
+#include <algorithm>
+
+#include "race_common.cuh"
+
+namespace race {
+
+// Instrumentation hooks implemented next to the C ABI: a launch counter and optional CUDA
+// event pairs around each launch.
+void prof_before(const char *name, cudaStream_t st);
+void prof_after(const char *name, cudaStream_t st);
+
+template <typename Kern, typename... Args>
+cudaError_t launch_kernel(const char *name, Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          Args... args)
+{
+    prof_before(name, st);
+    k<<<grid, block, smem, st>>>(args...);
+    cudaError_t e = cudaGetLastError();
+    prof_after(name, st);
+    return e;
+}
+
+// ---------------------------------------------------------------- CUDA-core kernels
+enum class GenericKernel { Sketch, Readout, QueryBwd, KeyBwd, CausalFwd, CausalBwd };
+size_t generic_smem_bytes(const Dims &D, GenericKernel which);
+int generic_token_tile();
+
+template <typename T>
+cudaError_t launch_sketch(const Dims &D, const T *X, const T *Y, const float2 *aux, const float *W,
+                          int64_t seg_len, int nsplit, float *part, int mode, cudaStream_t st);
+cudaError_t launch_combine(const Dims &D, const float *part, float *out, int nsplit, int mode, cudaStream_t st);
+template <typename T>
+cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const float *S, T *O, cudaStream_t st);
+template <typename T>
+cudaError_t launch_bwd_query(const Dims &D, const T *Q, const T *dO, const float *W, const float *S, T *dQ,
+                             float2 *aux, cudaStream_t st);
+template <typename T>
+cudaError_t launch_bwd_key(const Dims &D, const T *K, const T *V, const float *W, const float *G, T *dK, T *dV,
+                           cudaStream_t st);
+template <typename T>
+cudaError_t launch_causal_fwd(const Dims &D, const T *Q, const T *K, const T *V, const float *W, const float *S0,
+                              int64_t seg_len, int nseg, T *O, cudaStream_t st);
+template <typename T>
+cudaError_t launch_causal_bwd_q(const Dims &D, const T *Q, const T *K, const T *V, const T *dO, const float *W,
+                                const float *S0, int64_t seg_len, int nseg, T *dQ, float2 *aux, cudaStream_t st);
+template <typename T>
+cudaError_t launch_causal_bwd_kv(const Dims &D, const T *Q, const T *K, const T *V, const T *dO,
+                                 const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
+                                 T *dK, T *dV, cudaStream_t st);
+
+// ---------------------------------------------------------------- tensor-core causal path (bf16)
+bool causal_tc_supported(const Dims &D);
+int causal_tc_chunk();
+cudaError_t launch_causal_tc_totals(const Dims &D, const bf16_t *K, const bf16_t *V, const float *W,
+                                    int64_t seg_len, int nseg, float *Sout, cudaStream_t st);
+cudaError_t launch_causal_tc_fwd(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const float *W,
+                                 const float *S0, int64_t seg_len, int nseg, bf16_t *O, cudaStream_t st);
+
+}  // namespace race

@@ -3,12 +3,13 @@
 Plain gcc with OpenMP; no flags that reorder floating-point arithmetic.
 """
 import os
+import platform
 import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "race_oracle.c")
-LIB = os.path.join(HERE, "_race_oracle.so")
+LIB = os.path.join(HERE, "_race_oracle.%s.so" % platform.machine())
 
 
 def build(force: bool = False) -> str:

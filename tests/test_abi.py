@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every entry point the
+header declares, sizes its buffers, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_lsh_sketch_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "race_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    import linear_lsh_sketch_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(race_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("race_attn_fwd", "race_attn_bwd", "race_attn_workspace_bytes", "race_attn_state_bytes",
+              "race_attn_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.library_path)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def shape(lib, B=1, H=2, N=100, d=64, dtype=1):
+    return lib.make_shape(B, H, N, d, dtype)
+
+
+def test_sizes(lib):
+    s = shape(lib)
+    for causal in (0, 1):
+        f = lib.race_attn_workspace_bytes(s, 3, 3, causal, 0)
+        b = lib.race_attn_workspace_bytes(s, 3, 3, causal, 1)
+        st = lib.race_attn_state_bytes(s, 3, 3, causal)
+        assert 0 < f <= b
+        assert st >= 2 * 24 * 65 * 4  # at least one [A | B] per (b, h)
+        assert st % (24 * 65 * 4) == 0
+    # the saved sketch is one [LR, d+1] float32 block per (b, h) when non-causal
+    assert lib.race_attn_state_bytes(s, 3, 3, 0) == 2 * 24 * 65 * 4
+    # sizes depend on the shape only
+    assert lib.race_attn_state_bytes(s, 3, 3, 1) == lib.race_attn_state_bytes(shape(lib), 3, 3, 1)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(d=65), dict(d=0), dict(d=136), dict(N=0), dict(B=0), dict(dtype=7),
+    dict(P=0), dict(P=9), dict(L=0), dict(L=17), dict(P=7, L=4),
+])
+def test_invalid_sizes_report_zero(lib, bad):
+    P, L = bad.pop("P", 3), bad.pop("L", 3)
+    s = shape(lib, **bad)
+    assert lib.race_attn_workspace_bytes(s, L, P, 0, 1) == 0
+    assert lib.race_attn_state_bytes(s, L, P, 1) == 0
+
+
+def _raw(lib):
+    return lib.load_library()
+
+
+def test_fwd_rejects_before_launch(lib):
+    """Argument errors return a status without touching the GPU (safe on a machine without one)."""
+    L = _raw(lib)
+    s = shape(lib)
+    p = ctypes.c_void_p(4096)  # an aligned, never-dereferenced address
+    ws = lib.race_attn_workspace_bytes(s, 3, 3, 0, 0)
+    fwd = lambda *a: L.race_attn_fwd(*a)
+    assert fwd(None, p, p, p, p, 10.0, 3, 3, 0, p, None, p, ws, None) == -1
+    assert fwd(ctypes.byref(s), None, p, p, p, 10.0, 3, 3, 0, p, None, p, ws, None) == -1
+    assert fwd(ctypes.byref(s), p, p, p, p, float("nan"), 3, 3, 0, p, None, p, ws, None) == -1
+    assert fwd(ctypes.byref(s), p, p, p, p, -1.0, 3, 3, 0, p, None, p, ws, None) == -1
+    assert fwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 9, 0, p, None, p, ws, None) == -1
+    assert fwd(ctypes.byref(s), ctypes.c_void_p(4097), p, p, p, 10.0, 3, 3, 0, p, None, p, ws, None) == -5
+    assert fwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 0, p, None, p, ws - 1, None) == -3
+
+
+def test_bwd_rejects_before_launch(lib):
+    L = _raw(lib)
+    s = shape(lib)
+    p = ctypes.c_void_p(4096)
+    ws = lib.race_attn_workspace_bytes(s, 3, 3, 1, 1)
+    bwd = lambda *a: L.race_attn_bwd(*a)
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, None, p, p, p, None, p, ws, None) == -1
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, None, p, ws - 256, None) == -3
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, ctypes.c_void_p(4104), p, None, p, ws,
+               None) == -5
+
+
+def test_strerror(lib):
+    assert lib.race_attn_strerror(0) == "ok"
+    for rc in (-1, -2, -3, -4, -5):
+        assert lib.race_attn_strerror(rc) not in ("ok", "unknown status")
+    assert lib.race_attn_strerror(-99) == "unknown status"
+
+
+def test_instrumentation_defaults(lib):
+    assert lib.race_attn_launch_count() >= 0
+    lib.race_attn_profile_reset()
+    assert lib.race_attn_profile_read() == {}
