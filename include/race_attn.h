@@ -52,7 +52,8 @@ typedef enum {
     RACE_ERR_UNSUPPORTED = -2, /* valid arguments this build has no kernel for               */
     RACE_ERR_WORKSPACE = -3,   /* workspace_bytes smaller than race_attn_workspace_bytes()   */
     RACE_ERR_CUDA = -4,        /* a CUDA launch or runtime call failed                        */
-    RACE_ERR_ALIGN = -5        /* a tensor pointer is not 16-byte aligned                     */
+    RACE_ERR_ALIGN = -5,       /* a tensor pointer is not 16-byte aligned                     */
+    RACE_ERR_SCRATCH_LIMIT = -6 /* race_attn_fwd_noalloc: problem exceeds the built-in scratch */
 } race_status;
 
 /* Token-tensor shape and element type. */
@@ -96,6 +97,30 @@ int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const v
                   const float *W, float beta, int L, int P, int causal, const void *O,
                   const void *dO, void *dQ, void *dK, void *dV, const void *state,
                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Forward pass for callers that cannot allocate device memory (no counterpart in the paper).
+ *
+ * Some callers are not allowed to call cudaMalloc or to hand the library a workspace: code that
+ * runs under an allocator which owns all of the device's memory, or a latency-bound loop that
+ * must never allocate because an allocation can synchronise the device.  This entry point
+ * computes the same O as race_attn_fwd (same kernels, same arguments, no `state` output) but
+ * takes its scratch from a buffer of RACE_NOALLOC_SCRATCH_BYTES (32 MiB) that is compiled into
+ * the library as a static device array; every GPU on which the library is loaded holds that
+ * buffer until the process exits.  It calls no cudaMalloc, cudaFree or allocating routine.
+ *  - Problems whose race_attn_workspace_bytes(shape, L, P, causal, 0) exceeds
+ *    RACE_NOALLOC_SCRATCH_BYTES are rejected with RACE_ERR_SCRATCH_LIMIT before any launch.
+ *  - The first call on each device looks up the device address of the buffer (with that
+ *    device current); make that first call before any stream capture.
+ *  - All calls on a device share the one buffer and leave their data in it.  Every scratch
+ *    element a call reads is written earlier in the same call, so nothing needs clearing, but
+ *    two calls that overlap on the GPU (different streams, or different host threads) race
+ *    on the buffer and corrupt each other's results: serialise them.
+ */
+#define RACE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, const void *K, const void *V,
+                          const float *W, float beta, int L, int P, int causal, void *O,
+                          void *stream);
 
 /* Static description of a status code. */
 const char *race_attn_strerror(int status);

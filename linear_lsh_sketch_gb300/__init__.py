@@ -14,12 +14,15 @@ __all__ = [
     "RaceAttnError", "race_attn_fwd", "race_attn_bwd", "race_attn_workspace_bytes",
     "race_attn_state_bytes", "race_attn_strerror", "race_attn_launch_count", "race_attn_profile",
     "race_attn_profile_read", "race_attn_profile_reset", "library_path", "load_library",
+    "race_attn_fwd_noalloc", "RACE_NOALLOC_SCRATCH_BYTES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "librace_attn.so")
 
 RACE_F32, RACE_BF16 = 0, 1
+RACE_ERR_SCRATCH_LIMIT = -6
+RACE_NOALLOC_SCRATCH_BYTES = 32 << 20  # size of the library's built-in scratch buffer
 _DTYPES = {torch.float32: RACE_F32, torch.bfloat16: RACE_BF16}
 
 _lib = None
@@ -55,6 +58,8 @@ def load_library():
     L.race_attn_fwd.restype = i
     L.race_attn_bwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.race_attn_bwd.restype = i
+    L.race_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp]
+    L.race_attn_fwd_noalloc.restype = i
     L.race_attn_strerror.argtypes = [i]
     L.race_attn_strerror.restype = ctypes.c_char_p
     L.race_attn_launch_count.argtypes = []
@@ -200,3 +205,28 @@ def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, 
     if rc != 0:
         raise RaceAttnError(rc, "race_attn_bwd")
     return dQ, dK, dV
+
+
+def race_attn_fwd_noalloc(Q, K, V, W, beta, L, P, causal, O=None, stream=None):
+    """Forward pass through the entry point that allocates nothing and takes no workspace.
+
+    For callers that cannot allocate device memory: the library uses its own built-in scratch
+    buffer (RACE_NOALLOC_SCRATCH_BYTES per GPU) instead.  Calls that overlap on the GPU share
+    that buffer and must be serialised by the caller.  Only O is allocated here, and only when
+    it is not given.  Returns O.
+    """
+    shape = _shape_of(Q)
+    _check_like("K", K, Q)
+    _check_like("V", V, Q)
+    _check_like("Q", Q, Q)
+    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
+        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
+    if O is None:
+        O = torch.empty_like(Q)
+    _check_like("O", O, Q)
+    rc = load_library().race_attn_fwd_noalloc(
+        ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P), int(causal),
+        _ptr(O), _stream(stream))
+    if rc != 0:
+        raise RaceAttnError(rc, "race_attn_fwd_noalloc")
+    return O

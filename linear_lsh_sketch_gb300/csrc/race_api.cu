@@ -2,6 +2,7 @@
 // carving and kernel dispatch.  Declarations and the contract of each entry point are in
 // include/race_attn.h.
 #include <cmath>
+#include <mutex>
 #include <string>
 #include <type_traits>
 #include <vector>
@@ -324,6 +325,7 @@ const char *race_attn_strerror(int status)
         case RACE_ERR_WORKSPACE: return "workspace too small";
         case RACE_ERR_CUDA: return "CUDA launch or runtime error";
         case RACE_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+        case RACE_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in no-alloc buffer";
         default: return "unknown status";
     }
 }
@@ -354,3 +356,58 @@ void race_attn_profile_reset(void)
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ forward without a workspace
+//
+// Scratch for race_attn_fwd_noalloc: a static device array, so callers that may not allocate
+// device memory can still run the forward pass.  Host code must not use the symbol itself as a
+// pointer (on the host it names a shadow variable, not device memory); the device address is
+// looked up once per device with cudaGetSymbolAddress and cached.
+
+namespace race {
+namespace {
+
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RACE_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (nullptr on failure).
+void *noalloc_scratch()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace race
+
+extern "C" int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, const void *K, const void *V,
+                                     const float *W, float beta, int L, int P, int causal, void *O, void *stream)
+{
+    Plan pl;
+    int rc = make_plan(shape, L, P, causal, pl);
+    if (rc != RACE_OK) return rc;
+    if ((rc = check_beta(beta)) != RACE_OK) return rc;
+    if (!Q || !K || !V || !W || !O) return RACE_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(W) || !aligned16(O)) return RACE_ERR_ALIGN;
+    if (pl.ws_fwd > RACE_NOALLOC_SCRATCH_BYTES) return RACE_ERR_SCRATCH_LIMIT;
+    void *scratch = noalloc_scratch();
+    if (!scratch) return RACE_ERR_CUDA;
+    pl.D.beta = beta;
+    cudaStream_t st = (cudaStream_t)stream;
+    // state == nullptr: the forward keeps its sketch inside the scratch buffer
+    if (pl.bf16)
+        return forward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
+                                           (const __nv_bfloat16 *)V, W, (__nv_bfloat16 *)O, nullptr, (char *)scratch,
+                                           st);
+    return forward_impl<float>(pl, (const float *)Q, (const float *)K, (const float *)V, W, (float *)O, nullptr,
+                               (char *)scratch, st);
+}
