@@ -40,6 +40,10 @@ KERNEL_BYTES = {
     "causal_fwd": (4, 0),         # reads Q, K, V; writes O
     "causal_bwd_q": (5, 8),       # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
     "causal_bwd_kv": (6, 8),      # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
+    "tc_causal_totals": (2, 0),   # reads K, V
+    "tc_causal_fwd": (4, 0),      # reads Q, K, V; writes O
+    "tc_causal_bwd_q": (5, 8),    # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
+    "tc_causal_bwd_kv": (6, 8),   # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
 }
 
 
@@ -375,10 +379,14 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override N (sequence length) of the workload, e.g. for a small profiling capture")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
     from linear_lsh_sketch_gb300.workloads import CONFIGS
     w = CONFIGS[args.workload]
+    if args.tokens:
+        w = w.scaled(N=args.tokens, name="%s_N%d" % (w.name, args.tokens))
     if args.impl == "reference":
         run_reference(args, w)
     else:

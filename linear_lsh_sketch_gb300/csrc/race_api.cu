@@ -227,6 +227,20 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
     float *gsk = (float *)(ws + pl.off_gsk);
     float2 *aux = (float2 *)(ws + pl.off_aux);
     const float *S = state;
+    if constexpr (std::is_same<T, bf16_t>::value) {
+        if (use_tc<T>(pl) && causal_tc_bwd_supported(D)) {
+            if (!S) {
+                float *Sw = (float *)(ws + pl.off_sk);
+                RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, st));
+                RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 1, st));
+                S = Sw;
+            }
+            RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, st));
+            RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
+            RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, st));
+            return RACE_OK;
+        }
+    }
     if (!S) {
         float *Sw = (float *)(ws + pl.off_sk);
         RACE_TRY(launch_sketch<T>(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, 0, st));

@@ -20,6 +20,7 @@
 #include "race_common.cuh"
 #include "race_launch.h"
 #include "race_mma.cuh"
+#include "race_tc_common.cuh"
 
 namespace race {
 namespace tc {
@@ -27,142 +28,6 @@ namespace tc {
 using bf16 = __nv_bfloat16;
 using namespace race::mma;
 
-constexpr int C = 64;     // tokens per chunk
-constexpr int NTH = 256;  // 8 warps
-
-template <int D, int LRP, int LPP>
-struct CausalCfg {
-    static constexpr int XS = D + 8;        // row stride (elements) of token tiles
-    static constexpr int FS = LRP + 8;      // row stride of feature tiles
-    static constexpr int SS = D + 8;        // row stride of the bf16 state copies (d, mass, 7 zeros)
-    static constexpr int NWP = 2 * LPP;     // hyperplane rows: LPP hi rows then LPP lo rows
-    static constexpr int US = LPP + 1;      // row stride of the staged tanh projections (fp32)
-    static constexpr int NTO = D / 8 + 1;   // output / state n-tiles including the mass tile
-    static constexpr int KQ = D / 16;       // k-steps over d
-    static constexpr int KF = LRP / 16;     // k-steps over features
-    static constexpr int MT = LRP / 16;     // state m-tiles
-    static constexpr int SNT = (NTO + 7) / 8;  // state n-tiles per warp (warp w owns w, w+8, ...)
-    static constexpr int NLT = LPP / 16;    // lp tiles (of 8) per projection warp
-    static constexpr int X_BYTES = C * XS * 2;
-    static constexpr int OFF_XQ = 0;
-    static constexpr int OFF_XK = OFF_XQ + 2 * X_BYTES;
-    static constexpr int OFF_XV = OFF_XK + 2 * X_BYTES;
-    static constexpr int OFF_FQ = OFF_XV + 2 * X_BYTES;
-    static constexpr int OFF_FK = OFF_FQ + C * FS * 2;
-    static constexpr int OFF_SHI = OFF_FK + C * FS * 2;
-    static constexpr int OFF_SLO = OFF_SHI + LRP * SS * 2;
-    static constexpr int OFF_W = OFF_SLO + LRP * SS * 2;
-    static constexpr int OFF_U = OFF_W + NWP * XS * 2;
-    static constexpr int BYTES = OFF_U + 2 * C * US * 4;
-};
-
-// cp.async a [C, D] bf16 tile (rows n0 .. n0 + cnt of a [N, D] slice) into a padded smem tile;
-// rows past cnt are zero filled.
-template <int D, int XS>
-__device__ __forceinline__ void load_tile_async(bf16 *dst, const bf16 *__restrict__ src, int64_t n0, int cnt)
-{
-    constexpr int CH = D / 8;
-    for (int i = threadIdx.x; i < C * CH; i += NTH) {
-        const int r = i / CH, cc = i - r * CH;
-        const bf16 *s = src + (n0 + (r < cnt ? r : 0)) * D + cc * 8;
-        cp_async16(smem_u32(dst + r * XS + cc * 8), s, r < cnt ? 16 : 0);
-    }
-}
-
-// z = X W^T for 16 rows (warp row block rb) and this warp's lp tiles (half h), normalised by
-// 1/|x| and passed through tanh; the results go to ust[row][lp] (fp32).
-template <int D, int LRP, int LPP>
-__device__ __forceinline__ void project_rows(const bf16 *xs, const bf16 *wc, float *ust, int rb, int h, int lane)
-{
-    using Cf = CausalCfg<D, LRP, LPP>;
-    float zh[Cf::NLT][4], zl[Cf::NLT][4];
-#pragma unroll
-    for (int i = 0; i < Cf::NLT; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) zh[i][j] = zl[i][j] = 0.f;
-    float ss0 = 0.f, ss1 = 0.f;
-    const int arow = 16 * rb + (lane & 7) + 8 * ((lane >> 3) & 1);
-#pragma unroll
-    for (int ks = 0; ks < Cf::KQ; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(smem_u32(xs + arow * Cf::XS + 16 * ks + 8 * (lane >> 4)), a0, a1, a2, a3);
-        {
-            float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a0));
-            float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a1));
-            float2 f2 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a2));
-            float2 f3 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a3));
-            ss0 = fmaf(f0.x, f0.x, fmaf(f0.y, f0.y, fmaf(f2.x, f2.x, fmaf(f2.y, f2.y, ss0))));
-            ss1 = fmaf(f1.x, f1.x, fmaf(f1.y, f1.y, fmaf(f3.x, f3.x, fmaf(f3.y, f3.y, ss1))));
-        }
-#pragma unroll
-        for (int lt = 0; lt < Cf::NLT; ++lt) {
-            const int hirow = 8 * (h * Cf::NLT + lt);
-            const int wrow = ((lane >> 4) ? LPP + hirow : hirow) + (lane & 7);
-            uint32_t bh0, bh1, bl0, bl1;
-            ldsm_x4(smem_u32(wc + wrow * Cf::XS + 16 * ks + 8 * ((lane >> 3) & 1)), bh0, bh1, bl0, bl1);
-            mma16816(zh[lt], a0, a1, a2, a3, bh0, bh1);
-            mma16816(zl[lt], a0, a1, a2, a3, bl0, bl1);
-        }
-    }
-    ss0 += __shfl_xor_sync(0xffffffffu, ss0, 1);
-    ss0 += __shfl_xor_sync(0xffffffffu, ss0, 2);
-    ss1 += __shfl_xor_sync(0xffffffffu, ss1, 1);
-    ss1 += __shfl_xor_sync(0xffffffffu, ss1, 2);
-    const float inv0 = ss0 > 0.f ? 1.0f / sqrtf(ss0) : 0.f;
-    const float inv1 = ss1 > 0.f ? 1.0f / sqrtf(ss1) : 0.f;
-    const int g = lane >> 2, q = lane & 3;
-    const int r0 = 16 * rb + g, r1 = r0 + 8;
-#pragma unroll
-    for (int lt = 0; lt < Cf::NLT; ++lt) {
-        const int col = 8 * (h * Cf::NLT + lt) + 2 * q;
-        ust[r0 * Cf::US + col] = tanhf((zh[lt][0] + zl[lt][0]) * inv0);
-        ust[r0 * Cf::US + col + 1] = tanhf((zh[lt][1] + zl[lt][1]) * inv0);
-        ust[r1 * Cf::US + col] = tanhf((zh[lt][2] + zl[lt][2]) * inv1);
-        ust[r1 * Cf::US + col + 1] = tanhf((zh[lt][3] + zl[lt][3]) * inv1);
-    }
-}
-
-// Bucket features of the staged tanh projections: F[t][l*R + r] = prod_p sigmoid(+-2 beta u);
-// rows t >= cnt are zero.  Work items (side, table, token), lanes over tokens.
-template <int D, int LRP, int LPP>
-__device__ __forceinline__ void featurise_tiles(const Dims &Dm, const float *ust, bf16 *f0, bf16 *f1,
-                                                int nsides, int cnt)
-{
-    using Cf = CausalCfg<D, LRP, LPP>;
-    const int total = nsides * Dm.L * C;
-    for (int it = threadIdx.x; it < total; it += NTH) {
-        const int t = it % C;
-        const int l = (it / C) % Dm.L;
-        const int side = it / (C * Dm.L);
-        const float *u = ust + side * C * Cf::US + t * Cf::US + l * Dm.P;
-        bf16 *F = (side == 0 ? f0 : f1) + t * Cf::FS + l * Dm.R;
-        float pp[kMaxP], pm[kMaxP];
-#pragma unroll
-        for (int p = 0; p < kMaxP; ++p) {
-            pp[p] = pm[p] = 1.f;
-            if (p < Dm.P) {
-                const float a = 2.f * Dm.beta * u[p];
-                pp[p] = 1.f / (1.f + expf(-a));
-                pm[p] = 1.f / (1.f + expf(a));
-            }
-        }
-        const bool live = t < cnt;
-        for (int r = 0; r < Dm.R; ++r) {
-            float prod = 1.f;
-#pragma unroll
-            for (int p = 0; p < kMaxP; ++p)
-                if (p < Dm.P) prod *= ((r >> p) & 1) ? pp[p] : pm[p];
-            F[r] = __float2bfloat16_rn(live ? prod : 0.f);
-        }
-    }
-}
-
-// B fragment of the mass column: n = 0 holds ones, other columns zero.
-__device__ __forceinline__ void mass_fragment(int lane, uint32_t &b0, uint32_t &b1)
-{
-    const uint32_t one2 = 0x3F803F80u;  // two bf16 ones
-    b0 = b1 = (lane >> 2) == 0 ? one2 : 0u;
-}
 
 template <int D, int LRP, int LPP, bool TOTALS>
 __global__ void __launch_bounds__(NTH, 1)
