@@ -53,7 +53,8 @@ typedef enum {
     RACE_ERR_WORKSPACE = -3,   /* workspace_bytes smaller than race_attn_workspace_bytes()   */
     RACE_ERR_CUDA = -4,        /* a CUDA launch or runtime call failed                        */
     RACE_ERR_ALIGN = -5,       /* a tensor pointer is not 16-byte aligned                     */
-    RACE_ERR_SCRATCH_LIMIT = -6 /* race_attn_fwd_noalloc: problem exceeds the built-in scratch */
+    RACE_ERR_SCRATCH_LIMIT = -6, /* race_attn_fwd_noalloc: problem exceeds the built-in scratch */
+    RACE_ERR_DEVICE_TIMEOUT = -7 /* race_attn_status: a kernel stopped after a bounded wait     */
 } race_status;
 
 /* Token-tensor shape and element type. */
@@ -121,6 +122,16 @@ int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const v
 int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, const void *K, const void *V,
                           const float *W, float beta, int L, int P, int causal, void *O,
                           void *stream);
+
+/*
+ * Device-side status of the last race_attn_fwd / race_attn_bwd call that used `workspace`.
+ * Kernels that wait for asynchronous (bulk) copies bound every wait; if a wait runs out they
+ * record it in the first word of the workspace and return early, leaving their outputs
+ * incomplete.  This call synchronises `stream`, reads that word and returns RACE_OK or
+ * RACE_ERR_DEVICE_TIMEOUT (RACE_ERR_CUDA if the stream or the copy failed).  Every fwd/bwd
+ * call clears the word when it starts.
+ */
+int race_attn_status(const void *workspace, void *stream);
 
 /* Static description of a status code. */
 const char *race_attn_strerror(int status);

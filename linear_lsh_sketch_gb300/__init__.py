@@ -14,7 +14,7 @@ __all__ = [
     "RaceAttnError", "race_attn_fwd", "race_attn_bwd", "race_attn_workspace_bytes",
     "race_attn_state_bytes", "race_attn_strerror", "race_attn_launch_count", "race_attn_profile",
     "race_attn_profile_read", "race_attn_profile_reset", "library_path", "load_library",
-    "race_attn_fwd_noalloc", "RACE_NOALLOC_SCRATCH_BYTES",
+    "race_attn_fwd_noalloc", "RACE_NOALLOC_SCRATCH_BYTES", "race_attn_status",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -60,6 +60,8 @@ def load_library():
     L.race_attn_bwd.restype = i
     L.race_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp]
     L.race_attn_fwd_noalloc.restype = i
+    L.race_attn_status.argtypes = [vp, vp]
+    L.race_attn_status.restype = i
     L.race_attn_strerror.argtypes = [i]
     L.race_attn_strerror.restype = ctypes.c_char_p
     L.race_attn_launch_count.argtypes = []
@@ -120,6 +122,12 @@ def race_attn_state_bytes(shape, L, P, causal):
 
 def race_attn_strerror(status):
     return load_library().race_attn_strerror(int(status)).decode()
+
+
+def race_attn_status(workspace, stream=None):
+    """Synchronise and read the device status word of `workspace` (0 = ok, -7 = a bounded wait
+    ran out); see race_attn_status in include/race_attn.h."""
+    return load_library().race_attn_status(_ptr(workspace), _stream(stream))
 
 
 def race_attn_launch_count():

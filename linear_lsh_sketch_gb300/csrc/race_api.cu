@@ -100,6 +100,7 @@ struct Plan {
     int nsplit = 1;        // token ranges (non-causal) or segments (causal) per (b, h)
     int64_t seg_len = 0;   // tokens per range, a multiple of the token tile
     size_t E = 0;          // floats per sketch: LR * (d + 1)
+    size_t off_status = 0;  // one 32-bit device status word (error bits of bounded waits)
     size_t off_part = 0, off_sk = 0, off_gpart = 0, off_gsk = 0, off_aux = 0;
     size_t ws_fwd = 0, ws_bwd = 0, state = 0;
 };
@@ -149,7 +150,8 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     const size_t sk_one = pl.E * sizeof(float);
     const size_t per_split = (size_t)D.BH * pl.nsplit * sk_one;
     const size_t per_bh = (size_t)D.BH * sk_one;
-    pl.off_part = 0;
+    pl.off_status = 0;
+    pl.off_part = 256;
     pl.off_sk = align256(pl.off_part + per_split);
     const size_t sk_bytes = pl.causal ? per_split : per_bh;
     pl.ws_fwd = align256(pl.off_sk + sk_bytes);
@@ -198,11 +200,13 @@ int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float
     const Dims &D = pl.D;
     float *part = (float *)(ws + pl.off_part);
     float *S = state ? state : (float *)(ws + pl.off_sk);
+    unsigned *err = (unsigned *)(ws + pl.off_status);
+    RACE_TRY(cudaMemsetAsync(err, 0, sizeof(unsigned), st));
     if constexpr (std::is_same<T, bf16_t>::value) {
         if (use_tc<T>(pl)) {
-            RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, st));
+            RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
             RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
-            RACE_TRY(launch_causal_tc_fwd(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, st));
+            RACE_TRY(launch_causal_tc_fwd(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, err, st));
             return RACE_OK;
         }
     }
@@ -226,18 +230,20 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
     float *gpart = (float *)(ws + pl.off_gpart);
     float *gsk = (float *)(ws + pl.off_gsk);
     float2 *aux = (float2 *)(ws + pl.off_aux);
+    unsigned *err = (unsigned *)(ws + pl.off_status);
+    RACE_TRY(cudaMemsetAsync(err, 0, sizeof(unsigned), st));
     const float *S = state;
     if constexpr (std::is_same<T, bf16_t>::value) {
         if (use_tc<T>(pl) && causal_tc_bwd_supported(D)) {
             if (!S) {
                 float *Sw = (float *)(ws + pl.off_sk);
-                RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, st));
+                RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 1, st));
                 S = Sw;
             }
-            RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, st));
+            RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
-            RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, st));
+            RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, st));
             return RACE_OK;
         }
     }
@@ -340,8 +346,18 @@ const char *race_attn_strerror(int status)
         case RACE_ERR_CUDA: return "CUDA launch or runtime error";
         case RACE_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
         case RACE_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in no-alloc buffer";
+        case RACE_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting for an asynchronous copy";
         default: return "unknown status";
     }
+}
+
+int race_attn_status(const void *workspace, void *stream)
+{
+    if (!workspace) return RACE_ERR_INVALID_ARG;
+    unsigned bits = 0;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return RACE_ERR_CUDA;
+    if (cudaMemcpy(&bits, workspace, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess) return RACE_ERR_CUDA;
+    return bits ? RACE_ERR_DEVICE_TIMEOUT : RACE_OK;
 }
 
 uint64_t race_attn_launch_count(void) { return g_launches; }

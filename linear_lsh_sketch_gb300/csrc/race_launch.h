@@ -55,16 +55,18 @@ cudaError_t launch_causal_bwd_kv(const Dims &D, const T *Q, const T *K, const T 
 bool causal_tc_supported(const Dims &D);
 int causal_tc_chunk();
 cudaError_t launch_causal_tc_totals(const Dims &D, const bf16_t *K, const bf16_t *V, const float *W,
-                                    int64_t seg_len, int nseg, float *Sout, cudaStream_t st);
+                                    int64_t seg_len, int nseg, float *Sout, unsigned *err, cudaStream_t st);
 cudaError_t launch_causal_tc_fwd(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const float *W,
-                                 const float *S0, int64_t seg_len, int nseg, bf16_t *O, cudaStream_t st);
+                                 const float *S0, int64_t seg_len, int nseg, bf16_t *O, unsigned *err,
+                                 cudaStream_t st);
 
 bool causal_tc_bwd_supported(const Dims &D);
 cudaError_t launch_causal_tc_bwd_q(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V,
                                    const bf16_t *dO, const float *W, const float *S0, int64_t seg_len, int nseg,
-                                   bf16_t *dQ, float2 *aux, float *Gseg, cudaStream_t st);
+                                   bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, cudaStream_t st);
 cudaError_t launch_causal_tc_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V,
                                     const bf16_t *dO, const float2 *aux, const float *W, const float *G0,
-                                    int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, cudaStream_t st);
+                                    int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err,
+                                    cudaStream_t st);
 
 }  // namespace race

@@ -1,6 +1,6 @@
-// race_tc_common.cuh -- pieces shared by the tensor-core causal kernels: chunk geometry,
-// asynchronous tile loads, the tensor-core projection z = X (W_hi + W_lo)^T with tanh, the bucket
-// featuriser, and constant fragments.
+// race_tc_common.cuh -- pieces shared by the tensor-core causal kernels: chunk geometry, bulk
+// (TMA) row copies completing on mbarriers with bounded waits, the tensor-core projection
+// z = X (W_hi + W_lo)^T, the bucket featuriser, and constant fragments.
 #pragma once
 
 #include "race_common.cuh"
@@ -12,80 +12,146 @@ namespace tc {
 using bf16 = __nv_bfloat16;
 using namespace race::mma;
 
-constexpr int C = 64;     // tokens per chunk
-constexpr int NTH = 256;  // 8 warps
+constexpr int C = 64;      // tokens per chunk
+constexpr int NTH = 256;   // 8 warps
+constexpr int LPP = 16;    // projection columns (L * P <= 16), hi rows then lo rows in the W tile
 
-template <int D, int LRP, int LPP>
-struct CausalCfg {
-    static constexpr int XS = D + 8;        // row stride (elements) of token tiles
-    static constexpr int FS = LRP + 8;      // row stride of feature tiles
-    static constexpr int SS = D + 8;        // row stride of the bf16 state copies (d, mass, 7 zeros)
-    static constexpr int NWP = 2 * LPP;     // hyperplane rows: LPP hi rows then LPP lo rows
-    static constexpr int US = LPP + 1;      // row stride of the staged tanh projections (fp32)
-    static constexpr int NTO = D / 8 + 1;   // output / state n-tiles including the mass tile
-    static constexpr int KQ = D / 16;       // k-steps over d
-    static constexpr int KF = LRP / 16;     // k-steps over features
-    static constexpr int MT = LRP / 16;     // state m-tiles
-    static constexpr int SNT = (NTO + 7) / 8;  // state n-tiles per warp (warp w owns w, w+8, ...)
-    static constexpr int NLT = LPP / 16;    // lp tiles (of 8) per projection warp
-    static constexpr int X_BYTES = C * XS * 2;
-    static constexpr int OFF_XQ = 0;
-    static constexpr int OFF_XK = OFF_XQ + 2 * X_BYTES;
-    static constexpr int OFF_XV = OFF_XK + 2 * X_BYTES;
-    static constexpr int OFF_FQ = OFF_XV + 2 * X_BYTES;
-    static constexpr int OFF_FK = OFF_FQ + C * FS * 2;
-    static constexpr int OFF_SHI = OFF_FK + C * FS * 2;
-    static constexpr int OFF_SLO = OFF_SHI + LRP * SS * 2;
-    static constexpr int OFF_W = OFF_SLO + LRP * SS * 2;
-    static constexpr int OFF_U = OFF_W + NWP * XS * 2;
-    static constexpr int BYTES = OFF_U + 2 * C * US * 4;
-};
+// Error bits written to the workspace status word.
+constexpr unsigned kErrWaitTimeout = 1u;
 
-// cp.async a [C, D] bf16 tile (rows n0 .. n0 + cnt of a [N, D] slice) into a padded smem tile;
-// rows past cnt are zero filled.
-template <int D, int XS>
-__device__ __forceinline__ void load_tile_async(bf16 *dst, const bf16 *__restrict__ src, int64_t n0, int cnt)
+// ------------------------------------------------------------------ mbarriers and bulk copies
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
-    constexpr int CH = D / 8;
-    for (int i = threadIdx.x; i < C * CH; i += NTH) {
-        const int r = i / CH, cc = i - r * CH;
-        const bf16 *s = src + (n0 + (r < cnt ? r : 0)) * D + cc * 8;
-        cp_async16(smem_u32(dst + r * XS + cc * 8), s, r < cnt ? 16 : 0);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before later async-proxy
+// (bulk copy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bulk (TMA) copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global to
+// this CTA's shared memory, completing on the mbarrier at `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Waits for the mbarrier phase with parity `phase`; gives up after a bounded number of polls
+// (each poll may suspend the thread briefly) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase)
+{
+    for (int i = 0; i < (1 << 22); ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(phase)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// Issues the bulk row copies of up to 4 token tiles ([C][XS] bf16, rows n0 .. n0 + cnt of
+// [N, D] slices; tile i goes from src_i to dst_i).  Warp w copies rows 8 w .. 8 w + 7; lane l
+// handles tile l / 8.  The caller has registered ntiles * cnt * D * 2 expected bytes on `bar`.
+template <int D, int XS>
+__device__ __forceinline__ void issue_rows(bf16 *d0, bf16 *d1, bf16 *d2, bf16 *d3, const bf16 *s0, const bf16 *s1,
+                                           const bf16 *s2, const bf16 *s3, int ntiles, int64_t n0, int cnt,
+                                           uint32_t bar)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tile = lane >> 3, row = 8 * warp + (lane & 7);
+    if (tile < ntiles && row < cnt) {
+        bf16 *dst = tile == 0 ? d0 : tile == 1 ? d1 : tile == 2 ? d2 : d3;
+        const bf16 *src = tile == 0 ? s0 : tile == 1 ? s1 : tile == 2 ? s2 : s3;
+        bulk_g2s(smem_u32(dst + row * XS), src + (n0 + row) * D, D * 2, bar);
     }
 }
 
-// z = X W^T for 16 rows (warp row block rb) and this warp's lp tiles (half h), normalised by
-// 1/|x| and passed through tanh; the results go to ust[row][lp] (fp32).
-template <int D, int LRP, int LPP>
-__device__ __forceinline__ void project_rows(const bf16 *xs, const bf16 *wc, float *ust, int rb, int h, int lane,
-                                             float *inv_out = nullptr)
+// ------------------------------------------------------------------ nonlinearities
+
+// tanh with about 1e-7 absolute error (all that the bucket probabilities are sensitive to).
+__device__ __forceinline__ float tanh_abs(float x)
 {
-    using Cf = CausalCfg<D, LRP, LPP>;
-    float zh[Cf::NLT][4], zl[Cf::NLT][4];
+    return 1.f - 2.f * __frcp_rn(1.f + __expf(2.f * x));
+}
+
+// sigmoid(a) and sigmoid(-a) without overflow for any finite a.
+__device__ __forceinline__ void sigmoid_pair(float a, float &sp, float &sm)
+{
+    const float e = __expf(-fabsf(a));
+    const float big = __frcp_rn(1.f + e), small = e * big;
+    sp = a >= 0.f ? big : small;
+    sm = a >= 0.f ? small : big;
+}
+
+// The 2^P bucket probabilities of one table from its P tanh projections:
+// phi_r = prod_t sigmoid(2 beta u_t v_{r,t}), v_{r,t} = +1 iff bit t of r is set.
+template <int P>
+__device__ __forceinline__ void bucket_probs(const float *u, float beta, float (&ph)[1 << P])
+{
+    ph[0] = 1.f;
 #pragma unroll
-    for (int i = 0; i < Cf::NLT; ++i)
+    for (int p = 0; p < P; ++p) {
+        float sp, sm;
+        sigmoid_pair(2.f * beta * u[p], sp, sm);
+#pragma unroll
+        for (int r = 0; r < (1 << p); ++r) {
+            ph[r + (1 << p)] = ph[r] * sp;
+            ph[r] *= sm;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ projection and features
+
+// z = X (W_hi + W_lo)^T for the 16 rows at xs (row stride XS) and all LPP projection columns;
+// returns u = tanh(z / |x|) as fragments (tile lt: rows g, g+8; columns 8 lt + 2q, +1) and the
+// inverse row norms (0 for a zero row).
+template <int D, int XS>
+__device__ __forceinline__ void project16(const bf16 *xs, const bf16 *wc, int lane, float (&u)[LPP / 8][4],
+                                          float &inv0, float &inv1)
+{
+    float zh[LPP / 8][4], zl[LPP / 8][4];
+#pragma unroll
+    for (int i = 0; i < LPP / 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) zh[i][j] = zl[i][j] = 0.f;
     float ss0 = 0.f, ss1 = 0.f;
-    const int arow = 16 * rb + (lane & 7) + 8 * ((lane >> 3) & 1);
+    const uint32_t abase = smem_u32(xs + ((lane & 7) + 8 * ((lane >> 3) & 1)) * XS + 8 * (lane >> 4));
+    // W rows: lanes 0-15 address hi rows, 16-31 lo rows (x4: hi k0-7, hi k8-15, lo k0-7, lo k8-15)
+    const uint32_t wbase = smem_u32(wc + (((lane >> 4) ? LPP : 0) + (lane & 7)) * XS + 8 * ((lane >> 3) & 1));
 #pragma unroll
-    for (int ks = 0; ks < Cf::KQ; ++ks) {
+    for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(smem_u32(xs + arow * Cf::XS + 16 * ks + 8 * (lane >> 4)), a0, a1, a2, a3);
-        {
-            float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a0));
-            float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a1));
-            float2 f2 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a2));
-            float2 f3 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a3));
-            ss0 = fmaf(f0.x, f0.x, fmaf(f0.y, f0.y, fmaf(f2.x, f2.x, fmaf(f2.y, f2.y, ss0))));
-            ss1 = fmaf(f1.x, f1.x, fmaf(f1.y, f1.y, fmaf(f3.x, f3.x, fmaf(f3.y, f3.y, ss1))));
-        }
+        ldsm_x4(abase + 32 * ks, a0, a1, a2, a3);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a0));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a1));
+        const float2 f2 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a2));
+        const float2 f3 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&a3));
+        ss0 = fmaf(f0.x, f0.x, fmaf(f0.y, f0.y, fmaf(f2.x, f2.x, fmaf(f2.y, f2.y, ss0))));
+        ss1 = fmaf(f1.x, f1.x, fmaf(f1.y, f1.y, fmaf(f3.x, f3.x, fmaf(f3.y, f3.y, ss1))));
 #pragma unroll
-        for (int lt = 0; lt < Cf::NLT; ++lt) {
-            const int hirow = 8 * (h * Cf::NLT + lt);
-            const int wrow = ((lane >> 4) ? LPP + hirow : hirow) + (lane & 7);
+        for (int lt = 0; lt < LPP / 8; ++lt) {
             uint32_t bh0, bh1, bl0, bl1;
-            ldsm_x4(smem_u32(wc + wrow * Cf::XS + 16 * ks + 8 * ((lane >> 3) & 1)), bh0, bh1, bl0, bl1);
+            ldsm_x4(wbase + 2 * (8 * lt * XS + 16 * ks), bh0, bh1, bl0, bl1);
             mma16816(zh[lt], a0, a1, a2, a3, bh0, bh1);
             mma16816(zl[lt], a0, a1, a2, a3, bl0, bl1);
         }
@@ -94,61 +160,84 @@ __device__ __forceinline__ void project_rows(const bf16 *xs, const bf16 *wc, flo
     ss0 += __shfl_xor_sync(0xffffffffu, ss0, 2);
     ss1 += __shfl_xor_sync(0xffffffffu, ss1, 1);
     ss1 += __shfl_xor_sync(0xffffffffu, ss1, 2);
-    const float inv0 = ss0 > 0.f ? 1.0f / sqrtf(ss0) : 0.f;
-    const float inv1 = ss1 > 0.f ? 1.0f / sqrtf(ss1) : 0.f;
-    const int g = lane >> 2, q = lane & 3;
-    const int r0 = 16 * rb + g, r1 = r0 + 8;
-    if (inv_out && h == 0 && q == 0) {
-        inv_out[r0] = inv0;
-        inv_out[r1] = inv1;
-    }
+    inv0 = ss0 > 0.f ? rsqrtf(ss0) : 0.f;
+    inv1 = ss1 > 0.f ? rsqrtf(ss1) : 0.f;
 #pragma unroll
-    for (int lt = 0; lt < Cf::NLT; ++lt) {
-        const int col = 8 * (h * Cf::NLT + lt) + 2 * q;
-        ust[r0 * Cf::US + col] = tanhf((zh[lt][0] + zl[lt][0]) * inv0);
-        ust[r0 * Cf::US + col + 1] = tanhf((zh[lt][1] + zl[lt][1]) * inv0);
-        ust[r1 * Cf::US + col] = tanhf((zh[lt][2] + zl[lt][2]) * inv1);
-        ust[r1 * Cf::US + col + 1] = tanhf((zh[lt][3] + zl[lt][3]) * inv1);
+    for (int lt = 0; lt < LPP / 8; ++lt) {
+        u[lt][0] = tanh_abs((zh[lt][0] + zl[lt][0]) * inv0);
+        u[lt][1] = tanh_abs((zh[lt][1] + zl[lt][1]) * inv0);
+        u[lt][2] = tanh_abs((zh[lt][2] + zl[lt][2]) * inv1);
+        u[lt][3] = tanh_abs((zh[lt][3] + zl[lt][3]) * inv1);
     }
 }
 
-// Bucket features of the staged tanh projections: F[t][l*R + r] = prod_p sigmoid(+-2 beta u);
-// rows t >= cnt are zero.  Work items (side, table, token), lanes over tokens.
-template <int D, int LRP, int LPP>
-__device__ __forceinline__ void featurise_tiles(const Dims &Dm, const float *ust, bf16 *f0, bf16 *f1,
-                                                int nsides, int cnt, const float *scale0 = nullptr,
-                                                bf16 *f0s = nullptr)
+// Writes the u fragments of 16 rows to a warp-private [16][US] fp32 stage.
+template <int US>
+__device__ __forceinline__ void stage_u(const float (&u)[LPP / 8][4], float *ust, int lane)
 {
-    using Cf = CausalCfg<D, LRP, LPP>;
-    const int total = nsides * Dm.L * C;
-    for (int it = threadIdx.x; it < total; it += NTH) {
-        const int t = it % C;
-        const int l = (it / C) % Dm.L;
-        const int side = it / (C * Dm.L);
-        const float *u = ust + side * C * Cf::US + t * Cf::US + l * Dm.P;
-        bf16 *F = (side == 0 ? f0 : f1) + t * Cf::FS + l * Dm.R;
-        float pp[kMaxP], pm[kMaxP];
+    const int g = lane >> 2, q = lane & 3;
 #pragma unroll
-        for (int p = 0; p < kMaxP; ++p) {
-            pp[p] = pm[p] = 1.f;
-            if (p < Dm.P) {
-                const float a = 2.f * Dm.beta * u[p];
-                pp[p] = 1.f / (1.f + expf(-a));
-                pm[p] = 1.f / (1.f + expf(a));
-            }
-        }
-        const bool live = t < cnt;
-        const bool scaled = side == 0 && f0s != nullptr;
-        const float sc = scaled && live ? scale0[t] : 0.f;
-        bf16 *Fs = scaled ? f0s + t * Cf::FS + l * Dm.R : nullptr;
-        for (int r = 0; r < Dm.R; ++r) {
-            float prod = 1.f;
+    for (int lt = 0; lt < LPP / 8; ++lt) {
+        const int c = 8 * lt + 2 * q;
+        ust[g * US + c] = u[lt][0];
+        ust[g * US + c + 1] = u[lt][1];
+        ust[(g + 8) * US + c] = u[lt][2];
+        ust[(g + 8) * US + c + 1] = u[lt][3];
+    }
+}
+
+// Bucket features of 16 staged rows: F[row][l R + r] = phi^(l)_r (bf16), zero for rows with
+// t0 + row >= cnt; optionally also Fs = phi * scale[row] (bf16).  Items (row, table) over lanes.
+template <int P, int US, int FS>
+__device__ __forceinline__ void features16(const float *ust, int L, float beta, int t0, int cnt, bf16 *F, int lane,
+                                           const float *scale = nullptr, bf16 *Fs = nullptr)
+{
+    constexpr int R = 1 << P;
+    for (int it = lane; it < 16 * L; it += 32) {
+        const int row = it & 15, l = it >> 4;
+        float ph[R];
+        bucket_probs<P>(ust + row * US + l * P, beta, ph);
+        const float live = (t0 + row < cnt) ? 1.f : 0.f;
+        uint32_t *dst = reinterpret_cast<uint32_t *>(F + row * FS + l * R);
 #pragma unroll
-            for (int p = 0; p < kMaxP; ++p)
-                if (p < Dm.P) prod *= ((r >> p) & 1) ? pp[p] : pm[p];
-            F[r] = __float2bfloat16_rn(live ? prod : 0.f);
-            if (scaled) Fs[r] = __float2bfloat16_rn(prod * sc);
+        for (int r = 0; r < R; r += 2) dst[r / 2] = pack_bf16(ph[r] * live, ph[r + 1] * live);
+        if (Fs) {
+            const float sc = live * scale[t0 + row];
+            uint32_t *dss = reinterpret_cast<uint32_t *>(Fs + row * FS + l * R);
+#pragma unroll
+            for (int r = 0; r < R; r += 2) dss[r / 2] = pack_bf16(ph[r] * sc, ph[r + 1] * sc);
         }
+    }
+}
+
+// Chain rule back through the featuriser for 16 rows: u from the warp's stage ([16][US]),
+// dphi rows ([16][DPS], fp32).  phi is recomputed; writes
+// dz_p = beta * sum_r phi_r (dphi_r - phi . dphi) v_{r,p} * (1 - u_p^2) as bf16 to dz ([16][ZS]).
+template <int P, int US, int DPS, int ZS>
+__device__ __forceinline__ void features_backward16(const float *ust, const float *dphi, int L, float beta,
+                                                    bf16 *dz, int lane)
+{
+    constexpr int R = 1 << P;
+    for (int it = lane; it < 16 * L; it += 32) {
+        const int row = it & 15, l = it >> 4;
+        const float *u = ust + row * US + l * P;
+        float ph[R];
+        bucket_probs<P>(u, beta, ph);
+        const float *dph = dphi + row * DPS + l * R;
+        float c = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) c = fmaf(ph[r], dph[r], c);
+        float du[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) du[p] = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float ds = ph[r] * (dph[r] - c);
+#pragma unroll
+            for (int p = 0; p < P; ++p) du[p] += ((r >> p) & 1) ? ds : -ds;
+        }
+#pragma unroll
+        for (int p = 0; p < P; ++p) dz[row * ZS + l * P + p] = __float2bfloat16_rn(beta * du[p] * (1.f - u[p] * u[p]));
     }
 }
 
@@ -157,150 +246,6 @@ __device__ __forceinline__ void mass_fragment(int lane, uint32_t &b0, uint32_t &
 {
     const uint32_t one2 = 0x3F803F80u;  // two bf16 ones
     b0 = b1 = (lane >> 2) == 0 ? one2 : 0u;
-}
-
-// Chain rule back through the featuriser for the tokens of one tile, in float32.  u comes from
-// ust ([C][US], tanh projections), dphi from dphi_s ([C][DPS], fp32).  phi is recomputed from u.
-// Writes dz = beta * (sum_r phi_r (dphi_r - phi . dphi) v_{r,p}) * (1 - u_p^2) as bf16 into
-// dz_s[t][l * P + p] (row stride ZS).
-template <int US, int DPS, int ZS>
-__device__ __forceinline__ void featurise_backward_tiles(const Dims &Dm, const float *ust, const float *dphi_s,
-                                                         bf16 *dz_s)
-{
-    const int total = Dm.L * C;
-    for (int it = threadIdx.x; it < total; it += NTH) {
-        const int t = it % C, l = it / C;
-        const float *u = ust + t * US + l * Dm.P;
-        const float *dph = dphi_s + t * DPS + l * Dm.R;
-        float pp[kMaxP], pm[kMaxP];
-#pragma unroll
-        for (int p = 0; p < kMaxP; ++p) {
-            pp[p] = pm[p] = 1.f;
-            if (p < Dm.P) {
-                const float a = 2.f * Dm.beta * u[p];
-                pp[p] = 1.f / (1.f + expf(-a));
-                pm[p] = 1.f / (1.f + expf(a));
-            }
-        }
-        float c = 0.f;
-        for (int r = 0; r < Dm.R; ++r) {
-            float prod = 1.f;
-#pragma unroll
-            for (int p = 0; p < kMaxP; ++p)
-                if (p < Dm.P) prod *= ((r >> p) & 1) ? pp[p] : pm[p];
-            c = fmaf(prod, dph[r], c);
-        }
-        float du[kMaxP];
-#pragma unroll
-        for (int p = 0; p < kMaxP; ++p) du[p] = 0.f;
-        for (int r = 0; r < Dm.R; ++r) {
-            float prod = 1.f;
-#pragma unroll
-            for (int p = 0; p < kMaxP; ++p)
-                if (p < Dm.P) prod *= ((r >> p) & 1) ? pp[p] : pm[p];
-            const float ds = prod * (dph[r] - c);
-#pragma unroll
-            for (int p = 0; p < kMaxP; ++p)
-                if (p < Dm.P) du[p] += ((r >> p) & 1) ? ds : -ds;
-        }
-#pragma unroll
-        for (int p = 0; p < kMaxP; ++p)
-            if (p < Dm.P) dz_s[t * ZS + l * Dm.P + p] = __float2bfloat16_rn(Dm.beta * du[p] * (1.f - u[p] * u[p]));
-    }
-}
-
-// dxhat for 16 rows (row block rb) and this warp's column half h: dxhat = dz (W_hi + W_lo), with
-// dz [C][ZS] bf16 and W rows in wc ([2 LPP][XS]: hi rows then lo rows).  Returns the fragments
-// acc[D/16][4] (n-tile i covers columns 8 (h D/16 + i) ..), and adds the row partials of
-// x . dxhat over those columns into red[row] via shared-memory atomics-free quad reduction:
-// the caller passes red_half = red + h * C.
-template <int D, int LPP, int XS, int ZS>
-__device__ __forceinline__ void back_project(const bf16 *dz_s, const bf16 *wc, const bf16 *xs, int rb, int h,
-                                             int lane, float (&acc)[D / 16][4], float *red_half)
-{
-    constexpr int NC = D / 16;
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int i = 0; i < NC; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
-    const int arow = 16 * rb + (lane & 7) + 8 * ((lane >> 3) & 1);
-    const int vrow = (lane & 7) + 8 * ((lane >> 3) & 1);
-#pragma unroll
-    for (int kz = 0; kz < LPP / 16; ++kz) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(smem_u32(dz_s + arow * ZS + 16 * kz + 8 * (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-        for (int i = 0; i < NC; i += 2) {
-            const int col = 8 * (h * NC + i) + 8 * (lane >> 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(smem_u32(wc + (16 * kz + vrow) * XS + col), b0, b1, b2, b3);
-            mma16816(acc[i], a0, a1, a2, a3, b0, b1);
-            mma16816(acc[i + 1], a0, a1, a2, a3, b2, b3);
-            ldsm_x4_t(smem_u32(wc + (LPP + 16 * kz + vrow) * XS + col), b0, b1, b2, b3);
-            mma16816(acc[i], a0, a1, a2, a3, b0, b1);
-            mma16816(acc[i + 1], a0, a1, a2, a3, b2, b3);
-        }
-    }
-    float p0 = 0.f, p1 = 0.f;
-    const int t0 = 16 * rb + g;
-#pragma unroll
-    for (int i = 0; i < NC; ++i) {
-        const int c = 8 * (h * NC + i) + 2 * q;
-        const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(xs + t0 * XS + c));
-        const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(xs + (t0 + 8) * XS + c));
-        p0 = fmaf(x0.x, acc[i][0], fmaf(x0.y, acc[i][1], p0));
-        p1 = fmaf(x1.x, acc[i][2], fmaf(x1.y, acc[i][3], p1));
-    }
-    p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-    p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-    p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-    p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-    if (q == 0) {
-        red_half[t0] = p0;
-        red_half[t0 + 8] = p1;
-    }
-}
-
-// Finish the normalisation backward for the fragments of back_project and stage dx as bf16:
-// dx = inv (dxhat - x inv^2 (x . dxhat)), x . dxhat = red[t] + red[C + t].
-template <int D, int XS>
-__device__ __forceinline__ void stage_dx(const float (&acc)[D / 16][4], const bf16 *xs, const float *inv,
-                                         const float *red, int rb, int h, int lane, bf16 *stage)
-{
-    constexpr int NC = D / 16;
-    const int g = lane >> 2, q = lane & 3;
-    const int t0 = 16 * rb + g, t1 = t0 + 8;
-    const float i0 = inv[t0], i1 = inv[t1];
-    const float k0 = i0 * i0 * (red[t0] + red[C + t0]);
-    const float k1 = i1 * i1 * (red[t1] + red[C + t1]);
-#pragma unroll
-    for (int i = 0; i < NC; ++i) {
-        const int c = 8 * (h * NC + i) + 2 * q;
-        const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(xs + t0 * XS + c));
-        const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(xs + t1 * XS + c));
-        *reinterpret_cast<uint32_t *>(stage + t0 * XS + c) =
-            pack_bf16(i0 * (acc[i][0] - x0.x * k0), i0 * (acc[i][1] - x0.y * k0));
-        *reinterpret_cast<uint32_t *>(stage + t1 * XS + c) =
-            pack_bf16(i1 * (acc[i][2] - x1.x * k1), i1 * (acc[i][3] - x1.y * k1));
-    }
-}
-
-// Store 16 staged rows (row block rb), column half h, of a [C][XS] bf16 stage to global rows
-// n0 + t (t < cnt) of a [N, D] slice.
-template <int D, int XS>
-__device__ __forceinline__ void store_rows(const bf16 *stage, bf16 *__restrict__ dst, int64_t n0, int cnt, int rb,
-                                           int h, int lane)
-{
-    constexpr int CHR = D / 16;
-    for (int i = lane; i < 16 * CHR; i += 32) {
-        const int rr = i / CHR, cc = i - rr * CHR;
-        const int t = 16 * rb + rr;
-        if (t < cnt) {
-            const int c = h * (D / 2) + 8 * cc;
-            *reinterpret_cast<uint4 *>(dst + (n0 + t) * D + c) = *reinterpret_cast<const uint4 *>(stage + t * XS + c);
-        }
-    }
 }
 
 // Lower-triangular ones as an A fragment: element (row t, col j) = 1 if j <= t, for the 16x16
@@ -314,6 +259,28 @@ __device__ __forceinline__ void tril_ones_fragment(int row0, int col0, int lane,
         const int j = col0 + 2 * q + 8 * (r >> 1);
         a[r] = pack_bf16(j <= t ? 1.f : 0.f, j + 1 <= t ? 1.f : 0.f);
     }
+}
+
+// Hyperplanes as bf16 hi rows [0, LPP) and lo rows [LPP, 2 LPP) of a [2 LPP][XS] tile; rows
+// past L * P are zero.
+template <int D, int XS>
+__device__ __forceinline__ void load_w_split(const float *__restrict__ W, int LP, bf16 *wc)
+{
+    for (int i = threadIdx.x; i < LPP * D; i += NTH) {
+        const int row = i / D, k = i - row * D;
+        const float w = row < LP ? W[row * D + k] : 0.f;
+        bf16 hi, lo;
+        split_bf16(w, hi, lo);
+        wc[row * XS + k] = hi;
+        wc[(LPP + row) * XS + k] = lo;
+    }
+}
+
+// Zero-fills n bytes (multiple of 16) of shared memory.
+__device__ __forceinline__ void zero_smem(void *p, int nbytes)
+{
+    uint4 *q = reinterpret_cast<uint4 *>(p);
+    for (int i = threadIdx.x; i < nbytes / 16; i += NTH) q[i] = make_uint4(0, 0, 0, 0);
 }
 
 }  // namespace tc
