@@ -97,6 +97,7 @@ constexpr size_t kMaxSmem = 227 * 1024;
 struct Plan {
     Dims D{};
     bool causal = false, bf16 = false;
+    bool nc5 = false;      // non-causal bf16 problem on the tcgen05 kernels
     int nsplit = 1;        // token ranges (non-causal) or segments (causal) per (b, h)
     int64_t seg_len = 0;   // tokens per range, a multiple of the token tile
     size_t E = 0;          // floats per sketch: LR * (d + 1)
@@ -134,10 +135,13 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     pl.bf16 = s->dtype == RACE_BF16;
     pl.E = (size_t)D.LR * D.dv;
 
-    const int TT = 64;  // segment granule: a multiple of every kernel's token tile
+    pl.nc5 = !pl.causal && pl.bf16 && nc5_supported(D);
+    const int TT = pl.nc5 ? nc5_tile() : 64;  // segment granule: a multiple of every kernel's token tile
     const int64_t ntiles = ceil_div(D.N, TT);
     int64_t want;
-    if (!pl.causal) {
+    if (pl.nc5) {
+        want = ceil_div((int64_t)kSMs * nc5_sketch_ctas_per_sm(D), D.BH);
+    } else if (!pl.causal) {
         const int64_t chunks = ceil_div(D.LR, 64);
         want = ceil_div(4 * kSMs, chunks * D.BH);
     } else {
@@ -210,6 +214,14 @@ int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float
             return RACE_OK;
         }
     }
+    if constexpr (std::is_same<T, bf16_t>::value) {
+        if (pl.nc5) {
+            RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st));
+            RACE_TRY(launch_combine(D, part, S, pl.nsplit, 0, st));
+            RACE_TRY(launch_nc5_readout(D, Q, W, S, O, err, st));
+            return RACE_OK;
+        }
+    }
     RACE_TRY(launch_sketch<T>(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, 0, st));
     if (!pl.causal) {
         RACE_TRY(launch_combine(D, part, S, pl.nsplit, 0, st));
@@ -244,6 +256,21 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
             RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
             RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, st));
+            return RACE_OK;
+        }
+    }
+    if constexpr (std::is_same<T, bf16_t>::value) {
+        if (pl.nc5) {
+            if (!S) {
+                float *Sw = (float *)(ws + pl.off_sk);
+                RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st));
+                RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 0, st));
+                S = Sw;
+            }
+            RACE_TRY(launch_bwd_query<T>(D, Q, dO, W, S, dQ, aux, st));
+            RACE_TRY(launch_nc5_sketch(D, Q, dO, aux, W, pl.seg_len, pl.nsplit, gpart, err, st));
+            RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 0, st));
+            RACE_TRY(launch_bwd_key<T>(D, K, V, W, gsk, dK, dV, st));
             return RACE_OK;
         }
     }

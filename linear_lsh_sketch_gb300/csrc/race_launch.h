@@ -69,4 +69,13 @@ cudaError_t launch_causal_tc_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t
                                     int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err,
                                     cudaStream_t st);
 
+// ---------------------------------------------------------------- tcgen05 non-causal path (bf16)
+bool nc5_supported(const Dims &D);
+int nc5_tile();
+int nc5_sketch_ctas_per_sm(const Dims &D);
+cudaError_t launch_nc5_sketch(const Dims &D, const bf16_t *X, const bf16_t *Y, const float2 *aux, const float *W,
+                              int64_t seg_len, int nsplit, float *part, unsigned *err, cudaStream_t st);
+cudaError_t launch_nc5_readout(const Dims &D, const bf16_t *Q, const float *W, const float *S, bf16_t *O,
+                               unsigned *err, cudaStream_t st);
+
 }  // namespace race

@@ -1,0 +1,159 @@
+// race_nc5_common.cuh -- pieces shared by the tcgen05 (TMEM accumulator) RACE kernels: tile
+// geometry, the hyperplane operand tiles, row norms, the bucket-feature writer and bounded
+// mbarrier waits.
+//
+// Token tiles are C = 128 rows of a [N, d] slice, loaded by TMA as d / 64 SW128 column blocks
+// (race_tc5.cuh).  Eight warps share a tile: warp w reads TMEM lanes 32 (w % 4) .. + 31, so
+// thread (w, lane) owns token row t = 32 (w % 4) + lane, and the two warps of a lane quadrant
+// (half h = w / 4) split that row's work.
+#pragma once
+
+#include "race_common.cuh"
+#include "race_tc5.cuh"
+
+namespace race {
+namespace nc5 {
+
+using bf16 = __nv_bfloat16;
+using namespace race::tc5;
+
+constexpr int C = 128;           // tokens per tile
+constexpr int NTH = 256;         // threads per CTA
+constexpr uint32_t BLK = C * 128;  // bytes of one SW128 column block of a token tile
+constexpr int LPP = 32;          // projection columns (L * P <= 32): z occupies 32 TMEM columns
+constexpr uint32_t WBLK = LPP * 128;  // bytes of one SW128 column block of a hyperplane tile
+constexpr unsigned kErrTimeout = 1u;
+
+// Hyperplanes as bf16 hi and lo SW128 tiles [D / 64][LPP rows][64]: row p = W row p (p < L P),
+// zero rows after; hi + lo == W to about 2^-16 relative.
+template <int D>
+__device__ __forceinline__ void load_w_tiles(const float *__restrict__ W, int LP, unsigned char *whi,
+                                             unsigned char *wlo)
+{
+    for (int i = threadIdx.x; i < LPP * (D / 8); i += NTH) {
+        const int row = i / (D / 8), c = i - row * (D / 8);  // 8-element chunk c of row `row`
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float w0 = 0.f, w1 = 0.f;
+            if (row < LP) {
+                w0 = W[row * D + 8 * c + 2 * j];
+                w1 = W[row * D + 8 * c + 2 * j + 1];
+            }
+            const bf16 h0 = __float2bfloat16_rn(w0), h1 = __float2bfloat16_rn(w1);
+            h[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+            l[j] = mma::pack_bf16(w0 - __bfloat162float(h0), w1 - __bfloat162float(h1));
+        }
+        const uint32_t off = (c >> 3) * WBLK + sw_chunk(row, c & 7);
+        st_shared_v4(smem_addr(whi) + off, h[0], h[1], h[2], h[3]);
+        st_shared_v4(smem_addr(wlo) + off, l[0], l[1], l[2], l[3]);
+    }
+}
+
+__device__ __forceinline__ void zero_region(unsigned char *p, uint32_t nbytes)
+{
+    for (uint32_t i = threadIdx.x * 16; i < nbytes; i += NTH * 16) st_shared_v4(smem_addr(p) + i, 0, 0, 0, 0);
+}
+
+// Half h's share of sum_k x[t][k]^2 for row t of a token tile at `tile` (D / 64 column blocks).
+template <int D>
+__device__ __forceinline__ float half_sumsq(uint32_t tile, int t, int h)
+{
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+        const int c = h * (D / 16) + j;
+        s += sumsq8(ld_shared_v4(tile + (c >> 3) * BLK + sw_chunk(t, c & 7)));
+    }
+    return s;
+}
+
+// Bounded wait by every thread, then a CTA-wide vote: true if any thread's wait ran out.
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity)
+{
+    const bool ok = mbar_wait(bar, parity);
+    return __syncthreads_or(!ok) != 0;
+}
+
+// Writes one token row of bucket features into an SW128 feature tile ([lr / 64][C][64] bf16,
+// lr = l R + r), for the tables half h owns: tables l with l % 2 == h when R >= 8, else 16-byte
+// chunks (8 / R tables each) with chunk % 2 == h.  z holds the row's projections W x (LPP
+// columns), inv = 1 / |x|; phi^(l)_r = prod_t sigmoid(2 beta u_t v_{r,t}) with
+// u = tanh(z inv) (the softmax over hypercube corners in product form), times `scale`.
+// Tables >= L inside a written chunk are zero.
+template <int P>
+__device__ __forceinline__ void write_features(const float (&z)[LPP], float inv, float beta, int L, int h,
+                                               float scale, int t, uint32_t ftile)
+{
+    constexpr int R = 1 << P;
+    constexpr int LMAX = LPP / P;
+    if constexpr (R >= 8) {
+#pragma unroll
+        for (int l = 0; l < LMAX; ++l) {
+            if (l < L && (l & 1) == h) {
+                float u[P], ph[R];
+#pragma unroll
+                for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+                tc::bucket_probs<P>(u, beta, ph);
+#pragma unroll
+                for (int j = 0; j < R / 8; ++j) {
+                    const int c = l * (R / 8) + j;
+                    st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7),
+                                 mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
+                                 mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
+                                 mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
+                                 mma::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
+                }
+            }
+        }
+    } else {
+        constexpr int TPC = 8 / R;
+        constexpr int NCH = (LMAX + TPC - 1) / TPC;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            if (c * TPC < L && (c & 1) == h) {
+                float v[8];
+#pragma unroll
+                for (int k = 0; k < TPC; ++k) {
+                    const int l = c * TPC + k;
+                    float ph[R];
+                    if (l < L && l < LMAX) {
+                        float u[P];
+#pragma unroll
+                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[(l < LMAX ? l : 0) * P + p] * inv);
+                        tc::bucket_probs<P>(u, beta, ph);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < R; ++r) ph[r] = 0.f;
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) v[k * R + r] = ph[r] * scale;
+                }
+                st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7), mma::pack_bf16(v[0], v[1]),
+                             mma::pack_bf16(v[2], v[3]), mma::pack_bf16(v[4], v[5]), mma::pack_bf16(v[6], v[7]));
+            }
+        }
+    }
+}
+
+// Instruction descriptors.
+__host__ __device__ constexpr uint32_t idesc_proj() { return idesc_bf16(128, LPP, 0, 0); }
+
+// Issues z = X (W_hi + W_lo)^T for a token tile (D / 16 K steps per hyperplane copy).
+template <int D>
+__device__ __forceinline__ void issue_projection(uint32_t tz, uint32_t xtile, uint32_t whi, uint32_t wlo)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t ko = (ks >> 2) * BLK + (ks & 3) * 32, kw = (ks >> 2) * WBLK + (ks & 3) * 32;
+        umma(tz, desc_k(xtile + ko), desc_k(whi + kw), idesc_proj(), ks > 0);
+    }
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t ko = (ks >> 2) * BLK + (ks & 3) * 32, kw = (ks >> 2) * WBLK + (ks & 3) * 32;
+        umma(tz, desc_k(xtile + ko), desc_k(wlo + kw), idesc_proj(), true);
+    }
+}
+
+}  // namespace nc5
+}  // namespace race

@@ -7,6 +7,8 @@ import torch
 
 import linear_lsh_sketch_gb300 as race
 from linear_lsh_sketch_gb300.workloads import CONFIGS, Workload, make_inputs
+import oracle
+from linear_lsh_sketch_gb300.workloads import as_oracle_array
 from parity import assert_close, gpu_run, inputs_on_gpu, oracle_run
 
 pytestmark = pytest.mark.gpu
@@ -105,6 +107,30 @@ def test_beta_zero_mean():
         V = inp["V"].double().cpu()[0, 0]
         ref = V.cumsum(0) / torch.arange(1, 201, dtype=torch.float64)[:, None] if causal else V.mean(0).expand(200, 32)
         assert (O[0, 0] - ref).abs().max() < 1e-5
+
+
+@pytest.mark.parametrize("w", [
+    W_("sk_bf_d64", 1, 2, 1000, 64, 3, 3, False, "bf16"),
+    W_("sk_bf_d128_lr256", 1, 2, 700, 128, 6, 4, False, "bf16", clusters=8),
+    W_("sk_bf_p2_l5", 2, 1, 333, 128, 2, 5, False, "bf16"),
+    W_("sk_bf_p5_l5", 1, 1, 515, 64, 5, 5, False, "bf16"),
+], ids=lambda w: w.name)
+def test_noncausal_sketch_state(w):
+    """The saved non-causal sketch [A | B] = Phi_K^T [V | 1] (sketch rows L * R, d + 1 columns)
+    against the oracle's, normwise: relative L2 error over each (b, h) sketch."""
+    inp = inputs_on_gpu(w, seed=6)
+    shape = race.make_shape(w.B, w.H, w.N, w.d, w.torch_dtype)
+    state = torch.empty(race.race_attn_state_bytes(shape, w.L, w.P, w.causal), dtype=torch.uint8, device="cuda")
+    race.race_attn_fwd(inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal, state=state)
+    torch.cuda.synchronize()
+    got = state.view(torch.float32).double().cpu().numpy().reshape(w.B, w.H, w.LR, w.d + 1)
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V")}
+    _, ref = oracle.forward(a["Q"], a["K"], a["V"], inp["W"].double().cpu().numpy(), w.beta, False,
+                            want_sketch=True)
+    for b in range(w.B):
+        for h in range(w.H):
+            e = np.linalg.norm(got[b, h] - ref[b, h]) / np.linalg.norm(ref[b, h])
+            assert e <= 1e-2, "%s sketch (%d, %d) error %.3e" % (w.name, b, h, e)
 
 
 def _sampled_rows(N, n, seed):
