@@ -267,10 +267,10 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 0, st));
                 S = Sw;
             }
-            RACE_TRY(launch_bwd_query<T>(D, Q, dO, W, S, dQ, aux, st));
+            RACE_TRY(launch_nc5_bwd_query(D, Q, dO, W, S, dQ, aux, err, st));
             RACE_TRY(launch_nc5_sketch(D, Q, dO, aux, W, pl.seg_len, pl.nsplit, gpart, err, st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 0, st));
-            RACE_TRY(launch_bwd_key<T>(D, K, V, W, gsk, dK, dV, st));
+            RACE_TRY(launch_nc5_bwd_key(D, K, V, W, gsk, dK, dV, err, st));
             return RACE_OK;
         }
     }
