@@ -98,6 +98,7 @@ struct Plan {
     Dims D{};
     bool causal = false, bf16 = false;
     bool nc5 = false;      // non-causal bf16 problem on the tcgen05 kernels
+    bool c5 = false;       // causal bf16 problem whose forward runs on the tcgen05 kernels
     int nsplit = 1;        // token ranges (non-causal) or segments (causal) per (b, h)
     int64_t seg_len = 0;   // tokens per range, a multiple of the token tile
     size_t E = 0;          // floats per sketch: LR * (d + 1)
@@ -136,7 +137,9 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     pl.E = (size_t)D.LR * D.dv;
 
     pl.nc5 = !pl.causal && pl.bf16 && nc5_supported(D);
-    const int TT = pl.nc5 ? nc5_tile() : 64;  // segment granule: a multiple of every kernel's token tile
+    pl.c5 = pl.causal && pl.bf16 && c5_supported(D);
+    // segment granule: a multiple of every kernel's token tile
+    const int TT = (pl.nc5 || pl.c5) ? nc5_tile() : 64;
     const int64_t ntiles = ceil_div(D.N, TT);
     int64_t want;
     if (pl.nc5) {
@@ -207,6 +210,13 @@ int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float
     unsigned *err = (unsigned *)(ws + pl.off_status);
     RACE_TRY(cudaMemsetAsync(err, 0, sizeof(unsigned), st));
     if constexpr (std::is_same<T, bf16_t>::value) {
+        if (pl.c5) {
+            // segment sums of the causal sketch = the non-causal sketch of each segment
+            RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st));
+            RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
+            RACE_TRY(launch_c5_fwd(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, err, st));
+            return RACE_OK;
+        }
         if (use_tc<T>(pl)) {
             RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
             RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
@@ -249,7 +259,10 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
         if (use_tc<T>(pl) && causal_tc_bwd_supported(D)) {
             if (!S) {
                 float *Sw = (float *)(ws + pl.off_sk);
-                RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
+                if (pl.c5)
+                    RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st));
+                else
+                    RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 1, st));
                 S = Sw;
             }

@@ -1,0 +1,534 @@
+// race_c5_fwd.cu -- tcgen05 (TMEM accumulator) causal RACE attention forward, bf16 tensors.
+//
+// Algorithm 2 of the paper ("RACE Attention" slides, frame "Causality is a prefix update of the
+// same statistics"; reading notes section 2.6) evaluated in chunks of C = 128 tokens.  With F the
+// concatenated bucket features (L R columns) of a chunk and S = [A | B] the sketch of every
+// earlier token (A: L R x d content, B: L R mass):
+//
+//   [num | den] = mask_{j <= t}(F_Q F_K^T) [V | 1]  +  F_Q [A | B]      O = num / den
+//   A += F_K^T V,   B += F_K^T 1
+//
+// One CTA walks one segment of a (batch, head) sequence; the sketch at the segment start comes
+// from the segment sums (the non-causal sketch kernel restricted to each segment) and an
+// exclusive scan over segments.  Per chunk, on the tensor cores (M = 128, fp32 in TMEM):
+//   z = X (W_hi + W_lo)^T for the Q and K tiles;
+//   scores F_Q F_K^T with F_Q in TMEM (A operand) and F_K in a swizzled shared tile;
+//   P = the causally masked scores, written back to TMEM as bf16 (A operand);
+//   [num | den] = P V and P 1 plus F_Q [A | B], with [A | B] in shared memory as bf16 hi + lo
+//   (about 16 mantissa bits);
+//   A^T += V^T F_K (M = d, N = L R) and B += F_K^T 1 (M = L R), both accumulating in TMEM over
+//   the whole segment.
+// On CUDA cores: row norms, bucket features (tanh, products of sigmoids), the causal mask, the
+// num / den epilogue, and the conversion of the TMEM sketch to its bf16 operand copy.
+// Q and K tiles are single-buffered (refilled once the projection has read them); V tiles are
+// double-buffered and each also stages its chunk's output for the TMA store.
+#include "race_launch.h"
+#include "race_nc5_common.cuh"
+
+namespace race {
+namespace c5 {
+
+using namespace race::nc5;
+
+// TMEM columns (512 allocated).
+constexpr uint32_t T_O = 0;      // [num | den]: d + 16 columns
+constexpr uint32_t T_ST = 144;   // A^T (lanes = d), L R (<= 64) columns
+constexpr uint32_t T_MS = 208;   // B (lanes = sketch row), 16 columns (column 0 used)
+constexpr uint32_t T_ZQ = 224;   // projections of the Q tile
+constexpr uint32_t T_ZK = 256;   // projections of the K tile
+constexpr uint32_t T_FQ = 288;   // F_Q as bf16 pairs (A operand), L R / 2 columns
+constexpr uint32_t T_SC = 320;   // scores, 128 columns
+constexpr uint32_t T_P = 448;    // masked scores as bf16 pairs (A operand), 64 columns
+constexpr uint32_t T_COLS = 512;
+
+struct FwdLayout {
+    uint32_t q, k, v, fk, shi, slo, whi, wlo, ones, zero, bar, slot, bytes, kbb, sblk;
+    __host__ __device__ FwdLayout(int D)
+    {
+        kbb = (uint32_t)(D / 64) * BLK;  // bytes of one token tile
+        sblk = (uint32_t)(D + 16) * 128;
+        q = 0;
+        k = q + kbb;
+        v = k + kbb;       // two stages
+        fk = v + 2 * kbb;  // two 64-column blocks (the second stays zero)
+        shi = fk + 2 * BLK;
+        slo = shi + sblk;
+        whi = slo + sblk;
+        wlo = whi + (uint32_t)(D / 64) * WBLK;
+        ones = wlo + (uint32_t)(D / 64) * WBLK;
+        zero = ones + 4096;  // a zero 64-column block (d = 64: the upper half of V^T)
+        bar = zero + (D == 64 ? BLK : 0);
+        slot = bar + 64;
+        bytes = slot + 16;
+    }
+};
+
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, bf16 v)
+{
+    asm volatile("st.shared.b16 [%0], %1;\n" ::"r"(addr), "h"(*reinterpret_cast<unsigned short *>(&v)) : "memory");
+}
+
+__device__ __forceinline__ float bf16_rest(float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Writes this thread's lane of the fp32 TMEM sketch (row d of A^T, row lr of B) into the bf16
+// read-out operand: K-major rows n = output column (rows 0 .. d-1 content, row d mass), the 64
+// columns = sketch rows.  h = 0 writes the hi copy, h = 1 the lo copy (x - bf16(x)).
+template <int D>
+__device__ __forceinline__ void sketch_to_operand(uint32_t tlane, int q4, int lane, int h, int LR, int lrp,
+                                                  uint32_t shi, uint32_t slo)
+{
+    const int row = 32 * q4 + lane;
+    const uint32_t dst = h ? slo : shi;
+    if (32 * q4 < D) {  // content: lane = d
+        float v[64];
+        {
+            float a[32];
+            ld32(tlane + T_ST, a);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = a[j];
+        }
+        if (lrp > 32) {
+            float a[32];
+            ld32(tlane + T_ST + 32, a);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[32 + j] = a[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[32 + j] = 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (8 * c < lrp) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float x0 = 8 * c + 2 * j < LR ? v[8 * c + 2 * j] : 0.f;
+                    float x1 = 8 * c + 2 * j + 1 < LR ? v[8 * c + 2 * j + 1] : 0.f;
+                    if (h) {
+                        x0 = bf16_rest(x0);
+                        x1 = bf16_rest(x1);
+                    }
+                    w[j] = mma::pack_bf16(x0, x1);
+                }
+                st_shared_v4(dst + sw_chunk(row, c), w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+    if (32 * q4 < lrp) {  // mass: lane = sketch row
+        float m[1];
+        ldn<1>(tlane + T_MS, m);
+        float x = row < LR ? m[0] : 0.f;
+        if (h) x = bf16_rest(x);
+        st_shared_b16(dst + sw_elem(D, row), __float2bfloat16_rn(x));
+    }
+}
+
+// Failure bookkeeping: how many loads were issued / waited on per barrier.
+struct LoadCount {
+    int issued = 0, waited = 0;
+};
+
+template <int D, int P>
+__global__ void __launch_bounds__(NTH, 1)
+    k_causal_fwd5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, Dims Dm,
+                  const float *__restrict__ W, const float *__restrict__ S0, int64_t seg_len, int nseg,
+                  unsigned *__restrict__ err)
+{
+    constexpr int KB = D / 64;
+    constexpr int R = 1 << P;
+    constexpr int LMAX = LPP / P;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023) & ~1023u;
+    unsigned char *sm = smem_raw + (base - raw);
+    const FwdLayout Ly(D);
+    const uint32_t bar_qk = base + Ly.bar, bar_proj = bar_qk + 8, bar_sc = bar_qk + 16, bar_mma = bar_qk + 24,
+                   bar_v = bar_qk + 32;  // two
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = warp >> 2;
+    const int t = 32 * q4 + lane;  // token row (TMEM lane) of this thread
+    const int s = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int64_t n_begin = (int64_t)s * seg_len;
+    const int64_t n_end = min(Dm.N, n_begin + seg_len);
+    const int nchunk = n_end > n_begin ? (int)((n_end - n_begin + C - 1) / C) : 0;
+    const int LR = Dm.LR, lrp = (LR + 15) & ~15;
+    const float beta = Dm.beta;
+    const int L = Dm.L;
+
+    // ---- set-up
+    if (warp == 0) tmem_alloc(base + Ly.slot, T_COLS);
+    zero_region(sm + Ly.fk, 2 * BLK);
+    zero_region(sm + Ly.shi, 2 * Ly.sblk);
+    init_mass_tile(sm + Ly.ones, true);
+    if (D == 64) zero_region(sm + Ly.zero, BLK);
+    load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    if (tid == 0) {
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_proj, 1);
+        mbar_init(bar_sc, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_v + 8, 1);
+        tc::fence_mbar_init();
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmO);
+    }
+    tc::fence_proxy_async();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Ly.slot);
+    const uint32_t tlane = tmem + ((uint32_t)(32 * q4) << 16);
+
+    // sketch at the segment start -> TMEM accumulators (A^T lanes = d, B lanes = sketch row); the
+    // F_Q operand columns past L R stay zero
+    {
+        const float *Sb = S0 + ((int64_t)bh * nseg + s) * LR * (D + 1);
+        if (h == 0) {
+            if (t < D) {
+                for (int c0 = 0; c0 < lrp; c0 += 8) {
+                    uint32_t r[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r[j] = __float_as_uint(c0 + j < LR ? Sb[(c0 + j) * (D + 1) + t] : 0.f);
+                    stn<8>(tlane + T_ST + c0, r);
+                }
+            }
+            const uint32_t m[1] = {__float_as_uint(t < LR ? Sb[t * (D + 1) + D] : 0.f)};
+            stn<1>(tlane + T_MS, m);
+        } else {
+            const uint32_t zr[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int c0 = 0; c0 < 32; c0 += 8) stn<8>(tlane + T_FQ + c0, zr);
+        }
+        wait_st();
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    sketch_to_operand<D>(tlane, q4, lane, h, LR, lrp, base + Ly.shi, base + Ly.slo);
+
+    LoadCount cqk, cv[2];
+    auto load_qk = [&](int c) {
+        const int y = (int)(n_begin + (int64_t)c * C);
+        mbar_arrive_expect_tx(bar_qk, 2 * KB * BLK);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+            tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar_qk);
+            tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar_qk);
+        }
+    };
+    auto load_v = [&](int c) {
+        const int y = (int)(n_begin + (int64_t)c * C);
+        const uint32_t b = bar_v + 8 * (c & 1);
+        mbar_arrive_expect_tx(b, KB * BLK);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.v + (c & 1) * Ly.kbb + kb * BLK, &tmV, 64 * kb, y, (int)bh, b);
+    };
+    if (tid == 0 && nchunk > 0) {
+        load_qk(0);
+        load_v(0);
+        if (nchunk > 1) load_v(1);
+    }
+    cqk.issued = nchunk > 0 ? 1 : 0;
+    cv[0].issued = nchunk > 0 ? 1 : 0;
+    cv[1].issued = nchunk > 1 ? 1 : 0;
+
+    // output epilogue of chunk c: O = num / den (this half's columns), staged in V stage c & 1
+    auto epilogue = [&](int c) {
+        const uint32_t stage = base + Ly.v + (c & 1) * Ly.kbb;
+        float v[16];
+        ld16(tlane + T_O + D, v);
+        const float rd = __frcp_rn(v[0]);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+            const int c0 = h * (D / 2) + 16 * cc;
+            ld16(tlane + T_O + c0, v);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int ch = (c0 >> 3) + j;
+                st_shared_v4(stage + (ch >> 3) * BLK + sw_chunk(t, ch & 7),
+                             mma::pack_bf16(v[8 * j] * rd, v[8 * j + 1] * rd),
+                             mma::pack_bf16(v[8 * j + 2] * rd, v[8 * j + 3] * rd),
+                             mma::pack_bf16(v[8 * j + 4] * rd, v[8 * j + 5] * rd),
+                             mma::pack_bf16(v[8 * j + 6] * rd, v[8 * j + 7] * rd));
+            }
+        }
+    };
+    auto store_out = [&](int c) {
+        const uint32_t stage = base + Ly.v + (c & 1) * Ly.kbb;
+        const int y = (int)(n_begin + (int64_t)c * C);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) tma_store(&tmO, 64 * kb, y, (int)bh, stage + kb * BLK);
+        bulk_commit();
+    };
+
+    bool failed = false;
+    int c = 0;
+    for (; c < nchunk; ++c) {
+        const int64_t n0 = n_begin + (int64_t)c * C;
+        const int cnt = (int)min((int64_t)C, n_end - n0);
+        const uint32_t vst = base + Ly.v + (c & 1) * Ly.kbb;
+        if (wait_all(bar_qk, c & 1)) {
+            failed = true;
+            break;
+        }
+        cqk.waited++;
+        if (tid == 0) {
+            fence_after();
+            issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
+            issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
+            commit(bar_proj);
+        }
+        // row norm of this thread's row: warps 0-3 Q rows, warps 4-7 K rows
+        float inv;
+        {
+            const uint32_t tile = base + (h ? Ly.k : Ly.q);
+            const float ss = half_sumsq<D>(tile, t, 0) + half_sumsq<D>(tile, t, 1);
+            inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+        }
+        // output of the previous chunk and the sketch operand for this chunk's read-out
+        if (c >= 1) {
+            if (wait_all(bar_mma, (c - 1) & 1)) {
+                failed = true;
+                break;
+            }
+            fence_after();
+            epilogue(c - 1);
+            sketch_to_operand<D>(tlane, q4, lane, h, LR, lrp, base + Ly.shi, base + Ly.slo);
+            tc::fence_proxy_async();
+            fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                store_out(c - 1);
+                if (c + 1 < nchunk) {
+                    bulk_wait_read0();  // the store read V stage (c + 1) & 1
+                    load_v(c + 1);
+                }
+            }
+            if (c + 1 < nchunk) cv[(c + 1) & 1].issued++;
+        }
+        if (wait_all(bar_proj, c & 1)) {
+            failed = true;
+            break;
+        }
+        fence_after();
+        if (tid == 0 && c + 1 < nchunk) load_qk(c + 1);  // projection and norms have read the tiles
+        if (c + 1 < nchunk) cqk.issued++;
+
+        // features: warps 0-3 the Q row t (-> TMEM), warps 4-7 the K row t (-> shared F_K tile)
+        {
+            float z[LPP];
+            {
+                float a[32];
+                ld32(tlane + (h ? T_ZK : T_ZQ), a);
+#pragma unroll
+                for (int k = 0; k < LPP; ++k) z[k] = a[k];
+            }
+            const float scale = (h == 0 || t < cnt) ? 1.f : 0.f;
+#pragma unroll
+            for (int l = 0; l < LMAX; ++l) {
+                if (l < L) {
+                    float u[P], ph[R];
+#pragma unroll
+                    for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+                    tc::bucket_probs<P>(u, beta, ph);
+                    if (h == 0) {
+                        if constexpr (R >= 16) {
+#pragma unroll
+                            for (int b = 0; b < R / 16; ++b) {
+                                uint32_t r[8];
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(ph[16 * b + 2 * j], ph[16 * b + 2 * j + 1]);
+                                stn<8>(tlane + T_FQ + (l * R) / 2 + 8 * b, r);
+                            }
+                        } else {
+                            uint32_t r[R / 2];
+#pragma unroll
+                            for (int j = 0; j < R / 2; ++j) r[j] = mma::pack_bf16(ph[2 * j], ph[2 * j + 1]);
+                            stn<R / 2>(tlane + T_FQ + (l * R) / 2, r);
+                        }
+                    } else {
+                        if constexpr (R >= 8) {
+#pragma unroll
+                            for (int j = 0; j < R / 8; ++j) {
+                                const int ch = l * (R / 8) + j;
+                                st_shared_v4(base + Ly.fk + sw_chunk(t, ch),
+                                             mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
+                                             mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
+                                             mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
+                                             mma::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
+                            }
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < R; r += 2) {
+                                const int lr = l * R + r;
+                                const uint32_t w = mma::pack_bf16(ph[r] * scale, ph[r + 1] * scale);
+                                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fk + sw_elem(t, lr)), "r"(w)
+                                             : "memory");
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        wait_st();
+        tc::fence_proxy_async();
+        fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after();
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
+            for (int ks = 0; ks < lrp / 16; ++ks)
+                umma_ts(tmem + T_SC, tmem + T_FQ + 8 * ks, desc_k(base + Ly.fk + ks * 32), id_s, ks > 0);
+            commit(bar_sc);
+        }
+        if (wait_all(bar_sc, c & 1)) {
+            failed = true;
+            break;
+        }
+        fence_after();
+        // causal mask j <= t on this half's 64 key columns -> bf16 P in TMEM
+        {
+            const int j0 = 64 * h;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float a[32];
+                ld32(tlane + T_SC + j0 + 32 * b, a);
+                uint32_t r[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int jj = j0 + 32 * b + 2 * j;
+                    r[j] = mma::pack_bf16(jj <= t ? a[2 * j] : 0.f, jj + 1 <= t ? a[2 * j + 1] : 0.f);
+                }
+                uint32_t r0[8], r1[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    r0[j] = r[j];
+                    r1[j] = r[8 + j];
+                }
+                stn<8>(tlane + T_P + j0 / 2 + 16 * b, r0);
+                stn<8>(tlane + T_P + j0 / 2 + 16 * b + 8, r1);
+            }
+        }
+        wait_st();
+        if (wait_all(bar_v + 8 * (c & 1), (c >> 1) & 1)) {
+            failed = true;
+            break;
+        }
+        cv[c & 1].waited++;
+        fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after();
+            constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
+            constexpr uint32_t id_p1 = idesc_bf16(128, 16, 0, 0);
+            constexpr uint32_t id_ro = idesc_bf16(128, D + 16, 0, 0);
+            const uint32_t id_up = idesc_bf16(128, lrp, 1, 1);
+            constexpr uint32_t id_ms = idesc_bf16(128, 16, 1, 0);
+            const uint32_t vlbo = D == 128 ? BLK : (Ly.zero - (Ly.v + (c & 1) * Ly.kbb));
+#pragma unroll
+            for (int ks = 0; ks < C / 16; ++ks) {
+                umma_ts(tmem + T_O, tmem + T_P + 8 * ks, desc_mn(vst + ks * 2048, BLK), id_pv, ks > 0);
+                umma_ts(tmem + T_O + D, tmem + T_P + 8 * ks, desc_k(base + Ly.ones + (ks >> 2) * 2048 + (ks & 3) * 32),
+                        id_p1, ks > 0);
+            }
+            for (int ks = 0; ks < lrp / 16; ++ks) {
+                umma_ts(tmem + T_O, tmem + T_FQ + 8 * ks, desc_k(base + Ly.shi + ks * 32), id_ro, true);
+                umma_ts(tmem + T_O, tmem + T_FQ + 8 * ks, desc_k(base + Ly.slo + ks * 32), id_ro, true);
+            }
+#pragma unroll
+            for (int ks = 0; ks < C / 16; ++ks) {
+                umma(tmem + T_ST, desc_mn(vst + ks * 2048, vlbo), desc_mn(base + Ly.fk + ks * 2048, BLK), id_up, true);
+                umma(tmem + T_MS, desc_mn(base + Ly.fk + ks * 2048, BLK),
+                     desc_k(base + Ly.ones + (ks >> 2) * 2048 + (ks & 3) * 32), id_ms, true);
+            }
+            commit(bar_mma);
+        }
+    }
+    if (!failed && nchunk > 0) {
+        failed = wait_all(bar_mma, (nchunk - 1) & 1);
+        if (!failed) {
+            fence_after();
+            epilogue(nchunk - 1);
+            tc::fence_proxy_async();
+            fence_before();
+            __syncthreads();
+            if (tid == 0) store_out(nchunk - 1);
+        }
+    }
+    if (failed) {
+        if (tid == 0) atomicOr(err, kErrTimeout);
+        // let copies still in flight land before the CTA's shared memory goes away
+        if (cqk.issued > cqk.waited) mbar_wait(bar_qk, cqk.waited & 1);
+        for (int b = 0; b < 2; ++b)
+            if (cv[b].issued > cv[b].waited) mbar_wait(bar_v + 8 * b, cv[b].waited & 1);
+    }
+    if (tid == 0) bulk_wait0();
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after();
+        tmem_dealloc(tmem, T_COLS);
+    }
+}
+
+}  // namespace c5
+
+// ------------------------------------------------------------------ host side
+
+cudaError_t make_token_map(CUtensorMap *map, const void *base, const Dims &D);
+
+bool c5_supported(const Dims &D)
+{
+    return (D.d == 64 || D.d == 128) && D.P >= 1 && D.P <= 6 && D.LP <= nc5::LPP && D.LR <= 64 &&
+           D.N <= 0x7FFFFFFF;
+}
+
+namespace {
+
+template <int D, int P>
+cudaError_t causal_fwd5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                             const CUtensorMap &mo, const float *W, const float *S0, int64_t seg_len, int nseg,
+                             unsigned *err, cudaStream_t st)
+{
+    const c5::FwdLayout Ly(D);
+    const size_t smem = Ly.bytes + 1024;
+    auto kern = c5::k_causal_fwd5<D, P>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel("tc5_causal_fwd", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(nc5::NTH), smem, st, mq,
+                         mk, mv, mo, Dm, W, S0, seg_len, nseg, err);
+}
+
+}  // namespace
+
+cudaError_t launch_c5_fwd(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const float *W,
+                          const float *S0, int64_t seg_len, int nseg, bf16_t *O, unsigned *err, cudaStream_t st)
+{
+    CUtensorMap mq, mk, mv, mo;
+    cudaError_t e = make_token_map(&mq, Q, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mk, K, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mv, V, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mo, O, Dm);
+    if (e != cudaSuccess) return e;
+    switch (Dm.d * 16 + Dm.P) {
+        case 64 * 16 + 1: return causal_fwd5_inst<64, 1>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 2: return causal_fwd5_inst<64, 2>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 3: return causal_fwd5_inst<64, 3>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 4: return causal_fwd5_inst<64, 4>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 5: return causal_fwd5_inst<64, 5>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 6: return causal_fwd5_inst<64, 6>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 1: return causal_fwd5_inst<128, 1>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 2: return causal_fwd5_inst<128, 2>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 3: return causal_fwd5_inst<128, 3>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 4: return causal_fwd5_inst<128, 4>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 5: return causal_fwd5_inst<128, 5>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 6: return causal_fwd5_inst<128, 6>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace race

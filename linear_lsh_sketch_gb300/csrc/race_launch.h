@@ -77,6 +77,9 @@ cudaError_t launch_nc5_sketch(const Dims &D, const bf16_t *X, const bf16_t *Y, c
                               int64_t seg_len, int nsplit, float *part, unsigned *err, cudaStream_t st);
 cudaError_t launch_nc5_readout(const Dims &D, const bf16_t *Q, const float *W, const float *S, bf16_t *O,
                                unsigned *err, cudaStream_t st);
+bool c5_supported(const Dims &D);
+cudaError_t launch_c5_fwd(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const float *W,
+                          const float *S0, int64_t seg_len, int nseg, bf16_t *O, unsigned *err, cudaStream_t st);
 cudaError_t launch_nc5_bwd_query(const Dims &D, const bf16_t *Q, const bf16_t *dO, const float *W, const float *S,
                                  bf16_t *dQ, float2 *aux, unsigned *err, cudaStream_t st);
 cudaError_t launch_nc5_bwd_key(const Dims &D, const bf16_t *K, const bf16_t *V, const float *W, const float *G,

@@ -55,6 +55,18 @@ __device__ __forceinline__ void zero_region(unsigned char *p, uint32_t nbytes)
     for (uint32_t i = threadIdx.x * 16; i < nbytes; i += NTH * 16) st_shared_v4(smem_addr(p) + i, 0, 0, 0, 0);
 }
 
+// The 4 KB mass operand (K-major, N = 16 rows, K = 128 tokens as two 64-token SW128 blocks of
+// 2 KB): row 0 all ones when `ones`, every other element zero.  Row 0 of a swizzle atom is not
+// permuted, so it is the first 128 bytes of each block.  Each address has one writer.
+__device__ __forceinline__ void init_mass_tile(unsigned char *p, bool ones)
+{
+    const uint32_t one2 = ones ? 0x3F803F80u : 0u;
+    for (uint32_t i = threadIdx.x * 16; i < 4096; i += NTH * 16) {
+        const uint32_t v = (i & 2047) < 128 ? one2 : 0u;
+        st_shared_v4(smem_addr(p) + i, v, v, v, v);
+    }
+}
+
 // Half h's share of sum_k x[t][k]^2 for row t of a token tile at `tile` (D / 64 column blocks).
 template <int D>
 __device__ __forceinline__ float half_sumsq(uint32_t tile, int t, int h)

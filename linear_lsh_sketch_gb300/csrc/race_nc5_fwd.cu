@@ -83,15 +83,8 @@ __global__ void __launch_bounds__(NTH, 1)
     // ---- set-up
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
     zero_region(sm + Ly.f, 2 * nmb * BLK);
-    zero_region(sm + Ly.mass, 4096);
+    init_mass_tile(sm + Ly.mass, mode == 0);  // mode 1 writes rows 0 and 1 per tile
     load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
-    if (mode == 0) {
-        // mass operand (K-major, N = 16 rows, K = 128 tokens in two 64-token blocks of 2 KB):
-        // row 0 all ones (row 0 of a swizzle atom is not permuted), other rows zero
-        for (int i = tid; i < 16; i += NTH)
-            st_shared_v4(base + Ly.mass + (i >> 3) * 2048 + (i & 7) * 16, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u,
-                         0x3F803F80u);
-    }
     if (tid == 0) {
         mbar_init(bar_load, 1);
         mbar_init(bar_load + 8, 1);
