@@ -58,7 +58,7 @@ struct FwdLayout {
         ones = wlo + (uint32_t)(D / 64) * WBLK;
         zero = ones + 4096;  // a zero 64-column block (d = 64: the upper half of V^T)
         bar = zero + (D == 64 ? BLK : 0);
-        slot = bar + 64;
+        slot = bar + 128;
         bytes = slot + 16;
     }
 };
@@ -123,13 +123,13 @@ __device__ __forceinline__ void sketch_to_operand(uint32_t tlane, int q4, int la
     }
 }
 
-// Failure bookkeeping: how many loads were issued / waited on per barrier.
-struct LoadCount {
-    int issued = 0, waited = 0;
-};
+constexpr int NTHW = NTH + 32;  // 8 compute warps + 1 control warp (TMA and MMA issue)
+
+// Barrier slots (8 bytes each) after FwdLayout::bar.
+enum : uint32_t { B_QK, B_PROJ, B_SC, B_MMA, B_FEAT, B_MASK, B_SOP, B_V0, B_V1, B_COUNT };
 
 template <int D, int P>
-__global__ void __launch_bounds__(NTH, 1)
+__global__ void __launch_bounds__(NTHW, 1)
     k_causal_fwd5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, Dims Dm,
                   const float *__restrict__ W, const float *__restrict__ S0, int64_t seg_len, int nseg,
@@ -143,11 +143,12 @@ __global__ void __launch_bounds__(NTH, 1)
     const uint32_t base = (raw + 1023) & ~1023u;
     unsigned char *sm = smem_raw + (base - raw);
     const FwdLayout Ly(D);
-    const uint32_t bar_qk = base + Ly.bar, bar_proj = bar_qk + 8, bar_sc = bar_qk + 16, bar_mma = bar_qk + 24,
-                   bar_v = bar_qk + 32;  // two
+    auto bar = [&](uint32_t i) { return base + Ly.bar + 8 * i; };
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = warp >> 2;
-    const int t = 32 * q4 + lane;  // token row (TMEM lane) of this thread
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = (warp >> 2) & 1;
+    const bool compute = warp < 8;
+    const int t = 32 * q4 + lane;  // token row (TMEM lane) of a compute thread
     const int s = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int64_t n_begin = (int64_t)s * seg_len;
@@ -159,18 +160,16 @@ __global__ void __launch_bounds__(NTH, 1)
 
     // ---- set-up
     if (warp == 0) tmem_alloc(base + Ly.slot, T_COLS);
-    zero_region(sm + Ly.fk, 2 * BLK);
-    zero_region(sm + Ly.shi, 2 * Ly.sblk);
-    init_mass_tile(sm + Ly.ones, true);
-    if (D == 64) zero_region(sm + Ly.zero, BLK);
-    load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
-    if (tid == 0) {
-        mbar_init(bar_qk, 1);
-        mbar_init(bar_proj, 1);
-        mbar_init(bar_sc, 1);
-        mbar_init(bar_mma, 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_v + 8, 1);
+    if (compute) {
+        zero_region(sm + Ly.fk, 2 * BLK);
+        zero_region(sm + Ly.shi, 2 * Ly.sblk);
+        init_mass_tile(sm + Ly.ones, true);
+        if (D == 64) zero_region(sm + Ly.zero, BLK);
+        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    }
+    if (tid == NTH) {
+        for (uint32_t i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_FEAT || i == B_MASK || i == B_SOP) ? 8 : 1);
+        *abort = 0;
         tc::fence_mbar_init();
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
@@ -186,7 +185,7 @@ __global__ void __launch_bounds__(NTH, 1)
 
     // sketch at the segment start -> TMEM accumulators (A^T lanes = d, B lanes = sketch row); the
     // F_Q operand columns past L R stay zero
-    {
+    if (compute) {
         const float *Sb = S0 + ((int64_t)bh * nseg + s) * LR * (D + 1);
         if (h == 0) {
             if (t < D) {
@@ -208,265 +207,266 @@ __global__ void __launch_bounds__(NTH, 1)
     fence_before();
     __syncthreads();
     fence_after();
-    sketch_to_operand<D>(tlane, q4, lane, h, LR, lrp, base + Ly.shi, base + Ly.slo);
 
-    LoadCount cqk, cv[2];
-    auto load_qk = [&](int c) {
-        const int y = (int)(n_begin + (int64_t)c * C);
-        mbar_arrive_expect_tx(bar_qk, 2 * KB * BLK);
+    if (!compute) {
+        // ---------------------------------------------------------------- control warp
+        if (lane == 0) {
+            auto load_qk = [&](int c) {
+                const int y = (int)(n_begin + (int64_t)c * C);
+                mbar_arrive_expect_tx(bar(B_QK), 2 * KB * BLK);
 #pragma unroll
-        for (int kb = 0; kb < KB; ++kb) {
-            tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar_qk);
-            tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar_qk);
-        }
-    };
-    auto load_v = [&](int c) {
-        const int y = (int)(n_begin + (int64_t)c * C);
-        const uint32_t b = bar_v + 8 * (c & 1);
-        mbar_arrive_expect_tx(b, KB * BLK);
+                for (int kb = 0; kb < KB; ++kb) {
+                    tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_QK));
+                    tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar(B_QK));
+                }
+            };
+            auto load_v = [&](int c) {
+                const int y = (int)(n_begin + (int64_t)c * C);
+                const uint32_t b = bar(B_V0 + (c & 1));
+                mbar_arrive_expect_tx(b, KB * BLK);
 #pragma unroll
-        for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.v + (c & 1) * Ly.kbb + kb * BLK, &tmV, 64 * kb, y, (int)bh, b);
-    };
-    if (tid == 0 && nchunk > 0) {
-        load_qk(0);
-        load_v(0);
-        if (nchunk > 1) load_v(1);
-    }
-    cqk.issued = nchunk > 0 ? 1 : 0;
-    cv[0].issued = nchunk > 0 ? 1 : 0;
-    cv[1].issued = nchunk > 1 ? 1 : 0;
-
-    // output epilogue of chunk c: O = num / den (this half's columns), staged in V stage c & 1
-    auto epilogue = [&](int c) {
-        const uint32_t stage = base + Ly.v + (c & 1) * Ly.kbb;
-        float v[16];
-        ld16(tlane + T_O + D, v);
-        const float rd = __frcp_rn(v[0]);
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load(base + Ly.v + (c & 1) * Ly.kbb + kb * BLK, &tmV, 64 * kb, y, (int)bh, b);
+            };
+            auto store_out = [&](int c) {
+                const uint32_t stage = base + Ly.v + (c & 1) * Ly.kbb;
+                const int y = (int)(n_begin + (int64_t)c * C);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            const int c0 = h * (D / 2) + 16 * cc;
-            ld16(tlane + T_O + c0, v);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int ch = (c0 >> 3) + j;
-                st_shared_v4(stage + (ch >> 3) * BLK + sw_chunk(t, ch & 7),
-                             mma::pack_bf16(v[8 * j] * rd, v[8 * j + 1] * rd),
-                             mma::pack_bf16(v[8 * j + 2] * rd, v[8 * j + 3] * rd),
-                             mma::pack_bf16(v[8 * j + 4] * rd, v[8 * j + 5] * rd),
-                             mma::pack_bf16(v[8 * j + 6] * rd, v[8 * j + 7] * rd));
-            }
-        }
-    };
-    auto store_out = [&](int c) {
-        const uint32_t stage = base + Ly.v + (c & 1) * Ly.kbb;
-        const int y = (int)(n_begin + (int64_t)c * C);
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb) tma_store(&tmO, 64 * kb, y, (int)bh, stage + kb * BLK);
-        bulk_commit();
-    };
-
-    bool failed = false;
-    int c = 0;
-    for (; c < nchunk; ++c) {
-        const int64_t n0 = n_begin + (int64_t)c * C;
-        const int cnt = (int)min((int64_t)C, n_end - n0);
-        const uint32_t vst = base + Ly.v + (c & 1) * Ly.kbb;
-        if (wait_all(bar_qk, c & 1)) {
-            failed = true;
-            break;
-        }
-        cqk.waited++;
-        if (tid == 0) {
-            fence_after();
-            issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
-            issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
-            commit(bar_proj);
-        }
-        // row norm of this thread's row: warps 0-3 Q rows, warps 4-7 K rows
-        float inv;
-        {
-            const uint32_t tile = base + (h ? Ly.k : Ly.q);
-            const float ss = half_sumsq<D>(tile, t, 0) + half_sumsq<D>(tile, t, 1);
-            inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-        }
-        // output of the previous chunk and the sketch operand for this chunk's read-out
-        if (c >= 1) {
-            if (wait_all(bar_mma, (c - 1) & 1)) {
-                failed = true;
-                break;
-            }
-            fence_after();
-            epilogue(c - 1);
-            sketch_to_operand<D>(tlane, q4, lane, h, LR, lrp, base + Ly.shi, base + Ly.slo);
-            tc::fence_proxy_async();
-            fence_before();
-            __syncthreads();
-            if (tid == 0) {
-                store_out(c - 1);
-                if (c + 1 < nchunk) {
-                    bulk_wait_read0();  // the store read V stage (c + 1) & 1
-                    load_v(c + 1);
+                for (int kb = 0; kb < KB; ++kb) tma_store(&tmO, 64 * kb, y, (int)bh, stage + kb * BLK);
+                bulk_commit();
+            };
+            // loads issued and completions waited for, per barrier (to drain after an abort)
+            int qk_issued = 0, qk_done = 0, v_issued[2] = {0, 0}, v_done[2] = {0, 0};
+            if (nchunk > 0) {
+                load_qk(0);
+                load_v(0);
+                ++qk_issued;
+                ++v_issued[0];
+                if (nchunk > 1) {
+                    load_v(1);
+                    ++v_issued[1];
                 }
             }
-            if (c + 1 < nchunk) cv[(c + 1) & 1].issued++;
-        }
-        if (wait_all(bar_proj, c & 1)) {
-            failed = true;
-            break;
-        }
-        fence_after();
-        if (tid == 0 && c + 1 < nchunk) load_qk(c + 1);  // projection and norms have read the tiles
-        if (c + 1 < nchunk) cqk.issued++;
-
-        // features: warps 0-3 the Q row t (-> TMEM), warps 4-7 the K row t (-> shared F_K tile)
-        {
-            float z[LPP];
-            {
-                float a[32];
-                ld32(tlane + (h ? T_ZK : T_ZQ), a);
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
+            constexpr uint32_t id_p1 = idesc_bf16(128, 16, 0, 0);
+            constexpr uint32_t id_ro = idesc_bf16(128, D + 16, 0, 0);
+            constexpr uint32_t id_ms = idesc_bf16(128, 16, 1, 0);
+            const uint32_t id_up = idesc_bf16(128, lrp, 1, 1);
+            const uint64_t d_fk_k = desc_k(base + Ly.fk), d_fk_mn = desc_mn(base + Ly.fk, BLK);
+            const uint64_t d_ones = desc_k(base + Ly.ones);
+            const uint64_t d_shi = desc_k(base + Ly.shi), d_slo = desc_k(base + Ly.slo);
+            bool ok = true;
+            for (int c = 0; c < nchunk && ok; ++c) {
+                const uint32_t vst = base + Ly.v + (c & 1) * Ly.kbb;
+                // projections
+                if (!(ok = wait_phase(bar(B_QK), c & 1, abort))) break;
+                ++qk_done;
+                fence_after();
+                issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
+                issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
+                commit(bar(B_PROJ));
+                // scores once the features are in; then the Q / K tiles (read by the projection and
+                // the norms) take the next chunk
+                if (!(ok = wait_phase(bar(B_FEAT), c & 1, abort))) break;
+                fence_after();
+                for (int ks = 0; ks < lrp / 16; ++ks)
+                    umma_ts(tmem + T_SC, tmem + T_FQ + 8 * ks, d_fk_k + (uint64_t)(ks * 2), id_s, ks > 0);
+                commit(bar(B_SC));
+                if (c + 1 < nchunk) {
+                    load_qk(c + 1);
+                    ++qk_issued;
+                }
+                // the previous chunk's output is staged and this chunk's sketch operand is written
+                if (!(ok = wait_phase(bar(B_SOP), c & 1, abort))) break;
+                if (c >= 1) store_out(c - 1);
+                if (!(ok = wait_phase(bar(B_MASK), c & 1, abort))) break;
+                if (!(ok = wait_phase(bar(B_V0 + (c & 1)), (c >> 1) & 1, abort))) break;
+                ++v_done[c & 1];
+                fence_after();
+                const uint64_t d_v = desc_mn(vst, BLK);
+                const uint64_t d_vt = desc_mn(vst, D == 128 ? BLK : (Ly.zero - (Ly.v + (c & 1) * Ly.kbb)));
 #pragma unroll
-                for (int k = 0; k < LPP; ++k) z[k] = a[k];
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
+                    umma_ts(tmem + T_O, tmem + T_P + 8 * ks, d_v + ko, id_pv, ks > 0);
+                    umma_ts(tmem + T_O + D, tmem + T_P + 8 * ks, d_ones + kk, id_p1, ks > 0);
+                }
+                for (int ks = 0; ks < lrp / 16; ++ks) {
+                    umma_ts(tmem + T_O, tmem + T_FQ + 8 * ks, d_shi + (uint64_t)(ks * 2), id_ro, true);
+                    umma_ts(tmem + T_O, tmem + T_FQ + 8 * ks, d_slo + (uint64_t)(ks * 2), id_ro, true);
+                }
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_ST, d_vt + ko, d_fk_mn + ko, id_up, true);
+                    umma(tmem + T_MS, d_fk_mn + ko, d_ones + kk, id_ms, true);
+                }
+                commit(bar(B_MMA));
+                // V stage (c + 1) & 1 held chunk c - 1, whose output store must have read it
+                if (c >= 1 && c + 1 < nchunk) {
+                    bulk_wait_read0();
+                    load_v(c + 1);
+                    ++v_issued[(c + 1) & 1];
+                }
             }
-            const float scale = (h == 0 || t < cnt) ? 1.f : 0.f;
+            if (ok && nchunk > 0) {
+                ok = wait_phase(bar(B_SOP), nchunk & 1, abort);
+                if (ok) store_out(nchunk - 1);
+            }
+            if (!ok) {
+                atomicOr(err, kErrTimeout);
+                *abort = 1;
+                // let copies still in flight land before the CTA's shared memory goes away
+                if (qk_issued > qk_done) mbar_wait(bar(B_QK), qk_done & 1);
+                for (int b = 0; b < 2; ++b)
+                    if (v_issued[b] > v_done[b]) mbar_wait(bar(B_V0 + b), v_done[b] & 1);
+            }
+            bulk_wait0();
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        sketch_to_operand<D>(tlane, q4, lane, h, LR, lrp, base + Ly.shi, base + Ly.slo);
+        warp_signal(bar(B_SOP));
+
+        // output epilogue of chunk c: O = num / den (this half's columns), staged in V stage c & 1
+        auto epilogue = [&](int c) {
+            const uint32_t stage = base + Ly.v + (c & 1) * Ly.kbb;
+            float v[16];
+            ld16(tlane + T_O + D, v);
+            const float rd = __frcp_rn(v[0]);
 #pragma unroll
-            for (int l = 0; l < LMAX; ++l) {
-                if (l < L) {
-                    float u[P], ph[R];
+            for (int cc = 0; cc < D / 32; ++cc) {
+                const int c0 = h * (D / 2) + 16 * cc;
+                ld16(tlane + T_O + c0, v);
 #pragma unroll
-                    for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
-                    tc::bucket_probs<P>(u, beta, ph);
-                    if (h == 0) {
-                        if constexpr (R >= 16) {
+                for (int j = 0; j < 2; ++j) {
+                    const int ch = (c0 >> 3) + j;
+                    st_shared_v4(stage + (ch >> 3) * BLK + sw_chunk(t, ch & 7),
+                                 mma::pack_bf16(v[8 * j] * rd, v[8 * j + 1] * rd),
+                                 mma::pack_bf16(v[8 * j + 2] * rd, v[8 * j + 3] * rd),
+                                 mma::pack_bf16(v[8 * j + 4] * rd, v[8 * j + 5] * rd),
+                                 mma::pack_bf16(v[8 * j + 6] * rd, v[8 * j + 7] * rd));
+                }
+            }
+        };
+
+        for (int c = 0; c < nchunk; ++c) {
+            const int64_t n0 = n_begin + (int64_t)c * C;
+            const int cnt = (int)min((int64_t)C, n_end - n0);
+            // row norm of this thread's row: warps 0-3 Q rows, warps 4-7 K rows
+            if (!wait_phase(bar(B_QK), c & 1, abort)) break;
+            float inv;
+            {
+                const uint32_t tile = base + (h ? Ly.k : Ly.q);
+                const float ss = half_sumsq<D>(tile, t, 0) + half_sumsq<D>(tile, t, 1);
+                inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+            }
+            // output of the previous chunk, and the sketch operand for this chunk's read-out
+            if (c >= 1) {
+                if (!wait_phase(bar(B_MMA), (c - 1) & 1, abort)) break;
+                fence_after();
+                epilogue(c - 1);
+                sketch_to_operand<D>(tlane, q4, lane, h, LR, lrp, base + Ly.shi, base + Ly.slo);
+                warp_signal(bar(B_SOP));
+            }
+            // features: warps 0-3 the Q row t (-> TMEM), warps 4-7 the K row t (-> shared F_K tile)
+            if (!wait_phase(bar(B_PROJ), c & 1, abort)) break;
+            fence_after();
+            {
+                float z[LPP];
+                {
+                    float a[32];
+                    ld32(tlane + (h ? T_ZK : T_ZQ), a);
 #pragma unroll
-                            for (int b = 0; b < R / 16; ++b) {
-                                uint32_t r[8];
+                    for (int k = 0; k < LPP; ++k) z[k] = a[k];
+                }
+                const float scale = (h == 0 || t < cnt) ? 1.f : 0.f;
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(ph[16 * b + 2 * j], ph[16 * b + 2 * j + 1]);
-                                stn<8>(tlane + T_FQ + (l * R) / 2 + 8 * b, r);
+                for (int l = 0; l < LMAX; ++l) {
+                    if (l < L) {
+                        float u[P], ph[R];
+#pragma unroll
+                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+                        tc::bucket_probs<P>(u, beta, ph);
+                        if (h == 0) {
+                            if constexpr (R >= 16) {
+#pragma unroll
+                                for (int b = 0; b < R / 16; ++b) {
+                                    uint32_t r[8];
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j)
+                                        r[j] = mma::pack_bf16(ph[16 * b + 2 * j], ph[16 * b + 2 * j + 1]);
+                                    stn<8>(tlane + T_FQ + (l * R) / 2 + 8 * b, r);
+                                }
+                            } else {
+                                uint32_t r[R / 2];
+#pragma unroll
+                                for (int j = 0; j < R / 2; ++j) r[j] = mma::pack_bf16(ph[2 * j], ph[2 * j + 1]);
+                                stn<R / 2>(tlane + T_FQ + (l * R) / 2, r);
                             }
                         } else {
-                            uint32_t r[R / 2];
+                            if constexpr (R >= 8) {
 #pragma unroll
-                            for (int j = 0; j < R / 2; ++j) r[j] = mma::pack_bf16(ph[2 * j], ph[2 * j + 1]);
-                            stn<R / 2>(tlane + T_FQ + (l * R) / 2, r);
-                        }
-                    } else {
-                        if constexpr (R >= 8) {
+                                for (int j = 0; j < R / 8; ++j) {
+                                    const int ch = l * (R / 8) + j;
+                                    st_shared_v4(base + Ly.fk + sw_chunk(t, ch),
+                                                 mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
+                                                 mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
+                                                 mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
+                                                 mma::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
+                                }
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < R / 8; ++j) {
-                                const int ch = l * (R / 8) + j;
-                                st_shared_v4(base + Ly.fk + sw_chunk(t, ch),
-                                             mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
-                                             mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
-                                             mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
-                                             mma::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
-                            }
-                        } else {
-#pragma unroll
-                            for (int r = 0; r < R; r += 2) {
-                                const int lr = l * R + r;
-                                const uint32_t w = mma::pack_bf16(ph[r] * scale, ph[r + 1] * scale);
-                                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fk + sw_elem(t, lr)), "r"(w)
-                                             : "memory");
+                                for (int r = 0; r < R; r += 2) {
+                                    const int lr = l * R + r;
+                                    const uint32_t w = mma::pack_bf16(ph[r] * scale, ph[r + 1] * scale);
+                                    asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fk + sw_elem(t, lr)), "r"(w)
+                                                 : "memory");
+                                }
                             }
                         }
                     }
                 }
             }
-        }
-        wait_st();
-        tc::fence_proxy_async();
-        fence_before();
-        __syncthreads();
-        if (tid == 0) {
+            wait_st();
+            warp_signal(bar(B_FEAT));
+            // causal mask j <= t on this half's 64 key columns -> bf16 P in TMEM
+            if (!wait_phase(bar(B_SC), c & 1, abort)) break;
             fence_after();
-            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
-            for (int ks = 0; ks < lrp / 16; ++ks)
-                umma_ts(tmem + T_SC, tmem + T_FQ + 8 * ks, desc_k(base + Ly.fk + ks * 32), id_s, ks > 0);
-            commit(bar_sc);
-        }
-        if (wait_all(bar_sc, c & 1)) {
-            failed = true;
-            break;
-        }
-        fence_after();
-        // causal mask j <= t on this half's 64 key columns -> bf16 P in TMEM
-        {
-            const int j0 = 64 * h;
+            {
+                const int j0 = 64 * h;
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                float a[32];
-                ld32(tlane + T_SC + j0 + 32 * b, a);
-                uint32_t r[16];
+                for (int b = 0; b < 2; ++b) {
+                    const int jb = j0 + 32 * b;
+                    uint32_t r0[8], r1[8];
+                    if (jb <= t) {
+                        float a[32];
+                        ld32(tlane + T_SC + jb, a);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int jj = j0 + 32 * b + 2 * j;
-                    r[j] = mma::pack_bf16(jj <= t ? a[2 * j] : 0.f, jj + 1 <= t ? a[2 * j + 1] : 0.f);
+                        for (int j = 0; j < 8; ++j) {
+                            const int jj = jb + 2 * j;
+                            r0[j] = mma::pack_bf16(jj <= t ? a[2 * j] : 0.f, jj + 1 <= t ? a[2 * j + 1] : 0.f);
+                            r1[j] = mma::pack_bf16(jj + 16 <= t ? a[16 + 2 * j] : 0.f, jj + 17 <= t ? a[17 + 2 * j] : 0.f);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) r0[j] = r1[j] = 0u;
+                    }
+                    stn<8>(tlane + T_P + jb / 2, r0);
+                    stn<8>(tlane + T_P + jb / 2 + 8, r1);
                 }
-                uint32_t r0[8], r1[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    r0[j] = r[j];
-                    r1[j] = r[8 + j];
-                }
-                stn<8>(tlane + T_P + j0 / 2 + 16 * b, r0);
-                stn<8>(tlane + T_P + j0 / 2 + 16 * b + 8, r1);
             }
+            wait_st();
+            warp_signal(bar(B_MASK));
         }
-        wait_st();
-        if (wait_all(bar_v + 8 * (c & 1), (c >> 1) & 1)) {
-            failed = true;
-            break;
-        }
-        cv[c & 1].waited++;
-        fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            fence_after();
-            constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
-            constexpr uint32_t id_p1 = idesc_bf16(128, 16, 0, 0);
-            constexpr uint32_t id_ro = idesc_bf16(128, D + 16, 0, 0);
-            const uint32_t id_up = idesc_bf16(128, lrp, 1, 1);
-            constexpr uint32_t id_ms = idesc_bf16(128, 16, 1, 0);
-            const uint32_t vlbo = D == 128 ? BLK : (Ly.zero - (Ly.v + (c & 1) * Ly.kbb));
-#pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks) {
-                umma_ts(tmem + T_O, tmem + T_P + 8 * ks, desc_mn(vst + ks * 2048, BLK), id_pv, ks > 0);
-                umma_ts(tmem + T_O + D, tmem + T_P + 8 * ks, desc_k(base + Ly.ones + (ks >> 2) * 2048 + (ks & 3) * 32),
-                        id_p1, ks > 0);
-            }
-            for (int ks = 0; ks < lrp / 16; ++ks) {
-                umma_ts(tmem + T_O, tmem + T_FQ + 8 * ks, desc_k(base + Ly.shi + ks * 32), id_ro, true);
-                umma_ts(tmem + T_O, tmem + T_FQ + 8 * ks, desc_k(base + Ly.slo + ks * 32), id_ro, true);
-            }
-#pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks) {
-                umma(tmem + T_ST, desc_mn(vst + ks * 2048, vlbo), desc_mn(base + Ly.fk + ks * 2048, BLK), id_up, true);
-                umma(tmem + T_MS, desc_mn(base + Ly.fk + ks * 2048, BLK),
-                     desc_k(base + Ly.ones + (ks >> 2) * 2048 + (ks & 3) * 32), id_ms, true);
-            }
-            commit(bar_mma);
-        }
-    }
-    if (!failed && nchunk > 0) {
-        failed = wait_all(bar_mma, (nchunk - 1) & 1);
-        if (!failed) {
+        if (nchunk > 0 && wait_phase(bar(B_MMA), (nchunk - 1) & 1, abort)) {
             fence_after();
             epilogue(nchunk - 1);
-            tc::fence_proxy_async();
-            fence_before();
-            __syncthreads();
-            if (tid == 0) store_out(nchunk - 1);
+            warp_signal(bar(B_SOP));
         }
     }
-    if (failed) {
-        if (tid == 0) atomicOr(err, kErrTimeout);
-        // let copies still in flight land before the CTA's shared memory goes away
-        if (cqk.issued > cqk.waited) mbar_wait(bar_qk, cqk.waited & 1);
-        for (int b = 0; b < 2; ++b)
-            if (cv[b].issued > cv[b].waited) mbar_wait(bar_v + 8 * b, cv[b].waited & 1);
-    }
-    if (tid == 0) bulk_wait0();
     fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -499,7 +499,7 @@ cudaError_t causal_fwd5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtens
     auto kern = c5::k_causal_fwd5<D, P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel("tc5_causal_fwd", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(nc5::NTH), smem, st, mq,
+    return launch_kernel("tc5_causal_fwd", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5::NTHW), smem, st, mq,
                          mk, mv, mo, Dm, W, S0, seg_len, nseg, err);
 }
 

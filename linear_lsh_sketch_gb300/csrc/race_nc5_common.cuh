@@ -80,6 +80,41 @@ __device__ __forceinline__ float half_sumsq(uint32_t tile, int t, int h)
     return s;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Bounded wait for the phase with parity `parity` that also gives up as soon as another thread
+// of the CTA has raised `*abort`.  A wait that runs out raises `*abort` itself.  Returns true
+// when the phase completed.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort)
+{
+    for (int i = 0; i < (1 << 22); ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 15) == 15 && *abort) return false;
+    }
+    *abort = 1;
+    return false;
+}
+
+// Hands the warp's finished work to the issuing thread: every lane orders its shared-memory
+// writes before later async-proxy reads and its TMEM stores before the hand-off; lane 0 then
+// arrives once on `bar` (whose count is the number of handing-off warps).
+__device__ __forceinline__ void warp_signal(uint32_t bar)
+{
+    tc::fence_proxy_async();
+    fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Bounded wait by every thread, then a CTA-wide vote: true if any thread's wait ran out.
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity)
 {
@@ -146,6 +181,29 @@ __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv,
             }
         }
     }
+}
+
+// Chain rule from dphi (one table, R values, phi recomputed from u) to the table's P
+// projection gradients dz_p = beta * sum_r phi_r (dphi_r - phi . dphi) v_{r,p} * (1 - u_p^2).
+template <int P>
+__device__ __forceinline__ void table_backward(const float (&u)[P], const float (&ph)[1 << P],
+                                               const float (&dph)[1 << P], float beta, float *dz)
+{
+    constexpr int R = 1 << P;
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) s = fmaf(ph[r], dph[r], s);
+    float du[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) du[p] = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float ds = ph[r] * (dph[r] - s);
+#pragma unroll
+        for (int p = 0; p < P; ++p) du[p] += ((r >> p) & 1) ? ds : -ds;
+    }
+#pragma unroll
+    for (int p = 0; p < P; ++p) dz[p] = beta * du[p] * (1.f - u[p] * u[p]);
 }
 
 // Instruction descriptors.
