@@ -256,7 +256,8 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
     RACE_TRY(cudaMemsetAsync(err, 0, sizeof(unsigned), st));
     const float *S = state;
     if constexpr (std::is_same<T, bf16_t>::value) {
-        if (use_tc<T>(pl) && causal_tc_bwd_supported(D)) {
+        const bool c5b = pl.c5 && c5_bwd_supported(D);
+        if (c5b || (use_tc<T>(pl) && causal_tc_bwd_supported(D))) {
             if (!S) {
                 float *Sw = (float *)(ws + pl.off_sk);
                 if (pl.c5)
@@ -266,9 +267,15 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 1, st));
                 S = Sw;
             }
-            RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, st));
+            if (c5b)
+                RACE_TRY(launch_c5_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, st));
+            else
+                RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
-            RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, st));
+            if (c5b)
+                RACE_TRY(launch_c5_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, st));
+            else
+                RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, st));
             return RACE_OK;
         }
     }

@@ -1,0 +1,1204 @@
+// race_c5_bwd.cu -- tcgen05 (TMEM accumulator) causal RACE attention backward, key side, bf16.
+//
+// The chain rule through Algorithm 2 ("RACE Attention" slides, frame "Causality is a prefix
+// update of the same statistics"; the pages print no backward).  With den_t, c_t = dO_t . O_t
+// (from the query-side pass) and F'_Q = phi(Q_t) / den_t, the gradient sketch of every token at
+// or after j is G_j = [G_A | G_B] = sum_{t >= j} F'_Q(t)^T [dO_t | -c_t].  Then
+//
+//   dV_j        = G_j,A^T phi(K_j)
+//   dphi_K(j)   = G_j,A V_j + G_j,B
+//
+// In chunks of C = 128 tokens walked in reverse, with G_next the sketch of every later token:
+//   dV      = F_K G_next,A  +  mask_{t >= j}(F_K F'_Q^T) dO
+//   dphi_K  = V G_next,A^T + G_next,B  +  mask_{t >= j}(V dO^T - 1 c^T) F'_Q
+//   G_next += F'_Q^T [dO | -c]
+// followed by the key-side feature Jacobian (softmax over corners, tanh, projection, row
+// normalisation).  All products run on tcgen05 with fp32 accumulators in TMEM; F_K and both
+// masked matrices are written to TMEM by the CUDA cores and used as A operands; F'_Q stays in one
+// swizzled shared tile that serves as B operand (K- and MN-major) and as A operand; the carried
+// G_next is converted each chunk to a bf16 hi + lo shared operand.
+//
+// Roles: warp 8 issues every TMA copy and MMA; warps 0-3 featurise the Q rows, write dV and
+// convert G; warps 4-7 featurise the K rows, run the Jacobian and write dK.  Hand-offs use
+// mbarriers; dK and dV rows go straight from registers to global memory.
+#include "race_launch.h"
+#include "race_nc5_common.cuh"
+
+namespace race {
+namespace c5b {
+
+using namespace race::nc5;
+
+constexpr int NTHW = NTH + 32;
+
+// TMEM columns (512 allocated; L R <= 32).
+constexpr uint32_t T_SC = 0;     // F_K F'_Q^T, then P2 as bf16 pairs (in place, per half)
+constexpr uint32_t T_DV = 128;   // V dO^T, then M2 as bf16 pairs (in place), then dxhat
+constexpr uint32_t T_DVV = 256;  // dV (d columns)
+constexpr uint32_t T_ZQ = 256;   // projections (dead before dV is written)
+constexpr uint32_t T_ZK = 288;
+constexpr uint32_t T_DP = 384;   // dphi_K (L R columns)
+constexpr uint32_t T_FK = 416;   // F_K as bf16 pairs (A operand), 16 columns
+constexpr uint32_t T_DZ = 432;   // dz as bf16 pairs (A operand), 16 columns
+constexpr uint32_t T_GT = 448;   // G^T (lanes = d), 32 columns
+constexpr uint32_t T_GB = 480;   // G_B (lanes = sketch row), 16 columns (column 0 used)
+constexpr uint32_t T_COLS = 512;
+
+enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_COUNT };
+
+struct BwdLayout {
+    uint32_t q, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, bar, slot, bytes, kbb;
+    __host__ __device__ BwdLayout(int D)
+    {
+        kbb = (uint32_t)(D / 64) * BLK;
+        q = 0;
+        k = q + kbb;
+        v = k + kbb;
+        dO = v + kbb;
+        fq = dO + kbb;  // F'_Q [t][lr], one 64-column block
+        ghi = fq + BLK;
+        glo = ghi + BLK;  // G operand [d rows][lr], one block each
+        whi = glo + BLK;
+        wlo = whi + (uint32_t)(D / 64) * WBLK;
+        ncm = wlo + (uint32_t)(D / 64) * WBLK;  // -c as a K-major N = 16 operand (rows 0, 1 = hi, lo)
+        gb = ncm + 4096;                         // G_B fp32 [32]
+        cvec = gb + 128;                         // c_t fp32 [C]
+        bar = cvec + 4 * C;
+        slot = bar + 128;
+        bytes = slot + 16;
+    }
+};
+
+template <int D, int P>
+__global__ void __launch_bounds__(NTHW, 1)
+    k_causal_bwdkv5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
+                    const float *__restrict__ W, const float2 *__restrict__ aux, const float *__restrict__ G0,
+                    int64_t seg_len, int nseg, bf16 *__restrict__ dK, bf16 *__restrict__ dV,
+                    unsigned *__restrict__ err)
+{
+    constexpr int KB = D / 64;
+    constexpr int R = 1 << P;
+    constexpr int LMAX = LPP / P;
+    constexpr int LRMAX = 32;  // sketch rows this kernel supports
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023) & ~1023u;
+    unsigned char *sm = smem_raw + (base - raw);
+    const BwdLayout Ly(D);
+    auto bar = [&](uint32_t i) { return base + Ly.bar + 8 * i; };
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
+    float *gb = reinterpret_cast<float *>(sm + Ly.gb);
+    float *cvec = reinterpret_cast<float *>(sm + Ly.cvec);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = (warp >> 2) & 1;
+    const bool compute = warp < 8;
+    const int t = 32 * q4 + lane;
+    const int s = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int64_t n_begin = (int64_t)s * seg_len;
+    const int64_t n_end = min(Dm.N, n_begin + seg_len);
+    const int nchunk = n_end > n_begin ? (int)((n_end - n_begin + C - 1) / C) : 0;
+    const int LR = Dm.LR, lrp = (LR + 15) & ~15;
+    const float beta = Dm.beta;
+    const int L = Dm.L;
+    const int64_t off = bh * Dm.N * D;
+
+    // ---- set-up
+    if (warp == 0) tmem_alloc(base + Ly.slot, T_COLS);
+    if (compute) {
+        zero_region(sm + Ly.fq, BLK);
+        zero_region(sm + Ly.ghi, 2 * BLK);
+        init_mass_tile(sm + Ly.ncm, false);
+        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    }
+    if (tid == NTH) {
+        for (uint32_t i = 0; i < B_COUNT; ++i) {
+            uint32_t cnt = 1;
+            if (i == B_FEAT || i == B_MASK) cnt = 8;
+            if (i == B_JAC || i == B_GOP || i == B_DVR) cnt = 4;
+            if (i == B_CS1 || i == B_CS2) cnt = NTH;
+            mbar_init(bar(i), cnt);
+        }
+        *abort = 0;
+        tc::fence_mbar_init();
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmdO);
+    }
+    tc::fence_proxy_async();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Ly.slot);
+    const uint32_t tlane = tmem + ((uint32_t)(32 * q4) << 16);
+
+    // gradient sketch of every token after the segment -> TMEM (G^T lanes = d, G_B lanes = row);
+    // the F_K and dz operand columns past L R and L P stay zero
+    if (compute) {
+        const float *Gb = G0 + ((int64_t)bh * nseg + s) * LR * (D + 1);
+        if (h == 0) {
+            if (t < D) {
+                for (int c0 = 0; c0 < LRMAX; c0 += 8) {
+                    uint32_t r[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r[j] = __float_as_uint(c0 + j < LR ? Gb[(c0 + j) * (D + 1) + t] : 0.f);
+                    stn<8>(tlane + T_GT + c0, r);
+                }
+            }
+            const uint32_t m[2] = {__float_as_uint(t < LR ? Gb[t * (D + 1) + D] : 0.f), 0u};
+            stn<2>(tlane + T_GB, m);
+        } else {
+            const uint32_t zr[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int c0 = 0; c0 < 32; c0 += 8) stn<8>(tlane + T_FK + c0, zr);  // T_FK and T_DZ
+        }
+        wait_st();
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+
+    // G (TMEM) -> bf16 hi / lo operand rows d (columns = sketch rows) and fp32 G_B; warps 0-3
+    auto convert_g = [&]() {
+        if (t < D) {
+            float a[32];
+            ld32(tlane + T_GT, a);
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float x0 = 2 * j < LR ? a[2 * j] : 0.f, x1 = 2 * j + 1 < LR ? a[2 * j + 1] : 0.f;
+                const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+            }
+#pragma unroll
+            for (int c = 0; c < LRMAX / 8; ++c) {
+                st_shared_v4(base + Ly.ghi + sw_chunk(t, c), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                st_shared_v4(base + Ly.glo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+            }
+        }
+        if (q4 == 0) {
+            float m[2];
+            ldn<2>(tlane + T_GB, m);  // -sum F'_Q c with c split into bf16 hi and lo rows
+            gb[lane] = lane < LR ? m[0] + m[1] : 0.f;
+        }
+    };
+
+    if (!compute) {
+        // ---------------------------------------------------------------- control warp
+        if (lane == 0) {
+            auto load_tiles = [&](int k, uint32_t which) {  // which: 1 = Q,K  2 = V  4 = dO
+                const int c = nchunk - 1 - k;
+                const int y = (int)(n_begin + (int64_t)c * C);
+                if (which & 1) {
+                    mbar_arrive_expect_tx(bar(B_QK), 2 * KB * BLK);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) {
+                        tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_QK));
+                        tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar(B_QK));
+                    }
+                }
+                if (which & 2) {
+                    mbar_arrive_expect_tx(bar(B_V), KB * BLK);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.v + kb * BLK, &tmV, 64 * kb, y, (int)bh, bar(B_V));
+                }
+                if (which & 4) {
+                    mbar_arrive_expect_tx(bar(B_DO), KB * BLK);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load(base + Ly.dO + kb * BLK, &tmdO, 64 * kb, y, (int)bh, bar(B_DO));
+                }
+            };
+            int issued[3] = {0, 0, 0}, done[3] = {0, 0, 0};  // Q/K, V, dO loads issued / waited for
+            if (nchunk > 0) {
+                load_tiles(0, 7);
+                issued[0] = issued[1] = issued[2] = 1;
+            }
+            constexpr uint32_t id_sc = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_dvo = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_dp = idesc_bf16(128, 32, 0, 1);
+            constexpr uint32_t id_dv = idesc_bf16(128, D, 0, 0);
+            constexpr uint32_t id_pdo = idesc_bf16(128, D, 0, 1);
+            constexpr uint32_t id_mf = idesc_bf16(128, 32, 0, 1);
+            constexpr uint32_t id_x = idesc_bf16(128, D, 0, 1);
+            constexpr uint32_t id_gt = idesc_bf16(128, 32, 1, 1);
+            constexpr uint32_t id_gb = idesc_bf16(128, 16, 1, 0);
+            // MN-major A operands with M = 128 read a second 64-column block at start + LBO: for
+            // F'_Q (sketch rows 64..127) and for dO^T at d = 64 (rows d 64..127) that block only feeds
+            // accumulator lanes nobody reads, so it points at the next whole 16 KB tile
+            const uint64_t d_fq_k = desc_k(base + Ly.fq), d_fq_mn = desc_mn(base + Ly.fq, BLK);
+            const uint64_t d_ghi_k = desc_k(base + Ly.ghi), d_glo_k = desc_k(base + Ly.glo);
+            const uint64_t d_ghi_mn = desc_mn(base + Ly.ghi, BLK), d_glo_mn = desc_mn(base + Ly.glo, BLK);
+            const uint64_t d_v_k = desc_k(base + Ly.v), d_do_k = desc_k(base + Ly.dO);
+            const uint64_t d_do_mn = desc_mn(base + Ly.dO, BLK);
+            const uint64_t d_do_mt = desc_mn(base + Ly.dO, BLK);
+            const uint64_t d_ncm = desc_k(base + Ly.ncm);
+            const uint64_t d_whi = desc_mn(base + Ly.whi, WBLK), d_wlo = desc_mn(base + Ly.wlo, WBLK);
+            bool ok = true;
+            for (int k = 0; k < nchunk && ok; ++k) {
+                const uint32_t par = k & 1;
+                if (!(ok = wait_phase(bar(B_QK), par, abort))) break;
+                ++done[0];
+                // the projections reuse TMEM columns of the previous chunk's dV
+                if (k >= 1 && !(ok = wait_phase(bar(B_DVR), (k - 1) & 1, abort))) break;
+                fence_after();
+                issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
+                issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
+                commit(bar(B_PROJ));
+                // group A once the features and the previous chunk's G operand are in
+                if (!(ok = wait_phase(bar(B_FEAT), par, abort))) break;
+                if (k + 1 < nchunk) {  // projections and norms have read the Q / K tiles
+                    load_tiles(k + 1, 1);
+                    ++issued[0];
+                }
+                if (!(ok = wait_phase(bar(B_GOP), par, abort))) break;
+                if (!(ok = wait_phase(bar(B_V), par, abort))) break;
+                ++done[1];
+                if (!(ok = wait_phase(bar(B_DO), par, abort))) break;
+                ++done[2];
+                fence_after();
+                for (int ks = 0; ks < 2; ++ks)
+                    umma_ts(tmem + T_SC, tmem + T_FK + 8 * ks, d_fq_k + (uint64_t)(2 * ks), id_sc, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)((ks >> 2) * BLK + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_DV, d_v_k + ko, d_do_k + ko, id_dvo, ks > 0);
+                    umma(tmem + T_DP, d_v_k + ko, d_ghi_mn + (uint64_t)(ks * 128), id_dp, ks > 0);
+                    umma(tmem + T_DP, d_v_k + ko, d_glo_mn + (uint64_t)(ks * 128), id_dp, true);
+                }
+                for (int ks = 0; ks < 2; ++ks) {
+                    umma_ts(tmem + T_DVV, tmem + T_FK + 8 * ks, d_ghi_k + (uint64_t)(2 * ks), id_dv, ks > 0);
+                    umma_ts(tmem + T_DVV, tmem + T_FK + 8 * ks, d_glo_k + (uint64_t)(2 * ks), id_dv, true);
+                }
+                commit(bar(B_A));
+                // group B: masked products
+                if (!(ok = wait_phase(bar(B_MASK), par, abort))) break;
+                fence_after();
+                if (k + 1 < nchunk) {  // group A (the only reader of V) is complete
+                    load_tiles(k + 1, 2);
+                    ++issued[1];
+                }
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint32_t ac = (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4));  // in-place bf16 columns
+                    umma_ts(tmem + T_DVV, tmem + T_SC + ac, d_do_mn + (uint64_t)(ks * 128), id_pdo, true);
+                    umma_ts(tmem + T_DP, tmem + T_DV + ac, d_fq_mn + (uint64_t)(ks * 128), id_mf, true);
+                }
+                commit(bar(B_B));
+                // group C: dxhat and the gradient sketch update
+                if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
+                fence_after();
+                for (int ks = 0; ks < LPP / 16; ++ks) {
+                    umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_whi + (uint64_t)(ks * 128), id_x, ks > 0);
+                    umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_wlo + (uint64_t)(ks * 128), id_x, true);
+                }
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_GT, d_do_mt + ko, d_fq_mn + ko, id_gt, true);
+                    umma(tmem + T_GB, d_fq_mn + ko, d_ncm + kk, id_gb, true);
+                }
+                commit(bar(B_C));
+                if (k + 1 < nchunk) {  // dO is read by groups B and C only
+                    if (!(ok = wait_phase(bar(B_C), par, abort))) break;
+                    load_tiles(k + 1, 4);
+                    ++issued[2];
+                }
+            }
+            if (!ok) {
+                atomicOr(err, kErrTimeout);
+                *abort = 1;
+                const uint32_t bars[3] = {bar(B_QK), bar(B_V), bar(B_DO)};
+                for (int b = 0; b < 3; ++b)
+                    if (issued[b] > done[b]) mbar_wait(bars[b], done[b] & 1);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        if (h == 0) {
+            convert_g();
+            warp_signal(bar(B_GOP));
+        }
+        for (int k = 0; k < nchunk; ++k) {
+            const uint32_t par = k & 1;
+            const int c = nchunk - 1 - k;
+            const int64_t n0 = n_begin + (int64_t)c * C;
+            const int cnt = (int)min((int64_t)C, n_end - n0);
+            const bool live = t < cnt;
+            if (!wait_phase(bar(B_QK), par, abort)) break;
+            // the row this thread featurises: Q row t (warps 0-3) or K row t (warps 4-7)
+            uint4 xw[D / 8];
+            float inv;
+            {
+                const uint32_t tile = base + (h ? Ly.k : Ly.q);
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    xw[j] = ld_shared_v4(tile + (j >> 3) * BLK + sw_chunk(t, j & 7));
+                    ss += sumsq8(xw[j]);
+                }
+                inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+            }
+            float2 a2 = make_float2(0.f, 0.f);
+            if (h == 0 && live) a2 = aux[bh * Dm.N + n0 + t];
+            if (!wait_phase(bar(B_PROJ), par, abort)) break;
+            fence_after();
+            float z[LPP];
+            {
+                float a[32];
+                ld32(tlane + (h ? T_ZK : T_ZQ), a);
+#pragma unroll
+                for (int j = 0; j < LPP; ++j) z[j] = a[j];
+            }
+            float uk[LPP];  // K rows keep u for the Jacobian
+            if (h == 0) {
+                // F'_Q = phi(Q_t) / den_t -> shared tile row t;  -c_t -> rows 0 / 1 of the mass operand
+                const float sc = a2.x;
+#pragma unroll
+                for (int l = 0; l < LMAX; ++l) {
+                    if (l < L) {
+                        float u[P], ph[R];
+#pragma unroll
+                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+                        tc::bucket_probs<P>(u, beta, ph);
+                        if constexpr (R >= 8) {
+#pragma unroll
+                            for (int j = 0; j < R / 8; ++j) {
+                                const int ch = l * (R / 8) + j;
+                                st_shared_v4(base + Ly.fq + sw_chunk(t, ch), mma::pack_bf16(ph[8 * j] * sc, ph[8 * j + 1] * sc),
+                                             mma::pack_bf16(ph[8 * j + 2] * sc, ph[8 * j + 3] * sc),
+                                             mma::pack_bf16(ph[8 * j + 4] * sc, ph[8 * j + 5] * sc),
+                                             mma::pack_bf16(ph[8 * j + 6] * sc, ph[8 * j + 7] * sc));
+                            }
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < R; r += 2) {
+                                const uint32_t w = mma::pack_bf16(ph[r] * sc, ph[r + 1] * sc);
+                                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fq + sw_elem(t, l * R + r)), "r"(w)
+                                             : "memory");
+                            }
+                        }
+                    }
+                }
+                const float mcv = -a2.y;
+                const bf16 mhi = __float2bfloat16_rn(mcv);
+                const bf16 mlo = __float2bfloat16_rn(mcv - __bfloat162float(mhi));
+                unsigned char *mt = sm + Ly.ncm + (t >> 6) * 2048;
+                *reinterpret_cast<bf16 *>(mt + sw_elem(0, t & 63)) = mhi;
+                *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
+                cvec[t] = a2.y;
+            } else {
+                // F_K -> TMEM (A operand); keep u
+                float phk[LRMAX];
+#pragma unroll
+                for (int j = 0; j < LRMAX; ++j) phk[j] = 0.f;
+#pragma unroll
+                for (int l = 0; l < LMAX; ++l) {
+                    if (l < L && l * R < LRMAX) {
+                        float u[P], ph[R];
+#pragma unroll
+                        for (int p = 0; p < P; ++p) u[p] = uk[l * P + p] = tc::tanh_abs(z[l * P + p] * inv);
+                        tc::bucket_probs<P>(u, beta, ph);
+#pragma unroll
+                        for (int r = 0; r < R; ++r)
+                            if (l * R + r < LRMAX) phk[l * R + r] = ph[r];
+                    }
+                }
+                uint32_t r[8];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(phk[16 * b + 2 * j], phk[16 * b + 2 * j + 1]);
+                    stn<8>(tlane + T_FK + 8 * b, r);
+                }
+                wait_st();
+            }
+            if (!group_sync(bar(B_CS1), par, abort)) break;  // c_t visible to every compute warp
+            warp_signal(bar(B_FEAT));
+            // masks over this half's 64 query columns t': P2 = (F_K F'_Q^T)[j][t'] and
+            // M2 = (V dO^T)[j][t'] - c_t' for t' >= j (j = this thread's row), written in place
+            if (!wait_phase(bar(B_A), par, abort)) break;
+            fence_after();
+            {
+                const int j0 = 64 * h;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int tb = j0 + 16 * b;
+                    uint32_t pw[8], mw[8];
+                    if (tb + 15 >= 32 * q4) {  // warp-uniform: some lane of the warp keeps a column
+                        float a[16], e[16];
+                        ld16(tlane + T_SC + tb, a);
+                        ld16(tlane + T_DV + tb, e);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int q0 = tb + 2 * j;
+                            const bool k0 = q0 >= t, k1 = q0 + 1 >= t;
+                            pw[j] = mma::pack_bf16(k0 ? a[2 * j] : 0.f, k1 ? a[2 * j + 1] : 0.f);
+                            mw[j] = mma::pack_bf16(k0 ? e[2 * j] - cvec[q0] : 0.f, k1 ? e[2 * j + 1] - cvec[q0 + 1] : 0.f);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) pw[j] = mw[j] = 0u;
+                    }
+                    // bf16 pairs of this half's 64 columns go to its own first 32 columns
+                    stn<8>(tlane + T_SC + j0 + 8 * b, pw);
+                    stn<8>(tlane + T_DV + j0 + 8 * b, mw);
+                }
+            }
+            wait_st();
+            warp_signal(bar(B_MASK));
+            if (!wait_phase(bar(B_B), par, abort)) break;
+            fence_after();
+            if (h == 1) {
+                // key-side Jacobian: dphi_K + G_B -> dz (bf16 pairs in TMEM)
+                float dph[LRMAX];
+                {
+                    float a[32];
+                    ld32(tlane + T_DP, a);
+#pragma unroll
+                    for (int j = 0; j < LRMAX; ++j) dph[j] = a[j] + gb[j];
+                }
+                float dz[LPP];
+#pragma unroll
+                for (int j = 0; j < LPP; ++j) dz[j] = 0.f;
+#pragma unroll
+                for (int l = 0; l < LMAX; ++l) {
+                    if (l < L && l * R < LRMAX) {
+                        float u[P], ph[R], dp[R];
+#pragma unroll
+                        for (int p = 0; p < P; ++p) u[p] = uk[l * P + p];
+                        tc::bucket_probs<P>(u, beta, ph);
+#pragma unroll
+                        for (int r = 0; r < R; ++r) dp[r] = l * R + r < LRMAX ? dph[l * R + r] : 0.f;
+                        float tmp[P];
+                        table_backward<P>(u, ph, dp, beta, tmp);
+#pragma unroll
+                        for (int p = 0; p < P; ++p) dz[l * P + p] = tmp[p];
+                    }
+                }
+                uint32_t r[8];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(dz[16 * b + 2 * j], dz[16 * b + 2 * j + 1]);
+                    stn<8>(tlane + T_DZ + 8 * b, r);
+                }
+                wait_st();
+                warp_signal(bar(B_JAC));
+            } else {
+                // dV row t = F_K G_A + P2 dO, straight to global memory
+                bf16 *dst = dV + off + (n0 + t) * D;
+#pragma unroll
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    float v[16];
+                    ld16(tlane + T_DVV + 16 * cc, v);
+                    if (live) {
+                        *reinterpret_cast<uint4 *>(dst + 16 * cc) =
+                            make_uint4(mma::pack_bf16(v[0], v[1]), mma::pack_bf16(v[2], v[3]),
+                                       mma::pack_bf16(v[4], v[5]), mma::pack_bf16(v[6], v[7]));
+                        *reinterpret_cast<uint4 *>(dst + 16 * cc + 8) =
+                            make_uint4(mma::pack_bf16(v[8], v[9]), mma::pack_bf16(v[10], v[11]),
+                                       mma::pack_bf16(v[12], v[13]), mma::pack_bf16(v[14], v[15]));
+                    }
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_DVR));  // dV columns (shared with z) read
+            }
+            if (!wait_phase(bar(B_C), par, abort)) break;
+            fence_after();
+            if (h == 1) {
+                // dK row t = inv (dxhat - x inv^2 (x . dxhat)), straight to global memory
+                float dot = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    float v[16];
+                    ld16(tlane + T_DV + 16 * cc, v);
+                    const uint4 w0 = xw[2 * cc], w1 = xw[2 * cc + 1];
+                    const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        dot = fmaf(bf_lo(ww[j]), v[2 * j], dot);
+                        dot = fmaf(bf_hi(ww[j]), v[2 * j + 1], dot);
+                    }
+                }
+                const float kk = inv * inv * dot;
+                bf16 *dst = dK + off + (n0 + t) * D;
+#pragma unroll
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    float v[16];
+                    ld16(tlane + T_DV + 16 * cc, v);
+                    const uint4 w0 = xw[2 * cc], w1 = xw[2 * cc + 1];
+                    const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        o[j] = mma::pack_bf16(inv * (v[2 * j] - bf_lo(ww[j]) * kk), inv * (v[2 * j + 1] - bf_hi(ww[j]) * kk));
+                    if (live) {
+                        *reinterpret_cast<uint4 *>(dst + 16 * cc) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(dst + 16 * cc + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            } else {
+                convert_g();
+                warp_signal(bar(B_GOP));
+            }
+            fence_before();
+            if (!group_sync(bar(B_CS2), par, abort)) break;  // gb / TMEM reads done before the next chunk
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after();
+        tmem_dealloc(tmem, T_COLS);
+    }
+}
+
+}  // namespace c5b
+
+// ------------------------------------------------------------------ query side (forward order)
+//
+// With S_t the inclusive prefix sketch [A | B], B_t its mass row and g_t = A_t dO_t:
+//   den_t = phi(Q_t) . B_t,   c_t = phi(Q_t) . g_t / den_t,   dphi_Q(t) = (g_t - B_t c_t) / den_t
+// In chunks of C = 128 tokens walked forward, with S_prev the sketch of every earlier token:
+//   g   = dO A_prev^T + mask_{j <= t}(dO V^T) F_K
+//   B_t = B_prev + (tril 1) F_K
+// then the query-side feature Jacobian gives dQ; the pass also writes {1 / den_t, c_t} per token
+// and the segment's gradient-sketch sum G = sum_t F'_Q(t)^T [dO_t | -c_t] for the key side, and
+// carries S (A^T += V^T F_K, B += F_K^T 1) in TMEM.
+// Roles: warp 8 issues TMA and MMA; warps 0-3 own the Q rows (x kept in TMEM, den, c, the
+// Jacobian, dQ); warps 4-7 featurise the K rows and convert S to its bf16 operand copy.
+
+namespace c5q {
+
+using namespace race::nc5;
+
+constexpr int NTHW = NTH + 32;
+
+constexpr uint32_t T_ZQ = 0, T_ZK = 32;
+constexpr uint32_t T_DV = 64;     // dO V^T, then M1 as bf16 pairs (in place), then dxhat
+constexpr uint32_t T_G = 192;     // g (L R columns)
+constexpr uint32_t T_BT = 224;    // (tril 1) F_K
+constexpr uint32_t T_TRIL = 256;  // lower-triangular ones as bf16 pairs (A operand), 64 columns
+constexpr uint32_t T_DZ = 320;    // dz as bf16 pairs (A operand)
+constexpr uint32_t T_ST = 336;    // A^T (lanes = d)
+constexpr uint32_t T_MS = 368;    // B (lanes = sketch row), column 0
+constexpr uint32_t T_GT = 384;    // G^T (lanes = d)
+constexpr uint32_t T_GB = 416;    // G_B (lanes = sketch row), columns 0 + 1 (c split hi / lo)
+constexpr uint32_t T_X = 432;     // the Q row as stored (bf16 pairs), 64 columns
+constexpr uint32_t T_COLS = 512;
+
+enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_COUNT };
+
+struct QLayout {
+    uint32_t q, k, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, bprev, bar, slot, bytes, kbb;
+    __host__ __device__ QLayout(int D)
+    {
+        kbb = (uint32_t)(D / 64) * BLK;
+        q = 0;
+        k = q + kbb;
+        v = k + kbb;
+        dO = v + kbb;
+        fk = dO + kbb;   // F_K [j][lr]
+        fq = fk + BLK;   // F'_Q [t][lr]
+        shi = fq + BLK;  // S operand [d rows][lr] (MN-major B of dO A^T)
+        slo = shi + BLK;
+        whi = slo + BLK;
+        wlo = whi + (uint32_t)(D / 64) * WBLK;
+        ncm = wlo + (uint32_t)(D / 64) * WBLK;
+        ones = ncm + 4096;
+        bprev = ones + 4096;  // B_prev fp32 [32]
+        bar = bprev + 128;
+        slot = bar + 128;
+        bytes = slot + 16;
+    }
+};
+
+template <int D, int P>
+__global__ void __launch_bounds__(NTHW, 1)
+    k_causal_bwdq5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
+                   const float *__restrict__ W, const float *__restrict__ S0, int64_t seg_len, int nseg,
+                   bf16 *__restrict__ dQ, float2 *__restrict__ aux, float *__restrict__ Gseg,
+                   unsigned *__restrict__ err)
+{
+    constexpr int KB = D / 64;
+    constexpr int R = 1 << P;
+    constexpr int LMAX = LPP / P;
+    constexpr int LRMAX = 32;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023) & ~1023u;
+    unsigned char *sm = smem_raw + (base - raw);
+    const QLayout Ly(D);
+    auto bar = [&](uint32_t i) { return base + Ly.bar + 8 * i; };
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
+    float *bprev = reinterpret_cast<float *>(sm + Ly.bprev);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = (warp >> 2) & 1;
+    const bool compute = warp < 8;
+    const int t = 32 * q4 + lane;
+    const int s = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int64_t n_begin = (int64_t)s * seg_len;
+    const int64_t n_end = min(Dm.N, n_begin + seg_len);
+    const int nchunk = n_end > n_begin ? (int)((n_end - n_begin + C - 1) / C) : 0;
+    const int LR = Dm.LR;
+    const float beta = Dm.beta;
+    const int L = Dm.L;
+    const int64_t off = bh * Dm.N * D;
+
+    // ---- set-up
+    if (warp == 0) tmem_alloc(base + Ly.slot, T_COLS);
+    if (compute) {
+        zero_region(sm + Ly.fk, 4 * BLK);  // F_K, F'_Q, S hi, S lo
+        init_mass_tile(sm + Ly.ncm, false);
+        init_mass_tile(sm + Ly.ones, true);
+        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    }
+    if (tid == NTH) {
+        for (uint32_t i = 0; i < B_COUNT; ++i) {
+            uint32_t cnt = 1;
+            if (i == B_FEAT || i == B_MASK) cnt = 8;
+            if (i == B_JAC || i == B_SOP) cnt = 4;
+            if (i == B_CS) cnt = NTH;
+            mbar_init(bar(i), cnt);
+        }
+        *abort = 0;
+        tc::fence_mbar_init();
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmdO);
+    }
+    tc::fence_proxy_async();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Ly.slot);
+    const uint32_t tlane = tmem + ((uint32_t)(32 * q4) << 16);
+
+    // sketch at the segment start, zero gradient sketch, and the lower-triangular ones operand
+    if (compute) {
+        const uint32_t zr[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (h == 0) {
+            const float *Sb = S0 + ((int64_t)bh * nseg + s) * LR * (D + 1);
+            for (int c0 = 0; c0 < LRMAX; c0 += 8) {
+                uint32_t r[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    r[j] = __float_as_uint((t < D && c0 + j < LR) ? Sb[(c0 + j) * (D + 1) + t] : 0.f);
+                stn<8>(tlane + T_ST + c0, r);
+                stn<8>(tlane + T_GT + c0, zr);
+            }
+            const uint32_t m[2] = {__float_as_uint(t < LR ? Sb[t * (D + 1) + D] : 0.f), 0u};
+            stn<2>(tlane + T_MS, m);
+            stn<8>(tlane + T_GB, zr);
+        }
+        // tril[t][j] = 1 for j <= t: half h writes the columns of keys 64 h .. 64 h + 63
+        for (int c0 = 32 * h; c0 < 32 * h + 32; c0 += 8) {
+            uint32_t r[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k0 = 2 * (c0 + j);
+                r[j] = (k0 <= t ? 0x3F80u : 0u) | (k0 + 1 <= t ? 0x3F800000u : 0u);
+            }
+            stn<8>(tlane + T_TRIL + c0, r);
+        }
+        wait_st();
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+
+    // S (TMEM) -> bf16 hi / lo operand rows d and fp32 B_prev; warps 4-7
+    auto convert_s = [&]() {
+        if (t < D) {
+            float a[32];
+            ld32(tlane + T_ST, a);
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float x0 = 2 * j < LR ? a[2 * j] : 0.f, x1 = 2 * j + 1 < LR ? a[2 * j + 1] : 0.f;
+                const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+            }
+#pragma unroll
+            for (int c = 0; c < LRMAX / 8; ++c) {
+                st_shared_v4(base + Ly.shi + sw_chunk(t, c), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                st_shared_v4(base + Ly.slo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+            }
+        }
+        if (q4 == 0) {
+            float m[1];
+            ldn<1>(tlane + T_MS, m);
+            bprev[lane] = lane < LR ? m[0] : 0.f;
+        }
+    };
+
+    if (!compute) {
+        // ---------------------------------------------------------------- control warp
+        if (lane == 0) {
+            auto load_tiles = [&](int c, uint32_t which) {  // which: 1 = Q,K  2 = V  4 = dO
+                const int y = (int)(n_begin + (int64_t)c * C);
+                if (which & 1) {
+                    mbar_arrive_expect_tx(bar(B_QK), 2 * KB * BLK);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) {
+                        tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_QK));
+                        tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar(B_QK));
+                    }
+                }
+                if (which & 2) {
+                    mbar_arrive_expect_tx(bar(B_V), KB * BLK);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.v + kb * BLK, &tmV, 64 * kb, y, (int)bh, bar(B_V));
+                }
+                if (which & 4) {
+                    mbar_arrive_expect_tx(bar(B_DO), KB * BLK);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load(base + Ly.dO + kb * BLK, &tmdO, 64 * kb, y, (int)bh, bar(B_DO));
+                }
+            };
+            int issued[3] = {0, 0, 0}, done[3] = {0, 0, 0};
+            if (nchunk > 0) {
+                load_tiles(0, 7);
+                issued[0] = issued[1] = issued[2] = 1;
+            }
+            constexpr uint32_t id_dv = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_g1 = idesc_bf16(128, 32, 0, 1);
+            constexpr uint32_t id_bt = idesc_bf16(128, 32, 0, 1);
+            constexpr uint32_t id_x = idesc_bf16(128, D, 0, 1);
+            constexpr uint32_t id_gt = idesc_bf16(128, 32, 1, 1);
+            constexpr uint32_t id_m16 = idesc_bf16(128, 16, 1, 0);
+            // MN-major A operands with M = 128 read a second 64-column block at start + BLK; beyond
+            // d (d = 64) or beyond the sketch rows it feeds accumulator lanes nobody reads
+            const uint64_t d_v_k = desc_k(base + Ly.v), d_do_k = desc_k(base + Ly.dO);
+            const uint64_t d_v_mt = desc_mn(base + Ly.v, BLK), d_do_mt = desc_mn(base + Ly.dO, BLK);
+            const uint64_t d_fk_mn = desc_mn(base + Ly.fk, BLK), d_fq_mn = desc_mn(base + Ly.fq, BLK);
+            const uint64_t d_shi = desc_mn(base + Ly.shi, BLK), d_slo = desc_mn(base + Ly.slo, BLK);
+            const uint64_t d_ncm = desc_k(base + Ly.ncm), d_ones = desc_k(base + Ly.ones);
+            const uint64_t d_whi = desc_mn(base + Ly.whi, WBLK), d_wlo = desc_mn(base + Ly.wlo, WBLK);
+            bool ok = true;
+            for (int c = 0; c < nchunk && ok; ++c) {
+                const uint32_t par = c & 1;
+                if (!(ok = wait_phase(bar(B_QK), par, abort))) break;
+                ++done[0];
+                fence_after();
+                issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
+                issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
+                commit(bar(B_PROJ));
+                if (!(ok = wait_phase(bar(B_FEAT), par, abort))) break;
+                if (c + 1 < nchunk) {  // projections and norms have read the Q / K tiles
+                    load_tiles(c + 1, 1);
+                    ++issued[0];
+                }
+                if (!(ok = wait_phase(bar(B_SOP), par, abort))) break;
+                if (!(ok = wait_phase(bar(B_V), par, abort))) break;
+                ++done[1];
+                if (!(ok = wait_phase(bar(B_DO), par, abort))) break;
+                ++done[2];
+                fence_after();
+                // group A: dO V^T, g = dO A_prev^T, (tril 1) F_K
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)((ks >> 2) * BLK + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_DV, d_do_k + ko, d_v_k + ko, id_dv, ks > 0);
+                    umma(tmem + T_G, d_do_k + ko, d_shi + (uint64_t)(ks * 128), id_g1, ks > 0);
+                    umma(tmem + T_G, d_do_k + ko, d_slo + (uint64_t)(ks * 128), id_g1, true);
+                }
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    umma_ts(tmem + T_BT, tmem + T_TRIL + 8 * ks, d_fk_mn + (uint64_t)(ks * 128), id_bt, ks > 0);
+                commit(bar(B_A));
+                // group B: g += M1 F_K
+                if (!(ok = wait_phase(bar(B_MASK), par, abort))) break;
+                fence_after();
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint32_t ac = (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4));
+                    umma_ts(tmem + T_G, tmem + T_DV + ac, d_fk_mn + (uint64_t)(ks * 128), id_bt, true);
+                }
+                commit(bar(B_B));
+                // group C: dxhat, gradient sketch, sketch update
+                if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
+                fence_after();
+                for (int ks = 0; ks < LPP / 16; ++ks) {
+                    umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_whi + (uint64_t)(ks * 128), id_x, ks > 0);
+                    umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_wlo + (uint64_t)(ks * 128), id_x, true);
+                }
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_GT, d_do_mt + ko, d_fq_mn + ko, id_gt, true);
+                    umma(tmem + T_GB, d_fq_mn + ko, d_ncm + kk, id_m16, true);
+                    umma(tmem + T_ST, d_v_mt + ko, d_fk_mn + ko, id_gt, true);
+                    umma(tmem + T_MS, d_fk_mn + ko, d_ones + kk, id_m16, true);
+                }
+                commit(bar(B_C));
+                if (c + 1 < nchunk) {  // V and dO are last read by group C
+                    if (!(ok = wait_phase(bar(B_C), par, abort))) break;
+                    load_tiles(c + 1, 6);
+                    ++issued[1];
+                    ++issued[2];
+                }
+            }
+            if (!ok) {
+                atomicOr(err, kErrTimeout);
+                *abort = 1;
+                const uint32_t bars[3] = {bar(B_QK), bar(B_V), bar(B_DO)};
+                for (int b = 0; b < 3; ++b)
+                    if (issued[b] > done[b]) mbar_wait(bars[b], done[b] & 1);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        if (h == 1) {
+            convert_s();
+            warp_signal(bar(B_SOP));
+        }
+        bool ok = group_sync(bar(B_CS), 0, abort);  // B_prev visible to the Q warps
+        for (int c = 0; c < nchunk && ok; ++c) {
+            const uint32_t par = c & 1;
+            const int64_t n0 = n_begin + (int64_t)c * C;
+            const int cnt = (int)min((int64_t)C, n_end - n0);
+            const bool live = t < cnt;
+            if (!(ok = wait_phase(bar(B_QK), par, abort))) break;
+            float inv;
+            {
+                const uint32_t tile = base + (h ? Ly.k : Ly.q);
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < D / 8; j += 2) {
+                    const uint4 w0 = ld_shared_v4(tile + (j >> 3) * BLK + sw_chunk(t, j & 7));
+                    const uint4 w1 = ld_shared_v4(tile + ((j + 1) >> 3) * BLK + sw_chunk(t, (j + 1) & 7));
+                    ss += sumsq8(w0) + sumsq8(w1);
+                    if (h == 0) {  // keep the Q row in TMEM for the dQ epilogue
+                        const uint32_t r[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        stn<8>(tlane + T_X + 4 * j, r);
+                    }
+                }
+                inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+            }
+            if (!(ok = wait_phase(bar(B_PROJ), par, abort))) break;
+            fence_after();
+            float z[LPP];
+            {
+                float a[32];
+                ld32(tlane + (h ? T_ZK : T_ZQ), a);
+#pragma unroll
+                for (int j = 0; j < LPP; ++j) z[j] = a[j];
+            }
+            float uq[LPP];  // Q rows keep u for the Jacobian
+            if (h == 0) {
+#pragma unroll
+                for (int j = 0; j < LPP; ++j) uq[j] = j < Dm.LP ? tc::tanh_abs(z[j] * inv) : 0.f;
+            } else {
+                const float sc = live ? 1.f : 0.f;
+#pragma unroll
+                for (int l = 0; l < LMAX; ++l) {
+                    if (l < L) {
+                        float u[P], ph[R];
+#pragma unroll
+                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+                        tc::bucket_probs<P>(u, beta, ph);
+                        if constexpr (R >= 8) {
+#pragma unroll
+                            for (int j = 0; j < R / 8; ++j) {
+                                const int ch = l * (R / 8) + j;
+                                st_shared_v4(base + Ly.fk + sw_chunk(t, ch), mma::pack_bf16(ph[8 * j] * sc, ph[8 * j + 1] * sc),
+                                             mma::pack_bf16(ph[8 * j + 2] * sc, ph[8 * j + 3] * sc),
+                                             mma::pack_bf16(ph[8 * j + 4] * sc, ph[8 * j + 5] * sc),
+                                             mma::pack_bf16(ph[8 * j + 6] * sc, ph[8 * j + 7] * sc));
+                            }
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < R; r += 2) {
+                                const uint32_t w = mma::pack_bf16(ph[r] * sc, ph[r + 1] * sc);
+                                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fk + sw_elem(t, l * R + r)), "r"(w)
+                                             : "memory");
+                            }
+                        }
+                    }
+                }
+            }
+            wait_st();
+            warp_signal(bar(B_FEAT));
+            // M1 = mask_{j <= t}(dO V^T) on this half's 64 key columns, bf16 in place
+            if (!(ok = wait_phase(bar(B_A), par, abort))) break;
+            fence_after();
+            {
+                const int j0 = 64 * h;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int jb = j0 + 16 * b;
+                    uint32_t w[8];
+                    if (jb <= 32 * q4 + 31) {  // warp-uniform: some lane keeps a column
+                        float a[16];
+                        ld16(tlane + T_DV + jb, a);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            w[j] = mma::pack_bf16(jb + 2 * j <= t ? a[2 * j] : 0.f, jb + 2 * j + 1 <= t ? a[2 * j + 1] : 0.f);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) w[j] = 0u;
+                    }
+                    stn<8>(tlane + T_DV + j0 + 8 * b, w);
+                }
+            }
+            wait_st();
+            warp_signal(bar(B_MASK));
+            if (!(ok = wait_phase(bar(B_B), par, abort))) break;
+            fence_after();
+            if (h == 0) {
+                // den, c, dphi_Q and the feature Jacobian; F'_Q, -c and {1/den, c}, table by table
+                float den = 0.f, pg = 0.f;
+#pragma unroll
+                for (int l = 0; l < LMAX; ++l) {
+                    if (l < L && l * R < LRMAX) {
+                        float u[P], ph[R], g[R], bt[R];
+#pragma unroll
+                        for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
+                        tc::bucket_probs<P>(u, beta, ph);
+                        ld_cols<R>(tlane + T_G + l * R, g);
+                        ld_cols<R>(tlane + T_BT + l * R, bt);
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            den = fmaf(ph[r], bprev[l * R + r] + bt[r], den);
+                            pg = fmaf(ph[r], g[r], pg);
+                        }
+                    }
+                }
+                const float rd = live ? __frcp_rn(den) : 0.f;
+                const float cc = pg * rd;
+                if (live) aux[bh * Dm.N + n0 + t] = make_float2(rd, cc);
+                float dz[LPP];
+#pragma unroll
+                for (int j = 0; j < LPP; ++j) dz[j] = 0.f;
+#pragma unroll
+                for (int l = 0; l < LMAX; ++l) {
+                    if (l < L && l * R < LRMAX) {
+                        float u[P], ph[R], g[R], bt[R];
+#pragma unroll
+                        for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
+                        tc::bucket_probs<P>(u, beta, ph);
+                        ld_cols<R>(tlane + T_G + l * R, g);
+                        ld_cols<R>(tlane + T_BT + l * R, bt);
+#pragma unroll
+                        for (int r = 0; r < R; ++r) g[r] = (g[r] - (bprev[l * R + r] + bt[r]) * cc) * rd;
+                        float tmp[P];
+                        table_backward<P>(u, ph, g, beta, tmp);
+#pragma unroll
+                        for (int p = 0; p < P; ++p) dz[l * P + p] = tmp[p];
+                        // F'_Q = phi / den for this table
+                        if constexpr (R >= 8) {
+#pragma unroll
+                            for (int j = 0; j < R / 8; ++j) {
+                                const int ch = l * (R / 8) + j;
+                                st_shared_v4(base + Ly.fq + sw_chunk(t, ch), mma::pack_bf16(ph[8 * j] * rd, ph[8 * j + 1] * rd),
+                                             mma::pack_bf16(ph[8 * j + 2] * rd, ph[8 * j + 3] * rd),
+                                             mma::pack_bf16(ph[8 * j + 4] * rd, ph[8 * j + 5] * rd),
+                                             mma::pack_bf16(ph[8 * j + 6] * rd, ph[8 * j + 7] * rd));
+                            }
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < R; r += 2) {
+                                const uint32_t w = mma::pack_bf16(ph[r] * rd, ph[r + 1] * rd);
+                                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fq + sw_elem(t, l * R + r)), "r"(w)
+                                             : "memory");
+                            }
+                        }
+                    }
+                }
+                uint32_t r[8];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(dz[16 * b + 2 * j], dz[16 * b + 2 * j + 1]);
+                    stn<8>(tlane + T_DZ + 8 * b, r);
+                }
+                const float mcv = -cc;
+                const bf16 mhi = __float2bfloat16_rn(mcv);
+                const bf16 mlo = __float2bfloat16_rn(mcv - __bfloat162float(mhi));
+                unsigned char *mt = sm + Ly.ncm + (t >> 6) * 2048;
+                *reinterpret_cast<bf16 *>(mt + sw_elem(0, t & 63)) = mhi;
+                *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
+                wait_st();
+                warp_signal(bar(B_JAC));
+            }
+            if (!(ok = wait_phase(bar(B_C), par, abort))) break;
+            fence_after();
+            if (h == 0) {
+                // dQ row t = inv (dxhat - x inv^2 (x . dxhat)), straight to global memory
+                float dot = 0.f;
+#pragma unroll
+                for (int cc16 = 0; cc16 < D / 16; ++cc16) {
+                    float v[16], xv[8];
+                    ld16(tlane + T_DV + 16 * cc16, v);
+                    ldn<8>(tlane + T_X + 8 * cc16, xv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t w = __float_as_uint(xv[j]);
+                        dot = fmaf(bf_lo(w), v[2 * j], fmaf(bf_hi(w), v[2 * j + 1], dot));
+                    }
+                }
+                const float kk = inv * inv * dot;
+                bf16 *dst = dQ + off + (n0 + t) * D;
+#pragma unroll
+                for (int cc16 = 0; cc16 < D / 16; ++cc16) {
+                    float v[16], xv[8];
+                    ld16(tlane + T_DV + 16 * cc16, v);
+                    ldn<8>(tlane + T_X + 8 * cc16, xv);
+                    uint32_t o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t w = __float_as_uint(xv[j]);
+                        o[j] = mma::pack_bf16(inv * (v[2 * j] - bf_lo(w) * kk), inv * (v[2 * j + 1] - bf_hi(w) * kk));
+                    }
+                    if (live) {
+                        *reinterpret_cast<uint4 *>(dst + 16 * cc16) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(dst + 16 * cc16 + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            } else {
+                convert_s();
+                warp_signal(bar(B_SOP));
+            }
+            fence_before();
+            if (!(ok = group_sync(bar(B_CS), (c + 1) & 1, abort))) break;  // B_prev, TMEM reads: next chunk
+        }
+        // the segment's gradient-sketch sum: G^T (lanes d) and G_B (lanes = sketch row, hi + lo)
+        if (ok) {
+            fence_after();
+            float *out = Gseg + ((int64_t)bh * nseg + s) * LR * (D + 1);
+            if (h == 0 && t < D) {
+                float a[32];
+                ld32(tlane + T_GT, a);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < LR) out[(int64_t)j * (D + 1) + t] = a[j];
+            }
+            if (h == 1) {
+                float m[2];
+                ldn<2>(tlane + T_GB, m);
+                if (t < LR) out[(int64_t)t * (D + 1) + D] = m[0] + m[1];
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after();
+        tmem_dealloc(tmem, T_COLS);
+    }
+}
+
+}  // namespace c5q
+
+// ------------------------------------------------------------------ host side
+
+cudaError_t make_token_map(CUtensorMap *map, const void *base, const Dims &D);
+
+bool c5_bwd_supported(const Dims &D)
+{
+    return (D.d == 64 || D.d == 128) && D.P >= 1 && D.P <= 5 && D.LP <= nc5::LPP && D.LR <= 32 &&
+           D.N <= 0x7FFFFFFF;
+}
+
+namespace {
+
+template <int D, int P>
+cudaError_t bwdkv5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                        const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
+                        int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+{
+    const c5b::BwdLayout Ly(D);
+    const size_t smem = Ly.bytes + 1024;
+    auto kern = c5b::k_causal_bwdkv5<D, P>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel("tc5_causal_bwd_kv", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5b::NTHW), smem,
+                         st, mq, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err);
+}
+
+}  // namespace
+
+namespace {
+
+template <int D, int P>
+cudaError_t bwdq5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                       const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
+                       bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, cudaStream_t st)
+{
+    const c5q::QLayout Ly(D);
+    const size_t smem = Ly.bytes + 1024;
+    auto kern = c5q::k_causal_bwdq5<D, P>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel("tc5_causal_bwd_q", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5q::NTHW), smem, st,
+                         mq, mk, mv, mdo, Dm, W, S0, seg_len, nseg, dQ, aux, Gseg, err);
+}
+
+}  // namespace
+
+cudaError_t launch_c5_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
+                            const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
+                            float *Gseg, unsigned *err, cudaStream_t st)
+{
+    CUtensorMap mq, mk, mv, mdo;
+    cudaError_t e = make_token_map(&mq, Q, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mk, K, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mv, V, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mdo, dO, Dm);
+    if (e != cudaSuccess) return e;
+#define RACE_C5Q_CASE(DD, PP) \
+    case DD * 16 + PP: return bwdq5_inst<DD, PP>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, st);
+    switch (Dm.d * 16 + Dm.P) {
+        RACE_C5Q_CASE(64, 1)
+        RACE_C5Q_CASE(64, 2)
+        RACE_C5Q_CASE(64, 3)
+        RACE_C5Q_CASE(64, 4)
+        RACE_C5Q_CASE(64, 5)
+        RACE_C5Q_CASE(128, 1)
+        RACE_C5Q_CASE(128, 2)
+        RACE_C5Q_CASE(128, 3)
+        RACE_C5Q_CASE(128, 4)
+        RACE_C5Q_CASE(128, 5)
+        default: return cudaErrorInvalidValue;
+    }
+#undef RACE_C5Q_CASE
+}
+
+cudaError_t launch_c5_bwd_kv(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
+                             const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
+                             bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+{
+    CUtensorMap mq, mk, mv, mdo;
+    cudaError_t e = make_token_map(&mq, Q, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mk, K, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mv, V, Dm);
+    if (e == cudaSuccess) e = make_token_map(&mdo, dO, Dm);
+    if (e != cudaSuccess) return e;
+    switch (Dm.d * 16 + Dm.P) {
+        case 64 * 16 + 1: return bwdkv5_inst<64, 1>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 64 * 16 + 2: return bwdkv5_inst<64, 2>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 64 * 16 + 3: return bwdkv5_inst<64, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 64 * 16 + 4: return bwdkv5_inst<64, 4>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 64 * 16 + 5: return bwdkv5_inst<64, 5>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 128 * 16 + 1: return bwdkv5_inst<128, 1>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 128 * 16 + 2: return bwdkv5_inst<128, 2>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 128 * 16 + 3: return bwdkv5_inst<128, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 128 * 16 + 4: return bwdkv5_inst<128, 4>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 128 * 16 + 5: return bwdkv5_inst<128, 5>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace race

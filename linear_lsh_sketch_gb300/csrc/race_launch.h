@@ -80,6 +80,13 @@ cudaError_t launch_nc5_readout(const Dims &D, const bf16_t *Q, const float *W, c
 bool c5_supported(const Dims &D);
 cudaError_t launch_c5_fwd(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const float *W,
                           const float *S0, int64_t seg_len, int nseg, bf16_t *O, unsigned *err, cudaStream_t st);
+bool c5_bwd_supported(const Dims &D);
+cudaError_t launch_c5_bwd_q(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
+                            const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
+                            float *Gseg, unsigned *err, cudaStream_t st);
+cudaError_t launch_c5_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
+                             const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
+                             bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st);
 cudaError_t launch_nc5_bwd_query(const Dims &D, const bf16_t *Q, const bf16_t *dO, const float *W, const float *S,
                                  bf16_t *dQ, float2 *aux, unsigned *err, cudaStream_t st);
 cudaError_t launch_nc5_bwd_key(const Dims &D, const bf16_t *K, const bf16_t *V, const float *W, const float *G,

@@ -57,23 +57,6 @@ __device__ __forceinline__ void load_sketch_rows(const float *__restrict__ S, in
     for (int i = threadIdx.x; i < lrp; i += NTH) mass[i] = i < LR ? S[(int64_t)i * (D + 1) + D] : 0.f;
 }
 
-// R consecutive fp32 TMEM columns of this thread's lane.
-template <int R>
-__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[R])
-{
-    if constexpr (R <= 16) {
-        ldn<R>(taddr, v);
-    } else {
-#pragma unroll
-        for (int k = 0; k < R / 32; ++k) {
-            float a[32];
-            ld32(taddr + 32 * k, a);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[32 * k + j] = a[j];
-        }
-    }
-}
-
 // Packs n fp32 values (n even) as bf16 pairs into n / 2 TMEM columns of this thread's lane.
 template <int N>
 __device__ __forceinline__ void st_bf16_cols(uint32_t taddr, const float (&v)[N])
@@ -100,29 +83,6 @@ __device__ __forceinline__ void st_bf16_cols(uint32_t taddr, const float (&v)[N]
             stn<1>(taddr + j, r);
         }
     }
-}
-
-// Chain rule from dphi (one table, R values, phi recomputed from u) to the table's P
-// projection gradients dz_p = beta * sum_r phi_r (dphi_r - phi . dphi) v_{r,p} * (1 - u_p^2).
-template <int P>
-__device__ __forceinline__ void table_backward(const float (&u)[P], const float (&ph)[1 << P],
-                                               const float (&dph)[1 << P], float beta, float *dz)
-{
-    constexpr int R = 1 << P;
-    float s = 0.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) s = fmaf(ph[r], dph[r], s);
-    float du[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p) du[p] = 0.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const float ds = ph[r] * (dph[r] - s);
-#pragma unroll
-        for (int p = 0; p < P; ++p) du[p] += ((r >> p) & 1) ? ds : -ds;
-    }
-#pragma unroll
-    for (int p = 0; p < P; ++p) dz[p] = beta * du[p] * (1.f - u[p] * u[p]);
 }
 
 __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }

@@ -115,6 +115,15 @@ __device__ __forceinline__ void warp_signal(uint32_t bar)
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// Barrier among the threads that share `bar` (its count): arrive, then a bounded wait for the
+// phase with parity `parity`.  Unlike bar.sync it cannot strand a thread when another has left
+// its loop after an abort.
+__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t parity, volatile int *abort)
+{
+    mbar_arrive(bar);
+    return wait_phase(bar, parity, abort);
+}
+
 // Bounded wait by every thread, then a CTA-wide vote: true if any thread's wait ran out.
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity)
 {
@@ -204,6 +213,23 @@ __device__ __forceinline__ void table_backward(const float (&u)[P], const float 
     }
 #pragma unroll
     for (int p = 0; p < P; ++p) dz[p] = beta * du[p] * (1.f - u[p] * u[p]);
+}
+
+// R consecutive fp32 TMEM columns of this thread's lane.
+template <int R>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[R])
+{
+    if constexpr (R <= 16) {
+        ldn<R>(taddr, v);
+    } else {
+#pragma unroll
+        for (int k = 0; k < R / 32; ++k) {
+            float a[32];
+            ld32(taddr + 32 * k, a);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[32 * k + j] = a[j];
+        }
+    }
 }
 
 // Instruction descriptors.
