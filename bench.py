@@ -44,6 +44,14 @@ KERNEL_BYTES = {
     "tc_causal_fwd": (4, 0),      # reads Q, K, V; writes O
     "tc_causal_bwd_q": (5, 8),    # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
     "tc_causal_bwd_kv": (6, 8),   # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
+    "tc5_sketch_keys": (2, 0),    # reads K, V
+    "tc5_sketch_grad": (2, 8),    # reads Q, dO and {1/den, dO.O}
+    "tc5_readout": (2, 0),        # reads Q, writes O
+    "tc5_bwd_query": (3, 8),      # reads Q, dO; writes dQ and {1/den, dO.O}
+    "tc5_bwd_key": (4, 0),        # reads K, V; writes dK, dV
+    "tc5_causal_fwd": (4, 0),     # reads Q, K, V; writes O
+    "tc5_causal_bwd_q": (5, 8),   # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
+    "tc5_causal_bwd_kv": (6, 8),  # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
 }
 
 
