@@ -44,7 +44,7 @@ constexpr uint32_t T_GT = 448;   // G^T (lanes = d), 32 columns
 constexpr uint32_t T_GB = 480;   // G_B (lanes = sketch row), 16 columns (column 0 used)
 constexpr uint32_t T_COLS = 512;
 
-enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_COUNT };
+enum : uint32_t { B_Q, B_K, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_COUNT };
 
 struct BwdLayout {
     uint32_t q, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, bar, slot, bytes, kbb;
@@ -161,9 +161,20 @@ __global__ void __launch_bounds__(NTHW, 1)
 
     // G (TMEM) -> bf16 hi / lo operand rows d (columns = sketch rows) and fp32 G_B; warps 0-3
     auto convert_g = [&]() {
+        uint32_t ar[32], gb0 = 0, gb1 = 0;
+        if (t < D) ld32_nw(tlane + T_GT, ar);
+        if (q4 == 0) {
+            ld1_nw(tlane + T_GB, gb0);
+            ld1_nw(tlane + T_GB + 1, gb1);
+        }
+        wait_ld();
+        reg_fence(ar);
+        reg_fence1(gb0);
+        reg_fence1(gb1);
         if (t < D) {
             float a[32];
-            ld32(tlane + T_GT, a);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = uf(ar[j]);
             uint32_t hw[16], lw[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -178,26 +189,24 @@ __global__ void __launch_bounds__(NTHW, 1)
                 st_shared_v4(base + Ly.glo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
             }
         }
-        if (q4 == 0) {
-            float m[2];
-            ldn<2>(tlane + T_GB, m);  // -sum F'_Q c with c split into bf16 hi and lo rows
-            gb[lane] = lane < LR ? m[0] + m[1] : 0.f;
-        }
+        if (q4 == 0) gb[lane] = lane < LR ? uf(gb0) + uf(gb1) : 0.f;  // -sum F'_Q c, c as bf16 hi + lo
     };
 
     if (!compute) {
         // ---------------------------------------------------------------- control warp
         if (lane == 0) {
-            auto load_tiles = [&](int k, uint32_t which) {  // which: 1 = Q,K  2 = V  4 = dO
+            auto load_tiles = [&](int k, uint32_t which) {  // which: 1 = Q  2 = V  4 = dO  8 = K
                 const int c = nchunk - 1 - k;
                 const int y = (int)(n_begin + (int64_t)c * C);
                 if (which & 1) {
-                    mbar_arrive_expect_tx(bar(B_QK), 2 * KB * BLK);
+                    mbar_arrive_expect_tx(bar(B_Q), KB * BLK);
 #pragma unroll
-                    for (int kb = 0; kb < KB; ++kb) {
-                        tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_QK));
-                        tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar(B_QK));
-                    }
+                    for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_Q));
+                }
+                if (which & 8) {
+                    mbar_arrive_expect_tx(bar(B_K), KB * BLK);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar(B_K));
                 }
                 if (which & 2) {
                     mbar_arrive_expect_tx(bar(B_V), KB * BLK);
@@ -211,10 +220,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                         tma_load(base + Ly.dO + kb * BLK, &tmdO, 64 * kb, y, (int)bh, bar(B_DO));
                 }
             };
-            int issued[3] = {0, 0, 0}, done[3] = {0, 0, 0};  // Q/K, V, dO loads issued / waited for
+            int issued[4] = {0, 0, 0, 0}, done[4] = {0, 0, 0, 0};  // Q, V, dO, K loads issued / waited for
             if (nchunk > 0) {
-                load_tiles(0, 7);
-                issued[0] = issued[1] = issued[2] = 1;
+                load_tiles(0, 15);
+                issued[0] = issued[1] = issued[2] = issued[3] = 1;
             }
             constexpr uint32_t id_sc = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t id_dvo = idesc_bf16(128, 128, 0, 0);
@@ -239,8 +248,10 @@ __global__ void __launch_bounds__(NTHW, 1)
             bool ok = true;
             for (int k = 0; k < nchunk && ok; ++k) {
                 const uint32_t par = k & 1;
-                if (!(ok = wait_phase(bar(B_QK), par, abort))) break;
+                if (!(ok = wait_phase(bar(B_Q), par, abort))) break;
                 ++done[0];
+                if (!(ok = wait_phase(bar(B_K), par, abort))) break;
+                ++done[3];
                 // the projections reuse TMEM columns of the previous chunk's dV
                 if (k >= 1 && !(ok = wait_phase(bar(B_DVR), (k - 1) & 1, abort))) break;
                 fence_after();
@@ -249,7 +260,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 commit(bar(B_PROJ));
                 // group A once the features and the previous chunk's G operand are in
                 if (!(ok = wait_phase(bar(B_FEAT), par, abort))) break;
-                if (k + 1 < nchunk) {  // projections and norms have read the Q / K tiles
+                if (k + 1 < nchunk) {  // the projection and the norms have read the Q tile
                     load_tiles(k + 1, 1);
                     ++issued[0];
                 }
@@ -290,6 +301,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                 // group C: dxhat and the gradient sketch update
                 if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
                 fence_after();
+                if (k + 1 < nchunk) {  // the K rows are parked in TMEM by now
+                    load_tiles(k + 1, 8);
+                    ++issued[3];
+                }
                 for (int ks = 0; ks < LPP / 16; ++ks) {
                     umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_whi + (uint64_t)(ks * 128), id_x, ks > 0);
                     umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_wlo + (uint64_t)(ks * 128), id_x, true);
@@ -310,8 +325,8 @@ __global__ void __launch_bounds__(NTHW, 1)
             if (!ok) {
                 atomicOr(err, kErrTimeout);
                 *abort = 1;
-                const uint32_t bars[3] = {bar(B_QK), bar(B_V), bar(B_DO)};
-                for (int b = 0; b < 3; ++b)
+                const uint32_t bars[4] = {bar(B_Q), bar(B_V), bar(B_DO), bar(B_K)};
+                for (int b = 0; b < 4; ++b)
                     if (issued[b] > done[b]) mbar_wait(bars[b], done[b] & 1);
             }
         }
@@ -328,18 +343,12 @@ __global__ void __launch_bounds__(NTHW, 1)
             const int64_t n0 = n_begin + (int64_t)c * C;
             const int cnt = (int)min((int64_t)C, n_end - n0);
             const bool live = t < cnt;
-            if (!wait_phase(bar(B_QK), par, abort)) break;
+            if (!wait_phase(bar(h ? B_K : B_Q), par, abort)) break;
             // the row this thread featurises: Q row t (warps 0-3) or K row t (warps 4-7)
-            uint4 xw[D / 8];
             float inv;
             {
                 const uint32_t tile = base + (h ? Ly.k : Ly.q);
-                float ss = 0.f;
-#pragma unroll
-                for (int j = 0; j < D / 8; ++j) {
-                    xw[j] = ld_shared_v4(tile + (j >> 3) * BLK + sw_chunk(t, j & 7));
-                    ss += sumsq8(xw[j]);
-                }
+                const float ss = half_sumsq<D>(tile, t, 0) + half_sumsq<D>(tile, t, 1);
                 inv = ss > 0.f ? rsqrtf(ss) : 0.f;
             }
             float2 a2 = make_float2(0.f, 0.f);
@@ -425,27 +434,31 @@ __global__ void __launch_bounds__(NTHW, 1)
             {
                 const int j0 = 64 * h;
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int tb = j0 + 16 * b;
-                    uint32_t pw[8], mw[8];
-                    if (tb + 15 >= 32 * q4) {  // warp-uniform: some lane of the warp keeps a column
-                        float a[16], e[16];
-                        ld16(tlane + T_SC + tb, a);
-                        ld16(tlane + T_DV + tb, e);
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int tb = j0 + 32 * pass;
+                    uint32_t sa[32], sd[32];
+                    const bool need = tb + 31 >= 32 * q4;  // warp-uniform: some lane keeps a column
+                    if (need) {
+                        ld32_nw(tlane + T_SC + tb, sa);
+                        ld32_nw(tlane + T_DV + tb, sd);
+                    }
+                    wait_ld();
+                    reg_fence(sa);
+                    reg_fence(sd);
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        uint32_t pw[8], mw[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            const int q0 = tb + 2 * j;
-                            const bool k0 = q0 >= t, k1 = q0 + 1 >= t;
-                            pw[j] = mma::pack_bf16(k0 ? a[2 * j] : 0.f, k1 ? a[2 * j + 1] : 0.f);
-                            mw[j] = mma::pack_bf16(k0 ? e[2 * j] - cvec[q0] : 0.f, k1 ? e[2 * j + 1] - cvec[q0 + 1] : 0.f);
+                            const int e = 16 * b + 2 * j, q0 = tb + e;
+                            const bool k0 = need && q0 >= t, k1 = need && q0 + 1 >= t;
+                            pw[j] = mma::pack_bf16(k0 ? uf(sa[e]) : 0.f, k1 ? uf(sa[e + 1]) : 0.f);
+                            mw[j] = mma::pack_bf16(k0 ? uf(sd[e]) - cvec[q0] : 0.f, k1 ? uf(sd[e + 1]) - cvec[q0 + 1] : 0.f);
                         }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) pw[j] = mw[j] = 0u;
+                        // bf16 pairs of this half's 64 columns go to its own first 32 columns
+                        stn<8>(tlane + T_SC + j0 + 16 * pass + 8 * b, pw);
+                        stn<8>(tlane + T_DV + j0 + 16 * pass + 8 * b, mw);
                     }
-                    // bf16 pairs of this half's 64 columns go to its own first 32 columns
-                    stn<8>(tlane + T_SC + j0 + 8 * b, pw);
-                    stn<8>(tlane + T_DV + j0 + 8 * b, mw);
                 }
             }
             wait_st();
@@ -453,6 +466,15 @@ __global__ void __launch_bounds__(NTHW, 1)
             if (!wait_phase(bar(B_B), par, abort)) break;
             fence_after();
             if (h == 1) {
+                // park the K row in TMEM (the score columns are free once group B is done) so that
+                // the K tile can take the next chunk
+#pragma unroll
+                for (int j = 0; j < D / 8; j += 2) {
+                    const uint4 w0 = ld_shared_v4(base + Ly.k + (j >> 3) * BLK + sw_chunk(t, j & 7));
+                    const uint4 w1 = ld_shared_v4(base + Ly.k + ((j + 1) >> 3) * BLK + sw_chunk(t, (j + 1) & 7));
+                    const uint32_t r[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                    stn<8>(tlane + T_SC + 4 * j, r);
+                }
                 // key-side Jacobian: dphi_K + G_B -> dz (bf16 pairs in TMEM)
                 float dph[LRMAX];
                 {
@@ -492,16 +514,19 @@ __global__ void __launch_bounds__(NTHW, 1)
                 // dV row t = F_K G_A + P2 dO, straight to global memory
                 bf16 *dst = dV + off + (n0 + t) * D;
 #pragma unroll
-                for (int cc = 0; cc < D / 16; ++cc) {
-                    float v[16];
-                    ld16(tlane + T_DVV + 16 * cc, v);
+                for (int pass = 0; pass < D / 32; ++pass) {
+                    uint32_t v[32];
+                    ld32_nw(tlane + T_DVV + 32 * pass, v);
+                    wait_ld();
+                    reg_fence(v);
                     if (live) {
-                        *reinterpret_cast<uint4 *>(dst + 16 * cc) =
-                            make_uint4(mma::pack_bf16(v[0], v[1]), mma::pack_bf16(v[2], v[3]),
-                                       mma::pack_bf16(v[4], v[5]), mma::pack_bf16(v[6], v[7]));
-                        *reinterpret_cast<uint4 *>(dst + 16 * cc + 8) =
-                            make_uint4(mma::pack_bf16(v[8], v[9]), mma::pack_bf16(v[10], v[11]),
-                                       mma::pack_bf16(v[12], v[13]), mma::pack_bf16(v[14], v[15]));
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(dst + 32 * pass + 8 * q) =
+                                make_uint4(mma::pack_bf16(uf(v[8 * q]), uf(v[8 * q + 1])),
+                                           mma::pack_bf16(uf(v[8 * q + 2]), uf(v[8 * q + 3])),
+                                           mma::pack_bf16(uf(v[8 * q + 4]), uf(v[8 * q + 5])),
+                                           mma::pack_bf16(uf(v[8 * q + 6]), uf(v[8 * q + 7])));
                     }
                 }
                 fence_before();
@@ -511,35 +536,39 @@ __global__ void __launch_bounds__(NTHW, 1)
             if (!wait_phase(bar(B_C), par, abort)) break;
             fence_after();
             if (h == 1) {
-                // dK row t = inv (dxhat - x inv^2 (x . dxhat)), straight to global memory
+                // dK row t = inv (dxhat - x inv^2 (x . dxhat)), x parked in TMEM; straight to global memory
                 float dot = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < D / 16; ++cc) {
-                    float v[16];
-                    ld16(tlane + T_DV + 16 * cc, v);
-                    const uint4 w0 = xw[2 * cc], w1 = xw[2 * cc + 1];
-                    const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                for (int pass = 0; pass < D / 32; ++pass) {
+                    uint32_t v[32], xr[16];
+                    ld32_nw(tlane + T_DV + 32 * pass, v);
+                    ld16_nw(tlane + T_SC + 16 * pass, xr);
+                    wait_ld();
+                    reg_fence(v);
+                    reg_fence(xr);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        dot = fmaf(bf_lo(ww[j]), v[2 * j], dot);
-                        dot = fmaf(bf_hi(ww[j]), v[2 * j + 1], dot);
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        dot = fmaf(bf_lo(xr[j]), uf(v[2 * j]), fmaf(bf_hi(xr[j]), uf(v[2 * j + 1]), dot));
                 }
                 const float kk = inv * inv * dot;
                 bf16 *dst = dK + off + (n0 + t) * D;
 #pragma unroll
-                for (int cc = 0; cc < D / 16; ++cc) {
-                    float v[16];
-                    ld16(tlane + T_DV + 16 * cc, v);
-                    const uint4 w0 = xw[2 * cc], w1 = xw[2 * cc + 1];
-                    const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                    uint32_t o[8];
+                for (int pass = 0; pass < D / 32; ++pass) {
+                    uint32_t v[32], xr[16];
+                    ld32_nw(tlane + T_DV + 32 * pass, v);
+                    ld16_nw(tlane + T_SC + 16 * pass, xr);
+                    wait_ld();
+                    reg_fence(v);
+                    reg_fence(xr);
+                    uint32_t o[16];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        o[j] = mma::pack_bf16(inv * (v[2 * j] - bf_lo(ww[j]) * kk), inv * (v[2 * j + 1] - bf_hi(ww[j]) * kk));
+                    for (int j = 0; j < 16; ++j)
+                        o[j] = mma::pack_bf16(inv * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), inv * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
                     if (live) {
-                        *reinterpret_cast<uint4 *>(dst + 16 * cc) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(dst + 16 * cc + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(dst + 32 * pass + 8 * q) =
+                                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                     }
                 }
             } else {
@@ -717,9 +746,16 @@ __global__ void __launch_bounds__(NTHW, 1)
 
     // S (TMEM) -> bf16 hi / lo operand rows d and fp32 B_prev; warps 4-7
     auto convert_s = [&]() {
+        uint32_t ar[32], mv = 0;
+        if (t < D) ld32_nw(tlane + T_ST, ar);
+        if (q4 == 0) ld1_nw(tlane + T_MS, mv);
+        wait_ld();
+        reg_fence(ar);
+        reg_fence1(mv);
         if (t < D) {
             float a[32];
-            ld32(tlane + T_ST, a);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = uf(ar[j]);
             uint32_t hw[16], lw[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -734,11 +770,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 st_shared_v4(base + Ly.slo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
             }
         }
-        if (q4 == 0) {
-            float m[1];
-            ldn<1>(tlane + T_MS, m);
-            bprev[lane] = lane < LR ? m[0] : 0.f;
-        }
+        if (q4 == 0) bprev[lane] = lane < LR ? uf(mv) : 0.f;
     };
 
     if (!compute) {
@@ -937,20 +969,24 @@ __global__ void __launch_bounds__(NTHW, 1)
             {
                 const int j0 = 64 * h;
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int jb = j0 + 16 * b;
-                    uint32_t w[8];
-                    if (jb <= 32 * q4 + 31) {  // warp-uniform: some lane keeps a column
-                        float a[16];
-                        ld16(tlane + T_DV + jb, a);
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int jb = j0 + 32 * pass;
+                    const bool need = jb <= 32 * q4 + 31;  // warp-uniform: some lane keeps a column
+                    uint32_t a[32];
+                    if (need) ld32_nw(tlane + T_DV + jb, a);
+                    wait_ld();
+                    reg_fence(a);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            w[j] = mma::pack_bf16(jb + 2 * j <= t ? a[2 * j] : 0.f, jb + 2 * j + 1 <= t ? a[2 * j + 1] : 0.f);
-                    } else {
+                    for (int b = 0; b < 2; ++b) {
+                        uint32_t w[8];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) w[j] = 0u;
+                        for (int j = 0; j < 8; ++j) {
+                            const int e = 16 * b + 2 * j;
+                            w[j] = mma::pack_bf16(need && jb + e <= t ? uf(a[e]) : 0.f,
+                                                  need && jb + e + 1 <= t ? uf(a[e + 1]) : 0.f);
+                        }
+                        stn<8>(tlane + T_DV + j0 + 16 * pass + 8 * b, w);
                     }
-                    stn<8>(tlane + T_DV + j0 + 8 * b, w);
                 }
             }
             wait_st();
@@ -959,20 +995,25 @@ __global__ void __launch_bounds__(NTHW, 1)
             fence_after();
             if (h == 0) {
                 // den, c, dphi_Q and the feature Jacobian; F'_Q, -c and {1/den, c}, table by table
+                uint32_t gr[32], br[32];
+                ld32_nw(tlane + T_G, gr);
+                ld32_nw(tlane + T_BT, br);
+                wait_ld();
+                reg_fence(gr);
+                reg_fence(br);
                 float den = 0.f, pg = 0.f;
 #pragma unroll
                 for (int l = 0; l < LMAX; ++l) {
                     if (l < L && l * R < LRMAX) {
-                        float u[P], ph[R], g[R], bt[R];
+                        float u[P], ph[R];
 #pragma unroll
                         for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
                         tc::bucket_probs<P>(u, beta, ph);
-                        ld_cols<R>(tlane + T_G + l * R, g);
-                        ld_cols<R>(tlane + T_BT + l * R, bt);
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            den = fmaf(ph[r], bprev[l * R + r] + bt[r], den);
-                            pg = fmaf(ph[r], g[r], pg);
+                            const int lr = l * R + r < 32 ? l * R + r : 31;
+                            den = fmaf(ph[r], bprev[lr] + uf(br[lr]), den);
+                            pg = fmaf(ph[r], uf(gr[lr]), pg);
                         }
                     }
                 }
@@ -985,14 +1026,15 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                 for (int l = 0; l < LMAX; ++l) {
                     if (l < L && l * R < LRMAX) {
-                        float u[P], ph[R], g[R], bt[R];
+                        float u[P], ph[R], g[R];
 #pragma unroll
                         for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
                         tc::bucket_probs<P>(u, beta, ph);
-                        ld_cols<R>(tlane + T_G + l * R, g);
-                        ld_cols<R>(tlane + T_BT + l * R, bt);
 #pragma unroll
-                        for (int r = 0; r < R; ++r) g[r] = (g[r] - (bprev[l * R + r] + bt[r]) * cc) * rd;
+                        for (int r = 0; r < R; ++r) {
+                            const int lr = l * R + r < 32 ? l * R + r : 31;
+                            g[r] = (uf(gr[lr]) - (bprev[lr] + uf(br[lr])) * cc) * rd;
+                        }
                         float tmp[P];
                         table_backward<P>(u, ph, g, beta, tmp);
 #pragma unroll
@@ -1039,32 +1081,36 @@ __global__ void __launch_bounds__(NTHW, 1)
                 // dQ row t = inv (dxhat - x inv^2 (x . dxhat)), straight to global memory
                 float dot = 0.f;
 #pragma unroll
-                for (int cc16 = 0; cc16 < D / 16; ++cc16) {
-                    float v[16], xv[8];
-                    ld16(tlane + T_DV + 16 * cc16, v);
-                    ldn<8>(tlane + T_X + 8 * cc16, xv);
+                for (int pass = 0; pass < D / 32; ++pass) {
+                    uint32_t v[32], xr[16];
+                    ld32_nw(tlane + T_DV + 32 * pass, v);
+                    ld16_nw(tlane + T_X + 16 * pass, xr);
+                    wait_ld();
+                    reg_fence(v);
+                    reg_fence(xr);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t w = __float_as_uint(xv[j]);
-                        dot = fmaf(bf_lo(w), v[2 * j], fmaf(bf_hi(w), v[2 * j + 1], dot));
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        dot = fmaf(bf_lo(xr[j]), uf(v[2 * j]), fmaf(bf_hi(xr[j]), uf(v[2 * j + 1]), dot));
                 }
                 const float kk = inv * inv * dot;
                 bf16 *dst = dQ + off + (n0 + t) * D;
 #pragma unroll
-                for (int cc16 = 0; cc16 < D / 16; ++cc16) {
-                    float v[16], xv[8];
-                    ld16(tlane + T_DV + 16 * cc16, v);
-                    ldn<8>(tlane + T_X + 8 * cc16, xv);
-                    uint32_t o[8];
+                for (int pass = 0; pass < D / 32; ++pass) {
+                    uint32_t v[32], xr[16];
+                    ld32_nw(tlane + T_DV + 32 * pass, v);
+                    ld16_nw(tlane + T_X + 16 * pass, xr);
+                    wait_ld();
+                    reg_fence(v);
+                    reg_fence(xr);
+                    uint32_t o[16];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t w = __float_as_uint(xv[j]);
-                        o[j] = mma::pack_bf16(inv * (v[2 * j] - bf_lo(w) * kk), inv * (v[2 * j + 1] - bf_hi(w) * kk));
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        o[j] = mma::pack_bf16(inv * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), inv * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
                     if (live) {
-                        *reinterpret_cast<uint4 *>(dst + 16 * cc16) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(dst + 16 * cc16 + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(dst + 32 * pass + 8 * q) =
+                                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                     }
                 }
             } else {

@@ -79,47 +79,41 @@ __device__ __forceinline__ void sketch_to_operand(uint32_t tlane, int q4, int la
 {
     const int row = 32 * q4 + lane;
     const uint32_t dst = h ? slo : shi;
-    if (32 * q4 < D) {  // content: lane = d
-        float v[64];
-        {
-            float a[32];
-            ld32(tlane + T_ST, a);
+    const bool content = 32 * q4 < D, mass = 32 * q4 < lrp;  // warp-uniform
+    // one pass per 32 sketch columns so that only 32 values are in flight per wait
+    for (int half = 0; half < (lrp > 32 ? 2 : 1); ++half) {
+        uint32_t a[32], m0 = 0;
+        if (content) ld32_nw(tlane + T_ST + 32 * half, a);
+        if (mass && half == 0) ld1_nw(tlane + T_MS, m0);
+        wait_ld();
+        reg_fence(a);
+        reg_fence1(m0);
+        if (content) {  // lane = d
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = a[j];
-        }
-        if (lrp > 32) {
-            float a[32];
-            ld32(tlane + T_ST + 32, a);
+            for (int c = 0; c < 4; ++c) {
+                const int cg = 4 * half + c;  // 8-column chunk of the operand row
+                if (8 * cg < lrp) {
+                    uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[32 + j] = a[j];
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[32 + j] = 0.f;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            if (8 * c < lrp) {
-                uint32_t w[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float x0 = 8 * c + 2 * j < LR ? v[8 * c + 2 * j] : 0.f;
-                    float x1 = 8 * c + 2 * j + 1 < LR ? v[8 * c + 2 * j + 1] : 0.f;
-                    if (h) {
-                        x0 = bf16_rest(x0);
-                        x1 = bf16_rest(x1);
+                    for (int j = 0; j < 4; ++j) {
+                        const int k0 = 8 * c + 2 * j;
+                        float x0 = 32 * half + k0 < LR ? uf(a[k0]) : 0.f;
+                        float x1 = 32 * half + k0 + 1 < LR ? uf(a[k0 + 1]) : 0.f;
+                        if (h) {
+                            x0 = bf16_rest(x0);
+                            x1 = bf16_rest(x1);
+                        }
+                        w[j] = mma::pack_bf16(x0, x1);
                     }
-                    w[j] = mma::pack_bf16(x0, x1);
+                    st_shared_v4(dst + sw_chunk(row, cg), w[0], w[1], w[2], w[3]);
                 }
-                st_shared_v4(dst + sw_chunk(row, c), w[0], w[1], w[2], w[3]);
             }
         }
-    }
-    if (32 * q4 < lrp) {  // mass: lane = sketch row
-        float m[1];
-        ldn<1>(tlane + T_MS, m);
-        float x = row < LR ? m[0] : 0.f;
-        if (h) x = bf16_rest(x);
-        st_shared_b16(dst + sw_elem(D, row), __float2bfloat16_rn(x));
+        if (mass && half == 0) {  // lane = sketch row
+            float x = row < LR ? uf(m0) : 0.f;
+            if (h) x = bf16_rest(x);
+            st_shared_b16(dst + sw_elem(D, row), __float2bfloat16_rn(x));
+        }
     }
 }
 
@@ -333,21 +327,25 @@ __global__ void __launch_bounds__(NTHW, 1)
         // output epilogue of chunk c: O = num / den (this half's columns), staged in V stage c & 1
         auto epilogue = [&](int c) {
             const uint32_t stage = base + Ly.v + (c & 1) * Ly.kbb;
-            float v[16];
-            ld16(tlane + T_O + D, v);
-            const float rd = __frcp_rn(v[0]);
+            // this half's D / 2 columns in 32-column passes; den rides on the first
+            float rd = 0.f;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                const int c0 = h * (D / 2) + 16 * cc;
-                ld16(tlane + T_O + c0, v);
+            for (int pass = 0; pass < D / 64; ++pass) {
+                uint32_t v[32], dn = 0;
+                ld32_nw(tlane + T_O + h * (D / 2) + 32 * pass, v);
+                if (pass == 0) ld1_nw(tlane + T_O + D, dn);
+                wait_ld();
+                reg_fence(v);
+                reg_fence1(dn);
+                if (pass == 0) rd = __frcp_rn(uf(dn));
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int ch = (c0 >> 3) + j;
-                    st_shared_v4(stage + (ch >> 3) * BLK + sw_chunk(t, ch & 7),
-                                 mma::pack_bf16(v[8 * j] * rd, v[8 * j + 1] * rd),
-                                 mma::pack_bf16(v[8 * j + 2] * rd, v[8 * j + 3] * rd),
-                                 mma::pack_bf16(v[8 * j + 4] * rd, v[8 * j + 5] * rd),
-                                 mma::pack_bf16(v[8 * j + 6] * rd, v[8 * j + 7] * rd));
+                for (int j = 0; j < 4; ++j) {  // 8-column chunks of this pass
+                    const int ch = h * (D / 16) + 4 * pass + j;
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = uf(v[8 * j + e]) * rd;
+                    st_shared_v4(stage + (ch >> 3) * BLK + sw_chunk(t, ch & 7), mma::pack_bf16(x[0], x[1]),
+                                 mma::pack_bf16(x[2], x[3]), mma::pack_bf16(x[4], x[5]), mma::pack_bf16(x[6], x[7]));
                 }
             }
         };
@@ -437,22 +435,24 @@ __global__ void __launch_bounds__(NTHW, 1)
             fence_after();
             {
                 const int j0 = 64 * h;
+                const bool need0 = j0 <= 32 * q4 + 31, need1 = j0 + 32 <= 32 * q4 + 31;  // warp-uniform
+                uint32_t a0[32], a1[32];
+                if (need0) ld32_nw(tlane + T_SC + j0, a0);
+                if (need1) ld32_nw(tlane + T_SC + j0 + 32, a1);
+                wait_ld();
+                reg_fence(a0);
+                reg_fence(a1);
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     const int jb = j0 + 32 * b;
                     uint32_t r0[8], r1[8];
-                    if (jb <= t) {
-                        float a[32];
-                        ld32(tlane + T_SC + jb, a);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int jj = jb + 2 * j;
-                            r0[j] = mma::pack_bf16(jj <= t ? a[2 * j] : 0.f, jj + 1 <= t ? a[2 * j + 1] : 0.f);
-                            r1[j] = mma::pack_bf16(jj + 16 <= t ? a[16 + 2 * j] : 0.f, jj + 17 <= t ? a[17 + 2 * j] : 0.f);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) r0[j] = r1[j] = 0u;
+                    for (int j = 0; j < 8; ++j) {
+                        const int jj = jb + 2 * j;
+                        const uint32_t x0 = b ? a1[2 * j] : a0[2 * j], x1 = b ? a1[2 * j + 1] : a0[2 * j + 1];
+                        const uint32_t x2 = b ? a1[16 + 2 * j] : a0[16 + 2 * j], x3 = b ? a1[17 + 2 * j] : a0[17 + 2 * j];
+                        r0[j] = mma::pack_bf16(jj <= t ? uf(x0) : 0.f, jj + 1 <= t ? uf(x1) : 0.f);
+                        r1[j] = mma::pack_bf16(jj + 16 <= t ? uf(x2) : 0.f, jj + 17 <= t ? uf(x3) : 0.f);
                     }
                     stn<8>(tlane + T_P + jb / 2, r0);
                     stn<8>(tlane + T_P + jb / 2 + 8, r1);
