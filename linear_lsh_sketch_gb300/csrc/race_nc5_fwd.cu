@@ -25,22 +25,28 @@ namespace nc5 {
 
 // ------------------------------------------------------------------ sketch reduction
 
+constexpr int NTHW = NTH + 32;  // 8 compute warps + 1 control warp (TMA and MMA issue)
+
 struct SketchLayout {
-    uint32_t stg, x, f, whi, wlo, mass, red, bar, slot, bytes;
-    int nmb;
+    uint32_t stg, x, y, f, fbytes, whi, wlo, mass, red, bar, slot, bytes;
+    int nmb, nf;
     __host__ __device__ SketchLayout(int D, int LR)
     {
         const uint32_t KB = D / 64;
         nmb = (LR + 127) / 128;
-        stg = 2 * KB * BLK;
-        x = 0;
-        f = 2 * stg;
-        whi = f + 2 * nmb * BLK;
+        fbytes = 2 * nmb * BLK;  // one feature buffer: M = 128 sketch rows per block
+        const uint32_t fixed = 2 * 2 * KB * BLK + 2 * KB * WBLK + 2 * 4096 + 2 * 2 * C * 4 + 256;
+        nf = (fixed + 2 * fbytes + 1024 <= 227 * 1024) ? 2 : 1;  // double-buffer the features if they fit
+        stg = KB * BLK;
+        x = 0;                  // X stages [2][KB blocks]
+        y = x + 2 * stg;        // Y stages [2][KB blocks]
+        f = y + 2 * stg;        // feature buffers [nf]
+        whi = f + nf * fbytes;
         wlo = whi + KB * WBLK;
-        mass = wlo + KB * WBLK;
-        red = mass + 4096;
-        bar = red + 2 * C * 4;
-        slot = bar + 32;
+        mass = wlo + KB * WBLK;  // mass operand [2] (4 KB each)
+        red = mass + 2 * 4096;   // row-norm halves [2 parities][2][C]
+        bar = red + 2 * 2 * C * 4;
+        slot = bar + 128;
         bytes = slot + 16;
     }
 };
@@ -48,14 +54,20 @@ struct SketchLayout {
 __host__ __device__ inline uint32_t sketch_zcol(int D, int nmb) { return nmb == 1 ? ((D + 16 + 31) & ~31) : 448; }
 __host__ __device__ inline uint32_t sketch_tmem_cols(int D, int nmb)
 {
-    const uint32_t need = sketch_zcol(D, nmb) + LPP;
+    const uint32_t need = sketch_zcol(D, nmb) + 2 * LPP;  // two projection buffers
     return need <= 128 ? 128 : need <= 256 ? 256 : 512;
 }
 
+// The features of tile i + 1 can be ready before the issuing warp has observed those of tile i
+// (its projection is issued early), so "features ready" has one barrier per tile parity.
+enum : uint32_t { SB_X0, SB_X1, SB_Y0, SB_Y1, SB_P0, SB_P1, SB_S0, SB_S1, SB_F0, SB_F1, SB_CS, SB_DONE, SB_COUNT };
+
 // mode 0: X = K, Y = V, m = 1.  mode 1: X = Q, Y = dO, Phi scaled by aux.x = 1/den, m = -aux.y
 // (= -c, split into bf16 hi and lo rows).  part: [BH][nsplit][LR][d + 1] fp32.
+// Warp 8 issues the TMA copies and MMAs; the projection of tile i + 1 is issued ahead of the
+// sketch product of tile i, so the compute warps featurise tile i + 1 while it runs.
 template <int D, int P>
-__global__ void __launch_bounds__(NTH, 1)
+__global__ void __launch_bounds__(NTHW, 1)
     k_sketch5(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY, Dims Dm,
               const float *__restrict__ W, const float2 *__restrict__ aux, int64_t seg_len, int nsplit,
               float *__restrict__ part, unsigned *__restrict__ err, int mode)
@@ -66,11 +78,13 @@ __global__ void __launch_bounds__(NTH, 1)
     const uint32_t base = (raw + 1023) & ~1023u;
     unsigned char *sm = smem_raw + (base - raw);
     const SketchLayout Ly(D, Dm.LR);
-    const int nmb = Ly.nmb;
+    const int nmb = Ly.nmb, nf = Ly.nf;
     float *red = reinterpret_cast<float *>(sm + Ly.red);
-    const uint32_t bar_load = base + Ly.bar, bar_proj = bar_load + 16, bar_done = bar_load + 24;
+    auto bar = [&](uint32_t i) { return base + Ly.bar + 8 * i; };
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = warp >> 2;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = (warp >> 2) & 1;
+    const bool compute = warp < 8;
     const int t = 32 * q4 + lane;
     const int split = blockIdx.x;
     const int64_t bh = blockIdx.y;
@@ -78,18 +92,18 @@ __global__ void __launch_bounds__(NTH, 1)
     const int64_t n_end = min(Dm.N, n_begin + seg_len);
     const int ntile = n_end > n_begin ? (int)((n_end - n_begin + C - 1) / C) : 0;
     const uint32_t zcol = sketch_zcol(D, nmb), ncols = sketch_tmem_cols(D, nmb);
-    const uint32_t tile_bytes = 2 * KB * BLK;
 
     // ---- set-up
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
-    zero_region(sm + Ly.f, 2 * nmb * BLK);
-    init_mass_tile(sm + Ly.mass, mode == 0);  // mode 1 writes rows 0 and 1 per tile
-    load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
-    if (tid == 0) {
-        mbar_init(bar_load, 1);
-        mbar_init(bar_load + 8, 1);
-        mbar_init(bar_proj, 1);
-        mbar_init(bar_done, 1);
+    if (compute) {
+        zero_region(sm + Ly.f, nf * Ly.fbytes);
+        init_mass_tile(sm + Ly.mass, mode == 0);  // mode 1 writes rows 0 and 1 per tile
+        init_mass_tile(sm + Ly.mass + 4096, mode == 0);
+        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    }
+    if (tid == NTH) {
+        for (uint32_t i = 0; i < SB_COUNT; ++i) mbar_init(bar(i), (i == SB_F0 || i == SB_F1) ? 8 : i == SB_CS ? NTH : 1);
+        *abort = 0;
         tc::fence_mbar_init();
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmY);
@@ -101,124 +115,163 @@ __global__ void __launch_bounds__(NTH, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Ly.slot);
     const uint32_t tlane = tmem + ((uint32_t)(32 * q4) << 16);
 
-    auto issue_load = [&](int i) {
-        const int s = i & 1;
-        const uint32_t xs = base + Ly.x + s * Ly.stg, ys = xs + KB * BLK;
-        const int y = (int)(n_begin + (int64_t)i * C);
-        mbar_arrive_expect_tx(bar_load + 8 * s, tile_bytes);
+    if (!compute) {
+        // ---------------------------------------------------------------- control warp
+        if (lane == 0) {
+            auto load = [&](int i, bool is_y) {
+                const int s = i & 1;
+                const uint32_t b = bar((is_y ? SB_Y0 : SB_X0) + s);
+                const uint32_t dst = base + (is_y ? Ly.y : Ly.x) + s * Ly.stg;
+                mbar_arrive_expect_tx(b, KB * BLK);
 #pragma unroll
-        for (int kb = 0; kb < KB; ++kb) {
-            tma_load(xs + kb * BLK, &tmX, 64 * kb, y, (int)bh, bar_load + 8 * s);
-            tma_load(ys + kb * BLK, &tmY, 64 * kb, y, (int)bh, bar_load + 8 * s);
-        }
-    };
-    if (tid == 0) {
-        if (ntile > 0) issue_load(0);
-        if (ntile > 1) issue_load(1);
-    }
-
-    bool failed = false;
-    int i = 0;
-    for (; i < ntile; ++i) {
-        const int s = i & 1;
-        const int64_t n0 = n_begin + (int64_t)i * C;
-        const int cnt = (int)min((int64_t)C, n_end - n0);
-        const uint32_t xs = base + Ly.x + s * Ly.stg, ys = xs + KB * BLK;
-        if (wait_all(bar_load + 8 * s, (i >> 1) & 1)) {
-            failed = true;
-            break;
-        }
-        if (tid == 0) {
-            fence_after();
-            issue_projection<D>(tmem + zcol, xs, base + Ly.whi, base + Ly.wlo);
-            commit(bar_proj);
-        }
-        // the row norm does not need the projection
-        red[h * C + t] = half_sumsq<D>(xs, t, h);
-        if (wait_all(bar_proj, i & 1)) {
-            failed = true;
-            break;
-        }
-        fence_after();
-        // the projection of tile i completing implies the sketch MMAs of tile i - 1 did too, so
-        // the stage of tile i - 1 (and the feature tile) are free
-        if (tid == 0 && i >= 1 && i + 1 < ntile) issue_load(i + 1);
-        float z[LPP];
-        {
-            float a[32];
-            ld32(tlane + zcol, a);
-#pragma unroll
-            for (int k = 0; k < LPP; ++k) z[k] = a[k];
-        }
-        const float ssq = red[t] + red[C + t];
-        const float inv = ssq > 0.f ? rsqrtf(ssq) : 0.f;
-        const bool live = t < cnt;
-        float scale = live ? 1.f : 0.f;
-        if (mode == 1) {
-            float2 a = make_float2(0.f, 0.f);
-            if (live) a = aux[bh * Dm.N + n0 + t];
-            scale *= a.x;
-            if (h == 0) {
-                const float mcv = -a.y;
-                const bf16 mhi = __float2bfloat16_rn(mcv);
-                const bf16 mlo = __float2bfloat16_rn(mcv - __bfloat162float(mhi));
-                unsigned char *mt = sm + Ly.mass + (t >> 6) * 2048;
-                *reinterpret_cast<bf16 *>(mt + sw_elem(0, t & 63)) = mhi;
-                *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load(dst + kb * BLK, is_y ? &tmY : &tmX, 64 * kb, (int)(n_begin + (int64_t)i * C), (int)bh, b);
+            };
+            int issued[4] = {0, 0, 0, 0}, done[4] = {0, 0, 0, 0};  // X0, X1, Y0, Y1
+            for (int i = 0; i < 2 && i < ntile; ++i) {
+                load(i, false);
+                load(i, true);
+                ++issued[i];
+                ++issued[2 + i];
             }
-        }
-        write_features<P>(z, inv, Dm.beta, Dm.L, h, scale, t, base + Ly.f);
-        tc::fence_proxy_async();
-        fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            fence_after();
             constexpr uint32_t id_v = idesc_bf16(128, D, 1, 1);
             constexpr uint32_t id_m = idesc_bf16(128, 16, 1, 0);
-            for (int m = 0; m < nmb; ++m) {
-                const uint32_t acc = tmem + m * 256;
+            auto proj = [&](int i) {
+                const int s = i & 1;
+                if (!wait_phase(bar(SB_X0 + s), (i >> 1) & 1, abort)) return false;
+                ++done[s];
+                fence_after();
+                issue_projection<D>(tmem + zcol + LPP * s, base + Ly.x + s * Ly.stg, base + Ly.whi, base + Ly.wlo);
+                commit(bar(SB_P0 + s));
+                return true;
+            };
+            bool ok = ntile == 0 || proj(0);
+            for (int i = 0; i < ntile && ok; ++i) {
+                const int s = i & 1;
+                if (i + 1 < ntile && !(ok = proj(i + 1))) break;
+                if (!(ok = wait_phase(bar(SB_F0 + s), (i >> 1) & 1, abort))) break;
+                if (!(ok = wait_phase(bar(SB_Y0 + s), (i >> 1) & 1, abort))) break;
+                ++done[2 + s];
+                fence_after();
+                const uint32_t fbuf = base + Ly.f + (i % nf) * Ly.fbytes;
+                const uint32_t mbuf = base + Ly.mass + (mode ? (i & 1) * 4096 : 0);
+                const uint32_t ys = base + Ly.y + s * Ly.stg;
+                for (int m = 0; m < nmb; ++m) {
+                    const uint32_t acc = tmem + m * 256;
 #pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks) {
-                    const uint64_t a = desc_mn(base + Ly.f + 2 * m * BLK + ks * 2048, BLK);
-                    const bool accum = i > 0 || ks > 0;
-                    umma(acc, a, desc_mn(ys + ks * 2048, BLK), id_v, accum);
-                    umma(acc + D, a, desc_k(base + Ly.mass + (ks >> 2) * 2048 + (ks & 3) * 32), id_m, accum);
+                    for (int ks = 0; ks < C / 16; ++ks) {
+                        const uint64_t a = desc_mn(fbuf + 2 * m * BLK + ks * 2048, BLK);
+                        const bool accum = i > 0 || ks > 0;
+                        umma(acc, a, desc_mn(ys + ks * 2048, BLK), id_v, accum);
+                        umma(acc + D, a, desc_k(mbuf + (ks >> 2) * 2048 + (ks & 3) * 32), id_m, accum);
+                    }
+                }
+                commit(bar(SB_S0 + s));
+                // X stage s: read by the projection and the norms of tile i (both done: features are in)
+                if (i + 2 < ntile) {
+                    load(i + 2, false);
+                    ++issued[s];
+                }
+                // Y stage s ^ 1: read by the sketch product of tile i - 1
+                if (i >= 1 && i + 1 < ntile) {
+                    if (!(ok = wait_phase(bar(SB_S0 + (s ^ 1)), ((i - 1) >> 1) & 1, abort))) break;
+                    load(i + 1, true);
+                    ++issued[2 + (s ^ 1)];
                 }
             }
+            if (ok) commit(bar(SB_DONE));
+            if (!ok) {
+                atomicOr(err, kErrTimeout);
+                *abort = 1;
+                for (int b = 0; b < 4; ++b)
+                    if (issued[b] > done[b]) mbar_wait(bar(SB_X0 + b), done[b] & 1);
+            }
         }
-    }
-    if (tid == 0 && !failed) commit(bar_done);
-    if (!failed) failed = wait_all(bar_done, 0);
-    if (failed) {
-        if (tid == 0) atomicOr(err, kErrTimeout);
-        // let copies still in flight land before the CTA's shared memory goes away
-        if (i < ntile) mbar_wait(bar_load + 8 * (i & 1), (i >> 1) & 1);
-        if (i + 1 < ntile) mbar_wait(bar_load + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1);
+        __syncwarp();
     } else {
-        fence_after();
-        // epilogue: sketch row lr = 128 m + t of block m; the two halves split the columns
-        float *out = part + ((int64_t)bh * nsplit + split) * Dm.LR * (D + 1);
-        for (int m = 0; m < (ntile > 0 ? nmb : 0); ++m) {
-            const int lr = 128 * m + t;
-            const uint32_t acc = tlane + m * 256;
+        // ---------------------------------------------------------------- compute warps
+        bool ok = true;
+        for (int i = 0; i < ntile && ok; ++i) {
+            const int s = i & 1;
+            const int64_t n0 = n_begin + (int64_t)i * C;
+            const int cnt = (int)min((int64_t)C, n_end - n0);
+            if (!(ok = wait_phase(bar(SB_X0 + s), (i >> 1) & 1, abort))) break;
+            float *rd_ = red + (i & 1) * 2 * C;
+            rd_[h * C + t] = half_sumsq<D>(base + Ly.x + s * Ly.stg, t, h);
+            if (!(ok = group_sync(bar(SB_CS), i & 1, abort))) break;
+            const float ssq = rd_[t] + rd_[C + t];
+            const float inv = ssq > 0.f ? rsqrtf(ssq) : 0.f;
+            if (!(ok = wait_phase(bar(SB_P0 + s), (i >> 1) & 1, abort))) break;
+            fence_after();
+            float z[LPP];
+            {
+                uint32_t a[32];
+                ld32_nw(tlane + zcol + LPP * s, a);
+                wait_ld();
+                reg_fence(a);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                const int c0 = h * (D / 2) + 16 * cc;
-                float v[16];
-                ld16(acc + c0, v);
-                if (lr < Dm.LR) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) out[(int64_t)lr * (D + 1) + c0 + k] = v[k];
+                for (int k = 0; k < LPP; ++k) z[k] = uf(a[k]);
+            }
+            // the feature buffer (and mass operand) of this tile were last read by an earlier product
+            if (nf == 2 && i >= 2) {
+                if (!(ok = wait_phase(bar(SB_S0 + s), ((i - 2) >> 1) & 1, abort))) break;
+            } else if (nf == 1 && i >= 1) {
+                if (!(ok = wait_phase(bar(SB_S0 + (s ^ 1)), ((i - 1) >> 1) & 1, abort))) break;
+            }
+            if (mode == 1 && nf == 1 && i >= 2) {  // mass buffer s was read by the product of tile i - 2
+                if (!(ok = wait_phase(bar(SB_S0 + s), ((i - 2) >> 1) & 1, abort))) break;
+            }
+            const bool live = t < cnt;
+            float scale = live ? 1.f : 0.f;
+            if (mode == 1) {
+                float2 a = make_float2(0.f, 0.f);
+                if (live) a = aux[bh * Dm.N + n0 + t];
+                scale *= a.x;
+                if (h == 0) {
+                    const float mcv = -a.y;
+                    const bf16 mhi = __float2bfloat16_rn(mcv);
+                    const bf16 mlo = __float2bfloat16_rn(mcv - __bfloat162float(mhi));
+                    unsigned char *mt = sm + Ly.mass + (i & 1) * 4096 + (t >> 6) * 2048;
+                    *reinterpret_cast<bf16 *>(mt + sw_elem(0, t & 63)) = mhi;
+                    *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
                 }
             }
-            if (h == 1) {
-                float v[16];
-                ld16(acc + D, v);
-                if (lr < Dm.LR) out[(int64_t)lr * (D + 1) + D] = mode == 1 ? v[0] + v[1] : v[0];
-            }
+            write_features<P>(z, inv, Dm.beta, Dm.L, h, scale, t, base + Ly.f + (i % nf) * Ly.fbytes);
+            warp_signal(bar(SB_F0 + s));
         }
-        if (ntile == 0)  // an empty range contributes a zero partial (its accumulator was never written)
-            for (int e = tid; e < Dm.LR * (D + 1); e += NTH) out[e] = 0.f;
+        if (ok && ntile > 0) ok = wait_phase(bar(SB_DONE), 0, abort);
+        float *out = part + ((int64_t)bh * nsplit + split) * Dm.LR * (D + 1);
+        if (ok) {
+            fence_after();
+            // epilogue: sketch row lr = 128 m + t of block m; the two halves split the columns
+            for (int m = 0; m < (ntile > 0 ? nmb : 0); ++m) {
+                const int lr = 128 * m + t;
+                const uint32_t acc = tlane + m * 256;
+#pragma unroll
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    const int c0 = h * (D / 2) + 32 * cc;
+                    uint32_t v[32];
+                    ld32_nw(acc + c0, v);
+                    wait_ld();
+                    reg_fence(v);
+                    if (lr < Dm.LR) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) out[(int64_t)lr * (D + 1) + c0 + k] = uf(v[k]);
+                    }
+                }
+                if (h == 1) {
+                    uint32_t m0, m1;
+                    ld1_nw(acc + D, m0);
+                    ld1_nw(acc + D + 1, m1);
+                    wait_ld();
+                    reg_fence1(m0);
+                    reg_fence1(m1);
+                    if (lr < Dm.LR) out[(int64_t)lr * (D + 1) + D] = mode == 1 ? uf(m0) + uf(m1) : uf(m0);
+                }
+            }
+            if (ntile == 0)  // an empty range contributes a zero partial (its accumulator was never written)
+                for (int e = tid; e < Dm.LR * (D + 1); e += NTH) out[e] = 0.f;
+        }
     }
     fence_before();
     __syncthreads();
@@ -514,7 +567,7 @@ cudaError_t sketch_inst(const Dims &Dm, const CUtensorMap &mx, const CUtensorMap
     cudaError_t e = prep_smem(kern, smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(mode ? "tc5_sketch_grad" : "tc5_sketch_keys", kern, dim3(nsplit, (unsigned)Dm.BH),
-                         dim3(nc5::NTH), smem, st, mx, my, Dm, W, aux, seg_len, nsplit, part, err, mode);
+                         dim3(nc5::NTHW), smem, st, mx, my, Dm, W, aux, seg_len, nsplit, part, err, mode);
 }
 
 template <int D, int P>

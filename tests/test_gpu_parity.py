@@ -32,6 +32,16 @@ SMALL = [
     W_("bf_d128_c", 1, 2, 555, 128, 3, 3, True, "bf16"),
     W_("bf_lr256", 1, 2, 300, 128, 6, 4, False, "bf16", clusters=8),
     W_("bf_lr64_c", 2, 3, 257, 64, 4, 4, True, "bf16"),
+    # shapes of the tcgen05 paths: bucket counts 2 .. 64, tables 1 .. 16, ragged tails, d 64 / 128
+    W_("bf_p1_l16_c", 1, 2, 700, 64, 1, 16, True, "bf16"),
+    W_("bf_p5_l1_c", 1, 1, 333, 128, 5, 1, True, "bf16"),
+    W_("bf_p4_l2_c", 2, 1, 400, 128, 4, 2, True, "bf16"),
+    W_("bf_p2_l3_c", 1, 2, 260, 64, 2, 3, True, "bf16"),
+    W_("bf_p2_l5_c", 1, 1, 129, 128, 2, 5, True, "bf16"),
+    W_("bf_p1_l16", 1, 2, 700, 64, 1, 16, False, "bf16"),
+    W_("bf_p5_l5", 1, 1, 515, 64, 5, 5, False, "bf16"),
+    W_("bf_p6_l2", 1, 2, 390, 128, 6, 2, False, "bf16", clusters=4),
+    W_("bf_p3_l10", 1, 1, 260, 128, 3, 10, False, "bf16"),
     W_("beta0", 1, 1, 64, 32, 2, 2, False, "f32", beta=0.0),
     # near the hard-hash limit while every bucket probability stays a normal float32
     W_("beta_sharp", 1, 1, 64, 32, 2, 2, True, "f32", beta=12.0),
