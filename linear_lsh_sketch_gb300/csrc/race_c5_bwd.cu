@@ -621,10 +621,10 @@ constexpr uint32_t T_GB = 416;    // G_B (lanes = sketch row), columns 0 + 1 (c 
 constexpr uint32_t T_X = 432;     // the Q row as stored (bf16 pairs), 64 columns
 constexpr uint32_t T_COLS = 512;
 
-enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_COUNT };
+enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_CS2, B_COUNT };
 
 struct QLayout {
-    uint32_t q, k, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, bprev, bar, slot, bytes, kbb;
+    uint32_t q, k, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, bprev, invq, red, bar, slot, bytes, kbb;
     __host__ __device__ QLayout(int D)
     {
         kbb = (uint32_t)(D / 64) * BLK;
@@ -640,8 +640,10 @@ struct QLayout {
         wlo = whi + (uint32_t)(D / 64) * WBLK;
         ncm = wlo + (uint32_t)(D / 64) * WBLK;
         ones = ncm + 4096;
-        bprev = ones + 4096;  // B_prev fp32 [32]
-        bar = bprev + 128;
+        bprev = ones + 4096;  // B_prev fp32 [2 parities][32]
+        invq = bprev + 256;   // 1 / |Q row| fp32 [C]
+        red = invq + 4 * C;   // dQ dot halves fp32 [2][C]
+        bar = red + 8 * C;
         slot = bar + 128;
         bytes = slot + 16;
     }
@@ -667,6 +669,8 @@ __global__ void __launch_bounds__(NTHW, 1)
     auto bar = [&](uint32_t i) { return base + Ly.bar + 8 * i; };
     volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
     float *bprev = reinterpret_cast<float *>(sm + Ly.bprev);
+    float *invq_s = reinterpret_cast<float *>(sm + Ly.invq);
+    float *red = reinterpret_cast<float *>(sm + Ly.red);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = (warp >> 2) & 1;
     const bool compute = warp < 8;
@@ -694,7 +698,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             uint32_t cnt = 1;
             if (i == B_FEAT || i == B_MASK) cnt = 8;
             if (i == B_JAC || i == B_SOP) cnt = 4;
-            if (i == B_CS) cnt = NTH;
+            if (i == B_CS || i == B_CS2) cnt = NTH;
             mbar_init(bar(i), cnt);
         }
         *abort = 0;
@@ -745,7 +749,7 @@ __global__ void __launch_bounds__(NTHW, 1)
     fence_after();
 
     // S (TMEM) -> bf16 hi / lo operand rows d and fp32 B_prev; warps 4-7
-    auto convert_s = [&]() {
+    auto convert_s = [&](int par_out) {
         uint32_t ar[32], mv = 0;
         if (t < D) ld32_nw(tlane + T_ST, ar);
         if (q4 == 0) ld1_nw(tlane + T_MS, mv);
@@ -770,7 +774,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 st_shared_v4(base + Ly.slo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
             }
         }
-        if (q4 == 0) bprev[lane] = lane < LR ? uf(mv) : 0.f;
+        if (q4 == 0) bprev[32 * par_out + lane] = lane < LR ? uf(mv) : 0.f;
     };
 
     if (!compute) {
@@ -857,6 +861,14 @@ __global__ void __launch_bounds__(NTHW, 1)
                     const uint32_t ac = (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4));
                     umma_ts(tmem + T_G, tmem + T_DV + ac, d_fk_mn + (uint64_t)(ks * 128), id_bt, true);
                 }
+                // sketch update (its bf16 copy for the next chunk is made while the Q rows run the
+                // Jacobian)
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_ST, d_v_mt + ko, d_fk_mn + ko, id_gt, true);
+                    umma(tmem + T_MS, d_fk_mn + ko, d_ones + kk, id_m16, true);
+                }
                 commit(bar(B_B));
                 // group C: dxhat, gradient sketch, sketch update
                 if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
@@ -870,8 +882,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                     const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
                     umma(tmem + T_GT, d_do_mt + ko, d_fq_mn + ko, id_gt, true);
                     umma(tmem + T_GB, d_fq_mn + ko, d_ncm + kk, id_m16, true);
-                    umma(tmem + T_ST, d_v_mt + ko, d_fk_mn + ko, id_gt, true);
-                    umma(tmem + T_MS, d_fk_mn + ko, d_ones + kk, id_m16, true);
                 }
                 commit(bar(B_C));
                 if (c + 1 < nchunk) {  // V and dO are last read by group C
@@ -893,7 +903,7 @@ __global__ void __launch_bounds__(NTHW, 1)
     } else {
         // ---------------------------------------------------------------- compute warps
         if (h == 1) {
-            convert_s();
+            convert_s(0);
             warp_signal(bar(B_SOP));
         }
         bool ok = group_sync(bar(B_CS), 0, abort);  // B_prev visible to the Q warps
@@ -918,6 +928,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     }
                 }
                 inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+                if (h == 0) invq_s[t] = inv;
             }
             if (!(ok = wait_phase(bar(B_PROJ), par, abort))) break;
             fence_after();
@@ -1012,7 +1023,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const int lr = l * R + r < 32 ? l * R + r : 31;
-                            den = fmaf(ph[r], bprev[lr] + uf(br[lr]), den);
+                            den = fmaf(ph[r], bprev[32 * par + lr] + uf(br[lr]), den);
                             pg = fmaf(ph[r], uf(gr[lr]), pg);
                         }
                     }
@@ -1033,7 +1044,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const int lr = l * R + r < 32 ? l * R + r : 31;
-                            g[r] = (uf(gr[lr]) - (bprev[lr] + uf(br[lr])) * cc) * rd;
+                            g[r] = (uf(gr[lr]) - (bprev[32 * par + lr] + uf(br[lr])) * cc) * rd;
                         }
                         float tmp[P];
                         table_backward<P>(u, ph, g, beta, tmp);
@@ -1074,17 +1085,22 @@ __global__ void __launch_bounds__(NTHW, 1)
                 *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
                 wait_st();
                 warp_signal(bar(B_JAC));
+            } else {
+                // the sketch after this chunk -> bf16 operand and B_prev of the next chunk
+                convert_s(par ^ 1);
+                warp_signal(bar(B_SOP));
             }
             if (!(ok = wait_phase(bar(B_C), par, abort))) break;
             fence_after();
-            if (h == 0) {
-                // dQ row t = inv (dxhat - x inv^2 (x . dxhat)), straight to global memory
+            {
+                // dQ row t = inv (dxhat - x inv^2 (x . dxhat)); half h takes columns h D/2 .. (h+1) D/2
+                const float iq = invq_s[t];
                 float dot = 0.f;
 #pragma unroll
-                for (int pass = 0; pass < D / 32; ++pass) {
+                for (int pass = 0; pass < D / 64; ++pass) {
                     uint32_t v[32], xr[16];
-                    ld32_nw(tlane + T_DV + 32 * pass, v);
-                    ld16_nw(tlane + T_X + 16 * pass, xr);
+                    ld32_nw(tlane + T_DV + h * (D / 2) + 32 * pass, v);
+                    ld16_nw(tlane + T_X + h * (D / 4) + 16 * pass, xr);
                     wait_ld();
                     reg_fence(v);
                     reg_fence(xr);
@@ -1092,30 +1108,29 @@ __global__ void __launch_bounds__(NTHW, 1)
                     for (int j = 0; j < 16; ++j)
                         dot = fmaf(bf_lo(xr[j]), uf(v[2 * j]), fmaf(bf_hi(xr[j]), uf(v[2 * j + 1]), dot));
                 }
-                const float kk = inv * inv * dot;
-                bf16 *dst = dQ + off + (n0 + t) * D;
+                red[h * C + t] = dot;
+                if (!(ok = group_sync(bar(B_CS2), par, abort))) break;
+                const float kk = iq * iq * (red[t] + red[C + t]);
+                bf16 *dst = dQ + off + (n0 + t) * D + h * (D / 2);
 #pragma unroll
-                for (int pass = 0; pass < D / 32; ++pass) {
+                for (int pass = 0; pass < D / 64; ++pass) {
                     uint32_t v[32], xr[16];
-                    ld32_nw(tlane + T_DV + 32 * pass, v);
-                    ld16_nw(tlane + T_X + 16 * pass, xr);
+                    ld32_nw(tlane + T_DV + h * (D / 2) + 32 * pass, v);
+                    ld16_nw(tlane + T_X + h * (D / 4) + 16 * pass, xr);
                     wait_ld();
                     reg_fence(v);
                     reg_fence(xr);
                     uint32_t o[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        o[j] = mma::pack_bf16(inv * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), inv * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
+                        o[j] = mma::pack_bf16(iq * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), iq * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
                     if (live) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4 *>(dst + 32 * pass + 8 * q) =
-                                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        for (int qq = 0; qq < 4; ++qq)
+                            *reinterpret_cast<uint4 *>(dst + 32 * pass + 8 * qq) =
+                                make_uint4(o[4 * qq], o[4 * qq + 1], o[4 * qq + 2], o[4 * qq + 3]);
                     }
                 }
-            } else {
-                convert_s();
-                warp_signal(bar(B_SOP));
             }
             fence_before();
             if (!(ok = group_sync(bar(B_CS), (c + 1) & 1, abort))) break;  // B_prev, TMEM reads: next chunk
