@@ -151,6 +151,9 @@ __global__ void __launch_bounds__(NTHW, 1)
     const int LR = Dm.LR, lrp = (LR + 15) & ~15;
     const float beta = Dm.beta;
     const int L = Dm.L;
+    // L R <= 32: the features of consecutive chunks use alternate buffers (F_Q: 16 TMEM columns
+    // each, F_K: one 16 KB tile each), so chunk c featurises while chunk c - 1's products run
+    const bool pipe = lrp <= 32;
 
     // ---- set-up
     if (warp == 0) tmem_alloc(base + Ly.slot, T_COLS);
@@ -247,25 +250,34 @@ __global__ void __launch_bounds__(NTHW, 1)
             constexpr uint32_t id_ro = idesc_bf16(128, D + 16, 0, 0);
             constexpr uint32_t id_ms = idesc_bf16(128, 16, 1, 0);
             const uint32_t id_up = idesc_bf16(128, lrp, 1, 1);
-            const uint64_t d_fk_k = desc_k(base + Ly.fk), d_fk_mn = desc_mn(base + Ly.fk, BLK);
             const uint64_t d_ones = desc_k(base + Ly.ones);
             const uint64_t d_shi = desc_k(base + Ly.shi), d_slo = desc_k(base + Ly.slo);
-            bool ok = true;
-            for (int c = 0; c < nchunk && ok; ++c) {
-                const uint32_t vst = base + Ly.v + (c & 1) * Ly.kbb;
-                // projections
-                if (!(ok = wait_phase(bar(B_QK), c & 1, abort))) break;
-                ++qk_done;
+            auto project = [&](int c) {
                 fence_after();
                 issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
                 issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
                 commit(bar(B_PROJ));
+            };
+            bool ok = true, projected = false;  // projected: this chunk's projection went out early
+            for (int c = 0; c < nchunk && ok; ++c) {
+                const uint32_t vst = base + Ly.v + (c & 1) * Ly.kbb;
+                const uint32_t fq = T_FQ + (pipe ? 16u * (c & 1) : 0u);
+                const uint32_t fk = base + Ly.fk + (pipe ? (uint32_t)(c & 1) * BLK : 0u);
+                const uint64_t d_fk_k = desc_k(fk);
+                const uint64_t d_fk_mn = desc_mn(fk, BLK);       // B operand: one 64-column block
+                const uint64_t d_fk_mt = desc_mn(fk, base + Ly.shi - fk);  // A, M = 128: rows 64+ unread
+                if (!projected) {
+                    if (!(ok = wait_phase(bar(B_QK), c & 1, abort))) break;
+                    ++qk_done;
+                    project(c);
+                }
+                projected = false;
                 // scores once the features are in; then the Q / K tiles (read by the projection and
                 // the norms) take the next chunk
                 if (!(ok = wait_phase(bar(B_FEAT), c & 1, abort))) break;
                 fence_after();
                 for (int ks = 0; ks < lrp / 16; ++ks)
-                    umma_ts(tmem + T_SC, tmem + T_FQ + 8 * ks, d_fk_k + (uint64_t)(ks * 2), id_s, ks > 0);
+                    umma_ts(tmem + T_SC, tmem + fq + 8 * ks, d_fk_k + (uint64_t)(ks * 2), id_s, ks > 0);
                 commit(bar(B_SC));
                 if (c + 1 < nchunk) {
                     load_qk(c + 1);
@@ -277,6 +289,13 @@ __global__ void __launch_bounds__(NTHW, 1)
                 if (!(ok = wait_phase(bar(B_MASK), c & 1, abort))) break;
                 if (!(ok = wait_phase(bar(B_V0 + (c & 1)), (c >> 1) & 1, abort))) break;
                 ++v_done[c & 1];
+                // the next chunk's projection ahead of this chunk's products when its tiles are in,
+                // so its features are computed while these run
+                if (pipe && c + 1 < nchunk && mbar_test(bar(B_QK), (c + 1) & 1)) {
+                    ++qk_done;
+                    project(c + 1);
+                    projected = true;
+                }
                 fence_after();
                 const uint64_t d_v = desc_mn(vst, BLK);
                 const uint64_t d_vt = desc_mn(vst, D == 128 ? BLK : (Ly.zero - (Ly.v + (c & 1) * Ly.kbb)));
@@ -287,14 +306,14 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma_ts(tmem + T_O + D, tmem + T_P + 8 * ks, d_ones + kk, id_p1, ks > 0);
                 }
                 for (int ks = 0; ks < lrp / 16; ++ks) {
-                    umma_ts(tmem + T_O, tmem + T_FQ + 8 * ks, d_shi + (uint64_t)(ks * 2), id_ro, true);
-                    umma_ts(tmem + T_O, tmem + T_FQ + 8 * ks, d_slo + (uint64_t)(ks * 2), id_ro, true);
+                    umma_ts(tmem + T_O, tmem + fq + 8 * ks, d_shi + (uint64_t)(ks * 2), id_ro, true);
+                    umma_ts(tmem + T_O, tmem + fq + 8 * ks, d_slo + (uint64_t)(ks * 2), id_ro, true);
                 }
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks) {
                     const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
                     umma(tmem + T_ST, d_vt + ko, d_fk_mn + ko, id_up, true);
-                    umma(tmem + T_MS, d_fk_mn + ko, d_ones + kk, id_ms, true);
+                    umma(tmem + T_MS, d_fk_mt + ko, d_ones + kk, id_ms, true);
                 }
                 commit(bar(B_MMA));
                 // V stage (c + 1) & 1 held chunk c - 1, whose output store must have read it
@@ -350,9 +369,21 @@ __global__ void __launch_bounds__(NTHW, 1)
             }
         };
 
+        // output of the previous chunk, and the sketch operand for this chunk's read-out
+        auto previous = [&](int c) {
+            if (!wait_phase(bar(B_MMA), (c - 1) & 1, abort)) return false;
+            fence_after();
+            epilogue(c - 1);
+            sketch_to_operand<D>(tlane, q4, lane, h, LR, lrp, base + Ly.shi, base + Ly.slo);
+            warp_signal(bar(B_SOP));
+            return true;
+        };
+
         for (int c = 0; c < nchunk; ++c) {
             const int64_t n0 = n_begin + (int64_t)c * C;
             const int cnt = (int)min((int64_t)C, n_end - n0);
+            const uint32_t fq = T_FQ + (pipe ? 16u * (c & 1) : 0u);
+            const uint32_t fk = base + Ly.fk + (pipe ? (uint32_t)(c & 1) * BLK : 0u);
             // row norm of this thread's row: warps 0-3 Q rows, warps 4-7 K rows
             if (!wait_phase(bar(B_QK), c & 1, abort)) break;
             float inv;
@@ -361,14 +392,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 const float ss = half_sumsq<D>(tile, t, 0) + half_sumsq<D>(tile, t, 1);
                 inv = ss > 0.f ? rsqrtf(ss) : 0.f;
             }
-            // output of the previous chunk, and the sketch operand for this chunk's read-out
-            if (c >= 1) {
-                if (!wait_phase(bar(B_MMA), (c - 1) & 1, abort)) break;
-                fence_after();
-                epilogue(c - 1);
-                sketch_to_operand<D>(tlane, q4, lane, h, LR, lrp, base + Ly.shi, base + Ly.slo);
-                warp_signal(bar(B_SOP));
-            }
+            if (!pipe && c >= 1 && !previous(c)) break;
             // features: warps 0-3 the Q row t (-> TMEM), warps 4-7 the K row t (-> shared F_K tile)
             if (!wait_phase(bar(B_PROJ), c & 1, abort)) break;
             fence_after();
@@ -396,20 +420,20 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                                     for (int j = 0; j < 8; ++j)
                                         r[j] = mma::pack_bf16(ph[16 * b + 2 * j], ph[16 * b + 2 * j + 1]);
-                                    stn<8>(tlane + T_FQ + (l * R) / 2 + 8 * b, r);
+                                    stn<8>(tlane + fq + (l * R) / 2 + 8 * b, r);
                                 }
                             } else {
                                 uint32_t r[R / 2];
 #pragma unroll
                                 for (int j = 0; j < R / 2; ++j) r[j] = mma::pack_bf16(ph[2 * j], ph[2 * j + 1]);
-                                stn<R / 2>(tlane + T_FQ + (l * R) / 2, r);
+                                stn<R / 2>(tlane + fq + (l * R) / 2, r);
                             }
                         } else {
                             if constexpr (R >= 8) {
 #pragma unroll
                                 for (int j = 0; j < R / 8; ++j) {
                                     const int ch = l * (R / 8) + j;
-                                    st_shared_v4(base + Ly.fk + sw_chunk(t, ch),
+                                    st_shared_v4(fk + sw_chunk(t, ch),
                                                  mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
                                                  mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
                                                  mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
@@ -420,7 +444,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                                 for (int r = 0; r < R; r += 2) {
                                     const int lr = l * R + r;
                                     const uint32_t w = mma::pack_bf16(ph[r] * scale, ph[r + 1] * scale);
-                                    asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fk + sw_elem(t, lr)), "r"(w)
+                                    asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(fk + sw_elem(t, lr)), "r"(w)
                                                  : "memory");
                                 }
                             }
@@ -430,6 +454,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             }
             wait_st();
             warp_signal(bar(B_FEAT));
+            if (pipe && c >= 1 && !previous(c)) break;
             // causal mask j <= t on this half's 64 key columns -> bf16 P in TMEM
             if (!wait_phase(bar(B_SC), c & 1, abort)) break;
             fence_after();

@@ -104,6 +104,18 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     return false;
 }
 
+// Non-blocking check of the phase with parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Hands the warp's finished work to the issuing thread: every lane orders its shared-memory
 // writes before later async-proxy reads and its TMEM stores before the hand-off; lane 0 then
 // arrives once on `bar` (whose count is the number of handing-off warps).
