@@ -71,13 +71,23 @@ __device__ __forceinline__ void init_mass_tile(unsigned char *p, bool ones)
 template <int D>
 __device__ __forceinline__ float half_sumsq(uint32_t tile, int t, int h)
 {
-    float s = 0.f;
+    uint4 w[D / 16];  // all loads first, then four independent accumulation chains
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) {
         const int c = h * (D / 16) + j;
-        s += sumsq8(ld_shared_v4(tile + (c >> 3) * BLK + sw_chunk(t, c & 7)));
+        w[j] = ld_shared_v4(tile + (c >> 3) * BLK + sw_chunk(t, c & 7));
     }
-    return s;
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+        const uint32_t q[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = __uint_as_float(q[i] << 16), hi = __uint_as_float(q[i] & 0xFFFF0000u);
+            s[i] = fmaf(lo, lo, fmaf(hi, hi, s[i]));
+        }
+    }
+    return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)

@@ -87,17 +87,26 @@ __device__ __forceinline__ void issue_rows(bf16 *d0, bf16 *d1, bf16 *d2, bf16 *d
 
 // ------------------------------------------------------------------ nonlinearities
 
+// Reciprocal from the hardware approximation (about 1 ulp; denormal results flush to zero, which
+// only the saturated ends of tanh and sigmoid reach, where the exact value rounds to 0 as well).
+__device__ __forceinline__ float rcp_fast(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // tanh with about 1e-7 absolute error (all that the bucket probabilities are sensitive to).
 __device__ __forceinline__ float tanh_abs(float x)
 {
-    return 1.f - 2.f * __frcp_rn(1.f + __expf(2.f * x));
+    return 1.f - 2.f * rcp_fast(1.f + __expf(2.f * x));
 }
 
 // sigmoid(a) and sigmoid(-a) without overflow for any finite a.
 __device__ __forceinline__ void sigmoid_pair(float a, float &sp, float &sm)
 {
     const float e = __expf(-fabsf(a));
-    const float big = __frcp_rn(1.f + e), small = e * big;
+    const float big = rcp_fast(1.f + e), small = e * big;
     sp = a >= 0.f ? big : small;
     sm = a >= 0.f ? small : big;
 }
