@@ -47,7 +47,7 @@ constexpr uint32_t T_COLS = 512;
 enum : uint32_t { B_Q, B_K, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_COUNT };
 
 struct BwdLayout {
-    uint32_t q, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, bar, slot, bytes, kbb;
+    uint32_t q, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, zk, bar, slot, bytes, kbb;
     __host__ __device__ BwdLayout(int D)
     {
         kbb = (uint32_t)(D / 64) * BLK;
@@ -63,7 +63,8 @@ struct BwdLayout {
         ncm = wlo + (uint32_t)(D / 64) * WBLK;  // -c as a K-major N = 16 operand (rows 0, 1 = hi, lo)
         gb = ncm + 4096;                         // G_B fp32 [32]
         cvec = gb + 128;                         // c_t fp32 [C]
-        bar = cvec + 4 * C;
+        zk = cvec + 4 * C;   // z = W x of the K rows, fp32 [LPP][C]
+        bar = zk + 4 * LPP * C;
         slot = bar + 128;
         bytes = slot + 16;
     }
@@ -90,6 +91,8 @@ __global__ void __launch_bounds__(NTHW, 1)
     volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
     float *gb = reinterpret_cast<float *>(sm + Ly.gb);
     float *cvec = reinterpret_cast<float *>(sm + Ly.cvec);
+    float *zk_s = reinterpret_cast<float *>(sm + Ly.zk);
+    const bool wide = ((reinterpret_cast<uintptr_t>(dK) | reinterpret_cast<uintptr_t>(dV)) & 31) == 0;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = (warp >> 2) & 1;
     const bool compute = warp < 8;
@@ -337,12 +340,21 @@ __global__ void __launch_bounds__(NTHW, 1)
             convert_g();
             warp_signal(bar(B_GOP));
         }
+        // {1 / den, c} of the Q rows, loaded a chunk ahead; chunks run backwards and only the
+        // last one can be partial
+        float2 a2n = make_float2(0.f, 0.f);
+        if (h == 0 && nchunk > 0) {
+            const int64_t nl = n_begin + (int64_t)(nchunk - 1) * C;
+            if (nl + t < n_end) a2n = aux[bh * Dm.N + nl + t];
+        }
         for (int k = 0; k < nchunk; ++k) {
             const uint32_t par = k & 1;
             const int c = nchunk - 1 - k;
             const int64_t n0 = n_begin + (int64_t)c * C;
             const int cnt = (int)min((int64_t)C, n_end - n0);
             const bool live = t < cnt;
+            const float2 a2 = a2n;
+            if (h == 0 && c >= 1) a2n = aux[bh * Dm.N + n0 - C + t];
             if (!wait_phase(bar(h ? B_K : B_Q), par, abort)) break;
             // the row this thread featurises: Q row t (warps 0-3) or K row t (warps 4-7)
             float inv;
@@ -351,8 +363,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                 const float ss = half_sumsq<D>(tile, t, 0) + half_sumsq<D>(tile, t, 1);
                 inv = ss > 0.f ? rsqrtf(ss) : 0.f;
             }
-            float2 a2 = make_float2(0.f, 0.f);
-            if (h == 0 && live) a2 = aux[bh * Dm.N + n0 + t];
             if (!wait_phase(bar(B_PROJ), par, abort)) break;
             fence_after();
             float z[LPP];
@@ -362,7 +372,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                 for (int j = 0; j < LPP; ++j) z[j] = a[j];
             }
-            float uk[LPP];  // K rows keep u for the Jacobian
+            float uk[LPP];  // K rows keep u for the Jacobian (and z in shared memory)
             if (h == 0) {
                 // F'_Q = phi(Q_t) / den_t -> shared tile row t;  -c_t -> rows 0 / 1 of the mass operand
                 const float sc = a2.x;
@@ -401,6 +411,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                 cvec[t] = a2.y;
             } else {
                 // F_K -> TMEM (A operand); keep u
+#pragma unroll
+                for (int j = 0; j < LMAX * P; ++j) zk_s[j * C + t] = z[j];
                 float phk[LRMAX];
 #pragma unroll
                 for (int j = 0; j < LRMAX; ++j) phk[j] = 0.f;
@@ -465,6 +477,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             warp_signal(bar(B_MASK));
             if (!wait_phase(bar(B_B), par, abort)) break;
             fence_after();
+            float zdz = 0.f;  // x . dxhat of the K row
             if (h == 1) {
                 // park the K row in TMEM (the score columns are free once group B is done) so that
                 // the K tile can take the next chunk
@@ -508,6 +521,9 @@ __global__ void __launch_bounds__(NTHW, 1)
                     for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(dz[16 * b + 2 * j], dz[16 * b + 2 * j + 1]);
                     stn<8>(tlane + T_DZ + 8 * b, r);
                 }
+                // dxhat = W^T dz (dz rounded to bf16 as the product sees it), so x . dxhat = z . dz
+#pragma unroll
+                for (int j = 0; j < LMAX * P; ++j) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[j])), zk_s[j * C + t], zdz);
                 wait_st();
                 warp_signal(bar(B_JAC));
             } else {
@@ -519,15 +535,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                     ld32_nw(tlane + T_DVV + 32 * pass, v);
                     wait_ld();
                     reg_fence(v);
-                    if (live) {
+                    uint32_t o[16];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4 *>(dst + 32 * pass + 8 * q) =
-                                make_uint4(mma::pack_bf16(uf(v[8 * q]), uf(v[8 * q + 1])),
-                                           mma::pack_bf16(uf(v[8 * q + 2]), uf(v[8 * q + 3])),
-                                           mma::pack_bf16(uf(v[8 * q + 4]), uf(v[8 * q + 5])),
-                                           mma::pack_bf16(uf(v[8 * q + 6]), uf(v[8 * q + 7])));
-                    }
+                    for (int j = 0; j < 16; ++j) o[j] = mma::pack_bf16(uf(v[2 * j]), uf(v[2 * j + 1]));
+                    if (live) store_row32(dst + 32 * pass, o, wide);
                 }
                 fence_before();
                 __syncwarp();
@@ -537,20 +548,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             fence_after();
             if (h == 1) {
                 // dK row t = inv (dxhat - x inv^2 (x . dxhat)), x parked in TMEM; straight to global memory
-                float dot = 0.f;
-#pragma unroll
-                for (int pass = 0; pass < D / 32; ++pass) {
-                    uint32_t v[32], xr[16];
-                    ld32_nw(tlane + T_DV + 32 * pass, v);
-                    ld16_nw(tlane + T_SC + 16 * pass, xr);
-                    wait_ld();
-                    reg_fence(v);
-                    reg_fence(xr);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        dot = fmaf(bf_lo(xr[j]), uf(v[2 * j]), fmaf(bf_hi(xr[j]), uf(v[2 * j + 1]), dot));
-                }
-                const float kk = inv * inv * dot;
+                const float kk = inv * inv * zdz;
                 bf16 *dst = dK + off + (n0 + t) * D;
 #pragma unroll
                 for (int pass = 0; pass < D / 32; ++pass) {
@@ -564,12 +562,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         o[j] = mma::pack_bf16(inv * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), inv * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
-                    if (live) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4 *>(dst + 32 * pass + 8 * q) =
-                                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-                    }
+                    if (live) store_row32(dst + 32 * pass, o, wide);
                 }
             } else {
                 convert_g();
@@ -621,7 +614,7 @@ constexpr uint32_t T_GB = 416;    // G_B (lanes = sketch row), columns 0 + 1 (c 
 constexpr uint32_t T_X = 432;     // the Q row as stored (bf16 pairs), 64 columns
 constexpr uint32_t T_COLS = 512;
 
-enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_CS2, B_COUNT };
+enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_COUNT };
 
 struct QLayout {
     uint32_t q, k, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, bprev, invq, red, bar, slot, bytes, kbb;
@@ -642,8 +635,8 @@ struct QLayout {
         ones = ncm + 4096;
         bprev = ones + 4096;  // B_prev fp32 [2 parities][32]
         invq = bprev + 256;   // 1 / |Q row| fp32 [C]
-        red = invq + 4 * C;   // dQ dot halves fp32 [2][C]
-        bar = red + 8 * C;
+        red = invq + 4 * C;   // inv^2 (x . dxhat) of the Q rows, fp32 [C]
+        bar = red + 4 * C;
         slot = bar + 128;
         bytes = slot + 16;
     }
@@ -671,6 +664,7 @@ __global__ void __launch_bounds__(NTHW, 1)
     float *bprev = reinterpret_cast<float *>(sm + Ly.bprev);
     float *invq_s = reinterpret_cast<float *>(sm + Ly.invq);
     float *red = reinterpret_cast<float *>(sm + Ly.red);
+    const bool wide = (reinterpret_cast<uintptr_t>(dQ) & 31) == 0;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, h = (warp >> 2) & 1;
     const bool compute = warp < 8;
@@ -698,7 +692,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             uint32_t cnt = 1;
             if (i == B_FEAT || i == B_MASK) cnt = 8;
             if (i == B_JAC || i == B_SOP) cnt = 4;
-            if (i == B_CS || i == B_CS2) cnt = NTH;
+            if (i == B_CS) cnt = NTH;
             mbar_init(bar(i), cnt);
         }
         *abort = 0;
@@ -1077,6 +1071,15 @@ __global__ void __launch_bounds__(NTHW, 1)
                     for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(dz[16 * b + 2 * j], dz[16 * b + 2 * j + 1]);
                     stn<8>(tlane + T_DZ + 8 * b, r);
                 }
+                {
+                    // dxhat = W^T dz (dz rounded to bf16 as the product sees it), so x . dxhat = z . dz
+                    // with z = W x, still in TMEM
+                    float zq[32], zdz = 0.f;
+                    ld32(tlane + T_ZQ, zq);
+#pragma unroll
+                    for (int j = 0; j < LPP; ++j) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[j])), zq[j], zdz);
+                    red[t] = invq_s[t] * invq_s[t] * zdz;
+                }
                 const float mcv = -cc;
                 const bf16 mhi = __float2bfloat16_rn(mcv);
                 const bf16 mlo = __float2bfloat16_rn(mcv - __bfloat162float(mhi));
@@ -1093,24 +1096,11 @@ __global__ void __launch_bounds__(NTHW, 1)
             if (!(ok = wait_phase(bar(B_C), par, abort))) break;
             fence_after();
             {
-                // dQ row t = inv (dxhat - x inv^2 (x . dxhat)); half h takes columns h D/2 .. (h+1) D/2
+                // dQ row t = inv (dxhat - x inv^2 (x . dxhat)); half h takes columns h D/2 .. (h+1) D/2.
+                // inv^2 (x . dxhat) comes from the Q row's thread, published before its JAC arrival
+                if (h == 1 && !(ok = wait_phase(bar(B_JAC), par, abort))) break;
                 const float iq = invq_s[t];
-                float dot = 0.f;
-#pragma unroll
-                for (int pass = 0; pass < D / 64; ++pass) {
-                    uint32_t v[32], xr[16];
-                    ld32_nw(tlane + T_DV + h * (D / 2) + 32 * pass, v);
-                    ld16_nw(tlane + T_X + h * (D / 4) + 16 * pass, xr);
-                    wait_ld();
-                    reg_fence(v);
-                    reg_fence(xr);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        dot = fmaf(bf_lo(xr[j]), uf(v[2 * j]), fmaf(bf_hi(xr[j]), uf(v[2 * j + 1]), dot));
-                }
-                red[h * C + t] = dot;
-                if (!(ok = group_sync(bar(B_CS2), par, abort))) break;
-                const float kk = iq * iq * (red[t] + red[C + t]);
+                const float kk = red[t];
                 bf16 *dst = dQ + off + (n0 + t) * D + h * (D / 2);
 #pragma unroll
                 for (int pass = 0; pass < D / 64; ++pass) {
@@ -1124,12 +1114,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         o[j] = mma::pack_bf16(iq * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), iq * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
-                    if (live) {
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq)
-                            *reinterpret_cast<uint4 *>(dst + 32 * pass + 8 * qq) =
-                                make_uint4(o[4 * qq], o[4 * qq + 1], o[4 * qq + 2], o[4 * qq + 3]);
-                    }
+                    if (live) store_row32(dst + 32 * pass, o, wide);
                 }
             }
             fence_before();
