@@ -174,6 +174,21 @@ def _sampled_rows(N, n, seed):
     return np.array(sorted(rows), dtype=np.int64)
 
 
+@pytest.mark.parametrize("w", [
+    # one (b, h) split into 304 segments of 3 token tiles each, the last one ragged
+    W_("mc_bf_d128_c", 1, 1, 3 * 304 * 128 - 51, 128, 3, 3, True, "bf16"),
+    W_("mc_bf_d64_c", 1, 2, 3 * 152 * 128 + 300, 64, 2, 5, True, "bf16"),
+    W_("mc_bf_d128_p5_c", 2, 1, 4 * 152 * 128 + 1, 128, 5, 1, True, "bf16"),
+    W_("mc_bf_d128", 1, 1, 6 * 304 * 128 - 51, 128, 3, 3, False, "bf16"),
+], ids=lambda w: w.name)
+def test_multichunk_segments(w):
+    """Several token tiles per segment: every barrier phase of the per-chunk pipelines turns over
+    more than once (small shapes give each segment a single tile)."""
+    inp = inputs_on_gpu(w, seed=9)
+    rows = _sampled_rows(w.N, 64, 9)
+    assert_close(w, gpu_run(w, inp, rows=rows), oracle_run(w, inp, rows=rows), w.name)
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["c4_bf16_1m_lr256", "c5_bf16_causal_12m"])
 def test_config_full_size_sampled(name):
