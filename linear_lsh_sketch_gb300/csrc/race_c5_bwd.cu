@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(NTHW, 1)
     const int64_t n_begin = (int64_t)s * seg_len;
     const int64_t n_end = min(Dm.N, n_begin + seg_len);
     const int nchunk = n_end > n_begin ? (int)((n_end - n_begin + C - 1) / C) : 0;
-    const int LR = Dm.LR, lrp = (LR + 15) & ~15;
+    const int LR = Dm.LR;
     const float beta = Dm.beta;
     const int L = Dm.L;
     const int64_t off = bh * Dm.N * D;

@@ -115,6 +115,24 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 }
 
 // Non-blocking check of the phase with parity `parity`.
+// wait_phase for a converged warp: every lane polls and all lanes return the same result, so the
+// warp stays converged for the elect.sync issue that follows.
+__device__ __forceinline__ bool wait_phase_w(uint32_t bar, uint32_t parity, volatile int *abort)
+{
+    for (int i = 0; i < (1 << 22); ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (__all_sync(0xffffffffu, ok != 0)) return true;
+        if ((i & 15) == 15 && __any_sync(0xffffffffu, *abort != 0)) return false;
+    }
+    *abort = 1;
+    return false;
+}
+
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -289,6 +307,22 @@ __device__ __forceinline__ void issue_projection(uint32_t tz, uint32_t xtile, ui
     for (int ks = 0; ks < D / 16; ++ks) {
         const uint32_t ko = (ks >> 2) * BLK + (ks & 3) * 32, kw = (ks >> 2) * WBLK + (ks & 3) * 32;
         umma(tz, desc_k(xtile + ko), desc_k(wlo + kw), idesc_proj(), true);
+    }
+}
+
+// The same, issued by a converged warp (one elected lane).
+template <int D>
+__device__ __forceinline__ void issue_projection_w(uint32_t tz, uint32_t xtile, uint32_t whi, uint32_t wlo)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t ko = (ks >> 2) * BLK + (ks & 3) * 32, kw = (ks >> 2) * WBLK + (ks & 3) * 32;
+        umma_w(tz, desc_k(xtile + ko), desc_k(whi + kw), idesc_proj(), ks > 0);
+    }
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t ko = (ks >> 2) * BLK + (ks & 3) * 32, kw = (ks >> 2) * WBLK + (ks & 3) * 32;
+        umma_w(tz, desc_k(xtile + ko), desc_k(wlo + kw), idesc_proj(), true);
     }
 }
 

@@ -117,15 +117,15 @@ __global__ void __launch_bounds__(NTHW, 1)
 
     if (!compute) {
         // ---------------------------------------------------------------- control warp
-        if (lane == 0) {
+        {  // the whole control warp, converged: one elected lane issues each copy and product
             auto load = [&](int i, bool is_y) {
                 const int s = i & 1;
                 const uint32_t b = bar((is_y ? SB_Y0 : SB_X0) + s);
                 const uint32_t dst = base + (is_y ? Ly.y : Ly.x) + s * Ly.stg;
-                mbar_arrive_expect_tx(b, KB * BLK);
+                expect_tx_w(b, KB * BLK);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb)
-                    tma_load(dst + kb * BLK, is_y ? &tmY : &tmX, 64 * kb, (int)(n_begin + (int64_t)i * C), (int)bh, b);
+                    tma_load_w(dst + kb * BLK, is_y ? &tmY : &tmX, 64 * kb, (int)(n_begin + (int64_t)i * C), (int)bh, b);
             };
             int issued[4] = {0, 0, 0, 0}, done[4] = {0, 0, 0, 0};  // X0, X1, Y0, Y1
             for (int i = 0; i < 2 && i < ntile; ++i) {
@@ -138,19 +138,19 @@ __global__ void __launch_bounds__(NTHW, 1)
             constexpr uint32_t id_m = idesc_bf16(128, 16, 1, 0);
             auto proj = [&](int i) {
                 const int s = i & 1;
-                if (!wait_phase(bar(SB_X0 + s), (i >> 1) & 1, abort)) return false;
+                if (!wait_phase_w(bar(SB_X0 + s), (i >> 1) & 1, abort)) return false;
                 ++done[s];
                 fence_after();
-                issue_projection<D>(tmem + zcol + LPP * s, base + Ly.x + s * Ly.stg, base + Ly.whi, base + Ly.wlo);
-                commit(bar(SB_P0 + s));
+                issue_projection_w<D>(tmem + zcol + LPP * s, base + Ly.x + s * Ly.stg, base + Ly.whi, base + Ly.wlo);
+                commit_w(bar(SB_P0 + s));
                 return true;
             };
             bool ok = ntile == 0 || proj(0);
             for (int i = 0; i < ntile && ok; ++i) {
                 const int s = i & 1;
                 if (i + 1 < ntile && !(ok = proj(i + 1))) break;
-                if (!(ok = wait_phase(bar(SB_F0 + s), (i >> 1) & 1, abort))) break;
-                if (!(ok = wait_phase(bar(SB_Y0 + s), (i >> 1) & 1, abort))) break;
+                if (!(ok = wait_phase_w(bar(SB_F0 + s), (i >> 1) & 1, abort))) break;
+                if (!(ok = wait_phase_w(bar(SB_Y0 + s), (i >> 1) & 1, abort))) break;
                 ++done[2 + s];
                 fence_after();
                 const uint32_t fbuf = base + Ly.f + (i % nf) * Ly.fbytes;
@@ -162,11 +162,11 @@ __global__ void __launch_bounds__(NTHW, 1)
                     for (int ks = 0; ks < C / 16; ++ks) {
                         const uint64_t a = desc_mn(fbuf + 2 * m * BLK + ks * 2048, BLK);
                         const bool accum = i > 0 || ks > 0;
-                        umma(acc, a, desc_mn(ys + ks * 2048, BLK), id_v, accum);
-                        umma(acc + D, a, desc_k(mbuf + (ks >> 2) * 2048 + (ks & 3) * 32), id_m, accum);
+                        umma_w(acc, a, desc_mn(ys + ks * 2048, BLK), id_v, accum);
+                        umma_w(acc + D, a, desc_k(mbuf + (ks >> 2) * 2048 + (ks & 3) * 32), id_m, accum);
                     }
                 }
-                commit(bar(SB_S0 + s));
+                commit_w(bar(SB_S0 + s));
                 // X stage s: read by the projection and the norms of tile i (both done: features are in)
                 if (i + 2 < ntile) {
                     load(i + 2, false);
@@ -174,14 +174,14 @@ __global__ void __launch_bounds__(NTHW, 1)
                 }
                 // Y stage s ^ 1: read by the sketch product of tile i - 1
                 if (i >= 1 && i + 1 < ntile) {
-                    if (!(ok = wait_phase(bar(SB_S0 + (s ^ 1)), ((i - 1) >> 1) & 1, abort))) break;
+                    if (!(ok = wait_phase_w(bar(SB_S0 + (s ^ 1)), ((i - 1) >> 1) & 1, abort))) break;
                     load(i + 1, true);
                     ++issued[2 + (s ^ 1)];
                 }
             }
-            if (ok) commit(bar(SB_DONE));
+            if (ok) commit_w(bar(SB_DONE));
             if (!ok) {
-                atomicOr(err, kErrTimeout);
+                if (lane == 0) atomicOr(err, kErrTimeout);
                 *abort = 1;
                 for (int b = 0; b < 4; ++b)
                     if (issued[b] > done[b]) mbar_wait(bar(SB_X0 + b), done[b] & 1);
