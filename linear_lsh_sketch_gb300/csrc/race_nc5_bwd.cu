@@ -529,20 +529,20 @@ __global__ void __launch_bounds__(NTH, 1)
         wait_st();
         fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (warp == 0) {  // the run-time K loop issues from the converged warp (one elected lane)
             fence_after();
             constexpr uint32_t id_x = idesc_bf16(128, D, 0, 1);
             for (int ks = 0; ks < lrp / 16; ++ks) {
-                umma_ts(tmem, tmem + fkc + 8 * ks, desc_mn(base + Ly.shi + ks * 2048, Ly.sblk), id_x, ks > 0);
+                umma_ts_w(tmem, tmem + fkc + 8 * ks, desc_mn(base + Ly.shi + ks * 2048, Ly.sblk), id_x, ks > 0);
                 if (Ly.split)
-                    umma_ts(tmem, tmem + fkc + 8 * ks, desc_mn(base + Ly.slo + ks * 2048, Ly.sblk), id_x, true);
+                    umma_ts_w(tmem, tmem + fkc + 8 * ks, desc_mn(base + Ly.slo + ks * 2048, Ly.sblk), id_x, true);
             }
 #pragma unroll
             for (int ks = 0; ks < LPP / 16; ++ks) {
-                umma_ts(tmem + D, tmem + dzc + 8 * ks, desc_mn(base + Ly.whi + ks * 2048, WBLK), id_x, ks > 0);
-                umma_ts(tmem + D, tmem + dzc + 8 * ks, desc_mn(base + Ly.wlo + ks * 2048, WBLK), id_x, true);
+                umma_ts_w(tmem + D, tmem + dzc + 8 * ks, desc_mn(base + Ly.whi + ks * 2048, WBLK), id_x, ks > 0);
+                umma_ts_w(tmem + D, tmem + dzc + 8 * ks, desc_mn(base + Ly.wlo + ks * 2048, WBLK), id_x, true);
             }
-            commit(bar_b);
+            commit_w(bar_b);
         }
         if (wait_all(bar_b, i & 1)) {
             failed = true;

@@ -427,20 +427,21 @@ __global__ void __launch_bounds__(NTH, 1)
         tc::fence_proxy_async();
         fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (warp == 0) {  // the run-time K loop issues from the converged warp (one elected lane)
             fence_after();
             constexpr uint32_t id_o = idesc_bf16(128, NS, 0, 0);
             for (int ks = 0; ks < ksteps; ++ks) {
                 const uint32_t fo = (ks >> 2) * BLK + (ks & 3) * 32, so = (ks >> 2) * Ly.sblk + (ks & 3) * 32;
-                umma(tmem, desc_k(base + Ly.f + fo), desc_k(base + Ly.shi + so), id_o, ks > 0);
-                if (Ly.split) umma(tmem, desc_k(base + Ly.f + fo), desc_k(base + Ly.slo + so), id_o, true);
+                umma_w(tmem, desc_k(base + Ly.f + fo), desc_k(base + Ly.shi + so), id_o, ks > 0);
+                if (Ly.split) umma_w(tmem, desc_k(base + Ly.f + fo), desc_k(base + Ly.slo + so), id_o, true);
             }
-            commit(bar_o);
+            commit_w(bar_o);
             // the other stage was last read by tile i - 1's output store: let that finish, then refill
-            if (i >= 1 && i + 1 < ntile) {
+            if (lane == 0 && i >= 1 && i + 1 < ntile) {
                 bulk_wait_read0();
                 issue_load(i + 1);
             }
+            __syncwarp();
         }
         if (wait_all(bar_o, i & 1)) {
             failed = true;
