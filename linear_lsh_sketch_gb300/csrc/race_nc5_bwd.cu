@@ -273,7 +273,9 @@ __global__ void __launch_bounds__(NTH, 1)
         const float cc = (red[4 * C + t] + red[5 * C + t]) * rd;
         if (h == 0 && live) aux[bh * Dm.N + n0 + t] = make_float2(rd, cc);
 
-        // phase B: dphi = (g - B c) / den, then the feature Jacobian -> dz (bf16 pairs in TMEM)
+        // phase B: dphi = (g - B c) / den, then the feature Jacobian -> dz (bf16 pairs in TMEM);
+        // x . dxhat = z . dz (dxhat = W^T dz with dz as the product sees it, z = W x), this half's share
+        float zdz = 0.f;
 #pragma unroll
         for (int pr = 0; pr < NPAIR; ++pr) {
             if ((pr & 1) != h || 2 * pr >= L) continue;
@@ -294,9 +296,13 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
                 for (int r = 0; r < R; ++r) g[r] = (g[r] - mass[l * R + r] * cc) * rd;
                 table_backward<P>(u, ph, g, beta, dz + k * P);
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                    zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[k * P + p])), z[l * P + p], zdz);
             }
             st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
         }
+        red[(6 + h) * C + t] = zdz;
         wait_st();
         fence_before();
         __syncthreads();
@@ -319,7 +325,6 @@ __global__ void __launch_bounds__(NTH, 1)
         // epilogue: dQ = inv (dxhat - x inv^2 (x . dxhat)), this half's columns
         float dx[D / 2];
         uint4 xw[D / 16];
-        float dot = 0.f;
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
             const int c = h * (D / 16) + j;
@@ -332,17 +337,6 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
             for (int k = 0; k < 16; ++k) dx[16 * cc16 + k] = v[k];
         }
-#pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-            const uint32_t w4[4] = {xw[j].x, xw[j].y, xw[j].z, xw[j].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                dot = fmaf(bf_lo(w4[k]), dx[8 * j + 2 * k], dot);
-                dot = fmaf(bf_hi(w4[k]), dx[8 * j + 2 * k + 1], dot);
-            }
-        }
-        red[(6 + h) * C + t] = dot;
-        __syncthreads();
         const float kk = inv * inv * (red[6 * C + t] + red[7 * C + t]);
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
@@ -501,7 +495,9 @@ __global__ void __launch_bounds__(NTH, 1)
         const float ssq = red[t] + red[C + t];
         const float inv = ssq > 0.f ? rsqrtf(ssq) : 0.f;
 
-        // features -> TMEM (A operand of dV); dphi = V G_A^T + G_B -> feature Jacobian -> dz
+        // features -> TMEM (A operand of dV); dphi = V G_A^T + G_B -> feature Jacobian -> dz;
+        // x . dxhat = z . dz (dxhat = W^T dz with dz as the product sees it, z = W x), this half's share
+        float zdz = 0.f;
 #pragma unroll
         for (int pr = 0; pr < NPAIR; ++pr) {
             if ((pr & 1) != h || 2 * pr >= L) continue;
@@ -523,9 +519,13 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
                 for (int r = 0; r < R; ++r) dph[r] += gmass[l * R + r];
                 table_backward<P>(u, ph, dph, beta, dz + k * P);
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                    zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[k * P + p])), z[l * P + p], zdz);
             }
             st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
         }
+        red[(6 + h) * C + t] = zdz;
         wait_st();
         fence_before();
         __syncthreads();
@@ -553,7 +553,6 @@ __global__ void __launch_bounds__(NTH, 1)
         // epilogue: dK (normalisation backward) staged in the V tile, dV staged in the K tile
         float dx[D / 2];
         uint4 xw[D / 16];
-        float dot = 0.f;
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
             const int c = h * (D / 16) + j;
@@ -566,17 +565,7 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
             for (int k = 0; k < 16; ++k) dx[16 * cc16 + k] = v[k];
         }
-#pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-            const uint32_t w4[4] = {xw[j].x, xw[j].y, xw[j].z, xw[j].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                dot = fmaf(bf_lo(w4[k]), dx[8 * j + 2 * k], dot);
-                dot = fmaf(bf_hi(w4[k]), dx[8 * j + 2 * k + 1], dot);
-            }
-        }
-        red[(6 + h) * C + t] = dot;
-        __syncthreads();  // also: every thread holds its K row half in registers from here on
+        // each thread overwrites only the K-row half it has just read (its dV half)
         const float kk = inv * inv * (red[6 * C + t] + red[7 * C + t]);
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
