@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                 for (int j = 0; j < LPP; ++j) z[j] = a[j];
             }
-            float uk[LPP];  // K rows keep u for the Jacobian (and z in shared memory)
+            // K rows keep z in shared memory: the Jacobian recomputes u = tanh(z inv) from it
             if (h == 0) {
                 // F'_Q = phi(Q_t) / den_t -> shared tile row t;  -c_t -> rows 0 / 1 of the mass operand
                 const float sc = a2.x;
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     if (l < L && l * R < LRMAX) {
                         float u[P], ph[R];
 #pragma unroll
-                        for (int p = 0; p < P; ++p) u[p] = uk[l * P + p] = tc::tanh_abs(z[l * P + p] * inv);
+                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
                         tc::bucket_probs<P>(u, beta, ph);
 #pragma unroll
                         for (int r = 0; r < R; ++r)
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     if (l < L && l * R < LRMAX) {
                         float u[P], ph[R], dp[R];
 #pragma unroll
-                        for (int p = 0; p < P; ++p) u[p] = uk[l * P + p];
+                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(zk_s[(l * P + p) * C + t] * inv);
                         tc::bucket_probs<P>(u, beta, ph);
 #pragma unroll
                         for (int r = 0; r < R; ++r) dp[r] = l * R + r < LRMAX ? dph[l * R + r] : 0.f;

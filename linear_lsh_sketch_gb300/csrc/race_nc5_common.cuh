@@ -278,20 +278,24 @@ __host__ __device__ constexpr uint32_t idesc_proj() { return idesc_bf16(128, LPP
 // Issues z = X (W_hi + W_lo)^T for a token tile (D / 16 K steps per hyperplane copy).
 // 32 bf16 (64 bytes, packed pairs in o) of one output row to global memory: two 32-byte stores
 // when `wide` (the tensor's base is 32-byte aligned, so every row segment is), else four 16-byte
-// stores.  Full 32-byte sectors halve the store instructions of a row-per-thread epilogue.
+// stores.  Full 32-byte sectors halve the store instructions of a row-per-thread epilogue.  The
+// stores do not allocate in L1: with most of L1 given to shared memory, output lines would evict
+// the few lines that hold register spills.
 __device__ __forceinline__ void store_row32(bf16 *dst, const uint32_t (&o)[16], bool wide)
 {
     if (wide) {
-        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(dst), "r"(o[0]), "r"(o[1]),
-                     "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+        asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(dst), "r"(o[0]),
+                     "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
                      : "memory");
-        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(dst + 16), "r"(o[8]), "r"(o[9]),
-                     "r"(o[10]), "r"(o[11]), "r"(o[12]), "r"(o[13]), "r"(o[14]), "r"(o[15])
+        asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(dst + 16),
+                     "r"(o[8]), "r"(o[9]), "r"(o[10]), "r"(o[11]), "r"(o[12]), "r"(o[13]), "r"(o[14]), "r"(o[15])
                      : "memory");
     } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4 *>(dst + 8 * q) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"l"(dst + 8 * q), "r"(o[4 * q]),
+                         "r"(o[4 * q + 1]), "r"(o[4 * q + 2]), "r"(o[4 * q + 3])
+                         : "memory");
     }
 }
 
