@@ -864,6 +864,11 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma(tmem + T_MS, d_fk_mn + ko, d_ones + kk, id_m16, true);
                 }
                 commit(bar(B_B));
+                if (c + 1 < nchunk) {  // V is last read by group B
+                    if (!(ok = wait_phase(bar(B_B), par, abort))) break;
+                    load_tiles(c + 1, 2);
+                    ++issued[1];
+                }
                 // group C: dxhat, gradient sketch, sketch update
                 if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
                 fence_after();
@@ -878,10 +883,9 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma(tmem + T_GB, d_fq_mn + ko, d_ncm + kk, id_m16, true);
                 }
                 commit(bar(B_C));
-                if (c + 1 < nchunk) {  // V and dO are last read by group C
+                if (c + 1 < nchunk) {  // dO is last read by group C
                     if (!(ok = wait_phase(bar(B_C), par, abort))) break;
-                    load_tiles(c + 1, 6);
-                    ++issued[1];
+                    load_tiles(c + 1, 4);
                     ++issued[2];
                 }
             }
