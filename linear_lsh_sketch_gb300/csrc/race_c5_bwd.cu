@@ -847,6 +847,14 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int ks = 0; ks < C / 16; ++ks)
                     umma_ts(tmem + T_BT, tmem + T_TRIL + 8 * ks, d_fk_mn + (uint64_t)(ks * 128), id_bt, ks > 0);
                 commit(bar(B_A));
+                // sketch update A^T += V^T F_K and B += F_K^T 1 while the mask is applied (this chunk's
+                // products read the sketch from its shared copy; group B's commit covers these)
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_ST, d_v_mt + ko, d_fk_mn + ko, id_gt, true);
+                    umma(tmem + T_MS, d_fk_mn + ko, d_ones + kk, id_m16, true);
+                }
                 // group B: g += M1 F_K
                 if (!(ok = wait_phase(bar(B_MASK), par, abort))) break;
                 fence_after();
@@ -854,14 +862,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int ks = 0; ks < C / 16; ++ks) {
                     const uint32_t ac = (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4));
                     umma_ts(tmem + T_G, tmem + T_DV + ac, d_fk_mn + (uint64_t)(ks * 128), id_bt, true);
-                }
-                // sketch update (its bf16 copy for the next chunk is made while the Q rows run the
-                // Jacobian)
-#pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks) {
-                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
-                    umma(tmem + T_ST, d_v_mt + ko, d_fk_mn + ko, id_gt, true);
-                    umma(tmem + T_MS, d_fk_mn + ko, d_ones + kk, id_m16, true);
                 }
                 commit(bar(B_B));
                 if (c + 1 < nchunk) {  // V is last read by group B
