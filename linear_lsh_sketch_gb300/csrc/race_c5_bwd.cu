@@ -614,7 +614,7 @@ constexpr uint32_t T_GB = 416;    // G_B (lanes = sketch row), columns 0 + 1 (c 
 constexpr uint32_t T_X = 432;     // the Q row as stored (bf16 pairs), 64 columns
 constexpr uint32_t T_COLS = 512;
 
-enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_COUNT };
+enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_G, B_COUNT };
 
 struct QLayout {
     uint32_t q, k, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, bprev, invq, red, bar, slot, bytes, kbb;
@@ -869,22 +869,24 @@ __global__ void __launch_bounds__(NTHW, 1)
                     load_tiles(c + 1, 2);
                     ++issued[1];
                 }
-                // group C: dxhat, gradient sketch, sketch update
+                // group C: dxhat (the dQ epilogue starts on it), then the gradient sketch update
+                // G += F'_Q^T [dO | -c], which runs during the epilogue under its own commit
                 if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
                 fence_after();
                 for (int ks = 0; ks < LPP / 16; ++ks) {
                     umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_whi + (uint64_t)(ks * 128), id_x, ks > 0);
                     umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_wlo + (uint64_t)(ks * 128), id_x, true);
                 }
+                commit(bar(B_C));
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks) {
                     const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
                     umma(tmem + T_GT, d_do_mt + ko, d_fq_mn + ko, id_gt, true);
                     umma(tmem + T_GB, d_fq_mn + ko, d_ncm + kk, id_m16, true);
                 }
-                commit(bar(B_C));
-                if (c + 1 < nchunk) {  // dO is last read by group C
-                    if (!(ok = wait_phase(bar(B_C), par, abort))) break;
+                commit(bar(B_G));
+                if (c + 1 < nchunk) {  // dO is last read by the gradient sketch update
+                    if (!(ok = wait_phase(bar(B_G), par, abort))) break;
                     load_tiles(c + 1, 4);
                     ++issued[2];
                 }
@@ -1125,6 +1127,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             if (!(ok = group_sync(bar(B_CS), (c + 1) & 1, abort))) break;  // B_prev, TMEM reads: next chunk
         }
         // the segment's gradient-sketch sum: G^T (lanes d) and G_B (lanes = sketch row, hi + lo)
+        if (ok && nchunk > 0) ok = wait_phase(bar(B_G), (nchunk - 1) & 1, abort);
         if (ok) {
             fence_after();
             float *out = Gseg + ((int64_t)bh * nseg + s) * LR * (D + 1);

@@ -286,9 +286,20 @@ __global__ void __launch_bounds__(NTHW, 1)
                 // the previous chunk's output is staged and this chunk's sketch operand is written
                 if (!(ok = wait_phase(bar(B_SOP), c & 1, abort))) break;
                 if (c >= 1) store_out(c - 1);
-                if (!(ok = wait_phase(bar(B_MASK), c & 1, abort))) break;
                 if (!(ok = wait_phase(bar(B_V0 + (c & 1)), (c >> 1) & 1, abort))) break;
                 ++v_done[c & 1];
+                fence_after();
+                const uint64_t d_v = desc_mn(vst, BLK);
+                const uint64_t d_vt = desc_mn(vst, D == 128 ? BLK : (Ly.zero - (Ly.v + (c & 1) * Ly.kbb)));
+                // the sketch update needs only V and F_K, and the operand copy has read the sketch:
+                // it runs while the mask is applied (the products' commit below covers it)
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_ST, d_vt + ko, d_fk_mn + ko, id_up, true);
+                    umma(tmem + T_MS, d_fk_mt + ko, d_ones + kk, id_ms, true);
+                }
+                if (!(ok = wait_phase(bar(B_MASK), c & 1, abort))) break;
                 // the next chunk's projection ahead of this chunk's products when its tiles are in,
                 // so its features are computed while these run
                 if (pipe && c + 1 < nchunk && mbar_test(bar(B_QK), (c + 1) & 1)) {
@@ -297,8 +308,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                     projected = true;
                 }
                 fence_after();
-                const uint64_t d_v = desc_mn(vst, BLK);
-                const uint64_t d_vt = desc_mn(vst, D == 128 ? BLK : (Ly.zero - (Ly.v + (c & 1) * Ly.kbb)));
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks) {
                     const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
@@ -308,12 +317,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int ks = 0; ks < lrp / 16; ++ks) {
                     umma_ts(tmem + T_O, tmem + fq + 8 * ks, d_shi + (uint64_t)(ks * 2), id_ro, true);
                     umma_ts(tmem + T_O, tmem + fq + 8 * ks, d_slo + (uint64_t)(ks * 2), id_ro, true);
-                }
-#pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks) {
-                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
-                    umma(tmem + T_ST, d_vt + ko, d_fk_mn + ko, id_up, true);
-                    umma(tmem + T_MS, d_fk_mt + ko, d_ones + kk, id_ms, true);
                 }
                 commit(bar(B_MMA));
                 // V stage (c + 1) & 1 held chunk c - 1, whose output store must have read it
