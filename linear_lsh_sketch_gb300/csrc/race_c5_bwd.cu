@@ -70,7 +70,7 @@ struct BwdLayout {
     }
 };
 
-template <int D, int P>
+template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTHW, 1)
     k_causal_bwdkv5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
@@ -102,9 +102,11 @@ __global__ void __launch_bounds__(NTHW, 1)
     const int64_t n_begin = (int64_t)s * seg_len;
     const int64_t n_end = min(Dm.N, n_begin + seg_len);
     const int nchunk = n_end > n_begin ? (int)((n_end - n_begin + C - 1) / C) : 0;
-    const int LR = Dm.LR;
+    // LT > 0: the table count is a compile-time constant, so the per-table loops unroll without
+    // run-time guards and the tables' independent chains interleave
+    const int L = LT > 0 ? LT : Dm.L;
+    const int LR = LT > 0 ? LT * (1 << P) : Dm.LR;
     const float beta = Dm.beta;
-    const int L = Dm.L;
     const int64_t off = bh * Dm.N * D;
 
     // ---- set-up
@@ -642,7 +644,7 @@ struct QLayout {
     }
 };
 
-template <int D, int P>
+template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTHW, 1)
     k_causal_bwdq5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
@@ -674,9 +676,11 @@ __global__ void __launch_bounds__(NTHW, 1)
     const int64_t n_begin = (int64_t)s * seg_len;
     const int64_t n_end = min(Dm.N, n_begin + seg_len);
     const int nchunk = n_end > n_begin ? (int)((n_end - n_begin + C - 1) / C) : 0;
-    const int LR = Dm.LR;
+    // LT > 0: the table count is a compile-time constant, so the per-table loops unroll without
+    // run-time guards and the tables' independent chains interleave
+    const int L = LT > 0 ? LT : Dm.L;
+    const int LR = LT > 0 ? LT * (1 << P) : Dm.LR;
     const float beta = Dm.beta;
-    const int L = Dm.L;
     const int64_t off = bh * Dm.N * D;
 
     // ---- set-up
@@ -1167,36 +1171,58 @@ bool c5_bwd_supported(const Dims &D)
 
 namespace {
 
-template <int D, int P>
-cudaError_t bwdkv5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                        const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
-                        int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+template <int D, int P, int LT>
+cudaError_t bwdkv5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
+                          int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
 {
     const c5b::BwdLayout Ly(D);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = c5b::k_causal_bwdkv5<D, P>;
+    auto kern = c5b::k_causal_bwdkv5<D, P, LT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_bwd_kv", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5b::NTHW), smem,
                          st, mq, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err);
 }
 
+// (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
+template <int D, int P>
+cudaError_t bwdkv5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                        const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
+                        int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+{
+    if constexpr (D == 128 && P == 3)
+        if (Dm.L == 3) return bwdkv5_launch<D, P, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+    return bwdkv5_launch<D, P, 0>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+}
+
 }  // namespace
 
 namespace {
 
+template <int D, int P, int LT>
+cudaError_t bwdq5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                         const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
+                         bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, cudaStream_t st)
+{
+    const c5q::QLayout Ly(D);
+    const size_t smem = Ly.bytes + 1024;
+    auto kern = c5q::k_causal_bwdq5<D, P, LT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel("tc5_causal_bwd_q", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5q::NTHW), smem, st,
+                         mq, mk, mv, mdo, Dm, W, S0, seg_len, nseg, dQ, aux, Gseg, err);
+}
+
+// (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
 template <int D, int P>
 cudaError_t bwdq5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                        const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
                        bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, cudaStream_t st)
 {
-    const c5q::QLayout Ly(D);
-    const size_t smem = Ly.bytes + 1024;
-    auto kern = c5q::k_causal_bwdq5<D, P>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_kernel("tc5_causal_bwd_q", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5q::NTHW), smem, st,
-                         mq, mk, mv, mdo, Dm, W, S0, seg_len, nseg, dQ, aux, Gseg, err);
+    if constexpr (D == 128 && P == 3)
+        if (Dm.L == 3) return bwdq5_launch<D, P, 3>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, st);
+    return bwdq5_launch<D, P, 0>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, st);
 }
 
 }  // namespace
