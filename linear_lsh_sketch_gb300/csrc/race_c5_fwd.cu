@@ -122,7 +122,7 @@ constexpr int NTHW = NTH + 32;  // 8 compute warps + 1 control warp (TMA and MMA
 // Barrier slots (8 bytes each) after FwdLayout::bar.
 enum : uint32_t { B_QK, B_PROJ, B_SC, B_MMA, B_FEAT, B_MASK, B_SOP, B_V0, B_V1, B_COUNT };
 
-template <int D, int P>
+template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTHW, 1)
     k_causal_fwd5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, Dims Dm,
@@ -148,9 +148,10 @@ __global__ void __launch_bounds__(NTHW, 1)
     const int64_t n_begin = (int64_t)s * seg_len;
     const int64_t n_end = min(Dm.N, n_begin + seg_len);
     const int nchunk = n_end > n_begin ? (int)((n_end - n_begin + C - 1) / C) : 0;
-    const int LR = Dm.LR, lrp = (LR + 15) & ~15;
+    // LT > 0: the table count is a compile-time constant (per-table loops unroll without guards)
+    const int L = LT > 0 ? LT : Dm.L;
+    const int LR = LT > 0 ? LT * (1 << P) : Dm.LR, lrp = (LR + 15) & ~15;
     const float beta = Dm.beta;
-    const int L = Dm.L;
     // L R <= 32: the features of consecutive chunks use alternate buffers (F_Q: 16 TMEM columns
     // each, F_K: one 16 KB tile each), so chunk c featurises while chunk c - 1's products run
     const bool pipe = lrp <= 32;
@@ -517,18 +518,29 @@ bool c5_supported(const Dims &D)
 
 namespace {
 
+template <int D, int P, int LT>
+cudaError_t causal_fwd5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                               const CUtensorMap &mo, const float *W, const float *S0, int64_t seg_len, int nseg,
+                               unsigned *err, cudaStream_t st)
+{
+    const c5::FwdLayout Ly(D);
+    const size_t smem = Ly.bytes + 1024;
+    auto kern = c5::k_causal_fwd5<D, P, LT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel("tc5_causal_fwd", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5::NTHW), smem, st, mq,
+                         mk, mv, mo, Dm, W, S0, seg_len, nseg, err);
+}
+
+// (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
 template <int D, int P>
 cudaError_t causal_fwd5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                              const CUtensorMap &mo, const float *W, const float *S0, int64_t seg_len, int nseg,
                              unsigned *err, cudaStream_t st)
 {
-    const c5::FwdLayout Ly(D);
-    const size_t smem = Ly.bytes + 1024;
-    auto kern = c5::k_causal_fwd5<D, P>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_kernel("tc5_causal_fwd", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5::NTHW), smem, st, mq,
-                         mk, mv, mo, Dm, W, S0, seg_len, nseg, err);
+    if constexpr (D == 128 && P == 3)
+        if (Dm.L == 3) return causal_fwd5_launch<D, P, 3>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+    return causal_fwd5_launch<D, P, 0>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
 }
 
 }  // namespace

@@ -123,7 +123,7 @@ __host__ __device__ inline uint32_t bwdk_cols(int D, int lrp) { return pow2_cols
 // ------------------------------------------------------------------ query side
 
 // dQ and aux[t] = {1 / den_t, c_t} for the CTA's tiles.  S: combined key sketch [BH][LR][d + 1].
-template <int D, int P>
+template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTH, 1)
     k_bwdq5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
             const __grid_constant__ CUtensorMap tmdQ, Dims Dm, const float *__restrict__ W,
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const int lrp = Ly.lrp;
     const uint32_t zc = bwdq_zc(D, lrp), dzc = zc + 32, ncols = bwdq_cols(D, lrp);
     const float beta = Dm.beta;
-    const int L = Dm.L;
+    const int L = LT > 0 ? LT : Dm.L;  // LT > 0: per-table loops unroll without guards
 
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
     load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(NTH, 1)
 // ------------------------------------------------------------------ key side
 
 // dK and dV for the CTA's tiles.  G: combined gradient sketch [BH][LR][d + 1].
-template <int D, int P>
+template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTH, 1)
     k_bwdk5(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
             const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV, Dims Dm,
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const int lrp = Ly.lrp;
     const uint32_t zc = bwdk_zc(D, lrp), fkc = zc + 32, dzc = fkc + lrp / 2, ncols = bwdk_cols(D, lrp);
     const float beta = Dm.beta;
-    const int L = Dm.L;
+    const int L = LT > 0 ? LT : Dm.L;  // LT > 0: per-table loops unroll without guards
 
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
     load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
@@ -648,13 +648,13 @@ nc5::BwdLayout bwd_layout(const Dims &Dm)
     return nc5::BwdLayout(Dm.d, Dm.LR, with_lo.bytes + 1024 <= kSmemMax);
 }
 
-template <int D, int P>
-cudaError_t bwdq_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mdo, const CUtensorMap &mdq,
-                      const float *W, const float *S, float2 *aux, unsigned *err, cudaStream_t st)
+template <int D, int P, int LT>
+cudaError_t bwdq_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mdo, const CUtensorMap &mdq,
+                        const float *W, const float *S, float2 *aux, unsigned *err, cudaStream_t st)
 {
     const nc5::BwdLayout Ly = bwd_layout(Dm);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = nc5::k_bwdq5<D, P>;
+    auto kern = nc5::k_bwdq5<D, P, LT>;
     cudaError_t e = prep_bwd(kern, smem);
     if (e != cudaSuccess) return e;
     const int64_t seg = bwd_seg(Dm, smem);
@@ -663,19 +663,43 @@ cudaError_t bwdq_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &
                          mdo, mdq, Dm, W, S, aux, seg, (int)Ly.split, err);
 }
 
+// The named non-causal workloads' shapes run with L compiled in: (d, P, L) = (64, 3, 3), (128, 6, 4).
 template <int D, int P>
-cudaError_t bwdk_inst(const Dims &Dm, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdk,
-                      const CUtensorMap &mdv, const float *W, const float *G, unsigned *err, cudaStream_t st)
+cudaError_t bwdq_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mdo, const CUtensorMap &mdq,
+                      const float *W, const float *S, float2 *aux, unsigned *err, cudaStream_t st)
+{
+    if constexpr (D == 64 && P == 3)
+        if (Dm.L == 3) return bwdq_launch<D, P, 3>(Dm, mq, mdo, mdq, W, S, aux, err, st);
+    if constexpr (D == 128 && P == 6)
+        if (Dm.L == 4) return bwdq_launch<D, P, 4>(Dm, mq, mdo, mdq, W, S, aux, err, st);
+    return bwdq_launch<D, P, 0>(Dm, mq, mdo, mdq, W, S, aux, err, st);
+}
+
+template <int D, int P, int LT>
+cudaError_t bwdk_launch(const Dims &Dm, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdk,
+                        const CUtensorMap &mdv, const float *W, const float *G, unsigned *err, cudaStream_t st)
 {
     const nc5::BwdLayout Ly = bwd_layout(Dm);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = nc5::k_bwdk5<D, P>;
+    auto kern = nc5::k_bwdk5<D, P, LT>;
     cudaError_t e = prep_bwd(kern, smem);
     if (e != cudaSuccess) return e;
     const int64_t seg = bwd_seg(Dm, smem);
     const int64_t nseg = (Dm.N + seg - 1) / seg;
     return launch_kernel("tc5_bwd_key", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(nc5::NTH), smem, st, mk,
                          mv, mdk, mdv, Dm, W, G, seg, (int)Ly.split, err);
+}
+
+// The named non-causal workloads' shapes run with L compiled in: (d, P, L) = (64, 3, 3), (128, 6, 4).
+template <int D, int P>
+cudaError_t bwdk_inst(const Dims &Dm, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdk,
+                      const CUtensorMap &mdv, const float *W, const float *G, unsigned *err, cudaStream_t st)
+{
+    if constexpr (D == 64 && P == 3)
+        if (Dm.L == 3) return bwdk_launch<D, P, 3>(Dm, mk, mv, mdk, mdv, W, G, err, st);
+    if constexpr (D == 128 && P == 6)
+        if (Dm.L == 4) return bwdk_launch<D, P, 4>(Dm, mk, mv, mdk, mdv, W, G, err, st);
+    return bwdk_launch<D, P, 0>(Dm, mk, mv, mdk, mdv, W, G, err, st);
 }
 
 #define RACE_NC5B_DISPATCH(FN, ...)                        \

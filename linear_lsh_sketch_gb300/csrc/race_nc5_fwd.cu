@@ -66,7 +66,7 @@ enum : uint32_t { SB_X0, SB_X1, SB_Y0, SB_Y1, SB_P0, SB_P1, SB_S0, SB_S1, SB_F0,
 // (= -c, split into bf16 hi and lo rows).  part: [BH][nsplit][LR][d + 1] fp32.
 // Warp 8 issues the TMA copies and MMAs; the projection of tile i + 1 is issued ahead of the
 // sketch product of tile i, so the compute warps featurise tile i + 1 while it runs.
-template <int D, int P>
+template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTHW, 1)
     k_sketch5(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY, Dims Dm,
               const float *__restrict__ W, const float2 *__restrict__ aux, int64_t seg_len, int nsplit,
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
                 }
             }
-            write_features<P>(z, inv, Dm.beta, Dm.L, h, scale, t, base + Ly.f + (i % nf) * Ly.fbytes);
+            write_features<P>(z, inv, Dm.beta, LT > 0 ? LT : Dm.L, h, scale, t, base + Ly.f + (i % nf) * Ly.fbytes);
             warp_signal(bar(SB_F0 + s));
         }
         if (ok && ntile > 0) ok = wait_phase(bar(SB_DONE), 0, abort);
@@ -311,7 +311,7 @@ __host__ __device__ inline uint32_t readout_zcol(int D) { return (D + 16 + 31) &
 __host__ __device__ inline uint32_t readout_tmem_cols(int D) { return readout_zcol(D) + LPP <= 128 ? 128 : 256; }
 
 // O = Phi_Q [A | B] content / mass for the CTA's tiles.  S: combined sketch [BH][LR][d + 1].
-template <int D, int P>
+template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTH, 1)
     k_readout5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, Dims Dm,
                const float *__restrict__ W, const float *__restrict__ S, int64_t seg_len, int split_s,
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(NTH, 1)
         }
         const float ssq = red[t] + red[C + t];
         const float inv = ssq > 0.f ? rsqrtf(ssq) : 0.f;
-        write_features<P>(z, inv, Dm.beta, Dm.L, h, t < cnt ? 1.f : 0.f, t, base + Ly.f);
+        write_features<P>(z, inv, Dm.beta, LT > 0 ? LT : Dm.L, h, t < cnt ? 1.f : 0.f, t, base + Ly.f);
         tc::fence_proxy_async();
         fence_before();
         __syncthreads();
@@ -557,29 +557,42 @@ cudaError_t prep_smem(K kern, size_t bytes)
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <int D, int P>
-cudaError_t sketch_inst(const Dims &Dm, const CUtensorMap &mx, const CUtensorMap &my, const float *W,
-                        const float2 *aux, int64_t seg_len, int nsplit, float *part, unsigned *err, int mode,
-                        cudaStream_t st)
+template <int D, int P, int LT>
+cudaError_t sketch_launch(const Dims &Dm, const CUtensorMap &mx, const CUtensorMap &my, const float *W,
+                          const float2 *aux, int64_t seg_len, int nsplit, float *part, unsigned *err, int mode,
+                          cudaStream_t st)
 {
     const nc5::SketchLayout Ly(D, Dm.LR);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = nc5::k_sketch5<D, P>;
+    auto kern = nc5::k_sketch5<D, P, LT>;
     cudaError_t e = prep_smem(kern, smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(mode ? "tc5_sketch_grad" : "tc5_sketch_keys", kern, dim3(nsplit, (unsigned)Dm.BH),
                          dim3(nc5::NTHW), smem, st, mx, my, Dm, W, aux, seg_len, nsplit, part, err, mode);
 }
 
+// The named workloads' shapes run with L compiled in: (d, P, L) = (128, 3, 3), (64, 3, 3), (128, 6, 4).
 template <int D, int P>
-cudaError_t readout_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mo, const float *W,
-                         const float *S, unsigned *err, cudaStream_t st)
+cudaError_t sketch_inst(const Dims &Dm, const CUtensorMap &mx, const CUtensorMap &my, const float *W,
+                        const float2 *aux, int64_t seg_len, int nsplit, float *part, unsigned *err, int mode,
+                        cudaStream_t st)
+{
+    if constexpr (P == 3)
+        if (Dm.L == 3) return sketch_launch<D, P, 3>(Dm, mx, my, W, aux, seg_len, nsplit, part, err, mode, st);
+    if constexpr (D == 128 && P == 6)
+        if (Dm.L == 4) return sketch_launch<D, P, 4>(Dm, mx, my, W, aux, seg_len, nsplit, part, err, mode, st);
+    return sketch_launch<D, P, 0>(Dm, mx, my, W, aux, seg_len, nsplit, part, err, mode, st);
+}
+
+template <int D, int P, int LT>
+cudaError_t readout_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mo, const float *W,
+                           const float *S, unsigned *err, cudaStream_t st)
 {
     const nc5::ReadoutLayout with_lo(D, Dm.LR, true);
     const bool split = with_lo.bytes + 1024 <= 227 * 1024;
     const nc5::ReadoutLayout Ly(D, Dm.LR, split);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = nc5::k_readout5<D, P>;
+    auto kern = nc5::k_readout5<D, P, LT>;
     cudaError_t e = prep_smem(kern, smem);
     if (e != cudaSuccess) return e;
     const int per_sm = std::max<int>(1, std::min<int>(2, (int)((227 * 1024) / smem)));
@@ -590,6 +603,18 @@ cudaError_t readout_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMa
     const int64_t nseg = (Dm.N + seg - 1) / seg;
     return launch_kernel("tc5_readout", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(nc5::NTH), smem, st, mq,
                          mo, Dm, W, S, seg, (int)split, err);
+}
+
+// The named non-causal workloads' shapes run with L compiled in: (d, P, L) = (64, 3, 3), (128, 6, 4).
+template <int D, int P>
+cudaError_t readout_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mo, const float *W,
+                         const float *S, unsigned *err, cudaStream_t st)
+{
+    if constexpr (D == 64 && P == 3)
+        if (Dm.L == 3) return readout_launch<D, P, 3>(Dm, mq, mo, W, S, err, st);
+    if constexpr (D == 128 && P == 6)
+        if (Dm.L == 4) return readout_launch<D, P, 4>(Dm, mq, mo, W, S, err, st);
+    return readout_launch<D, P, 0>(Dm, mq, mo, W, S, err, st);
 }
 
 #define RACE_NC5_DISPATCH(FN, ...)                               \
