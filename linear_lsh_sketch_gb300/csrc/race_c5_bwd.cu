@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(NTHW, 1)
     // run-time guards and the tables' independent chains interleave
     const int L = LT > 0 ? LT : Dm.L;
     const int LR = LT > 0 ? LT * (1 << P) : Dm.LR;
+    const int LP = L * P;
     const float beta = Dm.beta;
     const int64_t off = bh * Dm.N * D;
 
@@ -414,7 +415,8 @@ __global__ void __launch_bounds__(NTHW, 1)
             } else {
                 // F_K -> TMEM (A operand); keep u
 #pragma unroll
-                for (int j = 0; j < LMAX * P; ++j) zk_s[j * C + t] = z[j];
+                for (int j = 0; j < LMAX * P; ++j)
+                    if (j < LP) zk_s[j * C + t] = z[j];
                 float phk[LRMAX];
 #pragma unroll
                 for (int j = 0; j < LRMAX; ++j) phk[j] = 0.f;
@@ -525,7 +527,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                 }
                 // dxhat = W^T dz (dz rounded to bf16 as the product sees it), so x . dxhat = z . dz
 #pragma unroll
-                for (int j = 0; j < LMAX * P; ++j) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[j])), zk_s[j * C + t], zdz);
+                for (int j = 0; j < LMAX * P; ++j)
+                    if (j < LP) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[j])), zk_s[j * C + t], zdz);
                 wait_st();
                 warp_signal(bar(B_JAC));
             } else {
@@ -680,6 +683,7 @@ __global__ void __launch_bounds__(NTHW, 1)
     // run-time guards and the tables' independent chains interleave
     const int L = LT > 0 ? LT : Dm.L;
     const int LR = LT > 0 ? LT * (1 << P) : Dm.LR;
+    const int LP = L * P;
     const float beta = Dm.beta;
     const int64_t off = bh * Dm.N * D;
 
@@ -946,7 +950,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             float uq[LPP];  // Q rows keep u for the Jacobian
             if (h == 0) {
 #pragma unroll
-                for (int j = 0; j < LPP; ++j) uq[j] = j < Dm.LP ? tc::tanh_abs(z[j] * inv) : 0.f;
+                for (int j = 0; j < LPP; ++j) uq[j] = j < LP ? tc::tanh_abs(z[j] * inv) : 0.f;
             } else {
                 const float sc = live ? 1.f : 0.f;
 #pragma unroll
@@ -1087,7 +1091,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                     float zq[32], zdz = 0.f;
                     ld32(tlane + T_ZQ, zq);
 #pragma unroll
-                    for (int j = 0; j < LPP; ++j) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[j])), zq[j], zdz);
+                    for (int j = 0; j < LPP; ++j)
+                        if (j < LP) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[j])), zq[j], zdz);
                     red[t] = invq_s[t] * invq_s[t] * zdz;
                 }
                 const float mcv = -cc;
