@@ -375,7 +375,9 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                 for (int j = 0; j < LPP; ++j) z[j] = a[j];
             }
-            // K rows keep z in shared memory: the Jacobian recomputes u = tanh(z inv) from it
+            // K rows keep z in shared memory; with L compiled in they also keep u = tanh(z inv) in
+            // registers (L P of them), otherwise the Jacobian recomputes it from z
+            float uk[LT > 0 ? LPP : 1];
             if (h == 0) {
                 // F'_Q = phi(Q_t) / den_t -> shared tile row t;  -c_t -> rows 0 / 1 of the mass operand
                 const float sc = a2.x;
@@ -425,7 +427,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                     if (l < L && l * R < LRMAX) {
                         float u[P], ph[R];
 #pragma unroll
-                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+                        for (int p = 0; p < P; ++p) {
+                            u[p] = tc::tanh_abs(z[l * P + p] * inv);
+                            if constexpr (LT > 0) uk[l * P + p] = u[p];
+                        }
                         tc::bucket_probs<P>(u, beta, ph);
 #pragma unroll
                         for (int r = 0; r < R; ++r)
@@ -508,7 +513,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                     if (l < L && l * R < LRMAX) {
                         float u[P], ph[R], dp[R];
 #pragma unroll
-                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(zk_s[(l * P + p) * C + t] * inv);
+                        for (int p = 0; p < P; ++p)
+                            u[p] = LT > 0 ? uk[(l * P + p) % (LT > 0 ? LPP : 1)] : tc::tanh_abs(zk_s[(l * P + p) * C + t] * inv);
                         tc::bucket_probs<P>(u, beta, ph);
 #pragma unroll
                         for (int r = 0; r < R; ++r) dp[r] = l * R + r < LRMAX ? dph[l * R + r] : 0.f;
@@ -1021,6 +1027,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 reg_fence(gr);
                 reg_fence(br);
                 float den = 0.f, pg = 0.f;
+                float phq[LT > 0 ? LRMAX : 1];  // with L compiled in: the row's bucket probabilities
 #pragma unroll
                 for (int l = 0; l < LMAX; ++l) {
                     if (l < L && l * R < LRMAX) {
@@ -1031,6 +1038,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const int lr = l * R + r < 32 ? l * R + r : 31;
+                            if constexpr (LT > 0) phq[lr] = ph[r];
                             den = fmaf(ph[r], bprev[32 * par + lr] + uf(br[lr]), den);
                             pg = fmaf(ph[r], uf(gr[lr]), pg);
                         }
@@ -1048,7 +1056,12 @@ __global__ void __launch_bounds__(NTHW, 1)
                         float u[P], ph[R], g[R];
 #pragma unroll
                         for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
-                        tc::bucket_probs<P>(u, beta, ph);
+                        if constexpr (LT > 0) {
+#pragma unroll
+                            for (int r = 0; r < R; ++r) ph[r] = phq[l * R + r < 32 ? l * R + r : 31];
+                        } else {
+                            tc::bucket_probs<P>(u, beta, ph);
+                        }
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const int lr = l * R + r < 32 ? l * R + r : 31;
