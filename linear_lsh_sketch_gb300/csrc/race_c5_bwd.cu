@@ -44,7 +44,8 @@ constexpr uint32_t T_GT = 448;   // G^T (lanes = d), 32 columns
 constexpr uint32_t T_GB = 480;   // G_B (lanes = sketch row), 16 columns (column 0 used)
 constexpr uint32_t T_COLS = 512;
 
-enum : uint32_t { B_Q, B_K, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_COUNT };
+enum : uint32_t { B_Q, B_K, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_G,
+                  B_COUNT };
 
 struct BwdLayout {
     uint32_t q, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, zk, bar, slot, bytes, kbb;
@@ -304,7 +305,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma_ts(tmem + T_DP, tmem + T_DV + ac, d_fq_mn + (uint64_t)(ks * 128), id_mf, true);
                 }
                 commit(bar(B_B));
-                // group C: dxhat and the gradient sketch update
+                // group C: dxhat (the dK epilogue starts on it), then the gradient sketch update under
+                // its own commit (the G conversion and the dO reload wait for that one)
                 if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
                 fence_after();
                 if (k + 1 < nchunk) {  // the K rows are parked in TMEM by now
@@ -315,15 +317,16 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_whi + (uint64_t)(ks * 128), id_x, ks > 0);
                     umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_wlo + (uint64_t)(ks * 128), id_x, true);
                 }
+                commit(bar(B_C));
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks) {
                     const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
                     umma(tmem + T_GT, d_do_mt + ko, d_fq_mn + ko, id_gt, true);
                     umma(tmem + T_GB, d_fq_mn + ko, d_ncm + kk, id_gb, true);
                 }
-                commit(bar(B_C));
-                if (k + 1 < nchunk) {  // dO is read by groups B and C only
-                    if (!(ok = wait_phase(bar(B_C), par, abort))) break;
+                commit(bar(B_G));
+                if (k + 1 < nchunk) {  // dO is last read by the gradient sketch update
+                    if (!(ok = wait_phase(bar(B_G), par, abort))) break;
                     load_tiles(k + 1, 4);
                     ++issued[2];
                 }
@@ -555,7 +558,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_DVR));  // dV columns (shared with z) read
             }
-            if (!wait_phase(bar(B_C), par, abort)) break;
+            // the K rows' dK needs dxhat; the Q rows' G conversion needs the gradient sketch update
+            if (!wait_phase(bar(h ? B_C : B_G), par, abort)) break;
             fence_after();
             if (h == 1) {
                 // dK row t = inv (dxhat - x inv^2 (x . dxhat)), x parked in TMEM; straight to global memory
