@@ -267,10 +267,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                 commit(bar(B_PROJ));
                 // group A once the features and the previous chunk's G operand are in
                 if (!(ok = wait_phase(bar(B_FEAT), par, abort))) break;
-                if (k + 1 < nchunk) {  // the projection and the norms have read the Q tile
-                    load_tiles(k + 1, 1);
-                    ++issued[0];
-                }
                 if (!(ok = wait_phase(bar(B_GOP), par, abort))) break;
                 if (!(ok = wait_phase(bar(B_V), par, abort))) break;
                 ++done[1];
@@ -291,6 +287,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma_ts(tmem + T_DVV, tmem + T_FK + 8 * ks, d_glo_k + (uint64_t)(2 * ks), id_dv, true);
                 }
                 commit(bar(B_A));
+                if (k + 1 < nchunk) {  // the projection and the norms have read the Q tile; issued after
+                    load_tiles(k + 1, 1);  // group A, which waits on this warp
+                    ++issued[0];
+                }
                 // group B: masked products
                 if (!(ok = wait_phase(bar(B_MASK), par, abort))) break;
                 fence_after();
@@ -843,10 +843,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                 issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
                 commit(bar(B_PROJ));
                 if (!(ok = wait_phase(bar(B_FEAT), par, abort))) break;
-                if (c + 1 < nchunk) {  // projections and norms have read the Q / K tiles
-                    load_tiles(c + 1, 1);
-                    ++issued[0];
-                }
                 if (!(ok = wait_phase(bar(B_SOP), par, abort))) break;
                 if (!(ok = wait_phase(bar(B_V), par, abort))) break;
                 ++done[1];
@@ -865,6 +861,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int ks = 0; ks < C / 16; ++ks)
                     umma_ts(tmem + T_BT, tmem + T_TRIL + 8 * ks, d_fk_mn + (uint64_t)(ks * 128), id_bt, ks > 0);
                 commit(bar(B_A));
+                if (c + 1 < nchunk) {  // projections and norms have read the Q / K tiles; issued after
+                    load_tiles(c + 1, 1);  // group A, which waits on this warp
+                    ++issued[0];
+                }
                 // sketch update A^T += V^T F_K and B += F_K^T 1 while the mask is applied (this chunk's
                 // products read the sketch from its shared copy; group B's commit covers these)
 #pragma unroll
