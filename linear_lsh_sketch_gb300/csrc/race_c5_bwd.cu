@@ -294,10 +294,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                 // group B: masked products
                 if (!(ok = wait_phase(bar(B_MASK), par, abort))) break;
                 fence_after();
-                if (k + 1 < nchunk) {  // group A (the only reader of V) is complete
-                    load_tiles(k + 1, 2);
-                    ++issued[1];
-                }
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks) {
                     const uint32_t ac = (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4));  // in-place bf16 columns
@@ -305,6 +301,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma_ts(tmem + T_DP, tmem + T_DV + ac, d_fq_mn + (uint64_t)(ks * 128), id_mf, true);
                 }
                 commit(bar(B_B));
+                if (k + 1 < nchunk) {  // group A (the only reader of V) completed before the mask
+                    load_tiles(k + 1, 2);
+                    ++issued[1];
+                }
                 // group C: dxhat (the dK epilogue starts on it), then the gradient sketch update under
                 // its own commit (the G conversion and the dO reload wait for that one)
                 if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
