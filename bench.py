@@ -70,6 +70,21 @@ def env_rank():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time per step (every rank receives it): replicas run the same
+    workload, so the job is done when the last one is."""
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tokens_per_s(world, tokens_per_rank, ms):
+    """Whole-job throughput of `world` replicas that each process `tokens_per_rank` tokens in
+    `ms` milliseconds (the max over ranks)."""
+    return world * tokens_per_rank / (ms / 1000.0)
+
+
 # ------------------------------------------------------------------ host oracle timing
 
 def oracle_sample_rate(w, target_s, cap_tokens=None):
@@ -261,12 +276,10 @@ def run_ours(args, w):
     race.race_attn_profile(False)
     prof = race.race_attn_profile_read()
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dist, dev)
 
     tokens = w.B * w.N
-    value = world * tokens / (ms / 1000.0)
+    value = weak_scaling_tokens_per_s(world, tokens, ms)
 
     # dominant kernel and its roofline
     roof = None
