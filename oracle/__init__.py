@@ -36,7 +36,7 @@ def lib():
                                           ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
         L.race_oracle_backward.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
                                            _vp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                                           ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _vp, _vp,
+                                           ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp,
                                            ctypes.c_int]
         for f in ("race_oracle_features", "race_oracle_readout_given_phi", "race_oracle_forward",
                   "race_oracle_backward"):
@@ -128,8 +128,9 @@ def forward(Q, K, V, W, beta, causal, normalize=True, rows=None, want_sketch=Fal
     return (O, sk) if want_sketch else O
 
 
-def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0):
-    """(dQ, dK, dV) for the output O and its cotangent dO; rows as in `forward`."""
+def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0, want_dbeta=False):
+    """(dQ, dK, dV) for the output O and its cotangent dO; rows as in `forward`.  With
+    want_dbeta also d(loss)/d(beta) per (b, h) [B, H], summed over every token."""
     Q, e = _tokens(Q)
     K, _ = _tokens(K)
     V, _ = _tokens(V)
@@ -143,7 +144,8 @@ def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0
     dQ = np.empty((B, H, nout, d))
     dK = np.empty((B, H, nout, d))
     dV = np.empty((B, H, nout, d))
+    db = np.zeros((B, H)) if want_dbeta else None
     _check(lib().race_oracle_backward(B, H, N, d, e, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(W),
                                       L, P, float(beta), int(causal), int(normalize), _ptr(r), nr,
-                                      _ptr(dQ), _ptr(dK), _ptr(dV), int(nthreads)), "backward")
-    return dQ, dK, dV
+                                      _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(db), int(nthreads)), "backward")
+    return (dQ, dK, dV, db) if want_dbeta else (dQ, dK, dV)

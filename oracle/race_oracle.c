@@ -134,6 +134,29 @@ static void features_backward(const double *x, const double *xhat, const double 
     for (int64_t k = 0; k < d; ++k) dx[k] = (dxhat[k] - xhat[k] * proj) / nrm;
 }
 
+/*
+ * d(loss)/d(beta) from one row's features: the logits are beta (u . v_r), so with the softmax
+ * gradient ds_r = phi_r (dphi_r - sum_r' phi_r' dphi_r') the row adds sum_l sum_r ds_r (u . v_r).
+ */
+static double features_dbeta(const double *u, const double *phi, const double *dphi, int L, int P)
+{
+    const int R = 1 << P;
+    double acc = 0.0;
+    for (int l = 0; l < L; ++l) {
+        const double *ph = phi + (int64_t)l * R;
+        const double *dph = dphi + (int64_t)l * R;
+        const double *ul = u + (int64_t)l * P;
+        double c = 0.0;
+        for (int r = 0; r < R; ++r) c += ph[r] * dph[r];
+        for (int r = 0; r < R; ++r) {
+            double uv = 0.0;
+            for (int t = 0; t < P; ++t) uv += ul[t] * vertex(r, t);
+            acc += ph[r] * (dph[r] - c) * uv;
+        }
+    }
+    return acc;
+}
+
 /* Sketch update with one key: S[j][c] += phi_j * v_c for the d value columns, S[j][d] += phi_j. */
 static void sketch_add(double *S, const double *phi, int64_t nfeat, const double *v, int64_t d)
 {
@@ -320,13 +343,15 @@ int race_oracle_forward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
  *   dphi_Q(i) = [A | B] [dnum_i ; dden_i]                         (sketch seen by query i),
  *   G = sum_i phi_Q(i) [dnum_i | dden_i]   (non-causal: all i; causal: suffix over i >= j),
  *   dV_j = G_A^T phi_K(j),   dphi_K(j) = G_A V_j + G_B,
- * followed by `features_backward` for each side.
+ * followed by `features_backward` for each side.  When `dbeta` is given (B * H values) every
+ * token's query and key features also contribute d(loss)/d(beta) (`features_dbeta`), whatever
+ * `rows` selects for dQ, dK, dV.
  */
 int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                          const void *Q, const void *K, const void *V, const void *dO,
                          const double *W, int L, int P, double beta, int causal, int normalize,
                          const int64_t *rows, int64_t nrows, double *dQ, double *dK, double *dV,
-                         int nthreads)
+                         double *dbeta, int nthreads)
 {
     if (check_args(B, H, N, d, elem, L, P, rows, nrows)) return -1;
     const int64_t R = (int64_t)1 << P, nfeat = (int64_t)L * R;
@@ -380,35 +405,47 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         for (int64_t c = 0; c < d; ++c) row[c] += phi[j] * dnum[c];
                         row[d] += phi[j] * dden;
                     }
-                    if (rows && (o >= nout || rows[o] != i)) continue;
+                    const int want = !rows || (o < nout && rows[o] == i);
+                    if (!want && !dbeta) continue;
                     for (int64_t j = 0; j < nfeat; ++j) {
                         const double *row = S + j * (d + 1);
                         double s = row[d] * dden;
                         for (int64_t c = 0; c < d; ++c) s += row[c] * dnum[c];
                         dphi[j] = s;
                     }
+                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P);
+                    if (!want) continue;
                     features_backward(x, xhat, u, phi, dphi, d, W, L, P, beta, normalize, dxhat, dx);
                     memcpy(dQbh + o * d, dx, sizeof(double) * d);
                     ++o;
                 }
-                /* key side on requested rows */
-                for (int64_t o2 = 0; o2 < nout; ++o2) {
-                    int64_t j0 = rows ? rows[o2] : o2;
+                /* key side on requested rows (every key when dbeta is wanted) */
+                int64_t o2 = 0;
+                for (int64_t j0 = 0; j0 < N; ++j0) {
+                    const int want = rows ? (o2 < nout && rows[o2] == j0) : 1;
+                    if (!want && !dbeta) {
+                        if (!rows || o2 >= nout) break;
+                        continue;
+                    }
                     load_row(K, elem, base + j0 * d, d, x);
                     features(x, d, W, L, P, beta, normalize, xhat, u, phi);
                     load_row(V, elem, base + j0 * d, d, v);
-                    for (int64_t c = 0; c < d; ++c) dVbh[o2 * d + c] = 0.0;
+                    if (want)
+                        for (int64_t c = 0; c < d; ++c) dVbh[o2 * d + c] = 0.0;
                     for (int64_t j = 0; j < nfeat; ++j) {
                         const double *row = G + j * (d + 1);
                         double s = row[d];
                         for (int64_t c = 0; c < d; ++c) {
-                            dVbh[o2 * d + c] += phi[j] * row[c];
+                            if (want) dVbh[o2 * d + c] += phi[j] * row[c];
                             s += row[c] * v[c];
                         }
                         dphi[j] = s;
                     }
+                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P);
+                    if (!want) continue;
                     features_backward(x, xhat, u, phi, dphi, d, W, L, P, beta, normalize, dxhat, dx);
                     memcpy(dKbh + o2 * d, dx, sizeof(double) * d);
+                    ++o2;
                 }
             } else {
                 /* forward order: prefix sketch S_t (Algorithm 2), den_t, dO_t . O_t, dQ */
@@ -426,7 +463,8 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                     for (int64_t c = 0; c < d; ++c) dOO += g[c] * (num[c] / den);
                     den_all[t] = den;
                     dOO_all[t] = dOO;
-                    if (rows && (o >= nout || rows[o] != t)) continue;
+                    const int want = !rows || (o < nout && rows[o] == t);
+                    if (!want && !dbeta) continue;
                     double dden = -dOO / den;
                     for (int64_t j = 0; j < nfeat; ++j) {
                         const double *row = S + j * (d + 1);
@@ -434,13 +472,15 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         for (int64_t c = 0; c < d; ++c) s += row[c] * (g[c] / den);
                         dphi[j] = s;
                     }
+                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P);
+                    if (!want) continue;
                     features_backward(x, xhat, u, phi, dphi, d, W, L, P, beta, normalize, dxhat, dx);
                     memcpy(dQbh + o * d, dx, sizeof(double) * d);
                     ++o;
                 }
                 /* reverse order: suffix sums G_j = sum_{t >= j} phi_Q(t) [dnum_t | dden_t], dK, dV */
                 int64_t o2 = nout - 1;
-                for (int64_t t = N - 1; t >= 0 && o2 >= 0; --t) {
+                for (int64_t t = N - 1; t >= 0 && (o2 >= 0 || dbeta); --t) {
                     load_row(Q, elem, base + t * d, d, x);
                     features(x, d, W, L, P, beta, normalize, xhat, u, phi);
                     load_row(dO, elem, base + t * d, d, g);
@@ -451,21 +491,25 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         for (int64_t c = 0; c < d; ++c) row[c] += phi[j] * dnum[c];
                         row[d] += phi[j] * dden;
                     }
-                    if (rows && rows[o2] != t) continue;
+                    const int want = rows ? (o2 >= 0 && rows[o2] == t) : 1;
+                    if (!want && !dbeta) continue;
                     int64_t slot = rows ? o2 : t;
                     load_row(K, elem, base + t * d, d, x);
                     features(x, d, W, L, P, beta, normalize, xhat, u, phi);
                     load_row(V, elem, base + t * d, d, v);
-                    for (int64_t c = 0; c < d; ++c) dVbh[slot * d + c] = 0.0;
+                    if (want)
+                        for (int64_t c = 0; c < d; ++c) dVbh[slot * d + c] = 0.0;
                     for (int64_t j = 0; j < nfeat; ++j) {
                         const double *row = G + j * (d + 1);
                         double s = row[d];
                         for (int64_t c = 0; c < d; ++c) {
-                            dVbh[slot * d + c] += phi[j] * row[c];
+                            if (want) dVbh[slot * d + c] += phi[j] * row[c];
                             s += row[c] * v[c];
                         }
                         dphi[j] = s;
                     }
+                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P);
+                    if (!want) continue;
                     features_backward(x, xhat, u, phi, dphi, d, W, L, P, beta, normalize, dxhat, dx);
                     memcpy(dKbh + slot * d, dx, sizeof(double) * d);
                     --o2;

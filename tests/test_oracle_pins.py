@@ -328,3 +328,41 @@ def test_zero_row_gradient_is_zero():
     W = _rand((2, 2, 8), 134)
     dQ, dK, _ = oracle.backward(Q, K, V, dO, W, 10.0, False)
     assert np.all(dQ[0, 0, 4] == 0) and np.all(dK[0, 0, 7] == 0)
+
+
+# ------------------------------------------------------------------ d(loss)/d(beta)
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("beta,P,L", [(10.0, 2, 2), (2.0, 3, 1), (5.0, 1, 3)])
+def test_dbeta_finite_differences(causal, beta, P, L):
+    """beta is trained with the layer ("RACE Attention" slides, "Soft corner assignments make
+    hashing differentiable"): d(sum O * dO)/d(beta) per (b, h) against central differences of the
+    independent product-form brute force (paper Eq. 3 with the implicit RACE kernel)."""
+    B, H, N, d = 1, 2, 10, 6
+    Q, K, V, dO = (_rand((B, H, N, d), s) for s in (140, 141, 142, 143))
+    W = _rand((L, P, d), 144)
+    *_, db = oracle.backward(Q, K, V, dO, W, beta, causal, want_dbeta=True)
+    h = 1e-6
+    for b in range(B):
+        for hh in range(H):
+            def loss(bt):
+                O = _attention_bruteforce(Q[b, hh], K[b, hh], V[b, hh], W, bt, causal)
+                return float((O * dO[b, hh]).sum())
+            fd = (loss(beta + h) - loss(beta - h)) / (2 * h)
+            assert abs(fd - db[b, hh]) <= 1e-6 * max(1.0, abs(fd)), (b, hh, fd, db[b, hh])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dbeta_sums_every_token_whatever_rows(causal):
+    """d(loss)/d(beta) covers every token even when only some rows' dQ, dK, dV are asked for, and
+    asking for it leaves dQ, dK, dV unchanged."""
+    Q, K, V, dO = (_rand((2, 1, 33, 8), s) for s in (150, 151, 152, 153))
+    W = _rand((3, 2, 8), 154)
+    full = oracle.backward(Q, K, V, dO, W, 7.0, causal, want_dbeta=True)
+    plain = oracle.backward(Q, K, V, dO, W, 7.0, causal)
+    rows = np.array([0, 5, 17, 32])
+    part = oracle.backward(Q, K, V, dO, W, 7.0, causal, rows=rows, want_dbeta=True)
+    np.testing.assert_array_equal(full[3], part[3])
+    for a, p, q in zip(full[:3], part[:3], plain):
+        np.testing.assert_array_equal(a, q)
+        np.testing.assert_array_equal(a[:, :, rows], p)
