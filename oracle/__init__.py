@@ -38,8 +38,11 @@ def lib():
                                            _vp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp,
                                            ctypes.c_int]
+        L.race_oracle_decode_step.argtypes = [_i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                              _vp, _vp]
         for f in ("race_oracle_features", "race_oracle_readout_given_phi", "race_oracle_forward",
-                  "race_oracle_backward"):
+                  "race_oracle_backward", "race_oracle_decode_step"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -149,3 +152,20 @@ def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0
                                       L, P, float(beta), int(causal), int(normalize), _ptr(r), nr,
                                       _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(db), int(nthreads)), "backward")
     return (dQ, dK, dV, db) if want_dbeta else (dQ, dK, dV)
+
+
+def decode_step(q, k, v, W, beta, state, normalize=True):
+    """One causal decode step per (b, h): state [B, H, L*R, d+1] float64 (updated in place) gains
+    key k / value v, then query q reads it.  q, k, v: [B, H, d].  Returns o [B, H, d]."""
+    q, e = _tokens(q)
+    k, e2 = _tokens(k)
+    v, e3 = _tokens(v)
+    assert e == e2 == e3 and q.shape == k.shape == v.shape and q.ndim == 3
+    W = _f64(W)
+    B, H, d = q.shape
+    L, P, _ = W.shape
+    assert state.dtype == np.float64 and state.flags.c_contiguous and state.shape == (B, H, L << P, d + 1)
+    o = np.empty((B, H, d))
+    _check(lib().race_oracle_decode_step(B, H, d, e, _ptr(q), _ptr(k), _ptr(v), _ptr(W), L, P, float(beta),
+                                         int(normalize), _ptr(state), _ptr(o)), "decode_step")
+    return o

@@ -265,6 +265,42 @@ static int check_args(int64_t B, int64_t H, int64_t N, int64_t d, int elem, int 
 }
 
 /*
+ * One causal decode step per (b, h) (the recurrent form of paper Algorithm 2, "Causality is a
+ * prefix update of the same statistics"): the new key is added to the prefix sketch, then the
+ * new query reads it.  q, k, v: [B, H, d] of element type `elem`; S: [B, H, L*R, d+1] float64,
+ * updated in place (zeros for an empty prefix, or the non-causal sketch [A | B] of a prefix);
+ * o: [B, H, d] float64.
+ */
+int race_oracle_decode_step(int64_t B, int64_t H, int64_t d, int elem, const void *q, const void *k,
+                            const void *v, const double *W, int L, int P, double beta, int normalize,
+                            double *S, double *o)
+{
+    if (check_args(B, H, 1, d, elem, L, P, NULL, 0)) return -1;
+    const int64_t R = (int64_t)1 << P, nfeat = (int64_t)L * R;
+    double *x = malloc(sizeof(double) * d), *xhat = malloc(sizeof(double) * d);
+    double *vv = malloc(sizeof(double) * d), *num = malloc(sizeof(double) * d);
+    double *u = malloc(sizeof(double) * L * P), *phi = malloc(sizeof(double) * nfeat);
+    int status = 0;
+    if (!x || !xhat || !vv || !num || !u || !phi) {
+        status = -2;
+    } else {
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            double *Sbh = S + bh * nfeat * (d + 1);
+            load_row(k, elem, bh * d, d, x);
+            features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+            load_row(v, elem, bh * d, d, vv);
+            sketch_add(Sbh, phi, nfeat, vv, d);
+            load_row(q, elem, bh * d, d, x);
+            features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+            double den = sketch_read(Sbh, phi, nfeat, d, num);
+            for (int64_t c = 0; c < d; ++c) o[bh * d + c] = num[c] / den;
+        }
+    }
+    free(x); free(xhat); free(vv); free(num); free(u); free(phi);
+    return status;
+}
+
+/*
  * Forward pass.  Q, K, V: [B, H, N, d] of element type `elem`; W: [L, P, d] float64.
  * rows == NULL: O is [B, H, N, d].  Otherwise O is [B, H, nrows, d] and holds only the listed
  * token rows (strictly increasing, the same for every (b, h)).

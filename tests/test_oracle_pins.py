@@ -366,3 +366,38 @@ def test_dbeta_sums_every_token_whatever_rows(causal):
     for a, p, q in zip(full[:3], part[:3], plain):
         np.testing.assert_array_equal(a, q)
         np.testing.assert_array_equal(a[:, :, rows], p)
+
+
+# ------------------------------------------------------------------ causal decode step
+
+@pytest.mark.parametrize("P,L", [(2, 2), (3, 3)])
+def test_decode_steps_reproduce_the_causal_forward(P, L):
+    """Algorithm 2 is a recurrence ("Causality is a prefix update of the same statistics"): adding
+    one key at a time to an empty prefix sketch and reading with the same token's query gives the
+    causal forward, row for row (the same sums in the same order: bit for bit)."""
+    B, H, N, d = 2, 2, 23, 8
+    Q, K, V = (_rand((B, H, N, d), s) for s in (160, 161, 162))
+    W = _rand((L, P, d), 163)
+    ref = oracle.forward(Q, K, V, W, 10.0, True)
+    state = np.zeros((B, H, L << P, d + 1))
+    for t in range(N):
+        o = oracle.decode_step(Q[:, :, t], K[:, :, t], V[:, :, t], W, 10.0, state)
+        np.testing.assert_array_equal(o, ref[:, :, t])
+
+
+def test_decode_continues_a_prefill_sketch():
+    """The state after a prompt is the prompt's non-causal sketch [A | B] (the sum over its keys),
+    so decoding on from it matches the causal forward of prompt + continuation; the independent
+    product-form brute force checks the same rows."""
+    B, H, N0, N, d, P, L = 1, 2, 15, 21, 8, 3, 2
+    Q, K, V = (_rand((B, H, N, d), s) for s in (170, 171, 172))
+    W = _rand((L, P, d), 173)
+    _, state = oracle.forward(Q[:, :, :N0], K[:, :, :N0], V[:, :, :N0], W, 10.0, False, want_sketch=True)
+    state = np.ascontiguousarray(state)
+    ref = oracle.forward(Q, K, V, W, 10.0, True)
+    for t in range(N0, N):
+        o = oracle.decode_step(Q[:, :, t], K[:, :, t], V[:, :, t], W, 10.0, state)
+        np.testing.assert_allclose(o, ref[:, :, t], rtol=1e-12, atol=1e-12)
+        for h in range(H):
+            bf = _attention_bruteforce(Q[0, h, :t + 1], K[0, h, :t + 1], V[0, h, :t + 1], W, 10.0, True)[-1]
+            np.testing.assert_allclose(o[0, h], bf, rtol=1e-10, atol=1e-12)
