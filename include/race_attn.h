@@ -124,6 +124,20 @@ int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, const void *K,
                           void *stream);
 
 /*
+ * One causal decode step per (batch, head): the recurrent form of paper Algorithm 2 ("RACE
+ * Attention" slides, frame "Causality is a prefix update of the same statistics").  For every
+ * (b, h) the new key k is added to the head's prefix sketch and the new query q reads it:
+ *     state[b,h] += phi(k) [v | 1],     o = phi(q) . state[b,h][:, :d] / phi(q) . state[b,h][:, d]
+ * shape: N must be 1; q, k, v, o are [B, H, 1, d] of shape->dtype (16-byte aligned).
+ * state: float32 [B, H, L * 2^P, d + 1], read and updated in place; race_attn_state_bytes(shape,
+ * L, P, 0) bytes.  Zeros start an empty prefix; the `state` that race_attn_fwd with causal = 0
+ * fills for a prompt's K and V is the sketch of that prompt, so decoding continues from it.
+ * Limits as above (L * P <= 64 follows from them).  No workspace; nothing is allocated.
+ */
+int race_attn_decode(const race_shape *shape, const void *q, const void *k, const void *v,
+                     const float *W, float beta, int L, int P, void *state, void *o, void *stream);
+
+/*
  * Device-side status of the last race_attn_fwd / race_attn_bwd call that used `workspace`.
  * Kernels that wait for asynchronous (bulk) copies bound every wait; if a wait runs out they
  * record it in the first word of the workspace and return early, leaving their outputs

@@ -60,6 +60,8 @@ def load_library():
     L.race_attn_bwd.restype = i
     L.race_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp]
     L.race_attn_fwd_noalloc.restype = i
+    L.race_attn_decode.argtypes = [shp, vp, vp, vp, vp, f, i, i, vp, vp, vp]
+    L.race_attn_decode.restype = i
     L.race_attn_status.argtypes = [vp, vp]
     L.race_attn_status.restype = i
     L.race_attn_strerror.argtypes = [i]
@@ -213,6 +215,26 @@ def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, 
     if rc != 0:
         raise RaceAttnError(rc, "race_attn_bwd")
     return dQ, dK, dV
+
+
+def race_attn_decode(q, k, v, W, beta, L, P, state, o=None, stream=None):
+    """One causal decode step: q, k, v [B, H, 1, d] (float32 or bfloat16, CUDA); state float32
+    [B, H, L * 2^P, d + 1] (updated in place).  Returns o [B, H, 1, d]."""
+    shape = _shape_of(q)
+    for n, t in (("k", k), ("v", v), ("q", q)):
+        _check_like(n, t, q)
+    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, q.shape[3]) or not W.is_contiguous():
+        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
+    want = (q.shape[0], q.shape[1], L << P, q.shape[3] + 1)
+    if state.dtype != torch.float32 or tuple(state.shape) != want or not state.is_contiguous():
+        raise ValueError("state must be a contiguous float32 tensor of shape %s" % (want,))
+    o = torch.empty_like(q) if o is None else o
+    _check_like("o", o, q)
+    rc = load_library().race_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(W), float(beta),
+                                         int(L), int(P), _ptr(state), _ptr(o), _stream(stream))
+    if rc != 0:
+        raise RaceAttnError(rc, "race_attn_decode")
+    return o
 
 
 def race_attn_fwd_noalloc(Q, K, V, W, beta, L, P, causal, O=None, stream=None):

@@ -398,6 +398,29 @@ const char *race_attn_strerror(int status)
     }
 }
 
+int race_attn_decode(const race_shape *shape, const void *q, const void *k, const void *v, const float *W,
+                     float beta, int L, int P, void *state, void *o, void *stream)
+{
+    Plan pl;
+    int rc = make_plan(shape, L, P, 0, pl);
+    if (rc != RACE_OK) return rc;
+    if (shape->N != 1 || check_beta(beta) != RACE_OK) return RACE_ERR_INVALID_ARG;
+    if (!q || !k || !v || !W || !state || !o) return RACE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(W) || !aligned16(state) || !aligned16(o))
+        return RACE_ERR_ALIGN;
+    if (!decode_supported(pl.D)) return RACE_ERR_UNSUPPORTED;
+    Dims D = pl.D;
+    D.beta = beta;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (pl.bf16)
+        RACE_TRY(launch_decode<bf16_t>(D, (const bf16_t *)q, (const bf16_t *)k, (const bf16_t *)v, W, (float *)state,
+                                       (bf16_t *)o, st));
+    else
+        RACE_TRY(launch_decode<float>(D, (const float *)q, (const float *)k, (const float *)v, W, (float *)state,
+                                      (float *)o, st));
+    return RACE_OK;
+}
+
 int race_attn_status(const void *workspace, void *stream)
 {
     if (!workspace) return RACE_ERR_INVALID_ARG;

@@ -23,6 +23,12 @@ cudaError_t launch_kernel(const char *name, Kern k, dim3 grid, dim3 block, size_
     return e;
 }
 
+// ---------------------------------------------------------------- causal decode step
+bool decode_supported(const Dims &D);
+template <typename T>
+cudaError_t launch_decode(const Dims &D, const T *q, const T *k, const T *v, const float *W, float *S, T *o,
+                          cudaStream_t st);
+
 // ---------------------------------------------------------------- CUDA-core kernels
 enum class GenericKernel { Sketch, Readout, QueryBwd, KeyBwd, CausalFwd, CausalBwd };
 size_t generic_smem_bytes(const Dims &D, GenericKernel which);

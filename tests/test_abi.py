@@ -100,6 +100,21 @@ def test_bwd_rejects_before_launch(lib):
                None) == -5
 
 
+def test_decode_rejects_before_launch(lib):
+    """The decode step takes one token per (b, h): N must be 1; null, misaligned or out-of-range
+    arguments are refused without a launch."""
+    L = _raw(lib)
+    s = shape(lib)  # N > 1
+    one = lib.make_shape(s.B, s.H, 1, s.d, s.dtype)
+    p = ctypes.c_void_p(4096)
+    dec = lambda *a: L.race_attn_decode(*a)
+    assert dec(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, p, p, None) == -1
+    assert dec(ctypes.byref(one), p, None, p, p, 10.0, 3, 3, p, p, None) == -1
+    assert dec(ctypes.byref(one), p, p, p, p, float("inf"), 3, 3, p, p, None) == -1
+    assert dec(ctypes.byref(one), p, p, p, p, 10.0, 3, 3, ctypes.c_void_p(4100), p, None) == -5
+    assert dec(None, p, p, p, p, 10.0, 3, 3, p, p, None) == -1
+
+
 def test_strerror(lib):
     assert lib.race_attn_strerror(0) == "ok"
     for rc in (-1, -2, -3, -4, -5):

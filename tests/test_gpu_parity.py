@@ -167,6 +167,54 @@ def test_noncausal_sketch_state(w):
             assert e <= 1e-2, "%s sketch (%d, %d) error %.3e" % (w.name, b, h, e)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_steps_match_oracle(dtype):
+    """Causal decode, one token per call from an empty prefix (the recurrence of Algorithm 2,
+    "Causality is a prefix update of the same statistics"), against the oracle's decode step on
+    the same inputs: every step's output and the final sketch."""
+    w = W_("decode", 2, 3, 40, 64, 3, 2, True, dtype)
+    inp = inputs_on_gpu(w, seed=11)
+    Q, K, V, W = inp["Q"], inp["K"], inp["V"], inp["W"]
+    B, H, N, d = Q.shape
+    LR = w.L << w.P
+    state = torch.zeros((B, H, LR, d + 1), dtype=torch.float32, device="cuda")
+    ref_state = np.zeros((B, H, LR, d + 1))
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V")}
+    Wd = W.double().cpu().numpy()
+    tol = 2e-5 if dtype == "f32" else 1e-2
+    for t in range(N):
+        tok = [x[:, :, t:t + 1].contiguous() for x in (Q, K, V)]
+        o = race.race_attn_decode(*tok, W, w.beta, w.L, w.P, state)
+        ref = oracle.decode_step(a["Q"][:, :, t], a["K"][:, :, t], a["V"][:, :, t], Wd, w.beta, ref_state)
+        got = o[:, :, 0].double().cpu().numpy()
+        assert np.abs(got - ref).max() <= tol * np.abs(ref).max(), t
+    got_state = state.double().cpu().numpy()
+    assert np.abs(got_state - ref_state).max() <= 1e-5 * np.abs(ref_state).max()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_after_prefill(dtype):
+    """The state race_attn_fwd (causal = 0) leaves for a prompt is the prompt's sketch; decoding
+    on from it gives the causal forward of prompt + continuation (oracle rows)."""
+    w = W_("prefill", 1, 2, 60, 64, 3, 3, True, dtype)
+    inp = inputs_on_gpu(w, seed=12)
+    Q, K, V, W = inp["Q"], inp["K"], inp["V"], inp["W"]
+    B, H, N, d = Q.shape
+    N0, LR = 45, w.L << w.P
+    pre = [x[:, :, :N0].contiguous() for x in (Q, K, V)]
+    shape = race.make_shape(B, H, N0, d, w.torch_dtype)
+    raw = torch.empty(race.race_attn_state_bytes(shape, w.L, w.P, False), dtype=torch.uint8, device="cuda")
+    race.race_attn_fwd(*pre, W, w.beta, w.L, w.P, False, state=raw)
+    state = raw.view(torch.float32).view(B, H, LR, d + 1)
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V")}
+    ref = oracle.forward(a["Q"], a["K"], a["V"], W.double().cpu().numpy(), w.beta, True)
+    tol = 1e-5 if dtype == "f32" else 2e-2
+    for t in range(N0, N):
+        tok = [x[:, :, t:t + 1].contiguous() for x in (Q, K, V)]
+        o = race.race_attn_decode(*tok, W, w.beta, w.L, w.P, state)[:, :, 0].double().cpu().numpy()
+        assert np.abs(o - ref[:, :, t]).max() <= tol * np.abs(ref[:, :, t]).max(), t
+
+
 def _sampled_rows(N, n, seed):
     rng = np.random.default_rng(seed)
     rows = set(rng.choice(N, size=n, replace=False).tolist())
