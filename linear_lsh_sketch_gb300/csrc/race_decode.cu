@@ -8,9 +8,10 @@
 //
 // One CTA per (b, h).  The block normalises q and k, projects them (u = tanh(W xhat)) and forms
 // their bucket probabilities in the product form phi_r = prod_t sigmoid(2 beta u_t v_{r,t}) (equal
-// to the softmax over the 2^P corners); then thread c owns sketch column c (c <= d), adds the key
-// row by row, writes the column back and accumulates the read-out.  fp32 throughout; the work per
-// step is one pass over the sketch, so a decode batch is bound by reading and writing it.
+// to the softmax over the 2^P corners); then the 8 warps split the sketch rows (lanes on
+// consecutive columns), add the key, write the rows back and accumulate partial read-outs that a
+// fixed-order shared-memory sum combines.  fp32 throughout; the work per step is one pass over
+// the sketch, so a decode batch is bound by reading and writing it.
 #include "race_launch.h"
 
 namespace race {
@@ -66,20 +67,44 @@ __global__ void __launch_bounds__(NT) k_decode(const T *__restrict__ q, const T 
         ph[side][j] = pr;
     }
     __syncthreads();
-    float acc = 0.f;
-    const int c = tid;
-    if (c <= d) {
-        float *col = S + bh * (int64_t)LR * (d + 1) + c;
-        const float vc = c < d ? ld_f(v, bh * d + c) : 1.f;
-        for (int j = 0; j < LR; ++j) {
-            const float s = fmaf(ph[1][j], vc, col[(int64_t)j * (d + 1)]);
-            col[(int64_t)j * (d + 1)] = s;
-            acc = fmaf(ph[0][j], s, acc);
+    // warp w takes sketch rows w, w + 8, ...; lane l columns l, l + 32, ... (up to 5 of the d + 1):
+    // all of a thread's loads are independent, and each warp's accesses to a row are contiguous
+    constexpr int NW = NT / 32, CPL = (MAXD + 1 + 31) / 32;
+    float acc[CPL], vc[CPL];
+#pragma unroll
+    for (int m = 0; m < CPL; ++m) {
+        const int c = lane + 32 * m;
+        acc[m] = 0.f;
+        vc[m] = c < d ? ld_f(v, bh * d + c) : 1.f;
+    }
+    float *Sbh = S + bh * (int64_t)LR * (d + 1);
+    for (int j = warp; j < LR; j += NW) {
+        float *row = Sbh + (int64_t)j * (d + 1);
+        const float pk = ph[1][j], pq = ph[0][j];
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+            const int c = lane + 32 * m;
+            if (c <= d) {
+                const float sv = fmaf(pk, vc[m], row[c]);
+                row[c] = sv;
+                acc[m] = fmaf(pq, sv, acc[m]);
+            }
         }
-        if (c == d) den_s = acc;
+    }
+    // per-warp partial read-outs -> column sums (fixed order over the warps)
+    __shared__ float part[NW][CPL * 32];
+#pragma unroll
+    for (int m = 0; m < CPL; ++m) part[warp][lane + 32 * m] = acc[m];
+    __syncthreads();
+    if (tid <= d) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) sum += part[w][tid];
+        if (tid == d) den_s = sum;
+        part[0][tid] = sum;
     }
     __syncthreads();
-    if (c < d) st_f(o, bh * d + c, acc / den_s);
+    if (tid < d) st_f(o, bh * d + tid, part[0][tid] / den_s);
 }
 
 }  // namespace dec
