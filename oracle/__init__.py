@@ -6,7 +6,10 @@ package. It shares no code with the GPU library and the GPU library never calls 
 Sources: "RACE Attention" slides (paper Algorithm 1, frames "Soft corner assignments make
 hashing differentiable", "Each bucket stores mass and a weighted value sum", "Normalize after
 combining the tables"; paper Algorithm 2, frame "Causality is a prefix update of the same
-statistics") and the reading notes, sections 2.4-2.6.  The C source states every step.
+statistics") and the reading notes, sections 2.4-2.6; the hard-hash limit and the angular kernel
+it collides with (frames "A hash collision estimates a powered angular kernel" and "Choose a
+nonnegative kernel that can be sketched"; reading notes 2.3 and 3.1).  The C source states every
+step.
 """
 import ctypes
 import os
@@ -32,17 +35,20 @@ def lib():
         L.race_oracle_readout_given_phi.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
                                                     _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp]
         L.race_oracle_forward.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
-                                          ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                                          ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                          ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
         L.race_oracle_backward.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
-                                           _vp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                           _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp,
                                            ctypes.c_int]
         L.race_oracle_decode_step.argtypes = [_i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
-                                              ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                                              _vp, _vp]
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                              ctypes.c_int, _vp, _vp]
+        L.race_oracle_angular_forward.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp,
+                                                  ctypes.c_double, ctypes.c_int, _vp, _i64, _vp,
+                                                  ctypes.c_int]
         for f in ("race_oracle_features", "race_oracle_readout_given_phi", "race_oracle_forward",
-                  "race_oracle_backward", "race_oracle_decode_step"):
+                  "race_oracle_backward", "race_oracle_decode_step", "race_oracle_angular_forward"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -73,8 +79,19 @@ def _check(status, what):
         raise ValueError("%s failed with status %d" % (what, status))
 
 
+def _hash(W, H):
+    """Hyperplanes as (float64 array, per_head, L, P): W is [L, P, d] shared by every head, or
+    [H, L, P, d], one set per head."""
+    W = _f64(W)
+    if W.ndim == 3:
+        return W, 0, W.shape[0], W.shape[1]
+    assert W.ndim == 4 and W.shape[0] == H, "W must be [L, P, d] or [H, L, P, d]"
+    return W, 1, W.shape[1], W.shape[2]
+
+
 def features(X, W, beta, normalize=True):
-    """Bucket probabilities of rows X [M, d] for W [L, P, d]: returns (phi [M, L, R], u [M, L, P])."""
+    """Bucket probabilities of rows X [M, d] for W [L, P, d]: returns (phi [M, L, R], u [M, L, P]).
+    beta = inf gives the hard hash (one corner per table; a zero projection splits evenly)."""
     X = _f64(X)
     W = _f64(W)
     M, d = X.shape
@@ -113,19 +130,19 @@ def _rows(rows):
 
 
 def forward(Q, K, V, W, beta, causal, normalize=True, rows=None, want_sketch=False, nthreads=0):
-    """O for Q, K, V [B, H, N, d] (float64/float32/bf16-bits). rows: sorted token rows to output."""
+    """O for Q, K, V [B, H, N, d] (float64/float32/bf16-bits). rows: sorted token rows to output.
+    W: [L, P, d] shared, or [H, L, P, d] per head.  beta = inf: hard hashing."""
     Q, e = _tokens(Q)
     K, e2 = _tokens(K)
     V, e3 = _tokens(V)
     assert e == e2 == e3 and Q.shape == K.shape == V.shape
-    W = _f64(W)
     B, H, N, d = Q.shape
-    L, P, _ = W.shape
+    W, ph, L, P = _hash(W, H)
     r, nr = _rows(rows)
     nout = nr if r is not None else N
     O = np.empty((B, H, nout, d))
     sk = np.empty((B, H, L << P, d + 1)) if (want_sketch and not causal) else None
-    _check(lib().race_oracle_forward(B, H, N, d, e, _ptr(Q), _ptr(K), _ptr(V), _ptr(W), L, P,
+    _check(lib().race_oracle_forward(B, H, N, d, e, _ptr(Q), _ptr(K), _ptr(V), _ptr(W), ph, L, P,
                                      float(beta), int(causal), int(normalize), _ptr(r), nr,
                                      _ptr(O), _ptr(sk), int(nthreads)), "forward")
     return (O, sk) if want_sketch else O
@@ -133,15 +150,15 @@ def forward(Q, K, V, W, beta, causal, normalize=True, rows=None, want_sketch=Fal
 
 def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0, want_dbeta=False):
     """(dQ, dK, dV) for the output O and its cotangent dO; rows as in `forward`.  With
-    want_dbeta also d(loss)/d(beta) per (b, h) [B, H], summed over every token."""
+    want_dbeta also d(loss)/d(beta) per (b, h) [B, H], summed over every token.  W and beta as in
+    `forward` (a hard hash passes no gradient to Q and K)."""
     Q, e = _tokens(Q)
     K, _ = _tokens(K)
     V, _ = _tokens(V)
     dO, e4 = _tokens(dO)
     assert e == e4
-    W = _f64(W)
     B, H, N, d = Q.shape
-    L, P, _ = W.shape
+    W, ph, L, P = _hash(W, H)
     r, nr = _rows(rows)
     nout = nr if r is not None else N
     dQ = np.empty((B, H, nout, d))
@@ -149,7 +166,7 @@ def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0
     dV = np.empty((B, H, nout, d))
     db = np.zeros((B, H)) if want_dbeta else None
     _check(lib().race_oracle_backward(B, H, N, d, e, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(W),
-                                      L, P, float(beta), int(causal), int(normalize), _ptr(r), nr,
+                                      ph, L, P, float(beta), int(causal), int(normalize), _ptr(r), nr,
                                       _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(db), int(nthreads)), "backward")
     return (dQ, dK, dV, db) if want_dbeta else (dQ, dK, dV)
 
@@ -161,11 +178,26 @@ def decode_step(q, k, v, W, beta, state, normalize=True):
     k, e2 = _tokens(k)
     v, e3 = _tokens(v)
     assert e == e2 == e3 and q.shape == k.shape == v.shape and q.ndim == 3
-    W = _f64(W)
     B, H, d = q.shape
-    L, P, _ = W.shape
+    W, ph, L, P = _hash(W, H)
     assert state.dtype == np.float64 and state.flags.c_contiguous and state.shape == (B, H, L << P, d + 1)
     o = np.empty((B, H, d))
-    _check(lib().race_oracle_decode_step(B, H, d, e, _ptr(q), _ptr(k), _ptr(v), _ptr(W), L, P, float(beta),
+    _check(lib().race_oracle_decode_step(B, H, d, e, _ptr(q), _ptr(k), _ptr(v), _ptr(W), ph, L, P, float(beta),
                                          int(normalize), _ptr(state), _ptr(o)), "decode_step")
     return o
+
+
+def angular_forward(Q, K, V, gamma, causal, rows=None, nthreads=0):
+    """Angular attention O_i = sum_j S_ij V_j / sum_j S_ij with S_ij = (1 - theta_ij / pi)^gamma
+    (j <= i when causal), O(N^2): the kernel a gamma-bit hard hash collides with."""
+    Q, e = _tokens(Q)
+    K, e2 = _tokens(K)
+    V, e3 = _tokens(V)
+    assert e == e2 == e3 and Q.shape == K.shape == V.shape
+    B, H, N, d = Q.shape
+    r, nr = _rows(rows)
+    O = np.empty((B, H, nr if r is not None else N, d))
+    _check(lib().race_oracle_angular_forward(B, H, N, d, e, _ptr(Q), _ptr(K), _ptr(V), float(gamma),
+                                             int(causal), _ptr(r), nr, _ptr(O), int(nthreads)),
+           "angular_forward")
+    return O

@@ -22,6 +22,14 @@
  *  - Naming: A = Phi_K^T V (content, R x d) and B = Phi_K^T 1 (mass, R); the packed per-table
  *    sketch is [A | B], R rows of d+1 numbers.  The 1/L factors cancel in the ratio.
  *  - The backward pass is the chain rule through these steps (the pages print none).
+ *  - beta = +infinity is the hard-hashing limit the slides name ("beta -> infinity: hard
+ *    hashing"; reading notes 2.3): each bit is the sign of the projection, so a row falls in one
+ *    corner with probability 1.  A projection that is exactly zero keeps the limit of the soft
+ *    bit, sigma(0) = 1/2, so it splits the row's mass evenly over both corners (a zero row is
+ *    uniform over all R).  Gradients through the hash are zero there (the limit of the soft
+ *    gradient away from ties); values still receive theirs.
+ *  - W is either one [L, P, d] array shared by every head, or one per head, [H, L, P, d] (the
+ *    pages are silent on this; `per_head` selects it).
  *
  * Element types of the token tensors: 0 = float64, 1 = float32, 2 = bfloat16 (raw 16-bit
  * patterns).  Every value is widened exactly to double before use.
@@ -77,6 +85,19 @@ static void features(const double *x, int64_t d, const double *W, int L, int P, 
             for (int64_t k = 0; k < d; ++k) z += w[k] * xhat[k];
             ul[t] = tanh(z);
         }
+        if (isinf(beta) && beta > 0) {
+            /* hard hash: corner r takes the row iff every coordinate of v_r has the sign of u
+             * (tanh keeps the sign of z); a zero coordinate halves the mass of both corners */
+            for (int r = 0; r < R; ++r) {
+                double pr = 1.0;
+                for (int t = 0; t < P; ++t) {
+                    if (ul[t] == 0.0) pr *= 0.5;
+                    else if ((ul[t] > 0.0) != (vertex(r, t) > 0.0)) pr = 0.0;
+                }
+                phi[(int64_t)l * R + r] = pr;
+            }
+            continue;
+        }
         /* beta-sharpened softmax over the R corners v_r of the hypercube */
         double m = -INFINITY;
         for (int r = 0; r < R; ++r) {
@@ -111,7 +132,7 @@ static void features_backward(const double *x, const double *xhat, const double 
         for (int t = 0; t < P; ++t) {
             double du = 0.0;
             for (int r = 0; r < R; ++r) du += ph[r] * (dph[r] - c) * vertex(r, t);
-            du *= beta;
+            du = isinf(beta) ? 0.0 : du * beta;  /* a hard hash passes no gradient */
             double ut = u[(int64_t)l * P + t];
             double dz = du * (1.0 - ut * ut);
             const double *w = W + ((int64_t)l * P + t) * d;
@@ -138,10 +159,12 @@ static void features_backward(const double *x, const double *xhat, const double 
  * d(loss)/d(beta) from one row's features: the logits are beta (u . v_r), so with the softmax
  * gradient ds_r = phi_r (dphi_r - sum_r' phi_r' dphi_r') the row adds sum_l sum_r ds_r (u . v_r).
  */
-static double features_dbeta(const double *u, const double *phi, const double *dphi, int L, int P)
+static double features_dbeta(const double *u, const double *phi, const double *dphi, int L, int P,
+                            double beta)
 {
     const int R = 1 << P;
     double acc = 0.0;
+    if (isinf(beta)) return 0.0;  /* saturated corners: the limit of the soft sum is zero */
     for (int l = 0; l < L; ++l) {
         const double *ph = phi + (int64_t)l * R;
         const double *dph = dphi + (int64_t)l * R;
@@ -272,8 +295,8 @@ static int check_args(int64_t B, int64_t H, int64_t N, int64_t d, int elem, int 
  * o: [B, H, d] float64.
  */
 int race_oracle_decode_step(int64_t B, int64_t H, int64_t d, int elem, const void *q, const void *k,
-                            const void *v, const double *W, int L, int P, double beta, int normalize,
-                            double *S, double *o)
+                            const void *v, const double *W, int per_head, int L, int P, double beta,
+                            int normalize, double *S, double *o)
 {
     if (check_args(B, H, 1, d, elem, L, P, NULL, 0)) return -1;
     const int64_t R = (int64_t)1 << P, nfeat = (int64_t)L * R;
@@ -286,12 +309,13 @@ int race_oracle_decode_step(int64_t B, int64_t H, int64_t d, int elem, const voi
     } else {
         for (int64_t bh = 0; bh < B * H; ++bh) {
             double *Sbh = S + bh * nfeat * (d + 1);
+            const double *Wh = W + (per_head ? (bh % H) * (int64_t)L * P * d : 0);
             load_row(k, elem, bh * d, d, x);
-            features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+            features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
             load_row(v, elem, bh * d, d, vv);
             sketch_add(Sbh, phi, nfeat, vv, d);
             load_row(q, elem, bh * d, d, x);
-            features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+            features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
             double den = sketch_read(Sbh, phi, nfeat, d, num);
             for (int64_t c = 0; c < d; ++c) o[bh * d + c] = num[c] / den;
         }
@@ -301,14 +325,15 @@ int race_oracle_decode_step(int64_t B, int64_t H, int64_t d, int elem, const voi
 }
 
 /*
- * Forward pass.  Q, K, V: [B, H, N, d] of element type `elem`; W: [L, P, d] float64.
+ * Forward pass.  Q, K, V: [B, H, N, d] of element type `elem`; W: [L, P, d] float64, or
+ * [H, L, P, d] with `per_head` (head h hashes with W[h]).
  * rows == NULL: O is [B, H, N, d].  Otherwise O is [B, H, nrows, d] and holds only the listed
  * token rows (strictly increasing, the same for every (b, h)).
  * sketch (nullable, non-causal only): the final [A | B] per (b, h), [B, H, L*R, d+1].
  */
 int race_oracle_forward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         const void *Q, const void *K, const void *V, const double *W,
-                        int L, int P, double beta, int causal, int normalize,
+                        int per_head, int L, int P, double beta, int causal, int normalize,
                         const int64_t *rows, int64_t nrows, double *O, double *sketch,
                         int nthreads)
 {
@@ -332,18 +357,19 @@ int race_oracle_forward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
             status = -2;
         } else {
             const int64_t base = bh * N * d;
+            const double *Wh = W + (per_head ? (bh % H) * (int64_t)L * P * d : 0);
             double *Obh = O + bh * nout * d;
             if (!causal) {
                 for (int64_t j = 0; j < N; ++j) {
                     load_row(K, elem, base + j * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     load_row(V, elem, base + j * d, d, v);
                     sketch_add(S, phi, nfeat, v, d);
                 }
                 for (int64_t o = 0; o < nout; ++o) {
                     int64_t i = rows ? rows[o] : o;
                     load_row(Q, elem, base + i * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     double den = sketch_read(S, phi, nfeat, d, num);
                     for (int64_t c = 0; c < d; ++c) Obh[o * d + c] = num[c] / den;
                 }
@@ -353,12 +379,12 @@ int race_oracle_forward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                 for (int64_t t = 0; t < N && o < nout; ++t) {
                     /* Algorithm 2: add key t to the prefix sketch, then read it with query t */
                     load_row(K, elem, base + t * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     load_row(V, elem, base + t * d, d, v);
                     sketch_add(S, phi, nfeat, v, d);
                     if (rows && rows[o] != t) continue;
                     load_row(Q, elem, base + t * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     double den = sketch_read(S, phi, nfeat, d, num);
                     for (int64_t c = 0; c < d; ++c) Obh[o * d + c] = num[c] / den;
                     ++o;
@@ -371,7 +397,8 @@ int race_oracle_forward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
 }
 
 /*
- * Backward pass of the loss-free output O: given dO, returns dQ, dK, dV (float64).
+ * Backward pass of the loss-free output O: given dO, returns dQ, dK, dV (float64); W as in
+ * `race_oracle_forward`.
  * rows == NULL: all [B, H, N, d].  Otherwise only the listed rows, [B, H, nrows, d].
  *
  * Chain rule (O_i = num_i / den_i):
@@ -385,7 +412,8 @@ int race_oracle_forward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
  */
 int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                          const void *Q, const void *K, const void *V, const void *dO,
-                         const double *W, int L, int P, double beta, int causal, int normalize,
+                         const double *W, int per_head, int L, int P, double beta, int causal,
+                         int normalize,
                          const int64_t *rows, int64_t nrows, double *dQ, double *dK, double *dV,
                          double *dbeta, int nthreads)
 {
@@ -416,12 +444,13 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
             status = -2;
         } else {
             const int64_t base = bh * N * d;
+            const double *Wh = W + (per_head ? (bh % H) * (int64_t)L * P * d : 0);
             double *dQbh = dQ + bh * nout * d, *dKbh = dK + bh * nout * d, *dVbh = dV + bh * nout * d;
             if (!causal) {
                 /* sketch of all keys */
                 for (int64_t j = 0; j < N; ++j) {
                     load_row(K, elem, base + j * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     load_row(V, elem, base + j * d, d, v);
                     sketch_add(S, phi, nfeat, v, d);
                 }
@@ -429,7 +458,7 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                 int64_t o = 0;
                 for (int64_t i = 0; i < N; ++i) {
                     load_row(Q, elem, base + i * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     double den = sketch_read(S, phi, nfeat, d, num);
                     load_row(dO, elem, base + i * d, d, g);
                     double dOO = 0.0;
@@ -449,9 +478,9 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         for (int64_t c = 0; c < d; ++c) s += row[c] * dnum[c];
                         dphi[j] = s;
                     }
-                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P);
+                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P, beta);
                     if (!want) continue;
-                    features_backward(x, xhat, u, phi, dphi, d, W, L, P, beta, normalize, dxhat, dx);
+                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx);
                     memcpy(dQbh + o * d, dx, sizeof(double) * d);
                     ++o;
                 }
@@ -464,7 +493,7 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         continue;
                     }
                     load_row(K, elem, base + j0 * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     load_row(V, elem, base + j0 * d, d, v);
                     if (want)
                         for (int64_t c = 0; c < d; ++c) dVbh[o2 * d + c] = 0.0;
@@ -477,9 +506,9 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         }
                         dphi[j] = s;
                     }
-                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P);
+                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P, beta);
                     if (!want) continue;
-                    features_backward(x, xhat, u, phi, dphi, d, W, L, P, beta, normalize, dxhat, dx);
+                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx);
                     memcpy(dKbh + o2 * d, dx, sizeof(double) * d);
                     ++o2;
                 }
@@ -488,11 +517,11 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                 int64_t o = 0;
                 for (int64_t t = 0; t < N; ++t) {
                     load_row(K, elem, base + t * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     load_row(V, elem, base + t * d, d, v);
                     sketch_add(S, phi, nfeat, v, d);
                     load_row(Q, elem, base + t * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     double den = sketch_read(S, phi, nfeat, d, num);
                     load_row(dO, elem, base + t * d, d, g);
                     double dOO = 0.0;
@@ -508,9 +537,9 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         for (int64_t c = 0; c < d; ++c) s += row[c] * (g[c] / den);
                         dphi[j] = s;
                     }
-                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P);
+                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P, beta);
                     if (!want) continue;
-                    features_backward(x, xhat, u, phi, dphi, d, W, L, P, beta, normalize, dxhat, dx);
+                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx);
                     memcpy(dQbh + o * d, dx, sizeof(double) * d);
                     ++o;
                 }
@@ -518,7 +547,7 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                 int64_t o2 = nout - 1;
                 for (int64_t t = N - 1; t >= 0 && (o2 >= 0 || dbeta); --t) {
                     load_row(Q, elem, base + t * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     load_row(dO, elem, base + t * d, d, g);
                     for (int64_t c = 0; c < d; ++c) dnum[c] = g[c] / den_all[t];
                     double dden = -dOO_all[t] / den_all[t];
@@ -531,7 +560,7 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                     if (!want && !dbeta) continue;
                     int64_t slot = rows ? o2 : t;
                     load_row(K, elem, base + t * d, d, x);
-                    features(x, d, W, L, P, beta, normalize, xhat, u, phi);
+                    features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     load_row(V, elem, base + t * d, d, v);
                     if (want)
                         for (int64_t c = 0; c < d; ++c) dVbh[slot * d + c] = 0.0;
@@ -544,9 +573,9 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         }
                         dphi[j] = s;
                     }
-                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P);
+                    if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P, beta);
                     if (!want) continue;
-                    features_backward(x, xhat, u, phi, dphi, d, W, L, P, beta, normalize, dxhat, dx);
+                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx);
                     memcpy(dKbh + slot * d, dx, sizeof(double) * d);
                     --o2;
                 }
@@ -554,6 +583,78 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
         }
         free(S); free(G); free(x); free(xhat); free(v); free(num); free(g); free(dnum);
         free(dxhat); free(dx); free(u); free(phi); free(dphi); free(den_all); free(dOO_all);
+    }
+    return status;
+}
+
+/*
+ * Angular attention, the target the soft hash estimates ("RACE Attention" slides, frame "Choose a
+ * nonnegative kernel that can be sketched", paper Eqs. (3)-(4); reading notes 3.1): O(N^2) by its
+ * definition,
+ *
+ *     O_i = sum_j S_ij V_j / sum_j S_ij,   S_ij = (1 - arccos(q_i . k_j / (|q_i| |k_j|)) / pi)^gamma,
+ *
+ * over j <= i when causal.  With gamma = P it is the kernel a P-bit hard hash collides with
+ * (frame "A hash collision estimates a powered angular kernel").  Reading where the pages are
+ * silent: a zero row has cosine 0 with every row (angle pi / 2, the value the soft features'
+ * uniform buckets give); the cosine is clamped to [-1, 1] before arccos; 0^0 = 1.
+ * Q, K, V: [B, H, N, d] of element type `elem`; O: [B, H, nout, d] float64 with `rows` as in
+ * `race_oracle_forward`.  Returns 2 if a row's sum_j S_ij is zero (every key antipodal).
+ */
+int race_oracle_angular_forward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
+                                const void *Q, const void *K, const void *V, double gamma,
+                                int causal, const int64_t *rows, int64_t nrows, double *O,
+                                int nthreads)
+{
+    if (check_args(B, H, N, d, elem, 1, 1, rows, nrows) || !(gamma >= 0.0)) return -1;
+    const int64_t nout = rows ? nrows : N;
+    const double pi = acos(-1.0);
+    int status = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        double *q = malloc(sizeof(double) * d), *k = malloc(sizeof(double) * d);
+        double *v = malloc(sizeof(double) * d), *num = malloc(sizeof(double) * d);
+        if (!q || !k || !v || !num) {
+#pragma omp atomic write
+            status = -2;
+        } else {
+            const int64_t base = bh * N * d;
+            for (int64_t o = 0; o < nout; ++o) {
+                const int64_t i = rows ? rows[o] : o;
+                load_row(Q, elem, base + i * d, d, q);
+                double qq = 0.0;
+                for (int64_t c = 0; c < d; ++c) qq += q[c] * q[c];
+                for (int64_t c = 0; c < d; ++c) num[c] = 0.0;
+                double den = 0.0;
+                const int64_t jend = causal ? i + 1 : N;
+                for (int64_t j = 0; j < jend; ++j) {
+                    load_row(K, elem, base + j * d, d, k);
+                    double kk = 0.0, qk = 0.0;
+                    for (int64_t c = 0; c < d; ++c) { kk += k[c] * k[c]; qk += q[c] * k[c]; }
+                    double cosang = (qq > 0.0 && kk > 0.0) ? qk / (sqrt(qq) * sqrt(kk)) : 0.0;
+                    if (cosang > 1.0) cosang = 1.0;
+                    if (cosang < -1.0) cosang = -1.0;
+                    const double s = pow(1.0 - acos(cosang) / pi, gamma);
+                    load_row(V, elem, base + j * d, d, v);
+                    for (int64_t c = 0; c < d; ++c) num[c] += s * v[c];
+                    den += s;
+                }
+                double *Oi = O + (bh * nout + o) * d;
+                if (!(den > 0.0)) {
+#pragma omp atomic write
+                    status = 2;
+                    for (int64_t c = 0; c < d; ++c) Oi[c] = NAN;
+                } else {
+                    for (int64_t c = 0; c < d; ++c) Oi[c] = num[c] / den;
+                }
+            }
+        }
+        free(q); free(k); free(v); free(num);
     }
     return status;
 }
