@@ -90,13 +90,20 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
  * Backward pass: given the output cotangent dO, writes dQ, dK, dV (all [B, H, N, d]).
  * O: the forward output.  It may be NULL: the kernels recompute what they need of O
  * (dO . O per row) from the sketch, which is cheaper than reading it.
+ * dbeta: NULL, or device float32 [B, H] (4-byte aligned) that receives d(loss)/d(beta) for each
+ * (b, h).  beta is trained with the layer ("RACE Attention" slides, frame "Soft corner
+ * assignments make hashing differentiable"); its logits are beta (u . v_r), so every query and
+ * key row adds sum_l sum_r ds_r (u . v_r), with ds the softmax gradient of its bucket
+ * probabilities.  The gradient of the one shared beta is the sum of the B * H values.  Each
+ * value is a sum in a fixed order (per-CTA partials, then a combine), so repeated calls give the
+ * same bits.  Overwritten, not accumulated.
  * state: NULL (the sketch is recomputed from K and V), or the buffer a race_attn_fwd call
  * with the same Q, K, V, W, beta, L, P and causal filled in.
- * Gradients with respect to W and beta are not produced.
+ * The gradient with respect to W is not produced.
  */
 int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const void *V,
                   const float *W, float beta, int L, int P, int causal, const void *O,
-                  const void *dO, void *dQ, void *dK, void *dV, const void *state,
+                  const void *dO, void *dQ, void *dK, void *dV, float *dbeta, const void *state,
                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*

@@ -56,7 +56,7 @@ def load_library():
     L.race_attn_state_bytes.restype = sz
     L.race_attn_fwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, sz, vp]
     L.race_attn_fwd.restype = i
-    L.race_attn_bwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.race_attn_bwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.race_attn_bwd.restype = i
     L.race_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp]
     L.race_attn_fwd_noalloc.restype = i
@@ -192,8 +192,10 @@ def race_attn_fwd(Q, K, V, W, beta, L, P, causal, O=None, state=None, workspace=
 
 
 def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, dV=None, state=None,
-                  workspace=None, stream=None):
-    """(dQ, dK, dV) of RACE attention for the output cotangent dO; allocates what is not given."""
+                  workspace=None, stream=None, want_dbeta=False, dbeta=None):
+    """(dQ, dK, dV) of RACE attention for the output cotangent dO; allocates what is not given.
+    With want_dbeta (or a float32 [B, H] `dbeta` given) also d(loss)/d(beta) per (b, h), returned
+    as a fourth element; the shared beta's gradient is its sum."""
     shape = _shape_of(Q)
     for n, t in (("K", K), ("V", V), ("dO", dO), ("Q", Q)):
         _check_like(n, t, Q)
@@ -204,17 +206,22 @@ def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, 
     dV = torch.empty_like(Q) if dV is None else dV
     for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
         _check_like(n, t, Q)
+    if dbeta is None and want_dbeta:
+        dbeta = torch.empty((Q.shape[0], Q.shape[1]), dtype=torch.float32, device=Q.device)
+    if dbeta is not None and (dbeta.dtype != torch.float32 or tuple(dbeta.shape) != tuple(Q.shape[:2])
+                              or not dbeta.is_contiguous() or dbeta.device != Q.device):
+        raise ValueError("dbeta must be a contiguous float32 tensor of shape [B, H] on Q's device")
     ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 1)
     if ws_bytes == 0:
         raise RaceAttnError(-1, "race_attn_bwd")
     workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
     rc = load_library().race_attn_bwd(
         ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
-        int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(state), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream))
+        int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dbeta), _ptr(state),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != 0:
         raise RaceAttnError(rc, "race_attn_bwd")
-    return dQ, dK, dV
+    return (dQ, dK, dV) if dbeta is None else (dQ, dK, dV, dbeta)
 
 
 def race_attn_decode(q, k, v, W, beta, L, P, state, o=None, stream=None):

@@ -28,6 +28,24 @@ __device__ __forceinline__ float ld_f(const __nv_bfloat16 *p, int64_t i) { retur
 __device__ __forceinline__ void st_f(float *p, int64_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void st_f(__nv_bfloat16 *p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
 
+// Sum of one float per thread over the CTA in a fixed order (butterflies within each warp, then
+// the warps in index order), so that a reduction gives the same bits on every run.  Every
+// thread of the block calls it; `scratch` holds one float per warp and may be in use until the
+// call.  The total is returned in thread 0.
+__device__ __forceinline__ float block_sum_fixed(float v, float *scratch)
+{
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    const int warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < nw; ++w) s += scratch[w];
+    return s;
+}
+
 // Bump allocator for dynamic shared memory layouts, usable on host (to size the launch) and
 // device (to find the regions); every region starts on a 16-byte boundary.
 struct SmemLayout {

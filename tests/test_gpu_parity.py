@@ -251,3 +251,41 @@ def test_config_full_size_sampled(name):
     ws = w.scaled(H=1)
     ref = oracle_run(ws, sub, rows=rows)
     assert_close(ws, got, ref, w.name)
+
+
+# d(loss)/d(beta): one workload per backward kernel family (CUDA-core non-causal / causal,
+# tcgen05 non-causal / causal, mma.sync causal L R = 64), ragged tails and several segments.
+DBETA = [
+    W_("db_f32", 1, 2, 100, 64, 2, 2, False, "f32"),
+    W_("db_f32_c", 1, 2, 100, 64, 2, 2, True, "f32"),
+    W_("db_bf_nc", 1, 2, 1000, 64, 3, 3, False, "bf16"),
+    W_("db_bf_lr256", 1, 2, 300, 128, 6, 4, False, "bf16", clusters=8),
+    W_("db_bf_c5", 1, 2, 5555, 128, 3, 3, True, "bf16"),
+    W_("db_bf_c5_p2", 2, 1, 700, 64, 2, 3, True, "bf16"),
+    W_("db_bf_lr64_c", 2, 3, 257, 64, 4, 4, True, "bf16"),
+]
+
+
+@pytest.mark.parametrize("w", DBETA, ids=lambda w: w.name)
+def test_dbeta_matches_oracle(w):
+    """d(sum O * dO)/d(beta) per (b, h) against the oracle (whose value is pinned to finite
+    differences of the brute force).  Tolerance relative to the largest |value|: 1e-4 for float32
+    tensors, 5e-2 for bfloat16 (the gradient tolerance).  Asking for it leaves dQ, dK, dV bit for
+    bit unchanged, and a second call gives the same bits."""
+    inp = inputs_on_gpu(w, seed=4)
+    args = (inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal, inp["dO"])
+    plain = race.race_attn_bwd(*args)
+    with_db = race.race_attn_bwd(*args, want_dbeta=True)
+    again = race.race_attn_bwd(*args, want_dbeta=True)
+    torch.cuda.synchronize()
+    for x, y in zip(plain, with_db[:3]):
+        assert torch.equal(x, y)
+    assert torch.equal(with_db[3], again[3])
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V", "dO")}
+    W = inp["W"].double().cpu().numpy()
+    *_, ref = oracle.backward(a["Q"], a["K"], a["V"], a["dO"], W, w.beta, w.causal, want_dbeta=True)
+    got = with_db[3].double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    tol = 1e-4 if w.dtype == "f32" else 5e-2
+    err = np.abs(got - ref).max() / np.abs(ref).max()
+    assert err <= tol, "%s dbeta error %.3e > %.1e (got %s, oracle %s)" % (w.name, err, tol, got, ref)
