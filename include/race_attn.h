@@ -20,8 +20,10 @@
  *  - Token tensors Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d], contiguous, d innermost, of
  *    element type `shape->dtype` (float32 or bfloat16), on the current CUDA device, 16-byte
  *    aligned.  Outputs are rounded to nearest-even from float32 arithmetic.
- *  - W is float32 [L, P, d] on the device, shared by Q and K, by all tables' rows, and by all
- *    (b, h).  beta is a finite scalar >= 0.
+ *  - W is float32 on the device, shared by Q and K and by all tables' rows: one [L, P, d] array
+ *    for every (b, h), or, with shape->per_head_w = 1, one set per head, [H, L, P, d], head h
+ *    hashing with W[h] for every batch entry (the pages do not say whether heads share their
+ *    hyperplanes; both layouts are offered).  beta is a finite scalar >= 0.
  *  - Limits: N >= 1; B * H <= 65535; d a multiple of 8 in [8, 128]; 1 <= P <= 8; 1 <= L <= 16;
  *    L * 2^P <= 256.
  *  - The caller owns every buffer, including `workspace` (size from race_attn_workspace_bytes)
@@ -57,10 +59,11 @@ typedef enum {
     RACE_ERR_DEVICE_TIMEOUT = -7 /* race_attn_status: a kernel stopped after a bounded wait     */
 } race_status;
 
-/* Token-tensor shape and element type. */
+/* Token-tensor shape and element type, and the layout of W. */
 typedef struct {
     int64_t B, H, N, d;
-    int32_t dtype; /* race_dtype */
+    int32_t dtype;      /* race_dtype */
+    int32_t per_head_w; /* 0: W is [L, P, d] for every head; 1: W is [H, L, P, d] */
 } race_shape;
 
 /*

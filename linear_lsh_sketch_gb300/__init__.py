@@ -36,7 +36,7 @@ class RaceAttnError(RuntimeError):
 
 class race_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64),
-                ("d", ctypes.c_int64), ("dtype", ctypes.c_int32)]
+                ("d", ctypes.c_int64), ("dtype", ctypes.c_int32), ("per_head_w", ctypes.c_int32)]
 
 
 def load_library():
@@ -80,18 +80,26 @@ def load_library():
     return L
 
 
-def make_shape(B, H, N, d, dtype):
+def make_shape(B, H, N, d, dtype, per_head_w=False):
     code = _DTYPES.get(dtype, dtype) if not isinstance(dtype, int) else dtype
-    return race_shape(int(B), int(H), int(N), int(d), int(code))
+    return race_shape(int(B), int(H), int(N), int(d), int(code), int(bool(per_head_w)))
 
 
-def _shape_of(Q):
+def _shape_of(Q, W=None, L=None, P=None):
+    """race_shape of the token tensor Q; with W also checks the hyperplanes: float32, contiguous,
+    [L, P, d] (shared by every head) or [H, L, P, d] (one set per head)."""
     if Q.dim() != 4:
         raise ValueError("token tensors must be [B, H, N, d]")
     if Q.dtype not in _DTYPES:
         raise TypeError("token tensors must be float32 or bfloat16")
     B, H, N, d = Q.shape
-    return make_shape(B, H, N, d, Q.dtype)
+    per_head = False
+    if W is not None:
+        shared, heads = (L, P, d), (H, L, P, d)
+        if W.dtype != torch.float32 or not W.is_contiguous() or tuple(W.shape) not in (shared, heads):
+            raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d] or [H, L, P, d]")
+        per_head = tuple(W.shape) == heads and W.dim() == 4
+    return make_shape(B, H, N, d, Q.dtype, per_head)
 
 
 def _ptr(t):
@@ -165,16 +173,15 @@ def _bytes_buffer(nbytes, device, given):
 
 
 def race_attn_fwd(Q, K, V, W, beta, L, P, causal, O=None, state=None, workspace=None, stream=None):
-    """O = RACE attention of Q, K, V ([B, H, N, d], float32 or bfloat16, CUDA); W float32 [L, P, d].
+    """O = RACE attention of Q, K, V ([B, H, N, d], float32 or bfloat16, CUDA); W float32 [L, P, d]
+    (shared by every head) or [H, L, P, d] (one set per head).
 
     O, state and workspace are allocated with torch when not given.  Returns O.
     """
-    shape = _shape_of(Q)
+    shape = _shape_of(Q, W, L, P)
     _check_like("K", K, Q)
     _check_like("V", V, Q)
     _check_like("Q", Q, Q)
-    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
-        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
     if O is None:
         O = torch.empty_like(Q)
     _check_like("O", O, Q)
@@ -196,11 +203,9 @@ def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, 
     """(dQ, dK, dV) of RACE attention for the output cotangent dO; allocates what is not given.
     With want_dbeta (or a float32 [B, H] `dbeta` given) also d(loss)/d(beta) per (b, h), returned
     as a fourth element; the shared beta's gradient is its sum."""
-    shape = _shape_of(Q)
+    shape = _shape_of(Q, W, L, P)
     for n, t in (("K", K), ("V", V), ("dO", dO), ("Q", Q)):
         _check_like(n, t, Q)
-    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
-        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(Q) if dK is None else dK
     dV = torch.empty_like(Q) if dV is None else dV
@@ -227,11 +232,9 @@ def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, 
 def race_attn_decode(q, k, v, W, beta, L, P, state, o=None, stream=None):
     """One causal decode step: q, k, v [B, H, 1, d] (float32 or bfloat16, CUDA); state float32
     [B, H, L * 2^P, d + 1] (updated in place).  Returns o [B, H, 1, d]."""
-    shape = _shape_of(q)
+    shape = _shape_of(q, W, L, P)
     for n, t in (("k", k), ("v", v), ("q", q)):
         _check_like(n, t, q)
-    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, q.shape[3]) or not W.is_contiguous():
-        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
     want = (q.shape[0], q.shape[1], L << P, q.shape[3] + 1)
     if state.dtype != torch.float32 or tuple(state.shape) != want or not state.is_contiguous():
         raise ValueError("state must be a contiguous float32 tensor of shape %s" % (want,))
@@ -252,12 +255,10 @@ def race_attn_fwd_noalloc(Q, K, V, W, beta, L, P, causal, O=None, stream=None):
     that buffer and must be serialised by the caller.  Only O is allocated here, and only when
     it is not given.  Returns O.
     """
-    shape = _shape_of(Q)
+    shape = _shape_of(Q, W, L, P)
     _check_like("K", K, Q)
     _check_like("V", V, Q)
     _check_like("Q", Q, Q)
-    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
-        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
     if O is None:
         O = torch.empty_like(Q)
     _check_like("O", O, Q)

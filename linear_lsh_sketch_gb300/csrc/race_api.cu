@@ -121,6 +121,7 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     if (P < 1 || P > kMaxP || L < 1 || L > kMaxL) return RACE_ERR_INVALID_ARG;
     if ((L << P) > kMaxLR) return RACE_ERR_INVALID_ARG;
     if (s->dtype != RACE_F32 && s->dtype != RACE_BF16) return RACE_ERR_INVALID_ARG;
+    if (s->per_head_w != 0 && s->per_head_w != 1) return RACE_ERR_INVALID_ARG;
     if (s->B > 65535 || s->H > 65535 || s->B * s->H > 65535 || s->N > ((int64_t)1 << 40) / (s->B * s->H))
         return RACE_ERR_INVALID_ARG;
     Dims &D = pl.D;
@@ -134,6 +135,8 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     D.LP = L * P;
     D.dv = D.d + 1;
     D.beta = 0.f;
+    D.H = s->H;
+    D.w_per_head = s->per_head_w;
     pl.causal = causal != 0;
     pl.bf16 = s->dtype == RACE_BF16;
     pl.E = (size_t)D.LR * D.dv;

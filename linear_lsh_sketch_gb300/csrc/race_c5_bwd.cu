@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         zero_region(sm + Ly.fq, BLK);
         zero_region(sm + Ly.ghi, 2 * BLK);
         init_mass_tile(sm + Ly.ncm, false);
-        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+        load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     }
     if (tid == NTH) {
         for (uint32_t i = 0; i < B_COUNT; ++i) {
@@ -710,7 +710,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         zero_region(sm + Ly.fk, 4 * BLK);  // F_K, F'_Q, S hi, S lo
         init_mass_tile(sm + Ly.ncm, false);
         init_mass_tile(sm + Ly.ones, true);
-        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+        load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     }
     if (tid == NTH) {
         for (uint32_t i = 0; i < B_COUNT; ++i) {

@@ -21,7 +21,15 @@ struct Dims {
     int64_t N;   // tokens per problem
     int d, L, P, R, LR, LP, dv;
     float beta;
+    int64_t H;       // heads (problem bh is head bh % H)
+    int w_per_head;  // 0: one W [L, P, d] for every head; 1: W is [H, L, P, d]
 };
+
+// The hyperplanes problem bh hashes with: the shared W, or its head's slice of a per-head W.
+__host__ __device__ inline const float *head_w(const float *W, const Dims &D, int64_t bh)
+{
+    return D.w_per_head ? W + (bh % D.H) * (int64_t)D.LP * D.d : W;
+}
 
 __device__ __forceinline__ float ld_f(const float *p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld_f(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }

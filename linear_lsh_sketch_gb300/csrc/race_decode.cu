@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(NT) k_decode(const T *__restrict__ q, const T 
     if (tid < 2 * MAXLP) {  // one projection per thread: side tid / MAXLP, row p = l P + t of W
         const int side = tid / MAXLP, p = tid - side * MAXLP;
         if (p < LP) {
-            const float *w = W + (int64_t)p * d;
+            const float *w = head_w(W, D, bh) + (int64_t)p * d;
             float z = 0.f;
             for (int c = 0; c < d; ++c) z = fmaf(w[c], xs[side][c], z);
             us[side][p] = tanhf(z * inv[side]);

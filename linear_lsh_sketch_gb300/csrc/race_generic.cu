@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(NT) k_sketch(Dims D, const T *__restrict__ X,
     const int l0 = f0 / D.R, l1 = (f1 - 1) / D.R + 1;
     const SketchSmem L(D, l1 - l0);
     float *ws = sm + L.ws, *xs = sm + L.xs, *ys = sm + L.ys, *fs = sm + L.fs, *inv = sm + L.inv;
-    load_w(W, D, l0, l1, ws);
+    load_w(head_w(W, D, bh), D, l0, l1, ws);
     const T *Xb = X + bh * D.N * D.d;
     const T *Yb = Y + bh * D.N * D.d;
     const int64_t n_begin = (int64_t)s * seg_len;
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(NT) k_readout(Dims D, const T *__restrict__ Q,
     const int64_t bh = blockIdx.y, n0 = (int64_t)blockIdx.x * TT;
     const int cnt = (int)min((int64_t)TT, D.N - n0);
     const int fst = D.LR + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     load_rows(Q + bh * D.N * D.d, n0, cnt, D.d, xs);
     __syncthreads();
     featurise(xs, D, ws, 0, D.LR, inv, nullptr, fs, fst);
@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(NT) k_bwd_query(Dims D, const T *__restrict__ 
     const int64_t bh = blockIdx.y, n0 = (int64_t)blockIdx.x * TT;
     const int cnt = (int)min((int64_t)TT, D.N - n0);
     const int dp = D.d + 1, fst = D.LR + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     load_rows(Q + bh * D.N * D.d, n0, cnt, D.d, xs);
     load_rows(dO + bh * D.N * D.d, n0, cnt, D.d, ys);
     __syncthreads();
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(NT) k_bwd_key(Dims D, const T *__restrict__ K,
     const int64_t bh = blockIdx.y, n0 = (int64_t)blockIdx.x * TT;
     const int cnt = (int)min((int64_t)TT, D.N - n0);
     const int dp = D.d + 1, fst = D.LR + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     load_rows(K + bh * D.N * D.d, n0, cnt, D.d, xs);
     load_values(V + bh * D.N * D.d, n0, cnt, D.d, vs);
     __syncthreads();
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(Dims D, const T *__restrict__
     const int s = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int fst = D.LR + 1, dv = D.dv, E = D.LR * D.dv;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     const float *S0b = S0 + ((int64_t)bh * nseg + s) * E;
     for (int i = threadIdx.x; i < E; i += NT) S[i] = S0b[i];
     const int64_t off = bh * D.N * D.d;
@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_q(Dims D, const T *__restrict
     const int s = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int fst = D.LR + 1, dv = D.dv, dp = D.d + 1, E = D.LR * D.dv, TP = TT + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     const float *S0b = S0 + ((int64_t)bh * nseg + s) * E;
     for (int i = threadIdx.x; i < E; i += NT) S[i] = S0b[i];
     const int64_t off = bh * D.N * D.d;
@@ -778,7 +778,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_kv(Dims D, const T *__restric
     const int s = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int fst = D.LR + 1, dv = D.dv, dp = D.d + 1, E = D.LR * D.dv, TP = TT + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     const float *G0b = G0 + ((int64_t)bh * nseg + s) * E;
     for (int i = threadIdx.x; i < E; i += NT) G[i] = G0b[i];
     const int64_t off = bh * D.N * D.d;

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const int L = LT > 0 ? LT : Dm.L;  // LT > 0: per-table loops unroll without guards
 
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
-    load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     load_sketch_rows<D>(S + bh * Dm.LR * (D + 1), Dm.LR, lrp, base + Ly.shi, base + Ly.slo, Ly.split,
                         reinterpret_cast<float *>(sm + Ly.mass));
     if (tid == 0) {
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const int L = LT > 0 ? LT : Dm.L;  // LT > 0: per-table loops unroll without guards
 
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
-    load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     load_sketch_rows<D>(G + bh * Dm.LR * (D + 1), Dm.LR, lrp, base + Ly.shi, base + Ly.slo, Ly.split,
                         reinterpret_cast<float *>(sm + Ly.mass));
     if (tid == 0) {

@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(NTH, 1)
     float db = 0.f;  // this thread's d(loss)/d(beta) share (dbpart only)
     const int t0 = 16 * rb + g, t1 = t0 + 8;
 
-    bwd_setup<D, P, LRP>(Dm, W, smem);
+    bwd_setup<D, P, LRP>(Dm, head_w(W, Dm, bh), smem);
     float st[B::SNT][B::MT][4], gacc[B::SNT][B::MT][4];
     load_sketch<D, P, LRP>(Dm, S0 + ((int64_t)bh * nseg + s) * Dm.LR * (D + 1), warp, lane, st, sh(0, 0), sh(0, 1));
 #pragma unroll
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(NTH, 1)
     float db = 0.f;  // this thread's d(loss)/d(beta) share (dbpart only)
     const int j0 = 16 * rb + g, j1 = j0 + 8;  // key rows of this warp's row block
 
-    bwd_setup<D, P, LRP>(Dm, W, smem);
+    bwd_setup<D, P, LRP>(Dm, head_w(W, Dm, bh), smem);
     float gst[B::SNT][B::MT][4];
     load_sketch<D, P, LRP>(Dm, G0 + ((int64_t)bh * nseg + s) * Dm.LR * (D + 1), warp, lane, gst, gh(0, 0), gh(0, 1));
     __syncthreads();

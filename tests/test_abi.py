@@ -129,3 +129,26 @@ def test_instrumentation_defaults(lib):
     assert lib.race_attn_launch_count() >= 0
     lib.race_attn_profile_reset()
     assert lib.race_attn_profile_read() == {}
+
+
+def test_per_head_w_layout(lib):
+    """race_shape.per_head_w selects W [H, L, P, d]: it changes no buffer size, takes only 0 or 1,
+    and the binding picks it from W's shape (checked before any call)."""
+    import torch
+    s = shape(lib)
+    ph = lib.make_shape(s.B, s.H, s.N, s.d, s.dtype, per_head_w=True)
+    assert ctypes.sizeof(type(s)) == 40
+    for causal in (0, 1):
+        for is_bwd in (0, 1):
+            assert lib.race_attn_workspace_bytes(ph, 3, 3, causal, is_bwd) == \
+                lib.race_attn_workspace_bytes(s, 3, 3, causal, is_bwd)
+    s.per_head_w = 2
+    assert lib.race_attn_workspace_bytes(s, 3, 3, 0, 1) == 0
+    Q = torch.zeros((2, 4, 8, 64), dtype=torch.bfloat16)
+    assert lib._shape_of(Q, torch.zeros((3, 2, 64)), 3, 2).per_head_w == 0
+    assert lib._shape_of(Q, torch.zeros((4, 3, 2, 64)), 3, 2).per_head_w == 1
+    for bad in ((2, 3, 2, 64), (3, 2, 32), (4, 3, 2)):
+        with pytest.raises(ValueError):
+            lib._shape_of(Q, torch.zeros(bad), 3, 2)
+    with pytest.raises(ValueError):
+        lib._shape_of(Q, torch.zeros((3, 2, 64), dtype=torch.float64), 3, 2)

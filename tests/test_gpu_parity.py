@@ -289,3 +289,53 @@ def test_dbeta_matches_oracle(w):
     tol = 1e-4 if w.dtype == "f32" else 5e-2
     err = np.abs(got - ref).max() / np.abs(ref).max()
     assert err <= tol, "%s dbeta error %.3e > %.1e (got %s, oracle %s)" % (w.name, err, tol, got, ref)
+
+
+# One set of hyperplanes per head (W [H, L, P, d]); B = 2 so that reading W by (b, h) instead of
+# by h would fail.  One workload per kernel family.
+PER_HEAD = [
+    W_("ph_f32", 2, 3, 100, 64, 2, 2, False, "f32"),
+    W_("ph_f32_c", 2, 3, 100, 64, 2, 2, True, "f32"),
+    W_("ph_bf_nc", 2, 3, 700, 64, 3, 3, False, "bf16"),
+    W_("ph_bf_lr256", 2, 2, 300, 128, 6, 4, False, "bf16", clusters=8),
+    W_("ph_bf_c5", 2, 3, 700, 128, 3, 3, True, "bf16"),
+    W_("ph_bf_lr64_c", 2, 3, 257, 64, 4, 4, True, "bf16"),
+]
+
+
+def _per_head_w(w, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((w.H, w.L, w.P, w.d), generator=g, dtype=torch.float32).cuda()
+
+
+@pytest.mark.parametrize("w", PER_HEAD, ids=lambda w: w.name)
+def test_per_head_w(w):
+    """Head h hashes with W[h]: forward and backward against the oracle's per-head layout, and
+    a per-head W whose heads are all equal gives the shared-W results bit for bit."""
+    inp = inputs_on_gpu(w, seed=6)
+    inp["W"] = _per_head_w(w, 60)
+    assert_close(w, gpu_run(w, inp), oracle_run(w, inp), w.name)
+    shared = dict(inp, W=inp["W"][1].contiguous())
+    same = dict(inp, W=inp["W"][1].expand(w.H, -1, -1, -1).contiguous())
+    for x, y in zip(gpu_run(w, shared), gpu_run(w, same)):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_per_head_w(dtype):
+    """Decode steps with one hyperplane set per head against the oracle's decode step."""
+    w = W_("decode_ph", 2, 3, 20, 64, 3, 2, True, dtype)
+    inp = inputs_on_gpu(w, seed=13)
+    Q, K, V = inp["Q"], inp["K"], inp["V"]
+    W = _per_head_w(w, 61)
+    B, H, N, d = Q.shape
+    state = torch.zeros((B, H, w.L << w.P, d + 1), dtype=torch.float32, device="cuda")
+    ref_state = np.zeros((B, H, w.L << w.P, d + 1))
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V")}
+    Wd = W.double().cpu().numpy()
+    tol = 2e-5 if dtype == "f32" else 1e-2
+    for t in range(N):
+        tok = [x[:, :, t:t + 1].contiguous() for x in (Q, K, V)]
+        o = race.race_attn_decode(*tok, W, w.beta, w.L, w.P, state)
+        ref = oracle.decode_step(a["Q"][:, :, t], a["K"][:, :, t], a["V"][:, :, t], Wd, w.beta, ref_state)
+        assert np.abs(o[:, :, 0].double().cpu().numpy() - ref).max() <= tol * np.abs(ref).max(), t
