@@ -23,7 +23,15 @@
  *  - W is float32 on the device, shared by Q and K and by all tables' rows: one [L, P, d] array
  *    for every (b, h), or, with shape->per_head_w = 1, one set per head, [H, L, P, d], head h
  *    hashing with W[h] for every batch entry (the pages do not say whether heads share their
- *    hyperplanes; both layouts are offered).  beta is a finite scalar >= 0.
+ *    hyperplanes; both layouts are offered).
+ *  - beta is a scalar >= 0: finite, or +INFINITY for hard hashing, the limit the slides name
+ *    ("beta -> infinity: hard hashing").  Each bit is then the sign of its projection, and a
+ *    row lands in one corner per table.  A projection that is exactly 0 splits the row evenly
+ *    over the two corners it separates (the limit sigmoid(0) = 1/2), so a zero row is uniform.
+ *    The features are computed as the soft ones at beta = 2^126, which equals the sign rule
+ *    exactly for every projection u with |u| >= 2^-119 and at u = 0.  No gradient reaches Q, K or
+ *    beta (dQ = dK = 0, dbeta = 0); dV is the hard sketch's.  A query whose corners hold no key
+ *    in any table has a zero denominator (its output is 0/0), which small inputs can meet.
  *  - Limits: N >= 1; B * H <= 65535; d a multiple of 8 in [8, 128]; 1 <= P <= 8; 1 <= L <= 16;
  *    L * 2^P <= 256.
  *  - The caller owns every buffer, including `workspace` (size from race_attn_workspace_bytes)

@@ -192,7 +192,18 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
-int check_beta(float beta) { return (std::isfinite(beta) && beta >= 0.f) ? RACE_OK : RACE_ERR_INVALID_ARG; }
+// beta: finite and >= 0, or +infinity for hard hashing.
+int check_beta(float beta) { return (!std::isnan(beta) && beta >= 0.f) ? RACE_OK : RACE_ERR_INVALID_ARG; }
+
+// Hard hashing (beta = +infinity, the limit "RACE Attention" slides, frame "Soft corner assignments
+// make hashing differentiable", call hard hashing) runs the soft kernels at the finite stand-in
+// 2^126.  Their sigmoid(2 beta u) is then exactly 1 or 0 for every |u| >= 2^-119 (the exponent
+// underflows) and exactly 1/2 at u = 0, the value a tied projection keeps in the limit.  So
+// the features are the hard corners, and the softmax gradient vanishes identically.  Only tied
+// rows (u = 0) would carry a Jacobian scaled by 2^126, and their dQ and dK are zero by definition.
+constexpr float kHardBeta = 8.507059e37f;  // 2^126
+bool hard_hash(float beta) { return std::isinf(beta); }
+float kernel_beta(float beta) { return hard_hash(beta) ? kHardBeta : beta; }
 
 #define RACE_TRY(expr)                                   \
     do {                                                 \
@@ -390,7 +401,7 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
         !aligned16(workspace) || (state && !aligned16(state)))
         return RACE_ERR_ALIGN;
     if (workspace_bytes < pl.ws_fwd) return RACE_ERR_WORKSPACE;
-    pl.D.beta = beta;
+    pl.D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
     if (pl.bf16)
         return forward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
@@ -415,16 +426,23 @@ int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const v
         ((uintptr_t)dbeta & 3) != 0)
         return RACE_ERR_ALIGN;
     if (workspace_bytes < pl.ws_bwd) return RACE_ERR_WORKSPACE;
-    pl.D.beta = beta;
+    pl.D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
     if (pl.bf16)
-        return backward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
-                                            (const __nv_bfloat16 *)V, W, (const __nv_bfloat16 *)dO,
-                                            (__nv_bfloat16 *)dQ, (__nv_bfloat16 *)dK, (__nv_bfloat16 *)dV, dbeta,
-                                            (const float *)state, (char *)workspace, st);
-    return backward_impl<float>(pl, (const float *)Q, (const float *)K, (const float *)V, W, (const float *)dO,
-                                (float *)dQ, (float *)dK, (float *)dV, dbeta, (const float *)state, (char *)workspace,
-                                st);
+        rc = backward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
+                                          (const __nv_bfloat16 *)V, W, (const __nv_bfloat16 *)dO,
+                                          (__nv_bfloat16 *)dQ, (__nv_bfloat16 *)dK, (__nv_bfloat16 *)dV, dbeta,
+                                          (const float *)state, (char *)workspace, st);
+    else
+        rc = backward_impl<float>(pl, (const float *)Q, (const float *)K, (const float *)V, W, (const float *)dO,
+                                  (float *)dQ, (float *)dK, (float *)dV, dbeta, (const float *)state,
+                                  (char *)workspace, st);
+    if (rc == RACE_OK && hard_hash(beta)) {  // a hard hash passes no gradient to Q and K
+        const size_t bytes = (size_t)pl.D.BH * pl.D.N * pl.D.d * (pl.bf16 ? 2 : 4);
+        RACE_TRY(cudaMemsetAsync(dQ, 0, bytes, st));
+        RACE_TRY(cudaMemsetAsync(dK, 0, bytes, st));
+    }
+    return rc;
 }
 
 const char *race_attn_strerror(int status)
@@ -454,7 +472,7 @@ int race_attn_decode(const race_shape *shape, const void *q, const void *k, cons
         return RACE_ERR_ALIGN;
     if (!decode_supported(pl.D)) return RACE_ERR_UNSUPPORTED;
     Dims D = pl.D;
-    D.beta = beta;
+    D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
     if (pl.bf16)
         RACE_TRY(launch_decode<bf16_t>(D, (const bf16_t *)q, (const bf16_t *)k, (const bf16_t *)v, W, (float *)state,
@@ -545,7 +563,7 @@ extern "C" int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, con
     if (pl.ws_fwd > RACE_NOALLOC_SCRATCH_BYTES) return RACE_ERR_SCRATCH_LIMIT;
     void *scratch = noalloc_scratch();
     if (!scratch) return RACE_ERR_CUDA;
-    pl.D.beta = beta;
+    pl.D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
     // state == nullptr: the forward keeps its sketch inside the scratch buffer
     if (pl.bf16)

@@ -113,7 +113,8 @@ def test_decode_rejects_before_launch(lib):
     dec = lambda *a: L.race_attn_decode(*a)
     assert dec(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, p, p, None) == -1
     assert dec(ctypes.byref(one), p, None, p, p, 10.0, 3, 3, p, p, None) == -1
-    assert dec(ctypes.byref(one), p, p, p, p, float("inf"), 3, 3, p, p, None) == -1
+    assert dec(ctypes.byref(one), p, p, p, p, float("nan"), 3, 3, p, p, None) == -1
+    assert dec(ctypes.byref(one), p, p, p, p, -1.0, 3, 3, p, p, None) == -1
     assert dec(ctypes.byref(one), p, p, p, p, 10.0, 3, 3, ctypes.c_void_p(4100), p, None) == -5
     assert dec(None, p, p, p, p, 10.0, 3, 3, p, p, None) == -1
 
@@ -152,3 +153,18 @@ def test_per_head_w_layout(lib):
             lib._shape_of(Q, torch.zeros(bad), 3, 2)
     with pytest.raises(ValueError):
         lib._shape_of(Q, torch.zeros((3, 2, 64), dtype=torch.float64), 3, 2)
+
+
+def test_beta_domain(lib):
+    """beta >= 0, finite or +inf (hard hashing); NaN and negatives are refused before any launch.
+    A short workspace makes an accepted beta stop at the workspace check instead."""
+    L = _raw(lib)
+    s = shape(lib)
+    p = ctypes.c_void_p(4096)
+    ws = lib.race_attn_workspace_bytes(s, 3, 3, 0, 0)
+    fwd = lambda b: L.race_attn_fwd(ctypes.byref(s), p, p, p, p, b, 3, 3, 0, p, None, p, ws - 256, None)
+    assert fwd(float("nan")) == -1
+    assert fwd(-0.5) == -1
+    assert fwd(float("-inf")) == -1
+    assert fwd(float("inf")) == -3
+    assert fwd(0.0) == -3

@@ -1,6 +1,8 @@
 """GPU parity: the library (called through its C ABI) against the float64 oracle on the same
 seeded inputs.  Small shapes span several token tiles and a ragged tail; the named workloads
 run at full size (sampled rows where the oracle would take too long)."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -9,7 +11,7 @@ import linear_lsh_sketch_gb300 as race
 from linear_lsh_sketch_gb300.workloads import CONFIGS, Workload, make_inputs
 import oracle
 from linear_lsh_sketch_gb300.workloads import as_oracle_array
-from parity import assert_close, gpu_run, inputs_on_gpu, oracle_run
+from parity import TOL, assert_close, gpu_run, inputs_on_gpu, oracle_run
 
 pytestmark = pytest.mark.gpu
 
@@ -339,3 +341,65 @@ def test_decode_per_head_w(dtype):
         o = race.race_attn_decode(*tok, W, w.beta, w.L, w.P, state)
         ref = oracle.decode_step(a["Q"][:, :, t], a["K"][:, :, t], a["V"][:, :, t], Wd, w.beta, ref_state)
         assert np.abs(o[:, :, 0].double().cpu().numpy() - ref).max() <= tol * np.abs(ref).max(), t
+
+
+# Hard hashing (beta = +inf).  Every Q and K row keeps each projection |w . xhat| >= 1e-3 away
+# from 0 (rows are redrawn until it does), so that the float32 projections on the GPU and the
+# float64 ones of the oracle give the same signs; each key is its query plus a little noise, so
+# that every query meets at least its own key in some table (no 0/0 rows).
+HARD = [
+    W_("hard_f32", 2, 2, 100, 64, 2, 3, False, "f32", beta=math.inf),
+    W_("hard_f32_c", 2, 2, 100, 64, 2, 3, True, "f32", beta=math.inf),
+    W_("hard_bf_nc", 1, 2, 700, 64, 3, 3, False, "bf16", beta=math.inf),
+    W_("hard_bf_c5", 1, 2, 700, 128, 3, 3, True, "bf16", beta=math.inf),
+    W_("hard_bf_lr64_c", 1, 2, 257, 64, 4, 4, True, "bf16", beta=math.inf),
+]
+
+
+def _hard_inputs(w, seed):
+    inp = make_inputs(w, seed=seed, device="cpu")
+    g = torch.Generator().manual_seed(seed + 1000)
+    Wd = inp["W"].double()
+    Q = inp["Q"].float()
+
+    def margins(X):  # smallest |w . xhat| per row, on the values as rounded to the tensors' dtype
+        Xr = X.to(w.torch_dtype).double()
+        Xh = Xr / Xr.norm(dim=-1, keepdim=True)
+        return torch.einsum("lpd,bhnd->bhnlp", Wd, Xh).abs().flatten(3).min(dim=3).values
+
+    def own_key_missed(Q, K):  # q_i and k_i share no corner in any table
+        sq = torch.einsum("lpd,bhnd->bhnlp", Wd, Q.to(w.torch_dtype).double()) > 0
+        sk = torch.einsum("lpd,bhnd->bhnlp", Wd, K.to(w.torch_dtype).double()) > 0
+        return ~(sq == sk).all(dim=4).any(dim=3)
+
+    K = Q + 0.05 * torch.randn(Q.shape, generator=g)
+    for _ in range(100):
+        bad = (margins(Q) < 1e-3) | (margins(K) < 1e-3) | own_key_missed(Q, K)
+        if not bad.any():
+            break
+        n = int(bad.sum())
+        Q[bad] = torch.randn((n, w.d), generator=g)
+        K[bad] = Q[bad] + 0.05 * torch.randn((n, w.d), generator=g)
+    assert not bad.any()
+    inp["Q"], inp["K"] = Q.to(w.torch_dtype), K.to(w.torch_dtype)
+    return {k: v.cuda() for k, v in inp.items()}
+
+
+@pytest.mark.parametrize("w", HARD, ids=lambda w: w.name)
+def test_hard_hash(w):
+    """beta = +inf: O and dV against the oracle's hard hash (sign bits); dQ, dK and
+    d(loss)/d(beta) exactly zero."""
+    inp = _hard_inputs(w, seed=7)
+    args = (inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal)
+    O = race.race_attn_fwd(*args)
+    dQ, dK, dV, db = race.race_attn_bwd(*args, inp["dO"], O=O, want_dbeta=True)
+    torch.cuda.synchronize()
+    assert torch.all(dQ == 0) and torch.all(dK == 0) and torch.all(db == 0)
+    got = (O.double().cpu().numpy(), dQ.double().cpu().numpy(), dK.double().cpu().numpy(),
+           dV.double().cpu().numpy())
+    ref = oracle_run(w, inp)
+    to, tg = TOL[w.dtype]
+    assert np.all(np.isfinite(got[0])) and np.all(np.isfinite(got[3]))
+    assert np.abs(got[0] - ref[0]).max() <= to * np.abs(ref[0]).max()
+    assert np.linalg.norm(got[3] - ref[3]) <= tg * np.linalg.norm(ref[3])
+    assert np.all(ref[1] == 0) and np.all(ref[2] == 0)
