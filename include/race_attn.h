@@ -156,6 +156,20 @@ int race_attn_decode(const race_shape *shape, const void *q, const void *k, cons
                      const float *W, float beta, int L, int P, void *state, void *o, void *stream);
 
 /*
+ * Exact angular attention, the kernel RACE attention estimates ("RACE Attention" slides, frame
+ * "Choose a nonnegative kernel that can be sketched", paper Eqs. (3)-(4)), in O(N^2):
+ *     O_i = sum_j S_ij V_j / sum_j S_ij,   S_ij = (1 - angle(Q_i, K_j) / pi)^gamma
+ * over j <= i when causal != 0.  With gamma = P it is the target of the P-bit hash (frame "A
+ * hash collision estimates a powered angular kernel"), the reference for measuring the
+ * approximation error of race_attn_fwd.  Q, K, V, O as for race_attn_fwd; gamma finite >= 0
+ * (0^0 = 1).  A zero row is at angle pi / 2 to every row.  A row whose weights are all zero
+ * (every admissible key antipodal) gets 0/0.  Quadratic in N: meant for evaluation sizes.
+ * No workspace; nothing is allocated; deterministic.
+ */
+int race_attn_angular(const race_shape *shape, const void *Q, const void *K, const void *V,
+                      float gamma, int causal, void *O, void *stream);
+
+/*
  * Device-side status of the last race_attn_fwd / race_attn_bwd call that used `workspace`.
  * Kernels that wait for asynchronous (bulk) copies bound every wait; if a wait runs out they
  * record it in the first word of the workspace and return early, leaving their outputs

@@ -14,7 +14,8 @@ __all__ = [
     "RaceAttnError", "race_attn_fwd", "race_attn_bwd", "race_attn_workspace_bytes",
     "race_attn_state_bytes", "race_attn_strerror", "race_attn_launch_count", "race_attn_profile",
     "race_attn_profile_read", "race_attn_profile_reset", "library_path", "load_library",
-    "race_attn_fwd_noalloc", "RACE_NOALLOC_SCRATCH_BYTES", "race_attn_status",
+    "race_attn_fwd_noalloc", "RACE_NOALLOC_SCRATCH_BYTES", "race_attn_status", "race_attn_decode",
+    "race_attn_angular",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -62,6 +63,8 @@ def load_library():
     L.race_attn_fwd_noalloc.restype = i
     L.race_attn_decode.argtypes = [shp, vp, vp, vp, vp, f, i, i, vp, vp, vp]
     L.race_attn_decode.restype = i
+    L.race_attn_angular.argtypes = [shp, vp, vp, vp, f, i, vp, vp]
+    L.race_attn_angular.restype = i
     L.race_attn_status.argtypes = [vp, vp]
     L.race_attn_status.restype = i
     L.race_attn_strerror.argtypes = [i]
@@ -245,6 +248,21 @@ def race_attn_decode(q, k, v, W, beta, L, P, state, o=None, stream=None):
     if rc != 0:
         raise RaceAttnError(rc, "race_attn_decode")
     return o
+
+
+def race_attn_angular(Q, K, V, gamma, causal, O=None, stream=None):
+    """Exact angular attention O_i = sum_j S_ij V_j / sum_j S_ij, S_ij = (1 - angle_ij / pi)^gamma
+    (j <= i when causal), O(N^2): the reference RACE attention approximates.  Returns O."""
+    shape = _shape_of(Q)
+    for n, t in (("K", K), ("V", V), ("Q", Q)):
+        _check_like(n, t, Q)
+    O = torch.empty_like(Q) if O is None else O
+    _check_like("O", O, Q)
+    rc = load_library().race_attn_angular(ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), float(gamma),
+                                          int(bool(causal)), _ptr(O), _stream(stream))
+    if rc != 0:
+        raise RaceAttnError(rc, "race_attn_angular")
+    return O
 
 
 def race_attn_fwd_noalloc(Q, K, V, W, beta, L, P, causal, O=None, stream=None):

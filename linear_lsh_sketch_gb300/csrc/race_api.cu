@@ -483,6 +483,25 @@ int race_attn_decode(const race_shape *shape, const void *q, const void *k, cons
     return RACE_OK;
 }
 
+int race_attn_angular(const race_shape *shape, const void *Q, const void *K, const void *V, float gamma, int causal,
+                      void *O, void *stream)
+{
+    Plan pl;
+    int rc = make_plan(shape, 1, 1, causal, pl);  // shape checks only: this path has no tables
+    if (rc != RACE_OK) return rc;
+    if (!std::isfinite(gamma) || gamma < 0.f) return RACE_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !O) return RACE_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return RACE_ERR_ALIGN;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (pl.bf16)
+        RACE_TRY(launch_angular<bf16_t>(pl.D, (const bf16_t *)Q, (const bf16_t *)K, (const bf16_t *)V, gamma,
+                                        causal != 0, (bf16_t *)O, st));
+    else
+        RACE_TRY(launch_angular<float>(pl.D, (const float *)Q, (const float *)K, (const float *)V, gamma,
+                                       causal != 0, (float *)O, st));
+    return RACE_OK;
+}
+
 int race_attn_status(const void *workspace, void *stream)
 {
     if (!workspace) return RACE_ERR_INVALID_ARG;

@@ -29,6 +29,11 @@ template <typename T>
 cudaError_t launch_decode(const Dims &D, const T *q, const T *k, const T *v, const float *W, float *S, T *o,
                           cudaStream_t st);
 
+// ---------------------------------------------------------------- exact angular attention
+template <typename T>
+cudaError_t launch_angular(const Dims &D, const T *Q, const T *K, const T *V, float gamma, int causal, T *O,
+                           cudaStream_t st);
+
 // ---------------------------------------------------------------- CUDA-core kernels
 enum class GenericKernel { Sketch, Readout, QueryBwd, KeyBwd, CausalFwd, CausalBwd };
 size_t generic_smem_bytes(const Dims &D, GenericKernel which);

@@ -168,3 +168,19 @@ def test_beta_domain(lib):
     assert fwd(float("-inf")) == -1
     assert fwd(float("inf")) == -3
     assert fwd(0.0) == -3
+
+
+def test_angular_rejects_before_launch(lib):
+    """race_attn_angular: gamma finite >= 0, non-null 16-byte aligned tensors, valid shape."""
+    L = _raw(lib)
+    s = shape(lib)
+    p = ctypes.c_void_p(4096)
+    ang = lambda sh, q, g, o: L.race_attn_angular(ctypes.byref(sh) if sh is not None else None, q, p, p, g, 0, o,
+                                                   None)
+    for g in (float("nan"), float("inf"), -1.0):
+        assert ang(s, p, g, p) == -1
+    assert ang(s, None, 2.0, p) == -1
+    assert ang(s, p, 2.0, None) == -1
+    assert ang(s, ctypes.c_void_p(4104), 2.0, p) == -5
+    assert ang(shape(lib, d=65), p, 2.0, p) == -1
+    assert ang(None, p, 2.0, p) == -1

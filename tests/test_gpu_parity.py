@@ -403,3 +403,70 @@ def test_hard_hash(w):
     assert np.abs(got[0] - ref[0]).max() <= to * np.abs(ref[0]).max()
     assert np.linalg.norm(got[3] - ref[3]) <= tg * np.linalg.norm(ref[3])
     assert np.all(ref[1] == 0) and np.all(ref[2] == 0)
+
+
+ANGULAR = [
+    W_("ang_f32", 2, 2, 77, 64, 3, 1, False, "f32"),
+    W_("ang_f32_c", 1, 3, 100, 32, 3, 1, True, "f32"),
+    W_("ang_bf", 1, 2, 300, 128, 3, 1, False, "bf16"),
+    W_("ang_bf_c", 2, 1, 129, 64, 3, 1, True, "bf16"),
+]
+
+
+@pytest.mark.parametrize("gamma", [0.0, 1.0, 3.0, 8.0, 2.5])
+@pytest.mark.parametrize("w", ANGULAR, ids=lambda w: w.name)
+def test_angular_matches_oracle(w, gamma):
+    """Exact angular attention (Eqs. 3-4) against the oracle's, with a zero Q row and a zero K
+    row; the float32 tolerance 1e-5 holds because the angle is formed stably (2 atan2 of the
+    half-chords), not as arccos of a rounded cosine."""
+    inp = inputs_on_gpu(w, seed=9)
+    inp["Q"][0, 0, 5] = 0
+    inp["K"][0, 0, 3] = 0
+    O = race.race_attn_angular(inp["Q"], inp["K"], inp["V"], gamma, w.causal)
+    torch.cuda.synchronize()
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V")}
+    ref = oracle.angular_forward(a["Q"], a["K"], a["V"], gamma, w.causal)
+    got = O.double().cpu().numpy()
+    tol = TOL[w.dtype][0]
+    assert np.abs(got - ref).max() <= tol * np.abs(ref).max()
+    again = race.race_attn_angular(inp["Q"], inp["K"], inp["V"], gamma, w.causal)
+    assert torch.equal(O, again)
+
+
+def test_angular_near_parallel_and_antipodal():
+    """Keys at angles 1e-4 and pi - 1e-4 from the query: the weights (1 - theta/pi)^8 are
+    1 - 2.5e-4 and 1.3e-35, which a float32 arccos of the cosine gets wrong by far more than the
+    float32 tolerance."""
+    d = 64
+    q = torch.zeros(d)
+    q[0] = 1.0
+    e = 1e-4
+    k0 = torch.zeros(d)
+    k0[0], k0[1] = math.cos(e), math.sin(e)
+    k1 = -k0
+    K = torch.stack([k0, k1, k0 * 2.0])
+    Q = torch.stack([q, q * 3.0, -q])
+    V = torch.randn((3, d), generator=torch.Generator().manual_seed(5))
+    Qg, Kg, Vg = (x[None, None].contiguous().cuda() for x in (Q, K, V))
+    O = race.race_attn_angular(Qg, Kg, Vg, 8.0, False)
+    a = {k: as_oracle_array(x) for k, x in (("Q", Qg), ("K", Kg), ("V", Vg))}
+    ref = oracle.angular_forward(a["Q"], a["K"], a["V"], 8.0, False)
+    assert np.abs(O.double().cpu().numpy() - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def test_race_error_against_angular_falls_with_beta_and_tables():
+    """The error bound's two terms ("The claimed bound separates bias and sampling error",
+    Theorem 2), measured on the GPU: RACE attention approaches P-powered angular attention as
+    beta grows (soft-hash bias) and as L grows (sampling error of the tables)."""
+    P, N, d = 2, 512, 64
+    g = torch.Generator().manual_seed(21)
+    Q, K, V = (torch.randn((1, 1, N, d), generator=g).cuda() for _ in range(3))
+    A = race.race_attn_angular(Q, K, V, float(P), False)
+
+    def err(beta, L):
+        W = torch.randn((L, P, d), generator=torch.Generator().manual_seed(22)).cuda()
+        O = race.race_attn_fwd(Q, K, V, W, beta, L, P, False)
+        return float(((O - A) ** 2).sum().sqrt() / math.sqrt(N))
+
+    assert err(50.0, 16) < 0.5 * err(0.5, 16)
+    assert err(50.0, 16) < 0.5 * err(50.0, 1)
