@@ -470,3 +470,24 @@ def test_race_error_against_angular_falls_with_beta_and_tables():
 
     assert err(50.0, 16) < 0.5 * err(0.5, 16)
     assert err(50.0, 16) < 0.5 * err(50.0, 1)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_hard_hash(dtype):
+    """Decode steps at beta = +inf against the oracle's hard-hash decode step (inputs as in
+    test_hard_hash: sign margins >= 1e-3, each query meets its own key)."""
+    w = W_("decode_hard", 2, 2, 24, 64, 3, 3, True, dtype, beta=math.inf)
+    inp = _hard_inputs(w, seed=14)
+    Q, K, V, W = inp["Q"], inp["K"], inp["V"], inp["W"]
+    B, H, N, d = Q.shape
+    state = torch.zeros((B, H, w.L << w.P, d + 1), dtype=torch.float32, device="cuda")
+    ref_state = np.zeros((B, H, w.L << w.P, d + 1))
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V")}
+    Wd = W.double().cpu().numpy()
+    tol = 2e-5 if dtype == "f32" else 1e-2
+    for t in range(N):
+        tok = [x[:, :, t:t + 1].contiguous() for x in (Q, K, V)]
+        o = race.race_attn_decode(*tok, W, w.beta, w.L, w.P, state)
+        ref = oracle.decode_step(a["Q"][:, :, t], a["K"][:, :, t], a["V"][:, :, t], Wd, w.beta, ref_state)
+        assert np.abs(o[:, :, 0].double().cpu().numpy() - ref).max() <= tol * np.abs(ref).max(), t
+    assert np.abs(state.double().cpu().numpy() - ref_state).max() <= 1e-5 * np.abs(ref_state).max()
