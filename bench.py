@@ -245,10 +245,12 @@ def run_ours(args, w):
     O, dQ, dK, dV = (torch.empty_like(Q) for _ in range(4))
     stream = torch.cuda.current_stream(dev)
 
+    dbeta = torch.empty((w.B, w.H), dtype=torch.float32, device=dev) if args.dbeta else None
+
     def step():
         race.race_attn_fwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, O=O, state=state, workspace=workspace)
         race.race_attn_bwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, dO, O=O, dQ=dQ, dK=dK, dV=dV, state=state,
-                           workspace=workspace)
+                           workspace=workspace, dbeta=dbeta)
 
     for _ in range(args.warmup):
         step()
@@ -307,7 +309,7 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": workload_config(w), "clocks": clocks, "roofline": roof,
+            "config": dict(workload_config(w), dbeta=bool(args.dbeta)), "clocks": clocks, "roofline": roof,
             "step_hbm": {"algorithmic_bytes": step_bytes, "achieved_gbs": step_bytes / (ms / 1000.0) / 1e9,
                          "frac": step_bytes / (ms / 1000.0) / 1e9 / hbm_peak,
                          "note": "12 * d * elem_bytes per (token, head): fwd reads Q,K,V writes O; "
@@ -389,6 +391,91 @@ def measure_e2e(args, w, race, inp, state, workspace):
             "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes}
 
 
+L2_BYTES = 129 * 2 ** 20
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 (FMA) x max SM clock
+
+
+def _timed(torch, dev, uuid, fn, warmup, steps, race):
+    """Mean ms per call of fn over `steps` calls (CUDA events on the current stream, after
+    `warmup` untimed calls), the clocks seen meanwhile and the library launches counted."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = race.race_attn_launch_count()
+    with ClockSampler(uuid) as clk:
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps, clk.summary(), race.race_attn_launch_count() - n0
+
+
+def run_row(args, w):
+    """One JSON line for a widening row: the causal decode step or exact angular attention."""
+    import torch
+
+    import linear_lsh_sketch_gb300 as race
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    race.load_library()
+    hbm_peak, _, peak_kind = load_peaks()
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    common = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+              "dtype": "bf16" if w.dtype == "bf16" else "f32"}
+    LR = w.L << w.P
+    if args.row == "decode":
+        per_head = LR * (w.d + 1) * 4
+        heads = max(args.heads, -(-2 * L2_BYTES // per_head))  # state at least twice L2: no flush
+        q, k, v = (torch.randn((1, heads, 1, w.d), generator=g, device=dev).to(w.torch_dtype) for _ in range(3))
+        W = torch.randn((w.L, w.P, w.d), generator=g, device=dev)
+        state = torch.randn((1, heads, LR, w.d + 1), generator=g, device=dev).abs_()
+        o = torch.empty_like(q)
+        ms, clocks, launches = _timed(torch, dev, uuid, lambda: race.race_attn_decode(
+            q, k, v, W, w.beta, w.L, w.P, state, o=o), args.warmup, args.steps, race)
+        alg = heads * (2 * per_head + 4 * w.d * w.elem_bytes)  # state read + write; q, k, v, o
+        gbs = alg / (ms / 1000.0) / 1e9
+        line = dict(common, metric="RACE causal decode step tokens/s (one token per (b, h))",
+                    value=heads / (ms / 1000.0), unit="tokens/s", ms_per_step=ms,
+                    config={"workload": "decode, %d heads, d %d, (P, L) = (%d, %d), state %.2f GB > L2, "
+                            "no flush" % (heads, w.d, w.P, w.L, heads * per_head / 1e9),
+                            "heads": heads, "d": w.d, "P": w.P, "L": w.L, "io_dtype": w.dtype},
+                    roofline={"bound": "hbm", "kernel": "decode", "achieved": gbs, "peak": hbm_peak,
+                              "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
+                              "algorithmic_bytes_per_launch": alg, "traffic": None},
+                    clocks=clocks, gpu_launches=launches)
+    else:
+        n = args.tokens or 8192
+        ws = w.scaled(N=n)
+        Q, K, V = (torch.randn((ws.B, ws.H, n, ws.d), generator=g, device=dev).to(ws.torch_dtype)
+                   for _ in range(3))
+        O = torch.empty_like(Q)
+        gamma = float(ws.P)
+        ms, clocks, launches = _timed(torch, dev, uuid, lambda: race.race_attn_angular(
+            Q, K, V, gamma, ws.causal, O=O), args.warmup, args.steps, race)
+        pairs = ws.B * ws.H * (n * (n + 1) // 2 if ws.causal else n * n)
+        flops = pairs * 8 * ws.d  # |a - b|^2, |a + b|^2 (6 d) and the weighted value sum (2 d)
+        tf = flops / (ms / 1000.0) / 1e12
+        line = dict(common, metric="exact angular attention (gamma = P) pair evaluations/s",
+                    value=pairs / (ms / 1000.0), unit="pairs/s", ms_per_step=ms,
+                    config={"workload": "angular attention, B %d H %d N %d d %d gamma %g causal %s" %
+                            (ws.B, ws.H, n, ws.d, gamma, ws.causal), "io_dtype": ws.dtype,
+                            "l2": "O(N^2) arithmetic on L2-resident rows; no flush"},
+                    roofline={"bound": "alu", "kernel": "angular", "achieved": tf, "peak": FP32_ALU_TFLOPS,
+                              "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
+                              "peak_kind": "FP32 CUDA-core FMA rate from unit counts and the 2070 MHz clock",
+                              "flops_per_launch": flops, "traffic": None},
+                    clocks=clocks, gpu_launches=launches)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,13 +489,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override N (sequence length) of the workload, e.g. for a small profiling capture")
+    ap.add_argument("--dbeta", action="store_true", help="the backward also writes d(loss)/d(beta)")
+    ap.add_argument("--row", choices=["step", "decode", "angular"], default="step",
+                    help="decode: one causal decode step per (b, h) of --heads heads; angular: exact angular "
+                         "attention at the workload's d and --tokens (default 8192) tokens")
+    ap.add_argument("--heads", type=int, default=1024, help="(b, h) problems of the decode batch")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
     from linear_lsh_sketch_gb300.workloads import CONFIGS
     w = CONFIGS[args.workload]
     if args.tokens:
         w = w.scaled(N=args.tokens, name="%s_N%d" % (w.name, args.tokens))
-    if args.impl == "reference":
+    if args.row != "step":
+        run_row(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)
