@@ -456,20 +456,32 @@ def test_angular_near_parallel_and_antipodal():
 
 def test_race_error_against_angular_falls_with_beta_and_tables():
     """The error bound's two terms ("The claimed bound separates bias and sampling error",
-    Theorem 2), measured on the GPU: RACE attention approaches P-powered angular attention as
-    beta grows (soft-hash bias) and as L grows (sampling error of the tables)."""
-    P, N, d = 2, 512, 64
+    Theorem 2), measured on the GPU against P-powered angular attention.  Sampling error: at
+    beta = 50 one table is far worse than 16.  Soft-hash bias: with the output averaged over 32
+    independent 16-table draws, so that sampling noise is small, beta = 2 beats beta = 0.5.  On
+    these seeded inputs the float64 oracle gives 0.146 vs 0.539 and 0.019 vs 0.050; beyond
+    beta ~ 2 the averaged error sits on the remaining sampling noise."""
+    P, N, d, L, M = 2, 512, 64, 16, 32
     g = torch.Generator().manual_seed(21)
     Q, K, V = (torch.randn((1, 1, N, d), generator=g).cuda() for _ in range(3))
     A = race.race_attn_angular(Q, K, V, float(P), False)
 
-    def err(beta, L):
-        W = torch.randn((L, P, d), generator=torch.Generator().manual_seed(22)).cuda()
-        O = race.race_attn_fwd(Q, K, V, W, beta, L, P, False)
+    def rms(O):
         return float(((O - A) ** 2).sum().sqrt() / math.sqrt(N))
 
-    assert err(50.0, 16) < 0.5 * err(0.5, 16)
-    assert err(50.0, 16) < 0.5 * err(50.0, 1)
+    def single(beta, Lx):
+        W = torch.randn((Lx, P, d), generator=torch.Generator().manual_seed(22)).cuda()
+        return rms(race.race_attn_fwd(Q, K, V, W, beta, Lx, P, False))
+
+    def averaged(beta):
+        acc = torch.zeros_like(A)
+        for m in range(M):
+            W = torch.randn((L, P, d), generator=torch.Generator().manual_seed(100 + m)).cuda()
+            acc += race.race_attn_fwd(Q, K, V, W, beta, L, P, False)
+        return rms(acc / M)
+
+    assert single(50.0, 16) < 0.5 * single(50.0, 1)
+    assert averaged(2.0) < 0.6 * averaged(0.5)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
