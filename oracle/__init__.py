@@ -40,7 +40,7 @@ def lib():
         L.race_oracle_backward.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
                                            _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp,
-                                           ctypes.c_int]
+                                           _vp, ctypes.c_int]
         L.race_oracle_decode_step.argtypes = [_i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                               ctypes.c_int, _vp, _vp]
@@ -148,10 +148,12 @@ def forward(Q, K, V, W, beta, causal, normalize=True, rows=None, want_sketch=Fal
     return (O, sk) if want_sketch else O
 
 
-def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0, want_dbeta=False):
+def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0, want_dbeta=False,
+             want_dW=False):
     """(dQ, dK, dV) for the output O and its cotangent dO; rows as in `forward`.  With
-    want_dbeta also d(loss)/d(beta) per (b, h) [B, H], summed over every token.  W and beta as in
-    `forward` (a hard hash passes no gradient to Q and K)."""
+    want_dbeta also d(loss)/d(beta) per (b, h) [B, H], and with want_dW d(loss)/d(W) per (b, h)
+    [B, H, L, P, d], both summed over every token and appended in that order.  W and beta as in
+    `forward` (a hard hash passes no gradient to Q, K, beta or W)."""
     Q, e = _tokens(Q)
     K, _ = _tokens(K)
     V, _ = _tokens(V)
@@ -165,10 +167,12 @@ def backward(Q, K, V, dO, W, beta, causal, normalize=True, rows=None, nthreads=0
     dK = np.empty((B, H, nout, d))
     dV = np.empty((B, H, nout, d))
     db = np.zeros((B, H)) if want_dbeta else None
+    dW = np.zeros((B, H, L, P, d)) if want_dW else None
     _check(lib().race_oracle_backward(B, H, N, d, e, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(W),
                                       ph, L, P, float(beta), int(causal), int(normalize), _ptr(r), nr,
-                                      _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(db), int(nthreads)), "backward")
-    return (dQ, dK, dV, db) if want_dbeta else (dQ, dK, dV)
+                                      _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(db), _ptr(dW), int(nthreads)),
+           "backward")
+    return (dQ, dK, dV) + ((db,) if want_dbeta else ()) + ((dW,) if want_dW else ())
 
 
 def decode_step(q, k, v, W, beta, state, normalize=True):

@@ -120,7 +120,8 @@ static void features(const double *x, int64_t d, const double *W, int L, int P, 
  */
 static void features_backward(const double *x, const double *xhat, const double *u,
                               const double *phi, const double *dphi, int64_t d, const double *W,
-                              int L, int P, double beta, int normalize, double *dxhat, double *dx)
+                              int L, int P, double beta, int normalize, double *dxhat, double *dx,
+                              double *dz_out)
 {
     const int R = 1 << P;
     for (int64_t k = 0; k < d; ++k) dxhat[k] = 0.0;
@@ -135,6 +136,7 @@ static void features_backward(const double *x, const double *xhat, const double 
             du = isinf(beta) ? 0.0 : du * beta;  /* a hard hash passes no gradient */
             double ut = u[(int64_t)l * P + t];
             double dz = du * (1.0 - ut * ut);
+            if (dz_out) dz_out[(int64_t)l * P + t] = dz;
             const double *w = W + ((int64_t)l * P + t) * d;
             for (int64_t k = 0; k < d; ++k) dxhat[k] += dz * w[k];
         }
@@ -178,6 +180,16 @@ static double features_dbeta(const double *u, const double *phi, const double *d
         }
     }
     return acc;
+}
+
+/*
+ * d(loss)/d(W) from one row: z^(l)_t = w^(l)_t . xhat, so the row adds dz^(l)_t xhat to the
+ * gradient of hyperplane row (l, t).  dW: [L*P, d].
+ */
+static void add_dW(double *dW, const double *dz, const double *xhat, int64_t d, int L, int P)
+{
+    for (int64_t j = 0; j < (int64_t)L * P; ++j)
+        for (int64_t k = 0; k < d; ++k) dW[j * d + k] += dz[j] * xhat[k];
 }
 
 /* Sketch update with one key: S[j][c] += phi_j * v_c for the d value columns, S[j][d] += phi_j. */
@@ -407,19 +419,23 @@ int race_oracle_forward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
  *   G = sum_i phi_Q(i) [dnum_i | dden_i]   (non-causal: all i; causal: suffix over i >= j),
  *   dV_j = G_A^T phi_K(j),   dphi_K(j) = G_A V_j + G_B,
  * followed by `features_backward` for each side.  When `dbeta` is given (B * H values) every
- * token's query and key features also contribute d(loss)/d(beta) (`features_dbeta`), whatever
- * `rows` selects for dQ, dK, dV.
+ * token's query and key features also contribute d(loss)/d(beta) (`features_dbeta`), and when
+ * `dW` is given ([B * H, L * P * d], zeroed by the caller) every token also adds dz xhat to the
+ * rows of the hyperplanes it was hashed with (`add_dW`), whatever `rows` selects for dQ, dK, dV.
+ * Both are per (b, h); the gradient of a shared W is their sum over (b, h), of a per-head W
+ * the sum over b.
  */
 int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                          const void *Q, const void *K, const void *V, const void *dO,
                          const double *W, int per_head, int L, int P, double beta, int causal,
                          int normalize,
                          const int64_t *rows, int64_t nrows, double *dQ, double *dK, double *dV,
-                         double *dbeta, int nthreads)
+                         double *dbeta, double *dW, int nthreads)
 {
     if (check_args(B, H, N, d, elem, L, P, rows, nrows)) return -1;
     const int64_t R = (int64_t)1 << P, nfeat = (int64_t)L * R;
     const int64_t nout = rows ? nrows : N;
+    const int wantg = dbeta != NULL || dW != NULL;  /* every token's features count */
     int status = 0;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -435,11 +451,11 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
         double *g = malloc(sizeof(double) * d), *dnum = malloc(sizeof(double) * d);
         double *dxhat = malloc(sizeof(double) * d), *dx = malloc(sizeof(double) * d);
         double *u = malloc(sizeof(double) * L * P), *phi = malloc(sizeof(double) * nfeat);
-        double *dphi = malloc(sizeof(double) * nfeat);
+        double *dphi = malloc(sizeof(double) * nfeat), *dz = malloc(sizeof(double) * L * P);
         /* per-token den_i and (dO_i . O_i), needed by the key side */
         double *den_all = malloc(sizeof(double) * N), *dOO_all = malloc(sizeof(double) * N);
         if (!S || !G || !x || !xhat || !v || !num || !g || !dnum || !dxhat || !dx || !u ||
-            !phi || !dphi || !den_all || !dOO_all) {
+            !phi || !dphi || !dz || !den_all || !dOO_all) {
 #pragma omp atomic write
             status = -2;
         } else {
@@ -471,7 +487,7 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         row[d] += phi[j] * dden;
                     }
                     const int want = !rows || (o < nout && rows[o] == i);
-                    if (!want && !dbeta) continue;
+                    if (!want && !wantg) continue;
                     for (int64_t j = 0; j < nfeat; ++j) {
                         const double *row = S + j * (d + 1);
                         double s = row[d] * dden;
@@ -479,8 +495,10 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         dphi[j] = s;
                     }
                     if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P, beta);
+                    if (!want && !dW) continue;
+                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx, dz);
+                    if (dW) add_dW(dW + bh * L * P * d, dz, xhat, d, L, P);
                     if (!want) continue;
-                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx);
                     memcpy(dQbh + o * d, dx, sizeof(double) * d);
                     ++o;
                 }
@@ -488,7 +506,7 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                 int64_t o2 = 0;
                 for (int64_t j0 = 0; j0 < N; ++j0) {
                     const int want = rows ? (o2 < nout && rows[o2] == j0) : 1;
-                    if (!want && !dbeta) {
+                    if (!want && !wantg) {
                         if (!rows || o2 >= nout) break;
                         continue;
                     }
@@ -507,8 +525,10 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         dphi[j] = s;
                     }
                     if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P, beta);
+                    if (!want && !dW) continue;
+                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx, dz);
+                    if (dW) add_dW(dW + bh * L * P * d, dz, xhat, d, L, P);
                     if (!want) continue;
-                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx);
                     memcpy(dKbh + o2 * d, dx, sizeof(double) * d);
                     ++o2;
                 }
@@ -529,7 +549,7 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                     den_all[t] = den;
                     dOO_all[t] = dOO;
                     const int want = !rows || (o < nout && rows[o] == t);
-                    if (!want && !dbeta) continue;
+                    if (!want && !wantg) continue;
                     double dden = -dOO / den;
                     for (int64_t j = 0; j < nfeat; ++j) {
                         const double *row = S + j * (d + 1);
@@ -538,14 +558,16 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         dphi[j] = s;
                     }
                     if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P, beta);
+                    if (!want && !dW) continue;
+                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx, dz);
+                    if (dW) add_dW(dW + bh * L * P * d, dz, xhat, d, L, P);
                     if (!want) continue;
-                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx);
                     memcpy(dQbh + o * d, dx, sizeof(double) * d);
                     ++o;
                 }
                 /* reverse order: suffix sums G_j = sum_{t >= j} phi_Q(t) [dnum_t | dden_t], dK, dV */
                 int64_t o2 = nout - 1;
-                for (int64_t t = N - 1; t >= 0 && (o2 >= 0 || dbeta); --t) {
+                for (int64_t t = N - 1; t >= 0 && (o2 >= 0 || wantg); --t) {
                     load_row(Q, elem, base + t * d, d, x);
                     features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
                     load_row(dO, elem, base + t * d, d, g);
@@ -557,7 +579,7 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         row[d] += phi[j] * dden;
                     }
                     const int want = rows ? (o2 >= 0 && rows[o2] == t) : 1;
-                    if (!want && !dbeta) continue;
+                    if (!want && !wantg) continue;
                     int64_t slot = rows ? o2 : t;
                     load_row(K, elem, base + t * d, d, x);
                     features(x, d, Wh, L, P, beta, normalize, xhat, u, phi);
@@ -574,15 +596,17 @@ int race_oracle_backward(int64_t B, int64_t H, int64_t N, int64_t d, int elem,
                         dphi[j] = s;
                     }
                     if (dbeta) dbeta[bh] += features_dbeta(u, phi, dphi, L, P, beta);
+                    if (!want && !dW) continue;
+                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx, dz);
+                    if (dW) add_dW(dW + bh * L * P * d, dz, xhat, d, L, P);
                     if (!want) continue;
-                    features_backward(x, xhat, u, phi, dphi, d, Wh, L, P, beta, normalize, dxhat, dx);
                     memcpy(dKbh + slot * d, dx, sizeof(double) * d);
                     --o2;
                 }
             }
         }
         free(S); free(G); free(x); free(xhat); free(v); free(num); free(g); free(dnum);
-        free(dxhat); free(dx); free(u); free(phi); free(dphi); free(den_all); free(dOO_all);
+        free(dxhat); free(dx); free(u); free(phi); free(dphi); free(dz); free(den_all); free(dOO_all);
     }
     return status;
 }

@@ -284,3 +284,69 @@ def test_soft_race_error_falls_with_beta_and_tables():
 
     assert err(50.0, 4096) < 0.5 * err(0.5, 4096)
     assert err(50.0, 4096) < 0.5 * err(50.0, 8)
+
+
+# ------------------------------------------------------------------ d(loss)/d(W)
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dW_finite_differences_shared(causal):
+    """The hyperplanes W are the layer's other parameter next to beta (their rows give
+    u = tanh(W xhat), "Soft corner assignments make hashing differentiable"): d(sum O * dO)/dW,
+    summed over (b, h) for a shared W, against central differences of the product-form brute
+    force on every entry."""
+    B, H, N, d, P, L, beta = 1, 2, 7, 4, 2, 2, 3.0
+    Q, K, V, dO = (_rand((B, H, N, d), s) for s in (410, 411, 412, 413))
+    W = _rand((L, P, d), 414)
+    *_, dW = oracle.backward(Q, K, V, dO, W, beta, causal, want_dW=True)
+    got = dW.sum(axis=(0, 1))
+
+    def loss(Wx):
+        return sum(float((_attention_bruteforce(Q[0, h], K[0, h], V[0, h], Wx, beta, causal) * dO[0, h]).sum())
+                   for h in range(H))
+
+    eps = 1e-6
+    fd = np.zeros_like(W)
+    for idx in np.ndindex(*W.shape):
+        Wp, Wm = W.copy(), W.copy()
+        Wp[idx] += eps
+        Wm[idx] -= eps
+        fd[idx] = (loss(Wp) - loss(Wm)) / (2 * eps)
+    assert np.abs(fd - got).max() <= 1e-6 * np.abs(fd).max() + 1e-9
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dW_finite_differences_per_head(causal):
+    """Per-head W: head h's gradient is the sum over the batch of its (b, h) terms (B = 2)."""
+    B, H, N, d, P, L, beta = 2, 2, 5, 4, 2, 1, 2.0
+    Q, K, V, dO = (_rand((B, H, N, d), s) for s in (420, 421, 422, 423))
+    W = _rand((H, L, P, d), 424)
+    *_, dW = oracle.backward(Q, K, V, dO, W, beta, causal, want_dW=True)
+    got = dW.sum(axis=0)  # [H, L, P, d]
+    eps = 1e-6
+    for h in range(H):
+        def loss(Wx):
+            return sum(float((_attention_bruteforce(Q[b, h], K[b, h], V[b, h], Wx, beta, causal)
+                              * dO[b, h]).sum()) for b in range(B))
+        fd = np.zeros_like(W[h])
+        for idx in np.ndindex(*W[h].shape):
+            Wp, Wm = W[h].copy(), W[h].copy()
+            Wp[idx] += eps
+            Wm[idx] -= eps
+            fd[idx] = (loss(Wp) - loss(Wm)) / (2 * eps)
+        assert np.abs(fd - got[h]).max() <= 1e-6 * np.abs(fd).max() + 1e-9, h
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dW_sums_every_token_whatever_rows(causal):
+    """Like d(loss)/d(beta), dW covers every token even when dQ, dK, dV are asked for a few rows;
+    at beta = +inf (hard hashing) it is zero."""
+    B, H, N, d, P, L = 1, 2, 13, 6, 3, 2
+    Q, K, V, dO = (_rand((B, H, N, d), s) for s in (430, 431, 432, 433))
+    W = _rand((L, P, d), 434)
+    full = oracle.backward(Q, K, V, dO, W, 4.0, causal, want_dbeta=True, want_dW=True)
+    part = oracle.backward(Q, K, V, dO, W, 4.0, causal, rows=[2, 9], want_dbeta=True, want_dW=True)
+    np.testing.assert_allclose(part[3], full[3], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(part[4], full[4], rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(part[0], full[0][:, :, [2, 9]])
+    *_, dWh = oracle.backward(Q, K, V, dO, W, math.inf, causal, want_dW=True)
+    assert np.all(dWh == 0)
