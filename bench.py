@@ -302,7 +302,13 @@ def run_ours(args, w):
 
     e2e = None
     if rank == 0 and not args.no_e2e:
-        e2e = measure_e2e(args, w, race, inp, state, workspace)
+        try:
+            e2e = measure_e2e_pipelined(args, w, race, inp) if w.B * w.H > 1 else None
+        except Exception as exc:  # keep the sequential measurement
+            print("pipelined e2e failed (%s); sequential copies instead" % exc, file=sys.stderr)
+            e2e = None
+        if e2e is None:
+            e2e = measure_e2e(args, w, race, inp, state, workspace)
 
     if rank == 0:
         line = {
@@ -346,6 +352,71 @@ def sources_sha():
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
+
+
+def measure_e2e_pipelined(args, w, race, inp):
+    """The e2e metric with the host link's two directions overlapped: the (b, h) problems are
+    independent, so each is one public-API call pair (forward + backward, B = H = 1) on a
+    compute stream, fed by pinned host -> device copies on a second stream and drained by
+    device -> host copies on a third; events order the three per (b, h)."""
+    import torch
+
+    dev = inp["Q"].device
+    B, H, N, d = inp["Q"].shape
+    host_in = {k: torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True) for k in ("Q", "K", "V", "dO")}
+    host_out = [torch.empty(inp["Q"].shape, dtype=inp["Q"].dtype, pin_memory=True) for _ in range(4)]
+    for k in host_in:
+        host_in[k].copy_(inp[k])
+    dev_in = {k: torch.empty_like(inp[k]) for k in ("Q", "K", "V", "dO")}
+    outs = [torch.empty_like(inp["Q"]) for _ in range(4)]
+    W = inp["W"]
+    one = race.make_shape(1, 1, N, d, w.torch_dtype)
+    ws = torch.empty(max(race.race_attn_workspace_bytes(one, w.L, w.P, w.causal, b) for b in (0, 1)),
+                     dtype=torch.uint8, device=dev)
+    st = torch.empty(race.race_attn_state_bytes(one, w.L, w.P, w.causal), dtype=torch.uint8, device=dev)
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    ev_in = [torch.cuda.Event() for _ in heads]
+    ev_cmp = [torch.cuda.Event() for _ in heads]
+
+    def sl(t, b, h):
+        return t[b:b + 1, h:h + 1]
+
+    def step():
+        for i, (b, h) in enumerate(heads):
+            with torch.cuda.stream(s_in):
+                for k in dev_in:
+                    sl(dev_in[k], b, h).copy_(sl(host_in[k], b, h), non_blocking=True)
+                ev_in[i].record(s_in)
+        for i, (b, h) in enumerate(heads):
+            s_cmp.wait_event(ev_in[i])
+            q, k_, v, g = (sl(dev_in[x], b, h) for x in ("Q", "K", "V", "dO"))
+            o, dq, dk, dv = (sl(x, b, h) for x in outs)
+            race.race_attn_fwd(q, k_, v, W, w.beta, w.L, w.P, w.causal, O=o, state=st, workspace=ws,
+                               stream=s_cmp)
+            race.race_attn_bwd(q, k_, v, W, w.beta, w.L, w.P, w.causal, g, O=o, dQ=dq, dK=dk, dV=dv,
+                               state=st, workspace=ws, stream=s_cmp)
+            ev_cmp[i].record(s_cmp)
+            s_out.wait_event(ev_cmp[i])
+            with torch.cuda.stream(s_out):
+                for hd, dd in zip(host_out, outs):
+                    sl(hd, b, h).copy_(sl(dd, b, h), non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    steps = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for _ in range(steps):
+        s_in.wait_stream(s_out)  # a step starts when the previous one's results are home
+        step()
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = inp["Q"].numel() * inp["Q"].element_size()
+    return {"value": w.B * w.N / (ms / 1000.0), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
+            "schedule": "per (b, h): H2D, compute and D2H on three streams, overlapped"}
 
 
 def measure_e2e(args, w, race, inp, state, workspace):
