@@ -215,6 +215,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def kernel_table(prof, w, hbm_peak):
+    """Per kernel of the timed region: launches, total ms, share of the kernel time, ms per launch
+    and, for the kernels with compulsory bytes in KERNEL_BYTES, achieved GB/s and its fraction of
+    the HBM peak.  prof: {name: (launches, total ms)}."""
+    total = sum(v[1] for v in prof.values())
+    out = {}
+    for name, (nl, ms) in prof.items():
+        row = {"launches": nl, "ms_total": ms, "share": ms / max(total, 1e-9),
+               "ms_per_launch": ms / max(nl, 1)}
+        if name in KERNEL_BYTES and nl > 0 and ms > 0:
+            mult, extra = KERNEL_BYTES[name]
+            nbytes = (mult * w.d * w.elem_bytes + extra) * w.B * w.H * w.N
+            gbs = nbytes / (row["ms_per_launch"] / 1000.0) / 1e9
+            row.update(achieved_gbs=gbs, frac=gbs / hbm_peak)
+        out[name] = row
+    return out
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -295,8 +313,7 @@ def run_ours(args, w):
                 "frac": achieved / hbm_peak, "peak_kind": peak_kind + " (copy bandwidth)",
                 "algorithmic_bytes_per_launch": alg, "ms_per_launch": per_launch_ms,
                 "traffic": traffic_for(name, w)}
-    kernels = {k: {"launches": v[0], "ms_total": v[1], "share": v[1] / max(1e-9, sum(x[1] for x in prof.values()))}
-               for k, v in prof.items()}
+    kernels = kernel_table(prof, w, hbm_peak)
     step_bytes = 12 * w.d * w.elem_bytes * w.B * w.H * w.N
     clocks = clk.summary()
 

@@ -60,3 +60,19 @@ def test_single_rank_defaults(monkeypatch):
         monkeypatch.delenv(k, raising=False)
     assert bench.env_rank() == (0, 1, 0)
     assert bench.weak_scaling_tokens_per_s(1, 12_000_000, 50.0) == pytest.approx(2.4e8)
+
+
+def test_kernel_table():
+    """Per-kernel shares and HBM fractions from a profile: compulsory bytes per (token, head)
+    times the tokens, over the time per launch; kernels without a byte count get no fraction."""
+    import bench
+    from linear_lsh_sketch_gb300.workloads import CONFIGS
+
+    w = CONFIGS["c5_bf16_causal_12m"]
+    prof = {"tc5_causal_fwd": (2, 18.0), "combine": (4, 0.2), "tc5_causal_bwd_kv": (2, 34.0)}
+    t = bench.kernel_table(prof, w, 6800.0)
+    assert abs(sum(r["share"] for r in t.values()) - 1.0) < 1e-12
+    fwd = t["tc5_causal_fwd"]
+    want = 4 * w.d * 2 * w.B * w.H * w.N / (9.0 / 1000.0) / 1e9
+    assert abs(fwd["achieved_gbs"] - want) < 1e-6 * want and abs(fwd["frac"] - want / 6800.0) < 1e-12
+    assert "frac" not in t["combine"] and t["combine"]["ms_per_launch"] == 0.05
