@@ -503,3 +503,24 @@ def test_decode_hard_hash(dtype):
         ref = oracle.decode_step(a["Q"][:, :, t], a["K"][:, :, t], a["V"][:, :, t], Wd, w.beta, ref_state)
         assert np.abs(o[:, :, 0].double().cpu().numpy() - ref).max() <= tol * np.abs(ref).max(), t
     assert np.abs(state.double().cpu().numpy() - ref_state).max() <= 1e-5 * np.abs(ref_state).max()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_split_count_equivalence(causal, dtype):
+    """The decomposition a multi-GPU run would use, on one GPU: each sequence is cut into segments
+    whose sketch sums are combined (non-causal) or scanned (causal) in a fixed order, and the
+    planner picks the segment count from B * H (about two CTAs per SM over all (b, h)).  One
+    sequence alone (B * H = 1: 157 segments at N = 20000) and the same sequence as one of 8 heads
+    (32 segments) give the same O, dQ, dK, dV up to float32 rounding (bf16 outputs: a last-bit
+    flip of the rounded value)."""
+    w8 = W_("split8", 1, 8, 20000, 64, 3, 3, causal, dtype)
+    inp = inputs_on_gpu(w8, seed=15)
+    full = gpu_run(w8, inp)
+    w1 = W_("split1", 1, 1, 20000, 64, 3, 3, causal, dtype)
+    one = {k: (v[:, 3:4].contiguous() if v.dim() == 4 else v) for k, v in inp.items()}
+    alone = gpu_run(w1, one)
+    tol = 1e-5 if dtype == "f32" else 1e-2
+    for name, a, b in zip(("O", "dQ", "dK", "dV"), full, alone):
+        e = np.abs(a[:, 3:4] - b).max() / np.abs(b).max()
+        assert e <= tol, "%s %s differs by %.2e across split counts" % (name, dtype, e)
