@@ -263,10 +263,12 @@ def run_ours(args, w):
     O, dQ, dK, dV = (torch.empty_like(Q) for _ in range(4))
     stream = torch.cuda.current_stream(dev)
 
+    dbeta = torch.empty((w.B, w.H), dtype=torch.float32, device=dev) if args.dbeta else None
+
     def step():
         race.race_attn_fwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, O=O, state=state, workspace=workspace)
         race.race_attn_bwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, dO, O=O, dQ=dQ, dK=dK, dV=dV, state=state,
-                           workspace=workspace)
+                           workspace=workspace, dbeta=dbeta)
 
     for _ in range(args.warmup):
         step()
@@ -317,14 +319,20 @@ def run_ours(args, w):
 
     e2e = None
     if rank == 0 and not args.no_e2e:
-        e2e = measure_e2e(args, w, race, inp, state, workspace)
+        try:
+            e2e = measure_e2e_pipelined(args, w, race, inp) if w.B * w.H > 1 else None
+        except Exception as exc:  # keep the sequential measurement
+            print("pipelined e2e failed (%s); sequential copies instead" % exc, file=sys.stderr)
+            e2e = None
+        if e2e is None:
+            e2e = measure_e2e(args, w, race, inp, state, workspace)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": workload_config(w), "clocks": clocks, "roofline": roof,
+            "config": dict(workload_config(w), dbeta=bool(args.dbeta)), "clocks": clocks, "roofline": roof,
             "step_hbm": {"algorithmic_bytes": step_bytes, "achieved_gbs": step_bytes / (ms / 1000.0) / 1e9,
                          "frac": step_bytes / (ms / 1000.0) / 1e9 / hbm_peak,
                          "note": "12 * d * elem_bytes per (token, head): fwd reads Q,K,V writes O; "
@@ -361,6 +369,71 @@ def sources_sha():
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
+
+
+def measure_e2e_pipelined(args, w, race, inp):
+    """The e2e metric with the host link's two directions overlapped: the (b, h) problems are
+    independent, so each is one public-API call pair (forward + backward, B = H = 1) on a
+    compute stream, fed by pinned host -> device copies on a second stream and drained by
+    device -> host copies on a third; events order the three per (b, h)."""
+    import torch
+
+    dev = inp["Q"].device
+    B, H, N, d = inp["Q"].shape
+    host_in = {k: torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True) for k in ("Q", "K", "V", "dO")}
+    host_out = [torch.empty(inp["Q"].shape, dtype=inp["Q"].dtype, pin_memory=True) for _ in range(4)]
+    for k in host_in:
+        host_in[k].copy_(inp[k])
+    dev_in = {k: torch.empty_like(inp[k]) for k in ("Q", "K", "V", "dO")}
+    outs = [torch.empty_like(inp["Q"]) for _ in range(4)]
+    W = inp["W"]
+    one = race.make_shape(1, 1, N, d, w.torch_dtype)
+    ws = torch.empty(max(race.race_attn_workspace_bytes(one, w.L, w.P, w.causal, b) for b in (0, 1)),
+                     dtype=torch.uint8, device=dev)
+    st = torch.empty(race.race_attn_state_bytes(one, w.L, w.P, w.causal), dtype=torch.uint8, device=dev)
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    ev_in = [torch.cuda.Event() for _ in heads]
+    ev_cmp = [torch.cuda.Event() for _ in heads]
+
+    def sl(t, b, h):
+        return t[b:b + 1, h:h + 1]
+
+    def step():
+        for i, (b, h) in enumerate(heads):
+            with torch.cuda.stream(s_in):
+                for k in dev_in:
+                    sl(dev_in[k], b, h).copy_(sl(host_in[k], b, h), non_blocking=True)
+                ev_in[i].record(s_in)
+        for i, (b, h) in enumerate(heads):
+            s_cmp.wait_event(ev_in[i])
+            q, k_, v, g = (sl(dev_in[x], b, h) for x in ("Q", "K", "V", "dO"))
+            o, dq, dk, dv = (sl(x, b, h) for x in outs)
+            race.race_attn_fwd(q, k_, v, W, w.beta, w.L, w.P, w.causal, O=o, state=st, workspace=ws,
+                               stream=s_cmp)
+            race.race_attn_bwd(q, k_, v, W, w.beta, w.L, w.P, w.causal, g, O=o, dQ=dq, dK=dk, dV=dv,
+                               state=st, workspace=ws, stream=s_cmp)
+            ev_cmp[i].record(s_cmp)
+            s_out.wait_event(ev_cmp[i])
+            with torch.cuda.stream(s_out):
+                for hd, dd in zip(host_out, outs):
+                    sl(hd, b, h).copy_(sl(dd, b, h), non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    steps = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for _ in range(steps):
+        s_in.wait_stream(s_out)  # a step starts when the previous one's results are home
+        step()
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = inp["Q"].numel() * inp["Q"].element_size()
+    return {"value": w.B * w.N / (ms / 1000.0), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
+            "schedule": "per (b, h): H2D, compute and D2H on three streams, overlapped"}
 
 
 def measure_e2e(args, w, race, inp, state, workspace):
@@ -406,6 +479,91 @@ def measure_e2e(args, w, race, inp, state, workspace):
             "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes}
 
 
+L2_BYTES = 129 * 2 ** 20
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 (FMA) x max SM clock
+
+
+def _timed(torch, dev, uuid, fn, warmup, steps, race):
+    """Mean ms per call of fn over `steps` calls (CUDA events on the current stream, after
+    `warmup` untimed calls), the clocks seen meanwhile and the library launches counted."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = race.race_attn_launch_count()
+    with ClockSampler(uuid) as clk:
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps, clk.summary(), race.race_attn_launch_count() - n0
+
+
+def run_row(args, w):
+    """One JSON line for a widening row: the causal decode step or exact angular attention."""
+    import torch
+
+    import linear_lsh_sketch_gb300 as race
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    race.load_library()
+    hbm_peak, _, peak_kind = load_peaks()
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    common = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+              "dtype": "bf16" if w.dtype == "bf16" else "f32"}
+    LR = w.L << w.P
+    if args.row == "decode":
+        per_head = LR * (w.d + 1) * 4
+        heads = max(args.heads, -(-2 * L2_BYTES // per_head))  # state at least twice L2: no flush
+        q, k, v = (torch.randn((1, heads, 1, w.d), generator=g, device=dev).to(w.torch_dtype) for _ in range(3))
+        W = torch.randn((w.L, w.P, w.d), generator=g, device=dev)
+        state = torch.randn((1, heads, LR, w.d + 1), generator=g, device=dev).abs_()
+        o = torch.empty_like(q)
+        ms, clocks, launches = _timed(torch, dev, uuid, lambda: race.race_attn_decode(
+            q, k, v, W, w.beta, w.L, w.P, state, o=o), args.warmup, args.steps, race)
+        alg = heads * (2 * per_head + 4 * w.d * w.elem_bytes)  # state read + write; q, k, v, o
+        gbs = alg / (ms / 1000.0) / 1e9
+        line = dict(common, metric="RACE causal decode step tokens/s (one token per (b, h))",
+                    value=heads / (ms / 1000.0), unit="tokens/s", ms_per_step=ms,
+                    config={"workload": "decode, %d heads, d %d, (P, L) = (%d, %d), state %.2f GB > L2, "
+                            "no flush" % (heads, w.d, w.P, w.L, heads * per_head / 1e9),
+                            "heads": heads, "d": w.d, "P": w.P, "L": w.L, "io_dtype": w.dtype},
+                    roofline={"bound": "hbm", "kernel": "decode", "achieved": gbs, "peak": hbm_peak,
+                              "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
+                              "algorithmic_bytes_per_launch": alg, "traffic": None},
+                    clocks=clocks, gpu_launches=launches)
+    else:
+        n = args.tokens or 8192
+        ws = w.scaled(N=n)
+        Q, K, V = (torch.randn((ws.B, ws.H, n, ws.d), generator=g, device=dev).to(ws.torch_dtype)
+                   for _ in range(3))
+        O = torch.empty_like(Q)
+        gamma = float(ws.P)
+        ms, clocks, launches = _timed(torch, dev, uuid, lambda: race.race_attn_angular(
+            Q, K, V, gamma, ws.causal, O=O), args.warmup, args.steps, race)
+        pairs = ws.B * ws.H * (n * (n + 1) // 2 if ws.causal else n * n)
+        flops = pairs * 8 * ws.d  # |a - b|^2, |a + b|^2 (6 d) and the weighted value sum (2 d)
+        tf = flops / (ms / 1000.0) / 1e12
+        line = dict(common, metric="exact angular attention (gamma = P) pair evaluations/s",
+                    value=pairs / (ms / 1000.0), unit="pairs/s", ms_per_step=ms,
+                    config={"workload": "angular attention, B %d H %d N %d d %d gamma %g causal %s" %
+                            (ws.B, ws.H, n, ws.d, gamma, ws.causal), "io_dtype": ws.dtype,
+                            "l2": "O(N^2) arithmetic on L2-resident rows; no flush"},
+                    roofline={"bound": "alu", "kernel": "angular", "achieved": tf, "peak": FP32_ALU_TFLOPS,
+                              "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
+                              "peak_kind": "FP32 CUDA-core FMA rate from unit counts and the 2070 MHz clock",
+                              "flops_per_launch": flops, "traffic": None},
+                    clocks=clocks, gpu_launches=launches)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,13 +577,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override N (sequence length) of the workload, e.g. for a small profiling capture")
+    ap.add_argument("--dbeta", action="store_true", help="the backward also writes d(loss)/d(beta)")
+    ap.add_argument("--row", choices=["step", "decode", "angular"], default="step",
+                    help="decode: one causal decode step per (b, h) of --heads heads; angular: exact angular "
+                         "attention at the workload's d and --tokens (default 8192) tokens")
+    ap.add_argument("--heads", type=int, default=1024, help="(b, h) problems of the decode batch")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
     from linear_lsh_sketch_gb300.workloads import CONFIGS
     w = CONFIGS[args.workload]
     if args.tokens:
         w = w.scaled(N=args.tokens, name="%s_N%d" % (w.name, args.tokens))
-    if args.impl == "reference":
+    if args.row != "step":
+        run_row(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)

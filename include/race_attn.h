@@ -20,8 +20,18 @@
  *  - Token tensors Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d], contiguous, d innermost, of
  *    element type `shape->dtype` (float32 or bfloat16), on the current CUDA device, 16-byte
  *    aligned.  Outputs are rounded to nearest-even from float32 arithmetic.
- *  - W is float32 [L, P, d] on the device, shared by Q and K, by all tables' rows, and by all
- *    (b, h).  beta is a finite scalar >= 0.
+ *  - W is float32 on the device, shared by Q and K and by all tables' rows: one [L, P, d] array
+ *    for every (b, h), or, with shape->per_head_w = 1, one set per head, [H, L, P, d], head h
+ *    hashing with W[h] for every batch entry (the pages do not say whether heads share their
+ *    hyperplanes; both layouts are offered).
+ *  - beta is a scalar >= 0: finite, or +INFINITY for hard hashing, the limit the slides name
+ *    ("beta -> infinity: hard hashing").  Each bit is then the sign of its projection, and a
+ *    row lands in one corner per table.  A projection that is exactly 0 splits the row evenly
+ *    over the two corners it separates (the limit sigmoid(0) = 1/2), so a zero row is uniform.
+ *    The features are computed as the soft ones at beta = 2^126, which equals the sign rule
+ *    exactly for every projection u with |u| >= 2^-119 and at u = 0.  No gradient reaches Q, K or
+ *    beta (dQ = dK = 0, dbeta = 0); dV is the hard sketch's.  A query whose corners hold no key
+ *    in any table has a zero denominator (its output is 0/0), which small inputs can meet.
  *  - Limits: N >= 1; B * H <= 65535; d a multiple of 8 in [8, 128]; 1 <= P <= 8; 1 <= L <= 16;
  *    L * 2^P <= 256.
  *  - The caller owns every buffer, including `workspace` (size from race_attn_workspace_bytes)
@@ -57,10 +67,11 @@ typedef enum {
     RACE_ERR_DEVICE_TIMEOUT = -7 /* race_attn_status: a kernel stopped after a bounded wait     */
 } race_status;
 
-/* Token-tensor shape and element type. */
+/* Token-tensor shape and element type, and the layout of W. */
 typedef struct {
     int64_t B, H, N, d;
-    int32_t dtype; /* race_dtype */
+    int32_t dtype;      /* race_dtype */
+    int32_t per_head_w; /* 0: W is [L, P, d] for every head; 1: W is [H, L, P, d] */
 } race_shape;
 
 /*
@@ -90,13 +101,20 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
  * Backward pass: given the output cotangent dO, writes dQ, dK, dV (all [B, H, N, d]).
  * O: the forward output.  It may be NULL: the kernels recompute what they need of O
  * (dO . O per row) from the sketch, which is cheaper than reading it.
+ * dbeta: NULL, or device float32 [B, H] (4-byte aligned) that receives d(loss)/d(beta) for each
+ * (b, h).  beta is trained with the layer ("RACE Attention" slides, frame "Soft corner
+ * assignments make hashing differentiable"); its logits are beta (u . v_r), so every query and
+ * key row adds sum_l sum_r ds_r (u . v_r), with ds the softmax gradient of its bucket
+ * probabilities.  The gradient of the one shared beta is the sum of the B * H values.  Each
+ * value is a sum in a fixed order (per-CTA partials, then a combine), so repeated calls give the
+ * same bits.  Overwritten, not accumulated.
  * state: NULL (the sketch is recomputed from K and V), or the buffer a race_attn_fwd call
  * with the same Q, K, V, W, beta, L, P and causal filled in.
- * Gradients with respect to W and beta are not produced.
+ * The gradient with respect to W is not produced.
  */
 int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const void *V,
                   const float *W, float beta, int L, int P, int causal, const void *O,
-                  const void *dO, void *dQ, void *dK, void *dV, const void *state,
+                  const void *dO, void *dQ, void *dK, void *dV, float *dbeta, const void *state,
                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -136,6 +154,20 @@ int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, const void *K,
  */
 int race_attn_decode(const race_shape *shape, const void *q, const void *k, const void *v,
                      const float *W, float beta, int L, int P, void *state, void *o, void *stream);
+
+/*
+ * Exact angular attention, the kernel RACE attention estimates ("RACE Attention" slides, frame
+ * "Choose a nonnegative kernel that can be sketched", paper Eqs. (3)-(4)), in O(N^2):
+ *     O_i = sum_j S_ij V_j / sum_j S_ij,   S_ij = (1 - angle(Q_i, K_j) / pi)^gamma
+ * over j <= i when causal != 0.  With gamma = P it is the target of the P-bit hash (frame "A
+ * hash collision estimates a powered angular kernel"), the reference for measuring the
+ * approximation error of race_attn_fwd.  Q, K, V, O as for race_attn_fwd; gamma finite >= 0
+ * (0^0 = 1).  A zero row is at angle pi / 2 to every row.  A row whose weights are all zero
+ * (every admissible key antipodal) gets 0/0.  Quadratic in N: meant for evaluation sizes.
+ * No workspace; nothing is allocated; deterministic.
+ */
+int race_attn_angular(const race_shape *shape, const void *Q, const void *K, const void *V,
+                      float gamma, int causal, void *O, void *stream);
 
 /*
  * Device-side status of the last race_attn_fwd / race_attn_bwd call that used `workspace`.

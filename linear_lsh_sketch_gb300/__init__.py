@@ -14,7 +14,8 @@ __all__ = [
     "RaceAttnError", "race_attn_fwd", "race_attn_bwd", "race_attn_workspace_bytes",
     "race_attn_state_bytes", "race_attn_strerror", "race_attn_launch_count", "race_attn_profile",
     "race_attn_profile_read", "race_attn_profile_reset", "library_path", "load_library",
-    "race_attn_fwd_noalloc", "RACE_NOALLOC_SCRATCH_BYTES", "race_attn_status",
+    "race_attn_fwd_noalloc", "RACE_NOALLOC_SCRATCH_BYTES", "race_attn_status", "race_attn_decode",
+    "race_attn_angular",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,7 +37,7 @@ class RaceAttnError(RuntimeError):
 
 class race_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64),
-                ("d", ctypes.c_int64), ("dtype", ctypes.c_int32)]
+                ("d", ctypes.c_int64), ("dtype", ctypes.c_int32), ("per_head_w", ctypes.c_int32)]
 
 
 def load_library():
@@ -56,12 +57,14 @@ def load_library():
     L.race_attn_state_bytes.restype = sz
     L.race_attn_fwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, sz, vp]
     L.race_attn_fwd.restype = i
-    L.race_attn_bwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.race_attn_bwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.race_attn_bwd.restype = i
     L.race_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp]
     L.race_attn_fwd_noalloc.restype = i
     L.race_attn_decode.argtypes = [shp, vp, vp, vp, vp, f, i, i, vp, vp, vp]
     L.race_attn_decode.restype = i
+    L.race_attn_angular.argtypes = [shp, vp, vp, vp, f, i, vp, vp]
+    L.race_attn_angular.restype = i
     L.race_attn_status.argtypes = [vp, vp]
     L.race_attn_status.restype = i
     L.race_attn_strerror.argtypes = [i]
@@ -80,18 +83,26 @@ def load_library():
     return L
 
 
-def make_shape(B, H, N, d, dtype):
+def make_shape(B, H, N, d, dtype, per_head_w=False):
     code = _DTYPES.get(dtype, dtype) if not isinstance(dtype, int) else dtype
-    return race_shape(int(B), int(H), int(N), int(d), int(code))
+    return race_shape(int(B), int(H), int(N), int(d), int(code), int(bool(per_head_w)))
 
 
-def _shape_of(Q):
+def _shape_of(Q, W=None, L=None, P=None):
+    """race_shape of the token tensor Q; with W also checks the hyperplanes: float32, contiguous,
+    [L, P, d] (shared by every head) or [H, L, P, d] (one set per head)."""
     if Q.dim() != 4:
         raise ValueError("token tensors must be [B, H, N, d]")
     if Q.dtype not in _DTYPES:
         raise TypeError("token tensors must be float32 or bfloat16")
     B, H, N, d = Q.shape
-    return make_shape(B, H, N, d, Q.dtype)
+    per_head = False
+    if W is not None:
+        shared, heads = (L, P, d), (H, L, P, d)
+        if W.dtype != torch.float32 or not W.is_contiguous() or tuple(W.shape) not in (shared, heads):
+            raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d] or [H, L, P, d]")
+        per_head = tuple(W.shape) == heads and W.dim() == 4
+    return make_shape(B, H, N, d, Q.dtype, per_head)
 
 
 def _ptr(t):
@@ -165,16 +176,15 @@ def _bytes_buffer(nbytes, device, given):
 
 
 def race_attn_fwd(Q, K, V, W, beta, L, P, causal, O=None, state=None, workspace=None, stream=None):
-    """O = RACE attention of Q, K, V ([B, H, N, d], float32 or bfloat16, CUDA); W float32 [L, P, d].
+    """O = RACE attention of Q, K, V ([B, H, N, d], float32 or bfloat16, CUDA); W float32 [L, P, d]
+    (shared by every head) or [H, L, P, d] (one set per head).
 
     O, state and workspace are allocated with torch when not given.  Returns O.
     """
-    shape = _shape_of(Q)
+    shape = _shape_of(Q, W, L, P)
     _check_like("K", K, Q)
     _check_like("V", V, Q)
     _check_like("Q", Q, Q)
-    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
-        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
     if O is None:
         O = torch.empty_like(Q)
     _check_like("O", O, Q)
@@ -192,39 +202,42 @@ def race_attn_fwd(Q, K, V, W, beta, L, P, causal, O=None, state=None, workspace=
 
 
 def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, dV=None, state=None,
-                  workspace=None, stream=None):
-    """(dQ, dK, dV) of RACE attention for the output cotangent dO; allocates what is not given."""
-    shape = _shape_of(Q)
+                  workspace=None, stream=None, want_dbeta=False, dbeta=None):
+    """(dQ, dK, dV) of RACE attention for the output cotangent dO; allocates what is not given.
+    With want_dbeta (or a float32 [B, H] `dbeta` given) also d(loss)/d(beta) per (b, h), returned
+    as a fourth element; the shared beta's gradient is its sum."""
+    shape = _shape_of(Q, W, L, P)
     for n, t in (("K", K), ("V", V), ("dO", dO), ("Q", Q)):
         _check_like(n, t, Q)
-    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
-        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(Q) if dK is None else dK
     dV = torch.empty_like(Q) if dV is None else dV
     for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
         _check_like(n, t, Q)
+    if dbeta is None and want_dbeta:
+        dbeta = torch.empty((Q.shape[0], Q.shape[1]), dtype=torch.float32, device=Q.device)
+    if dbeta is not None and (dbeta.dtype != torch.float32 or tuple(dbeta.shape) != tuple(Q.shape[:2])
+                              or not dbeta.is_contiguous() or dbeta.device != Q.device):
+        raise ValueError("dbeta must be a contiguous float32 tensor of shape [B, H] on Q's device")
     ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 1)
     if ws_bytes == 0:
         raise RaceAttnError(-1, "race_attn_bwd")
     workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
     rc = load_library().race_attn_bwd(
         ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
-        int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(state), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream))
+        int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dbeta), _ptr(state),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != 0:
         raise RaceAttnError(rc, "race_attn_bwd")
-    return dQ, dK, dV
+    return (dQ, dK, dV) if dbeta is None else (dQ, dK, dV, dbeta)
 
 
 def race_attn_decode(q, k, v, W, beta, L, P, state, o=None, stream=None):
     """One causal decode step: q, k, v [B, H, 1, d] (float32 or bfloat16, CUDA); state float32
     [B, H, L * 2^P, d + 1] (updated in place).  Returns o [B, H, 1, d]."""
-    shape = _shape_of(q)
+    shape = _shape_of(q, W, L, P)
     for n, t in (("k", k), ("v", v), ("q", q)):
         _check_like(n, t, q)
-    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, q.shape[3]) or not W.is_contiguous():
-        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
     want = (q.shape[0], q.shape[1], L << P, q.shape[3] + 1)
     if state.dtype != torch.float32 or tuple(state.shape) != want or not state.is_contiguous():
         raise ValueError("state must be a contiguous float32 tensor of shape %s" % (want,))
@@ -237,6 +250,21 @@ def race_attn_decode(q, k, v, W, beta, L, P, state, o=None, stream=None):
     return o
 
 
+def race_attn_angular(Q, K, V, gamma, causal, O=None, stream=None):
+    """Exact angular attention O_i = sum_j S_ij V_j / sum_j S_ij, S_ij = (1 - angle_ij / pi)^gamma
+    (j <= i when causal), O(N^2): the reference RACE attention approximates.  Returns O."""
+    shape = _shape_of(Q)
+    for n, t in (("K", K), ("V", V), ("Q", Q)):
+        _check_like(n, t, Q)
+    O = torch.empty_like(Q) if O is None else O
+    _check_like("O", O, Q)
+    rc = load_library().race_attn_angular(ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), float(gamma),
+                                          int(bool(causal)), _ptr(O), _stream(stream))
+    if rc != 0:
+        raise RaceAttnError(rc, "race_attn_angular")
+    return O
+
+
 def race_attn_fwd_noalloc(Q, K, V, W, beta, L, P, causal, O=None, stream=None):
     """Forward pass through the entry point that allocates nothing and takes no workspace.
 
@@ -245,12 +273,10 @@ def race_attn_fwd_noalloc(Q, K, V, W, beta, L, P, causal, O=None, stream=None):
     that buffer and must be serialised by the caller.  Only O is allocated here, and only when
     it is not given.  Returns O.
     """
-    shape = _shape_of(Q)
+    shape = _shape_of(Q, W, L, P)
     _check_like("K", K, Q)
     _check_like("V", V, Q)
     _check_like("Q", Q, Q)
-    if W.dtype != torch.float32 or tuple(W.shape) != (L, P, Q.shape[3]) or not W.is_contiguous():
-        raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d]")
     if O is None:
         O = torch.empty_like(Q)
     _check_like("O", O, Q)

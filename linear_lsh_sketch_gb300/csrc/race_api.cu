@@ -104,6 +104,8 @@ struct Plan {
     size_t E = 0;          // floats per sketch: LR * (d + 1)
     size_t off_status = 0;  // one 32-bit device status word (error bits of bounded waits)
     size_t off_part = 0, off_sk = 0, off_gpart = 0, off_gsk = 0, off_aux = 0;
+    size_t off_db = 0;     // d(loss)/d(beta) partials: [2][BH][db_cap] floats
+    int64_t db_cap = 0;    // partial slots per (side, b, h): at least every backward kernel's grid x
     size_t ws_fwd = 0, ws_bwd = 0, state = 0;
 };
 
@@ -119,6 +121,7 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     if (P < 1 || P > kMaxP || L < 1 || L > kMaxL) return RACE_ERR_INVALID_ARG;
     if ((L << P) > kMaxLR) return RACE_ERR_INVALID_ARG;
     if (s->dtype != RACE_F32 && s->dtype != RACE_BF16) return RACE_ERR_INVALID_ARG;
+    if (s->per_head_w != 0 && s->per_head_w != 1) return RACE_ERR_INVALID_ARG;
     if (s->B > 65535 || s->H > 65535 || s->B * s->H > 65535 || s->N > ((int64_t)1 << 40) / (s->B * s->H))
         return RACE_ERR_INVALID_ARG;
     Dims &D = pl.D;
@@ -132,6 +135,8 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     D.LP = L * P;
     D.dv = D.d + 1;
     D.beta = 0.f;
+    D.H = s->H;
+    D.w_per_head = s->per_head_w;
     pl.causal = causal != 0;
     pl.bf16 = s->dtype == RACE_BF16;
     pl.E = (size_t)D.LR * D.dv;
@@ -165,7 +170,9 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     pl.off_gpart = pl.ws_fwd;
     pl.off_gsk = align256(pl.off_gpart + per_split);
     pl.off_aux = align256(pl.off_gsk + sk_bytes);
-    pl.ws_bwd = align256(pl.off_aux + (size_t)D.BH * D.N * sizeof(float2));
+    pl.off_db = align256(pl.off_aux + (size_t)D.BH * D.N * sizeof(float2));
+    pl.db_cap = std::max<int64_t>(pl.nsplit, ceil_div(D.N, generic_token_tile()));
+    pl.ws_bwd = align256(pl.off_db + 2 * (size_t)D.BH * pl.db_cap * sizeof(float));
     pl.state = sk_bytes;
 
     // every kernel of the chosen path must fit in shared memory
@@ -185,7 +192,18 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
-int check_beta(float beta) { return (std::isfinite(beta) && beta >= 0.f) ? RACE_OK : RACE_ERR_INVALID_ARG; }
+// beta: finite and >= 0, or +infinity for hard hashing.
+int check_beta(float beta) { return (!std::isnan(beta) && beta >= 0.f) ? RACE_OK : RACE_ERR_INVALID_ARG; }
+
+// Hard hashing (beta = +infinity, the limit "RACE Attention" slides, frame "Soft corner assignments
+// make hashing differentiable", call hard hashing) runs the soft kernels at the finite stand-in
+// 2^126.  Their sigmoid(2 beta u) is then exactly 1 or 0 for every |u| >= 2^-119 (the exponent
+// underflows) and exactly 1/2 at u = 0, the value a tied projection keeps in the limit.  So
+// the features are the hard corners, and the softmax gradient vanishes identically.  Only tied
+// rows (u = 0) would carry a Jacobian scaled by 2^126, and their dQ and dK are zero by definition.
+constexpr float kHardBeta = 8.507059e37f;  // 2^126
+bool hard_hash(float beta) { return std::isinf(beta); }
+float kernel_beta(float beta) { return hard_hash(beta) ? kHardBeta : beta; }
 
 #define RACE_TRY(expr)                                   \
     do {                                                 \
@@ -243,9 +261,32 @@ int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float
     return RACE_OK;
 }
 
+// d(loss)/d(beta): each backward kernel's CTA (slot x, b, h) writes one partial of its side to
+// dbq / dbk[(b, h) * slots + x]; a fixed-order combine then sums both sides into dbeta[b, h].
+struct DbetaOut {
+    float *dbq = nullptr, *dbk = nullptr, *out = nullptr;
+    int slots = 0;
+};
+
+cudaError_t dbeta_begin(const Plan &pl, char *ws, float *dbeta, int slots, DbetaOut &db, cudaStream_t st)
+{
+    if (!dbeta) return cudaSuccess;
+    db.slots = slots;
+    db.out = dbeta;
+    db.dbq = (float *)(ws + pl.off_db);
+    db.dbk = db.dbq + pl.D.BH * slots;
+    return cudaMemsetAsync(db.dbq, 0, 2 * (size_t)pl.D.BH * slots * sizeof(float), st);
+}
+
+cudaError_t dbeta_end(const Plan &pl, const DbetaOut &db, cudaStream_t st)
+{
+    if (!db.out) return cudaSuccess;
+    return launch_dbeta_combine(pl.D, db.dbq, db.slots, db.out, st);
+}
+
 template <typename T>
 int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float *W, const T *dO, T *dQ, T *dK,
-                  T *dV, const float *state, char *ws, cudaStream_t st)
+                  T *dV, float *dbeta, const float *state, char *ws, cudaStream_t st)
 {
     const Dims &D = pl.D;
     float *part = (float *)(ws + pl.off_part);
@@ -255,6 +296,7 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
     unsigned *err = (unsigned *)(ws + pl.off_status);
     RACE_TRY(cudaMemsetAsync(err, 0, sizeof(unsigned), st));
     const float *S = state;
+    DbetaOut db;
     if constexpr (std::is_same<T, bf16_t>::value) {
         const bool c5b = pl.c5 && c5_bwd_supported(D);
         if (c5b || (use_tc<T>(pl) && causal_tc_bwd_supported(D))) {
@@ -267,15 +309,21 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 1, st));
                 S = Sw;
             }
+            RACE_TRY(dbeta_begin(pl, ws, dbeta, pl.nsplit, db, st));
             if (c5b)
-                RACE_TRY(launch_c5_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, st));
+                RACE_TRY(launch_c5_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, db.dbq,
+                                         st));
             else
-                RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, st));
+                RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err,
+                                                db.dbq, st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
             if (c5b)
-                RACE_TRY(launch_c5_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, st));
+                RACE_TRY(launch_c5_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, db.dbk,
+                                          st));
             else
-                RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, st));
+                RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err,
+                                                 db.dbk, st));
+            RACE_TRY(dbeta_end(pl, db, st));
             return RACE_OK;
         }
     }
@@ -287,10 +335,12 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 0, st));
                 S = Sw;
             }
-            RACE_TRY(launch_nc5_bwd_query(D, Q, dO, W, S, dQ, aux, err, st));
+            RACE_TRY(dbeta_begin(pl, ws, dbeta, nc5_bwd_nseg(D), db, st));
+            RACE_TRY(launch_nc5_bwd_query(D, Q, dO, W, S, dQ, aux, err, db.dbq, st));
             RACE_TRY(launch_nc5_sketch(D, Q, dO, aux, W, pl.seg_len, pl.nsplit, gpart, err, st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 0, st));
-            RACE_TRY(launch_nc5_bwd_key(D, K, V, W, gsk, dK, dV, err, st));
+            RACE_TRY(launch_nc5_bwd_key(D, K, V, W, gsk, dK, dV, err, db.dbk, st));
+            RACE_TRY(dbeta_end(pl, db, st));
             return RACE_OK;
         }
     }
@@ -301,16 +351,19 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
         S = Sw;
     }
     if (!pl.causal) {
-        RACE_TRY(launch_bwd_query<T>(D, Q, dO, W, S, dQ, aux, st));
+        RACE_TRY(dbeta_begin(pl, ws, dbeta, (int)ceil_div(D.N, generic_token_tile()), db, st));
+        RACE_TRY(launch_bwd_query<T>(D, Q, dO, W, S, dQ, aux, db.dbq, st));
         RACE_TRY(launch_sketch<T>(D, Q, dO, aux, W, pl.seg_len, pl.nsplit, gpart, 1, st));
         RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 0, st));
-        RACE_TRY(launch_bwd_key<T>(D, K, V, W, gsk, dK, dV, st));
+        RACE_TRY(launch_bwd_key<T>(D, K, V, W, gsk, dK, dV, db.dbk, st));
     } else {
-        RACE_TRY(launch_causal_bwd_q<T>(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, st));
+        RACE_TRY(dbeta_begin(pl, ws, dbeta, pl.nsplit, db, st));
+        RACE_TRY(launch_causal_bwd_q<T>(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, db.dbq, st));
         RACE_TRY(launch_sketch<T>(D, Q, dO, aux, W, pl.seg_len, pl.nsplit, gpart, 1, st));
         RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
-        RACE_TRY(launch_causal_bwd_kv<T>(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, st));
+        RACE_TRY(launch_causal_bwd_kv<T>(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, db.dbk, st));
     }
+    RACE_TRY(dbeta_end(pl, db, st));
     return RACE_OK;
 }
 
@@ -348,7 +401,7 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
         !aligned16(workspace) || (state && !aligned16(state)))
         return RACE_ERR_ALIGN;
     if (workspace_bytes < pl.ws_fwd) return RACE_ERR_WORKSPACE;
-    pl.D.beta = beta;
+    pl.D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
     if (pl.bf16)
         return forward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
@@ -360,7 +413,7 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
 
 int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const void *V, const float *W, float beta,
                   int L, int P, int causal, const void *O, const void *dO, void *dQ, void *dK, void *dV,
-                  const void *state, void *workspace, size_t workspace_bytes, void *stream)
+                  float *dbeta, const void *state, void *workspace, size_t workspace_bytes, void *stream)
 {
     (void)O;
     Plan pl;
@@ -369,18 +422,27 @@ int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const v
     if ((rc = check_beta(beta)) != RACE_OK) return rc;
     if (!Q || !K || !V || !W || !dO || !dQ || !dK || !dV || !workspace) return RACE_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(W) || !aligned16(dO) || !aligned16(dQ) ||
-        !aligned16(dK) || !aligned16(dV) || !aligned16(workspace) || (state && !aligned16(state)))
+        !aligned16(dK) || !aligned16(dV) || !aligned16(workspace) || (state && !aligned16(state)) ||
+        ((uintptr_t)dbeta & 3) != 0)
         return RACE_ERR_ALIGN;
     if (workspace_bytes < pl.ws_bwd) return RACE_ERR_WORKSPACE;
-    pl.D.beta = beta;
+    pl.D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
     if (pl.bf16)
-        return backward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
-                                            (const __nv_bfloat16 *)V, W, (const __nv_bfloat16 *)dO,
-                                            (__nv_bfloat16 *)dQ, (__nv_bfloat16 *)dK, (__nv_bfloat16 *)dV,
-                                            (const float *)state, (char *)workspace, st);
-    return backward_impl<float>(pl, (const float *)Q, (const float *)K, (const float *)V, W, (const float *)dO,
-                                (float *)dQ, (float *)dK, (float *)dV, (const float *)state, (char *)workspace, st);
+        rc = backward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
+                                          (const __nv_bfloat16 *)V, W, (const __nv_bfloat16 *)dO,
+                                          (__nv_bfloat16 *)dQ, (__nv_bfloat16 *)dK, (__nv_bfloat16 *)dV, dbeta,
+                                          (const float *)state, (char *)workspace, st);
+    else
+        rc = backward_impl<float>(pl, (const float *)Q, (const float *)K, (const float *)V, W, (const float *)dO,
+                                  (float *)dQ, (float *)dK, (float *)dV, dbeta, (const float *)state,
+                                  (char *)workspace, st);
+    if (rc == RACE_OK && hard_hash(beta)) {  // a hard hash passes no gradient to Q and K
+        const size_t bytes = (size_t)pl.D.BH * pl.D.N * pl.D.d * (pl.bf16 ? 2 : 4);
+        RACE_TRY(cudaMemsetAsync(dQ, 0, bytes, st));
+        RACE_TRY(cudaMemsetAsync(dK, 0, bytes, st));
+    }
+    return rc;
 }
 
 const char *race_attn_strerror(int status)
@@ -410,7 +472,7 @@ int race_attn_decode(const race_shape *shape, const void *q, const void *k, cons
         return RACE_ERR_ALIGN;
     if (!decode_supported(pl.D)) return RACE_ERR_UNSUPPORTED;
     Dims D = pl.D;
-    D.beta = beta;
+    D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
     if (pl.bf16)
         RACE_TRY(launch_decode<bf16_t>(D, (const bf16_t *)q, (const bf16_t *)k, (const bf16_t *)v, W, (float *)state,
@@ -418,6 +480,25 @@ int race_attn_decode(const race_shape *shape, const void *q, const void *k, cons
     else
         RACE_TRY(launch_decode<float>(D, (const float *)q, (const float *)k, (const float *)v, W, (float *)state,
                                       (float *)o, st));
+    return RACE_OK;
+}
+
+int race_attn_angular(const race_shape *shape, const void *Q, const void *K, const void *V, float gamma, int causal,
+                      void *O, void *stream)
+{
+    Plan pl;
+    int rc = make_plan(shape, 1, 1, causal, pl);  // shape checks only: this path has no tables
+    if (rc != RACE_OK) return rc;
+    if (!std::isfinite(gamma) || gamma < 0.f) return RACE_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !O) return RACE_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return RACE_ERR_ALIGN;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (pl.bf16)
+        RACE_TRY(launch_angular<bf16_t>(pl.D, (const bf16_t *)Q, (const bf16_t *)K, (const bf16_t *)V, gamma,
+                                        causal != 0, (bf16_t *)O, st));
+    else
+        RACE_TRY(launch_angular<float>(pl.D, (const float *)Q, (const float *)K, (const float *)V, gamma,
+                                       causal != 0, (float *)O, st));
     return RACE_OK;
 }
 
@@ -501,7 +582,7 @@ extern "C" int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, con
     if (pl.ws_fwd > RACE_NOALLOC_SCRATCH_BYTES) return RACE_ERR_SCRATCH_LIMIT;
     void *scratch = noalloc_scratch();
     if (!scratch) return RACE_ERR_CUDA;
-    pl.D.beta = beta;
+    pl.D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
     // state == nullptr: the forward keeps its sketch inside the scratch buffer
     if (pl.bf16)

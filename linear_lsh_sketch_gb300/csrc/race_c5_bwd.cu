@@ -71,13 +71,14 @@ struct BwdLayout {
     }
 };
 
-template <int D, int P, int LT>
+// DB: also the CTA's key-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
+template <int D, int P, int LT, bool DB>
 __global__ void __launch_bounds__(NTHW, 1)
     k_causal_bwdkv5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
                     const float *__restrict__ W, const float2 *__restrict__ aux, const float *__restrict__ G0,
                     int64_t seg_len, int nseg, bf16 *__restrict__ dK, bf16 *__restrict__ dV,
-                    unsigned *__restrict__ err)
+                    unsigned *__restrict__ err, float *__restrict__ dbpart)
 {
     constexpr int KB = D / 64;
     constexpr int R = 1 << P;
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         zero_region(sm + Ly.fq, BLK);
         zero_region(sm + Ly.ghi, 2 * BLK);
         init_mass_tile(sm + Ly.ncm, false);
-        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+        load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     }
     if (tid == NTH) {
         for (uint32_t i = 0; i < B_COUNT; ++i) {
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         if (q4 == 0) gb[lane] = lane < LR ? uf(gb0) + uf(gb1) : 0.f;  // -sum F'_Q c, c as bf16 hi + lo
     };
 
+    float db = 0.f;  // this thread's d(loss)/d(beta) share (DB only)
     if (!compute) {
         // ---------------------------------------------------------------- control warp
         if (lane == 0) {
@@ -522,7 +524,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                         for (int r = 0; r < R; ++r) dp[r] = l * R + r < LRMAX ? dph[l * R + r] : 0.f;
                         float tmp[P];
-                        table_backward<P>(u, ph, dp, beta, tmp);
+                        table_backward<P, DB>(u, ph, dp, beta, tmp, &db);
 #pragma unroll
                         for (int p = 0; p < P; ++p) dz[l * P + p] = tmp[p];
                     }
@@ -586,6 +588,10 @@ __global__ void __launch_bounds__(NTHW, 1)
             fence_before();
             if (!group_sync(bar(B_CS2), par, abort)) break;  // gb / TMEM reads done before the next chunk
         }
+    }
+    if constexpr (DB) {  // this CTA's d(loss)/d(beta) partial, summed in a fixed order
+        const float sdb = block_sum_fixed(db, cvec);
+        if (tid == 0) dbpart[bh * gridDim.x + blockIdx.x] = sdb;
     }
     fence_before();
     __syncthreads();
@@ -657,13 +663,14 @@ struct QLayout {
     }
 };
 
-template <int D, int P, int LT>
+// DB: also the CTA's query-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
+template <int D, int P, int LT, bool DB>
 __global__ void __launch_bounds__(NTHW, 1)
     k_causal_bwdq5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
                    const float *__restrict__ W, const float *__restrict__ S0, int64_t seg_len, int nseg,
                    bf16 *__restrict__ dQ, float2 *__restrict__ aux, float *__restrict__ Gseg,
-                   unsigned *__restrict__ err)
+                   unsigned *__restrict__ err, float *__restrict__ dbpart)
 {
     constexpr int KB = D / 64;
     constexpr int R = 1 << P;
@@ -703,7 +710,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         zero_region(sm + Ly.fk, 4 * BLK);  // F_K, F'_Q, S hi, S lo
         init_mass_tile(sm + Ly.ncm, false);
         init_mass_tile(sm + Ly.ones, true);
-        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+        load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     }
     if (tid == NTH) {
         for (uint32_t i = 0; i < B_COUNT; ++i) {
@@ -789,6 +796,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         if (q4 == 0) bprev[32 * par_out + lane] = lane < LR ? uf(mv) : 0.f;
     };
 
+    float db = 0.f;  // this thread's d(loss)/d(beta) share (DB only)
     if (!compute) {
         // ---------------------------------------------------------------- control warp
         if (lane == 0) {
@@ -1072,7 +1080,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                             g[r] = (uf(gr[lr]) - (bprev[32 * par + lr] + uf(br[lr])) * cc) * rd;
                         }
                         float tmp[P];
-                        table_backward<P>(u, ph, g, beta, tmp);
+                        table_backward<P, DB>(u, ph, g, beta, tmp, &db);
 #pragma unroll
                         for (int p = 0; p < P; ++p) dz[l * P + p] = tmp[p];
                         // F'_Q = phi / den for this table
@@ -1171,6 +1179,10 @@ __global__ void __launch_bounds__(NTHW, 1)
             }
         }
     }
+    if constexpr (DB) {  // this CTA's d(loss)/d(beta) partial, summed in a fixed order
+        const float sdb = block_sum_fixed(db, red);
+        if (tid == 0) dbpart[bh * gridDim.x + blockIdx.x] = sdb;
+    }
     fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -1196,26 +1208,27 @@ namespace {
 template <int D, int P, int LT>
 cudaError_t bwdkv5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                           const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
-                          int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+                          int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
     const c5b::BwdLayout Ly(D);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = c5b::k_causal_bwdkv5<D, P, LT>;
+    auto kern = dbpart ? c5b::k_causal_bwdkv5<D, P, LT, true> : c5b::k_causal_bwdkv5<D, P, LT, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_bwd_kv", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5b::NTHW), smem,
-                         st, mq, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err);
+                         st, mq, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart);
 }
 
 // (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
 template <int D, int P>
 cudaError_t bwdkv5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                         const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
-                        int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+                        int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
     if constexpr (D == 128 && P == 3)
-        if (Dm.L == 3) return bwdkv5_launch<D, P, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-    return bwdkv5_launch<D, P, 0>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        if (Dm.L == 3)
+            return bwdkv5_launch<D, P, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+    return bwdkv5_launch<D, P, 0>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
 }
 
 }  // namespace
@@ -1225,33 +1238,34 @@ namespace {
 template <int D, int P, int LT>
 cudaError_t bwdq5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                          const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
-                         bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, cudaStream_t st)
+                         bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, float *dbpart, cudaStream_t st)
 {
     const c5q::QLayout Ly(D);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = c5q::k_causal_bwdq5<D, P, LT>;
+    auto kern = dbpart ? c5q::k_causal_bwdq5<D, P, LT, true> : c5q::k_causal_bwdq5<D, P, LT, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_bwd_q", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5q::NTHW), smem, st,
-                         mq, mk, mv, mdo, Dm, W, S0, seg_len, nseg, dQ, aux, Gseg, err);
+                         mq, mk, mv, mdo, Dm, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart);
 }
 
 // (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
 template <int D, int P>
 cudaError_t bwdq5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                        const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
-                       bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, cudaStream_t st)
+                       bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, float *dbpart, cudaStream_t st)
 {
     if constexpr (D == 128 && P == 3)
-        if (Dm.L == 3) return bwdq5_launch<D, P, 3>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, st);
-    return bwdq5_launch<D, P, 0>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, st);
+        if (Dm.L == 3)
+            return bwdq5_launch<D, P, 3>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart, st);
+    return bwdq5_launch<D, P, 0>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart, st);
 }
 
 }  // namespace
 
 cudaError_t launch_c5_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
                             const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
-                            float *Gseg, unsigned *err, cudaStream_t st)
+                            float *Gseg, unsigned *err, float *dbpart, cudaStream_t st)
 {
     CUtensorMap mq, mk, mv, mdo;
     cudaError_t e = make_token_map(&mq, Q, Dm);
@@ -1260,7 +1274,8 @@ cudaError_t launch_c5_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *K, co
     if (e == cudaSuccess) e = make_token_map(&mdo, dO, Dm);
     if (e != cudaSuccess) return e;
 #define RACE_C5Q_CASE(DD, PP) \
-    case DD * 16 + PP: return bwdq5_inst<DD, PP>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, st);
+    case DD * 16 + PP:        \
+        return bwdq5_inst<DD, PP>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart, st);
     switch (Dm.d * 16 + Dm.P) {
         RACE_C5Q_CASE(64, 1)
         RACE_C5Q_CASE(64, 2)
@@ -1279,7 +1294,7 @@ cudaError_t launch_c5_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *K, co
 
 cudaError_t launch_c5_bwd_kv(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
                              const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
-                             bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+                             bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
     CUtensorMap mq, mk, mv, mdo;
     cudaError_t e = make_token_map(&mq, Q, Dm);
@@ -1288,16 +1303,16 @@ cudaError_t launch_c5_bwd_kv(const Dims &Dm, const bf16_t *Q, const bf16_t *K, c
     if (e == cudaSuccess) e = make_token_map(&mdo, dO, Dm);
     if (e != cudaSuccess) return e;
     switch (Dm.d * 16 + Dm.P) {
-        case 64 * 16 + 1: return bwdkv5_inst<64, 1>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 64 * 16 + 2: return bwdkv5_inst<64, 2>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 64 * 16 + 3: return bwdkv5_inst<64, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 64 * 16 + 4: return bwdkv5_inst<64, 4>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 64 * 16 + 5: return bwdkv5_inst<64, 5>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 128 * 16 + 1: return bwdkv5_inst<128, 1>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 128 * 16 + 2: return bwdkv5_inst<128, 2>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 128 * 16 + 3: return bwdkv5_inst<128, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 128 * 16 + 4: return bwdkv5_inst<128, 4>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
-        case 128 * 16 + 5: return bwdkv5_inst<128, 5>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, st);
+        case 64 * 16 + 1: return bwdkv5_inst<64, 1>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 64 * 16 + 2: return bwdkv5_inst<64, 2>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 64 * 16 + 3: return bwdkv5_inst<64, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 64 * 16 + 4: return bwdkv5_inst<64, 4>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 64 * 16 + 5: return bwdkv5_inst<64, 5>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 128 * 16 + 1: return bwdkv5_inst<128, 1>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 128 * 16 + 2: return bwdkv5_inst<128, 2>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 128 * 16 + 3: return bwdkv5_inst<128, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 128 * 16 + 4: return bwdkv5_inst<128, 4>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        case 128 * 16 + 5: return bwdkv5_inst<128, 5>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         zero_region(sm + Ly.shi, 2 * Ly.sblk);
         init_mass_tile(sm + Ly.ones, true);
         if (D == 64) zero_region(sm + Ly.zero, BLK);
-        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+        load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     }
     if (tid == NTH) {
         for (uint32_t i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_FEAT || i == B_MASK || i == B_SOP) ? 8 : 1);

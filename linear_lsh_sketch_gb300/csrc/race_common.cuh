@@ -21,12 +21,38 @@ struct Dims {
     int64_t N;   // tokens per problem
     int d, L, P, R, LR, LP, dv;
     float beta;
+    int64_t H;       // heads (problem bh is head bh % H)
+    int w_per_head;  // 0: one W [L, P, d] for every head; 1: W is [H, L, P, d]
 };
+
+// The hyperplanes problem bh hashes with: the shared W, or its head's slice of a per-head W.
+__host__ __device__ inline const float *head_w(const float *W, const Dims &D, int64_t bh)
+{
+    return D.w_per_head ? W + (bh % D.H) * (int64_t)D.LP * D.d : W;
+}
 
 __device__ __forceinline__ float ld_f(const float *p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld_f(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
 __device__ __forceinline__ void st_f(float *p, int64_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void st_f(__nv_bfloat16 *p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+// Sum of one float per thread over the CTA in a fixed order (butterflies within each warp, then
+// the warps in index order), so that a reduction gives the same bits on every run.  Every
+// thread of the block calls it; `scratch` holds one float per warp and may be in use until the
+// call.  The total is returned in thread 0.
+__device__ __forceinline__ float block_sum_fixed(float v, float *scratch)
+{
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    const int warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < nw; ++w) s += scratch[w];
+    return s;
+}
 
 // Bump allocator for dynamic shared memory layouts, usable on host (to size the launch) and
 // device (to find the regions); every region starts on a 16-byte boundary.

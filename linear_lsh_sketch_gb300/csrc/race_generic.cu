@@ -112,11 +112,15 @@ __device__ void featurise(const float *xs, const Dims &D, const float *ws, int f
 // softmax: ds_r = phi_r (dphi_r - sum phi dphi); logits: du_t = beta sum_r ds_r v_{r,t};
 // tanh: dz = du (1 - u^2); projection: dxhat = sum W^T dz; normalisation:
 // dx = (dxhat - xhat (xhat . dxhat)) / |x|, and 0 for a zero row.
-__device__ void featurise_backward(const float *xs, const Dims &D, const float *ws,
-                                   const float *inv_s, const float *u_s, const float *f_s,
-                                   const float *dphi_s, int fst, float *dz_s, float *dx_s,
-                                   float *red_s)
+// Returns this thread's share of d(loss)/d(beta): the logits are beta (u . v_r), so each
+// (token, table) adds sum_r ds_r (u . v_r) = sum_t u_t sum_r ds_r v_{r,t}.  Rows past a tile's
+// count are zero, so their u = 0 and they add nothing.
+__device__ float featurise_backward(const float *xs, const Dims &D, const float *ws,
+                                    const float *inv_s, const float *u_s, const float *f_s,
+                                    const float *dphi_s, int fst, float *dz_s, float *dx_s,
+                                    float *red_s)
 {
+    float db = 0.f;
     const int dp = D.d + 1;
     for (int pair = threadIdx.x; pair < TT * D.L; pair += NT) {
         const int t = pair % TT, l = pair / TT;
@@ -137,6 +141,7 @@ __device__ void featurise_backward(const float *xs, const Dims &D, const float *
         for (int p = 0; p < kMaxP; ++p) {
             if (p < D.P) {
                 const float u = u_s[t * D.LP + l * D.P + p];
+                db = fmaf(u, du[p], db);
                 dz_s[t * D.LP + l * D.P + p] = D.beta * du[p] * (1.f - u * u);
             }
         }
@@ -160,6 +165,16 @@ __device__ void featurise_backward(const float *xs, const Dims &D, const float *
         dx_s[t * dp + k] = inv_s[t] * (dx_s[t * dp + k] - xs[t * dp + k] * red_s[t]);
     }
     __syncthreads();
+    return db;
+}
+
+// The CTA's d(loss)/d(beta) partial (one float per thread, summed in a fixed order) to
+// dbpart[bh][blockIdx.x]; nothing when dbpart is null.  Every thread calls it.
+__device__ void store_dbeta_partial(float db, float *scratch, float *dbpart, int64_t bh)
+{
+    if (!dbpart) return;
+    const float s = block_sum_fixed(db, scratch);
+    if (threadIdx.x == 0) dbpart[bh * gridDim.x + blockIdx.x] = s;
 }
 
 // ------------------------------------------------------------------ shared-memory layouts
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(NT) k_sketch(Dims D, const T *__restrict__ X,
     const int l0 = f0 / D.R, l1 = (f1 - 1) / D.R + 1;
     const SketchSmem L(D, l1 - l0);
     float *ws = sm + L.ws, *xs = sm + L.xs, *ys = sm + L.ys, *fs = sm + L.fs, *inv = sm + L.inv;
-    load_w(W, D, l0, l1, ws);
+    load_w(head_w(W, D, bh), D, l0, l1, ws);
     const T *Xb = X + bh * D.N * D.d;
     const T *Yb = Y + bh * D.N * D.d;
     const int64_t n_begin = (int64_t)s * seg_len;
@@ -385,6 +400,23 @@ __global__ void k_combine(const float *__restrict__ part, float *__restrict__ ou
     }
 }
 
+// d(loss)/d(beta) per (b, h) from the backward kernels' CTA partials: part holds two [BH][slots]
+// arrays (query side, then key side), zero where no CTA wrote; out[bh] = their sum, taken in a
+// fixed order (a strided share per thread, then the block in thread order).  Grid (BH), 256 threads.
+__global__ void __launch_bounds__(256) k_dbeta_combine(const float *__restrict__ part, int slots, int64_t BH,
+                                                        float *__restrict__ out)
+{
+    __shared__ float scratch[8];
+    const int64_t bh = blockIdx.x;
+    float s = 0.f;
+    for (int side = 0; side < 2; ++side) {
+        const float *p = part + ((int64_t)side * BH + bh) * slots;
+        for (int i = threadIdx.x; i < slots; i += blockDim.x) s += p[i];
+    }
+    s = block_sum_fixed(s, scratch);
+    if (threadIdx.x == 0) out[bh] = s;
+}
+
 // Non-causal read-out: O_t = sum_f phi_f(Q_t) A[f] / sum_f phi_f(Q_t) B[f] with S = [A | B]
 // ([BH][LR][dv]).  Grid (ceil(N / TT), BH).
 template <typename T>
@@ -399,7 +431,7 @@ __global__ void __launch_bounds__(NT) k_readout(Dims D, const T *__restrict__ Q,
     const int64_t bh = blockIdx.y, n0 = (int64_t)blockIdx.x * TT;
     const int cnt = (int)min((int64_t)TT, D.N - n0);
     const int fst = D.LR + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     load_rows(Q + bh * D.N * D.d, n0, cnt, D.d, xs);
     __syncthreads();
     featurise(xs, D, ws, 0, D.LR, inv, nullptr, fs, fst);
@@ -445,7 +477,7 @@ __global__ void __launch_bounds__(NT) k_bwd_query(Dims D, const T *__restrict__ 
                                                   const T *__restrict__ dO,
                                                   const float *__restrict__ W,
                                                   const float *__restrict__ S, T *__restrict__ dQ,
-                                                  float2 *__restrict__ aux)
+                                                  float2 *__restrict__ aux, float *__restrict__ dbpart)
 {
     extern __shared__ float sm[];
     const QueryBwdSmem L(D);
@@ -455,7 +487,7 @@ __global__ void __launch_bounds__(NT) k_bwd_query(Dims D, const T *__restrict__ 
     const int64_t bh = blockIdx.y, n0 = (int64_t)blockIdx.x * TT;
     const int cnt = (int)min((int64_t)TT, D.N - n0);
     const int dp = D.d + 1, fst = D.LR + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     load_rows(Q + bh * D.N * D.d, n0, cnt, D.d, xs);
     load_rows(dO + bh * D.N * D.d, n0, cnt, D.d, ys);
     __syncthreads();
@@ -490,13 +522,14 @@ __global__ void __launch_bounds__(NT) k_bwd_query(Dims D, const T *__restrict__ 
         gs[t * fst + f] = (gs[t * fst + f] - sb[f] * cc[t]) / den[t];
     }
     __syncthreads();
-    featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red);
+    const float db = featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red);
     T *dQb = dQ + bh * D.N * D.d;
     for (int i = threadIdx.x; i < cnt * D.d; i += NT) {
         const int t = i / D.d, c = i - t * D.d;
         st_f(dQb, (n0 + t) * D.d + c, dx[t * dp + c]);
     }
     for (int t = threadIdx.x; t < cnt; t += NT) aux[bh * D.N + n0 + t] = make_float2(1.f / den[t], cc[t]);
+    store_dbeta_partial(db, red, dbpart, bh);
 }
 
 // Non-causal backward, key side.  With G = [dA | dB] = sum_t phi(Q_t) [dO_t/den_t | -c_t/den_t]:
@@ -507,7 +540,7 @@ __global__ void __launch_bounds__(NT) k_bwd_key(Dims D, const T *__restrict__ K,
                                                 const T *__restrict__ V,
                                                 const float *__restrict__ W,
                                                 const float *__restrict__ G, T *__restrict__ dK,
-                                                T *__restrict__ dV)
+                                                T *__restrict__ dV, float *__restrict__ dbpart)
 {
     extern __shared__ float sm[];
     const KeyBwdSmem L(D);
@@ -517,7 +550,7 @@ __global__ void __launch_bounds__(NT) k_bwd_key(Dims D, const T *__restrict__ K,
     const int64_t bh = blockIdx.y, n0 = (int64_t)blockIdx.x * TT;
     const int cnt = (int)min((int64_t)TT, D.N - n0);
     const int dp = D.d + 1, fst = D.LR + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     load_rows(K + bh * D.N * D.d, n0, cnt, D.d, xs);
     load_values(V + bh * D.N * D.d, n0, cnt, D.d, vs);
     __syncthreads();
@@ -549,7 +582,7 @@ __global__ void __launch_bounds__(NT) k_bwd_key(Dims D, const T *__restrict__ K,
         }
     }
     __syncthreads();
-    featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red);
+    const float db = featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red);
     T *dKb = dK + bh * D.N * D.d, *dVb = dV + bh * D.N * D.d;
 #pragma unroll
     for (int k = 0; k < KOUT; ++k) {
@@ -563,6 +596,7 @@ __global__ void __launch_bounds__(NT) k_bwd_key(Dims D, const T *__restrict__ K,
         const int t = i / D.d, c = i - t * D.d;
         st_f(dKb, (n0 + t) * D.d + c, dx[t * dp + c]);
     }
+    store_dbeta_partial(db, red, dbpart, bh);
 }
 
 // Causal forward over one segment (Algorithm 2 in tiles).  S starts as the sketch of all keys
@@ -584,7 +618,7 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(Dims D, const T *__restrict__
     const int s = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int fst = D.LR + 1, dv = D.dv, E = D.LR * D.dv;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     const float *S0b = S0 + ((int64_t)bh * nseg + s) * E;
     for (int i = threadIdx.x; i < E; i += NT) S[i] = S0b[i];
     const int64_t off = bh * D.N * D.d;
@@ -639,7 +673,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_q(Dims D, const T *__restrict
                                                      const float *__restrict__ W,
                                                      const float *__restrict__ S0, int64_t seg_len,
                                                      int nseg, T *__restrict__ dQ,
-                                                     float2 *__restrict__ aux)
+                                                     float2 *__restrict__ aux, float *__restrict__ dbpart)
 {
     extern __shared__ float sm[];
     const CausalBwdSmem L(D);
@@ -650,11 +684,12 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_q(Dims D, const T *__restrict
     const int s = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int fst = D.LR + 1, dv = D.dv, dp = D.d + 1, E = D.LR * D.dv, TP = TT + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     const float *S0b = S0 + ((int64_t)bh * nseg + s) * E;
     for (int i = threadIdx.x; i < E; i += NT) S[i] = S0b[i];
     const int64_t off = bh * D.N * D.d;
     const int64_t n_end = min(D.N, (int64_t)(s + 1) * seg_len);
+    float db = 0.f;
     for (int64_t n0 = (int64_t)s * seg_len; n0 < n_end; n0 += TT) {
         const int cnt = (int)min((int64_t)TT, n_end - n0);
         __syncthreads();
@@ -702,7 +737,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_q(Dims D, const T *__restrict
             gs[t * fst + f] = (gs[t * fst + f] - sb * cc[t]) / den[t];
         }
         __syncthreads();
-        featurise_backward(xq, D, ws, invq, us, fq, gs, fst, dz, dx, red);
+        db += featurise_backward(xq, D, ws, invq, us, fq, gs, fst, dz, dx, red);
         for (int i = threadIdx.x; i < cnt * D.d; i += NT) {
             const int t = i / D.d, c = i - t * D.d;
             st_f(dQ + off, (n0 + t) * D.d + c, dx[t * dp + c]);
@@ -715,6 +750,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_q(Dims D, const T *__restrict
             S[o] = a;
         }
     }
+    store_dbeta_partial(db, red, dbpart, bh);
 }
 
 // Causal backward, reverse-order pass over one segment.  G starts as the suffix gradient
@@ -731,7 +767,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_kv(Dims D, const T *__restric
                                                       const float *__restrict__ W,
                                                       const float *__restrict__ G0, int64_t seg_len,
                                                       int nseg, T *__restrict__ dK,
-                                                      T *__restrict__ dV)
+                                                      T *__restrict__ dV, float *__restrict__ dbpart)
 {
     extern __shared__ float sm[];
     const CausalBwdSmem L(D);
@@ -742,7 +778,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_kv(Dims D, const T *__restric
     const int s = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int fst = D.LR + 1, dv = D.dv, dp = D.d + 1, E = D.LR * D.dv, TP = TT + 1;
-    load_w(W, D, 0, D.L, ws);
+    load_w(head_w(W, D, bh), D, 0, D.L, ws);
     const float *G0b = G0 + ((int64_t)bh * nseg + s) * E;
     for (int i = threadIdx.x; i < E; i += NT) G[i] = G0b[i];
     const int64_t off = bh * D.N * D.d;
@@ -750,6 +786,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_kv(Dims D, const T *__restric
     const int64_t n_end = min(D.N, n_begin + seg_len);
     if (n_begin >= n_end) return;
     const int64_t last = n_begin + ((n_end - 1 - n_begin) / TT) * TT;
+    float db = 0.f;
     for (int64_t n0 = last; n0 >= n_begin; n0 -= TT) {
         const int cnt = (int)min((int64_t)TT, n_end - n0);
         __syncthreads();
@@ -800,7 +837,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_kv(Dims D, const T *__restric
             gs[j * fst + f] = g;
         }
         __syncthreads();
-        featurise_backward(xk, D, ws, invk, us, fk, gs, fst, dz, dx, red);
+        db += featurise_backward(xk, D, ws, invk, us, fk, gs, fst, dz, dx, red);
 #pragma unroll
         for (int k = 0; k < KOUT; ++k) {
             const int o = threadIdx.x + k * NT;
@@ -820,6 +857,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_kv(Dims D, const T *__restric
             G[o] = a;
         }
     }
+    store_dbeta_partial(db, red, dbpart, bh);
 }
 
 }  // namespace gen
@@ -873,6 +911,12 @@ cudaError_t launch_combine(const Dims &D, const float *part, float *out, int nsp
     return launch_kernel("combine", gen::k_combine, grid, dim3(256), 0, st, part, out, E, nsplit, mode);
 }
 
+cudaError_t launch_dbeta_combine(const Dims &D, const float *part, int slots, float *dbeta, cudaStream_t st)
+{
+    return launch_kernel("dbeta_combine", gen::k_dbeta_combine, dim3((unsigned)D.BH), dim3(256), 0, st, part,
+                         slots, D.BH, dbeta);
+}
+
 template <typename T>
 cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const float *S, T *O, cudaStream_t st)
 {
@@ -885,24 +929,26 @@ cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const floa
 
 template <typename T>
 cudaError_t launch_bwd_query(const Dims &D, const T *Q, const T *dO, const float *W, const float *S, T *dQ,
-                             float2 *aux, cudaStream_t st)
+                             float2 *aux, float *dbpart, cudaStream_t st)
 {
     const size_t smem = generic_smem_bytes(D, GenericKernel::QueryBwd);
     cudaError_t e = prep(gen::k_bwd_query<T>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((D.N + gen::TT - 1) / gen::TT), (unsigned)D.BH);
-    return launch_kernel("bwd_query", gen::k_bwd_query<T>, grid, dim3(gen::NT), smem, st, D, Q, dO, W, S, dQ, aux);
+    return launch_kernel("bwd_query", gen::k_bwd_query<T>, grid, dim3(gen::NT), smem, st, D, Q, dO, W, S, dQ, aux,
+                         dbpart);
 }
 
 template <typename T>
 cudaError_t launch_bwd_key(const Dims &D, const T *K, const T *V, const float *W, const float *G, T *dK, T *dV,
-                           cudaStream_t st)
+                           float *dbpart, cudaStream_t st)
 {
     const size_t smem = generic_smem_bytes(D, GenericKernel::KeyBwd);
     cudaError_t e = prep(gen::k_bwd_key<T>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((D.N + gen::TT - 1) / gen::TT), (unsigned)D.BH);
-    return launch_kernel("bwd_key", gen::k_bwd_key<T>, grid, dim3(gen::NT), smem, st, D, K, V, W, G, dK, dV);
+    return launch_kernel("bwd_key", gen::k_bwd_key<T>, grid, dim3(gen::NT), smem, st, D, K, V, W, G, dK, dV,
+                         dbpart);
 }
 
 template <typename T>
@@ -919,27 +965,28 @@ cudaError_t launch_causal_fwd(const Dims &D, const T *Q, const T *K, const T *V,
 
 template <typename T>
 cudaError_t launch_causal_bwd_q(const Dims &D, const T *Q, const T *K, const T *V, const T *dO, const float *W,
-                                const float *S0, int64_t seg_len, int nseg, T *dQ, float2 *aux, cudaStream_t st)
+                                const float *S0, int64_t seg_len, int nseg, T *dQ, float2 *aux, float *dbpart,
+                                cudaStream_t st)
 {
     const size_t smem = generic_smem_bytes(D, GenericKernel::CausalBwd);
     cudaError_t e = prep(gen::k_causal_bwd_q<T>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(nseg, (unsigned)D.BH);
     return launch_kernel("causal_bwd_q", gen::k_causal_bwd_q<T>, grid, dim3(gen::NT), smem, st, D, Q, K, V, dO, W,
-                         S0, seg_len, nseg, dQ, aux);
+                         S0, seg_len, nseg, dQ, aux, dbpart);
 }
 
 template <typename T>
 cudaError_t launch_causal_bwd_kv(const Dims &D, const T *Q, const T *K, const T *V, const T *dO,
                                  const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
-                                 T *dK, T *dV, cudaStream_t st)
+                                 T *dK, T *dV, float *dbpart, cudaStream_t st)
 {
     const size_t smem = generic_smem_bytes(D, GenericKernel::CausalBwd);
     cudaError_t e = prep(gen::k_causal_bwd_kv<T>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(nseg, (unsigned)D.BH);
     return launch_kernel("causal_bwd_kv", gen::k_causal_bwd_kv<T>, grid, dim3(gen::NT), smem, st, D, Q, K, V, dO,
-                         aux, W, G0, seg_len, nseg, dK, dV);
+                         aux, W, G0, seg_len, nseg, dK, dV, dbpart);
 }
 
 #define RACE_INSTANTIATE(T)                                                                                    \
@@ -948,17 +995,17 @@ cudaError_t launch_causal_bwd_kv(const Dims &D, const T *Q, const T *K, const T 
     template cudaError_t launch_readout<T>(const Dims &, const T *, const float *, const float *, T *,         \
                                            cudaStream_t);                                                      \
     template cudaError_t launch_bwd_query<T>(const Dims &, const T *, const T *, const float *, const float *, \
-                                             T *, float2 *, cudaStream_t);                                     \
+                                             T *, float2 *, float *, cudaStream_t);                            \
     template cudaError_t launch_bwd_key<T>(const Dims &, const T *, const T *, const float *, const float *,   \
-                                           T *, T *, cudaStream_t);                                            \
+                                           T *, T *, float *, cudaStream_t);                                   \
     template cudaError_t launch_causal_fwd<T>(const Dims &, const T *, const T *, const T *, const float *,    \
                                               const float *, int64_t, int, T *, cudaStream_t);                 \
     template cudaError_t launch_causal_bwd_q<T>(const Dims &, const T *, const T *, const T *, const T *,      \
                                                 const float *, const float *, int64_t, int, T *, float2 *,     \
-                                                cudaStream_t);                                                 \
+                                                float *, cudaStream_t);                                        \
     template cudaError_t launch_causal_bwd_kv<T>(const Dims &, const T *, const T *, const T *, const T *,     \
                                                  const float2 *, const float *, const float *, int64_t, int,   \
-                                                 T *, T *, cudaStream_t);
+                                                 T *, T *, float *, cudaStream_t);
 
 RACE_INSTANTIATE(float)
 RACE_INSTANTIATE(__nv_bfloat16)

@@ -29,6 +29,11 @@ template <typename T>
 cudaError_t launch_decode(const Dims &D, const T *q, const T *k, const T *v, const float *W, float *S, T *o,
                           cudaStream_t st);
 
+// ---------------------------------------------------------------- exact angular attention
+template <typename T>
+cudaError_t launch_angular(const Dims &D, const T *Q, const T *K, const T *V, float gamma, int causal, T *O,
+                           cudaStream_t st);
+
 // ---------------------------------------------------------------- CUDA-core kernels
 enum class GenericKernel { Sketch, Readout, QueryBwd, KeyBwd, CausalFwd, CausalBwd };
 size_t generic_smem_bytes(const Dims &D, GenericKernel which);
@@ -38,24 +43,27 @@ template <typename T>
 cudaError_t launch_sketch(const Dims &D, const T *X, const T *Y, const float2 *aux, const float *W,
                           int64_t seg_len, int nsplit, float *part, int mode, cudaStream_t st);
 cudaError_t launch_combine(const Dims &D, const float *part, float *out, int nsplit, int mode, cudaStream_t st);
+// dbeta[bh] from the backward kernels' d(loss)/d(beta) partials, two [BH][slots] float arrays.
+cudaError_t launch_dbeta_combine(const Dims &D, const float *part, int slots, float *dbeta, cudaStream_t st);
 template <typename T>
 cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const float *S, T *O, cudaStream_t st);
 template <typename T>
 cudaError_t launch_bwd_query(const Dims &D, const T *Q, const T *dO, const float *W, const float *S, T *dQ,
-                             float2 *aux, cudaStream_t st);
+                             float2 *aux, float *dbpart, cudaStream_t st);
 template <typename T>
 cudaError_t launch_bwd_key(const Dims &D, const T *K, const T *V, const float *W, const float *G, T *dK, T *dV,
-                           cudaStream_t st);
+                           float *dbpart, cudaStream_t st);
 template <typename T>
 cudaError_t launch_causal_fwd(const Dims &D, const T *Q, const T *K, const T *V, const float *W, const float *S0,
                               int64_t seg_len, int nseg, T *O, cudaStream_t st);
 template <typename T>
 cudaError_t launch_causal_bwd_q(const Dims &D, const T *Q, const T *K, const T *V, const T *dO, const float *W,
-                                const float *S0, int64_t seg_len, int nseg, T *dQ, float2 *aux, cudaStream_t st);
+                                const float *S0, int64_t seg_len, int nseg, T *dQ, float2 *aux, float *dbpart,
+                                cudaStream_t st);
 template <typename T>
 cudaError_t launch_causal_bwd_kv(const Dims &D, const T *Q, const T *K, const T *V, const T *dO,
                                  const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
-                                 T *dK, T *dV, cudaStream_t st);
+                                 T *dK, T *dV, float *dbpart, cudaStream_t st);
 
 // ---------------------------------------------------------------- tensor-core causal path (bf16)
 bool causal_tc_supported(const Dims &D);
@@ -69,11 +77,12 @@ cudaError_t launch_causal_tc_fwd(const Dims &D, const bf16_t *Q, const bf16_t *K
 bool causal_tc_bwd_supported(const Dims &D);
 cudaError_t launch_causal_tc_bwd_q(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V,
                                    const bf16_t *dO, const float *W, const float *S0, int64_t seg_len, int nseg,
-                                   bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, cudaStream_t st);
+                                   bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, float *dbpart,
+                                   cudaStream_t st);
 cudaError_t launch_causal_tc_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V,
                                     const bf16_t *dO, const float2 *aux, const float *W, const float *G0,
                                     int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err,
-                                    cudaStream_t st);
+                                    float *dbpart, cudaStream_t st);
 
 // ---------------------------------------------------------------- tcgen05 non-causal path (bf16)
 bool nc5_supported(const Dims &D);
@@ -89,13 +98,15 @@ cudaError_t launch_c5_fwd(const Dims &D, const bf16_t *Q, const bf16_t *K, const
 bool c5_bwd_supported(const Dims &D);
 cudaError_t launch_c5_bwd_q(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
                             const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
-                            float *Gseg, unsigned *err, cudaStream_t st);
+                            float *Gseg, unsigned *err, float *dbpart, cudaStream_t st);
 cudaError_t launch_c5_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
                              const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
-                             bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st);
+                             bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st);
+// Token segments per (b, h) of the two non-causal tcgen05 backward kernels (their grid's x).
+int nc5_bwd_nseg(const Dims &D);
 cudaError_t launch_nc5_bwd_query(const Dims &D, const bf16_t *Q, const bf16_t *dO, const float *W, const float *S,
-                                 bf16_t *dQ, float2 *aux, unsigned *err, cudaStream_t st);
+                                 bf16_t *dQ, float2 *aux, unsigned *err, float *dbpart, cudaStream_t st);
 cudaError_t launch_nc5_bwd_key(const Dims &D, const bf16_t *K, const bf16_t *V, const float *W, const float *G,
-                               bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st);
+                               bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st);
 
 }  // namespace race

@@ -123,12 +123,13 @@ __host__ __device__ inline uint32_t bwdk_cols(int D, int lrp) { return pow2_cols
 // ------------------------------------------------------------------ query side
 
 // dQ and aux[t] = {1 / den_t, c_t} for the CTA's tiles.  S: combined key sketch [BH][LR][d + 1].
-template <int D, int P, int LT>
+// DB: also the CTA's query-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
+template <int D, int P, int LT, bool DB>
 __global__ void __launch_bounds__(NTH, 1)
     k_bwdq5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
             const __grid_constant__ CUtensorMap tmdQ, Dims Dm, const float *__restrict__ W,
             const float *__restrict__ S, float2 *__restrict__ aux, int64_t seg_len, int split_s,
-            unsigned *__restrict__ err)
+            unsigned *__restrict__ err, float *__restrict__ dbpart)
 {
     constexpr int KB = D / 64;
     constexpr int R = 1 << P;
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const int L = LT > 0 ? LT : Dm.L;  // LT > 0: per-table loops unroll without guards
 
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
-    load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     load_sketch_rows<D>(S + bh * Dm.LR * (D + 1), Dm.LR, lrp, base + Ly.shi, base + Ly.slo, Ly.split,
                         reinterpret_cast<float *>(sm + Ly.mass));
     if (tid == 0) {
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(NTH, 1)
     }
 
     bool failed = false;
+    float db = 0.f;  // this thread's d(loss)/d(beta) share (DB only)
     int i = 0;
     for (; i < ntile; ++i) {
         const int s = i & 1;
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(NTH, 1)
                 ld_cols<R>(tlane + l * R, g);
 #pragma unroll
                 for (int r = 0; r < R; ++r) g[r] = (g[r] - mass[l * R + r] * cc) * rd;
-                table_backward<P>(u, ph, g, beta, dz + k * P);
+                table_backward<P, DB>(u, ph, g, beta, dz + k * P, &db);
 #pragma unroll
                 for (int p = 0; p < P; ++p)
                     zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[k * P + p])), z[l * P + p], zdz);
@@ -363,6 +365,10 @@ __global__ void __launch_bounds__(NTH, 1)
         if (i < ntile) mbar_wait(bar_load + 8 * (i & 1), (i >> 1) & 1);
         if (i + 1 < ntile) mbar_wait(bar_load + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1);
     }
+    if constexpr (DB) {
+        const float sdb = block_sum_fixed(db, red);
+        if (tid == 0) dbpart[bh * gridDim.x + blockIdx.x] = sdb;
+    }
     if (tid == 0) bulk_wait0();
     fence_before();
     __syncthreads();
@@ -375,12 +381,13 @@ __global__ void __launch_bounds__(NTH, 1)
 // ------------------------------------------------------------------ key side
 
 // dK and dV for the CTA's tiles.  G: combined gradient sketch [BH][LR][d + 1].
-template <int D, int P, int LT>
+// DB: also the CTA's key-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
+template <int D, int P, int LT, bool DB>
 __global__ void __launch_bounds__(NTH, 1)
     k_bwdk5(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
             const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV, Dims Dm,
             const float *__restrict__ W, const float *__restrict__ G, int64_t seg_len, int split_s,
-            unsigned *__restrict__ err)
+            unsigned *__restrict__ err, float *__restrict__ dbpart)
 {
     constexpr int KB = D / 64;
     constexpr int R = 1 << P;
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const int L = LT > 0 ? LT : Dm.L;  // LT > 0: per-table loops unroll without guards
 
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
-    load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     load_sketch_rows<D>(G + bh * Dm.LR * (D + 1), Dm.LR, lrp, base + Ly.shi, base + Ly.slo, Ly.split,
                         reinterpret_cast<float *>(sm + Ly.mass));
     if (tid == 0) {
@@ -454,6 +461,7 @@ __global__ void __launch_bounds__(NTH, 1)
     }
 
     bool failed = false;
+    float db = 0.f;  // this thread's d(loss)/d(beta) share (DB only)
     int i = 0;
     for (; i < ntile; ++i) {
         const int s = i & 1;
@@ -518,7 +526,7 @@ __global__ void __launch_bounds__(NTH, 1)
                 ld_cols<R>(tlane + l * R, dph);
 #pragma unroll
                 for (int r = 0; r < R; ++r) dph[r] += gmass[l * R + r];
-                table_backward<P>(u, ph, dph, beta, dz + k * P);
+                table_backward<P, DB>(u, ph, dph, beta, dz + k * P, &db);
 #pragma unroll
                 for (int p = 0; p < P; ++p)
                     zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[k * P + p])), z[l * P + p], zdz);
@@ -607,6 +615,10 @@ __global__ void __launch_bounds__(NTH, 1)
         if (i < ntile) mbar_wait(bar_load + 8 * (i & 1), (i >> 1) & 1);
         if (i + 1 < ntile) mbar_wait(bar_load + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1);
     }
+    if constexpr (DB) {
+        const float sdb = block_sum_fixed(db, red);
+        if (tid == 0) dbpart[bh * gridDim.x + blockIdx.x] = sdb;
+    }
     if (tid == 0) bulk_wait0();
     fence_before();
     __syncthreads();
@@ -650,56 +662,58 @@ nc5::BwdLayout bwd_layout(const Dims &Dm)
 
 template <int D, int P, int LT>
 cudaError_t bwdq_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mdo, const CUtensorMap &mdq,
-                        const float *W, const float *S, float2 *aux, unsigned *err, cudaStream_t st)
+                        const float *W, const float *S, float2 *aux, unsigned *err, float *dbpart, cudaStream_t st)
 {
     const nc5::BwdLayout Ly = bwd_layout(Dm);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = nc5::k_bwdq5<D, P, LT>;
+    auto kern = dbpart ? nc5::k_bwdq5<D, P, LT, true> : nc5::k_bwdq5<D, P, LT, false>;
     cudaError_t e = prep_bwd(kern, smem);
     if (e != cudaSuccess) return e;
     const int64_t seg = bwd_seg(Dm, smem);
     const int64_t nseg = (Dm.N + seg - 1) / seg;
     return launch_kernel("tc5_bwd_query", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(nc5::NTH), smem, st, mq,
-                         mdo, mdq, Dm, W, S, aux, seg, (int)Ly.split, err);
+                         mdo, mdq, Dm, W, S, aux, seg, (int)Ly.split, err, dbpart);
 }
 
 // The named non-causal workloads' shapes run with L compiled in: (d, P, L) = (64, 3, 3), (128, 6, 4).
 template <int D, int P>
 cudaError_t bwdq_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mdo, const CUtensorMap &mdq,
-                      const float *W, const float *S, float2 *aux, unsigned *err, cudaStream_t st)
+                      const float *W, const float *S, float2 *aux, unsigned *err, float *dbpart, cudaStream_t st)
 {
     if constexpr (D == 64 && P == 3)
-        if (Dm.L == 3) return bwdq_launch<D, P, 3>(Dm, mq, mdo, mdq, W, S, aux, err, st);
+        if (Dm.L == 3) return bwdq_launch<D, P, 3>(Dm, mq, mdo, mdq, W, S, aux, err, dbpart, st);
     if constexpr (D == 128 && P == 6)
-        if (Dm.L == 4) return bwdq_launch<D, P, 4>(Dm, mq, mdo, mdq, W, S, aux, err, st);
-    return bwdq_launch<D, P, 0>(Dm, mq, mdo, mdq, W, S, aux, err, st);
+        if (Dm.L == 4) return bwdq_launch<D, P, 4>(Dm, mq, mdo, mdq, W, S, aux, err, dbpart, st);
+    return bwdq_launch<D, P, 0>(Dm, mq, mdo, mdq, W, S, aux, err, dbpart, st);
 }
 
 template <int D, int P, int LT>
 cudaError_t bwdk_launch(const Dims &Dm, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdk,
-                        const CUtensorMap &mdv, const float *W, const float *G, unsigned *err, cudaStream_t st)
+                        const CUtensorMap &mdv, const float *W, const float *G, unsigned *err, float *dbpart,
+                        cudaStream_t st)
 {
     const nc5::BwdLayout Ly = bwd_layout(Dm);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = nc5::k_bwdk5<D, P, LT>;
+    auto kern = dbpart ? nc5::k_bwdk5<D, P, LT, true> : nc5::k_bwdk5<D, P, LT, false>;
     cudaError_t e = prep_bwd(kern, smem);
     if (e != cudaSuccess) return e;
     const int64_t seg = bwd_seg(Dm, smem);
     const int64_t nseg = (Dm.N + seg - 1) / seg;
     return launch_kernel("tc5_bwd_key", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(nc5::NTH), smem, st, mk,
-                         mv, mdk, mdv, Dm, W, G, seg, (int)Ly.split, err);
+                         mv, mdk, mdv, Dm, W, G, seg, (int)Ly.split, err, dbpart);
 }
 
 // The named non-causal workloads' shapes run with L compiled in: (d, P, L) = (64, 3, 3), (128, 6, 4).
 template <int D, int P>
 cudaError_t bwdk_inst(const Dims &Dm, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdk,
-                      const CUtensorMap &mdv, const float *W, const float *G, unsigned *err, cudaStream_t st)
+                      const CUtensorMap &mdv, const float *W, const float *G, unsigned *err, float *dbpart,
+                      cudaStream_t st)
 {
     if constexpr (D == 64 && P == 3)
-        if (Dm.L == 3) return bwdk_launch<D, P, 3>(Dm, mk, mv, mdk, mdv, W, G, err, st);
+        if (Dm.L == 3) return bwdk_launch<D, P, 3>(Dm, mk, mv, mdk, mdv, W, G, err, dbpart, st);
     if constexpr (D == 128 && P == 6)
-        if (Dm.L == 4) return bwdk_launch<D, P, 4>(Dm, mk, mv, mdk, mdv, W, G, err, st);
-    return bwdk_launch<D, P, 0>(Dm, mk, mv, mdk, mdv, W, G, err, st);
+        if (Dm.L == 4) return bwdk_launch<D, P, 4>(Dm, mk, mv, mdk, mdv, W, G, err, dbpart, st);
+    return bwdk_launch<D, P, 0>(Dm, mk, mv, mdk, mdv, W, G, err, dbpart, st);
 }
 
 #define RACE_NC5B_DISPATCH(FN, ...)                        \
@@ -721,19 +735,25 @@ cudaError_t bwdk_inst(const Dims &Dm, const CUtensorMap &mk, const CUtensorMap &
 
 }  // namespace
 
+int nc5_bwd_nseg(const Dims &Dm)
+{
+    const int64_t seg = bwd_seg(Dm, bwd_layout(Dm).bytes + 1024);
+    return (int)((Dm.N + seg - 1) / seg);
+}
+
 cudaError_t launch_nc5_bwd_query(const Dims &Dm, const bf16_t *Q, const bf16_t *dO, const float *W, const float *S,
-                                 bf16_t *dQ, float2 *aux, unsigned *err, cudaStream_t st)
+                                 bf16_t *dQ, float2 *aux, unsigned *err, float *dbpart, cudaStream_t st)
 {
     CUtensorMap mq, mdo, mdq;
     cudaError_t e = make_token_map(&mq, Q, Dm);
     if (e == cudaSuccess) e = make_token_map(&mdo, dO, Dm);
     if (e == cudaSuccess) e = make_token_map(&mdq, dQ, Dm);
     if (e != cudaSuccess) return e;
-    RACE_NC5B_DISPATCH(bwdq_inst, Dm, mq, mdo, mdq, W, S, aux, err, st)
+    RACE_NC5B_DISPATCH(bwdq_inst, Dm, mq, mdo, mdq, W, S, aux, err, dbpart, st)
 }
 
 cudaError_t launch_nc5_bwd_key(const Dims &Dm, const bf16_t *K, const bf16_t *V, const float *W, const float *G,
-                               bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+                               bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
     CUtensorMap mk, mv, mdk, mdv;
     cudaError_t e = make_token_map(&mk, K, Dm);
@@ -741,7 +761,7 @@ cudaError_t launch_nc5_bwd_key(const Dims &Dm, const bf16_t *K, const bf16_t *V,
     if (e == cudaSuccess) e = make_token_map(&mdk, dK, Dm);
     if (e == cudaSuccess) e = make_token_map(&mdv, dV, Dm);
     if (e != cudaSuccess) return e;
-    RACE_NC5B_DISPATCH(bwdk_inst, Dm, mk, mv, mdk, mdv, W, G, err, st)
+    RACE_NC5B_DISPATCH(bwdk_inst, Dm, mk, mv, mdk, mdv, W, G, err, dbpart, st)
 }
 
 }  // namespace race

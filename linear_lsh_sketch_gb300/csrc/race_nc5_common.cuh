@@ -234,9 +234,13 @@ __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv,
 
 // Chain rule from dphi (one table, R values, phi recomputed from u) to the table's P
 // projection gradients dz_p = beta * sum_r phi_r (dphi_r - phi . dphi) v_{r,p} * (1 - u_p^2).
-template <int P>
+// DB: also adds the table's d(loss)/d(beta) share to *db.  The logits are beta (u . v_r), so
+// that share is sum_r ds_r (u . v_r) = sum_p u_p du_p with du_p = sum_r ds_r v_{r,p}, the sum
+// formed here before the scaling by beta.
+template <int P, bool DB = false>
 __device__ __forceinline__ void table_backward(const float (&u)[P], const float (&ph)[1 << P],
-                                               const float (&dph)[1 << P], float beta, float *dz)
+                                               const float (&dph)[1 << P], float beta, float *dz,
+                                               float *db = nullptr)
 {
     constexpr int R = 1 << P;
     float s = 0.f;
@@ -250,6 +254,12 @@ __device__ __forceinline__ void table_backward(const float (&u)[P], const float 
         const float ds = ph[r] * (dph[r] - s);
 #pragma unroll
         for (int p = 0; p < P; ++p) du[p] += ((r >> p) & 1) ? ds : -ds;
+    }
+    if constexpr (DB) {
+        float a = *db;
+#pragma unroll
+        for (int p = 0; p < P; ++p) a = fmaf(u[p], du[p], a);
+        *db = a;
     }
 #pragma unroll
     for (int p = 0; p < P; ++p) dz[p] = beta * du[p] * (1.f - u[p] * u[p]);

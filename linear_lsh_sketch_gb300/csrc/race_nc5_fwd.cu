@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         zero_region(sm + Ly.f, nf * Ly.fbytes);
         init_mass_tile(sm + Ly.mass, mode == 0);  // mode 1 writes rows 0 and 1 per tile
         init_mass_tile(sm + Ly.mass + 4096, mode == 0);
-        load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+        load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     }
     if (tid == NTH) {
         for (uint32_t i = 0; i < SB_COUNT; ++i) mbar_init(bar(i), (i == SB_F0 || i == SB_F1) ? 8 : i == SB_CS ? NTH : 1);
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(NTH, 1)
     // ---- set-up: sketch operand (K-major B: row n = output column, 64-column blocks of lr)
     if (warp == 0) tmem_alloc(base + Ly.slot, ncols);
     zero_region(sm + Ly.f, Ly.fb * BLK);
-    load_w_tiles<D>(W, Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+    load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
     {
         const float *Sb = S + bh * Dm.LR * (D + 1);
         const int nchunk = Ly.fb * 8;  // 8-lr chunks per operand row

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(NTH, 1)
     // ---- set-up: zero tiles (stale rows past the sequence end stay finite), W split, state
     zero_smem(smem, Cf::OFF_W);
     __syncthreads();
-    load_w_split<D, Cf::XS>(W, Dm.LP, wc);
+    load_w_split<D, Cf::XS>(head_w(W, Dm, bh), Dm.LP, wc);
     float st[Cf::SNT][Cf::MT][4];
     const float *S0b = TOTALS ? nullptr : S0 + ((int64_t)bh * nseg + s) * Dm.LR * (D + 1);
 #pragma unroll

@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(NTH, 1)
     k_causal_bwd_q_tc(Dims Dm, const bf16 *__restrict__ Q, const bf16 *__restrict__ K, const bf16 *__restrict__ V,
                       const bf16 *__restrict__ dO, const float *__restrict__ W, const float *__restrict__ S0,
                       int64_t seg_len, int nseg, bf16 *__restrict__ dQ, float2 *__restrict__ aux,
-                      float *__restrict__ Gseg, unsigned *__restrict__ err)
+                      float *__restrict__ Gseg, unsigned *__restrict__ err, float *__restrict__ dbpart)
 {
     using B = BwdCfg<D, P, LRP>;
     constexpr int NC = B::NC;
@@ -343,9 +343,10 @@ __global__ void __launch_bounds__(NTH, 1)
     const int64_t off = bh * Dm.N * D;
     const int64_t n_begin = (int64_t)s * seg_len;
     const int64_t n_end = min(Dm.N, n_begin + seg_len);
+    float db = 0.f;  // this thread's d(loss)/d(beta) share (dbpart only)
     const int t0 = 16 * rb + g, t1 = t0 + 8;
 
-    bwd_setup<D, P, LRP>(Dm, W, smem);
+    bwd_setup<D, P, LRP>(Dm, head_w(W, Dm, bh), smem);
     float st[B::SNT][B::MT][4], gacc[B::SNT][B::MT][4];
     load_sketch<D, P, LRP>(Dm, S0 + ((int64_t)bh * nseg + s) * Dm.LR * (D + 1), warp, lane, st, sh(0, 0), sh(0, 1));
 #pragma unroll
@@ -572,7 +573,8 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             __syncwarp();
             features_backward16<P, B::US, B::DPS, B::ZS>(ust, dphi + 16 * rb * B::DPS, Dm.L, Dm.beta,
-                                                         dzs + 16 * rb * B::ZS, lane);
+                                                         dzs + 16 * rb * B::ZS, lane, dbpart ? &db : nullptr,
+                                                         16 * rb, cnt);
         }
         sketch_update<D, P, LRP, false>(st, fk, xvb, warp, lane);
         refresh_sketch<D, P, LRP>(st, warp, lane, sh(buf ^ 1, 0), sh(buf ^ 1, 1));
@@ -590,6 +592,10 @@ __global__ void __launch_bounds__(NTH, 1)
         store_rows<D, B::XS>(xkb, dQ + off, n0, cnt, rb, h, lane);
     }
     store_sketch<D, P, LRP>(Dm, gacc, Gseg + ((int64_t)bh * nseg + s) * Dm.LR * (D + 1), warp, lane);
+    if (dbpart) {  // this CTA's query-side d(loss)/d(beta) partial, summed in a fixed order
+        const float sdb = block_sum_fixed(db, red);
+        if (tid == 0) dbpart[bh * gridDim.x + blockIdx.x] = sdb;
+    }
 }
 
 // ------------------------------------------------------------------ pass 2: dK, dV
@@ -599,7 +605,7 @@ __global__ void __launch_bounds__(NTH, 1)
     k_causal_bwd_kv_tc(Dims Dm, const bf16 *__restrict__ Q, const bf16 *__restrict__ K, const bf16 *__restrict__ V,
                        const bf16 *__restrict__ dO, const float2 *__restrict__ aux, const float *__restrict__ W,
                        const float *__restrict__ G0, int64_t seg_len, int nseg, bf16 *__restrict__ dK,
-                       bf16 *__restrict__ dV, unsigned *__restrict__ err)
+                       bf16 *__restrict__ dV, unsigned *__restrict__ err, float *__restrict__ dbpart)
 {
     using B = BwdCfg<D, P, LRP>;
     constexpr int NC = B::NC;
@@ -626,9 +632,10 @@ __global__ void __launch_bounds__(NTH, 1)
     const int64_t off = bh * Dm.N * D;
     const int64_t n_begin = (int64_t)s * seg_len;
     const int64_t n_end = min(Dm.N, n_begin + seg_len);
+    float db = 0.f;  // this thread's d(loss)/d(beta) share (dbpart only)
     const int j0 = 16 * rb + g, j1 = j0 + 8;  // key rows of this warp's row block
 
-    bwd_setup<D, P, LRP>(Dm, W, smem);
+    bwd_setup<D, P, LRP>(Dm, head_w(W, Dm, bh), smem);
     float gst[B::SNT][B::MT][4];
     load_sketch<D, P, LRP>(Dm, G0 + ((int64_t)bh * nseg + s) * Dm.LR * (D + 1), warp, lane, gst, gh(0, 0), gh(0, 1));
     __syncthreads();
@@ -858,7 +865,8 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             __syncwarp();
             features_backward16<P, B::US, B::DPS, B::ZS>(ust, dphi + 16 * rb * B::DPS, Dm.L, Dm.beta,
-                                                         dzs + 16 * rb * B::ZS, lane);
+                                                         dzs + 16 * rb * B::ZS, lane, dbpart ? &db : nullptr,
+                                                         16 * rb, cnt);
         }
         __syncthreads();
 
@@ -871,6 +879,10 @@ __global__ void __launch_bounds__(NTH, 1)
         stage_dx<D, B::XS>(dx, xkb, invk, red, rb, h, lane, xvb);
         __syncwarp();
         store_rows<D, B::XS>(xvb, dK + off, n0, cnt, rb, h, lane);
+    }
+    if (dbpart) {  // this CTA's key-side d(loss)/d(beta) partial, summed in a fixed order
+        const float sdb = block_sum_fixed(db, red);
+        if (tid == 0) dbpart[bh * gridDim.x + blockIdx.x] = sdb;
     }
 }
 
@@ -891,7 +903,7 @@ constexpr bool bwd_fits()
 template <int D, int P, int LRP>
 cudaError_t launch_bwd_q_inst(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
                               const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
-                              float *Gseg, unsigned *err, cudaStream_t st)
+                              float *Gseg, unsigned *err, float *dbpart, cudaStream_t st)
 {
     using B = tc::BwdCfg<D, P, LRP>;
     if constexpr (!bwd_fits<D, P, LRP>()) {
@@ -901,14 +913,14 @@ cudaError_t launch_bwd_q_inst(const Dims &Dm, const bf16_t *Q, const bf16_t *K, 
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B::BYTES);
         if (e != cudaSuccess) return e;
         return launch_kernel("tc_causal_bwd_q", kern, dim3(nseg, (unsigned)Dm.BH), dim3(tc::NTH), (size_t)B::BYTES,
-                             st, Dm, Q, K, V, dO, W, S0, seg_len, nseg, dQ, aux, Gseg, err);
+                             st, Dm, Q, K, V, dO, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart);
     }
 }
 
 template <int D, int P, int LRP>
 cudaError_t launch_bwd_kv_inst(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
                                const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
-                               bf16_t *dK, bf16_t *dV, unsigned *err, cudaStream_t st)
+                               bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
     using B = tc::BwdCfg<D, P, LRP>;
     if constexpr (!bwd_fits<D, P, LRP>()) {
@@ -918,7 +930,7 @@ cudaError_t launch_bwd_kv_inst(const Dims &Dm, const bf16_t *Q, const bf16_t *K,
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B::BYTES);
         if (e != cudaSuccess) return e;
         return launch_kernel("tc_causal_bwd_kv", kern, dim3(nseg, (unsigned)Dm.BH), dim3(tc::NTH), (size_t)B::BYTES,
-                             st, Dm, Q, K, V, dO, aux, W, G0, seg_len, nseg, dK, dV, err);
+                             st, Dm, Q, K, V, dO, aux, W, G0, seg_len, nseg, dK, dV, err, dbpart);
     }
 }
 
@@ -940,11 +952,12 @@ bool causal_tc_bwd_supported(const Dims &Dm)
 
 cudaError_t launch_causal_tc_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V,
                                    const bf16_t *dO, const float *W, const float *S0, int64_t seg_len, int nseg,
-                                   bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, cudaStream_t st)
+                                   bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, float *dbpart,
+                                   cudaStream_t st)
 {
 #define RACE_CASE(DD, PP, LRPP)                               \
     if (Dm.d == DD && Dm.P == PP && Dm.LR <= LRPP)            \
-        return launch_bwd_q_inst<DD, PP, LRPP>(Dm, Q, K, V, dO, W, S0, seg_len, nseg, dQ, aux, Gseg, err, st);
+        return launch_bwd_q_inst<DD, PP, LRPP>(Dm, Q, K, V, dO, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart, st);
     RACE_TC_BWD_CASES(RACE_CASE)
 #undef RACE_CASE
     return cudaErrorInvalidValue;
@@ -953,11 +966,11 @@ cudaError_t launch_causal_tc_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t
 cudaError_t launch_causal_tc_bwd_kv(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V,
                                     const bf16_t *dO, const float2 *aux, const float *W, const float *G0,
                                     int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err,
-                                    cudaStream_t st)
+                                    float *dbpart, cudaStream_t st)
 {
 #define RACE_CASE(DD, PP, LRPP)                               \
     if (Dm.d == DD && Dm.P == PP && Dm.LR <= LRPP)            \
-        return launch_bwd_kv_inst<DD, PP, LRPP>(Dm, Q, K, V, dO, aux, W, G0, seg_len, nseg, dK, dV, err, st);
+        return launch_bwd_kv_inst<DD, PP, LRPP>(Dm, Q, K, V, dO, aux, W, G0, seg_len, nseg, dK, dV, err, dbpart, st);
     RACE_TC_BWD_CASES(RACE_CASE)
 #undef RACE_CASE
     return cudaErrorInvalidValue;

@@ -222,9 +222,12 @@ __device__ __forceinline__ void features16(const float *ust, int L, float beta, 
 // Chain rule back through the featuriser for 16 rows: u from the warp's stage ([16][US]),
 // dphi rows ([16][DPS], fp32).  phi is recomputed; writes
 // dz_p = beta * sum_r phi_r (dphi_r - phi . dphi) v_{r,p} * (1 - u_p^2) as bf16 to dz ([16][ZS]).
+// db (optional): adds the d(loss)/d(beta) share sum_p u_p sum_r ds_r v_{r,p} of the rows
+// t0 + row < cnt (the logits are beta (u . v_r)); stale rows past cnt add nothing.
 template <int P, int US, int DPS, int ZS>
 __device__ __forceinline__ void features_backward16(const float *ust, const float *dphi, int L, float beta,
-                                                    bf16 *dz, int lane)
+                                                    bf16 *dz, int lane, float *db = nullptr, int t0 = 0,
+                                                    int cnt = 0)
 {
     constexpr int R = 1 << P;
     for (int it = lane; it < 16 * L; it += 32) {
@@ -244,6 +247,12 @@ __device__ __forceinline__ void features_backward16(const float *ust, const floa
             const float ds = ph[r] * (dph[r] - c);
 #pragma unroll
             for (int p = 0; p < P; ++p) du[p] += ((r >> p) & 1) ? ds : -ds;
+        }
+        if (db && t0 + row < cnt) {
+            float a = *db;
+#pragma unroll
+            for (int p = 0; p < P; ++p) a = fmaf(u[p], du[p], a);
+            *db = a;
         }
 #pragma unroll
         for (int p = 0; p < P; ++p) dz[row * ZS + l * P + p] = __float2bfloat16_rn(beta * du[p] * (1.f - u[p] * u[p]));

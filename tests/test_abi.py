@@ -94,9 +94,12 @@ def test_bwd_rejects_before_launch(lib):
     p = ctypes.c_void_p(4096)
     ws = lib.race_attn_workspace_bytes(s, 3, 3, 1, 1)
     bwd = lambda *a: L.race_attn_bwd(*a)
-    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, None, p, p, p, None, p, ws, None) == -1
-    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, None, p, ws - 256, None) == -3
-    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, ctypes.c_void_p(4104), p, None, p, ws,
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, None, p, p, p, None, None, p, ws, None) == -1
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, None, None, p, ws - 256, None) == -3
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, ctypes.c_void_p(4104), p, None, None, p, ws,
+               None) == -5
+    # d(loss)/d(beta) output: float32, so 4-byte alignment is required
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, ctypes.c_void_p(4098), None, p, ws,
                None) == -5
 
 
@@ -110,7 +113,8 @@ def test_decode_rejects_before_launch(lib):
     dec = lambda *a: L.race_attn_decode(*a)
     assert dec(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, p, p, None) == -1
     assert dec(ctypes.byref(one), p, None, p, p, 10.0, 3, 3, p, p, None) == -1
-    assert dec(ctypes.byref(one), p, p, p, p, float("inf"), 3, 3, p, p, None) == -1
+    assert dec(ctypes.byref(one), p, p, p, p, float("nan"), 3, 3, p, p, None) == -1
+    assert dec(ctypes.byref(one), p, p, p, p, -1.0, 3, 3, p, p, None) == -1
     assert dec(ctypes.byref(one), p, p, p, p, 10.0, 3, 3, ctypes.c_void_p(4100), p, None) == -5
     assert dec(None, p, p, p, p, 10.0, 3, 3, p, p, None) == -1
 
@@ -126,3 +130,57 @@ def test_instrumentation_defaults(lib):
     assert lib.race_attn_launch_count() >= 0
     lib.race_attn_profile_reset()
     assert lib.race_attn_profile_read() == {}
+
+
+def test_per_head_w_layout(lib):
+    """race_shape.per_head_w selects W [H, L, P, d]: it changes no buffer size, takes only 0 or 1,
+    and the binding picks it from W's shape (checked before any call)."""
+    import torch
+    s = shape(lib)
+    ph = lib.make_shape(s.B, s.H, s.N, s.d, s.dtype, per_head_w=True)
+    assert ctypes.sizeof(type(s)) == 40
+    for causal in (0, 1):
+        for is_bwd in (0, 1):
+            assert lib.race_attn_workspace_bytes(ph, 3, 3, causal, is_bwd) == \
+                lib.race_attn_workspace_bytes(s, 3, 3, causal, is_bwd)
+    s.per_head_w = 2
+    assert lib.race_attn_workspace_bytes(s, 3, 3, 0, 1) == 0
+    Q = torch.zeros((2, 4, 8, 64), dtype=torch.bfloat16)
+    assert lib._shape_of(Q, torch.zeros((3, 2, 64)), 3, 2).per_head_w == 0
+    assert lib._shape_of(Q, torch.zeros((4, 3, 2, 64)), 3, 2).per_head_w == 1
+    for bad in ((2, 3, 2, 64), (3, 2, 32), (4, 3, 2)):
+        with pytest.raises(ValueError):
+            lib._shape_of(Q, torch.zeros(bad), 3, 2)
+    with pytest.raises(ValueError):
+        lib._shape_of(Q, torch.zeros((3, 2, 64), dtype=torch.float64), 3, 2)
+
+
+def test_beta_domain(lib):
+    """beta >= 0, finite or +inf (hard hashing); NaN and negatives are refused before any launch.
+    A short workspace makes an accepted beta stop at the workspace check instead."""
+    L = _raw(lib)
+    s = shape(lib)
+    p = ctypes.c_void_p(4096)
+    ws = lib.race_attn_workspace_bytes(s, 3, 3, 0, 0)
+    fwd = lambda b: L.race_attn_fwd(ctypes.byref(s), p, p, p, p, b, 3, 3, 0, p, None, p, ws - 256, None)
+    assert fwd(float("nan")) == -1
+    assert fwd(-0.5) == -1
+    assert fwd(float("-inf")) == -1
+    assert fwd(float("inf")) == -3
+    assert fwd(0.0) == -3
+
+
+def test_angular_rejects_before_launch(lib):
+    """race_attn_angular: gamma finite >= 0, non-null 16-byte aligned tensors, valid shape."""
+    L = _raw(lib)
+    s = shape(lib)
+    p = ctypes.c_void_p(4096)
+    ang = lambda sh, q, g, o: L.race_attn_angular(ctypes.byref(sh) if sh is not None else None, q, p, p, g, 0, o,
+                                                   None)
+    for g in (float("nan"), float("inf"), -1.0):
+        assert ang(s, p, g, p) == -1
+    assert ang(s, None, 2.0, p) == -1
+    assert ang(s, p, 2.0, None) == -1
+    assert ang(s, ctypes.c_void_p(4104), 2.0, p) == -5
+    assert ang(shape(lib, d=65), p, 2.0, p) == -1
+    assert ang(None, p, 2.0, p) == -1
