@@ -64,7 +64,9 @@ typedef enum {
     RACE_ERR_CUDA = -4,        /* a CUDA launch or runtime call failed                        */
     RACE_ERR_ALIGN = -5,       /* a tensor pointer is not 16-byte aligned                     */
     RACE_ERR_SCRATCH_LIMIT = -6, /* race_attn_fwd_noalloc: problem exceeds the built-in scratch */
-    RACE_ERR_DEVICE_TIMEOUT = -7 /* race_attn_status: a kernel stopped after a bounded wait     */
+    RACE_ERR_DEVICE_TIMEOUT = -7, /* race_attn_status: a kernel stopped after a bounded wait    */
+    RACE_ERR_NUMERIC = -8,       /* race_attn_status: an output row had a degenerate denominator */
+    RACE_ERR_NOALLOC_SETUP = -9  /* the no-alloc scratch could not be set up on this device     */
 } race_status;
 
 /* Token-tensor shape and element type, and the layout of W. */
@@ -76,7 +78,8 @@ typedef struct {
 
 /*
  * Bytes of scratch memory race_attn_fwd (is_bwd = 0) or race_attn_bwd (is_bwd = 1) needs for
- * this problem.  Returns 0 if the arguments are invalid.  Pure host function.
+ * this problem.  Returns 0 if the arguments are invalid.  Host function: it launches nothing,
+ * but it queries the current device's multiprocessor count (152 when there is no device).
  */
 size_t race_attn_workspace_bytes(const race_shape *shape, int L, int P, int causal, int is_bwd);
 
@@ -84,7 +87,9 @@ size_t race_attn_workspace_bytes(const race_shape *shape, int L, int P, int caus
  * Bytes of the optional saved-sketch buffer `state`: non-causal, the final [A | B] per (b, h)
  * as float32 [B, H, L*2^P, d+1] (columns 0..d-1 = A, column d = B); causal, the sketch at the
  * start of each of the library's sequence segments, float32 [B, H, nseg, L*2^P, d+1], where
- * nseg is a function of the shape only.  Returns 0 if the arguments are invalid.
+ * nseg is a function of the shape and of the current device's multiprocessor count (the work
+ * is split to fill the device).  Returns 0 if the arguments are invalid.  The same holds for
+ * race_attn_workspace_bytes: size buffers with the device current that will run the calls.
  */
 size_t race_attn_state_bytes(const race_shape *shape, int L, int P, int causal);
 
@@ -98,7 +103,16 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Backward pass: given the output cotangent dO, writes dQ, dK, dV (all [B, H, N, d]).
+ * Backward pass: given the output cotangent dO, writes dQ, dK, dV (all [B, H, N, d]).  The pages
+ * print no backward pass; this is the chain rule through the forward's steps ("RACE Attention"
+ * slides, frames "Soft corner assignments make hashing differentiable" (Algorithm 1), "Normalize
+ * after combining the tables" and, when causal, "Causality is a prefix update of the same
+ * statistics" (Algorithm 2)).  With den_i = phi(Q_i) . B and O_i = num_i / den_i:
+ *     dnum_i = dO_i / den_i,   dden_i = -(dO_i . O_i) / den_i,
+ *     dphi(Q_i) = [A | B] [dnum_i ; dden_i]   (the sketch query i read),
+ *     G = sum_i phi(Q_i) [dnum_i | dden_i]   (causal: the suffix sum over i >= j for key j),
+ *     dV_j = G_A^T phi(K_j),   dphi(K_j) = G_A V_j + G_B,
+ * then, for each Q and K row, the softmax, tanh, projection and normalisation Jacobians.
  * O: the forward output.  It may be NULL: the kernels recompute what they need of O
  * (dO . O per row) from the sketch, which is cheaper than reading it.
  * dbeta: NULL, or device float32 [B, H] (4-byte aligned) that receives d(loss)/d(beta) for each
@@ -129,17 +143,35 @@ int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const v
  * buffer until the process exits.  It calls no cudaMalloc, cudaFree or allocating routine.
  *  - Problems whose race_attn_workspace_bytes(shape, L, P, causal, 0) exceeds
  *    RACE_NOALLOC_SCRATCH_BYTES are rejected with RACE_ERR_SCRATCH_LIMIT before any launch.
- *  - The first call on each device looks up the device address of the buffer (with that
- *    device current); make that first call before any stream capture.
+ *  - Set-up: the driver loads the buffer onto a device when the library first looks up its
+ *    address there (under lazy module loading, the CUDA default, not when the library is
+ *    loaded).  race_attn_noalloc_init does that for the current device; call it once per device
+ *    before a caller's allocator takes the device's memory and before any stream capture.
+ *    Otherwise the first race_attn_fwd_noalloc call on the device does it, and returns
+ *    RACE_ERR_NOALLOC_SETUP if the device has no room for the buffer or if `stream` is being
+ *    captured at that moment.
  *  - All calls on a device share the one buffer and leave their data in it.  Every scratch
- *    element a call reads is written earlier in the same call, so nothing needs clearing, but
- *    two calls that overlap on the GPU (different streams, or different host threads) race
- *    on the buffer and corrupt each other's results: serialise them.
+ *    element a call reads is written earlier in the same call (its status word is cleared when
+ *    it starts), so nothing needs clearing, but two calls that overlap on the GPU (different
+ *    streams, or different host threads) race on the buffer and corrupt each other's results:
+ *    serialise them.
+ *  - Device-side errors (a bounded wait that ran out, a degenerate denominator) are recorded in
+ *    the buffer's status word; race_attn_noalloc_status reads it.
  */
 #define RACE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, const void *K, const void *V,
                           const float *W, float beta, int L, int P, int causal, void *O,
                           void *stream);
+
+/* Sets up the built-in scratch buffer of race_attn_fwd_noalloc on the current device (see
+ * there).  Returns RACE_OK (also when it is already set up), RACE_ERR_NOALLOC_SETUP when the
+ * device has no room for it, or RACE_ERR_CUDA. */
+int race_attn_noalloc_init(void);
+
+/* Device-side status of the last race_attn_fwd_noalloc call on the current device, as
+ * race_attn_status reports it for a workspace: synchronises `stream` and reads the status word
+ * of the built-in buffer.  RACE_OK when no such call has run on this device. */
+int race_attn_noalloc_status(void *stream);
 
 /*
  * One causal decode step per (batch, head): the recurrent form of paper Algorithm 2 ("RACE
@@ -171,13 +203,31 @@ int race_attn_angular(const race_shape *shape, const void *Q, const void *K, con
 
 /*
  * Device-side status of the last race_attn_fwd / race_attn_bwd call that used `workspace`.
- * Kernels that wait for asynchronous (bulk) copies bound every wait; if a wait runs out they
- * record it in the first word of the workspace and return early, leaving their outputs
- * incomplete.  This call synchronises `stream`, reads that word and returns RACE_OK or
- * RACE_ERR_DEVICE_TIMEOUT (RACE_ERR_CUDA if the stream or the copy failed).  Every fwd/bwd
- * call clears the word when it starts.
+ * The kernels record two kinds of trouble in the first word of the workspace:
+ *  - Kernels that wait for asynchronous (bulk) copies or for each other bound every wait (about
+ *    2 s, or 2^22 polls); if a wait runs out they record it and return early, leaving their
+ *    outputs incomplete: RACE_ERR_DEVICE_TIMEOUT.
+ *  - The forward records an output row whose denominator phi(Q_i) . B is zero, negative or not
+ *    finite: the row is then 0/0 or NaN, as the definition gives it (the "Long-context
+ *    architectures: Visual walkthrough", Step 6, case A: a query that meets no key mass).  At
+ *    float32 this needs every bucket a query can reach to be empty, e.g. beta so large that
+ *    sigmoid(-2 beta)^P underflows, or non-finite inputs: RACE_ERR_NUMERIC.
+ * This call synchronises `stream`, reads that word and returns RACE_OK, RACE_ERR_DEVICE_TIMEOUT
+ * (which takes precedence) or RACE_ERR_NUMERIC (RACE_ERR_CUDA if the stream or the copy
+ * failed).  Every fwd/bwd call clears the word when it starts.  race_attn_decode and
+ * race_attn_angular take no workspace and report neither.
  */
 int race_attn_status(const void *workspace, void *stream);
+
+/*
+ * Test hook for the failure path above, not for production use.  While `enable` is non-zero,
+ * the causal bfloat16 tcgen05 forward kernel (the one race_attn_fwd and race_attn_fwd_noalloc
+ * run for causal bf16 problems with d in {64, 128}, P <= 6, L * P <= 32, L * 2^P <= 64) never
+ * requests its first Q / K tiles, so every wait on them runs out: the kernel takes its abort
+ * path (drains the copies it did issue, frees its tensor memory) and returns, and the status
+ * word reports RACE_ERR_DEVICE_TIMEOUT.  Process-wide; returns RACE_OK.
+ */
+int race_attn_test_withhold_first_load(int enable);
 
 /* Static description of a status code. */
 const char *race_attn_strerror(int status);

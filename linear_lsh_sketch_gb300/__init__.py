@@ -15,7 +15,8 @@ __all__ = [
     "race_attn_state_bytes", "race_attn_strerror", "race_attn_launch_count", "race_attn_profile",
     "race_attn_profile_read", "race_attn_profile_reset", "library_path", "load_library",
     "race_attn_fwd_noalloc", "RACE_NOALLOC_SCRATCH_BYTES", "race_attn_status", "race_attn_decode",
-    "race_attn_angular",
+    "race_attn_angular", "race_attn_noalloc_init", "race_attn_noalloc_status",
+    "race_attn_test_withhold_first_load",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -23,6 +24,9 @@ library_path = os.path.join(_PKG, "librace_attn.so")
 
 RACE_F32, RACE_BF16 = 0, 1
 RACE_ERR_SCRATCH_LIMIT = -6
+RACE_ERR_DEVICE_TIMEOUT = -7
+RACE_ERR_NUMERIC = -8
+RACE_ERR_NOALLOC_SETUP = -9
 RACE_NOALLOC_SCRATCH_BYTES = 32 << 20  # size of the library's built-in scratch buffer
 _DTYPES = {torch.float32: RACE_F32, torch.bfloat16: RACE_BF16}
 
@@ -67,6 +71,12 @@ def load_library():
     L.race_attn_angular.restype = i
     L.race_attn_status.argtypes = [vp, vp]
     L.race_attn_status.restype = i
+    L.race_attn_noalloc_init.argtypes = []
+    L.race_attn_noalloc_init.restype = i
+    L.race_attn_noalloc_status.argtypes = [vp]
+    L.race_attn_noalloc_status.restype = i
+    L.race_attn_test_withhold_first_load.argtypes = [i]
+    L.race_attn_test_withhold_first_load.restype = i
     L.race_attn_strerror.argtypes = [i]
     L.race_attn_strerror.restype = ctypes.c_char_p
     L.race_attn_launch_count.argtypes = []
@@ -102,6 +112,8 @@ def _shape_of(Q, W=None, L=None, P=None):
         if W.dtype != torch.float32 or not W.is_contiguous() or tuple(W.shape) not in (shared, heads):
             raise ValueError("W must be a contiguous float32 tensor of shape [L, P, d] or [H, L, P, d]")
         per_head = tuple(W.shape) == heads and W.dim() == 4
+        if W.device != Q.device:
+            raise ValueError("W must be on the token tensors' device")
     return make_shape(B, H, N, d, Q.dtype, per_head)
 
 
@@ -138,9 +150,34 @@ def race_attn_strerror(status):
 
 
 def race_attn_status(workspace, stream=None):
-    """Synchronise and read the device status word of `workspace` (0 = ok, -7 = a bounded wait
-    ran out); see race_attn_status in include/race_attn.h."""
-    return load_library().race_attn_status(_ptr(workspace), _stream(stream))
+    """Synchronise and read the device status word of `workspace`: 0 = ok, -7 = a bounded wait
+    ran out, -8 = an output row had a zero or non-finite denominator (see race_attn_status in
+    include/race_attn.h)."""
+    with torch.cuda.device(workspace.device):
+        return load_library().race_attn_status(_ptr(workspace), _stream(stream))
+
+
+def race_attn_noalloc_init(device=None):
+    """Set up the built-in scratch buffer of race_attn_fwd_noalloc on `device` (default: the
+    current one); do it before an allocator takes the device's memory and before any capture."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        rc = load_library().race_attn_noalloc_init()
+    if rc != 0:
+        raise RaceAttnError(rc, "race_attn_noalloc_init")
+
+
+def race_attn_noalloc_status(device=None, stream=None):
+    """Synchronise and read the device status word of the last race_attn_fwd_noalloc call on
+    `device` (codes as race_attn_status)."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return load_library().race_attn_noalloc_status(_stream(stream))
+
+
+def race_attn_test_withhold_first_load(enable):
+    """Test hook of the failure path (see include/race_attn.h): while enabled, the causal bf16
+    tcgen05 forward never requests its first tiles, its waits run out and the status word reports
+    a timeout."""
+    return load_library().race_attn_test_withhold_first_load(int(bool(enable)))
 
 
 def race_attn_launch_count():
@@ -181,24 +218,25 @@ def race_attn_fwd(Q, K, V, W, beta, L, P, causal, O=None, state=None, workspace=
 
     O, state and workspace are allocated with torch when not given.  Returns O.
     """
-    shape = _shape_of(Q, W, L, P)
-    _check_like("K", K, Q)
-    _check_like("V", V, Q)
-    _check_like("Q", Q, Q)
-    if O is None:
-        O = torch.empty_like(Q)
-    _check_like("O", O, Q)
-    ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 0)
-    if ws_bytes == 0:
-        raise RaceAttnError(-1, "race_attn_fwd")
-    workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
-    rc = load_library().race_attn_fwd(
-        ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
-        int(causal), _ptr(O), _ptr(state), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream))
-    if rc != 0:
-        raise RaceAttnError(rc, "race_attn_fwd")
-    return O
+    with torch.cuda.device(Q.device):
+        shape = _shape_of(Q, W, L, P)
+        _check_like("K", K, Q)
+        _check_like("V", V, Q)
+        _check_like("Q", Q, Q)
+        if O is None:
+            O = torch.empty_like(Q)
+        _check_like("O", O, Q)
+        ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 0)
+        if ws_bytes == 0:
+            raise RaceAttnError(-1, "race_attn_fwd")
+        workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
+        rc = load_library().race_attn_fwd(
+            ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
+            int(causal), _ptr(O), _ptr(state), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream))
+        if rc != 0:
+            raise RaceAttnError(rc, "race_attn_fwd")
+        return O
 
 
 def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, dV=None, state=None,
@@ -206,63 +244,66 @@ def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, 
     """(dQ, dK, dV) of RACE attention for the output cotangent dO; allocates what is not given.
     With want_dbeta (or a float32 [B, H] `dbeta` given) also d(loss)/d(beta) per (b, h), returned
     as a fourth element; the shared beta's gradient is its sum."""
-    shape = _shape_of(Q, W, L, P)
-    for n, t in (("K", K), ("V", V), ("dO", dO), ("Q", Q)):
-        _check_like(n, t, Q)
-    dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty_like(Q) if dK is None else dK
-    dV = torch.empty_like(Q) if dV is None else dV
-    for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
-        _check_like(n, t, Q)
-    if dbeta is None and want_dbeta:
-        dbeta = torch.empty((Q.shape[0], Q.shape[1]), dtype=torch.float32, device=Q.device)
-    if dbeta is not None and (dbeta.dtype != torch.float32 or tuple(dbeta.shape) != tuple(Q.shape[:2])
-                              or not dbeta.is_contiguous() or dbeta.device != Q.device):
-        raise ValueError("dbeta must be a contiguous float32 tensor of shape [B, H] on Q's device")
-    ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 1)
-    if ws_bytes == 0:
-        raise RaceAttnError(-1, "race_attn_bwd")
-    workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
-    rc = load_library().race_attn_bwd(
-        ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
-        int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dbeta), _ptr(state),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
-    if rc != 0:
-        raise RaceAttnError(rc, "race_attn_bwd")
-    return (dQ, dK, dV) if dbeta is None else (dQ, dK, dV, dbeta)
+    with torch.cuda.device(Q.device):
+        shape = _shape_of(Q, W, L, P)
+        for n, t in (("K", K), ("V", V), ("dO", dO), ("Q", Q)):
+            _check_like(n, t, Q)
+        dQ = torch.empty_like(Q) if dQ is None else dQ
+        dK = torch.empty_like(Q) if dK is None else dK
+        dV = torch.empty_like(Q) if dV is None else dV
+        for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+            _check_like(n, t, Q)
+        if dbeta is None and want_dbeta:
+            dbeta = torch.empty((Q.shape[0], Q.shape[1]), dtype=torch.float32, device=Q.device)
+        if dbeta is not None and (dbeta.dtype != torch.float32 or tuple(dbeta.shape) != tuple(Q.shape[:2])
+                                  or not dbeta.is_contiguous() or dbeta.device != Q.device):
+            raise ValueError("dbeta must be a contiguous float32 tensor of shape [B, H] on Q's device")
+        ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 1)
+        if ws_bytes == 0:
+            raise RaceAttnError(-1, "race_attn_bwd")
+        workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
+        rc = load_library().race_attn_bwd(
+            ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
+            int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dbeta), _ptr(state),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+        if rc != 0:
+            raise RaceAttnError(rc, "race_attn_bwd")
+        return (dQ, dK, dV) if dbeta is None else (dQ, dK, dV, dbeta)
 
 
 def race_attn_decode(q, k, v, W, beta, L, P, state, o=None, stream=None):
     """One causal decode step: q, k, v [B, H, 1, d] (float32 or bfloat16, CUDA); state float32
     [B, H, L * 2^P, d + 1] (updated in place).  Returns o [B, H, 1, d]."""
-    shape = _shape_of(q, W, L, P)
-    for n, t in (("k", k), ("v", v), ("q", q)):
-        _check_like(n, t, q)
-    want = (q.shape[0], q.shape[1], L << P, q.shape[3] + 1)
-    if state.dtype != torch.float32 or tuple(state.shape) != want or not state.is_contiguous():
-        raise ValueError("state must be a contiguous float32 tensor of shape %s" % (want,))
-    o = torch.empty_like(q) if o is None else o
-    _check_like("o", o, q)
-    rc = load_library().race_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(W), float(beta),
-                                         int(L), int(P), _ptr(state), _ptr(o), _stream(stream))
-    if rc != 0:
-        raise RaceAttnError(rc, "race_attn_decode")
-    return o
+    with torch.cuda.device(q.device):
+        shape = _shape_of(q, W, L, P)
+        for n, t in (("k", k), ("v", v), ("q", q)):
+            _check_like(n, t, q)
+        want = (q.shape[0], q.shape[1], L << P, q.shape[3] + 1)
+        if state.dtype != torch.float32 or tuple(state.shape) != want or not state.is_contiguous():
+            raise ValueError("state must be a contiguous float32 tensor of shape %s" % (want,))
+        o = torch.empty_like(q) if o is None else o
+        _check_like("o", o, q)
+        rc = load_library().race_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(W), float(beta),
+                                             int(L), int(P), _ptr(state), _ptr(o), _stream(stream))
+        if rc != 0:
+            raise RaceAttnError(rc, "race_attn_decode")
+        return o
 
 
 def race_attn_angular(Q, K, V, gamma, causal, O=None, stream=None):
     """Exact angular attention O_i = sum_j S_ij V_j / sum_j S_ij, S_ij = (1 - angle_ij / pi)^gamma
     (j <= i when causal), O(N^2): the reference RACE attention approximates.  Returns O."""
-    shape = _shape_of(Q)
-    for n, t in (("K", K), ("V", V), ("Q", Q)):
-        _check_like(n, t, Q)
-    O = torch.empty_like(Q) if O is None else O
-    _check_like("O", O, Q)
-    rc = load_library().race_attn_angular(ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), float(gamma),
-                                          int(bool(causal)), _ptr(O), _stream(stream))
-    if rc != 0:
-        raise RaceAttnError(rc, "race_attn_angular")
-    return O
+    with torch.cuda.device(Q.device):
+        shape = _shape_of(Q)
+        for n, t in (("K", K), ("V", V), ("Q", Q)):
+            _check_like(n, t, Q)
+        O = torch.empty_like(Q) if O is None else O
+        _check_like("O", O, Q)
+        rc = load_library().race_attn_angular(ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), float(gamma),
+                                              int(bool(causal)), _ptr(O), _stream(stream))
+        if rc != 0:
+            raise RaceAttnError(rc, "race_attn_angular")
+        return O
 
 
 def race_attn_fwd_noalloc(Q, K, V, W, beta, L, P, causal, O=None, stream=None):
@@ -273,16 +314,17 @@ def race_attn_fwd_noalloc(Q, K, V, W, beta, L, P, causal, O=None, stream=None):
     that buffer and must be serialised by the caller.  Only O is allocated here, and only when
     it is not given.  Returns O.
     """
-    shape = _shape_of(Q, W, L, P)
-    _check_like("K", K, Q)
-    _check_like("V", V, Q)
-    _check_like("Q", Q, Q)
-    if O is None:
-        O = torch.empty_like(Q)
-    _check_like("O", O, Q)
-    rc = load_library().race_attn_fwd_noalloc(
-        ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P), int(causal),
-        _ptr(O), _stream(stream))
-    if rc != 0:
-        raise RaceAttnError(rc, "race_attn_fwd_noalloc")
-    return O
+    with torch.cuda.device(Q.device):
+        shape = _shape_of(Q, W, L, P)
+        _check_like("K", K, Q)
+        _check_like("V", V, Q)
+        _check_like("Q", Q, Q)
+        if O is None:
+            O = torch.empty_like(Q)
+        _check_like("O", O, Q)
+        rc = load_library().race_attn_fwd_noalloc(
+            ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P), int(causal),
+            _ptr(O), _stream(stream))
+        if rc != 0:
+            raise RaceAttnError(rc, "race_attn_fwd_noalloc")
+        return O

@@ -90,9 +90,33 @@ void prof_after(const char *name, cudaStream_t st)
 // ------------------------------------------------------------------ planning
 
 namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {};  // per device, filled on first use
+}  // namespace
 
-constexpr int kSMs = 152;
+int device_sm_count()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 152;
+    }
+    int *cache = g_sm_count;
+    if (cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = 152;
+    }
+    cache[dev] = n;
+    return n;
+}
+
+namespace {
+
 constexpr size_t kMaxSmem = 227 * 1024;
+
+int g_withhold = 0;  // failure-path test hook (race_attn_test_withhold_first_load)
 
 struct Plan {
     Dims D{};
@@ -137,6 +161,8 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     D.beta = 0.f;
     D.H = s->H;
     D.w_per_head = s->per_head_w;
+    D.sms = device_sm_count();
+    D.withhold = 0;
     pl.causal = causal != 0;
     pl.bf16 = s->dtype == RACE_BF16;
     pl.E = (size_t)D.LR * D.dv;
@@ -148,12 +174,12 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     const int64_t ntiles = ceil_div(D.N, TT);
     int64_t want;
     if (pl.nc5) {
-        want = ceil_div((int64_t)kSMs * nc5_sketch_ctas_per_sm(D), D.BH);
+        want = ceil_div((int64_t)D.sms * nc5_sketch_ctas_per_sm(D), D.BH);
     } else if (!pl.causal) {
         const int64_t chunks = ceil_div(D.LR, 64);
-        want = ceil_div(4 * kSMs, chunks * D.BH);
+        want = ceil_div(4 * (int64_t)D.sms, chunks * D.BH);
     } else {
-        want = ceil_div(2 * kSMs, D.BH);
+        want = ceil_div(2 * (int64_t)D.sms, D.BH);
     }
     want = std::max<int64_t>(1, std::min(want, ntiles));
     pl.seg_len = ceil_div(ceil_div(D.N, want), TT) * TT;
@@ -191,6 +217,15 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+// The status a device status word reports: a timed-out wait first (its outputs are incomplete),
+// then a degenerate denominator.
+int status_of(unsigned bits)
+{
+    if (bits & kErrTimeout) return RACE_ERR_DEVICE_TIMEOUT;
+    if (bits & kErrNumeric) return RACE_ERR_NUMERIC;
+    return RACE_OK;
+}
 
 // beta: finite and >= 0, or +infinity for hard hashing.
 int check_beta(float beta) { return (!std::isnan(beta) && beta >= 0.f) ? RACE_OK : RACE_ERR_INVALID_ARG; }
@@ -253,10 +288,10 @@ int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float
     RACE_TRY(launch_sketch<T>(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, 0, st));
     if (!pl.causal) {
         RACE_TRY(launch_combine(D, part, S, pl.nsplit, 0, st));
-        RACE_TRY(launch_readout<T>(D, Q, W, S, O, st));
+        RACE_TRY(launch_readout<T>(D, Q, W, S, O, err, st));
     } else {
         RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
-        RACE_TRY(launch_causal_fwd<T>(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, st));
+        RACE_TRY(launch_causal_fwd<T>(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, err, st));
     }
     return RACE_OK;
 }
@@ -402,6 +437,7 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
         return RACE_ERR_ALIGN;
     if (workspace_bytes < pl.ws_fwd) return RACE_ERR_WORKSPACE;
     pl.D.beta = kernel_beta(beta);
+    pl.D.withhold = g_withhold;
     cudaStream_t st = (cudaStream_t)stream;
     if (pl.bf16)
         return forward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
@@ -456,6 +492,10 @@ const char *race_attn_strerror(int status)
         case RACE_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
         case RACE_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in no-alloc buffer";
         case RACE_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting for an asynchronous copy";
+        case RACE_ERR_NUMERIC: return "an output row has a zero, negative or non-finite denominator";
+        case RACE_ERR_NOALLOC_SETUP:
+            return "the built-in no-alloc scratch could not be set up on this device (out of memory, or first use "
+                   "inside a stream capture: call race_attn_noalloc_init first)";
         default: return "unknown status";
     }
 }
@@ -508,7 +548,13 @@ int race_attn_status(const void *workspace, void *stream)
     unsigned bits = 0;
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return RACE_ERR_CUDA;
     if (cudaMemcpy(&bits, workspace, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess) return RACE_ERR_CUDA;
-    return bits ? RACE_ERR_DEVICE_TIMEOUT : RACE_OK;
+    return status_of(bits);
+}
+
+int race_attn_test_withhold_first_load(int enable)
+{
+    g_withhold = enable != 0;
+    return RACE_OK;
 }
 
 uint64_t race_attn_launch_count(void) { return g_launches; }
@@ -548,27 +594,62 @@ void race_attn_profile_reset(void)
 namespace race {
 namespace {
 
-constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[RACE_NOALLOC_SCRATCH_BYTES];
 std::mutex g_noalloc_mutex;
 void *g_noalloc_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (nullptr on failure).
-void *noalloc_scratch()
+// Device address of the scratch array on the current device, looked up on first use (which,
+// under lazy module loading, is when the driver loads the array).  `st`: the caller's stream,
+// checked for an ongoing capture before a first use when check_capture is set.
+int noalloc_scratch(cudaStream_t st, bool check_capture, void **out)
 {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return RACE_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     if (!g_noalloc_ptr[dev]) {
+        if (check_capture) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+                cudaGetLastError();
+                return RACE_ERR_NOALLOC_SETUP;
+            }
+        }
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return e == cudaErrorMemoryAllocation ? RACE_ERR_NOALLOC_SETUP : RACE_ERR_CUDA;
+        }
         g_noalloc_ptr[dev] = p;
     }
-    return g_noalloc_ptr[dev];
+    *out = g_noalloc_ptr[dev];
+    return RACE_OK;
 }
 
 }  // namespace
 }  // namespace race
+
+extern "C" int race_attn_noalloc_init(void)
+{
+    void *p = nullptr;
+    return noalloc_scratch(nullptr, false, &p);
+}
+
+extern "C" int race_attn_noalloc_status(void *stream)
+{
+    void *p = nullptr;
+    {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RACE_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        p = g_noalloc_ptr[dev];
+    }
+    if (!p) return RACE_OK;  // no allocation-free call has run on this device
+    return race_attn_status(p, stream);
+}
 
 extern "C" int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, const void *K, const void *V,
                                      const float *W, float beta, int L, int P, int causal, void *O, void *stream)
@@ -580,10 +661,11 @@ extern "C" int race_attn_fwd_noalloc(const race_shape *shape, const void *Q, con
     if (!Q || !K || !V || !W || !O) return RACE_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(W) || !aligned16(O)) return RACE_ERR_ALIGN;
     if (pl.ws_fwd > RACE_NOALLOC_SCRATCH_BYTES) return RACE_ERR_SCRATCH_LIMIT;
-    void *scratch = noalloc_scratch();
-    if (!scratch) return RACE_ERR_CUDA;
-    pl.D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
+    void *scratch = nullptr;
+    if ((rc = noalloc_scratch(st, true, &scratch)) != RACE_OK) return rc;
+    pl.D.beta = kernel_beta(beta);
+    pl.D.withhold = g_withhold;
     // state == nullptr: the forward keeps its sketch inside the scratch buffer
     if (pl.bf16)
         return forward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,

@@ -236,9 +236,13 @@ __global__ void __launch_bounds__(NTHW, 1)
             // loads issued and completions waited for, per barrier (to drain after an abort)
             int qk_issued = 0, qk_done = 0, v_issued[2] = {0, 0}, v_done[2] = {0, 0};
             if (nchunk > 0) {
-                load_qk(0);
+                // withhold (a test of the failure path): the first Q / K tiles are never requested,
+                // so every wait on them runs out and the CTA takes the abort path below
+                if (!Dm.withhold) {
+                    load_qk(0);
+                    ++qk_issued;
+                }
                 load_v(0);
-                ++qk_issued;
                 ++v_issued[0];
                 if (nchunk > 1) {
                     load_v(1);
@@ -360,7 +364,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                 wait_ld();
                 reg_fence(v);
                 reg_fence1(dn);
-                if (pass == 0) rd = __frcp_rn(uf(dn));
+                if (pass == 0) {
+                    rd = __frcp_rn(uf(dn));
+                    if (h == 0 && t < (int)min((int64_t)C, n_end - n_begin - (int64_t)c * C)) flag_den(uf(dn), err);
+                }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {  // 8-column chunks of this pass
                     const int ch = h * (D / 16) + 4 * pass + j;

@@ -23,7 +23,20 @@ struct Dims {
     float beta;
     int64_t H;       // heads (problem bh is head bh % H)
     int w_per_head;  // 0: one W [L, P, d] for every head; 1: W is [H, L, P, d]
+    int sms;         // streaming multiprocessors of the device the work is planned for
+    int withhold;    // failure-path test hook: the causal tcgen05 forward skips its first tile load
 };
+
+// Bits of the device status word (the first word of a workspace): a bounded wait ran out, or a
+// read-out met a denominator that is zero, negative or not finite (its output row is 0/0).
+constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrNumeric = 2u;
+
+// Records a degenerate denominator of one output row in the status word (err may be null).
+__device__ __forceinline__ void flag_den(float den, unsigned *err)
+{
+    if (err != nullptr && !(den > 0.f && den <= 3.402823466e38f)) atomicOr(err, kErrNumeric);
+}
 
 // The hyperplanes problem bh hashes with: the shared W, or its head's slice of a per-head W.
 __host__ __device__ inline const float *head_w(const float *W, const Dims &D, int64_t bh)

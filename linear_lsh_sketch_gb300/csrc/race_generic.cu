@@ -422,7 +422,8 @@ __global__ void __launch_bounds__(256) k_dbeta_combine(const float *__restrict__
 template <typename T>
 __global__ void __launch_bounds__(NT) k_readout(Dims D, const T *__restrict__ Q,
                                                 const float *__restrict__ W,
-                                                const float *__restrict__ S, T *__restrict__ O)
+                                                const float *__restrict__ S, T *__restrict__ O,
+                                                unsigned *__restrict__ err)
 {
     extern __shared__ float sm[];
     const ReadoutSmem L(D);
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(NT) k_readout(Dims D, const T *__restrict__ Q,
     T *Ob = O + bh * D.N * D.d;
     for (int i = threadIdx.x; i < cnt * D.d; i += NT) {
         const int t = i / D.d, c = i - t * D.d;
+        if (c == 0) flag_den(outs[t * D.dv + D.d], err);
         st_f(Ob, (n0 + t) * D.d + c, outs[t * D.dv + c] / outs[t * D.dv + D.d]);
     }
 }
@@ -609,7 +611,7 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(Dims D, const T *__restrict__
                                                    const T *__restrict__ V,
                                                    const float *__restrict__ W,
                                                    const float *__restrict__ S0, int64_t seg_len,
-                                                   int nseg, T *__restrict__ O)
+                                                   int nseg, T *__restrict__ O, unsigned *__restrict__ err)
 {
     extern __shared__ float sm[];
     const CausalFwdSmem L(D);
@@ -650,6 +652,7 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(Dims D, const T *__restrict__
         __syncthreads();
         for (int i = threadIdx.x; i < cnt * D.d; i += NT) {
             const int t = i / D.d, c = i - t * D.d;
+            if (c == 0) flag_den(outs[t * dv + D.d], err);
             st_f(O + off, (n0 + t) * D.d + c, outs[t * dv + c] / outs[t * dv + D.d]);
         }
         for (int o = threadIdx.x; o < E; o += NT) {
@@ -918,13 +921,14 @@ cudaError_t launch_dbeta_combine(const Dims &D, const float *part, int slots, fl
 }
 
 template <typename T>
-cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const float *S, T *O, cudaStream_t st)
+cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const float *S, T *O, unsigned *err,
+                           cudaStream_t st)
 {
     const size_t smem = generic_smem_bytes(D, GenericKernel::Readout);
     cudaError_t e = prep(gen::k_readout<T>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((D.N + gen::TT - 1) / gen::TT), (unsigned)D.BH);
-    return launch_kernel("readout", gen::k_readout<T>, grid, dim3(gen::NT), smem, st, D, Q, W, S, O);
+    return launch_kernel("readout", gen::k_readout<T>, grid, dim3(gen::NT), smem, st, D, Q, W, S, O, err);
 }
 
 template <typename T>
@@ -953,14 +957,14 @@ cudaError_t launch_bwd_key(const Dims &D, const T *K, const T *V, const float *W
 
 template <typename T>
 cudaError_t launch_causal_fwd(const Dims &D, const T *Q, const T *K, const T *V, const float *W, const float *S0,
-                              int64_t seg_len, int nseg, T *O, cudaStream_t st)
+                              int64_t seg_len, int nseg, T *O, unsigned *err, cudaStream_t st)
 {
     const size_t smem = generic_smem_bytes(D, GenericKernel::CausalFwd);
     cudaError_t e = prep(gen::k_causal_fwd<T>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(nseg, (unsigned)D.BH);
     return launch_kernel("causal_fwd", gen::k_causal_fwd<T>, grid, dim3(gen::NT), smem, st, D, Q, K, V, W, S0,
-                         seg_len, nseg, O);
+                         seg_len, nseg, O, err);
 }
 
 template <typename T>
@@ -993,13 +997,13 @@ cudaError_t launch_causal_bwd_kv(const Dims &D, const T *Q, const T *K, const T 
     template cudaError_t launch_sketch<T>(const Dims &, const T *, const T *, const float2 *, const float *,   \
                                           int64_t, int, float *, int, cudaStream_t);                           \
     template cudaError_t launch_readout<T>(const Dims &, const T *, const float *, const float *, T *,         \
-                                           cudaStream_t);                                                      \
+                                           unsigned *, cudaStream_t);                                          \
     template cudaError_t launch_bwd_query<T>(const Dims &, const T *, const T *, const float *, const float *, \
                                              T *, float2 *, float *, cudaStream_t);                            \
     template cudaError_t launch_bwd_key<T>(const Dims &, const T *, const T *, const float *, const float *,   \
                                            T *, T *, float *, cudaStream_t);                                   \
     template cudaError_t launch_causal_fwd<T>(const Dims &, const T *, const T *, const T *, const float *,    \
-                                              const float *, int64_t, int, T *, cudaStream_t);                 \
+                                              const float *, int64_t, int, T *, unsigned *, cudaStream_t);     \
     template cudaError_t launch_causal_bwd_q<T>(const Dims &, const T *, const T *, const T *, const T *,      \
                                                 const float *, const float *, int64_t, int, T *, float2 *,     \
                                                 float *, cudaStream_t);                                        \

@@ -23,6 +23,9 @@ cudaError_t launch_kernel(const char *name, Kern k, dim3 grid, dim3 block, size_
     return e;
 }
 
+// Streaming multiprocessors of the current device (152 when no device can be queried).
+int device_sm_count();
+
 // ---------------------------------------------------------------- causal decode step
 bool decode_supported(const Dims &D);
 template <typename T>
@@ -46,7 +49,8 @@ cudaError_t launch_combine(const Dims &D, const float *part, float *out, int nsp
 // dbeta[bh] from the backward kernels' d(loss)/d(beta) partials, two [BH][slots] float arrays.
 cudaError_t launch_dbeta_combine(const Dims &D, const float *part, int slots, float *dbeta, cudaStream_t st);
 template <typename T>
-cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const float *S, T *O, cudaStream_t st);
+cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const float *S, T *O, unsigned *err,
+                           cudaStream_t st);
 template <typename T>
 cudaError_t launch_bwd_query(const Dims &D, const T *Q, const T *dO, const float *W, const float *S, T *dQ,
                              float2 *aux, float *dbpart, cudaStream_t st);
@@ -55,7 +59,7 @@ cudaError_t launch_bwd_key(const Dims &D, const T *K, const T *V, const float *W
                            float *dbpart, cudaStream_t st);
 template <typename T>
 cudaError_t launch_causal_fwd(const Dims &D, const T *Q, const T *K, const T *V, const float *W, const float *S0,
-                              int64_t seg_len, int nseg, T *O, cudaStream_t st);
+                              int64_t seg_len, int nseg, T *O, unsigned *err, cudaStream_t st);
 template <typename T>
 cudaError_t launch_causal_bwd_q(const Dims &D, const T *Q, const T *K, const T *V, const T *dO, const float *W,
                                 const float *S0, int64_t seg_len, int nseg, T *dQ, float2 *aux, float *dbpart,

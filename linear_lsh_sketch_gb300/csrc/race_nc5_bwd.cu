@@ -644,12 +644,12 @@ cudaError_t prep_bwd(K kern, size_t bytes)
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-// Persistent split of the token tiles: about (152 x CTAs per SM) CTAs over all (b, h).
+// Persistent split of the token tiles: about (SMs x CTAs per SM) CTAs over all (b, h).
 int64_t bwd_seg(const Dims &Dm, size_t smem)
 {
     const int per_sm = std::max<int>(1, std::min<int>(2, (int)(kSmemMax / smem)));
     const int64_t ntiles = (Dm.N + nc5::C - 1) / nc5::C;
-    int64_t want = std::max<int64_t>(1, (152 * per_sm + Dm.BH - 1) / Dm.BH);
+    int64_t want = std::max<int64_t>(1, ((int64_t)Dm.sms * per_sm + Dm.BH - 1) / Dm.BH);
     want = std::min(want, ntiles);
     return ((ntiles + want - 1) / want) * nc5::C;
 }

@@ -22,7 +22,6 @@ constexpr int NTH = 256;         // threads per CTA
 constexpr uint32_t BLK = C * 128;  // bytes of one SW128 column block of a token tile
 constexpr int LPP = 32;          // projection columns (L * P <= 32): z occupies 32 TMEM columns
 constexpr uint32_t WBLK = LPP * 128;  // bytes of one SW128 column block of a hyperplane tile
-constexpr unsigned kErrTimeout = 1u;
 
 // Hyperplanes as bf16 hi and lo SW128 tiles [D / 64][LPP rows][64]: row p = W row p (p < L P),
 // zero rows after; hi + lo == W to about 2^-16 relative.
@@ -96,43 +95,41 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 }
 
 // Bounded wait for the phase with parity `parity` that also gives up as soon as another thread
-// of the CTA has raised `*abort`.  A wait that runs out raises `*abort` itself.  Returns true
-// when the phase completed.
+// of the CTA has raised `*abort`.  A wait that runs out (tc::kWaitLimitNs or 2^22 polls) raises
+// `*abort` itself.  Returns true when the phase completed.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort)
 {
-    for (int i = 0; i < (1 << 22); ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if ((i & 15) == 15 && *abort) return false;
+    if (tc::mbar_try(bar, parity)) return true;
+    const uint64_t t0 = tc::globaltimer_ns();
+    for (int i = 1; i < (1 << 22); ++i) {
+        if (tc::mbar_try(bar, parity)) return true;
+        if ((i & 15) == 0) {
+            if (*abort) return false;
+            if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) break;
+        }
+    }
+    *abort = 1;
+    return false;
+}
+
+// wait_phase for a converged warp: every lane polls and all lanes return the same result, so the
+// warp stays converged for the elect.sync issue that follows.
+__device__ __forceinline__ bool wait_phase_w(uint32_t bar, uint32_t parity, volatile int *abort)
+{
+    if (__all_sync(0xffffffffu, tc::mbar_try(bar, parity))) return true;
+    const uint64_t t0 = tc::globaltimer_ns();
+    for (int i = 1; i < (1 << 22); ++i) {
+        if (__all_sync(0xffffffffu, tc::mbar_try(bar, parity))) return true;
+        if ((i & 15) == 0) {
+            if (__any_sync(0xffffffffu, *abort != 0)) return false;
+            if (__any_sync(0xffffffffu, tc::globaltimer_ns() - t0 > tc::kWaitLimitNs)) break;
+        }
     }
     *abort = 1;
     return false;
 }
 
 // Non-blocking check of the phase with parity `parity`.
-// wait_phase for a converged warp: every lane polls and all lanes return the same result, so the
-// warp stays converged for the elect.sync issue that follows.
-__device__ __forceinline__ bool wait_phase_w(uint32_t bar, uint32_t parity, volatile int *abort)
-{
-    for (int i = 0; i < (1 << 22); ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (__all_sync(0xffffffffu, ok != 0)) return true;
-        if ((i & 15) == 15 && __any_sync(0xffffffffu, *abort != 0)) return false;
-    }
-    *abort = 1;
-    return false;
-}
-
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;

@@ -453,6 +453,7 @@ __global__ void __launch_bounds__(NTH, 1)
             float v[16];
             ld16(tlane + D, v);
             const float rd = __frcp_rn(v[0]);
+            if (h == 0 && t < cnt) flag_den(v[0], err);
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 const int c0 = h * (D / 2) + 16 * cc;
@@ -597,7 +598,7 @@ cudaError_t readout_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensor
     if (e != cudaSuccess) return e;
     const int per_sm = std::max<int>(1, std::min<int>(2, (int)((227 * 1024) / smem)));
     const int64_t ntiles = (Dm.N + nc5::C - 1) / nc5::C;
-    int64_t want = std::max<int64_t>(1, (152 * per_sm + Dm.BH - 1) / Dm.BH);
+    int64_t want = std::max<int64_t>(1, ((int64_t)Dm.sms * per_sm + Dm.BH - 1) / Dm.BH);
     want = std::min(want, ntiles);
     const int64_t seg = ((ntiles + want - 1) / want) * nc5::C;
     const int64_t nseg = (Dm.N + seg - 1) / seg;

@@ -52,18 +52,40 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
-// Waits for the mbarrier phase with parity `phase`; gives up after a bounded number of polls
-// (each poll may suspend the thread briefly) and returns false.
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Every wait on an asynchronous copy or a peer warp gives up after this many nanoseconds (or
+// 2^22 polls, whichever comes first): a healthy wait ends within microseconds, and a stalled one
+// must end the kernel rather than hold the GPU.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// One poll of the mbarrier phase with parity `phase` (may suspend the thread briefly).
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t phase)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the mbarrier phase with parity `phase`; gives up after the bounds above and returns
+// false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase)
 {
-    for (int i = 0; i < (1 << 22); ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(phase)
-            : "memory");
-        if (ok) return true;
+    if (mbar_try(bar, phase)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (int i = 1; i < (1 << 22); ++i) {
+        if (mbar_try(bar, phase)) return true;
+        if ((i & 15) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
     }
     return false;
 }

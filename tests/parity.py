@@ -16,9 +16,10 @@ from linear_lsh_sketch_gb300.workloads import as_oracle_array, make_inputs
 TOL = {"f32": (1e-5, 1e-5), "bf16": (2e-2, 5e-2)}
 
 
-def gpu_run(w, inp, with_state=True, rows=None, heads=None):
+def gpu_run(w, inp, with_state=True, rows=None, heads=None, keep_on_device=False):
     """Forward then backward through the C ABI; returns float64 host copies (O, dQ, dK, dV),
-    optionally only token `rows` of the first `heads` heads."""
+    optionally only token `rows` of the first `heads` heads, or, with keep_on_device, the four
+    device tensors themselves."""
     dev = inp["Q"].device
     state = None
     if with_state:
@@ -29,6 +30,8 @@ def gpu_run(w, inp, with_state=True, rows=None, heads=None):
     dQ, dK, dV = race.race_attn_bwd(inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal,
                                     inp["dO"], O=O, state=state)
     torch.cuda.synchronize()
+    if keep_on_device:
+        return O, dQ, dK, dV
     out = []
     for t in (O, dQ, dK, dV):
         if heads is not None:

@@ -121,7 +121,7 @@ def test_decode_rejects_before_launch(lib):
 
 def test_strerror(lib):
     assert lib.race_attn_strerror(0) == "ok"
-    for rc in (-1, -2, -3, -4, -5):
+    for rc in (-1, -2, -3, -4, -5, -6, -7, -8, -9):
         assert lib.race_attn_strerror(rc) not in ("ok", "unknown status")
     assert lib.race_attn_strerror(-99) == "unknown status"
 

@@ -6,7 +6,6 @@ kernels on the library's built-in static scratch buffer instead of a caller work
 file is named to be collected last, so a run that stops at the first failure has run every
 other test before it.
 """
-import numpy as np
 import pytest
 import torch
 
@@ -33,13 +32,26 @@ def _err(a, b):
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_noalloc_matches_regular_forward_on_two_calls(w):
+    """Two calls in a row (the second sees what the first left in the shared scratch) match the
+    regular forward, report a clean status, and allocate nothing: torch's allocator and the
+    device's free memory are unchanged across the second call, whose output buffer is given."""
+    race.race_attn_noalloc_init()
     inp = {k: v.cuda() for k, v in make_inputs(w, seed=7, device="cpu").items()}
     ref = race.race_attn_fwd(inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal)
     torch.cuda.synchronize()
     assert torch.isfinite(ref.float()).all()
-    for _ in range(2):  # the second call sees the scratch contents the first call left behind
-        O = race.race_attn_fwd_noalloc(inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal)
+    O = torch.empty_like(ref)
+    for call in range(2):
+        if call == 1:
+            torch.cuda.synchronize()
+            allocs = torch.cuda.memory_stats()["allocation.all.allocated"]
+            free = torch.cuda.mem_get_info()[0]
+        race.race_attn_fwd_noalloc(inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal, O=O)
         torch.cuda.synchronize()
+        if call == 1:
+            assert torch.cuda.memory_stats()["allocation.all.allocated"] == allocs
+            assert torch.cuda.mem_get_info()[0] == free
+        assert race.race_attn_noalloc_status() == 0
         assert _err(O, ref) <= TOL[w.dtype]
 
 
