@@ -55,6 +55,24 @@ KERNEL_BYTES = {
 }
 
 
+# Each kernel's share of the step's algorithmic bytes (12 d e per (token, head): the forward
+# reads Q, K, V and writes O; the backward reads Q, K, V, O, dO and writes dQ, dK, dV), in
+# multiples of d * elem_bytes: the token tensors of that list it is the one to read or write.
+# Re-reads (the causal segment sums' K and V, the key side's Q and dO) are not algorithmic.
+KERNEL_ALG_SHARE = {
+    "sketch_keys": 2, "readout": 2, "bwd_query": 3, "sketch_grad": 0, "bwd_key": 4,
+    "causal_fwd": 4, "causal_bwd_q": 3, "causal_bwd_kv": 4,
+    "tc_causal_totals": 0, "tc_causal_fwd": 4, "tc_causal_bwd_q": 3, "tc_causal_bwd_kv": 4,
+    "tc5_sketch_keys": 2, "tc5_readout": 2, "tc5_bwd_query": 3, "tc5_sketch_grad": 0, "tc5_bwd_key": 4,
+    "tc5_causal_fwd": 4, "tc5_causal_bwd_q": 3, "tc5_causal_bwd_kv": 4,
+}
+# The causal path's segment-sum pass reads K and V but owns none of the algorithmic bytes.
+CAUSAL_SEGMENT_SUMS = {"sketch_keys", "tc5_sketch_keys"}
+
+# Other workloads timed after the headline one (each a few steps; no e2e line).
+SIDE_CONFIGS = ["c2_bf16_65k", "c3_bf16_causal_lm", "c4_bf16_1m_lr256"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -87,7 +105,7 @@ def weak_scaling_tokens_per_s(world, tokens_per_rank, ms):
 
 # ------------------------------------------------------------------ host oracle timing
 
-def oracle_sample_rate(w, target_s, cap_tokens=None):
+def oracle_sample_rate(w, target_s, cap_tokens=None, threads=None):
     """Time the float64 oracle (forward + backward) on a token prefix of workload w sized to take
     about target_s seconds; returns (tokens/s, threads used, description)."""
     import torch
@@ -95,7 +113,8 @@ def oracle_sample_rate(w, target_s, cap_tokens=None):
     import oracle
     from linear_lsh_sketch_gb300.workloads import as_oracle_array, make_inputs
 
-    threads = min(os.cpu_count() or 1, w.B * w.H)
+    if threads is None:
+        threads = min(os.cpu_count() or 1, w.B * w.H)
 
     def run(n):
         ws = w.scaled(N=n)
@@ -153,8 +172,8 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "host_cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -217,20 +236,47 @@ class ClockSampler:
 
 def kernel_table(prof, w, hbm_peak):
     """Per kernel of the timed region: launches, total ms, share of the kernel time, ms per launch
-    and, for the kernels with compulsory bytes in KERNEL_BYTES, achieved GB/s and its fraction of
-    the HBM peak.  prof: {name: (launches, total ms)}."""
+    and, for the kernels in KERNEL_BYTES, two HBM fractions of the peak: `frac` against the
+    kernel's own compulsory bytes (what it must move as written) and `alg_frac` against its share
+    of the step's algorithmic bytes.  prof: {name: (launches, total ms)}."""
     total = sum(v[1] for v in prof.values())
     out = {}
+    unit = w.d * w.elem_bytes * w.B * w.H * w.N
     for name, (nl, ms) in prof.items():
         row = {"launches": nl, "ms_total": ms, "share": ms / max(total, 1e-9),
                "ms_per_launch": ms / max(nl, 1)}
         if name in KERNEL_BYTES and nl > 0 and ms > 0:
             mult, extra = KERNEL_BYTES[name]
             nbytes = (mult * w.d * w.elem_bytes + extra) * w.B * w.H * w.N
-            gbs = nbytes / (row["ms_per_launch"] / 1000.0) / 1e9
-            row.update(achieved_gbs=gbs, frac=gbs / hbm_peak)
+            sec = row["ms_per_launch"] / 1000.0
+            gbs = nbytes / sec / 1e9
+            share = 0 if (w.causal and name in CAUSAL_SEGMENT_SUMS) else KERNEL_ALG_SHARE.get(name, 0)
+            alg = share * unit
+            row.update(achieved_gbs=gbs, frac=gbs / hbm_peak, compulsory_bytes=nbytes, alg_bytes=alg,
+                       alg_gbs=alg / sec / 1e9, alg_frac=alg / sec / 1e9 / hbm_peak)
         out[name] = row
     return out
+
+
+def step_roofline(w, ms, prof, hbm_peak, peak_kind):
+    """The step's roofline: 12 d e algorithmic bytes per (token, head) over the step time, with the
+    dominant kernel (largest share of the kernel time) and its own fractions beside it."""
+    step_bytes = 12 * w.d * w.elem_bytes * w.B * w.H * w.N
+    gbs = step_bytes / (ms / 1000.0) / 1e9
+    roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+            "peak_kind": peak_kind + " (copy bandwidth)", "algorithmic_bytes_per_step": step_bytes,
+            "basis": "12 * d * elem_bytes per (token, head) over ms_per_step: the forward reads Q, K, V and "
+                     "writes O; the backward reads Q, K, V, O, dO and writes dQ, dK, dV",
+            "traffic": traffic_for_step(w, prof)}
+    table = kernel_table(prof, w, hbm_peak) if prof else {}
+    if table:
+        name = max(table, key=lambda k: table[k]["ms_total"])
+        k = table[name]
+        roof["dominant_kernel"] = {
+            "name": name, "ms_per_launch": k["ms_per_launch"], "alg_bytes_per_launch": k.get("alg_bytes"),
+            "alg_frac": k.get("alg_frac"), "compulsory_bytes_per_launch": k.get("compulsory_bytes"),
+            "compulsory_frac": k.get("frac"), "traffic": traffic_for(name, w)}
+    return roof, table
 
 
 def run_ours(args, w):
@@ -238,7 +284,7 @@ def run_ours(args, w):
     import torch.distributed as dist
 
     import linear_lsh_sketch_gb300 as race
-    from linear_lsh_sketch_gb300.workloads import make_inputs
+    from linear_lsh_sketch_gb300.workloads import CONFIGS, make_inputs
 
     rank, world, local = env_rank()
     if world > 1:
@@ -252,7 +298,10 @@ def run_ours(args, w):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, threads, desc, _, _ = oracle_sample_rate(w, args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "host_cores": os.cpu_count(),
+               "kind": "oracle", "sample": desc,
+               "note": "the oracle runs one thread per (batch, head) problem, so it uses min(host cores, B*H) "
+                       "threads"}
 
     inp = make_inputs(w, seed=rank, device=dev)
     Q, K, V, dO, W = inp["Q"], inp["K"], inp["V"], inp["dO"], inp["W"]
@@ -301,20 +350,7 @@ def run_ours(args, w):
     tokens = w.B * w.N
     value = weak_scaling_tokens_per_s(world, tokens, ms)
 
-    # dominant kernel and its roofline
-    roof = None
-    if prof:
-        name, (nl, tot) = max(prof.items(), key=lambda kv: kv[1][1])
-        per_launch_ms = tot / max(nl, 1)
-        mult, extra = KERNEL_BYTES.get(name, (0, 0))
-        alg = (mult * w.d * w.elem_bytes + extra) * w.B * w.H * w.N
-        achieved = alg / (per_launch_ms / 1000.0) / 1e9
-        roof = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "peak_kind": peak_kind + " (copy bandwidth)",
-                "algorithmic_bytes_per_launch": alg, "ms_per_launch": per_launch_ms,
-                "traffic": traffic_for(name, w)}
-    kernels = kernel_table(prof, w, hbm_peak)
-    step_bytes = 12 * w.d * w.elem_bytes * w.B * w.H * w.N
+    roof, kernels = step_roofline(w, ms, prof, hbm_peak, peak_kind)
     clocks = clk.summary()
 
     e2e = None
@@ -333,12 +369,13 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": dict(workload_config(w), dbeta=bool(args.dbeta)), "clocks": clocks, "roofline": roof,
-            "step_hbm": {"algorithmic_bytes": step_bytes, "achieved_gbs": step_bytes / (ms / 1000.0) / 1e9,
-                         "frac": step_bytes / (ms / 1000.0) / 1e9 / hbm_peak,
-                         "note": "12 * d * elem_bytes per (token, head): fwd reads Q,K,V writes O; "
-                                 "bwd reads Q,K,V,O,dO writes dQ,dK,dV"},
             "kernels": kernels, "gpu_launches": launches, "cpu_baseline": cpu, "e2e": e2e,
         }
+        if world == 1 and not args.no_configs and not args.tokens:
+            del Q, K, V, dO, W, O, dQ, dK, dV, state, workspace, inp
+            torch.cuda.empty_cache()
+            line["configs"] = {name: time_side_config(args, CONFIGS[name], race, dev, uuid, hbm_peak, peak_kind)
+                               for name in SIDE_CONFIGS if name != w.name}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -359,6 +396,93 @@ def traffic_for(name, w):
     if ent.get("sources_sha") != sources_sha():
         return None
     return ent.get("bytes_per_launch")
+
+
+def traffic_for_step(w, prof):
+    """Sum over the step's kernels of their measured DRAM bytes per launch times launches per step,
+    when the committed ncu summary covers every one of them for this workload; else None."""
+    if not prof:
+        return None
+    total = 0.0
+    for name, (nl, _) in prof.items():
+        if name in ("combine", "dbeta_combine"):
+            continue
+        t = traffic_for(name, w)
+        if t is None:
+            return None
+        total += t * nl
+    return total
+
+
+def _flush_l2(torch, buf):
+    buf.add_(1)
+
+
+def time_side_config(args, w, race, dev, uuid, hbm_peak, peak_kind):
+    """ms per fwd+bwd step of workload w on resident synthetic inputs (CUDA events around each
+    step; when the inputs fit in L2 a 512 MB buffer is rewritten before every step, outside the
+    events), its step roofline and per-kernel table, the clocks, and the float64 oracle on the
+    host cores (all threads it can use, and one thread) for the workloads the oracle finishes in
+    seconds per thousand tokens."""
+    import torch
+    from linear_lsh_sketch_gb300.workloads import make_inputs
+
+    inp = make_inputs(w, seed=0, device=dev)
+    Q, K, V, dO, W = inp["Q"], inp["K"], inp["V"], inp["dO"], inp["W"]
+    shape = race.make_shape(w.B, w.H, w.N, w.d, w.torch_dtype)
+    state = torch.empty(race.race_attn_state_bytes(shape, w.L, w.P, w.causal), dtype=torch.uint8, device=dev)
+    workspace = torch.empty(max(race.race_attn_workspace_bytes(shape, w.L, w.P, w.causal, b) for b in (0, 1)),
+                            dtype=torch.uint8, device=dev)
+    O, dQ, dK, dV = (torch.empty_like(Q) for _ in range(4))
+    tensor_bytes = Q.numel() * Q.element_size()
+    flush = 4 * tensor_bytes < 2 * L2_BYTES
+    fbuf = torch.zeros(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        race.race_attn_fwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, O=O, state=state, workspace=workspace)
+        race.race_attn_bwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, dO, O=O, dQ=dQ, dK=dK, dV=dV, state=state,
+                           workspace=workspace)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    # enough steps to span about a second, so the clock sampler sees the timed region
+    t0 = time.perf_counter()
+    step()
+    torch.cuda.synchronize(dev)
+    est = time.perf_counter() - t0
+    steps = int(max(3, args.side_steps, min(5000, 1.0 / max(est, 1e-6))))
+    race.race_attn_profile_reset()
+    race.race_attn_profile(True)
+    n0 = race.race_attn_launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(uuid) as clk:
+        for e0, e1 in ev:
+            if flush:
+                _flush_l2(torch, fbuf)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+    race.race_attn_profile(False)
+    prof = race.race_attn_profile_read()
+    launches = race.race_attn_launch_count() - n0
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    roof, kernels = step_roofline(w, ms, prof, hbm_peak, peak_kind)
+    out = {"workload": w.describe(), "ms_per_step": ms, "steps": steps, "value": w.B * w.N / (ms / 1000.0),
+           "unit": "tokens/s", "roofline": roof, "kernels": kernels, "clocks": clk.summary(),
+           "gpu_launches": launches,
+           "l2": ("inputs fit in L2: a 512 MB buffer is rewritten before each step, outside the timed events"
+                  if flush else "every input tensor is larger than L2; no flush")}
+    del inp, Q, K, V, dO, W, O, dQ, dK, dV, state, workspace, fbuf
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline and w.N * w.B <= 2 ** 17:
+        rate, threads, desc, _, _ = oracle_sample_rate(w, args.side_cpu_seconds)
+        rate1, _, desc1, _, _ = oracle_sample_rate(w, args.side_cpu_seconds, threads=1)
+        out["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads, "host_cores": os.cpu_count(),
+                               "kind": "oracle", "sample": desc, "one_thread": {"value": rate1, "sample": desc1}}
+    return out
 
 
 def sources_sha():
@@ -582,6 +706,11 @@ def main():
                     help="decode: one causal decode step per (b, h) of --heads heads; angular: exact angular "
                          "attention at the workload's d and --tokens (default 8192) tokens")
     ap.add_argument("--heads", type=int, default=1024, help="(b, h) problems of the decode batch")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads timed after the headline one (the `configs` key)")
+    ap.add_argument("--side-steps", type=int, default=10, help="timed steps of each other workload")
+    ap.add_argument("--side-cpu-seconds", type=float, default=4.0,
+                    help="seconds of oracle time per host-baseline sample of the small workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
     from linear_lsh_sketch_gb300.workloads import CONFIGS
