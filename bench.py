@@ -29,30 +29,45 @@ SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.
               "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
               "clocks_event_reasons.sw_power_cap"]
 
-# Compulsory HBM bytes per (token, head) of each kernel, as (multiples of d * elem_bytes,
-# extra bytes): the token tensors it must read or write once, plus per-token float32 scalars.
+# Compulsory HBM bytes per (token, head) of each kernel, as (multiples of d * elem_bytes, extra
+# bytes, feature rows): the token tensors it must read or write once, per-token float32 scalars,
+# and rows of bf16 bucket features (L R values padded to a multiple of 8) it writes or reads.
 KERNEL_BYTES = {
-    "sketch_keys": (2, 0),        # reads K, V
-    "sketch_grad": (2, 8),        # reads Q, dO and {1/den, dO.O}
-    "readout": (2, 0),            # reads Q, writes O
-    "bwd_query": (3, 8),          # reads Q, dO; writes dQ and {1/den, dO.O}
-    "bwd_key": (4, 0),            # reads K, V; writes dK, dV
-    "causal_fwd": (4, 0),         # reads Q, K, V; writes O
-    "causal_bwd_q": (5, 8),       # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
-    "causal_bwd_kv": (6, 8),      # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
-    "tc_causal_totals": (2, 0),   # reads K, V
-    "tc_causal_fwd": (4, 0),      # reads Q, K, V; writes O
-    "tc_causal_bwd_q": (5, 8),    # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
-    "tc_causal_bwd_kv": (6, 8),   # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
-    "tc5_sketch_keys": (2, 0),    # reads K, V
-    "tc5_sketch_grad": (2, 8),    # reads Q, dO and {1/den, dO.O}
-    "tc5_readout": (2, 0),        # reads Q, writes O
-    "tc5_bwd_query": (3, 8),      # reads Q, dO; writes dQ and {1/den, dO.O}
-    "tc5_bwd_key": (4, 0),        # reads K, V; writes dK, dV
-    "tc5_causal_fwd": (4, 0),     # reads Q, K, V; writes O
-    "tc5_causal_bwd_q": (5, 8),   # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
-    "tc5_causal_bwd_kv": (6, 8),  # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
+    "sketch_keys": (2, 0, 0),        # reads K, V
+    "sketch_grad": (2, 8, 0),        # reads Q, dO and {1/den, dO.O}
+    "readout": (2, 0, 0),            # reads Q, writes O
+    "bwd_query": (3, 8, 0),          # reads Q, dO; writes dQ and {1/den, dO.O}
+    "bwd_key": (4, 0, 0),            # reads K, V; writes dK, dV
+    "causal_fwd": (4, 0, 0),         # reads Q, K, V; writes O
+    "causal_bwd_q": (5, 8, 0),       # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
+    "causal_bwd_kv": (6, 8, 0),      # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
+    "tc_causal_totals": (2, 0, 0),   # reads K, V
+    "tc_causal_fwd": (4, 0, 0),      # reads Q, K, V; writes O
+    "tc_causal_bwd_q": (5, 8, 0),    # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
+    "tc_causal_bwd_kv": (6, 8, 0),   # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
+    "tc5_sketch_keys": (2, 0, 0),    # reads K, V
+    "tc5_sketch_grad": (2, 8, 0),    # reads Q, dO and {1/den, dO.O}
+    "tc5_readout": (2, 0, 0),        # reads Q, writes O
+    "tc5_bwd_query": (3, 8, 0),      # reads Q, dO; writes dQ and {1/den, dO.O}
+    "tc5_bwd_key": (4, 0, 0),        # reads K, V; writes dK, dV
+    "tc5_causal_fwd": (3, 0, 1),     # reads Q, phi(K) rows, V; writes O
+    "tc5_causal_bwd_q": (4, 8, 2),   # reads Q, phi(K) rows, V, dO; writes dQ, {1/den, dO.O} and F'_Q
+    "tc5_causal_bwd_kv": (5, 8, 1),  # reads F'_Q, K, V, dO and {1/den, dO.O}; writes dK, dV
 }
+# On the causal path the segment-sum pass also writes every key's phi(K) row.
+CAUSAL_FEATURE_WRITERS = {"tc5_sketch_keys"}
+
+
+def feature_row_bytes(w):
+    """Bytes of one stored bucket-feature row: L R bf16 values padded to a multiple of 8."""
+    return 2 * ((w.LR + 7) // 8 * 8)
+
+
+def compulsory_bytes(name, w):
+    mult, extra, feat = KERNEL_BYTES[name]
+    if w.causal and name in CAUSAL_FEATURE_WRITERS:
+        feat += 1
+    return (mult * w.d * w.elem_bytes + extra + feat * feature_row_bytes(w)) * w.B * w.H * w.N
 
 
 # Each kernel's share of the step's algorithmic bytes (12 d e per (token, head): the forward
@@ -246,8 +261,7 @@ def kernel_table(prof, w, hbm_peak):
         row = {"launches": nl, "ms_total": ms, "share": ms / max(total, 1e-9),
                "ms_per_launch": ms / max(nl, 1)}
         if name in KERNEL_BYTES and nl > 0 and ms > 0:
-            mult, extra = KERNEL_BYTES[name]
-            nbytes = (mult * w.d * w.elem_bytes + extra) * w.B * w.H * w.N
+            nbytes = compulsory_bytes(name, w)
             sec = row["ms_per_launch"] / 1000.0
             gbs = nbytes / sec / 1e9
             share = 0 if (w.causal and name in CAUSAL_SEGMENT_SUMS) else KERNEL_ALG_SHARE.get(name, 0)

@@ -129,6 +129,9 @@ struct Plan {
     size_t off_status = 0;  // one 32-bit device status word (error bits of bounded waits)
     size_t off_part = 0, off_sk = 0, off_gpart = 0, off_gsk = 0, off_aux = 0;
     size_t off_db = 0;     // d(loss)/d(beta) partials: [2][BH][db_cap] floats
+    size_t off_fq = 0;     // causal tcgen05 backward: F'_Q rows handed from the query to the key side
+    size_t off_fk = 0;     // causal tcgen05 path without `state`: the keys' bucket-feature rows
+    size_t state_fk = 0;   // causal tcgen05 path: offset of the keys' feature rows inside `state`
     int64_t db_cap = 0;    // partial slots per (side, b, h): at least every backward kernel's grid x
     size_t ws_fwd = 0, ws_bwd = 0, state = 0;
 };
@@ -192,14 +195,20 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     pl.off_part = 256;
     pl.off_sk = align256(pl.off_part + per_split);
     const size_t sk_bytes = pl.causal ? per_split : per_bh;
-    pl.ws_fwd = align256(pl.off_sk + sk_bytes);
+    // the causal tcgen05 path keeps every key's bucket features (bf16) from the segment-sum pass
+    const size_t fk_bytes = pl.c5 ? c5_feature_rows_bytes(D) : 0;
+    pl.off_fk = align256(pl.off_sk + sk_bytes);
+    pl.ws_fwd = align256(pl.off_fk + fk_bytes);
     pl.off_gpart = pl.ws_fwd;
     pl.off_gsk = align256(pl.off_gpart + per_split);
     pl.off_aux = align256(pl.off_gsk + sk_bytes);
     pl.off_db = align256(pl.off_aux + (size_t)D.BH * D.N * sizeof(float2));
     pl.db_cap = std::max<int64_t>(pl.nsplit, ceil_div(D.N, generic_token_tile()));
-    pl.ws_bwd = align256(pl.off_db + 2 * (size_t)D.BH * pl.db_cap * sizeof(float));
-    pl.state = sk_bytes;
+    pl.off_fq = align256(pl.off_db + 2 * (size_t)D.BH * pl.db_cap * sizeof(float));
+    const size_t fq_bytes = (pl.c5 && c5_bwd_supported(D)) ? c5_feature_rows_bytes(D) : 0;
+    pl.ws_bwd = align256(pl.off_fq + fq_bytes);
+    pl.state_fk = align256(sk_bytes);
+    pl.state = pl.c5 ? pl.state_fk + fk_bytes : sk_bytes;
 
     // every kernel of the chosen path must fit in shared memory
     if (pl.causal) {
@@ -264,10 +273,12 @@ int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float
     RACE_TRY(cudaMemsetAsync(err, 0, sizeof(unsigned), st));
     if constexpr (std::is_same<T, bf16_t>::value) {
         if (pl.c5) {
-            // segment sums of the causal sketch = the non-causal sketch of each segment
-            RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st));
+            // segment sums of the causal sketch = the non-causal sketch of each segment; the pass
+            // also stores every key's bucket features, which the chunk kernel reads instead of K
+            bf16_t *fk = state ? (bf16_t *)((char *)state + pl.state_fk) : (bf16_t *)(ws + pl.off_fk);
+            RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st, fk));
             RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
-            RACE_TRY(launch_c5_fwd(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, err, st));
+            RACE_TRY(launch_c5_fwd(D, Q, fk, V, W, S, pl.seg_len, pl.nsplit, O, err, st));
             return RACE_OK;
         }
         if (use_tc<T>(pl)) {
@@ -335,25 +346,29 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
     if constexpr (std::is_same<T, bf16_t>::value) {
         const bool c5b = pl.c5 && c5_bwd_supported(D);
         if (c5b || (use_tc<T>(pl) && causal_tc_bwd_supported(D))) {
+            // the keys' bucket-feature rows: from the forward's state, or stored again here
+            const bf16_t *fk = S ? (const bf16_t *)((const char *)S + pl.state_fk) : (const bf16_t *)(ws + pl.off_fk);
             if (!S) {
                 float *Sw = (float *)(ws + pl.off_sk);
                 if (pl.c5)
-                    RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st));
+                    RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st,
+                                               c5b ? (bf16_t *)(ws + pl.off_fk) : nullptr));
                 else
                     RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 1, st));
                 S = Sw;
             }
             RACE_TRY(dbeta_begin(pl, ws, dbeta, pl.nsplit, db, st));
+            bf16_t *fq = (bf16_t *)(ws + pl.off_fq);
             if (c5b)
-                RACE_TRY(launch_c5_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err, db.dbq,
-                                         st));
+                RACE_TRY(launch_c5_bwd_q(D, Q, fk, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, fq, gpart, err,
+                                         db.dbq, st));
             else
                 RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err,
                                                 db.dbq, st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
             if (c5b)
-                RACE_TRY(launch_c5_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, db.dbk,
+                RACE_TRY(launch_c5_bwd_kv(D, fq, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, db.dbk,
                                           st));
             else
                 RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err,

@@ -18,9 +18,11 @@
 // swizzled shared tile that serves as B operand (K- and MN-major) and as A operand; the carried
 // G_next is converted each chunk to a bf16 hi + lo shared operand.
 //
-// Roles: warp 8 issues every TMA copy and MMA; warps 0-3 featurise the Q rows, write dV and
-// convert G; warps 4-7 featurise the K rows, run the Jacobian and write dK.  Hand-offs use
-// mbarriers; dK and dV rows go straight from registers to global memory.
+// F'_Q is not recomputed here: the query-side pass, which forms it for its own gradient-sketch
+// sum, writes it out (L R bf16 per token) and this pass reads it instead of Q.
+// Roles: warp 8 issues every TMA copy and MMA; warps 0-3 copy the F'_Q rows into their tile,
+// write dV and convert G; warps 4-7 featurise the K rows, run the Jacobian and write dK.
+// Hand-offs use mbarriers; dK and dV rows go straight from registers to global memory.
 #include "race_launch.h"
 #include "race_nc5_common.cuh"
 
@@ -35,8 +37,7 @@ constexpr int NTHW = NTH + 32;
 constexpr uint32_t T_SC = 0;     // F_K F'_Q^T, then P2 as bf16 pairs (in place, per half)
 constexpr uint32_t T_DV = 128;   // V dO^T, then M2 as bf16 pairs (in place), then dxhat
 constexpr uint32_t T_DVV = 256;  // dV (d columns)
-constexpr uint32_t T_ZQ = 256;   // projections (dead before dV is written)
-constexpr uint32_t T_ZK = 288;
+constexpr uint32_t T_ZK = 288;   // K-row projections (dead before dV is written)
 constexpr uint32_t T_DP = 384;   // dphi_K (L R columns)
 constexpr uint32_t T_FK = 416;   // F_K as bf16 pairs (A operand), 16 columns
 constexpr uint32_t T_DZ = 432;   // dz as bf16 pairs (A operand), 16 columns
@@ -47,13 +48,16 @@ constexpr uint32_t T_COLS = 512;
 enum : uint32_t { B_Q, B_K, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_G,
                   B_COUNT };
 
+// Staging of one chunk's F'_Q rows (64-byte slots) and {1/den, c} pairs, copied in a chunk ahead.
+constexpr uint32_t STG_FQ = C * 64, STG = STG_FQ + C * 8;
+
 struct BwdLayout {
-    uint32_t q, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, zk, bar, slot, bytes, kbb;
+    uint32_t stage, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, zk, bar, slot, bytes, kbb;
     __host__ __device__ BwdLayout(int D)
     {
         kbb = (uint32_t)(D / 64) * BLK;
-        q = 0;
-        k = q + kbb;
+        stage = 0;  // two staging buffers
+        k = stage + 2 * STG;
         v = k + kbb;
         dO = v + kbb;
         fq = dO + kbb;  // F'_Q [t][lr], one 64-column block
@@ -74,7 +78,7 @@ struct BwdLayout {
 // DB: also the CTA's key-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
 template <int D, int P, int LT, bool DB>
 __global__ void __launch_bounds__(NTHW, 1)
-    k_causal_bwdkv5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    k_causal_bwdkv5(const bf16 *__restrict__ fq_in, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
                     const float *__restrict__ W, const float2 *__restrict__ aux, const float *__restrict__ G0,
                     int64_t seg_len, int nseg, bf16 *__restrict__ dK, bf16 *__restrict__ dV,
@@ -130,7 +134,6 @@ __global__ void __launch_bounds__(NTHW, 1)
         }
         *abort = 0;
         tc::fence_mbar_init();
-        prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmdO);
@@ -204,14 +207,9 @@ __global__ void __launch_bounds__(NTHW, 1)
     if (!compute) {
         // ---------------------------------------------------------------- control warp
         if (lane == 0) {
-            auto load_tiles = [&](int k, uint32_t which) {  // which: 1 = Q  2 = V  4 = dO  8 = K
+            auto load_tiles = [&](int k, uint32_t which) {  // which: 2 = V  4 = dO  8 = K
                 const int c = nchunk - 1 - k;
                 const int y = (int)(n_begin + (int64_t)c * C);
-                if (which & 1) {
-                    mbar_arrive_expect_tx(bar(B_Q), KB * BLK);
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_Q));
-                }
                 if (which & 8) {
                     mbar_arrive_expect_tx(bar(B_K), KB * BLK);
 #pragma unroll
@@ -229,10 +227,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                         tma_load(base + Ly.dO + kb * BLK, &tmdO, 64 * kb, y, (int)bh, bar(B_DO));
                 }
             };
-            int issued[4] = {0, 0, 0, 0}, done[4] = {0, 0, 0, 0};  // Q, V, dO, K loads issued / waited for
+            int issued[4] = {0, 0, 0, 0}, done[4] = {0, 0, 0, 0};  // -, V, dO, K loads issued / waited for
             if (nchunk > 0) {
-                load_tiles(0, 15);
-                issued[0] = issued[1] = issued[2] = issued[3] = 1;
+                load_tiles(0, 14);
+                issued[1] = issued[2] = issued[3] = 1;
             }
             constexpr uint32_t id_sc = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t id_dvo = idesc_bf16(128, 128, 0, 0);
@@ -257,14 +255,11 @@ __global__ void __launch_bounds__(NTHW, 1)
             bool ok = true;
             for (int k = 0; k < nchunk && ok; ++k) {
                 const uint32_t par = k & 1;
-                if (!(ok = wait_phase(bar(B_Q), par, abort))) break;
-                ++done[0];
                 if (!(ok = wait_phase(bar(B_K), par, abort))) break;
                 ++done[3];
-                // the projections reuse TMEM columns of the previous chunk's dV
+                // the projection reuses TMEM columns of the previous chunk's dV
                 if (k >= 1 && !(ok = wait_phase(bar(B_DVR), (k - 1) & 1, abort))) break;
                 fence_after();
-                issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
                 issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
                 commit(bar(B_PROJ));
                 // group A once the features and the previous chunk's G operand are in
@@ -289,10 +284,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma_ts(tmem + T_DVV, tmem + T_FK + 8 * ks, d_glo_k + (uint64_t)(2 * ks), id_dv, true);
                 }
                 commit(bar(B_A));
-                if (k + 1 < nchunk) {  // the projection and the norms have read the Q tile; issued after
-                    load_tiles(k + 1, 1);  // group A, which waits on this warp
-                    ++issued[0];
-                }
                 // group B: masked products
                 if (!(ok = wait_phase(bar(B_MASK), par, abort))) break;
                 fence_after();
@@ -336,8 +327,8 @@ __global__ void __launch_bounds__(NTHW, 1)
             if (!ok) {
                 atomicOr(err, kErrTimeout);
                 *abort = 1;
-                const uint32_t bars[4] = {bar(B_Q), bar(B_V), bar(B_DO), bar(B_K)};
-                for (int b = 0; b < 4; ++b)
+                const uint32_t bars[4] = {0u, bar(B_V), bar(B_DO), bar(B_K)};
+                for (int b = 1; b < 4; ++b)
                     if (issued[b] > done[b]) mbar_wait(bars[b], done[b] & 1);
             }
         }
@@ -348,78 +339,70 @@ __global__ void __launch_bounds__(NTHW, 1)
             convert_g();
             warp_signal(bar(B_GOP));
         }
-        // {1 / den, c} of the Q rows, loaded a chunk ahead; chunks run backwards and only the
-        // last one can be partial
-        float2 a2n = make_float2(0.f, 0.f);
-        if (h == 0 && nchunk > 0) {
-            const int64_t nl = n_begin + (int64_t)(nchunk - 1) * C;
-            if (nl + t < n_end) a2n = aux[bh * Dm.N + nl + t];
-        }
+        // F'_Q rows and {1/den, c} of the Q rows, copied into a staging buffer a chunk ahead by the
+        // thread that owns the row; chunks run backwards and only the last one can be partial
+        const int lrs = feature_row_stride(LR);
+        const bf16 *fq_bh = fq_in + bh * Dm.N * lrs;
+        const float2 *aux_bh = aux + bh * Dm.N;
+        auto stage_rows = [&](int kk) {
+            const int64_t row = n_begin + (int64_t)(nchunk - 1 - kk) * C + t;
+            const uint32_t buf = base + Ly.stage + (uint32_t)(kk & 1) * STG;
+            if (row < n_end) {
+#pragma unroll
+                for (int ch = 0; ch < LRMAX / 8; ++ch)
+                    if (8 * ch < lrs) cp_async16(buf + t * 64 + 16 * ch, fq_bh + row * lrs + 8 * ch);
+                cp_async8(buf + STG_FQ + t * 8, aux_bh + row);
+            }
+            cp_async_commit();
+        };
+        if (h == 0 && nchunk > 0) stage_rows(0);
         for (int k = 0; k < nchunk; ++k) {
             const uint32_t par = k & 1;
             const int c = nchunk - 1 - k;
             const int64_t n0 = n_begin + (int64_t)c * C;
             const int cnt = (int)min((int64_t)C, n_end - n0);
             const bool live = t < cnt;
-            const float2 a2 = a2n;
-            if (h == 0 && c >= 1) a2n = aux[bh * Dm.N + n0 - C + t];
-            if (!wait_phase(bar(h ? B_K : B_Q), par, abort)) break;
-            // the row this thread featurises: Q row t (warps 0-3) or K row t (warps 4-7)
-            float inv;
-            {
-                const uint32_t tile = base + (h ? Ly.k : Ly.q);
-                const float ss = half_sumsq<D>(tile, t, 0) + half_sumsq<D>(tile, t, 1);
-                inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-            }
-            if (!wait_phase(bar(B_PROJ), par, abort)) break;
-            fence_after();
+            float inv = 0.f;  // 1 / |K row| (warps 4-7)
             float z[LPP];
-            {
-                float a[32];
-                ld32(tlane + (h ? T_ZK : T_ZQ), a);
-#pragma unroll
-                for (int j = 0; j < LPP; ++j) z[j] = a[j];
-            }
             // K rows keep z in shared memory; with L compiled in they also keep u = tanh(z inv) in
             // registers (L P of them), otherwise the Jacobian recomputes it from z
             float uk[LT > 0 ? LPP : 1];
             if (h == 0) {
-                // F'_Q = phi(Q_t) / den_t -> shared tile row t;  -c_t -> rows 0 / 1 of the mass operand
-                const float sc = a2.x;
+                // F'_Q row t -> shared tile row t (zero past the end);  -c_t -> rows 0 / 1 of the
+                // mass operand; then the next chunk's rows into the other staging buffer
+                cp_async_wait_all();
+                const uint32_t buf = base + Ly.stage + par * STG;
 #pragma unroll
-                for (int l = 0; l < LMAX; ++l) {
-                    if (l < L) {
-                        float u[P], ph[R];
-#pragma unroll
-                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
-                        tc::bucket_probs<P>(u, beta, ph);
-                        if constexpr (R >= 8) {
-#pragma unroll
-                            for (int j = 0; j < R / 8; ++j) {
-                                const int ch = l * (R / 8) + j;
-                                st_shared_v4(base + Ly.fq + sw_chunk(t, ch), mma::pack_bf16(ph[8 * j] * sc, ph[8 * j + 1] * sc),
-                                             mma::pack_bf16(ph[8 * j + 2] * sc, ph[8 * j + 3] * sc),
-                                             mma::pack_bf16(ph[8 * j + 4] * sc, ph[8 * j + 5] * sc),
-                                             mma::pack_bf16(ph[8 * j + 6] * sc, ph[8 * j + 7] * sc));
-                            }
-                        } else {
-#pragma unroll
-                            for (int r = 0; r < R; r += 2) {
-                                const uint32_t w = mma::pack_bf16(ph[r] * sc, ph[r + 1] * sc);
-                                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fq + sw_elem(t, l * R + r)), "r"(w)
-                                             : "memory");
-                            }
-                        }
+                for (int ch = 0; ch < LRMAX / 8; ++ch) {
+                    if (8 * ch < lrs) {
+                        const uint4 v = live ? ld_shared_v4(buf + t * 64 + 16 * ch) : make_uint4(0u, 0u, 0u, 0u);
+                        st_shared_v4(base + Ly.fq + sw_chunk(t, ch), v.x, v.y, v.z, v.w);
                     }
                 }
-                const float mcv = -a2.y;
+                const float cv = live ? reinterpret_cast<const float2 *>(sm + Ly.stage + par * STG + STG_FQ)[t].y : 0.f;
+                if (k + 1 < nchunk) stage_rows(k + 1);
+                const float mcv = -cv;
                 const bf16 mhi = __float2bfloat16_rn(mcv);
                 const bf16 mlo = __float2bfloat16_rn(mcv - __bfloat162float(mhi));
                 unsigned char *mt = sm + Ly.ncm + (t >> 6) * 2048;
                 *reinterpret_cast<bf16 *>(mt + sw_elem(0, t & 63)) = mhi;
                 *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
-                cvec[t] = a2.y;
+                cvec[t] = cv;
             } else {
+                // the K row this thread featurises: norm, then z from the projection
+                if (!wait_phase(bar(B_K), par, abort)) break;
+                {
+                    const float ss = half_sumsq<D>(base + Ly.k, t, 0) + half_sumsq<D>(base + Ly.k, t, 1);
+                    inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+                }
+                if (!wait_phase(bar(B_PROJ), par, abort)) break;
+                fence_after();
+                {
+                    float a[32];
+                    ld32(tlane + T_ZK, a);
+#pragma unroll
+                    for (int j = 0; j < LPP; ++j) z[j] = a[j];
+                }
                 // F_K -> TMEM (A operand); keep u
 #pragma unroll
                 for (int j = 0; j < LMAX * P; ++j)
@@ -589,6 +572,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             if (!group_sync(bar(B_CS2), par, abort)) break;  // gb / TMEM reads done before the next chunk
         }
     }
+    cp_async_wait_all();  // no copy into the staging buffers outlives the CTA (after an abort)
     if constexpr (DB) {  // this CTA's d(loss)/d(beta) partial, summed in a fixed order
         const float sdb = block_sum_fixed(db, cvec);
         if (tid == 0) dbpart[bh * gridDim.x + blockIdx.x] = sdb;
@@ -613,8 +597,11 @@ __global__ void __launch_bounds__(NTHW, 1)
 // then the query-side feature Jacobian gives dQ; the pass also writes {1 / den_t, c_t} per token
 // and the segment's gradient-sketch sum G = sum_t F'_Q(t)^T [dO_t | -c_t] for the key side, and
 // carries S (A^T += V^T F_K, B += F_K^T 1) in TMEM.
+// The keys' features F_K come from the rows the forward's segment-sum pass stored (L R bf16 per
+// token), not from K.
 // Roles: warp 8 issues TMA and MMA; warps 0-3 own the Q rows (x kept in TMEM, den, c, the
-// Jacobian, dQ); warps 4-7 featurise the K rows and convert S to its bf16 operand copy.
+// Jacobian, dQ); warps 4-7 copy the F_K rows into their tile and convert S to its bf16 operand
+// copy.
 
 namespace c5q {
 
@@ -622,7 +609,7 @@ using namespace race::nc5;
 
 constexpr int NTHW = NTH + 32;
 
-constexpr uint32_t T_ZQ = 0, T_ZK = 32;
+constexpr uint32_t T_ZQ = 0;
 constexpr uint32_t T_DV = 64;     // dO V^T, then M1 as bf16 pairs (in place), then dxhat
 constexpr uint32_t T_G = 192;     // g (L R columns)
 constexpr uint32_t T_BT = 224;    // (tril 1) F_K
@@ -637,14 +624,16 @@ constexpr uint32_t T_COLS = 512;
 
 enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_G, B_COUNT };
 
+constexpr uint32_t STG_FK = C * 128;  // one staging buffer of F_K rows (128-byte slots)
+
 struct QLayout {
-    uint32_t q, k, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, bprev, invq, red, bar, slot, bytes, kbb;
+    uint32_t q, stage, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, bprev, invq, red, bar, slot, bytes, kbb;
     __host__ __device__ QLayout(int D)
     {
         kbb = (uint32_t)(D / 64) * BLK;
         q = 0;
-        k = q + kbb;
-        v = k + kbb;
+        stage = q + kbb;  // two F_K staging buffers
+        v = stage + 2 * STG_FK;
         dO = v + kbb;
         fk = dO + kbb;   // F_K [j][lr]
         fq = fk + BLK;   // F'_Q [t][lr]
@@ -666,11 +655,11 @@ struct QLayout {
 // DB: also the CTA's query-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
 template <int D, int P, int LT, bool DB>
 __global__ void __launch_bounds__(NTHW, 1)
-    k_causal_bwdq5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    k_causal_bwdq5(const __grid_constant__ CUtensorMap tmQ, const bf16 *__restrict__ fk_in,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
                    const float *__restrict__ W, const float *__restrict__ S0, int64_t seg_len, int nseg,
-                   bf16 *__restrict__ dQ, float2 *__restrict__ aux, float *__restrict__ Gseg,
-                   unsigned *__restrict__ err, float *__restrict__ dbpart)
+                   bf16 *__restrict__ dQ, float2 *__restrict__ aux, bf16 *__restrict__ fq_out,
+                   float *__restrict__ Gseg, unsigned *__restrict__ err, float *__restrict__ dbpart)
 {
     constexpr int KB = D / 64;
     constexpr int R = 1 << P;
@@ -723,7 +712,6 @@ __global__ void __launch_bounds__(NTHW, 1)
         *abort = 0;
         tc::fence_mbar_init();
         prefetch_tmap(&tmQ);
-        prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmdO);
     }
@@ -800,15 +788,12 @@ __global__ void __launch_bounds__(NTHW, 1)
     if (!compute) {
         // ---------------------------------------------------------------- control warp
         if (lane == 0) {
-            auto load_tiles = [&](int c, uint32_t which) {  // which: 1 = Q,K  2 = V  4 = dO
+            auto load_tiles = [&](int c, uint32_t which) {  // which: 1 = Q  2 = V  4 = dO
                 const int y = (int)(n_begin + (int64_t)c * C);
                 if (which & 1) {
-                    mbar_arrive_expect_tx(bar(B_QK), 2 * KB * BLK);
+                    mbar_arrive_expect_tx(bar(B_QK), KB * BLK);
 #pragma unroll
-                    for (int kb = 0; kb < KB; ++kb) {
-                        tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_QK));
-                        tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar(B_QK));
-                    }
+                    for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_QK));
                 }
                 if (which & 2) {
                     mbar_arrive_expect_tx(bar(B_V), KB * BLK);
@@ -848,7 +833,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                 ++done[0];
                 fence_after();
                 issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
-                issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
                 commit(bar(B_PROJ));
                 if (!(ok = wait_phase(bar(B_FEAT), par, abort))) break;
                 if (!(ok = wait_phase(bar(B_SOP), par, abort))) break;
@@ -932,71 +916,67 @@ __global__ void __launch_bounds__(NTHW, 1)
             convert_s(0);
             warp_signal(bar(B_SOP));
         }
+        // F_K rows of chunk c -> staging buffer c & 1, by the thread that owns the row (warps 4-7)
+        const int lrs = feature_row_stride(LR);
+        const bf16 *fk_bh = fk_in + bh * Dm.N * lrs;
+        auto stage_rows = [&](int c) {
+            const int64_t row = n_begin + (int64_t)c * C + t;
+            if (row < n_end) {
+                const uint32_t buf = base + Ly.stage + (uint32_t)(c & 1) * STG_FK;
+#pragma unroll
+                for (int ch = 0; ch < LRMAX / 8; ++ch)
+                    if (8 * ch < lrs) cp_async16(buf + t * 128 + 16 * ch, fk_bh + row * lrs + 8 * ch);
+            }
+            cp_async_commit();
+        };
+        if (h == 1 && nchunk > 0) stage_rows(0);
         bool ok = group_sync(bar(B_CS), 0, abort);  // B_prev visible to the Q warps
         for (int c = 0; c < nchunk && ok; ++c) {
             const uint32_t par = c & 1;
             const int64_t n0 = n_begin + (int64_t)c * C;
             const int cnt = (int)min((int64_t)C, n_end - n0);
             const bool live = t < cnt;
-            if (!(ok = wait_phase(bar(B_QK), par, abort))) break;
-            float inv;
-            {
-                const uint32_t tile = base + (h ? Ly.k : Ly.q);
-                float ss = 0.f;
+            float uq[LPP];  // Q rows keep u for the Jacobian
+            if (h == 0) {
+                if (!(ok = wait_phase(bar(B_QK), par, abort))) break;
+                float inv;
+                {
+                    float ss = 0.f;
 #pragma unroll
-                for (int j = 0; j < D / 8; j += 2) {
-                    const uint4 w0 = ld_shared_v4(tile + (j >> 3) * BLK + sw_chunk(t, j & 7));
-                    const uint4 w1 = ld_shared_v4(tile + ((j + 1) >> 3) * BLK + sw_chunk(t, (j + 1) & 7));
-                    ss += sumsq8(w0) + sumsq8(w1);
-                    if (h == 0) {  // keep the Q row in TMEM for the dQ epilogue
+                    for (int j = 0; j < D / 8; j += 2) {
+                        const uint4 w0 = ld_shared_v4(base + Ly.q + (j >> 3) * BLK + sw_chunk(t, j & 7));
+                        const uint4 w1 = ld_shared_v4(base + Ly.q + ((j + 1) >> 3) * BLK + sw_chunk(t, (j + 1) & 7));
+                        ss += sumsq8(w0) + sumsq8(w1);
+                        // keep the Q row in TMEM for the dQ epilogue
                         const uint32_t r[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                         stn<8>(tlane + T_X + 4 * j, r);
                     }
+                    inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+                    invq_s[t] = inv;
                 }
-                inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-                if (h == 0) invq_s[t] = inv;
-            }
-            if (!(ok = wait_phase(bar(B_PROJ), par, abort))) break;
-            fence_after();
-            float z[LPP];
-            {
-                float a[32];
-                ld32(tlane + (h ? T_ZK : T_ZQ), a);
+                if (!(ok = wait_phase(bar(B_PROJ), par, abort))) break;
+                fence_after();
+                float z[LPP];
+                {
+                    float a[32];
+                    ld32(tlane + T_ZQ, a);
 #pragma unroll
-                for (int j = 0; j < LPP; ++j) z[j] = a[j];
-            }
-            float uq[LPP];  // Q rows keep u for the Jacobian
-            if (h == 0) {
+                    for (int j = 0; j < LPP; ++j) z[j] = a[j];
+                }
 #pragma unroll
                 for (int j = 0; j < LPP; ++j) uq[j] = j < LP ? tc::tanh_abs(z[j] * inv) : 0.f;
             } else {
-                const float sc = live ? 1.f : 0.f;
+                // the F_K row t (zero past the end) -> shared F_K tile; then the next chunk's rows
+                cp_async_wait_all();
+                const uint32_t buf = base + Ly.stage + par * STG_FK;
 #pragma unroll
-                for (int l = 0; l < LMAX; ++l) {
-                    if (l < L) {
-                        float u[P], ph[R];
-#pragma unroll
-                        for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
-                        tc::bucket_probs<P>(u, beta, ph);
-                        if constexpr (R >= 8) {
-#pragma unroll
-                            for (int j = 0; j < R / 8; ++j) {
-                                const int ch = l * (R / 8) + j;
-                                st_shared_v4(base + Ly.fk + sw_chunk(t, ch), mma::pack_bf16(ph[8 * j] * sc, ph[8 * j + 1] * sc),
-                                             mma::pack_bf16(ph[8 * j + 2] * sc, ph[8 * j + 3] * sc),
-                                             mma::pack_bf16(ph[8 * j + 4] * sc, ph[8 * j + 5] * sc),
-                                             mma::pack_bf16(ph[8 * j + 6] * sc, ph[8 * j + 7] * sc));
-                            }
-                        } else {
-#pragma unroll
-                            for (int r = 0; r < R; r += 2) {
-                                const uint32_t w = mma::pack_bf16(ph[r] * sc, ph[r + 1] * sc);
-                                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fk + sw_elem(t, l * R + r)), "r"(w)
-                                             : "memory");
-                            }
-                        }
+                for (int ch = 0; ch < LRMAX / 8; ++ch) {
+                    if (8 * ch < lrs) {
+                        const uint4 v = live ? ld_shared_v4(buf + t * 128 + 16 * ch) : make_uint4(0u, 0u, 0u, 0u);
+                        st_shared_v4(base + Ly.fk + sw_chunk(t, ch), v.x, v.y, v.z, v.w);
                     }
                 }
+                if (c + 1 < nchunk) stage_rows(c + 1);
             }
             wait_st();
             warp_signal(bar(B_FEAT));
@@ -1103,6 +1083,13 @@ __global__ void __launch_bounds__(NTHW, 1)
                         }
                     }
                 }
+                if (live) {  // the row of F'_Q the key-side pass reads instead of recomputing it
+                    const int lrs = feature_row_stride(LR);
+                    bf16 *dst = fq_out + (bh * Dm.N + n0 + t) * lrs;
+#pragma unroll
+                    for (int ch = 0; ch < LRMAX / 8; ++ch)
+                        if (8 * ch < lrs) st_global_v4(dst + 8 * ch, ld_shared_v4(base + Ly.fq + sw_chunk(t, ch)));
+                }
                 uint32_t r[8];
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
@@ -1179,6 +1166,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             }
         }
     }
+    cp_async_wait_all();  // no copy into the staging buffers outlives the CTA (after an abort)
     if constexpr (DB) {  // this CTA's d(loss)/d(beta) partial, summed in a fixed order
         const float sdb = block_sum_fixed(db, red);
         if (tid == 0) dbpart[bh * gridDim.x + blockIdx.x] = sdb;
@@ -1197,6 +1185,11 @@ __global__ void __launch_bounds__(NTHW, 1)
 
 cudaError_t make_token_map(CUtensorMap *map, const void *base, const Dims &D);
 
+size_t c5_feature_rows_bytes(const Dims &D)
+{
+    return (size_t)D.BH * D.N * nc5::feature_row_stride(D.LR) * sizeof(bf16_t);
+}
+
 bool c5_bwd_supported(const Dims &D)
 {
     return (D.d == 64 || D.d == 128) && D.P >= 1 && D.P <= 5 && D.LP <= nc5::LPP && D.LR <= 32 &&
@@ -1206,7 +1199,7 @@ bool c5_bwd_supported(const Dims &D)
 namespace {
 
 template <int D, int P, int LT>
-cudaError_t bwdkv5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+cudaError_t bwdkv5_launch(const Dims &Dm, const bf16_t *fq, const CUtensorMap &mk, const CUtensorMap &mv,
                           const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
                           int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
@@ -1216,29 +1209,26 @@ cudaError_t bwdkv5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorM
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_bwd_kv", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5b::NTHW), smem,
-                         st, mq, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart);
+                         st, fq, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart);
 }
 
 // (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
 template <int D, int P>
-cudaError_t bwdkv5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+cudaError_t bwdkv5_inst(const Dims &Dm, const bf16_t *fq, const CUtensorMap &mk, const CUtensorMap &mv,
                         const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
                         int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
     if constexpr (D == 128 && P == 3)
         if (Dm.L == 3)
-            return bwdkv5_launch<D, P, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-    return bwdkv5_launch<D, P, 0>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+            return bwdkv5_launch<D, P, 3>(Dm, fq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+    return bwdkv5_launch<D, P, 0>(Dm, fq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
 }
 
-}  // namespace
-
-namespace {
-
 template <int D, int P, int LT>
-cudaError_t bwdq5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+cudaError_t bwdq5_launch(const Dims &Dm, const CUtensorMap &mq, const bf16_t *fk, const CUtensorMap &mv,
                          const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
-                         bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, float *dbpart, cudaStream_t st)
+                         bf16_t *dQ, float2 *aux, bf16_t *fq, float *Gseg, unsigned *err, float *dbpart,
+                         cudaStream_t st)
 {
     const c5q::QLayout Ly(D);
     const size_t smem = Ly.bytes + 1024;
@@ -1246,75 +1236,62 @@ cudaError_t bwdq5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMa
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_bwd_q", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5q::NTHW), smem, st,
-                         mq, mk, mv, mdo, Dm, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart);
+                         mq, fk, mv, mdo, Dm, W, S0, seg_len, nseg, dQ, aux, fq, Gseg, err, dbpart);
 }
 
 // (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
 template <int D, int P>
-cudaError_t bwdq5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+cudaError_t bwdq5_inst(const Dims &Dm, const CUtensorMap &mq, const bf16_t *fk, const CUtensorMap &mv,
                        const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
-                       bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, float *dbpart, cudaStream_t st)
+                       bf16_t *dQ, float2 *aux, bf16_t *fq, float *Gseg, unsigned *err, float *dbpart,
+                       cudaStream_t st)
 {
     if constexpr (D == 128 && P == 3)
         if (Dm.L == 3)
-            return bwdq5_launch<D, P, 3>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart, st);
-    return bwdq5_launch<D, P, 0>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart, st);
+            return bwdq5_launch<D, P, 3>(Dm, mq, fk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, fq, Gseg, err, dbpart,
+                                         st);
+    return bwdq5_launch<D, P, 0>(Dm, mq, fk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, fq, Gseg, err, dbpart, st);
 }
 
 }  // namespace
 
-cudaError_t launch_c5_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
+#define RACE_C5B_SHAPES(X) X(64, 1) X(64, 2) X(64, 3) X(64, 4) X(64, 5) X(128, 1) X(128, 2) X(128, 3) X(128, 4) X(128, 5)
+
+cudaError_t launch_c5_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *fk, const bf16_t *V, const bf16_t *dO,
                             const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
-                            float *Gseg, unsigned *err, float *dbpart, cudaStream_t st)
+                            bf16_t *fq, float *Gseg, unsigned *err, float *dbpart, cudaStream_t st)
 {
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mv, mdo;
     cudaError_t e = make_token_map(&mq, Q, Dm);
-    if (e == cudaSuccess) e = make_token_map(&mk, K, Dm);
     if (e == cudaSuccess) e = make_token_map(&mv, V, Dm);
     if (e == cudaSuccess) e = make_token_map(&mdo, dO, Dm);
     if (e != cudaSuccess) return e;
 #define RACE_C5Q_CASE(DD, PP) \
-    case DD * 16 + PP:        \
-        return bwdq5_inst<DD, PP>(Dm, mq, mk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, Gseg, err, dbpart, st);
+    case DD * 16 + PP: return bwdq5_inst<DD, PP>(Dm, mq, fk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, fq, Gseg, err, dbpart, st);
     switch (Dm.d * 16 + Dm.P) {
-        RACE_C5Q_CASE(64, 1)
-        RACE_C5Q_CASE(64, 2)
-        RACE_C5Q_CASE(64, 3)
-        RACE_C5Q_CASE(64, 4)
-        RACE_C5Q_CASE(64, 5)
-        RACE_C5Q_CASE(128, 1)
-        RACE_C5Q_CASE(128, 2)
-        RACE_C5Q_CASE(128, 3)
-        RACE_C5Q_CASE(128, 4)
-        RACE_C5Q_CASE(128, 5)
+        RACE_C5B_SHAPES(RACE_C5Q_CASE)
         default: return cudaErrorInvalidValue;
     }
 #undef RACE_C5Q_CASE
 }
 
-cudaError_t launch_c5_bwd_kv(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
+cudaError_t launch_c5_bwd_kv(const Dims &Dm, const bf16_t *fq, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
                              const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
                              bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
-    CUtensorMap mq, mk, mv, mdo;
-    cudaError_t e = make_token_map(&mq, Q, Dm);
-    if (e == cudaSuccess) e = make_token_map(&mk, K, Dm);
+    CUtensorMap mk, mv, mdo;
+    cudaError_t e = make_token_map(&mk, K, Dm);
     if (e == cudaSuccess) e = make_token_map(&mv, V, Dm);
     if (e == cudaSuccess) e = make_token_map(&mdo, dO, Dm);
     if (e != cudaSuccess) return e;
+#define RACE_C5KV_CASE(DD, PP) \
+    case DD * 16 + PP: return bwdkv5_inst<DD, PP>(Dm, fq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
     switch (Dm.d * 16 + Dm.P) {
-        case 64 * 16 + 1: return bwdkv5_inst<64, 1>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 64 * 16 + 2: return bwdkv5_inst<64, 2>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 64 * 16 + 3: return bwdkv5_inst<64, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 64 * 16 + 4: return bwdkv5_inst<64, 4>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 64 * 16 + 5: return bwdkv5_inst<64, 5>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 128 * 16 + 1: return bwdkv5_inst<128, 1>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 128 * 16 + 2: return bwdkv5_inst<128, 2>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 128 * 16 + 3: return bwdkv5_inst<128, 3>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 128 * 16 + 4: return bwdkv5_inst<128, 4>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-        case 128 * 16 + 5: return bwdkv5_inst<128, 5>(Dm, mq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        RACE_C5B_SHAPES(RACE_C5KV_CASE)
         default: return cudaErrorInvalidValue;
     }
+#undef RACE_C5KV_CASE
 }
+#undef RACE_C5B_SHAPES
 
 }  // namespace race

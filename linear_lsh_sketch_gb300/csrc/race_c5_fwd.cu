@@ -10,18 +10,22 @@
 //
 // One CTA walks one segment of a (batch, head) sequence; the sketch at the segment start comes
 // from the segment sums (the non-causal sketch kernel restricted to each segment) and an
-// exclusive scan over segments.  Per chunk, on the tensor cores (M = 128, fp32 in TMEM):
-//   z = X (W_hi + W_lo)^T for the Q and K tiles;
+// exclusive scan over segments.  The segment-sum pass also stores every key's bucket features
+// F_K (L R bf16 per token), which this kernel reads instead of K.  Per chunk, on the tensor
+// cores (M = 128, fp32 in TMEM):
+//   z = Q (W_hi + W_lo)^T;
 //   scores F_Q F_K^T with F_Q in TMEM (A operand) and F_K in a swizzled shared tile;
 //   P = the causally masked scores, written back to TMEM as bf16 (A operand);
 //   [num | den] = P V and P 1 plus F_Q [A | B], with [A | B] in shared memory as bf16 hi + lo
 //   (about 16 mantissa bits);
 //   A^T += V^T F_K (M = d, N = L R) and B += F_K^T 1 (M = L R), both accumulating in TMEM over
 //   the whole segment.
-// On CUDA cores: row norms, bucket features (tanh, products of sigmoids), the causal mask, the
-// num / den epilogue, and the conversion of the TMEM sketch to its bf16 operand copy.
-// Q and K tiles are single-buffered (refilled once the projection has read them); V tiles are
-// double-buffered and each also stages its chunk's output for the TMA store.
+// On CUDA cores: Q row norms and bucket features (tanh, products of sigmoids), the copy of the F_K
+// rows into their tile, the causal mask, the num / den epilogue, and the conversion of the TMEM
+// sketch to its bf16 operand copy.  The Q tile is single-buffered (refilled once the projection
+// has read it); V tiles are double-buffered and each also stages its chunk's output for the TMA
+// store; the F_K rows come in a chunk ahead (cp.async by the row's thread) into two staging
+// buffers.
 #include "race_launch.h"
 #include "race_nc5_common.cuh"
 
@@ -35,21 +39,22 @@ constexpr uint32_t T_O = 0;      // [num | den]: d + 16 columns
 constexpr uint32_t T_ST = 144;   // A^T (lanes = d), L R (<= 64) columns
 constexpr uint32_t T_MS = 208;   // B (lanes = sketch row), 16 columns (column 0 used)
 constexpr uint32_t T_ZQ = 224;   // projections of the Q tile
-constexpr uint32_t T_ZK = 256;   // projections of the K tile
 constexpr uint32_t T_FQ = 288;   // F_Q as bf16 pairs (A operand), L R / 2 columns
 constexpr uint32_t T_SC = 320;   // scores, 128 columns
 constexpr uint32_t T_P = 448;    // masked scores as bf16 pairs (A operand), 64 columns
 constexpr uint32_t T_COLS = 512;
 
+constexpr uint32_t STG_FK = C * 128;  // one staging buffer of F_K rows (128-byte slots: L R <= 64)
+
 struct FwdLayout {
-    uint32_t q, k, v, fk, shi, slo, whi, wlo, ones, zero, bar, slot, bytes, kbb, sblk;
+    uint32_t q, stage, v, fk, shi, slo, whi, wlo, ones, zero, bar, slot, bytes, kbb, sblk;
     __host__ __device__ FwdLayout(int D)
     {
         kbb = (uint32_t)(D / 64) * BLK;  // bytes of one token tile
         sblk = (uint32_t)(D + 16) * 128;
         q = 0;
-        k = q + kbb;
-        v = k + kbb;       // two stages
+        stage = q + kbb;   // two F_K staging buffers
+        v = stage + 2 * STG_FK;  // two stages
         fk = v + 2 * kbb;  // two 64-column blocks (the second stays zero)
         shi = fk + 2 * BLK;
         slo = shi + sblk;
@@ -124,7 +129,7 @@ enum : uint32_t { B_QK, B_PROJ, B_SC, B_MMA, B_FEAT, B_MASK, B_SOP, B_V0, B_V1, 
 
 template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTHW, 1)
-    k_causal_fwd5(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    k_causal_fwd5(const __grid_constant__ CUtensorMap tmQ, const bf16 *__restrict__ fk_in,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, Dims Dm,
                   const float *__restrict__ W, const float *__restrict__ S0, int64_t seg_len, int nseg,
                   unsigned *__restrict__ err)
@@ -170,7 +175,6 @@ __global__ void __launch_bounds__(NTHW, 1)
         *abort = 0;
         tc::fence_mbar_init();
         prefetch_tmap(&tmQ);
-        prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmO);
     }
@@ -209,14 +213,11 @@ __global__ void __launch_bounds__(NTHW, 1)
     if (!compute) {
         // ---------------------------------------------------------------- control warp
         if (lane == 0) {
-            auto load_qk = [&](int c) {
+            auto load_qk = [&](int c) {  // the Q tile (the keys arrive as feature rows)
                 const int y = (int)(n_begin + (int64_t)c * C);
-                mbar_arrive_expect_tx(bar(B_QK), 2 * KB * BLK);
+                mbar_arrive_expect_tx(bar(B_QK), KB * BLK);
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_QK));
-                    tma_load(base + Ly.k + kb * BLK, &tmK, 64 * kb, y, (int)bh, bar(B_QK));
-                }
+                for (int kb = 0; kb < KB; ++kb) tma_load(base + Ly.q + kb * BLK, &tmQ, 64 * kb, y, (int)bh, bar(B_QK));
             };
             auto load_v = [&](int c) {
                 const int y = (int)(n_begin + (int64_t)c * C);
@@ -260,7 +261,6 @@ __global__ void __launch_bounds__(NTHW, 1)
             auto project = [&](int c) {
                 fence_after();
                 issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
-                issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
                 commit(bar(B_PROJ));
             };
             bool ok = true, projected = false;  // projected: this chunk's projection went out early
@@ -390,32 +390,45 @@ __global__ void __launch_bounds__(NTHW, 1)
             return true;
         };
 
+        // F_K rows of chunk c -> staging buffer c & 1, by the thread that owns the row (warps 4-7)
+        const int lrs = feature_row_stride(LR);
+        const bf16 *fk_bh = fk_in + bh * Dm.N * lrs;
+        auto stage_rows = [&](int c) {
+            const int64_t row = n_begin + (int64_t)c * C + t;
+            if (row < n_end) {
+                const uint32_t buf = base + Ly.stage + (uint32_t)(c & 1) * STG_FK;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    if (8 * ch < lrs) cp_async16(buf + t * 128 + 16 * ch, fk_bh + row * lrs + 8 * ch);
+            }
+            cp_async_commit();
+        };
+        if (h == 1 && nchunk > 0) stage_rows(0);
+
         for (int c = 0; c < nchunk; ++c) {
             const int64_t n0 = n_begin + (int64_t)c * C;
             const int cnt = (int)min((int64_t)C, n_end - n0);
             const uint32_t fq = T_FQ + (pipe ? 16u * (c & 1) : 0u);
             const uint32_t fk = base + Ly.fk + (pipe ? (uint32_t)(c & 1) * BLK : 0u);
-            // row norm of this thread's row: warps 0-3 Q rows, warps 4-7 K rows
-            if (!wait_phase(bar(B_QK), c & 1, abort)) break;
-            float inv;
-            {
-                const uint32_t tile = base + (h ? Ly.k : Ly.q);
-                const float ss = half_sumsq<D>(tile, t, 0) + half_sumsq<D>(tile, t, 1);
+            // row norm of this thread's Q row (warps 0-3)
+            float inv = 0.f;
+            if (h == 0) {
+                if (!wait_phase(bar(B_QK), c & 1, abort)) break;
+                const float ss = half_sumsq<D>(base + Ly.q, t, 0) + half_sumsq<D>(base + Ly.q, t, 1);
                 inv = ss > 0.f ? rsqrtf(ss) : 0.f;
             }
             if (!pipe && c >= 1 && !previous(c)) break;
-            // features: warps 0-3 the Q row t (-> TMEM), warps 4-7 the K row t (-> shared F_K tile)
-            if (!wait_phase(bar(B_PROJ), c & 1, abort)) break;
-            fence_after();
-            {
+            if (h == 0) {
+                // features of the Q row t -> TMEM
+                if (!wait_phase(bar(B_PROJ), c & 1, abort)) break;
+                fence_after();
                 float z[LPP];
                 {
                     float a[32];
-                    ld32(tlane + (h ? T_ZK : T_ZQ), a);
+                    ld32(tlane + T_ZQ, a);
 #pragma unroll
                     for (int k = 0; k < LPP; ++k) z[k] = a[k];
                 }
-                const float scale = (h == 0 || t < cnt) ? 1.f : 0.f;
 #pragma unroll
                 for (int l = 0; l < LMAX; ++l) {
                     if (l < L) {
@@ -423,45 +436,35 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                         for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
                         tc::bucket_probs<P>(u, beta, ph);
-                        if (h == 0) {
-                            if constexpr (R >= 16) {
+                        if constexpr (R >= 16) {
 #pragma unroll
-                                for (int b = 0; b < R / 16; ++b) {
-                                    uint32_t r[8];
+                            for (int b = 0; b < R / 16; ++b) {
+                                uint32_t r[8];
 #pragma unroll
-                                    for (int j = 0; j < 8; ++j)
-                                        r[j] = mma::pack_bf16(ph[16 * b + 2 * j], ph[16 * b + 2 * j + 1]);
-                                    stn<8>(tlane + fq + (l * R) / 2 + 8 * b, r);
-                                }
-                            } else {
-                                uint32_t r[R / 2];
-#pragma unroll
-                                for (int j = 0; j < R / 2; ++j) r[j] = mma::pack_bf16(ph[2 * j], ph[2 * j + 1]);
-                                stn<R / 2>(tlane + fq + (l * R) / 2, r);
+                                for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(ph[16 * b + 2 * j], ph[16 * b + 2 * j + 1]);
+                                stn<8>(tlane + fq + (l * R) / 2 + 8 * b, r);
                             }
                         } else {
-                            if constexpr (R >= 8) {
+                            uint32_t r[R / 2];
 #pragma unroll
-                                for (int j = 0; j < R / 8; ++j) {
-                                    const int ch = l * (R / 8) + j;
-                                    st_shared_v4(fk + sw_chunk(t, ch),
-                                                 mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
-                                                 mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
-                                                 mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
-                                                 mma::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
-                                }
-                            } else {
-#pragma unroll
-                                for (int r = 0; r < R; r += 2) {
-                                    const int lr = l * R + r;
-                                    const uint32_t w = mma::pack_bf16(ph[r] * scale, ph[r + 1] * scale);
-                                    asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(fk + sw_elem(t, lr)), "r"(w)
-                                                 : "memory");
-                                }
-                            }
+                            for (int j = 0; j < R / 2; ++j) r[j] = mma::pack_bf16(ph[2 * j], ph[2 * j + 1]);
+                            stn<R / 2>(tlane + fq + (l * R) / 2, r);
                         }
                     }
                 }
+            } else {
+                // the F_K row t (zero past the end) -> shared F_K tile; then the next chunk's rows
+                cp_async_wait_all();
+                const bool live = t < cnt;
+                const uint32_t buf = base + Ly.stage + (uint32_t)(c & 1) * STG_FK;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    if (8 * ch < lrs) {
+                        const uint4 v = live ? ld_shared_v4(buf + t * 128 + 16 * ch) : make_uint4(0u, 0u, 0u, 0u);
+                        st_shared_v4(fk + sw_chunk(t, ch), v.x, v.y, v.z, v.w);
+                    }
+                }
+                if (c + 1 < nchunk) stage_rows(c + 1);
             }
             wait_st();
             warp_signal(bar(B_FEAT));
@@ -502,6 +505,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             epilogue(nchunk - 1);
             warp_signal(bar(B_SOP));
         }
+        cp_async_wait_all();  // no copy into the staging buffers outlives the CTA (after an abort)
     }
     fence_before();
     __syncthreads();
@@ -526,7 +530,7 @@ bool c5_supported(const Dims &D)
 namespace {
 
 template <int D, int P, int LT>
-cudaError_t causal_fwd5_launch(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+cudaError_t causal_fwd5_launch(const Dims &Dm, const CUtensorMap &mq, const bf16_t *fk, const CUtensorMap &mv,
                                const CUtensorMap &mo, const float *W, const float *S0, int64_t seg_len, int nseg,
                                unsigned *err, cudaStream_t st)
 {
@@ -536,44 +540,43 @@ cudaError_t causal_fwd5_launch(const Dims &Dm, const CUtensorMap &mq, const CUte
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_fwd", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5::NTHW), smem, st, mq,
-                         mk, mv, mo, Dm, W, S0, seg_len, nseg, err);
+                         fk, mv, mo, Dm, W, S0, seg_len, nseg, err);
 }
 
 // (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
 template <int D, int P>
-cudaError_t causal_fwd5_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+cudaError_t causal_fwd5_inst(const Dims &Dm, const CUtensorMap &mq, const bf16_t *fk, const CUtensorMap &mv,
                              const CUtensorMap &mo, const float *W, const float *S0, int64_t seg_len, int nseg,
                              unsigned *err, cudaStream_t st)
 {
     if constexpr (D == 128 && P == 3)
-        if (Dm.L == 3) return causal_fwd5_launch<D, P, 3>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-    return causal_fwd5_launch<D, P, 0>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        if (Dm.L == 3) return causal_fwd5_launch<D, P, 3>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+    return causal_fwd5_launch<D, P, 0>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
 }
 
 }  // namespace
 
-cudaError_t launch_c5_fwd(const Dims &Dm, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const float *W,
+cudaError_t launch_c5_fwd(const Dims &Dm, const bf16_t *Q, const bf16_t *fk, const bf16_t *V, const float *W,
                           const float *S0, int64_t seg_len, int nseg, bf16_t *O, unsigned *err, cudaStream_t st)
 {
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mv, mo;
     cudaError_t e = make_token_map(&mq, Q, Dm);
-    if (e == cudaSuccess) e = make_token_map(&mk, K, Dm);
     if (e == cudaSuccess) e = make_token_map(&mv, V, Dm);
     if (e == cudaSuccess) e = make_token_map(&mo, O, Dm);
     if (e != cudaSuccess) return e;
     switch (Dm.d * 16 + Dm.P) {
-        case 64 * 16 + 1: return causal_fwd5_inst<64, 1>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 64 * 16 + 2: return causal_fwd5_inst<64, 2>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 64 * 16 + 3: return causal_fwd5_inst<64, 3>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 64 * 16 + 4: return causal_fwd5_inst<64, 4>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 64 * 16 + 5: return causal_fwd5_inst<64, 5>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 64 * 16 + 6: return causal_fwd5_inst<64, 6>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 128 * 16 + 1: return causal_fwd5_inst<128, 1>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 128 * 16 + 2: return causal_fwd5_inst<128, 2>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 128 * 16 + 3: return causal_fwd5_inst<128, 3>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 128 * 16 + 4: return causal_fwd5_inst<128, 4>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 128 * 16 + 5: return causal_fwd5_inst<128, 5>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
-        case 128 * 16 + 6: return causal_fwd5_inst<128, 6>(Dm, mq, mk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 1: return causal_fwd5_inst<64, 1>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 2: return causal_fwd5_inst<64, 2>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 3: return causal_fwd5_inst<64, 3>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 4: return causal_fwd5_inst<64, 4>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 5: return causal_fwd5_inst<64, 5>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 64 * 16 + 6: return causal_fwd5_inst<64, 6>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 1: return causal_fwd5_inst<128, 1>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 2: return causal_fwd5_inst<128, 2>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 3: return causal_fwd5_inst<128, 3>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 4: return causal_fwd5_inst<128, 4>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 5: return causal_fwd5_inst<128, 5>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
+        case 128 * 16 + 6: return causal_fwd5_inst<128, 6>(Dm, mq, fk, mv, mo, W, S0, seg_len, nseg, err, st);
         default: return cudaErrorInvalidValue;
     }
 }

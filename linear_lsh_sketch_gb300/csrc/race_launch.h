@@ -92,18 +92,26 @@ cudaError_t launch_causal_tc_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t
 bool nc5_supported(const Dims &D);
 int nc5_tile();
 int nc5_sketch_ctas_per_sm(const Dims &D);
+// frows (optional): also every token's bucket-feature row of X, bf16 [BH][N][feature row stride].
 cudaError_t launch_nc5_sketch(const Dims &D, const bf16_t *X, const bf16_t *Y, const float2 *aux, const float *W,
-                              int64_t seg_len, int nsplit, float *part, unsigned *err, cudaStream_t st);
+                              int64_t seg_len, int nsplit, float *part, unsigned *err, cudaStream_t st,
+                              bf16_t *frows = nullptr);
 cudaError_t launch_nc5_readout(const Dims &D, const bf16_t *Q, const float *W, const float *S, bf16_t *O,
                                unsigned *err, cudaStream_t st);
 bool c5_supported(const Dims &D);
-cudaError_t launch_c5_fwd(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const float *W,
+// fk: every key's bucket-feature row, bf16 [BH][N][feature row stride], as the segment-sum pass
+// (launch_nc5_sketch with frows) stores it.
+cudaError_t launch_c5_fwd(const Dims &D, const bf16_t *Q, const bf16_t *fk, const bf16_t *V, const float *W,
                           const float *S0, int64_t seg_len, int nseg, bf16_t *O, unsigned *err, cudaStream_t st);
 bool c5_bwd_supported(const Dims &D);
-cudaError_t launch_c5_bwd_q(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
+// Bytes of one [BH][N][feature row stride] bf16 array of bucket-feature rows.  The query-side
+// pass reads the keys' rows fk (as the forward's segment-sum pass stored them) in place of K, and
+// writes F'_Q = phi(Q_t) / den_t (fq), which the key-side pass reads in place of Q.
+size_t c5_feature_rows_bytes(const Dims &D);
+cudaError_t launch_c5_bwd_q(const Dims &D, const bf16_t *Q, const bf16_t *fk, const bf16_t *V, const bf16_t *dO,
                             const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
-                            float *Gseg, unsigned *err, float *dbpart, cudaStream_t st);
-cudaError_t launch_c5_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
+                            bf16_t *fq, float *Gseg, unsigned *err, float *dbpart, cudaStream_t st);
+cudaError_t launch_c5_bwd_kv(const Dims &D, const bf16_t *fq, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
                              const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
                              bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st);
 // Token segments per (b, h) of the two non-causal tcgen05 backward kernels (their grid's x).

@@ -168,15 +168,51 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity)
     return __syncthreads_or(!ok) != 0;
 }
 
+// 16 bytes from global memory that no kernel writes while this one runs (no L1 allocation).
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Asynchronous global -> shared copies that complete per thread (cp.async): 16 bytes (L2 only)
+// or 8 bytes; commit closes this thread's group, wait_all waits for all of its groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// 16 bytes to global memory without allocating in L1.
+__device__ __forceinline__ void st_global_v4(void *p, uint4 v)
+{
+    asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Stored bucket-feature rows (phi(K) of the keys, F'_Q of the causal backward) hold L R bf16 values
+// padded with zeros to a multiple of 8, so that every row is a whole number of 16-byte chunks.
+__host__ __device__ constexpr int feature_row_stride(int LR) { return (LR + 7) & ~7; }
+
 // Writes one token row of bucket features into an SW128 feature tile ([lr / 64][C][64] bf16,
 // lr = l R + r), for the tables half h owns: tables l with l % 2 == h when R >= 8, else 16-byte
 // chunks (8 / R tables each) with chunk % 2 == h.  z holds the row's projections W x (LPP
 // columns), inv = 1 / |x|; phi^(l)_r = prod_t sigmoid(2 beta u_t v_{r,t}) with
 // u = tanh(z inv) (the softmax over hypercube corners in product form), times `scale`.
-// Tables >= L inside a written chunk are zero.
+// Tables >= L inside a written chunk are zero.  grow (may be null): the token's stored feature
+// row in global memory (feature_row_stride(L R) bf16), which receives the same 16-byte chunks.
 template <int P>
 __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv, float beta, int L, int h,
-                                               float scale, int t, uint32_t ftile)
+                                               float scale, int t, uint32_t ftile, bf16 *grow = nullptr)
 {
     constexpr int R = 1 << P;
     constexpr int LMAX = LPP / P;
@@ -191,11 +227,12 @@ __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv,
 #pragma unroll
                 for (int j = 0; j < R / 8; ++j) {
                     const int c = l * (R / 8) + j;
-                    st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7),
-                                 mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
-                                 mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
-                                 mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
-                                 mma::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
+                    const uint4 v = make_uint4(mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
+                                               mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
+                                               mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
+                                               mma::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
+                    st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7), v.x, v.y, v.z, v.w);
+                    if (grow) st_global_v4(grow + 8 * c, v);
                 }
             }
         }
@@ -222,8 +259,10 @@ __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv,
 #pragma unroll
                     for (int r = 0; r < R; ++r) v[k * R + r] = ph[r] * scale;
                 }
-                st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7), mma::pack_bf16(v[0], v[1]),
-                             mma::pack_bf16(v[2], v[3]), mma::pack_bf16(v[4], v[5]), mma::pack_bf16(v[6], v[7]));
+                const uint4 w = make_uint4(mma::pack_bf16(v[0], v[1]), mma::pack_bf16(v[2], v[3]),
+                                           mma::pack_bf16(v[4], v[5]), mma::pack_bf16(v[6], v[7]));
+                st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7), w.x, w.y, w.z, w.w);
+                if (grow) st_global_v4(grow + 8 * c, w);
             }
         }
     }
@@ -282,7 +321,6 @@ __device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[R])
 // Instruction descriptors.
 __host__ __device__ constexpr uint32_t idesc_proj() { return idesc_bf16(128, LPP, 0, 0); }
 
-// Issues z = X (W_hi + W_lo)^T for a token tile (D / 16 K steps per hyperplane copy).
 // 32 bf16 (64 bytes, packed pairs in o) of one output row to global memory: two 32-byte stores
 // when `wide` (the tensor's base is 32-byte aligned, so every row segment is), else four 16-byte
 // stores.  Full 32-byte sectors halve the store instructions of a row-per-thread epilogue.  The
@@ -306,6 +344,7 @@ __device__ __forceinline__ void store_row32(bf16 *dst, const uint32_t (&o)[16], 
     }
 }
 
+// Issues z = X (W_hi + W_lo)^T for a token tile (D / 16 K steps per hyperplane copy).
 template <int D>
 __device__ __forceinline__ void issue_projection(uint32_t tz, uint32_t xtile, uint32_t whi, uint32_t wlo)
 {
