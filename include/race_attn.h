@@ -89,10 +89,11 @@ size_t race_attn_workspace_bytes(const race_shape *shape, int L, int P, int caus
  * start of each of the library's sequence segments, float32 [B, H, nseg, L*2^P, d+1], where
  * nseg is a function of the shape and of the current device's multiprocessor count (the work
  * is split to fill the device).  For causal bfloat16 problems with d in {64, 128}, P <= 6,
- * L * P <= 32 and L * 2^P <= 64 the state also holds, after the sketches (at the next multiple
- * of 256 bytes), every key's bucket features phi(K_t) as bf16 [B, H, N, F] with F = L * 2^P
- * rounded up to a multiple of 8: the forward computes them once and the backward reads them
- * instead of K.  Returns 0 if the arguments are invalid.  The same holds for
+ * L * P <= 32 and L * 2^P <= 64 the state also holds, after the sketches (each array at the
+ * next multiple of 256 bytes), every key's bucket features phi(K_t) as bf16 [B, H, N, F] with
+ * F = L * 2^P rounded up to a multiple of 8, and every key's 1 / |K_t| as float32 [B, H, N]:
+ * the forward computes them once and the backward reads them instead of recomputing them from
+ * K.  Returns 0 if the arguments are invalid.  The same holds for
  * race_attn_workspace_bytes: size buffers with the device current that will run the calls.
  */
 size_t race_attn_state_bytes(const race_shape *shape, int L, int P, int causal);

@@ -130,8 +130,10 @@ struct Plan {
     size_t off_part = 0, off_sk = 0, off_gpart = 0, off_gsk = 0, off_aux = 0;
     size_t off_db = 0;     // d(loss)/d(beta) partials: [2][BH][db_cap] floats
     size_t off_fq = 0;     // causal tcgen05 backward: F'_Q rows handed from the query to the key side
-    size_t off_fk = 0;     // causal tcgen05 path without `state`: the keys' bucket-feature rows
-    size_t state_fk = 0;   // causal tcgen05 path: offset of the keys' feature rows inside `state`
+    size_t off_fk = 0;     // causal tcgen05 path without `state`: the keys' bucket-feature rows,
+    size_t off_kinv = 0;   //   then their 1 / |k|
+    size_t state_fk = 0;   // causal tcgen05 path: the same two arrays inside `state`
+    size_t state_kinv = 0;
     int64_t db_cap = 0;    // partial slots per (side, b, h): at least every backward kernel's grid x
     size_t ws_fwd = 0, ws_bwd = 0, state = 0;
 };
@@ -197,8 +199,10 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     const size_t sk_bytes = pl.causal ? per_split : per_bh;
     // the causal tcgen05 path keeps every key's bucket features (bf16) from the segment-sum pass
     const size_t fk_bytes = pl.c5 ? c5_feature_rows_bytes(D) : 0;
+    const size_t kinv_bytes = pl.c5 ? (size_t)D.BH * D.N * sizeof(float) : 0;
     pl.off_fk = align256(pl.off_sk + sk_bytes);
-    pl.ws_fwd = align256(pl.off_fk + fk_bytes);
+    pl.off_kinv = align256(pl.off_fk + fk_bytes);
+    pl.ws_fwd = align256(pl.off_kinv + kinv_bytes);
     pl.off_gpart = pl.ws_fwd;
     pl.off_gsk = align256(pl.off_gpart + per_split);
     pl.off_aux = align256(pl.off_gsk + sk_bytes);
@@ -208,7 +212,8 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     const size_t fq_bytes = (pl.c5 && c5_bwd_supported(D)) ? c5_feature_rows_bytes(D) : 0;
     pl.ws_bwd = align256(pl.off_fq + fq_bytes);
     pl.state_fk = align256(sk_bytes);
-    pl.state = pl.c5 ? pl.state_fk + fk_bytes : sk_bytes;
+    pl.state_kinv = align256(pl.state_fk + fk_bytes);
+    pl.state = pl.c5 ? pl.state_kinv + kinv_bytes : sk_bytes;
 
     // every kernel of the chosen path must fit in shared memory
     if (pl.causal) {
@@ -276,7 +281,8 @@ int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float
             // segment sums of the causal sketch = the non-causal sketch of each segment; the pass
             // also stores every key's bucket features, which the chunk kernel reads instead of K
             bf16_t *fk = state ? (bf16_t *)((char *)state + pl.state_fk) : (bf16_t *)(ws + pl.off_fk);
-            RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st, fk));
+            float *kinv = state ? (float *)((char *)state + pl.state_kinv) : (float *)(ws + pl.off_kinv);
+            RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st, fk, kinv));
             RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
             RACE_TRY(launch_c5_fwd(D, Q, fk, V, W, S, pl.seg_len, pl.nsplit, O, err, st));
             return RACE_OK;
@@ -348,11 +354,13 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
         if (c5b || (use_tc<T>(pl) && causal_tc_bwd_supported(D))) {
             // the keys' bucket-feature rows: from the forward's state, or stored again here
             const bf16_t *fk = S ? (const bf16_t *)((const char *)S + pl.state_fk) : (const bf16_t *)(ws + pl.off_fk);
+            const float *kinv = S ? (const float *)((const char *)S + pl.state_kinv) : (const float *)(ws + pl.off_kinv);
             if (!S) {
                 float *Sw = (float *)(ws + pl.off_sk);
                 if (pl.c5)
                     RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st,
-                                               c5b ? (bf16_t *)(ws + pl.off_fk) : nullptr));
+                                               c5b ? (bf16_t *)(ws + pl.off_fk) : nullptr,
+                                               c5b ? (float *)(ws + pl.off_kinv) : nullptr));
                 else
                     RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 1, st));
@@ -368,8 +376,8 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
                                                 db.dbq, st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
             if (c5b)
-                RACE_TRY(launch_c5_bwd_kv(D, fq, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err, db.dbk,
-                                          st));
+                RACE_TRY(launch_c5_bwd_kv(D, fq, fk, kinv, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err,
+                                          db.dbk, st));
             else
                 RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err,
                                                  db.dbk, st));

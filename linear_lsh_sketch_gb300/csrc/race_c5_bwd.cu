@@ -18,11 +18,15 @@
 // swizzled shared tile that serves as B operand (K- and MN-major) and as A operand; the carried
 // G_next is converted each chunk to a bf16 hi + lo shared operand.
 //
-// F'_Q is not recomputed here: the query-side pass, which forms it for its own gradient-sketch
-// sum, writes it out (L R bf16 per token) and this pass reads it instead of Q.
-// Roles: warp 8 issues every TMA copy and MMA; warps 0-3 copy the F'_Q rows into their tile,
-// write dV and convert G; warps 4-7 featurise the K rows, run the Jacobian and write dK.
-// Hand-offs use mbarriers; dK and dV rows go straight from registers to global memory.
+// Nothing of the features is recomputed here: the query-side pass writes F'_Q (L R bf16 per
+// token), and the forward's segment-sum pass stored phi(K) and 1 / |k| for every key; this pass
+// reads those rows.  K is still read, for its projection (the Jacobian's u = tanh(W k / |k|)) and
+// for dK.  The gradient-sketch update of a chunk is issued right after its first product group,
+// so it runs, and its bf16 operand copy is made, while the masks are applied.
+// Roles: warp 8 issues every TMA copy and MMA; warps 0-3 copy the F'_Q and phi(K) rows into
+// their tile and TMEM, write dV and convert G; warps 4-7 take u from the projection, run the
+// Jacobian and write dK.  Hand-offs use mbarriers; dK and dV rows go straight from registers to
+// global memory.
 #include "race_launch.h"
 #include "race_nc5_common.cuh"
 
@@ -48,8 +52,10 @@ constexpr uint32_t T_COLS = 512;
 enum : uint32_t { B_Q, B_K, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_G,
                   B_COUNT };
 
-// Staging of one chunk's F'_Q rows (64-byte slots) and {1/den, c} pairs, copied in a chunk ahead.
-constexpr uint32_t STG_FQ = C * 64, STG = STG_FQ + C * 8;
+// Staging of one chunk's rows, copied in a chunk ahead: F'_Q and phi(K) (64-byte slots), c and
+// 1 / |k| (4 bytes each).
+constexpr uint32_t STG_FQ = 0, STG_FK = C * 64, STG_C = 2 * C * 64, STG_KI = STG_C + C * 4, STG = STG_KI + C * 4;
+constexpr int LPZ = 16;  // projection rows kept per K row (L P <= 16 whenever L R <= 32)
 
 struct BwdLayout {
     uint32_t stage, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, zk, bar, slot, bytes, kbb;
@@ -66,10 +72,10 @@ struct BwdLayout {
         whi = glo + BLK;
         wlo = whi + (uint32_t)(D / 64) * WBLK;
         ncm = wlo + (uint32_t)(D / 64) * WBLK;  // -c as a K-major N = 16 operand (rows 0, 1 = hi, lo)
-        gb = ncm + 4096;                         // G_B fp32 [32]
-        cvec = gb + 128;                         // c_t fp32 [C]
-        zk = cvec + 4 * C;   // z = W x of the K rows, fp32 [LPP][C]
-        bar = zk + 4 * LPP * C;
+        gb = ncm + 4096;                         // G_B fp32 [2 parities][32]
+        cvec = gb + 256;                         // c_t fp32 [C]
+        zk = cvec + 4 * C;   // z = W x of the K rows, fp32 [LPZ][C]
+        bar = zk + 4 * LPZ * C;
         slot = bar + 128;
         bytes = slot + 16;
     }
@@ -78,7 +84,8 @@ struct BwdLayout {
 // DB: also the CTA's key-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
 template <int D, int P, int LT, bool DB>
 __global__ void __launch_bounds__(NTHW, 1)
-    k_causal_bwdkv5(const bf16 *__restrict__ fq_in, const __grid_constant__ CUtensorMap tmK,
+    k_causal_bwdkv5(const bf16 *__restrict__ fq_in, const bf16 *__restrict__ fk_in, const float *__restrict__ kinv_in,
+                    const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
                     const float *__restrict__ W, const float2 *__restrict__ aux, const float *__restrict__ G0,
                     int64_t seg_len, int nseg, bf16 *__restrict__ dK, bf16 *__restrict__ dV,
@@ -170,8 +177,9 @@ __global__ void __launch_bounds__(NTHW, 1)
     __syncthreads();
     fence_after();
 
-    // G (TMEM) -> bf16 hi / lo operand rows d (columns = sketch rows) and fp32 G_B; warps 0-3
-    auto convert_g = [&]() {
+    // G (TMEM) -> bf16 hi / lo operand rows d (columns = sketch rows) and fp32 G_B (buffer
+    // par_out, read by the Jacobian of the chunk that uses this G); warps 0-3
+    auto convert_g = [&](int par_out) {
         uint32_t ar[32], gb0 = 0, gb1 = 0;
         if (t < D) ld32_nw(tlane + T_GT, ar);
         if (q4 == 0) {
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 st_shared_v4(base + Ly.glo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
             }
         }
-        if (q4 == 0) gb[lane] = lane < LR ? uf(gb0) + uf(gb1) : 0.f;  // -sum F'_Q c, c as bf16 hi + lo
+        if (q4 == 0) gb[32 * par_out + lane] = lane < LR ? uf(gb0) + uf(gb1) : 0.f;  // -sum F'_Q c, c as bf16 hi + lo
     };
 
     float db = 0.f;  // this thread's d(loss)/d(beta) share (DB only)
@@ -284,6 +292,15 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma_ts(tmem + T_DVV, tmem + T_FK + 8 * ks, d_glo_k + (uint64_t)(2 * ks), id_dv, true);
                 }
                 commit(bar(B_A));
+                // the gradient sketch G += F'_Q^T [dO | -c] of this chunk (under its own commit: the G
+                // conversion waits for it while the masks are applied)
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
+                    umma(tmem + T_GT, d_do_mt + ko, d_fq_mn + ko, id_gt, true);
+                    umma(tmem + T_GB, d_fq_mn + ko, d_ncm + kk, id_gb, true);
+                }
+                commit(bar(B_G));
                 // group B: masked products
                 if (!(ok = wait_phase(bar(B_MASK), par, abort))) break;
                 fence_after();
@@ -297,9 +314,12 @@ __global__ void __launch_bounds__(NTHW, 1)
                 if (k + 1 < nchunk) {  // group A (the only reader of V) completed before the mask
                     load_tiles(k + 1, 2);
                     ++issued[1];
+                    // dO is last read by group B
+                    if (!(ok = wait_phase(bar(B_B), par, abort))) break;
+                    load_tiles(k + 1, 4);
+                    ++issued[2];
                 }
-                // group C: dxhat (the dK epilogue starts on it), then the gradient sketch update under
-                // its own commit (the G conversion and the dO reload wait for that one)
+                // group C: dxhat, for the dK epilogue
                 if (!(ok = wait_phase(bar(B_JAC), par, abort))) break;
                 fence_after();
                 if (k + 1 < nchunk) {  // the K rows are parked in TMEM by now
@@ -311,18 +331,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma_ts(tmem + T_DV, tmem + T_DZ + 8 * ks, d_wlo + (uint64_t)(ks * 128), id_x, true);
                 }
                 commit(bar(B_C));
-#pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks) {
-                    const uint64_t ko = (uint64_t)(ks * 2048) >> 4, kk = (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 32) >> 4;
-                    umma(tmem + T_GT, d_do_mt + ko, d_fq_mn + ko, id_gt, true);
-                    umma(tmem + T_GB, d_fq_mn + ko, d_ncm + kk, id_gb, true);
-                }
-                commit(bar(B_G));
-                if (k + 1 < nchunk) {  // dO is last read by the gradient sketch update
-                    if (!(ok = wait_phase(bar(B_G), par, abort))) break;
-                    load_tiles(k + 1, 4);
-                    ++issued[2];
-                }
             }
             if (!ok) {
                 atomicOr(err, kErrTimeout);
@@ -336,50 +344,70 @@ __global__ void __launch_bounds__(NTHW, 1)
     } else {
         // ---------------------------------------------------------------- compute warps
         if (h == 0) {
-            convert_g();
+            convert_g(0);
             warp_signal(bar(B_GOP));
         }
-        // F'_Q rows and {1/den, c} of the Q rows, copied into a staging buffer a chunk ahead by the
-        // thread that owns the row; chunks run backwards and only the last one can be partial
+        // Row data of chunk kk (in reverse order), copied into staging buffer kk & 1 a chunk ahead by
+        // the thread that consumes it: F'_Q, phi(K) and c of row t (warps 0-3), 1 / |k| (warps 4-7).
+        // Chunks run backwards and only the last one can be partial.
         const int lrs = feature_row_stride(LR);
         const bf16 *fq_bh = fq_in + bh * Dm.N * lrs;
-        const float2 *aux_bh = aux + bh * Dm.N;
+        const bf16 *fk_bh = fk_in + bh * Dm.N * lrs;
+        const float *c_bh = reinterpret_cast<const float *>(aux + bh * Dm.N) + 1;  // .y of each {1/den, c}
+        const float *kinv_bh = kinv_in + bh * Dm.N;
         auto stage_rows = [&](int kk) {
             const int64_t row = n_begin + (int64_t)(nchunk - 1 - kk) * C + t;
             const uint32_t buf = base + Ly.stage + (uint32_t)(kk & 1) * STG;
             if (row < n_end) {
+                if (h == 0) {
 #pragma unroll
-                for (int ch = 0; ch < LRMAX / 8; ++ch)
-                    if (8 * ch < lrs) cp_async16(buf + t * 64 + 16 * ch, fq_bh + row * lrs + 8 * ch);
-                cp_async8(buf + STG_FQ + t * 8, aux_bh + row);
+                    for (int ch = 0; ch < LRMAX / 8; ++ch) {
+                        if (8 * ch < lrs) {
+                            cp_async16(buf + STG_FQ + t * 64 + 16 * ch, fq_bh + row * lrs + 8 * ch);
+                            cp_async16(buf + STG_FK + t * 64 + 16 * ch, fk_bh + row * lrs + 8 * ch);
+                        }
+                    }
+                    cp_async4(buf + STG_C + t * 4, c_bh + 2 * row);
+                } else {
+                    cp_async4(buf + STG_KI + t * 4, kinv_bh + row);
+                }
             }
             cp_async_commit();
         };
-        if (h == 0 && nchunk > 0) stage_rows(0);
+        if (nchunk > 0) stage_rows(0);
         for (int k = 0; k < nchunk; ++k) {
             const uint32_t par = k & 1;
             const int c = nchunk - 1 - k;
             const int64_t n0 = n_begin + (int64_t)c * C;
             const int cnt = (int)min((int64_t)C, n_end - n0);
             const bool live = t < cnt;
+            const uint32_t buf = base + Ly.stage + par * STG;
             float inv = 0.f;  // 1 / |K row| (warps 4-7)
-            float z[LPP];
             // K rows keep z in shared memory; with L compiled in they also keep u = tanh(z inv) in
             // registers (L P of them), otherwise the Jacobian recomputes it from z
-            float uk[LT > 0 ? LPP : 1];
+            float uk[LT > 0 ? LPZ : 1];
+            cp_async_wait_all();
             if (h == 0) {
-                // F'_Q row t -> shared tile row t (zero past the end);  -c_t -> rows 0 / 1 of the
-                // mass operand; then the next chunk's rows into the other staging buffer
-                cp_async_wait_all();
-                const uint32_t buf = base + Ly.stage + par * STG;
+                // F'_Q row t -> shared tile row t and phi(K) row t -> TMEM (zero past the end);
+                // -c_t -> rows 0 / 1 of the mass operand; then the next chunk's rows
+                uint32_t fk0[8], fk1[8];  // phi(K) row t as bf16 pairs, L R <= 32
 #pragma unroll
                 for (int ch = 0; ch < LRMAX / 8; ++ch) {
-                    if (8 * ch < lrs) {
-                        const uint4 v = live ? ld_shared_v4(buf + t * 64 + 16 * ch) : make_uint4(0u, 0u, 0u, 0u);
-                        st_shared_v4(base + Ly.fq + sw_chunk(t, ch), v.x, v.y, v.z, v.w);
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u), w = make_uint4(0u, 0u, 0u, 0u);
+                    if (8 * ch < lrs && live) {
+                        v = ld_shared_v4(buf + STG_FQ + t * 64 + 16 * ch);
+                        w = ld_shared_v4(buf + STG_FK + t * 64 + 16 * ch);
                     }
+                    if (8 * ch < lrs) st_shared_v4(base + Ly.fq + sw_chunk(t, ch), v.x, v.y, v.z, v.w);
+                    uint32_t *dst = ch < 2 ? fk0 + 4 * ch : fk1 + 4 * (ch - 2);
+                    dst[0] = w.x;
+                    dst[1] = w.y;
+                    dst[2] = w.z;
+                    dst[3] = w.w;
                 }
-                const float cv = live ? reinterpret_cast<const float2 *>(sm + Ly.stage + par * STG + STG_FQ)[t].y : 0.f;
+                stn<8>(tlane + T_FK, fk0);
+                stn<8>(tlane + T_FK + 8, fk1);
+                const float cv = live ? reinterpret_cast<const float *>(sm + Ly.stage + par * STG + STG_C)[t] : 0.f;
                 if (k + 1 < nchunk) stage_rows(k + 1);
                 const float mcv = -cv;
                 const bf16 mhi = __float2bfloat16_rn(mcv);
@@ -388,51 +416,25 @@ __global__ void __launch_bounds__(NTHW, 1)
                 *reinterpret_cast<bf16 *>(mt + sw_elem(0, t & 63)) = mhi;
                 *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
                 cvec[t] = cv;
+                wait_st();
             } else {
-                // the K row this thread featurises: norm, then z from the projection
-                if (!wait_phase(bar(B_K), par, abort)) break;
-                {
-                    const float ss = half_sumsq<D>(base + Ly.k, t, 0) + half_sumsq<D>(base + Ly.k, t, 1);
-                    inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-                }
+                // this thread's K row: 1 / |k| as stored, z = W k from the projection, u = tanh(z / |k|)
+                inv = live ? reinterpret_cast<const float *>(sm + Ly.stage + par * STG + STG_KI)[t] : 0.f;
+                if (k + 1 < nchunk) stage_rows(k + 1);
                 if (!wait_phase(bar(B_PROJ), par, abort)) break;
                 fence_after();
+                float z[LPZ];
                 {
-                    float a[32];
-                    ld32(tlane + T_ZK, a);
+                    float a[LPZ];
+                    ldn<LPZ>(tlane + T_ZK, a);
 #pragma unroll
-                    for (int j = 0; j < LPP; ++j) z[j] = a[j];
+                    for (int j = 0; j < LPZ; ++j) z[j] = a[j];
                 }
-                // F_K -> TMEM (A operand); keep u
 #pragma unroll
-                for (int j = 0; j < LMAX * P; ++j)
+                for (int j = 0; j < LPZ; ++j) {
                     if (j < LP) zk_s[j * C + t] = z[j];
-                float phk[LRMAX];
-#pragma unroll
-                for (int j = 0; j < LRMAX; ++j) phk[j] = 0.f;
-#pragma unroll
-                for (int l = 0; l < LMAX; ++l) {
-                    if (l < L && l * R < LRMAX) {
-                        float u[P], ph[R];
-#pragma unroll
-                        for (int p = 0; p < P; ++p) {
-                            u[p] = tc::tanh_abs(z[l * P + p] * inv);
-                            if constexpr (LT > 0) uk[l * P + p] = u[p];
-                        }
-                        tc::bucket_probs<P>(u, beta, ph);
-#pragma unroll
-                        for (int r = 0; r < R; ++r)
-                            if (l * R + r < LRMAX) phk[l * R + r] = ph[r];
-                    }
+                    if constexpr (LT > 0) uk[j] = j < LP ? tc::tanh_abs(z[j] * inv) : 0.f;
                 }
-                uint32_t r[8];
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(phk[16 * b + 2 * j], phk[16 * b + 2 * j + 1]);
-                    stn<8>(tlane + T_FK + 8 * b, r);
-                }
-                wait_st();
             }
             if (!group_sync(bar(B_CS1), par, abort)) break;  // c_t visible to every compute warp
             warp_signal(bar(B_FEAT));
@@ -472,6 +474,14 @@ __global__ void __launch_bounds__(NTHW, 1)
             }
             wait_st();
             warp_signal(bar(B_MASK));
+            if (h == 0) {
+                // the gradient sketch with this chunk added -> the next chunk's bf16 operand and G_B
+                // (its update was issued right after group A and ran during the masks)
+                if (!wait_phase(bar(B_G), par, abort)) break;
+                fence_after();
+                convert_g(par ^ 1);
+                warp_signal(bar(B_GOP));
+            }
             if (!wait_phase(bar(B_B), par, abort)) break;
             fence_after();
             float zdz = 0.f;  // x . dxhat of the K row
@@ -491,7 +501,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     float a[32];
                     ld32(tlane + T_DP, a);
 #pragma unroll
-                    for (int j = 0; j < LRMAX; ++j) dph[j] = a[j] + gb[j];
+                    for (int j = 0; j < LRMAX; ++j) dph[j] = a[j] + gb[32 * par + j];
                 }
                 float dz[LPP];
 #pragma unroll
@@ -502,7 +512,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                         float u[P], ph[R], dp[R];
 #pragma unroll
                         for (int p = 0; p < P; ++p)
-                            u[p] = LT > 0 ? uk[(l * P + p) % (LT > 0 ? LPP : 1)] : tc::tanh_abs(zk_s[(l * P + p) * C + t] * inv);
+                            u[p] = LT > 0 ? uk[(l * P + p) % (LT > 0 ? LPZ : 1)] : tc::tanh_abs(zk_s[(l * P + p) * C + t] * inv);
                         tc::bucket_probs<P>(u, beta, ph);
 #pragma unroll
                         for (int r = 0; r < R; ++r) dp[r] = l * R + r < LRMAX ? dph[l * R + r] : 0.f;
@@ -543,11 +553,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_DVR));  // dV columns (shared with z) read
             }
-            // the K rows' dK needs dxhat; the Q rows' G conversion needs the gradient sketch update
-            if (!wait_phase(bar(h ? B_C : B_G), par, abort)) break;
-            fence_after();
             if (h == 1) {
                 // dK row t = inv (dxhat - x inv^2 (x . dxhat)), x parked in TMEM; straight to global memory
+                if (!wait_phase(bar(B_C), par, abort)) break;
+                fence_after();
                 const float kk = inv * inv * zdz;
                 bf16 *dst = dK + off + (n0 + t) * D;
 #pragma unroll
@@ -564,9 +573,6 @@ __global__ void __launch_bounds__(NTHW, 1)
                         o[j] = mma::pack_bf16(inv * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), inv * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
                     if (live) store_row32(dst + 32 * pass, o, wide);
                 }
-            } else {
-                convert_g();
-                warp_signal(bar(B_GOP));
             }
             fence_before();
             if (!group_sync(bar(B_CS2), par, abort)) break;  // gb / TMEM reads done before the next chunk
@@ -1199,7 +1205,8 @@ bool c5_bwd_supported(const Dims &D)
 namespace {
 
 template <int D, int P, int LT>
-cudaError_t bwdkv5_launch(const Dims &Dm, const bf16_t *fq, const CUtensorMap &mk, const CUtensorMap &mv,
+cudaError_t bwdkv5_launch(const Dims &Dm, const bf16_t *fq, const bf16_t *fk, const float *kinv, const CUtensorMap &mk,
+                          const CUtensorMap &mv,
                           const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
                           int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
@@ -1209,19 +1216,21 @@ cudaError_t bwdkv5_launch(const Dims &Dm, const bf16_t *fq, const CUtensorMap &m
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_bwd_kv", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5b::NTHW), smem,
-                         st, fq, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart);
+                         st, fq, fk, kinv, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart);
 }
 
 // (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
 template <int D, int P>
-cudaError_t bwdkv5_inst(const Dims &Dm, const bf16_t *fq, const CUtensorMap &mk, const CUtensorMap &mv,
+cudaError_t bwdkv5_inst(const Dims &Dm, const bf16_t *fq, const bf16_t *fk, const float *kinv, const CUtensorMap &mk,
+                        const CUtensorMap &mv,
                         const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
                         int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
 {
     if constexpr (D == 128 && P == 3)
         if (Dm.L == 3)
-            return bwdkv5_launch<D, P, 3>(Dm, fq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
-    return bwdkv5_launch<D, P, 0>(Dm, fq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+            return bwdkv5_launch<D, P, 3>(Dm, fq, fk, kinv, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart,
+                                          st);
+    return bwdkv5_launch<D, P, 0>(Dm, fq, fk, kinv, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
 }
 
 template <int D, int P, int LT>
@@ -1275,9 +1284,10 @@ cudaError_t launch_c5_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *fk, c
 #undef RACE_C5Q_CASE
 }
 
-cudaError_t launch_c5_bwd_kv(const Dims &Dm, const bf16_t *fq, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
-                             const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
-                             bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
+cudaError_t launch_c5_bwd_kv(const Dims &Dm, const bf16_t *fq, const bf16_t *fk, const float *kinv, const bf16_t *K,
+                             const bf16_t *V, const bf16_t *dO, const float2 *aux, const float *W, const float *G0,
+                             int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart,
+                             cudaStream_t st)
 {
     CUtensorMap mk, mv, mdo;
     cudaError_t e = make_token_map(&mk, K, Dm);
@@ -1285,7 +1295,7 @@ cudaError_t launch_c5_bwd_kv(const Dims &Dm, const bf16_t *fq, const bf16_t *K, 
     if (e == cudaSuccess) e = make_token_map(&mdo, dO, Dm);
     if (e != cudaSuccess) return e;
 #define RACE_C5KV_CASE(DD, PP) \
-    case DD * 16 + PP: return bwdkv5_inst<DD, PP>(Dm, fq, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+    case DD * 16 + PP: return bwdkv5_inst<DD, PP>(Dm, fq, fk, kinv, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
     switch (Dm.d * 16 + Dm.P) {
         RACE_C5B_SHAPES(RACE_C5KV_CASE)
         default: return cudaErrorInvalidValue;

@@ -92,10 +92,11 @@ cudaError_t launch_causal_tc_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t
 bool nc5_supported(const Dims &D);
 int nc5_tile();
 int nc5_sketch_ctas_per_sm(const Dims &D);
-// frows (optional): also every token's bucket-feature row of X, bf16 [BH][N][feature row stride].
+// frows, invrows (optional, together): also every token's bucket-feature row of X, bf16
+// [BH][N][feature row stride], and its 1 / |x|, fp32 [BH][N].
 cudaError_t launch_nc5_sketch(const Dims &D, const bf16_t *X, const bf16_t *Y, const float2 *aux, const float *W,
                               int64_t seg_len, int nsplit, float *part, unsigned *err, cudaStream_t st,
-                              bf16_t *frows = nullptr);
+                              bf16_t *frows = nullptr, float *invrows = nullptr);
 cudaError_t launch_nc5_readout(const Dims &D, const bf16_t *Q, const float *W, const float *S, bf16_t *O,
                                unsigned *err, cudaStream_t st);
 bool c5_supported(const Dims &D);
@@ -111,9 +112,12 @@ size_t c5_feature_rows_bytes(const Dims &D);
 cudaError_t launch_c5_bwd_q(const Dims &D, const bf16_t *Q, const bf16_t *fk, const bf16_t *V, const bf16_t *dO,
                             const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
                             bf16_t *fq, float *Gseg, unsigned *err, float *dbpart, cudaStream_t st);
-cudaError_t launch_c5_bwd_kv(const Dims &D, const bf16_t *fq, const bf16_t *K, const bf16_t *V, const bf16_t *dO,
-                             const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
-                             bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st);
+// The key-side pass also reads the keys' feature rows fk and their 1 / |k| (kinv), as the
+// forward's segment-sum pass stored them, instead of normalising and featurising K again.
+cudaError_t launch_c5_bwd_kv(const Dims &D, const bf16_t *fq, const bf16_t *fk, const float *kinv, const bf16_t *K,
+                             const bf16_t *V, const bf16_t *dO, const float2 *aux, const float *W, const float *G0,
+                             int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart,
+                             cudaStream_t st);
 // Token segments per (b, h) of the two non-causal tcgen05 backward kernels (their grid's x).
 int nc5_bwd_nseg(const Dims &D);
 cudaError_t launch_nc5_bwd_query(const Dims &D, const bf16_t *Q, const bf16_t *dO, const float *W, const float *S,

@@ -178,8 +178,8 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void *p)
     return v;
 }
 
-// Asynchronous global -> shared copies that complete per thread (cp.async): 16 bytes (L2 only)
-// or 8 bytes; commit closes this thread's group, wait_all waits for all of its groups.
+// Asynchronous global -> shared copies that complete per thread (cp.async): 16 bytes (L2 only),
+// 8 or 4 bytes; commit closes this thread's group, wait_all waits for all of its groups.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
@@ -187,6 +187,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }

@@ -64,14 +64,16 @@ enum : uint32_t { SB_X0, SB_X1, SB_Y0, SB_Y1, SB_P0, SB_P1, SB_S0, SB_S1, SB_F0,
 
 // mode 0: X = K, Y = V, m = 1.  mode 1: X = Q, Y = dO, Phi scaled by aux.x = 1/den, m = -aux.y
 // (= -c, split into bf16 hi and lo rows).  part: [BH][nsplit][LR][d + 1] fp32.  frows (may be
-// null): every token's feature row, bf16 [BH][N][feature_row_stride(LR)], for later passes.
+// null): every token's feature row, bf16 [BH][N][feature_row_stride(LR)], and its 1 / |x|, fp32
+// [BH][N] (invrows), for later passes.
 // Warp 8 issues the TMA copies and MMAs; the projection of tile i + 1 is issued ahead of the
 // sketch product of tile i, so the compute warps featurise tile i + 1 while it runs.
 template <int D, int P, int LT>
 __global__ void __launch_bounds__(NTHW, 1)
     k_sketch5(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY, Dims Dm,
               const float *__restrict__ W, const float2 *__restrict__ aux, int64_t seg_len, int nsplit,
-              float *__restrict__ part, bf16 *__restrict__ frows, unsigned *__restrict__ err, int mode)
+              float *__restrict__ part, bf16 *__restrict__ frows, float *__restrict__ invrows,
+              unsigned *__restrict__ err, int mode)
 {
     constexpr int KB = D / 64;
     extern __shared__ unsigned char smem_raw[];
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 }
             }
             bf16 *grow = (frows != nullptr && live) ? frows + (bh * Dm.N + n0 + t) * feature_row_stride(Dm.LR) : nullptr;
+            if (grow != nullptr && h == 0) invrows[bh * Dm.N + n0 + t] = inv;
             write_features<P>(z, inv, Dm.beta, LT > 0 ? LT : Dm.L, h, scale, t, base + Ly.f + (i % nf) * Ly.fbytes,
                               grow);
             warp_signal(bar(SB_F0 + s));
@@ -563,8 +566,8 @@ cudaError_t prep_smem(K kern, size_t bytes)
 
 template <int D, int P, int LT>
 cudaError_t sketch_launch(const Dims &Dm, const CUtensorMap &mx, const CUtensorMap &my, const float *W,
-                          const float2 *aux, int64_t seg_len, int nsplit, float *part, bf16_t *frows, unsigned *err,
-                          int mode, cudaStream_t st)
+                          const float2 *aux, int64_t seg_len, int nsplit, float *part, bf16_t *frows, float *invrows,
+                          unsigned *err, int mode, cudaStream_t st)
 {
     const nc5::SketchLayout Ly(D, Dm.LR);
     const size_t smem = Ly.bytes + 1024;
@@ -572,22 +575,23 @@ cudaError_t sketch_launch(const Dims &Dm, const CUtensorMap &mx, const CUtensorM
     cudaError_t e = prep_smem(kern, smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(mode ? "tc5_sketch_grad" : "tc5_sketch_keys", kern, dim3(nsplit, (unsigned)Dm.BH),
-                         dim3(nc5::NTHW), smem, st, mx, my, Dm, W, aux, seg_len, nsplit, part, frows, err, mode);
+                         dim3(nc5::NTHW), smem, st, mx, my, Dm, W, aux, seg_len, nsplit, part, frows, invrows, err,
+                         mode);
 }
 
 // The named workloads' shapes run with L compiled in: (d, P, L) = (128, 3, 3), (64, 3, 3), (128, 6, 4).
 template <int D, int P>
 cudaError_t sketch_inst(const Dims &Dm, const CUtensorMap &mx, const CUtensorMap &my, const float *W,
-                        const float2 *aux, int64_t seg_len, int nsplit, float *part, bf16_t *frows, unsigned *err,
-                        int mode, cudaStream_t st)
+                        const float2 *aux, int64_t seg_len, int nsplit, float *part, bf16_t *frows, float *invrows,
+                        unsigned *err, int mode, cudaStream_t st)
 {
     if constexpr (P == 3)
         if (Dm.L == 3)
-            return sketch_launch<D, P, 3>(Dm, mx, my, W, aux, seg_len, nsplit, part, frows, err, mode, st);
+            return sketch_launch<D, P, 3>(Dm, mx, my, W, aux, seg_len, nsplit, part, frows, invrows, err, mode, st);
     if constexpr (D == 128 && P == 6)
         if (Dm.L == 4)
-            return sketch_launch<D, P, 4>(Dm, mx, my, W, aux, seg_len, nsplit, part, frows, err, mode, st);
-    return sketch_launch<D, P, 0>(Dm, mx, my, W, aux, seg_len, nsplit, part, frows, err, mode, st);
+            return sketch_launch<D, P, 4>(Dm, mx, my, W, aux, seg_len, nsplit, part, frows, invrows, err, mode, st);
+    return sketch_launch<D, P, 0>(Dm, mx, my, W, aux, seg_len, nsplit, part, frows, invrows, err, mode, st);
 }
 
 template <int D, int P, int LT>
@@ -644,14 +648,15 @@ cudaError_t readout_inst(const Dims &Dm, const CUtensorMap &mq, const CUtensorMa
 
 cudaError_t launch_nc5_sketch(const Dims &Dm, const bf16_t *X, const bf16_t *Y, const float2 *aux, const float *W,
                               int64_t seg_len, int nsplit, float *part, unsigned *err, cudaStream_t st,
-                              bf16_t *frows)
+                              bf16_t *frows, float *invrows)
 {
     CUtensorMap mx, my;
     cudaError_t e = make_token_map(&mx, X, Dm);
     if (e == cudaSuccess) e = make_token_map(&my, Y, Dm);
     if (e != cudaSuccess) return e;
     const int mode = aux ? 1 : 0;
-    RACE_NC5_DISPATCH(sketch_inst, Dm, mx, my, W, aux, seg_len, nsplit, part, frows, err, mode, st)
+    if ((frows == nullptr) != (invrows == nullptr)) return cudaErrorInvalidValue;
+    RACE_NC5_DISPATCH(sketch_inst, Dm, mx, my, W, aux, seg_len, nsplit, part, frows, invrows, err, mode, st)
 }
 
 cudaError_t launch_nc5_readout(const Dims &Dm, const bf16_t *Q, const float *W, const float *S, bf16_t *O,

@@ -53,9 +53,10 @@ def test_sizes(lib):
     # the saved sketch is one [LR, d+1] float32 block per (b, h) when non-causal
     assert lib.race_attn_state_bytes(s, 3, 3, 0) == 2 * 24 * 65 * 4
     # causal float32: whole segment sketches only; causal bf16 (tcgen05 path): the segment
-    # sketches, then every key's bucket features (bf16, L R = 24 per token) at a 256-byte offset
+    # sketches, then every key's bucket features (bf16, L R = 24 per token) at a 256-byte offset,
+    # then every key's 1 / |k| (float32), again at a 256-byte offset
     assert lib.race_attn_state_bytes(shape(lib, dtype=0), 3, 3, 1) % (24 * 65 * 4) == 0
-    sk = lib.race_attn_state_bytes(s, 3, 3, 1) - 2 * 100 * 24 * 2
+    sk = lib.race_attn_state_bytes(s, 3, 3, 1) - 2 * 100 * 4 - (2 * 100 * 24 * 2 + 255) // 256 * 256
     nseg = sk // (2 * 24 * 65 * 4)
     assert sk % 256 == 0 and nseg >= 1 and sk - 256 < nseg * 2 * 24 * 65 * 4 <= sk
     # sizes depend on the shape only

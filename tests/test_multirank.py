@@ -73,6 +73,10 @@ def test_kernel_table():
     t = bench.kernel_table(prof, w, 6800.0)
     assert abs(sum(r["share"] for r in t.values()) - 1.0) < 1e-12
     fwd = t["tc5_causal_fwd"]
-    want = 4 * w.d * 2 * w.B * w.H * w.N / (9.0 / 1000.0) / 1e9
+    # reads Q and V and the keys' stored feature rows (L R = 24 bf16), writes O
+    want = (3 * w.d * 2 + 24 * 2) * w.B * w.H * w.N / (9.0 / 1000.0) / 1e9
     assert abs(fwd["achieved_gbs"] - want) < 1e-6 * want and abs(fwd["frac"] - want / 6800.0) < 1e-12
+    # its share of the step's algorithmic bytes: Q, K, V in and O out
+    alg = 4 * w.d * 2 * w.B * w.H * w.N / (9.0 / 1000.0) / 1e9
+    assert abs(fwd["alg_gbs"] - alg) < 1e-6 * alg
     assert "frac" not in t["combine"] and t["combine"]["ms_per_launch"] == 0.05
