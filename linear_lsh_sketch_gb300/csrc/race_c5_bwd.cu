@@ -37,33 +37,43 @@ using namespace race::nc5;
 
 constexpr int NTHW = NTH + 32;
 
-// TMEM columns (512 allocated; L R <= 32).
-constexpr uint32_t T_SC = 0;     // F_K F'_Q^T, then P2 as bf16 pairs (in place, per half)
-constexpr uint32_t T_DV = 128;   // V dO^T, then M2 as bf16 pairs (in place), then dxhat
-constexpr uint32_t T_DVV = 256;  // dV (d columns)
-constexpr uint32_t T_ZK = 288;   // K-row projections (dead before dV is written)
-constexpr uint32_t T_DP = 384;   // dphi_K (L R columns)
-constexpr uint32_t T_FK = 416;   // F_K as bf16 pairs (A operand), 16 columns
-constexpr uint32_t T_DZ = 432;   // dz as bf16 pairs (A operand), 16 columns
-constexpr uint32_t T_GT = 448;   // G^T (lanes = d), 32 columns
-constexpr uint32_t T_GB = 480;   // G_B (lanes = sketch row), 16 columns (column 0 used)
+// TMEM columns (512 allocated) for sketch widths L R <= LRM (32, or 64 when d = 64).
+template <int D, int LRM>
+struct KvCols {
+    static constexpr uint32_t SC = 0;          // F_K F'_Q^T, then P2 as bf16 pairs (in place, per half)
+    static constexpr uint32_t DV = 128;        // V dO^T, then M2 as bf16 pairs (in place), then dxhat
+    static constexpr uint32_t DVV = 256;       // dV (d columns)
+    static constexpr uint32_t ZK = 288;        // K-row projections, 32 columns (dead before dV is written)
+    static constexpr uint32_t DP = DVV + D;    // dphi_K (LRM columns)
+    static constexpr uint32_t FK = DP + LRM;   // F_K as bf16 pairs (A operand), LRM / 2 columns
+    static constexpr uint32_t DZ = FK + LRM / 2;  // dz as bf16 pairs (A operand), 16 columns
+    static constexpr uint32_t GT = DZ + 16;    // G^T (lanes = d), LRM columns
+    static constexpr uint32_t GB = GT + LRM;   // G_B (lanes = sketch row), 16 columns (0 and 1 used)
+    static_assert(GB + 16 <= 512 && ZK + 32 <= DVV + D, "key-side TMEM budget");
+};
 constexpr uint32_t T_COLS = 512;
 
 enum : uint32_t { B_Q, B_K, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_GOP, B_DVR, B_CS1, B_CS2, B_G,
                   B_COUNT };
 
-// Staging of one chunk's rows, copied in a chunk ahead: F'_Q and phi(K) (64-byte slots), c and
-// 1 / |k| (4 bytes each).
-constexpr uint32_t STG_FQ = 0, STG_FK = C * 64, STG_C = 2 * C * 64, STG_KI = STG_C + C * 4, STG = STG_KI + C * 4;
-constexpr int LPZ = 16;  // projection rows kept per K row (L P <= 16 whenever L R <= 32)
+// Staging of one chunk's rows, copied in a chunk ahead: F'_Q and phi(K) (2 LRM-byte slots), c
+// and 1 / |k| (4 bytes each); z of the K rows keeps LP <= LPZ rows (L P <= 16 whenever L R <= 32).
+template <int LRM>
+struct KvStage {
+    static constexpr uint32_t SLOT = 2 * LRM;
+    static constexpr uint32_t FQ = 0, FK = C * SLOT, CV = 2 * C * SLOT, KI = CV + C * 4, BYTES = KI + C * 4;
+    static constexpr int LPZ = LRM == 64 ? 32 : 16;
+};
 
 struct BwdLayout {
     uint32_t stage, k, v, dO, fq, ghi, glo, whi, wlo, ncm, gb, cvec, zk, bar, slot, bytes, kbb;
-    __host__ __device__ BwdLayout(int D)
+    __host__ __device__ BwdLayout(int D, int LRM)
     {
+        const uint32_t stg = (uint32_t)C * (4 * LRM + 8);
+        const uint32_t lpz = LRM == 64 ? 32 : 16;
         kbb = (uint32_t)(D / 64) * BLK;
         stage = 0;  // two staging buffers
-        k = stage + 2 * STG;
+        k = stage + 2 * stg;
         v = k + kbb;
         dO = v + kbb;
         fq = dO + kbb;  // F'_Q [t][lr], one 64-column block
@@ -72,17 +82,18 @@ struct BwdLayout {
         whi = glo + BLK;
         wlo = whi + (uint32_t)(D / 64) * WBLK;
         ncm = wlo + (uint32_t)(D / 64) * WBLK;  // -c as a K-major N = 16 operand (rows 0, 1 = hi, lo)
-        gb = ncm + 4096;                         // G_B fp32 [2 parities][32]
-        cvec = gb + 256;                         // c_t fp32 [C]
-        zk = cvec + 4 * C;   // z = W x of the K rows, fp32 [LPZ][C]
-        bar = zk + 4 * LPZ * C;
+        gb = ncm + 4096;                         // G_B fp32 [2 parities][LRM]
+        cvec = gb + 8 * LRM;                     // c_t fp32 [C]
+        zk = cvec + 4 * C;   // z = W x of the K rows, fp32 [lpz][C]
+        bar = zk + 4 * lpz * C;
         slot = bar + 128;
         bytes = slot + 16;
     }
 };
 
-// DB: also the CTA's key-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
-template <int D, int P, int LT, bool DB>
+// DB: also the CTA's key-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].  LRM: the
+// widest L R the instance supports (32, or 64 when d = 64).
+template <int D, int P, int LT, int LRM, bool DB>
 __global__ void __launch_bounds__(NTHW, 1)
     k_causal_bwdkv5(const bf16 *__restrict__ fq_in, const bf16 *__restrict__ fk_in, const float *__restrict__ kinv_in,
                     const __grid_constant__ CUtensorMap tmK,
@@ -94,12 +105,19 @@ __global__ void __launch_bounds__(NTHW, 1)
     constexpr int KB = D / 64;
     constexpr int R = 1 << P;
     constexpr int LMAX = LPP / P;
-    constexpr int LRMAX = 32;  // sketch rows this kernel supports
+    constexpr int LRMAX = LRM;  // sketch rows this instance supports
+    using Cols = KvCols<D, LRM>;
+    constexpr uint32_t T_SC = Cols::SC, T_DV = Cols::DV, T_DVV = Cols::DVV, T_ZK = Cols::ZK, T_DP = Cols::DP;
+    constexpr uint32_t T_FK = Cols::FK, T_DZ = Cols::DZ, T_GT = Cols::GT, T_GB = Cols::GB;
+    using Stg = KvStage<LRM>;
+    constexpr uint32_t STG_FQ = Stg::FQ, STG_FK = Stg::FK, STG_C = Stg::CV, STG_KI = Stg::KI, STG = Stg::BYTES;
+    constexpr uint32_t SLOT = Stg::SLOT;
+    constexpr int LPZ = Stg::LPZ;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023) & ~1023u;
     unsigned char *sm = smem_raw + (base - raw);
-    const BwdLayout Ly(D);
+    const BwdLayout Ly(D, LRM);
     auto bar = [&](uint32_t i) { return base + Ly.bar + 8 * i; };
     volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
     float *gb = reinterpret_cast<float *>(sm + Ly.gb);
@@ -169,7 +187,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             stn<2>(tlane + T_GB, m);
         } else {
             const uint32_t zr[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            for (int c0 = 0; c0 < 32; c0 += 8) stn<8>(tlane + T_FK + c0, zr);  // T_FK and T_DZ
+            for (int c0 = 0; c0 < LRMAX / 2 + 16; c0 += 8) stn<8>(tlane + T_FK + c0, zr);  // T_FK and T_DZ
         }
         wait_st();
     }
@@ -177,38 +195,74 @@ __global__ void __launch_bounds__(NTHW, 1)
     __syncthreads();
     fence_after();
 
-    // G (TMEM) -> bf16 hi / lo operand rows d (columns = sketch rows) and fp32 G_B (buffer
-    // par_out, read by the Jacobian of the chunk that uses this G); warps 0-3
+    // G (TMEM) -> bf16 hi / lo operand rows d (columns = sketch rows, 32 at a time) and fp32 G_B
+    // (buffer par_out, read by the Jacobian of the chunk that uses this G); warps 0-3
     auto convert_g = [&](int par_out) {
-        uint32_t ar[32], gb0 = 0, gb1 = 0;
-        if (t < D) ld32_nw(tlane + T_GT, ar);
-        if (q4 == 0) {
-            ld1_nw(tlane + T_GB, gb0);
-            ld1_nw(tlane + T_GB + 1, gb1);
-        }
-        wait_ld();
-        reg_fence(ar);
-        reg_fence1(gb0);
-        reg_fence1(gb1);
-        if (t < D) {
-            float a[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = uf(ar[j]);
-            uint32_t hw[16], lw[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float x0 = 2 * j < LR ? a[2 * j] : 0.f, x1 = 2 * j + 1 < LR ? a[2 * j + 1] : 0.f;
-                const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-                lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+        if constexpr (LRMAX == 32) {
+            uint32_t ar[32], gb0 = 0, gb1 = 0;
+            if (t < D) ld32_nw(tlane + T_GT, ar);
+            if (q4 == 0) {
+                ld1_nw(tlane + T_GB, gb0);
+                ld1_nw(tlane + T_GB + 1, gb1);
             }
+            wait_ld();
+            reg_fence(ar);
+            reg_fence1(gb0);
+            reg_fence1(gb1);
+            if (t < D) {
+                float a[32];
 #pragma unroll
-            for (int c = 0; c < LRMAX / 8; ++c) {
-                st_shared_v4(base + Ly.ghi + sw_chunk(t, c), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
-                st_shared_v4(base + Ly.glo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+                for (int j = 0; j < 32; ++j) a[j] = uf(ar[j]);
+                uint32_t hw[16], lw[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float x0 = 2 * j < LR ? a[2 * j] : 0.f, x1 = 2 * j + 1 < LR ? a[2 * j + 1] : 0.f;
+                    const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                    hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                    lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    st_shared_v4(base + Ly.ghi + sw_chunk(t, c), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                    st_shared_v4(base + Ly.glo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+                }
+            }
+            if (q4 == 0) gb[32 * par_out + lane] = lane < LR ? uf(gb0) + uf(gb1) : 0.f;  // -sum F'_Q c, c as hi + lo
+        } else {
+#pragma unroll
+            for (int half = 0; half < LRMAX / 32; ++half) {
+                uint32_t ar[32];
+                if (t < D) ld32_nw(tlane + T_GT + 32 * half, ar);
+                wait_ld();
+                reg_fence(ar);
+                if (t < D) {
+                    uint32_t hw[16], lw[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int c0 = 32 * half + 2 * j;
+                        const float x0 = c0 < LR ? uf(ar[2 * j]) : 0.f, x1 = c0 + 1 < LR ? uf(ar[2 * j + 1]) : 0.f;
+                        const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                        hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                        lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int ch = 4 * half + c;
+                        st_shared_v4(base + Ly.ghi + sw_chunk(t, ch), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                        st_shared_v4(base + Ly.glo + sw_chunk(t, ch), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+                    }
+                }
+            }
+            if (32 * q4 < LRMAX) {  // lane = sketch row: -sum F'_Q c, c as bf16 hi + lo
+                uint32_t gb0 = 0, gb1 = 0;
+                ld1_nw(tlane + T_GB, gb0);
+                ld1_nw(tlane + T_GB + 1, gb1);
+                wait_ld();
+                reg_fence1(gb0);
+                reg_fence1(gb1);
+                gb[LRMAX * par_out + t] = t < LR ? uf(gb0) + uf(gb1) : 0.f;
             }
         }
-        if (q4 == 0) gb[32 * par_out + lane] = lane < LR ? uf(gb0) + uf(gb1) : 0.f;  // -sum F'_Q c, c as bf16 hi + lo
     };
 
     float db = 0.f;  // this thread's d(loss)/d(beta) share (DB only)
@@ -242,12 +296,12 @@ __global__ void __launch_bounds__(NTHW, 1)
             }
             constexpr uint32_t id_sc = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t id_dvo = idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t id_dp = idesc_bf16(128, 32, 0, 1);
+            constexpr uint32_t id_dp = idesc_bf16(128, LRMAX, 0, 1);
             constexpr uint32_t id_dv = idesc_bf16(128, D, 0, 0);
             constexpr uint32_t id_pdo = idesc_bf16(128, D, 0, 1);
-            constexpr uint32_t id_mf = idesc_bf16(128, 32, 0, 1);
+            constexpr uint32_t id_mf = idesc_bf16(128, LRMAX, 0, 1);
             constexpr uint32_t id_x = idesc_bf16(128, D, 0, 1);
-            constexpr uint32_t id_gt = idesc_bf16(128, 32, 1, 1);
+            constexpr uint32_t id_gt = idesc_bf16(128, LRMAX, 1, 1);
             constexpr uint32_t id_gb = idesc_bf16(128, 16, 1, 0);
             // MN-major A operands with M = 128 read a second 64-column block at start + LBO: for
             // F'_Q (sketch rows 64..127) and for dO^T at d = 64 (rows d 64..127) that block only feeds
@@ -278,7 +332,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 if (!(ok = wait_phase(bar(B_DO), par, abort))) break;
                 ++done[2];
                 fence_after();
-                for (int ks = 0; ks < 2; ++ks)
+                for (int ks = 0; ks < LRMAX / 16; ++ks)
                     umma_ts(tmem + T_SC, tmem + T_FK + 8 * ks, d_fq_k + (uint64_t)(2 * ks), id_sc, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -287,7 +341,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma(tmem + T_DP, d_v_k + ko, d_ghi_mn + (uint64_t)(ks * 128), id_dp, ks > 0);
                     umma(tmem + T_DP, d_v_k + ko, d_glo_mn + (uint64_t)(ks * 128), id_dp, true);
                 }
-                for (int ks = 0; ks < 2; ++ks) {
+                for (int ks = 0; ks < LRMAX / 16; ++ks) {
                     umma_ts(tmem + T_DVV, tmem + T_FK + 8 * ks, d_ghi_k + (uint64_t)(2 * ks), id_dv, ks > 0);
                     umma_ts(tmem + T_DVV, tmem + T_FK + 8 * ks, d_glo_k + (uint64_t)(2 * ks), id_dv, true);
                 }
@@ -363,8 +417,8 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                     for (int ch = 0; ch < LRMAX / 8; ++ch) {
                         if (8 * ch < lrs) {
-                            cp_async16(buf + STG_FQ + t * 64 + 16 * ch, fq_bh + row * lrs + 8 * ch);
-                            cp_async16(buf + STG_FK + t * 64 + 16 * ch, fk_bh + row * lrs + 8 * ch);
+                            cp_async16(buf + STG_FQ + t * SLOT + 16 * ch, fq_bh + row * lrs + 8 * ch);
+                            cp_async16(buf + STG_FK + t * SLOT + 16 * ch, fk_bh + row * lrs + 8 * ch);
                         }
                     }
                     cp_async4(buf + STG_C + t * 4, c_bh + 2 * row);
@@ -390,23 +444,44 @@ __global__ void __launch_bounds__(NTHW, 1)
             if (h == 0) {
                 // F'_Q row t -> shared tile row t and phi(K) row t -> TMEM (zero past the end);
                 // -c_t -> rows 0 / 1 of the mass operand; then the next chunk's rows
-                uint32_t fk0[8], fk1[8];  // phi(K) row t as bf16 pairs, L R <= 32
+                if constexpr (LRMAX == 32) {
+                    uint32_t fk0[8], fk1[8];  // phi(K) row t as bf16 pairs
 #pragma unroll
-                for (int ch = 0; ch < LRMAX / 8; ++ch) {
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u), w = make_uint4(0u, 0u, 0u, 0u);
-                    if (8 * ch < lrs && live) {
-                        v = ld_shared_v4(buf + STG_FQ + t * 64 + 16 * ch);
-                        w = ld_shared_v4(buf + STG_FK + t * 64 + 16 * ch);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u), w = make_uint4(0u, 0u, 0u, 0u);
+                        if (8 * ch < lrs && live) {
+                            v = ld_shared_v4(buf + STG_FQ + t * SLOT + 16 * ch);
+                            w = ld_shared_v4(buf + STG_FK + t * SLOT + 16 * ch);
+                        }
+                        if (8 * ch < lrs) st_shared_v4(base + Ly.fq + sw_chunk(t, ch), v.x, v.y, v.z, v.w);
+                        uint32_t *dst = ch < 2 ? fk0 + 4 * ch : fk1 + 4 * (ch - 2);
+                        dst[0] = w.x;
+                        dst[1] = w.y;
+                        dst[2] = w.z;
+                        dst[3] = w.w;
                     }
-                    if (8 * ch < lrs) st_shared_v4(base + Ly.fq + sw_chunk(t, ch), v.x, v.y, v.z, v.w);
-                    uint32_t *dst = ch < 2 ? fk0 + 4 * ch : fk1 + 4 * (ch - 2);
-                    dst[0] = w.x;
-                    dst[1] = w.y;
-                    dst[2] = w.z;
-                    dst[3] = w.w;
+                    stn<8>(tlane + T_FK, fk0);
+                    stn<8>(tlane + T_FK + 8, fk1);
+                } else
+#pragma unroll
+                for (int g = 0; g < LRMAX / 16; ++g) {  // 16 features (8 TMEM columns) at a time
+                    uint32_t fk[8];  // phi(K) row t as bf16 pairs
+#pragma unroll
+                    for (int hc = 0; hc < 2; ++hc) {
+                        const int ch = 2 * g + hc;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u), w = make_uint4(0u, 0u, 0u, 0u);
+                        if (8 * ch < lrs && live) {
+                            v = ld_shared_v4(buf + STG_FQ + t * SLOT + 16 * ch);
+                            w = ld_shared_v4(buf + STG_FK + t * SLOT + 16 * ch);
+                        }
+                        if (8 * ch < lrs) st_shared_v4(base + Ly.fq + sw_chunk(t, ch), v.x, v.y, v.z, v.w);
+                        fk[4 * hc] = w.x;
+                        fk[4 * hc + 1] = w.y;
+                        fk[4 * hc + 2] = w.z;
+                        fk[4 * hc + 3] = w.w;
+                    }
+                    stn<8>(tlane + T_FK + 8 * g, fk);
                 }
-                stn<8>(tlane + T_FK, fk0);
-                stn<8>(tlane + T_FK + 8, fk1);
                 const float cv = live ? reinterpret_cast<const float *>(sm + Ly.stage + par * STG + STG_C)[t] : 0.f;
                 if (k + 1 < nchunk) stage_rows(k + 1);
                 const float mcv = -cv;
@@ -426,7 +501,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 float z[LPZ];
                 {
                     float a[LPZ];
-                    ldn<LPZ>(tlane + T_ZK, a);
+                    ld_cols<LPZ>(tlane + T_ZK, a);
 #pragma unroll
                     for (int j = 0; j < LPZ; ++j) z[j] = a[j];
                 }
@@ -496,12 +571,12 @@ __global__ void __launch_bounds__(NTHW, 1)
                     stn<8>(tlane + T_SC + 4 * j, r);
                 }
                 // key-side Jacobian: dphi_K + G_B -> dz (bf16 pairs in TMEM)
-                float dph[LRMAX];
-                {
+                float dph[LRMAX == 32 ? 32 : 1];
+                if constexpr (LRMAX == 32) {
                     float a[32];
                     ld32(tlane + T_DP, a);
 #pragma unroll
-                    for (int j = 0; j < LRMAX; ++j) dph[j] = a[j] + gb[32 * par + j];
+                    for (int j = 0; j < 32; ++j) dph[j] = a[j] + gb[LRMAX * par + j];
                 }
                 float dz[LPP];
 #pragma unroll
@@ -514,8 +589,14 @@ __global__ void __launch_bounds__(NTHW, 1)
                         for (int p = 0; p < P; ++p)
                             u[p] = LT > 0 ? uk[(l * P + p) % (LT > 0 ? LPZ : 1)] : tc::tanh_abs(zk_s[(l * P + p) * C + t] * inv);
                         tc::bucket_probs<P>(u, beta, ph);
+                        if constexpr (LRMAX == 32) {
 #pragma unroll
-                        for (int r = 0; r < R; ++r) dp[r] = l * R + r < LRMAX ? dph[l * R + r] : 0.f;
+                            for (int r = 0; r < R; ++r) dp[r] = l * R + r < LRMAX ? dph[(l * R + r) % 32] : 0.f;
+                        } else {  // this table's R columns only (wider sketches keep one table in registers)
+                            ld_cols<R>(tlane + T_DP + l * R, dp);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) dp[r] += gb[LRMAX * par + l * R + r];
+                        }
                         float tmp[P];
                         table_backward<P, DB>(u, ph, dp, beta, tmp, &db);
 #pragma unroll
@@ -615,17 +696,24 @@ using namespace race::nc5;
 
 constexpr int NTHW = NTH + 32;
 
-constexpr uint32_t T_ZQ = 0;
-constexpr uint32_t T_DV = 64;     // dO V^T, then M1 as bf16 pairs (in place), then dxhat
-constexpr uint32_t T_G = 192;     // g (L R columns)
-constexpr uint32_t T_BT = 224;    // (tril 1) F_K
-constexpr uint32_t T_TRIL = 256;  // lower-triangular ones as bf16 pairs (A operand), 64 columns
-constexpr uint32_t T_DZ = 320;    // dz as bf16 pairs (A operand)
-constexpr uint32_t T_ST = 336;    // A^T (lanes = d)
-constexpr uint32_t T_MS = 368;    // B (lanes = sketch row), column 0
-constexpr uint32_t T_GT = 384;    // G^T (lanes = d)
-constexpr uint32_t T_GB = 416;    // G_B (lanes = sketch row), columns 0 + 1 (c split hi / lo)
-constexpr uint32_t T_X = 432;     // the Q row as stored (bf16 pairs), 64 columns
+// TMEM columns (512 allocated) for sketch widths L R <= LRM (32, or 64 when d = 64); with LRM = 64
+// the lower-triangular ones operand moves to shared memory.
+template <int D, int LRM>
+struct QCols {
+    static constexpr bool TRIL_TMEM = LRM == 32;
+    static constexpr uint32_t ZQ = 0;                        // projections of the Q tile, 32 columns
+    static constexpr uint32_t DV = LRM == 32 ? 64 : 32;      // dO V^T, then M1 as bf16 pairs (in place), then dxhat
+    static constexpr uint32_t G = DV + 128;                  // g (L R columns)
+    static constexpr uint32_t BT = G + LRM;                  // (tril 1) F_K
+    static constexpr uint32_t TRIL = BT + LRM;               // lower-triangular ones as bf16 pairs (A operand), 64 columns
+    static constexpr uint32_t DZ = TRIL_TMEM ? TRIL + 64 : TRIL;  // dz as bf16 pairs (A operand), 16 columns
+    static constexpr uint32_t ST = DZ + 16;                  // A^T (lanes = d)
+    static constexpr uint32_t MS = ST + LRM;                 // B (lanes = sketch row), column 0
+    static constexpr uint32_t GT = MS + 16;                  // G^T (lanes = d)
+    static constexpr uint32_t GB = GT + LRM;                 // G_B (lanes = sketch row), columns 0 + 1 (c split hi / lo)
+    static constexpr uint32_t X = GB + 16;                   // the Q row as stored (bf16 pairs), D / 2 columns
+    static_assert(X + D / 2 <= 512, "query-side TMEM budget");
+};
 constexpr uint32_t T_COLS = 512;
 
 enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC, B_SOP, B_CS, B_G, B_COUNT };
@@ -633,8 +721,8 @@ enum : uint32_t { B_QK, B_V, B_DO, B_PROJ, B_A, B_B, B_C, B_FEAT, B_MASK, B_JAC,
 constexpr uint32_t STG_FK = C * 128;  // one staging buffer of F_K rows (128-byte slots)
 
 struct QLayout {
-    uint32_t q, stage, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, bprev, invq, red, bar, slot, bytes, kbb;
-    __host__ __device__ QLayout(int D)
+    uint32_t q, stage, v, dO, fk, fq, shi, slo, whi, wlo, ncm, ones, tril, bprev, invq, red, bar, slot, bytes, kbb;
+    __host__ __device__ QLayout(int D, int LRM)
     {
         kbb = (uint32_t)(D / 64) * BLK;
         q = 0;
@@ -649,8 +737,9 @@ struct QLayout {
         wlo = whi + (uint32_t)(D / 64) * WBLK;
         ncm = wlo + (uint32_t)(D / 64) * WBLK;
         ones = ncm + 4096;
-        bprev = ones + 4096;  // B_prev fp32 [2 parities][32]
-        invq = bprev + 256;   // 1 / |Q row| fp32 [C]
+        tril = ones + 4096;   // LRM = 64: lower-triangular ones, K-major [t][j] in two 64-column blocks
+        bprev = tril + (LRM == 64 ? 2 * BLK : 0);  // B_prev fp32 [2 parities][LRM]
+        invq = bprev + 8 * LRM;   // 1 / |Q row| fp32 [C]
         red = invq + 4 * C;   // inv^2 (x . dxhat) of the Q rows, fp32 [C]
         bar = red + 4 * C;
         slot = bar + 128;
@@ -658,8 +747,9 @@ struct QLayout {
     }
 };
 
-// DB: also the CTA's query-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].
-template <int D, int P, int LT, bool DB>
+// DB: also the CTA's query-side d(loss)/d(beta) partial to dbpart[bh][blockIdx.x].  LRM: the
+// widest L R the instance supports (32, or 64 when d = 64).
+template <int D, int P, int LT, int LRM, bool DB>
 __global__ void __launch_bounds__(NTHW, 1)
     k_causal_bwdq5(const __grid_constant__ CUtensorMap tmQ, const bf16 *__restrict__ fk_in,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, Dims Dm,
@@ -670,12 +760,16 @@ __global__ void __launch_bounds__(NTHW, 1)
     constexpr int KB = D / 64;
     constexpr int R = 1 << P;
     constexpr int LMAX = LPP / P;
-    constexpr int LRMAX = 32;
+    constexpr int LRMAX = LRM;
+    using Cols = QCols<D, LRM>;
+    constexpr uint32_t T_ZQ = Cols::ZQ, T_DV = Cols::DV, T_G = Cols::G, T_BT = Cols::BT, T_TRIL = Cols::TRIL;
+    constexpr uint32_t T_DZ = Cols::DZ, T_ST = Cols::ST, T_MS = Cols::MS, T_GT = Cols::GT, T_GB = Cols::GB;
+    constexpr uint32_t T_X = Cols::X;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023) & ~1023u;
     unsigned char *sm = smem_raw + (base - raw);
-    const QLayout Ly(D);
+    const QLayout Ly(D, LRM);
     auto bar = [&](uint32_t i) { return base + Ly.bar + 8 * i; };
     volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
     float *bprev = reinterpret_cast<float *>(sm + Ly.bprev);
@@ -746,14 +840,26 @@ __global__ void __launch_bounds__(NTHW, 1)
             stn<8>(tlane + T_GB, zr);
         }
         // tril[t][j] = 1 for j <= t: half h writes the columns of keys 64 h .. 64 h + 63
-        for (int c0 = 32 * h; c0 < 32 * h + 32; c0 += 8) {
-            uint32_t r[8];
+        if constexpr (Cols::TRIL_TMEM) {
+            for (int c0 = 32 * h; c0 < 32 * h + 32; c0 += 8) {
+                uint32_t r[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int k0 = 2 * (c0 + j);
-                r[j] = (k0 <= t ? 0x3F80u : 0u) | (k0 + 1 <= t ? 0x3F800000u : 0u);
+                for (int j = 0; j < 8; ++j) {
+                    const int k0 = 2 * (c0 + j);
+                    r[j] = (k0 <= t ? 0x3F80u : 0u) | (k0 + 1 <= t ? 0x3F800000u : 0u);
+                }
+                stn<8>(tlane + T_TRIL + c0, r);
             }
-            stn<8>(tlane + T_TRIL + c0, r);
+        } else {
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t r[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int k0 = 64 * h + 8 * ch + 2 * j;
+                    r[j] = (k0 <= t ? 0x3F80u : 0u) | (k0 + 1 <= t ? 0x3F800000u : 0u);
+                }
+                st_shared_v4(base + Ly.tril + h * BLK + sw_chunk(t, ch), r[0], r[1], r[2], r[3]);
+            }
         }
         wait_st();
     }
@@ -761,33 +867,68 @@ __global__ void __launch_bounds__(NTHW, 1)
     __syncthreads();
     fence_after();
 
-    // S (TMEM) -> bf16 hi / lo operand rows d and fp32 B_prev; warps 4-7
+    // S (TMEM) -> bf16 hi / lo operand rows d (32 sketch columns at a time) and fp32 B_prev;
+    // warps 4-7
     auto convert_s = [&](int par_out) {
-        uint32_t ar[32], mv = 0;
-        if (t < D) ld32_nw(tlane + T_ST, ar);
-        if (q4 == 0) ld1_nw(tlane + T_MS, mv);
-        wait_ld();
-        reg_fence(ar);
-        reg_fence1(mv);
-        if (t < D) {
-            float a[32];
+        if constexpr (LRMAX == 32) {
+            uint32_t ar[32], mv = 0;
+            if (t < D) ld32_nw(tlane + T_ST, ar);
+            if (q4 == 0) ld1_nw(tlane + T_MS, mv);
+            wait_ld();
+            reg_fence(ar);
+            reg_fence1(mv);
+            if (t < D) {
+                float a[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = uf(ar[j]);
-            uint32_t hw[16], lw[16];
+                for (int j = 0; j < 32; ++j) a[j] = uf(ar[j]);
+                uint32_t hw[16], lw[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float x0 = 2 * j < LR ? a[2 * j] : 0.f, x1 = 2 * j + 1 < LR ? a[2 * j + 1] : 0.f;
-                const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-                lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                for (int j = 0; j < 16; ++j) {
+                    const float x0 = 2 * j < LR ? a[2 * j] : 0.f, x1 = 2 * j + 1 < LR ? a[2 * j + 1] : 0.f;
+                    const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                    hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                    lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    st_shared_v4(base + Ly.shi + sw_chunk(t, c), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                    st_shared_v4(base + Ly.slo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+                }
             }
+            if (q4 == 0) bprev[32 * par_out + lane] = lane < LR ? uf(mv) : 0.f;
+        } else {
 #pragma unroll
-            for (int c = 0; c < LRMAX / 8; ++c) {
-                st_shared_v4(base + Ly.shi + sw_chunk(t, c), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
-                st_shared_v4(base + Ly.slo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+            for (int half = 0; half < LRMAX / 32; ++half) {
+                uint32_t ar[32];
+                if (t < D) ld32_nw(tlane + T_ST + 32 * half, ar);
+                wait_ld();
+                reg_fence(ar);
+                if (t < D) {
+                    uint32_t hw[16], lw[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int c0 = 32 * half + 2 * j;
+                        const float x0 = c0 < LR ? uf(ar[2 * j]) : 0.f, x1 = c0 + 1 < LR ? uf(ar[2 * j + 1]) : 0.f;
+                        const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                        hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                        lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int ch = 4 * half + c;
+                        st_shared_v4(base + Ly.shi + sw_chunk(t, ch), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                        st_shared_v4(base + Ly.slo + sw_chunk(t, ch), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+                    }
+                }
+            }
+            if (32 * q4 < LRMAX) {  // lane = sketch row
+                uint32_t mv = 0;
+                ld1_nw(tlane + T_MS, mv);
+                wait_ld();
+                reg_fence1(mv);
+                bprev[LRMAX * par_out + t] = t < LR ? uf(mv) : 0.f;
             }
         }
-        if (q4 == 0) bprev[32 * par_out + lane] = lane < LR ? uf(mv) : 0.f;
     };
 
     float db = 0.f;  // this thread's d(loss)/d(beta) share (DB only)
@@ -819,10 +960,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                 issued[0] = issued[1] = issued[2] = 1;
             }
             constexpr uint32_t id_dv = idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t id_g1 = idesc_bf16(128, 32, 0, 1);
-            constexpr uint32_t id_bt = idesc_bf16(128, 32, 0, 1);
+            constexpr uint32_t id_g1 = idesc_bf16(128, LRMAX, 0, 1);
+            constexpr uint32_t id_bt = idesc_bf16(128, LRMAX, 0, 1);
             constexpr uint32_t id_x = idesc_bf16(128, D, 0, 1);
-            constexpr uint32_t id_gt = idesc_bf16(128, 32, 1, 1);
+            constexpr uint32_t id_gt = idesc_bf16(128, LRMAX, 1, 1);
             constexpr uint32_t id_m16 = idesc_bf16(128, 16, 1, 0);
             // MN-major A operands with M = 128 read a second 64-column block at start + BLK; beyond
             // d (d = 64) or beyond the sketch rows it feeds accumulator lanes nobody reads
@@ -856,8 +997,14 @@ __global__ void __launch_bounds__(NTHW, 1)
                     umma(tmem + T_G, d_do_k + ko, d_slo + (uint64_t)(ks * 128), id_g1, true);
                 }
 #pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks)
-                    umma_ts(tmem + T_BT, tmem + T_TRIL + 8 * ks, d_fk_mn + (uint64_t)(ks * 128), id_bt, ks > 0);
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    if constexpr (Cols::TRIL_TMEM) {
+                        umma_ts(tmem + T_BT, tmem + T_TRIL + 8 * ks, d_fk_mn + (uint64_t)(ks * 128), id_bt, ks > 0);
+                    } else {
+                        const uint64_t ko = (uint64_t)((ks >> 2) * BLK + (ks & 3) * 32) >> 4;
+                        umma(tmem + T_BT, desc_k(base + Ly.tril) + ko, d_fk_mn + (uint64_t)(ks * 128), id_bt, ks > 0);
+                    }
+                }
                 commit(bar(B_A));
                 if (c + 1 < nchunk) {  // projections and norms have read the Q / K tiles; issued after
                     load_tiles(c + 1, 1);  // group A, which waits on this warp
@@ -1018,74 +1165,120 @@ __global__ void __launch_bounds__(NTHW, 1)
             fence_after();
             if (h == 0) {
                 // den, c, dphi_Q and the feature Jacobian; F'_Q, -c and {1/den, c}, table by table
-                uint32_t gr[32], br[32];
-                ld32_nw(tlane + T_G, gr);
-                ld32_nw(tlane + T_BT, br);
-                wait_ld();
-                reg_fence(gr);
-                reg_fence(br);
-                float den = 0.f, pg = 0.f;
-                float phq[LT > 0 ? LRMAX : 1];  // with L compiled in: the row's bucket probabilities
+                auto write_fq = [&](int l, const float (&ph)[R], float rd) {  // F'_Q = phi / den, one table
+                    if constexpr (R >= 8) {
 #pragma unroll
-                for (int l = 0; l < LMAX; ++l) {
-                    if (l < L && l * R < LRMAX) {
-                        float u[P], ph[R];
+                        for (int j = 0; j < R / 8; ++j) {
+                            const int ch = l * (R / 8) + j;
+                            st_shared_v4(base + Ly.fq + sw_chunk(t, ch), mma::pack_bf16(ph[8 * j] * rd, ph[8 * j + 1] * rd),
+                                         mma::pack_bf16(ph[8 * j + 2] * rd, ph[8 * j + 3] * rd),
+                                         mma::pack_bf16(ph[8 * j + 4] * rd, ph[8 * j + 5] * rd),
+                                         mma::pack_bf16(ph[8 * j + 6] * rd, ph[8 * j + 7] * rd));
+                        }
+                    } else {
 #pragma unroll
-                        for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
-                        tc::bucket_probs<P>(u, beta, ph);
-#pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            const int lr = l * R + r < 32 ? l * R + r : 31;
-                            if constexpr (LT > 0) phq[lr] = ph[r];
-                            den = fmaf(ph[r], bprev[32 * par + lr] + uf(br[lr]), den);
-                            pg = fmaf(ph[r], uf(gr[lr]), pg);
+                        for (int r = 0; r < R; r += 2) {
+                            const uint32_t w = mma::pack_bf16(ph[r] * rd, ph[r + 1] * rd);
+                            asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fq + sw_elem(t, l * R + r)), "r"(w)
+                                         : "memory");
                         }
                     }
-                }
-                const float rd = live ? __frcp_rn(den) : 0.f;
-                const float cc = pg * rd;
-                if (live) aux[bh * Dm.N + n0 + t] = make_float2(rd, cc);
+                };
                 float dz[LPP];
 #pragma unroll
                 for (int j = 0; j < LPP; ++j) dz[j] = 0.f;
+                float rd = 0.f, cc = 0.f;
+                if constexpr (LRMAX == 32) {
+                    uint32_t gr[32], br[32];
+                    ld32_nw(tlane + T_G, gr);
+                    ld32_nw(tlane + T_BT, br);
+                    wait_ld();
+                    reg_fence(gr);
+                    reg_fence(br);
+                    float den = 0.f, pg = 0.f;
+                    float phq[LT > 0 ? LRMAX : 1];  // with L compiled in: the row's bucket probabilities
 #pragma unroll
-                for (int l = 0; l < LMAX; ++l) {
-                    if (l < L && l * R < LRMAX) {
-                        float u[P], ph[R], g[R];
+                    for (int l = 0; l < LMAX; ++l) {
+                        if (l < L && l * R < LRMAX) {
+                            float u[P], ph[R];
 #pragma unroll
-                        for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
-                        if constexpr (LT > 0) {
-#pragma unroll
-                            for (int r = 0; r < R; ++r) ph[r] = phq[l * R + r < 32 ? l * R + r : 31];
-                        } else {
+                            for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
                             tc::bucket_probs<P>(u, beta, ph);
-                        }
 #pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            const int lr = l * R + r < 32 ? l * R + r : 31;
-                            g[r] = (uf(gr[lr]) - (bprev[32 * par + lr] + uf(br[lr])) * cc) * rd;
-                        }
-                        float tmp[P];
-                        table_backward<P, DB>(u, ph, g, beta, tmp, &db);
-#pragma unroll
-                        for (int p = 0; p < P; ++p) dz[l * P + p] = tmp[p];
-                        // F'_Q = phi / den for this table
-                        if constexpr (R >= 8) {
-#pragma unroll
-                            for (int j = 0; j < R / 8; ++j) {
-                                const int ch = l * (R / 8) + j;
-                                st_shared_v4(base + Ly.fq + sw_chunk(t, ch), mma::pack_bf16(ph[8 * j] * rd, ph[8 * j + 1] * rd),
-                                             mma::pack_bf16(ph[8 * j + 2] * rd, ph[8 * j + 3] * rd),
-                                             mma::pack_bf16(ph[8 * j + 4] * rd, ph[8 * j + 5] * rd),
-                                             mma::pack_bf16(ph[8 * j + 6] * rd, ph[8 * j + 7] * rd));
+                            for (int r = 0; r < R; ++r) {
+                                const int lr = l * R + r < 32 ? l * R + r : 31;
+                                if constexpr (LT > 0) phq[lr] = ph[r];
+                                den = fmaf(ph[r], bprev[32 * par + lr] + uf(br[lr]), den);
+                                pg = fmaf(ph[r], uf(gr[lr]), pg);
                             }
-                        } else {
+                        }
+                    }
+                    rd = live ? __frcp_rn(den) : 0.f;
+                    cc = pg * rd;
+                    if (live) aux[bh * Dm.N + n0 + t] = make_float2(rd, cc);
 #pragma unroll
-                            for (int r = 0; r < R; r += 2) {
-                                const uint32_t w = mma::pack_bf16(ph[r] * rd, ph[r + 1] * rd);
-                                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fq + sw_elem(t, l * R + r)), "r"(w)
-                                             : "memory");
+                    for (int l = 0; l < LMAX; ++l) {
+                        if (l < L && l * R < LRMAX) {
+                            float u[P], ph[R], g[R];
+#pragma unroll
+                            for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
+                            if constexpr (LT > 0) {
+#pragma unroll
+                                for (int r = 0; r < R; ++r) ph[r] = phq[l * R + r < 32 ? l * R + r : 31];
+                            } else {
+                                tc::bucket_probs<P>(u, beta, ph);
                             }
+#pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                const int lr = l * R + r < 32 ? l * R + r : 31;
+                                g[r] = (uf(gr[lr]) - (bprev[32 * par + lr] + uf(br[lr])) * cc) * rd;
+                            }
+                            float tmp[P];
+                            table_backward<P, DB>(u, ph, g, beta, tmp, &db);
+#pragma unroll
+                            for (int p = 0; p < P; ++p) dz[l * P + p] = tmp[p];
+                            write_fq(l, ph, rd);
+                        }
+                    }
+                } else {
+                    // wider sketches: one table's g and B_t columns at a time, in two passes (den and
+                    // c need every table before any table's gradient)
+                    float den = 0.f, pg = 0.f;
+#pragma unroll
+                    for (int l = 0; l < LMAX; ++l) {
+                        if (l < L && l * R < LRMAX) {
+                            float u[P], ph[R], gg[R], bb[R];
+#pragma unroll
+                            for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
+                            tc::bucket_probs<P>(u, beta, ph);
+                            ld_cols<R>(tlane + T_G + l * R, gg);
+                            ld_cols<R>(tlane + T_BT + l * R, bb);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                den = fmaf(ph[r], bprev[LRMAX * par + l * R + r] + bb[r], den);
+                                pg = fmaf(ph[r], gg[r], pg);
+                            }
+                        }
+                    }
+                    rd = live ? __frcp_rn(den) : 0.f;
+                    cc = pg * rd;
+                    if (live) aux[bh * Dm.N + n0 + t] = make_float2(rd, cc);
+#pragma unroll
+                    for (int l = 0; l < LMAX; ++l) {
+                        if (l < L && l * R < LRMAX) {
+                            float u[P], ph[R], gg[R], bb[R], g[R];
+#pragma unroll
+                            for (int p = 0; p < P; ++p) u[p] = uq[l * P + p];
+                            tc::bucket_probs<P>(u, beta, ph);
+                            ld_cols<R>(tlane + T_G + l * R, gg);
+                            ld_cols<R>(tlane + T_BT + l * R, bb);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) g[r] = (gg[r] - (bprev[LRMAX * par + l * R + r] + bb[r]) * cc) * rd;
+                            float tmp[P];
+                            table_backward<P, DB>(u, ph, g, beta, tmp, &db);
+#pragma unroll
+                            for (int p = 0; p < P; ++p) dz[l * P + p] = tmp[p];
+                            write_fq(l, ph, rd);
                         }
                     }
                 }
@@ -1159,11 +1352,14 @@ __global__ void __launch_bounds__(NTHW, 1)
             fence_after();
             float *out = Gseg + ((int64_t)bh * nseg + s) * LR * (D + 1);
             if (h == 0 && t < D) {
-                float a[32];
-                ld32(tlane + T_GT, a);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j < LR) out[(int64_t)j * (D + 1) + t] = a[j];
+                for (int half = 0; half < LRMAX / 32; ++half) {
+                    float a[32];
+                    ld32(tlane + T_GT + 32 * half, a);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (32 * half + j < LR) out[(int64_t)(32 * half + j) * (D + 1) + t] = a[j];
+                }
             }
             if (h == 1) {
                 float m[2];
@@ -1198,73 +1394,86 @@ size_t c5_feature_rows_bytes(const Dims &D)
 
 bool c5_bwd_supported(const Dims &D)
 {
-    return (D.d == 64 || D.d == 128) && D.P >= 1 && D.P <= 5 && D.LP <= nc5::LPP && D.LR <= 32 &&
+    // L R <= 32 at d = 64 or 128; L R <= 64 at d = 64 (the TMEM budget of the key side: 512 columns)
+    const bool width = D.LR <= 32 || (D.d == 64 && D.LR <= 64);
+    return (D.d == 64 || D.d == 128) && D.P >= 1 && D.P <= (D.d == 64 ? 6 : 5) && D.LP <= nc5::LPP && width &&
            D.N <= 0x7FFFFFFF;
 }
 
 namespace {
 
-template <int D, int P, int LT>
+template <int D, int P, int LT, int LRM>
 cudaError_t bwdkv5_launch(const Dims &Dm, const bf16_t *fq, const bf16_t *fk, const float *kinv, const CUtensorMap &mk,
-                          const CUtensorMap &mv,
-                          const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
-                          int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
+                          const CUtensorMap &mv, const CUtensorMap &mdo, const float *W, const float2 *aux,
+                          const float *G0, int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err,
+                          float *dbpart, cudaStream_t st)
 {
-    const c5b::BwdLayout Ly(D);
+    const c5b::BwdLayout Ly(D, LRM);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = dbpart ? c5b::k_causal_bwdkv5<D, P, LT, true> : c5b::k_causal_bwdkv5<D, P, LT, false>;
+    auto kern = dbpart ? c5b::k_causal_bwdkv5<D, P, LT, LRM, true> : c5b::k_causal_bwdkv5<D, P, LT, LRM, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_bwd_kv", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5b::NTHW), smem,
                          st, fq, fk, kinv, mk, mv, mdo, Dm, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart);
 }
 
-// (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
+// (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.  L R > 32
+// (d = 64 only) takes the LRM = 64 instances (with L compiled in they spill three times as much).
 template <int D, int P>
 cudaError_t bwdkv5_inst(const Dims &Dm, const bf16_t *fq, const bf16_t *fk, const float *kinv, const CUtensorMap &mk,
-                        const CUtensorMap &mv,
-                        const CUtensorMap &mdo, const float *W, const float2 *aux, const float *G0, int64_t seg_len,
-                        int nseg, bf16_t *dK, bf16_t *dV, unsigned *err, float *dbpart, cudaStream_t st)
+                        const CUtensorMap &mv, const CUtensorMap &mdo, const float *W, const float2 *aux,
+                        const float *G0, int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err,
+                        float *dbpart, cudaStream_t st)
 {
+#define RACE_KV_ARGS Dm, fq, fk, kinv, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st
+    if constexpr (D == 64 && P >= 2) {
+        if (Dm.LR > 32) return bwdkv5_launch<D, P, 0, 64>(RACE_KV_ARGS);
+    }
     if constexpr (D == 128 && P == 3)
-        if (Dm.L == 3)
-            return bwdkv5_launch<D, P, 3>(Dm, fq, fk, kinv, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart,
-                                          st);
-    return bwdkv5_launch<D, P, 0>(Dm, fq, fk, kinv, mk, mv, mdo, W, aux, G0, seg_len, nseg, dK, dV, err, dbpart, st);
+        if (Dm.L == 3) return bwdkv5_launch<D, P, 3, 32>(RACE_KV_ARGS);
+    if constexpr (P <= 5) return bwdkv5_launch<D, P, 0, 32>(RACE_KV_ARGS);
+    return cudaErrorInvalidValue;
+#undef RACE_KV_ARGS
 }
 
-template <int D, int P, int LT>
+template <int D, int P, int LT, int LRM>
 cudaError_t bwdq5_launch(const Dims &Dm, const CUtensorMap &mq, const bf16_t *fk, const CUtensorMap &mv,
                          const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
                          bf16_t *dQ, float2 *aux, bf16_t *fq, float *Gseg, unsigned *err, float *dbpart,
                          cudaStream_t st)
 {
-    const c5q::QLayout Ly(D);
+    const c5q::QLayout Ly(D, LRM);
     const size_t smem = Ly.bytes + 1024;
-    auto kern = dbpart ? c5q::k_causal_bwdq5<D, P, LT, true> : c5q::k_causal_bwdq5<D, P, LT, false>;
+    auto kern = dbpart ? c5q::k_causal_bwdq5<D, P, LT, LRM, true> : c5q::k_causal_bwdq5<D, P, LT, LRM, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel("tc5_causal_bwd_q", kern, dim3((unsigned)nseg, (unsigned)Dm.BH), dim3(c5q::NTHW), smem, st,
                          mq, fk, mv, mdo, Dm, W, S0, seg_len, nseg, dQ, aux, fq, Gseg, err, dbpart);
 }
 
-// (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.
+// (d, P, L) = (128, 3, 3) runs with L compiled in; every other shape with L at run time.  L R > 32
+// (d = 64 only) takes the LRM = 64 instances (with L compiled in they spill three times as much).
 template <int D, int P>
 cudaError_t bwdq5_inst(const Dims &Dm, const CUtensorMap &mq, const bf16_t *fk, const CUtensorMap &mv,
                        const CUtensorMap &mdo, const float *W, const float *S0, int64_t seg_len, int nseg,
                        bf16_t *dQ, float2 *aux, bf16_t *fq, float *Gseg, unsigned *err, float *dbpart,
                        cudaStream_t st)
 {
+#define RACE_Q_ARGS Dm, mq, fk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, fq, Gseg, err, dbpart, st
+    if constexpr (D == 64 && P >= 2) {
+        if (Dm.LR > 32) return bwdq5_launch<D, P, 0, 64>(RACE_Q_ARGS);
+    }
     if constexpr (D == 128 && P == 3)
-        if (Dm.L == 3)
-            return bwdq5_launch<D, P, 3>(Dm, mq, fk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, fq, Gseg, err, dbpart,
-                                         st);
-    return bwdq5_launch<D, P, 0>(Dm, mq, fk, mv, mdo, W, S0, seg_len, nseg, dQ, aux, fq, Gseg, err, dbpart, st);
+        if (Dm.L == 3) return bwdq5_launch<D, P, 3, 32>(RACE_Q_ARGS);
+    if constexpr (P <= 5) return bwdq5_launch<D, P, 0, 32>(RACE_Q_ARGS);
+    return cudaErrorInvalidValue;
+#undef RACE_Q_ARGS
 }
 
 }  // namespace
 
-#define RACE_C5B_SHAPES(X) X(64, 1) X(64, 2) X(64, 3) X(64, 4) X(64, 5) X(128, 1) X(128, 2) X(128, 3) X(128, 4) X(128, 5)
+#define RACE_C5B_SHAPES(X) \
+    X(64, 1) X(64, 2) X(64, 3) X(64, 4) X(64, 5) X(64, 6) X(128, 1) X(128, 2) X(128, 3) X(128, 4) X(128, 5)
 
 cudaError_t launch_c5_bwd_q(const Dims &Dm, const bf16_t *Q, const bf16_t *fk, const bf16_t *V, const bf16_t *dO,
                             const float *W, const float *S0, int64_t seg_len, int nseg, bf16_t *dQ, float2 *aux,
