@@ -41,10 +41,6 @@ KERNEL_BYTES = {
     "causal_fwd": (4, 0, 0),         # reads Q, K, V; writes O
     "causal_bwd_q": (5, 8, 0),       # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
     "causal_bwd_kv": (6, 8, 0),      # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
-    "tc_causal_totals": (2, 0, 0),   # reads K, V
-    "tc_causal_fwd": (4, 0, 0),      # reads Q, K, V; writes O
-    "tc_causal_bwd_q": (5, 8, 0),    # reads Q, K, V, dO; writes dQ and {1/den, dO.O}
-    "tc_causal_bwd_kv": (6, 8, 0),   # reads Q, K, V, dO and {1/den, dO.O}; writes dK, dV
     "tc5_sketch_keys": (2, 0, 0),    # reads K, V
     "tc5_sketch_grad": (2, 8, 0),    # reads Q, dO and {1/den, dO.O}
     "tc5_readout": (2, 0, 0),        # reads Q, writes O
@@ -77,7 +73,6 @@ def compulsory_bytes(name, w):
 KERNEL_ALG_SHARE = {
     "sketch_keys": 2, "readout": 2, "bwd_query": 3, "sketch_grad": 0, "bwd_key": 4,
     "causal_fwd": 4, "causal_bwd_q": 3, "causal_bwd_kv": 4,
-    "tc_causal_totals": 0, "tc_causal_fwd": 4, "tc_causal_bwd_q": 3, "tc_causal_bwd_kv": 4,
     "tc5_sketch_keys": 2, "tc5_readout": 2, "tc5_bwd_query": 3, "tc5_sketch_grad": 0, "tc5_bwd_key": 4,
     "tc5_causal_fwd": 4, "tc5_causal_bwd_q": 3, "tc5_causal_bwd_kv": 4,
 }

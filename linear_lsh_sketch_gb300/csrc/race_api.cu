@@ -261,13 +261,6 @@ float kernel_beta(float beta) { return hard_hash(beta) ? kHardBeta : beta; }
     } while (0)
 
 template <typename T>
-bool use_tc(const Plan &pl)
-{
-    if (!std::is_same<T, bf16_t>::value) return false;
-    return pl.causal && causal_tc_supported(pl.D);
-}
-
-template <typename T>
 int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float *W, T *O, float *state,
                  char *ws, cudaStream_t st)
 {
@@ -285,12 +278,6 @@ int forward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const float
             RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st, fk, kinv));
             RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
             RACE_TRY(launch_c5_fwd(D, Q, fk, V, W, S, pl.seg_len, pl.nsplit, O, err, st));
-            return RACE_OK;
-        }
-        if (use_tc<T>(pl)) {
-            RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
-            RACE_TRY(launch_combine(D, part, S, pl.nsplit, 1, st));
-            RACE_TRY(launch_causal_tc_fwd(D, Q, K, V, W, S, pl.seg_len, pl.nsplit, O, err, st));
             return RACE_OK;
         }
     }
@@ -350,37 +337,24 @@ int backward_impl(const Plan &pl, const T *Q, const T *K, const T *V, const floa
     const float *S = state;
     DbetaOut db;
     if constexpr (std::is_same<T, bf16_t>::value) {
-        const bool c5b = pl.c5 && c5_bwd_supported(D);
-        if (c5b || (use_tc<T>(pl) && causal_tc_bwd_supported(D))) {
+        if (pl.c5 && c5_bwd_supported(D)) {
             // the keys' bucket-feature rows: from the forward's state, or stored again here
             const bf16_t *fk = S ? (const bf16_t *)((const char *)S + pl.state_fk) : (const bf16_t *)(ws + pl.off_fk);
             const float *kinv = S ? (const float *)((const char *)S + pl.state_kinv) : (const float *)(ws + pl.off_kinv);
             if (!S) {
                 float *Sw = (float *)(ws + pl.off_sk);
-                if (pl.c5)
-                    RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st,
-                                               c5b ? (bf16_t *)(ws + pl.off_fk) : nullptr,
-                                               c5b ? (float *)(ws + pl.off_kinv) : nullptr));
-                else
-                    RACE_TRY(launch_causal_tc_totals(D, K, V, W, pl.seg_len, pl.nsplit, part, err, st));
+                RACE_TRY(launch_nc5_sketch(D, K, V, nullptr, W, pl.seg_len, pl.nsplit, part, err, st,
+                                           (bf16_t *)(ws + pl.off_fk), (float *)(ws + pl.off_kinv)));
                 RACE_TRY(launch_combine(D, part, Sw, pl.nsplit, 1, st));
                 S = Sw;
             }
             RACE_TRY(dbeta_begin(pl, ws, dbeta, pl.nsplit, db, st));
             bf16_t *fq = (bf16_t *)(ws + pl.off_fq);
-            if (c5b)
-                RACE_TRY(launch_c5_bwd_q(D, Q, fk, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, fq, gpart, err,
-                                         db.dbq, st));
-            else
-                RACE_TRY(launch_causal_tc_bwd_q(D, Q, K, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, gpart, err,
-                                                db.dbq, st));
+            RACE_TRY(launch_c5_bwd_q(D, Q, fk, V, dO, W, S, pl.seg_len, pl.nsplit, dQ, aux, fq, gpart, err, db.dbq,
+                                     st));
             RACE_TRY(launch_combine(D, gpart, gsk, pl.nsplit, 2, st));
-            if (c5b)
-                RACE_TRY(launch_c5_bwd_kv(D, fq, fk, kinv, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err,
-                                          db.dbk, st));
-            else
-                RACE_TRY(launch_causal_tc_bwd_kv(D, Q, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err,
-                                                 db.dbk, st));
+            RACE_TRY(launch_c5_bwd_kv(D, fq, fk, kinv, K, V, dO, aux, W, gsk, pl.seg_len, pl.nsplit, dK, dV, err,
+                                      db.dbk, st));
             RACE_TRY(dbeta_end(pl, db, st));
             return RACE_OK;
         }

@@ -218,8 +218,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int j = 0; j < 16; ++j) {
                     const float x0 = 2 * j < LR ? a[2 * j] : 0.f, x1 = 2 * j + 1 < LR ? a[2 * j + 1] : 0.f;
                     const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                    hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-                    lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                    hw[j] = bfp::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                    lw[j] = bfp::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
                 }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                         const int c0 = 32 * half + 2 * j;
                         const float x0 = c0 < LR ? uf(ar[2 * j]) : 0.f, x1 = c0 + 1 < LR ? uf(ar[2 * j + 1]) : 0.f;
                         const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                        hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-                        lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                        hw[j] = bfp::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                        lw[j] = bfp::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
                     }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -538,8 +538,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                         for (int j = 0; j < 8; ++j) {
                             const int e = 16 * b + 2 * j, q0 = tb + e;
                             const bool k0 = need && q0 >= t, k1 = need && q0 + 1 >= t;
-                            pw[j] = mma::pack_bf16(k0 ? uf(sa[e]) : 0.f, k1 ? uf(sa[e + 1]) : 0.f);
-                            mw[j] = mma::pack_bf16(k0 ? uf(sd[e]) - cvec[q0] : 0.f, k1 ? uf(sd[e + 1]) - cvec[q0 + 1] : 0.f);
+                            pw[j] = bfp::pack_bf16(k0 ? uf(sa[e]) : 0.f, k1 ? uf(sa[e + 1]) : 0.f);
+                            mw[j] = bfp::pack_bf16(k0 ? uf(sd[e]) - cvec[q0] : 0.f, k1 ? uf(sd[e + 1]) - cvec[q0 + 1] : 0.f);
                         }
                         // bf16 pairs of this half's 64 columns go to its own first 32 columns
                         stn<8>(tlane + T_SC + j0 + 16 * pass + 8 * b, pw);
@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(dz[16 * b + 2 * j], dz[16 * b + 2 * j + 1]);
+                    for (int j = 0; j < 8; ++j) r[j] = bfp::pack_bf16(dz[16 * b + 2 * j], dz[16 * b + 2 * j + 1]);
                     stn<8>(tlane + T_DZ + 8 * b, r);
                 }
                 // dxhat = W^T dz (dz rounded to bf16 as the product sees it), so x . dxhat = z . dz
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     reg_fence(v);
                     uint32_t o[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) o[j] = mma::pack_bf16(uf(v[2 * j]), uf(v[2 * j + 1]));
+                    for (int j = 0; j < 16; ++j) o[j] = bfp::pack_bf16(uf(v[2 * j]), uf(v[2 * j + 1]));
                     if (live) store_row32(dst + 32 * pass, o, wide);
                 }
                 fence_before();
@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     uint32_t o[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        o[j] = mma::pack_bf16(inv * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), inv * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
+                        o[j] = bfp::pack_bf16(inv * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), inv * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
                     if (live) store_row32(dst + 32 * pass, o, wide);
                 }
             }
@@ -886,8 +886,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int j = 0; j < 16; ++j) {
                     const float x0 = 2 * j < LR ? a[2 * j] : 0.f, x1 = 2 * j + 1 < LR ? a[2 * j + 1] : 0.f;
                     const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                    hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-                    lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                    hw[j] = bfp::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                    lw[j] = bfp::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
                 }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -910,8 +910,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                         const int c0 = 32 * half + 2 * j;
                         const float x0 = c0 < LR ? uf(ar[2 * j]) : 0.f, x1 = c0 + 1 < LR ? uf(ar[2 * j + 1]) : 0.f;
                         const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                        hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-                        lw[j] = mma::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+                        hw[j] = bfp::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                        lw[j] = bfp::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
                     }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -1152,7 +1152,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const int e = 16 * b + 2 * j;
-                            w[j] = mma::pack_bf16(need && jb + e <= t ? uf(a[e]) : 0.f,
+                            w[j] = bfp::pack_bf16(need && jb + e <= t ? uf(a[e]) : 0.f,
                                                   need && jb + e + 1 <= t ? uf(a[e + 1]) : 0.f);
                         }
                         stn<8>(tlane + T_DV + j0 + 16 * pass + 8 * b, w);
@@ -1170,15 +1170,15 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                         for (int j = 0; j < R / 8; ++j) {
                             const int ch = l * (R / 8) + j;
-                            st_shared_v4(base + Ly.fq + sw_chunk(t, ch), mma::pack_bf16(ph[8 * j] * rd, ph[8 * j + 1] * rd),
-                                         mma::pack_bf16(ph[8 * j + 2] * rd, ph[8 * j + 3] * rd),
-                                         mma::pack_bf16(ph[8 * j + 4] * rd, ph[8 * j + 5] * rd),
-                                         mma::pack_bf16(ph[8 * j + 6] * rd, ph[8 * j + 7] * rd));
+                            st_shared_v4(base + Ly.fq + sw_chunk(t, ch), bfp::pack_bf16(ph[8 * j] * rd, ph[8 * j + 1] * rd),
+                                         bfp::pack_bf16(ph[8 * j + 2] * rd, ph[8 * j + 3] * rd),
+                                         bfp::pack_bf16(ph[8 * j + 4] * rd, ph[8 * j + 5] * rd),
+                                         bfp::pack_bf16(ph[8 * j + 6] * rd, ph[8 * j + 7] * rd));
                         }
                     } else {
 #pragma unroll
                         for (int r = 0; r < R; r += 2) {
-                            const uint32_t w = mma::pack_bf16(ph[r] * rd, ph[r + 1] * rd);
+                            const uint32_t w = bfp::pack_bf16(ph[r] * rd, ph[r + 1] * rd);
                             asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(base + Ly.fq + sw_elem(t, l * R + r)), "r"(w)
                                          : "memory");
                         }
@@ -1293,7 +1293,7 @@ __global__ void __launch_bounds__(NTHW, 1)
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(dz[16 * b + 2 * j], dz[16 * b + 2 * j + 1]);
+                    for (int j = 0; j < 8; ++j) r[j] = bfp::pack_bf16(dz[16 * b + 2 * j], dz[16 * b + 2 * j + 1]);
                     stn<8>(tlane + T_DZ + 8 * b, r);
                 }
                 {
@@ -1339,7 +1339,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                     uint32_t o[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        o[j] = mma::pack_bf16(iq * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), iq * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
+                        o[j] = bfp::pack_bf16(iq * (uf(v[2 * j]) - bf_lo(xr[j]) * kk), iq * (uf(v[2 * j + 1]) - bf_hi(xr[j]) * kk));
                     if (live) store_row32(dst + 32 * pass, o, wide);
                 }
             }

@@ -108,7 +108,7 @@ __device__ __forceinline__ void sketch_to_operand(uint32_t tlane, int q4, int la
                             x0 = bf16_rest(x0);
                             x1 = bf16_rest(x1);
                         }
-                        w[j] = mma::pack_bf16(x0, x1);
+                        w[j] = bfp::pack_bf16(x0, x1);
                     }
                     st_shared_v4(dst + sw_chunk(row, cg), w[0], w[1], w[2], w[3]);
                 }
@@ -374,8 +374,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = uf(v[8 * j + e]) * rd;
-                    st_shared_v4(stage + (ch >> 3) * BLK + sw_chunk(t, ch & 7), mma::pack_bf16(x[0], x[1]),
-                                 mma::pack_bf16(x[2], x[3]), mma::pack_bf16(x[4], x[5]), mma::pack_bf16(x[6], x[7]));
+                    st_shared_v4(stage + (ch >> 3) * BLK + sw_chunk(t, ch & 7), bfp::pack_bf16(x[0], x[1]),
+                                 bfp::pack_bf16(x[2], x[3]), bfp::pack_bf16(x[4], x[5]), bfp::pack_bf16(x[6], x[7]));
                 }
             }
         };
@@ -441,13 +441,13 @@ __global__ void __launch_bounds__(NTHW, 1)
                             for (int b = 0; b < R / 16; ++b) {
                                 uint32_t r[8];
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(ph[16 * b + 2 * j], ph[16 * b + 2 * j + 1]);
+                                for (int j = 0; j < 8; ++j) r[j] = bfp::pack_bf16(ph[16 * b + 2 * j], ph[16 * b + 2 * j + 1]);
                                 stn<8>(tlane + fq + (l * R) / 2 + 8 * b, r);
                             }
                         } else {
                             uint32_t r[R / 2];
 #pragma unroll
-                            for (int j = 0; j < R / 2; ++j) r[j] = mma::pack_bf16(ph[2 * j], ph[2 * j + 1]);
+                            for (int j = 0; j < R / 2; ++j) r[j] = bfp::pack_bf16(ph[2 * j], ph[2 * j + 1]);
                             stn<R / 2>(tlane + fq + (l * R) / 2, r);
                         }
                     }
@@ -490,8 +490,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                         const int jj = jb + 2 * j;
                         const uint32_t x0 = b ? a1[2 * j] : a0[2 * j], x1 = b ? a1[2 * j + 1] : a0[2 * j + 1];
                         const uint32_t x2 = b ? a1[16 + 2 * j] : a0[16 + 2 * j], x3 = b ? a1[17 + 2 * j] : a0[17 + 2 * j];
-                        r0[j] = mma::pack_bf16(jj <= t ? uf(x0) : 0.f, jj + 1 <= t ? uf(x1) : 0.f);
-                        r1[j] = mma::pack_bf16(jj + 16 <= t ? uf(x2) : 0.f, jj + 17 <= t ? uf(x3) : 0.f);
+                        r0[j] = bfp::pack_bf16(jj <= t ? uf(x0) : 0.f, jj + 1 <= t ? uf(x1) : 0.f);
+                        r1[j] = bfp::pack_bf16(jj + 16 <= t ? uf(x2) : 0.f, jj + 17 <= t ? uf(x3) : 0.f);
                     }
                     stn<8>(tlane + T_P + jb / 2, r0);
                     stn<8>(tlane + T_P + jb / 2 + 8, r1);

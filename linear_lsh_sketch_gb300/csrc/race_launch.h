@@ -69,25 +69,6 @@ cudaError_t launch_causal_bwd_kv(const Dims &D, const T *Q, const T *K, const T 
                                  const float2 *aux, const float *W, const float *G0, int64_t seg_len, int nseg,
                                  T *dK, T *dV, float *dbpart, cudaStream_t st);
 
-// ---------------------------------------------------------------- tensor-core causal path (bf16)
-bool causal_tc_supported(const Dims &D);
-int causal_tc_chunk();
-cudaError_t launch_causal_tc_totals(const Dims &D, const bf16_t *K, const bf16_t *V, const float *W,
-                                    int64_t seg_len, int nseg, float *Sout, unsigned *err, cudaStream_t st);
-cudaError_t launch_causal_tc_fwd(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V, const float *W,
-                                 const float *S0, int64_t seg_len, int nseg, bf16_t *O, unsigned *err,
-                                 cudaStream_t st);
-
-bool causal_tc_bwd_supported(const Dims &D);
-cudaError_t launch_causal_tc_bwd_q(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V,
-                                   const bf16_t *dO, const float *W, const float *S0, int64_t seg_len, int nseg,
-                                   bf16_t *dQ, float2 *aux, float *Gseg, unsigned *err, float *dbpart,
-                                   cudaStream_t st);
-cudaError_t launch_causal_tc_bwd_kv(const Dims &D, const bf16_t *Q, const bf16_t *K, const bf16_t *V,
-                                    const bf16_t *dO, const float2 *aux, const float *W, const float *G0,
-                                    int64_t seg_len, int nseg, bf16_t *dK, bf16_t *dV, unsigned *err,
-                                    float *dbpart, cudaStream_t st);
-
 // ---------------------------------------------------------------- tcgen05 non-causal path (bf16)
 bool nc5_supported(const Dims &D);
 int nc5_tile();

@@ -47,8 +47,8 @@ __device__ __forceinline__ void load_sketch_rows(const float *__restrict__ S, in
                 v1 = S[(int64_t)lr * (D + 1) + 8 * c + 2 * j + 1];
             }
             const bf16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
-            hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-            lw[j] = mma::pack_bf16(v0 - __bfloat162float(h0), v1 - __bfloat162float(h1));
+            hw[j] = bfp::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+            lw[j] = bfp::pack_bf16(v0 - __bfloat162float(h0), v1 - __bfloat162float(h1));
         }
         const uint32_t off = (c >> 3) * blk + sw_chunk(lr, c & 7);
         st_shared_v4(hi + off, hw[0], hw[1], hw[2], hw[3]);
@@ -66,20 +66,20 @@ __device__ __forceinline__ void st_bf16_cols(uint32_t taddr, const float (&v)[N]
     if constexpr (W <= 8 && (W & (W - 1)) == 0) {
         uint32_t r[W];
 #pragma unroll
-        for (int j = 0; j < W; ++j) r[j] = mma::pack_bf16(v[2 * j], v[2 * j + 1]);
+        for (int j = 0; j < W; ++j) r[j] = bfp::pack_bf16(v[2 * j], v[2 * j + 1]);
         stn<W>(taddr, r);
     } else if constexpr (W % 8 == 0) {
 #pragma unroll
         for (int b = 0; b < W / 8; ++b) {
             uint32_t r[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) r[j] = mma::pack_bf16(v[16 * b + 2 * j], v[16 * b + 2 * j + 1]);
+            for (int j = 0; j < 8; ++j) r[j] = bfp::pack_bf16(v[16 * b + 2 * j], v[16 * b + 2 * j + 1]);
             stn<8>(taddr + 8 * b, r);
         }
     } else {
 #pragma unroll
         for (int j = 0; j < W; ++j) {
-            const uint32_t r[1] = {mma::pack_bf16(v[2 * j], v[2 * j + 1])};
+            const uint32_t r[1] = {bfp::pack_bf16(v[2 * j], v[2 * j + 1])};
             stn<1>(taddr + j, r);
         }
     }
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(NTH, 1)
             uint32_t o[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                o[k] = mma::pack_bf16(inv * (dx[8 * j + 2 * k] - bf_lo(w4[k]) * kk),
+                o[k] = bfp::pack_bf16(inv * (dx[8 * j + 2 * k] - bf_lo(w4[k]) * kk),
                                       inv * (dx[8 * j + 2 * k + 1] - bf_hi(w4[k]) * kk));
             st_shared_v4(ys + (c >> 3) * BLK + sw_chunk(t, c & 7), o[0], o[1], o[2], o[3]);
         }
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(NTH, 1)
             uint32_t o[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                o[k] = mma::pack_bf16(inv * (dx[8 * j + 2 * k] - bf_lo(w4[k]) * kk),
+                o[k] = bfp::pack_bf16(inv * (dx[8 * j + 2 * k] - bf_lo(w4[k]) * kk),
                                       inv * (dx[8 * j + 2 * k + 1] - bf_hi(w4[k]) * kk));
             st_shared_v4(ys + (c >> 3) * BLK + sw_chunk(t, c & 7), o[0], o[1], o[2], o[3]);
         }
@@ -593,9 +593,9 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int c = h * (D / 16) + 2 * cc16 + j;
-                st_shared_v4(xs + (c >> 3) * BLK + sw_chunk(t, c & 7), mma::pack_bf16(v[8 * j], v[8 * j + 1]),
-                             mma::pack_bf16(v[8 * j + 2], v[8 * j + 3]), mma::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                             mma::pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+                st_shared_v4(xs + (c >> 3) * BLK + sw_chunk(t, c & 7), bfp::pack_bf16(v[8 * j], v[8 * j + 1]),
+                             bfp::pack_bf16(v[8 * j + 2], v[8 * j + 3]), bfp::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                             bfp::pack_bf16(v[8 * j + 6], v[8 * j + 7]));
             }
         }
         tc::fence_proxy_async();

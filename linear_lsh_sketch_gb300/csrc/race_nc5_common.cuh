@@ -40,8 +40,8 @@ __device__ __forceinline__ void load_w_tiles(const float *__restrict__ W, int LP
                 w1 = W[row * D + 8 * c + 2 * j + 1];
             }
             const bf16 h0 = __float2bfloat16_rn(w0), h1 = __float2bfloat16_rn(w1);
-            h[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-            l[j] = mma::pack_bf16(w0 - __bfloat162float(h0), w1 - __bfloat162float(h1));
+            h[j] = bfp::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+            l[j] = bfp::pack_bf16(w0 - __bfloat162float(h0), w1 - __bfloat162float(h1));
         }
         const uint32_t off = (c >> 3) * WBLK + sw_chunk(row, c & 7);
         st_shared_v4(smem_addr(whi) + off, h[0], h[1], h[2], h[3]);
@@ -231,10 +231,10 @@ __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv,
 #pragma unroll
                 for (int j = 0; j < R / 8; ++j) {
                     const int c = l * (R / 8) + j;
-                    const uint4 v = make_uint4(mma::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
-                                               mma::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
-                                               mma::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
-                                               mma::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
+                    const uint4 v = make_uint4(bfp::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
+                                               bfp::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
+                                               bfp::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
+                                               bfp::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
                     st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7), v.x, v.y, v.z, v.w);
                     if (grow) st_global_v4(grow + 8 * c, v);
                 }
@@ -263,8 +263,8 @@ __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv,
 #pragma unroll
                     for (int r = 0; r < R; ++r) v[k * R + r] = ph[r] * scale;
                 }
-                const uint4 w = make_uint4(mma::pack_bf16(v[0], v[1]), mma::pack_bf16(v[2], v[3]),
-                                           mma::pack_bf16(v[4], v[5]), mma::pack_bf16(v[6], v[7]));
+                const uint4 w = make_uint4(bfp::pack_bf16(v[0], v[1]), bfp::pack_bf16(v[2], v[3]),
+                                           bfp::pack_bf16(v[4], v[5]), bfp::pack_bf16(v[6], v[7]));
                 st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7), w.x, w.y, w.z, w.w);
                 if (grow) st_global_v4(grow + 8 * c, w);
             }

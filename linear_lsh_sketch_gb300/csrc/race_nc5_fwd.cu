@@ -361,8 +361,8 @@ __global__ void __launch_bounds__(NTH, 1)
                     v[e] = (n <= D && k < Dm.LR) ? Sb[(int64_t)k * (D + 1) + n] : 0.f;
                 }
                 const bf16 h0 = __float2bfloat16_rn(v[0]), h1 = __float2bfloat16_rn(v[1]);
-                hw[j] = mma::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-                lw[j] = mma::pack_bf16(v[0] - __bfloat162float(h0), v[1] - __bfloat162float(h1));
+                hw[j] = bfp::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                lw[j] = bfp::pack_bf16(v[0] - __bfloat162float(h0), v[1] - __bfloat162float(h1));
             }
             const uint32_t off = (c >> 3) * Ly.sblk + sw_chunk(n, c & 7);
             st_shared_v4(base + Ly.shi + off, hw[0], hw[1], hw[2], hw[3]);
@@ -468,10 +468,10 @@ __global__ void __launch_bounds__(NTH, 1)
                 for (int j = 0; j < 2; ++j) {
                     const int ch = (c0 >> 3) + j;
                     st_shared_v4(xs + (ch >> 3) * BLK + sw_chunk(t, ch & 7),
-                                 mma::pack_bf16(v[8 * j] * rd, v[8 * j + 1] * rd),
-                                 mma::pack_bf16(v[8 * j + 2] * rd, v[8 * j + 3] * rd),
-                                 mma::pack_bf16(v[8 * j + 4] * rd, v[8 * j + 5] * rd),
-                                 mma::pack_bf16(v[8 * j + 6] * rd, v[8 * j + 7] * rd));
+                                 bfp::pack_bf16(v[8 * j] * rd, v[8 * j + 1] * rd),
+                                 bfp::pack_bf16(v[8 * j + 2] * rd, v[8 * j + 3] * rd),
+                                 bfp::pack_bf16(v[8 * j + 4] * rd, v[8 * j + 5] * rd),
+                                 bfp::pack_bf16(v[8 * j + 6] * rd, v[8 * j + 7] * rd));
                 }
             }
         }

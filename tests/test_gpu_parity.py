@@ -34,6 +34,14 @@ SMALL = [
     W_("bf_d128_c", 1, 2, 555, 128, 3, 3, True, "bf16"),
     W_("bf_lr256", 1, 2, 300, 128, 6, 4, False, "bf16", clusters=8),
     W_("bf_lr64_c", 2, 3, 257, 64, 4, 4, True, "bf16"),
+    # causal bf16 with L R = 48 at d = 128: forward on tcgen05, backward on the CUDA-core kernels
+    # (the tcgen05 backward's TMEM holds L R > 32 only at d = 64)
+    W_("bf_d128_lr48_c", 1, 2, 300, 128, 4, 3, True, "bf16"),
+    # L R = 64 at d = 64 with P = 6, 5, 3, 2 (run-time L) on the tcgen05 backward
+    W_("bf_p6_l1_c", 1, 2, 333, 64, 6, 1, True, "bf16"),
+    W_("bf_p5_l2_c", 1, 1, 300, 64, 5, 2, True, "bf16"),
+    W_("bf_p3_l8_c", 1, 1, 260, 64, 3, 8, True, "bf16"),
+    W_("bf_p2_l12_c", 1, 1, 200, 64, 2, 12, True, "bf16"),
     # shapes of the tcgen05 paths: bucket counts 2 .. 64, tables 1 .. 16, ragged tails, d 64 / 128
     W_("bf_p1_l16_c", 1, 2, 700, 64, 1, 16, True, "bf16"),
     W_("bf_p5_l1_c", 1, 1, 333, 128, 5, 1, True, "bf16"),
@@ -341,7 +349,8 @@ def test_c5_full_size_every_head():
 
 
 # d(loss)/d(beta): one workload per backward kernel family (CUDA-core non-causal / causal,
-# tcgen05 non-causal / causal, mma.sync causal L R = 64), ragged tails and several segments.
+# tcgen05 non-causal / causal, the tcgen05 causal backward at L R = 64), ragged tails and several
+# segments.
 DBETA = [
     W_("db_f32", 1, 2, 100, 64, 2, 2, False, "f32"),
     W_("db_f32_c", 1, 2, 100, 64, 2, 2, True, "f32"),
