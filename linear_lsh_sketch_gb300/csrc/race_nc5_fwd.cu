@@ -6,7 +6,8 @@
 // sum" (the per-table sketches A = Phi_K^T V and B = Phi_K^T 1) and "Normalize after combining
 // the tables" (O = sum_l Phi_Q A / sum_l Phi_Q B); reading notes sections 2.4-2.5.
 //
-// Both kernels walk 128-token tiles brought in by TMA (two stages).  Per tile one thread issues
+// Both kernels walk 128-token tiles brought in by TMA (two stages; three for the sketch's X tiles
+// when L R <= 64).  Per tile one thread issues
 // the projection z = X (W_hi + W_lo)^T on the tensor cores into TMEM; every thread turns its
 // token row of z into bucket probabilities (tanh, products of sigmoids) and writes them, bf16,
 // into a 128-byte-swizzled feature tile Phi (token rows, L * R columns).  Then:
@@ -29,17 +30,25 @@ constexpr int NTHW = NTH + 32;  // 8 compute warps + 1 control warp (TMA and MMA
 
 struct SketchLayout {
     uint32_t stg, x, y, f, fbytes, whi, wlo, mass, red, bar, slot, bytes;
-    int nmb, nf;
+    int nmb, nf, nx;
     __host__ __device__ SketchLayout(int D, int LR)
     {
         const uint32_t KB = D / 64;
         nmb = (LR + 127) / 128;
-        fbytes = 2 * nmb * BLK;  // one feature buffer: M = 128 sketch rows per block
+        // one feature buffer: M = 128 sketch rows per block, as two 64-column blocks; with L R <= 64
+        // the second block of each M = 128 operand is padding (its accumulator lanes are never
+        // read), so the buffer keeps only the first and the operand's second block points at the
+        // next 16 KB of shared memory (the other buffer, or the W tiles after it)
+        const bool half_f = LR <= 64;
+        fbytes = half_f ? BLK : 2 * nmb * BLK;
         const uint32_t fixed = 2 * 2 * KB * BLK + 2 * KB * WBLK + 2 * 4096 + 2 * 2 * C * 4 + 256;
         nf = (fixed + 2 * fbytes + 1024 <= 227 * 1024) ? 2 : 1;  // double-buffer the features if they fit
+        // a third X stage when it fits: the X tile of tile i + 3 is requested once tile i's
+        // features are in, which keeps enough bytes in flight to cover the load latency
+        nx = (half_f && fixed + KB * BLK + nf * fbytes + 1024 <= 227 * 1024) ? 3 : 2;
         stg = KB * BLK;
-        x = 0;                  // X stages [2][KB blocks]
-        y = x + 2 * stg;        // Y stages [2][KB blocks]
+        x = 0;                  // X stages [nx][KB blocks]
+        y = x + nx * stg;       // Y stages [2][KB blocks]
         f = y + 2 * stg;        // feature buffers [nf]
         whi = f + nf * fbytes;
         wlo = whi + KB * WBLK;
@@ -60,7 +69,8 @@ __host__ __device__ inline uint32_t sketch_tmem_cols(int D, int nmb)
 
 // The features of tile i + 1 can be ready before the issuing warp has observed those of tile i
 // (its projection is issued early), so "features ready" has one barrier per tile parity.
-enum : uint32_t { SB_X0, SB_X1, SB_Y0, SB_Y1, SB_P0, SB_P1, SB_S0, SB_S1, SB_F0, SB_F1, SB_CS, SB_DONE, SB_COUNT };
+enum : uint32_t { SB_X0, SB_X1, SB_X2, SB_Y0, SB_Y1, SB_P0, SB_P1, SB_S0, SB_S1, SB_F0, SB_F1, SB_CS, SB_DONE,
+                  SB_COUNT };
 
 // mode 0: X = K, Y = V, m = 1.  mode 1: X = Q, Y = dO, Phi scaled by aux.x = 1/den, m = -aux.y
 // (= -c, split into bf16 hi and lo rows).  part: [BH][nsplit][LR][d + 1] fp32.  frows (may be
@@ -81,7 +91,7 @@ __global__ void __launch_bounds__(NTHW, 1)
     const uint32_t base = (raw + 1023) & ~1023u;
     unsigned char *sm = smem_raw + (base - raw);
     const SketchLayout Ly(D, Dm.LR);
-    const int nmb = Ly.nmb, nf = Ly.nf;
+    const int nmb = Ly.nmb, nf = Ly.nf, nx = Ly.nx;
     float *red = reinterpret_cast<float *>(sm + Ly.red);
     auto bar = [&](uint32_t i) { return base + Ly.bar + 8 * i; };
     volatile int *abort = reinterpret_cast<volatile int *>(sm + Ly.slot + 8);
@@ -122,7 +132,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         // ---------------------------------------------------------------- control warp
         {  // the whole control warp, converged: one elected lane issues each copy and product
             auto load = [&](int i, bool is_y) {
-                const int s = i & 1;
+                const int s = is_y ? i & 1 : i % nx;
                 const uint32_t b = bar((is_y ? SB_Y0 : SB_X0) + s);
                 const uint32_t dst = base + (is_y ? Ly.y : Ly.x) + s * Ly.stg;
                 expect_tx_w(b, KB * BLK);
@@ -130,21 +140,23 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int kb = 0; kb < KB; ++kb)
                     tma_load_w(dst + kb * BLK, is_y ? &tmY : &tmX, 64 * kb, (int)(n_begin + (int64_t)i * C), (int)bh, b);
             };
-            int issued[4] = {0, 0, 0, 0}, done[4] = {0, 0, 0, 0};  // X0, X1, Y0, Y1
-            for (int i = 0; i < 2 && i < ntile; ++i) {
+            int issued[5] = {0, 0, 0, 0, 0}, done[5] = {0, 0, 0, 0, 0};  // X0, X1, X2, Y0, Y1
+            for (int i = 0; i < nx && i < ntile; ++i) {
                 load(i, false);
-                load(i, true);
                 ++issued[i];
-                ++issued[2 + i];
+            }
+            for (int i = 0; i < 2 && i < ntile; ++i) {
+                load(i, true);
+                ++issued[3 + i];
             }
             constexpr uint32_t id_v = idesc_bf16(128, D, 1, 1);
             constexpr uint32_t id_m = idesc_bf16(128, 16, 1, 0);
             auto proj = [&](int i) {
-                const int s = i & 1;
-                if (!wait_phase_w(bar(SB_X0 + s), (i >> 1) & 1, abort)) return false;
-                ++done[s];
+                const int s = i & 1, sx = i % nx;
+                if (!wait_phase_w(bar(SB_X0 + sx), (i / nx) & 1, abort)) return false;
+                ++done[sx];
                 fence_after();
-                issue_projection_w<D>(tmem + zcol + LPP * s, base + Ly.x + s * Ly.stg, base + Ly.whi, base + Ly.wlo);
+                issue_projection_w<D>(tmem + zcol + LPP * s, base + Ly.x + sx * Ly.stg, base + Ly.whi, base + Ly.wlo);
                 commit_w(bar(SB_P0 + s));
                 return true;
             };
@@ -154,7 +166,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 if (i + 1 < ntile && !(ok = proj(i + 1))) break;
                 if (!(ok = wait_phase_w(bar(SB_F0 + s), (i >> 1) & 1, abort))) break;
                 if (!(ok = wait_phase_w(bar(SB_Y0 + s), (i >> 1) & 1, abort))) break;
-                ++done[2 + s];
+                ++done[3 + s];
                 fence_after();
                 const uint32_t fbuf = base + Ly.f + (i % nf) * Ly.fbytes;
                 const uint32_t mbuf = base + Ly.mass + (mode ? (i & 1) * 4096 : 0);
@@ -163,30 +175,30 @@ __global__ void __launch_bounds__(NTHW, 1)
                     const uint32_t acc = tmem + m * 256;
 #pragma unroll
                     for (int ks = 0; ks < C / 16; ++ks) {
-                        const uint64_t a = desc_mn(fbuf + 2 * m * BLK + ks * 2048, BLK);
+                        const uint64_t a = desc_mn(fbuf + 2 * m * BLK + ks * 2048, BLK);  // rows 64+: next 16 KB
                         const bool accum = i > 0 || ks > 0;
                         umma_w(acc, a, desc_mn(ys + ks * 2048, BLK), id_v, accum);
                         umma_w(acc + D, a, desc_k(mbuf + (ks >> 2) * 2048 + (ks & 3) * 32), id_m, accum);
                     }
                 }
                 commit_w(bar(SB_S0 + s));
-                // X stage s: read by the projection and the norms of tile i (both done: features are in)
-                if (i + 2 < ntile) {
-                    load(i + 2, false);
-                    ++issued[s];
+                // X stage of tile i: read by its projection and norms (both done: features are in)
+                if (i + nx < ntile) {
+                    load(i + nx, false);
+                    ++issued[i % nx];
                 }
                 // Y stage s ^ 1: read by the sketch product of tile i - 1
                 if (i >= 1 && i + 1 < ntile) {
                     if (!(ok = wait_phase_w(bar(SB_S0 + (s ^ 1)), ((i - 1) >> 1) & 1, abort))) break;
                     load(i + 1, true);
-                    ++issued[2 + (s ^ 1)];
+                    ++issued[3 + (s ^ 1)];
                 }
             }
             if (ok) commit_w(bar(SB_DONE));
             if (!ok) {
                 if (lane == 0) atomicOr(err, kErrTimeout);
                 *abort = 1;
-                for (int b = 0; b < 4; ++b)
+                for (int b = 0; b < 5; ++b)
                     if (issued[b] > done[b]) mbar_wait(bar(SB_X0 + b), done[b] & 1);
             }
         }
@@ -198,9 +210,9 @@ __global__ void __launch_bounds__(NTHW, 1)
             const int s = i & 1;
             const int64_t n0 = n_begin + (int64_t)i * C;
             const int cnt = (int)min((int64_t)C, n_end - n0);
-            if (!(ok = wait_phase(bar(SB_X0 + s), (i >> 1) & 1, abort))) break;
+            if (!(ok = wait_phase(bar(SB_X0 + i % nx), (i / nx) & 1, abort))) break;
             float *rd_ = red + (i & 1) * 2 * C;
-            rd_[h * C + t] = half_sumsq<D>(base + Ly.x + s * Ly.stg, t, h);
+            rd_[h * C + t] = half_sumsq<D>(base + Ly.x + (i % nx) * Ly.stg, t, h);
             if (!(ok = group_sync(bar(SB_CS), i & 1, abort))) break;
             const float ssq = rd_[t] + rd_[C + t];
             const float inv = ssq > 0.f ? rsqrtf(ssq) : 0.f;
