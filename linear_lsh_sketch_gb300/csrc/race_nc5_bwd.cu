@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(NTH, 1)
     constexpr int R = 1 << P;
     constexpr int LMAX = LPP / P;
     constexpr int NPAIR = (LMAX + 1) / 2;
+    // with 32 or more buckets per table the per-table code is long: one copy of it, looped over
+    // the tables at run time (unrolled copies overflowed the instruction cache)
+    constexpr bool ROLL = R >= 32;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023) & ~1023u;
@@ -248,22 +251,30 @@ __global__ void __launch_bounds__(NTH, 1)
 
         // phase A: den and phi . g over this half's tables
         float den_p = 0.f, pg_p = 0.f;
+        auto den_table = [&](int l) {
+            float u[P], ph[R], g[R];
 #pragma unroll
-        for (int pr = 0; pr < NPAIR; ++pr) {
-            if ((pr & 1) != h || 2 * pr >= L) continue;
+            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+            tc::bucket_probs<P>(u, beta, ph);
+            ld_cols<R>(tlane + l * R, g);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int l = 2 * pr + k;
-                if (l >= LMAX || l >= L) continue;
-                float u[P], ph[R], g[R];
+            for (int r = 0; r < R; ++r) {
+                den_p = fmaf(ph[r], mass[l * R + r], den_p);
+                pg_p = fmaf(ph[r], g[r], pg_p);
+            }
+        };
+        if constexpr (ROLL) {
+#pragma unroll 1
+            for (int l = 2 * h; l < L; l += (l & 1) ? 3 : 1) den_table(l);  // pairs h, h + 2, ...
+        } else {
 #pragma unroll
-                for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
-                tc::bucket_probs<P>(u, beta, ph);
-                ld_cols<R>(tlane + l * R, g);
+            for (int pr = 0; pr < NPAIR; ++pr) {
+                if ((pr & 1) != h || 2 * pr >= L) continue;
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    den_p = fmaf(ph[r], mass[l * R + r], den_p);
-                    pg_p = fmaf(ph[r], g[r], pg_p);
+                for (int k = 0; k < 2; ++k) {
+                    const int l = 2 * pr + k;
+                    if (l >= LMAX || l >= L) continue;
+                    den_table(l);
                 }
             }
         }
@@ -278,31 +289,51 @@ __global__ void __launch_bounds__(NTH, 1)
         // phase B: dphi = (g - B c) / den, then the feature Jacobian -> dz (bf16 pairs in TMEM);
         // x . dxhat = z . dz (dxhat = W^T dz with dz as the product sees it, z = W x), this half's share
         float zdz = 0.f;
+        auto jac_table = [&](int l, float *dzl) {
+            float u[P], ph[R], g[R];
 #pragma unroll
-        for (int pr = 0; pr < NPAIR; ++pr) {
-            if ((pr & 1) != h || 2 * pr >= L) continue;
-            float dz[2 * P];
+            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+            tc::bucket_probs<P>(u, beta, ph);
+            ld_cols<R>(tlane + l * R, g);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int l = 2 * pr + k;
-                if (l >= LMAX || l >= L) {
+            for (int r = 0; r < R; ++r) g[r] = (g[r] - mass[l * R + r] * cc) * rd;
+            table_backward<P, DB>(u, ph, g, beta, dzl, &db);
 #pragma unroll
-                    for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
-                    continue;
+            for (int p = 0; p < P; ++p) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dzl[p])), z[l * P + p], zdz);
+        };
+        if constexpr (ROLL) {
+#pragma unroll 1
+            for (int pr = h; 2 * pr < L; pr += 2) {
+                float dz[2 * P];
+#pragma unroll 1
+                for (int k = 0; k < 2; ++k) {
+                    const int l = 2 * pr + k;
+                    if (l < L) {
+                        jac_table(l, dz + k * P);
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
+                    }
                 }
-                float u[P], ph[R], g[R];
-#pragma unroll
-                for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
-                tc::bucket_probs<P>(u, beta, ph);
-                ld_cols<R>(tlane + l * R, g);
-#pragma unroll
-                for (int r = 0; r < R; ++r) g[r] = (g[r] - mass[l * R + r] * cc) * rd;
-                table_backward<P, DB>(u, ph, g, beta, dz + k * P, &db);
-#pragma unroll
-                for (int p = 0; p < P; ++p)
-                    zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[k * P + p])), z[l * P + p], zdz);
+                st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
             }
-            st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
+        } else {
+#pragma unroll
+            for (int pr = 0; pr < NPAIR; ++pr) {
+                if ((pr & 1) != h || 2 * pr >= L) continue;
+                float dz[2 * P];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int l = 2 * pr + k;
+                    if (l >= LMAX || l >= L) {
+#pragma unroll
+                        for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
+                        continue;
+                    }
+                    jac_table(l, dz + k * P);
+                }
+                st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
+            }
         }
         red[(6 + h) * C + t] = zdz;
         wait_st();
@@ -393,6 +424,9 @@ __global__ void __launch_bounds__(NTH, 1)
     constexpr int R = 1 << P;
     constexpr int LMAX = LPP / P;
     constexpr int NPAIR = (LMAX + 1) / 2;
+    // with 32 or more buckets per table the per-table code is long: one copy of it, looped over
+    // the tables at run time (unrolled copies overflowed the instruction cache)
+    constexpr bool ROLL = R >= 32;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023) & ~1023u;
@@ -506,32 +540,52 @@ __global__ void __launch_bounds__(NTH, 1)
         // features -> TMEM (A operand of dV); dphi = V G_A^T + G_B -> feature Jacobian -> dz;
         // x . dxhat = z . dz (dxhat = W^T dz with dz as the product sees it, z = W x), this half's share
         float zdz = 0.f;
+        auto key_table = [&](int l, float *dzl) {
+            float u[P], ph[R], dph[R];
 #pragma unroll
-        for (int pr = 0; pr < NPAIR; ++pr) {
-            if ((pr & 1) != h || 2 * pr >= L) continue;
-            float dz[2 * P];
+            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+            tc::bucket_probs<P>(u, beta, ph);
+            st_bf16_cols<R>(tlane + fkc + l * (R / 2), ph);
+            ld_cols<R>(tlane + l * R, dph);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int l = 2 * pr + k;
-                if (l >= LMAX || l >= L) {
+            for (int r = 0; r < R; ++r) dph[r] += gmass[l * R + r];
+            table_backward<P, DB>(u, ph, dph, beta, dzl, &db);
 #pragma unroll
-                    for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
-                    continue;
+            for (int p = 0; p < P; ++p) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dzl[p])), z[l * P + p], zdz);
+        };
+        if constexpr (ROLL) {
+#pragma unroll 1
+            for (int pr = h; 2 * pr < L; pr += 2) {
+                float dz[2 * P];
+#pragma unroll 1
+                for (int k = 0; k < 2; ++k) {
+                    const int l = 2 * pr + k;
+                    if (l < L) {
+                        key_table(l, dz + k * P);
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
+                    }
                 }
-                float u[P], ph[R], dph[R];
-#pragma unroll
-                for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
-                tc::bucket_probs<P>(u, beta, ph);
-                st_bf16_cols<R>(tlane + fkc + l * (R / 2), ph);
-                ld_cols<R>(tlane + l * R, dph);
-#pragma unroll
-                for (int r = 0; r < R; ++r) dph[r] += gmass[l * R + r];
-                table_backward<P, DB>(u, ph, dph, beta, dz + k * P, &db);
-#pragma unroll
-                for (int p = 0; p < P; ++p)
-                    zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[k * P + p])), z[l * P + p], zdz);
+                st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
             }
-            st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
+        } else {
+#pragma unroll
+            for (int pr = 0; pr < NPAIR; ++pr) {
+                if ((pr & 1) != h || 2 * pr >= L) continue;
+                float dz[2 * P];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int l = 2 * pr + k;
+                    if (l >= LMAX || l >= L) {
+#pragma unroll
+                        for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
+                        continue;
+                    }
+                    key_table(l, dz + k * P);
+                }
+                st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
+            }
         }
         red[(6 + h) * C + t] = zdz;
         wait_st();

@@ -214,31 +214,39 @@ __host__ __device__ constexpr int feature_row_stride(int LR) { return (LR + 7) &
 // u = tanh(z inv) (the softmax over hypercube corners in product form), times `scale`.
 // Tables >= L inside a written chunk are zero.  grow (may be null): the token's stored feature
 // row in global memory (feature_row_stride(L R) bf16), which receives the same 16-byte chunks.
-template <int P>
+// ROLL: one copy of the per-table code, looped over the tables at run time (with 32 or more
+// buckets per table the unrolled copies overflow the instruction cache of the segment-sum pass;
+// the read-out measured faster unrolled).
+template <int P, bool ROLL = (1 << P) >= 32>
 __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv, float beta, int L, int h,
                                                float scale, int t, uint32_t ftile, bf16 *grow = nullptr)
 {
     constexpr int R = 1 << P;
     constexpr int LMAX = LPP / P;
     if constexpr (R >= 8) {
+        auto table = [&](int l) {
+            float u[P], ph[R];
 #pragma unroll
-        for (int l = 0; l < LMAX; ++l) {
-            if (l < L && (l & 1) == h) {
-                float u[P], ph[R];
+            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+            tc::bucket_probs<P>(u, beta, ph);
 #pragma unroll
-                for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
-                tc::bucket_probs<P>(u, beta, ph);
-#pragma unroll
-                for (int j = 0; j < R / 8; ++j) {
-                    const int c = l * (R / 8) + j;
-                    const uint4 v = make_uint4(bfp::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
-                                               bfp::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
-                                               bfp::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
-                                               bfp::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
-                    st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7), v.x, v.y, v.z, v.w);
-                    if (grow) st_global_v4(grow + 8 * c, v);
-                }
+            for (int j = 0; j < R / 8; ++j) {
+                const int c = l * (R / 8) + j;
+                const uint4 v = make_uint4(bfp::pack_bf16(ph[8 * j] * scale, ph[8 * j + 1] * scale),
+                                           bfp::pack_bf16(ph[8 * j + 2] * scale, ph[8 * j + 3] * scale),
+                                           bfp::pack_bf16(ph[8 * j + 4] * scale, ph[8 * j + 5] * scale),
+                                           bfp::pack_bf16(ph[8 * j + 6] * scale, ph[8 * j + 7] * scale));
+                st_shared_v4(ftile + (c >> 3) * BLK + sw_chunk(t, c & 7), v.x, v.y, v.z, v.w);
+                if (grow) st_global_v4(grow + 8 * c, v);
             }
+        };
+        if constexpr (ROLL) {
+#pragma unroll 1
+            for (int l = h; l < L; l += 2) table(l);
+        } else {
+#pragma unroll
+            for (int l = 0; l < LMAX; ++l)
+                if (l < L && (l & 1) == h) table(l);
         }
     } else {
         constexpr int TPC = 8 / R;
