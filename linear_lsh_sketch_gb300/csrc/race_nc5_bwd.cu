@@ -252,9 +252,10 @@ __global__ void __launch_bounds__(NTH, 1)
         // phase A: den and phi . g over this half's tables
         float den_p = 0.f, pg_p = 0.f;
         auto den_table = [&](int l) {
-            float u[P], ph[R], g[R];
+            float u[P], ph[R], g[R], zl[P];
+            table_z<P>(z, l, zl);
 #pragma unroll
-            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(zl[p] * inv);
             tc::bucket_probs<P>(u, beta, ph);
             ld_cols<R>(tlane + l * R, g);
 #pragma unroll
@@ -289,17 +290,18 @@ __global__ void __launch_bounds__(NTH, 1)
         // phase B: dphi = (g - B c) / den, then the feature Jacobian -> dz (bf16 pairs in TMEM);
         // x . dxhat = z . dz (dxhat = W^T dz with dz as the product sees it, z = W x), this half's share
         float zdz = 0.f;
-        auto jac_table = [&](int l, float *dzl) {
-            float u[P], ph[R], g[R];
+        auto jac_table = [&](int l, float (&dzl)[P]) {
+            float u[P], ph[R], g[R], zl[P];
+            table_z<P>(z, l, zl);
 #pragma unroll
-            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(zl[p] * inv);
             tc::bucket_probs<P>(u, beta, ph);
             ld_cols<R>(tlane + l * R, g);
 #pragma unroll
             for (int r = 0; r < R; ++r) g[r] = (g[r] - mass[l * R + r] * cc) * rd;
             table_backward<P, DB>(u, ph, g, beta, dzl, &db);
 #pragma unroll
-            for (int p = 0; p < P; ++p) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dzl[p])), z[l * P + p], zdz);
+            for (int p = 0; p < P; ++p) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dzl[p])), zl[p], zdz);
         };
         if constexpr (ROLL) {
 #pragma unroll 1
@@ -308,11 +310,17 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll 1
                 for (int k = 0; k < 2; ++k) {
                     const int l = 2 * pr + k;
+                    float dzl[P];
                     if (l < L) {
-                        jac_table(l, dz + k * P);
+                        jac_table(l, dzl);
                     } else {
 #pragma unroll
-                        for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
+                        for (int p = 0; p < P; ++p) dzl[p] = 0.f;
+                    }
+#pragma unroll
+                    for (int p = 0; p < P; ++p) {  // static indices: dz stays in registers
+                        if (k == 0) dz[p] = dzl[p];
+                        else dz[P + p] = dzl[p];
                     }
                 }
                 st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
@@ -330,7 +338,10 @@ __global__ void __launch_bounds__(NTH, 1)
                         for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
                         continue;
                     }
-                    jac_table(l, dz + k * P);
+                    float dzl[P];
+                    jac_table(l, dzl);
+#pragma unroll
+                    for (int p = 0; p < P; ++p) dz[k * P + p] = dzl[p];
                 }
                 st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
             }
@@ -540,10 +551,11 @@ __global__ void __launch_bounds__(NTH, 1)
         // features -> TMEM (A operand of dV); dphi = V G_A^T + G_B -> feature Jacobian -> dz;
         // x . dxhat = z . dz (dxhat = W^T dz with dz as the product sees it, z = W x), this half's share
         float zdz = 0.f;
-        auto key_table = [&](int l, float *dzl) {
-            float u[P], ph[R], dph[R];
+        auto key_table = [&](int l, float (&dzl)[P]) {
+            float u[P], ph[R], dph[R], zl[P];
+            table_z<P>(z, l, zl);
 #pragma unroll
-            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(zl[p] * inv);
             tc::bucket_probs<P>(u, beta, ph);
             st_bf16_cols<R>(tlane + fkc + l * (R / 2), ph);
             ld_cols<R>(tlane + l * R, dph);
@@ -551,7 +563,7 @@ __global__ void __launch_bounds__(NTH, 1)
             for (int r = 0; r < R; ++r) dph[r] += gmass[l * R + r];
             table_backward<P, DB>(u, ph, dph, beta, dzl, &db);
 #pragma unroll
-            for (int p = 0; p < P; ++p) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dzl[p])), z[l * P + p], zdz);
+            for (int p = 0; p < P; ++p) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dzl[p])), zl[p], zdz);
         };
         if constexpr (ROLL) {
 #pragma unroll 1
@@ -560,11 +572,17 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll 1
                 for (int k = 0; k < 2; ++k) {
                     const int l = 2 * pr + k;
+                    float dzl[P];
                     if (l < L) {
-                        key_table(l, dz + k * P);
+                        key_table(l, dzl);
                     } else {
 #pragma unroll
-                        for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
+                        for (int p = 0; p < P; ++p) dzl[p] = 0.f;
+                    }
+#pragma unroll
+                    for (int p = 0; p < P; ++p) {  // static indices: dz stays in registers
+                        if (k == 0) dz[p] = dzl[p];
+                        else dz[P + p] = dzl[p];
                     }
                 }
                 st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
@@ -582,7 +600,10 @@ __global__ void __launch_bounds__(NTH, 1)
                         for (int p = 0; p < P; ++p) dz[k * P + p] = 0.f;
                         continue;
                     }
-                    key_table(l, dz + k * P);
+                    float dzl[P];
+                    key_table(l, dzl);
+#pragma unroll
+                    for (int p = 0; p < P; ++p) dz[k * P + p] = dzl[p];
                 }
                 st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
             }

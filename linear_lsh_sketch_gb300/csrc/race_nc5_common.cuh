@@ -207,6 +207,23 @@ __device__ __forceinline__ void st_global_v4(void *p, uint4 v)
 // padded with zeros to a multiple of 8, so that every row is a whole number of 16-byte chunks.
 __host__ __device__ constexpr int feature_row_stride(int LR) { return (LR + 7) & ~7; }
 
+// The P projections of table l (run time, warp-uniform) from the register array z, by selects:
+// indexing z with a run-time l would move it to local memory.
+template <int P>
+__device__ __forceinline__ void table_z(const float (&z)[LPP], int l, float (&zl)[P])
+{
+    constexpr int LMAX = LPP / P;
+#pragma unroll
+    for (int p = 0; p < P; ++p) zl[p] = z[p];
+#pragma unroll
+    for (int j = 1; j < LMAX; ++j) {
+        if (l == j) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) zl[p] = z[j * P + p];
+        }
+    }
+}
+
 // Writes one token row of bucket features into an SW128 feature tile ([lr / 64][C][64] bf16,
 // lr = l R + r), for the tables half h owns: tables l with l % 2 == h when R >= 8, else 16-byte
 // chunks (8 / R tables each) with chunk % 2 == h.  z holds the row's projections W x (LPP
@@ -225,9 +242,10 @@ __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv,
     constexpr int LMAX = LPP / P;
     if constexpr (R >= 8) {
         auto table = [&](int l) {
-            float u[P], ph[R];
+            float u[P], ph[R], zl[P];
+            table_z<P>(z, l, zl);
 #pragma unroll
-            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(z[l * P + p] * inv);
+            for (int p = 0; p < P; ++p) u[p] = tc::tanh_abs(zl[p] * inv);
             tc::bucket_probs<P>(u, beta, ph);
 #pragma unroll
             for (int j = 0; j < R / 8; ++j) {
