@@ -232,8 +232,7 @@ __device__ __forceinline__ void table_z(const float (&z)[LPP], int l, float (&zl
 // Tables >= L inside a written chunk are zero.  grow (may be null): the token's stored feature
 // row in global memory (feature_row_stride(L R) bf16), which receives the same 16-byte chunks.
 // ROLL: one copy of the per-table code, looped over the tables at run time (with 32 or more
-// buckets per table the unrolled copies overflow the instruction cache of the segment-sum pass;
-// the read-out measured faster unrolled).
+// buckets per table the unrolled copies overflow the instruction cache).
 template <int P, bool ROLL = (1 << P) >= 32>
 __device__ __forceinline__ void write_features(const float (&z)[LPP], float inv, float beta, int L, int h,
                                                float scale, int t, uint32_t ftile, bf16 *grow = nullptr)

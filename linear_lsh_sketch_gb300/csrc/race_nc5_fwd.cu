@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(NTH, 1)
         }
         const float ssq = red[t] + red[C + t];
         const float inv = ssq > 0.f ? rsqrtf(ssq) : 0.f;
-        write_features<P, false>(z, inv, Dm.beta, LT > 0 ? LT : Dm.L, h, t < cnt ? 1.f : 0.f, t, base + Ly.f);
+        write_features<P>(z, inv, Dm.beta, LT > 0 ? LT : Dm.L, h, t < cnt ? 1.f : 0.f, t, base + Ly.f);
         tc::fence_proxy_async();
         fence_before();
         __syncthreads();
