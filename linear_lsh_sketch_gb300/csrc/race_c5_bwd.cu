@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 atomicOr(err, kErrTimeout);
                 *abort = 1;
                 const uint32_t bars[4] = {0u, bar(B_V), bar(B_DO), bar(B_K)};
+#pragma unroll
                 for (int b = 1; b < 4; ++b)
                     if (issued[b] > done[b]) mbar_wait(bars[b], done[b] & 1);
             }
@@ -1058,6 +1059,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 atomicOr(err, kErrTimeout);
                 *abort = 1;
                 const uint32_t bars[3] = {bar(B_QK), bar(B_V), bar(B_DO)};
+#pragma unroll
                 for (int b = 0; b < 3; ++b)
                     if (issued[b] > done[b]) mbar_wait(bars[b], done[b] & 1);
             }

@@ -235,7 +235,8 @@ __global__ void __launch_bounds__(NTHW, 1)
                 bulk_commit();
             };
             // loads issued and completions waited for, per barrier (to drain after an abort)
-            int qk_issued = 0, qk_done = 0, v_issued[2] = {0, 0}, v_done[2] = {0, 0};
+            int qk_issued = 0, qk_done = 0;
+            Counts<2> v_issued, v_done;
             if (nchunk > 0) {
                 // withhold (a test of the failure path): the first Q / K tiles are never requested,
                 // so every wait on them runs out and the CTA takes the abort path below
@@ -244,10 +245,10 @@ __global__ void __launch_bounds__(NTHW, 1)
                     ++qk_issued;
                 }
                 load_v(0);
-                ++v_issued[0];
+                v_issued.inc(0);
                 if (nchunk > 1) {
                     load_v(1);
-                    ++v_issued[1];
+                    v_issued.inc(1);
                 }
             }
             constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 if (!(ok = wait_phase(bar(B_SOP), c & 1, abort))) break;
                 if (c >= 1) store_out(c - 1);
                 if (!(ok = wait_phase(bar(B_V0 + (c & 1)), (c >> 1) & 1, abort))) break;
-                ++v_done[c & 1];
+                v_done.inc(c & 1);
                 fence_after();
                 const uint64_t d_v = desc_mn(vst, BLK);
                 const uint64_t d_vt = desc_mn(vst, D == 128 ? BLK : (Ly.zero - (Ly.v + (c & 1) * Ly.kbb)));
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 if (c >= 1 && c + 1 < nchunk) {
                     bulk_wait_read0();
                     load_v(c + 1);
-                    ++v_issued[(c + 1) & 1];
+                    v_issued.inc((c + 1) & 1);
                 }
             }
             if (ok && nchunk > 0) {
@@ -340,8 +341,9 @@ __global__ void __launch_bounds__(NTHW, 1)
                 *abort = 1;
                 // let copies still in flight land before the CTA's shared memory goes away
                 if (qk_issued > qk_done) mbar_wait(bar(B_QK), qk_done & 1);
+#pragma unroll
                 for (int b = 0; b < 2; ++b)
-                    if (v_issued[b] > v_done[b]) mbar_wait(bar(B_V0 + b), v_done[b] & 1);
+                    if (v_issued.v[b] > v_done.v[b]) mbar_wait(bar(B_V0 + b), v_done.v[b] & 1);
             }
             bulk_wait0();
         }

@@ -129,6 +129,24 @@ __device__ __forceinline__ bool wait_phase_w(uint32_t bar, uint32_t parity, vola
     return false;
 }
 
+// Per-barrier counts of copies issued or waited for (to drain the copies in flight after an
+// abort), kept in registers: a run-time index into a plain array would put it in local memory,
+// whose lines the small L1 left beside a large shared-memory carve-out does not keep.
+template <int N>
+struct Counts {
+    int v[N];
+    __device__ __forceinline__ Counts()
+    {
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = 0;
+    }
+    __device__ __forceinline__ void inc(int b)
+    {
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] += j == b ? 1 : 0;
+    }
+};
+
 // Non-blocking check of the phase with parity `parity`.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
 {

@@ -140,21 +140,21 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int kb = 0; kb < KB; ++kb)
                     tma_load_w(dst + kb * BLK, is_y ? &tmY : &tmX, 64 * kb, (int)(n_begin + (int64_t)i * C), (int)bh, b);
             };
-            int issued[5] = {0, 0, 0, 0, 0}, done[5] = {0, 0, 0, 0, 0};  // X0, X1, X2, Y0, Y1
+            Counts<5> issued, done;  // X0, X1, X2, Y0, Y1
             for (int i = 0; i < nx && i < ntile; ++i) {
                 load(i, false);
-                ++issued[i];
+                issued.inc(i);
             }
             for (int i = 0; i < 2 && i < ntile; ++i) {
                 load(i, true);
-                ++issued[3 + i];
+                issued.inc(3 + i);
             }
             constexpr uint32_t id_v = idesc_bf16(128, D, 1, 1);
             constexpr uint32_t id_m = idesc_bf16(128, 16, 1, 0);
             auto proj = [&](int i) {
                 const int s = i & 1, sx = i % nx;
                 if (!wait_phase_w(bar(SB_X0 + sx), (i / nx) & 1, abort)) return false;
-                ++done[sx];
+                done.inc(sx);
                 fence_after();
                 issue_projection_w<D>(tmem + zcol + LPP * s, base + Ly.x + sx * Ly.stg, base + Ly.whi, base + Ly.wlo);
                 commit_w(bar(SB_P0 + s));
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 if (i + 1 < ntile && !(ok = proj(i + 1))) break;
                 if (!(ok = wait_phase_w(bar(SB_F0 + s), (i >> 1) & 1, abort))) break;
                 if (!(ok = wait_phase_w(bar(SB_Y0 + s), (i >> 1) & 1, abort))) break;
-                ++done[3 + s];
+                done.inc(3 + s);
                 fence_after();
                 const uint32_t fbuf = base + Ly.f + (i % nf) * Ly.fbytes;
                 const uint32_t mbuf = base + Ly.mass + (mode ? (i & 1) * 4096 : 0);
@@ -185,21 +185,22 @@ __global__ void __launch_bounds__(NTHW, 1)
                 // X stage of tile i: read by its projection and norms (both done: features are in)
                 if (i + nx < ntile) {
                     load(i + nx, false);
-                    ++issued[i % nx];
+                    issued.inc(i % nx);
                 }
                 // Y stage s ^ 1: read by the sketch product of tile i - 1
                 if (i >= 1 && i + 1 < ntile) {
                     if (!(ok = wait_phase_w(bar(SB_S0 + (s ^ 1)), ((i - 1) >> 1) & 1, abort))) break;
                     load(i + 1, true);
-                    ++issued[3 + (s ^ 1)];
+                    issued.inc(3 + (s ^ 1));
                 }
             }
             if (ok) commit_w(bar(SB_DONE));
             if (!ok) {
                 if (lane == 0) atomicOr(err, kErrTimeout);
                 *abort = 1;
+#pragma unroll
                 for (int b = 0; b < 5; ++b)
-                    if (issued[b] > done[b]) mbar_wait(bar(SB_X0 + b), done[b] & 1);
+                    if (issued.v[b] > done.v[b]) mbar_wait(bar(SB_X0 + b), done.v[b] & 1);
             }
         }
         __syncwarp();
