@@ -29,9 +29,10 @@
  *    row lands in one corner per table.  A projection that is exactly 0 splits the row evenly
  *    over the two corners it separates (the limit sigmoid(0) = 1/2), so a zero row is uniform.
  *    The features are computed as the soft ones at beta = 2^126, which equals the sign rule
- *    exactly for every projection u with |u| >= 2^-119 and at u = 0.  No gradient reaches Q, K or
- *    beta (dQ = dK = 0, dbeta = 0); dV is the hard sketch's.  A query whose corners hold no key
- *    in any table has a zero denominator (its output is 0/0), which small inputs can meet.
+ *    exactly for every projection u with |u| >= 2^-119 and at u = 0.  No gradient reaches Q, K,
+ *    beta or W (dQ = dK = 0, dbeta = 0, dW = 0); dV is the hard sketch's.  A query whose corners
+ *    hold no key in any table has a zero denominator (its output is 0/0), which small inputs can
+ *    meet.
  *  - Limits: N >= 1; B * H <= 65535; d a multiple of 8 in [8, 128]; 1 <= P <= 8; 1 <= L <= 16;
  *    L * 2^P <= 256.
  *  - The caller owns every buffer, including `workspace` (size from race_attn_workspace_bytes)
@@ -77,8 +78,9 @@ typedef struct {
 } race_shape;
 
 /*
- * Bytes of scratch memory race_attn_fwd (is_bwd = 0) or race_attn_bwd (is_bwd = 1) needs for
- * this problem.  Returns 0 if the arguments are invalid.  Host function: it launches nothing,
+ * Bytes of scratch memory race_attn_fwd (is_bwd = 0), race_attn_bwd (is_bwd = 1) or
+ * race_attn_bwd with a dW output (is_bwd = 2: also every row's dz / |x|, 8 L P bytes per token and
+ * (b, h)) needs for this problem.  Returns 0 if the arguments are invalid.  Host function: it launches nothing,
  * but it queries the current device's multiprocessor count (152 when there is no device).
  */
 size_t race_attn_workspace_bytes(const race_shape *shape, int L, int P, int causal, int is_bwd);
@@ -127,14 +129,22 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
  * probabilities.  The gradient of the one shared beta is the sum of the B * H values.  Each
  * value is a sum in a fixed order (per-CTA partials, then a combine), so repeated calls give the
  * same bits.  Overwritten, not accumulated.
+ * dW: NULL, or device float32 [B, H, L, P, d] (4-byte aligned) that receives d(loss)/d(W) for
+ * each (b, h).  The hyperplanes project the unit rows, z = W x / |x| (slides, frame "Soft corner
+ * assignments make hashing differentiable"), so with dz the gradient at z of a Q or K row (the
+ * tanh and softmax Jacobians above) d(loss)/d(W) = sum over the Q and K rows of dz (x / |x|)^T.
+ * The backward kernels write each row's dz / |x| to the workspace and a reduction forms the sum
+ * per (b, h) in a fixed order (repeated calls give the same bits).  A W shared by every head has
+ * the sum over b and h as its gradient; a per-head W (per_head_w = 1) the sum over b.  Needs
+ * race_attn_workspace_bytes(..., is_bwd = 2) bytes of workspace.  Zero for a hard hash.
+ * Overwritten, not accumulated.
  * state: NULL (the sketch is recomputed from K and V), or the buffer a race_attn_fwd call
  * with the same Q, K, V, W, beta, L, P and causal filled in.
- * The gradient with respect to W is not produced.
  */
 int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const void *V,
                   const float *W, float beta, int L, int P, int causal, const void *O,
-                  const void *dO, void *dQ, void *dK, void *dV, float *dbeta, const void *state,
-                  void *workspace, size_t workspace_bytes, void *stream);
+                  const void *dO, void *dQ, void *dK, void *dV, float *dbeta, float *dW,
+                  const void *state, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Forward pass for callers that cannot allocate device memory (no counterpart in the paper).

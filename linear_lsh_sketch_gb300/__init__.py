@@ -61,7 +61,7 @@ def load_library():
     L.race_attn_state_bytes.restype = sz
     L.race_attn_fwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, sz, vp]
     L.race_attn_fwd.restype = i
-    L.race_attn_bwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.race_attn_bwd.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.race_attn_bwd.restype = i
     L.race_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, f, i, i, i, vp, vp]
     L.race_attn_fwd_noalloc.restype = i
@@ -240,10 +240,12 @@ def race_attn_fwd(Q, K, V, W, beta, L, P, causal, O=None, state=None, workspace=
 
 
 def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, dV=None, state=None,
-                  workspace=None, stream=None, want_dbeta=False, dbeta=None):
+                  workspace=None, stream=None, want_dbeta=False, dbeta=None, want_dW=False, dW=None):
     """(dQ, dK, dV) of RACE attention for the output cotangent dO; allocates what is not given.
     With want_dbeta (or a float32 [B, H] `dbeta` given) also d(loss)/d(beta) per (b, h), returned
-    as a fourth element; the shared beta's gradient is its sum."""
+    next; the shared beta's gradient is its sum.  With want_dW (or a float32 [B, H, L, P, d] `dW`
+    given) also d(loss)/d(W) per (b, h), returned last; a shared W's gradient is its sum over b
+    and h, a per-head W's its sum over b."""
     with torch.cuda.device(Q.device):
         shape = _shape_of(Q, W, L, P)
         for n, t in (("K", K), ("V", V), ("dO", dO), ("Q", Q)):
@@ -258,17 +260,23 @@ def race_attn_bwd(Q, K, V, W, beta, L, P, causal, dO, O=None, dQ=None, dK=None, 
         if dbeta is not None and (dbeta.dtype != torch.float32 or tuple(dbeta.shape) != tuple(Q.shape[:2])
                                   or not dbeta.is_contiguous() or dbeta.device != Q.device):
             raise ValueError("dbeta must be a contiguous float32 tensor of shape [B, H] on Q's device")
-        ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 1)
+        dw_shape = (Q.shape[0], Q.shape[1], L, P, Q.shape[3])
+        if dW is None and want_dW:
+            dW = torch.empty(dw_shape, dtype=torch.float32, device=Q.device)
+        if dW is not None and (dW.dtype != torch.float32 or tuple(dW.shape) != dw_shape or not dW.is_contiguous()
+                               or dW.device != Q.device):
+            raise ValueError("dW must be a contiguous float32 tensor of shape [B, H, L, P, d] on Q's device")
+        ws_bytes = race_attn_workspace_bytes(shape, L, P, causal, 2 if dW is not None else 1)
         if ws_bytes == 0:
             raise RaceAttnError(-1, "race_attn_bwd")
         workspace = _bytes_buffer(ws_bytes, Q.device, workspace)
         rc = load_library().race_attn_bwd(
             ctypes.byref(shape), _ptr(Q), _ptr(K), _ptr(V), _ptr(W), float(beta), int(L), int(P),
-            int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dbeta), _ptr(state),
+            int(causal), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dbeta), _ptr(dW), _ptr(state),
             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
         if rc != 0:
             raise RaceAttnError(rc, "race_attn_bwd")
-        return (dQ, dK, dV) if dbeta is None else (dQ, dK, dV, dbeta)
+        return (dQ, dK, dV) + ((dbeta,) if dbeta is not None else ()) + ((dW,) if dW is not None else ())
 
 
 def race_attn_decode(q, k, v, W, beta, L, P, state, o=None, stream=None):

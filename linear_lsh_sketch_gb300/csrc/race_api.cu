@@ -135,7 +135,9 @@ struct Plan {
     size_t state_fk = 0;   // causal tcgen05 path: the same two arrays inside `state`
     size_t state_kinv = 0;
     int64_t db_cap = 0;    // partial slots per (side, b, h): at least every backward kernel's grid x
-    size_t ws_fwd = 0, ws_bwd = 0, state = 0;
+    size_t off_dzq = 0, off_dzk = 0, off_dwpart = 0;  // d(loss)/d(W): dz / |x| rows, then partials
+    int dw_nblk = 1;       // token ranges per (b, h) of the d(loss)/d(W) reduction
+    size_t ws_fwd = 0, ws_bwd = 0, ws_bwd_dw = 0, state = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -211,6 +213,12 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     pl.off_fq = align256(pl.off_db + 2 * (size_t)D.BH * pl.db_cap * sizeof(float));
     const size_t fq_bytes = (pl.c5 && c5_bwd_supported(D)) ? c5_feature_rows_bytes(D) : 0;
     pl.ws_bwd = align256(pl.off_fq + fq_bytes);
+    pl.dw_nblk = (int)std::max<int64_t>(1, std::min(ceil_div(D.N, 32), ceil_div(2 * (int64_t)D.sms, D.BH)));
+    const size_t dz_bytes = (size_t)D.BH * D.N * D.LP * sizeof(float);
+    pl.off_dzq = pl.ws_bwd;
+    pl.off_dzk = align256(pl.off_dzq + dz_bytes);
+    pl.off_dwpart = align256(pl.off_dzk + dz_bytes);
+    pl.ws_bwd_dw = align256(pl.off_dwpart + (size_t)D.BH * pl.dw_nblk * D.LP * D.d * sizeof(float));
     pl.state_fk = align256(sk_bytes);
     pl.state_kinv = align256(pl.state_fk + fk_bytes);
     pl.state = pl.c5 ? pl.state_kinv + kinv_bytes : sk_bytes;
@@ -309,7 +317,9 @@ struct DbetaOut {
 
 cudaError_t dbeta_begin(const Plan &pl, char *ws, float *dbeta, int slots, DbetaOut &db, cudaStream_t st)
 {
-    if (!dbeta) return cudaSuccess;
+    // the kernels' d(beta) instances also write the rows' dz when d(loss)/d(W) is asked for, so
+    // they run then too (their d(beta) partials go unused without a dbeta output)
+    if (!dbeta && pl.D.dzq == nullptr) return cudaSuccess;
     db.slots = slots;
     db.out = dbeta;
     db.dbq = (float *)(ws + pl.off_db);
@@ -410,7 +420,7 @@ size_t race_attn_workspace_bytes(const race_shape *shape, int L, int P, int caus
 {
     Plan pl;
     if (make_plan(shape, L, P, causal, pl) != RACE_OK) return 0;
-    return is_bwd ? pl.ws_bwd : pl.ws_fwd;
+    return is_bwd == 2 ? pl.ws_bwd_dw : is_bwd ? pl.ws_bwd : pl.ws_fwd;
 }
 
 size_t race_attn_state_bytes(const race_shape *shape, int L, int P, int causal)
@@ -446,7 +456,8 @@ int race_attn_fwd(const race_shape *shape, const void *Q, const void *K, const v
 
 int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const void *V, const float *W, float beta,
                   int L, int P, int causal, const void *O, const void *dO, void *dQ, void *dK, void *dV,
-                  float *dbeta, const void *state, void *workspace, size_t workspace_bytes, void *stream)
+                  float *dbeta, float *dW, const void *state, void *workspace, size_t workspace_bytes,
+                  void *stream)
 {
     (void)O;
     Plan pl;
@@ -456,11 +467,16 @@ int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const v
     if (!Q || !K || !V || !W || !dO || !dQ || !dK || !dV || !workspace) return RACE_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(W) || !aligned16(dO) || !aligned16(dQ) ||
         !aligned16(dK) || !aligned16(dV) || !aligned16(workspace) || (state && !aligned16(state)) ||
-        ((uintptr_t)dbeta & 3) != 0)
+        ((uintptr_t)dbeta & 3) != 0 || ((uintptr_t)dW & 3) != 0)
         return RACE_ERR_ALIGN;
-    if (workspace_bytes < pl.ws_bwd) return RACE_ERR_WORKSPACE;
+    if (workspace_bytes < (dW ? pl.ws_bwd_dw : pl.ws_bwd)) return RACE_ERR_WORKSPACE;
     pl.D.beta = kernel_beta(beta);
     cudaStream_t st = (cudaStream_t)stream;
+    const bool want_dw = dW != nullptr && !hard_hash(beta);
+    if (want_dw) {  // the backward kernels also write every row's dz / |x|
+        pl.D.dzq = (float *)((char *)workspace + pl.off_dzq);
+        pl.D.dzk = (float *)((char *)workspace + pl.off_dzk);
+    }
     if (pl.bf16)
         rc = backward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
                                           (const __nv_bfloat16 *)V, W, (const __nv_bfloat16 *)dO,
@@ -470,10 +486,18 @@ int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const v
         rc = backward_impl<float>(pl, (const float *)Q, (const float *)K, (const float *)V, W, (const float *)dO,
                                   (float *)dQ, (float *)dK, (float *)dV, dbeta, (const float *)state,
                                   (char *)workspace, st);
-    if (rc == RACE_OK && hard_hash(beta)) {  // a hard hash passes no gradient to Q and K
+    if (rc == RACE_OK && want_dw) {
+        float *dwpart = (float *)((char *)workspace + pl.off_dwpart);
+        if (pl.bf16)
+            RACE_TRY(launch_dw(pl.D, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K, pl.dw_nblk, dwpart, dW, st));
+        else
+            RACE_TRY(launch_dw(pl.D, (const float *)Q, (const float *)K, pl.dw_nblk, dwpart, dW, st));
+    }
+    if (rc == RACE_OK && hard_hash(beta)) {  // a hard hash passes no gradient to Q, K or W
         const size_t bytes = (size_t)pl.D.BH * pl.D.N * pl.D.d * (pl.bf16 ? 2 : 4);
         RACE_TRY(cudaMemsetAsync(dQ, 0, bytes, st));
         RACE_TRY(cudaMemsetAsync(dK, 0, bytes, st));
+        if (dW) RACE_TRY(cudaMemsetAsync(dW, 0, (size_t)pl.D.BH * pl.D.LP * pl.D.d * sizeof(float), st));
     }
     return rc;
 }

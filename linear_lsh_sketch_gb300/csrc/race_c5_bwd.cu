@@ -617,6 +617,12 @@ __global__ void __launch_bounds__(NTHW, 1)
                     if (j < LP) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[j])), zk_s[j * C + t], zdz);
                 wait_st();
                 warp_signal(bar(B_JAC));
+                if (Dm.dzk != nullptr && live) {  // d(loss)/d(W): this K row's dz / |k|
+                    float *o = Dm.dzk + (bh * Dm.N + n0 + t) * LP;
+#pragma unroll
+                    for (int j = 0; j < LMAX * P; ++j)
+                        if (j < LP) o[j] = dz[j] * inv;
+                }
             } else {
                 // dV row t = F_K G_A + P2 dO, straight to global memory
                 bf16 *dst = dV + off + (n0 + t) * D;
@@ -1316,6 +1322,13 @@ __global__ void __launch_bounds__(NTHW, 1)
                 *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
                 wait_st();
                 warp_signal(bar(B_JAC));
+                if (Dm.dzq != nullptr && live) {  // d(loss)/d(W): this Q row's dz / |q|
+                    float *o = Dm.dzq + (bh * Dm.N + n0 + t) * LP;
+                    const float iq = invq_s[t];
+#pragma unroll
+                    for (int j = 0; j < LPP; ++j)
+                        if (j < LP) o[j] = dz[j] * iq;
+                }
             } else {
                 // the sketch after this chunk -> bf16 operand and B_prev of the next chunk
                 convert_s(par ^ 1);

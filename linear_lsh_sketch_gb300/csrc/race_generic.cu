@@ -118,7 +118,7 @@ __device__ void featurise(const float *xs, const Dims &D, const float *ws, int f
 __device__ float featurise_backward(const float *xs, const Dims &D, const float *ws,
                                     const float *inv_s, const float *u_s, const float *f_s,
                                     const float *dphi_s, int fst, float *dz_s, float *dx_s,
-                                    float *red_s)
+                                    float *red_s, float *dz_g = nullptr, int cnt = 0)
 {
     float db = 0.f;
     const int dp = D.d + 1;
@@ -147,6 +147,8 @@ __device__ float featurise_backward(const float *xs, const Dims &D, const float 
         }
     }
     __syncthreads();
+    if (dz_g)  // the tile's live rows of dz / |x| (d(loss)/d(W) is their product with the rows)
+        for (int i = threadIdx.x; i < cnt * D.LP; i += NT) dz_g[i] = dz_s[i] * inv_s[i / D.LP];
     for (int i = threadIdx.x; i < TT * D.d; i += NT) {
         const int t = i / D.d, k = i - t * D.d;
         float s = 0.f;
@@ -417,6 +419,55 @@ __global__ void __launch_bounds__(256) k_dbeta_combine(const float *__restrict__
     if (threadIdx.x == 0) out[bh] = s;
 }
 
+// d(loss)/d(W) of problem bh, partial over the token range [blockIdx.x * span, + span): the
+// projection z = W xhat has d(loss)/d(W) = sum over Q and K rows of dz xhat^T, and the backward
+// kernels stored dz / |x| per row, so part[bh][blockIdx.x][lp][k] = sum over the range's rows n
+// of dzq[n][lp] Q[n][k] + dzk[n][lp] K[n][k], in a fixed order (tiles of 32 rows, the Q rows then
+// the K rows of each).  Grid (blocks, BH), NT threads, 32 (d + L P) floats of shared memory.
+constexpr int DW_ROWS = 32;
+constexpr int DW_EPT = (64 * kMaxD + NT - 1) / NT;  // (lp, k) entries per thread, L P <= 64
+
+template <typename T>
+__global__ void __launch_bounds__(NT) k_dw_partial(Dims D, const T *__restrict__ Q, const T *__restrict__ K,
+                                                    int64_t span, float *__restrict__ part)
+{
+    extern __shared__ float sm[];
+    const int d = D.d, LP = D.LP, E = LP * d;
+    float *xs = sm, *zs = sm + DW_ROWS * d;
+    const int64_t bh = blockIdx.y;
+    const int64_t r0 = (int64_t)blockIdx.x * span, r1 = min(D.N, r0 + span);
+    float acc[DW_EPT];
+#pragma unroll
+    for (int j = 0; j < DW_EPT; ++j) acc[j] = 0.f;
+    for (int64_t n0 = r0; n0 < r1; n0 += DW_ROWS) {
+        const int cnt = (int)min((int64_t)DW_ROWS, r1 - n0);
+        for (int side = 0; side < 2; ++side) {
+            const T *X = (side ? K : Q) + (bh * D.N + n0) * d;
+            const float *Z = (side ? D.dzk : D.dzq) + (bh * D.N + n0) * LP;
+            __syncthreads();
+            for (int i = threadIdx.x; i < cnt * d; i += NT) xs[i] = ld_f(X, i);
+            for (int i = threadIdx.x; i < cnt * LP; i += NT) zs[i] = Z[i];
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < DW_EPT; ++j) {
+                const int e = threadIdx.x + j * NT;
+                if (e < E) {
+                    const int lp = e / d, k = e - lp * d;
+                    float a = acc[j];
+                    for (int r = 0; r < cnt; ++r) a = fmaf(zs[r * LP + lp], xs[r * d + k], a);
+                    acc[j] = a;
+                }
+            }
+        }
+    }
+    float *out = part + ((int64_t)bh * gridDim.x + blockIdx.x) * E;
+#pragma unroll
+    for (int j = 0; j < DW_EPT; ++j) {
+        const int e = threadIdx.x + j * NT;
+        if (e < E) out[e] = acc[j];
+    }
+}
+
 // Non-causal read-out: O_t = sum_f phi_f(Q_t) A[f] / sum_f phi_f(Q_t) B[f] with S = [A | B]
 // ([BH][LR][dv]).  Grid (ceil(N / TT), BH).
 template <typename T>
@@ -524,7 +575,8 @@ __global__ void __launch_bounds__(NT) k_bwd_query(Dims D, const T *__restrict__ 
         gs[t * fst + f] = (gs[t * fst + f] - sb[f] * cc[t]) / den[t];
     }
     __syncthreads();
-    const float db = featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red);
+    const float db = featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red,
+                                        D.dzq ? D.dzq + (bh * D.N + n0) * D.LP : nullptr, cnt);
     T *dQb = dQ + bh * D.N * D.d;
     for (int i = threadIdx.x; i < cnt * D.d; i += NT) {
         const int t = i / D.d, c = i - t * D.d;
@@ -584,7 +636,8 @@ __global__ void __launch_bounds__(NT) k_bwd_key(Dims D, const T *__restrict__ K,
         }
     }
     __syncthreads();
-    const float db = featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red);
+    const float db = featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red,
+                                        D.dzk ? D.dzk + (bh * D.N + n0) * D.LP : nullptr, cnt);
     T *dKb = dK + bh * D.N * D.d, *dVb = dV + bh * D.N * D.d;
 #pragma unroll
     for (int k = 0; k < KOUT; ++k) {
@@ -740,7 +793,8 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_q(Dims D, const T *__restrict
             gs[t * fst + f] = (gs[t * fst + f] - sb * cc[t]) / den[t];
         }
         __syncthreads();
-        db += featurise_backward(xq, D, ws, invq, us, fq, gs, fst, dz, dx, red);
+        db += featurise_backward(xq, D, ws, invq, us, fq, gs, fst, dz, dx, red,
+                                 D.dzq ? D.dzq + (bh * D.N + n0) * D.LP : nullptr, cnt);
         for (int i = threadIdx.x; i < cnt * D.d; i += NT) {
             const int t = i / D.d, c = i - t * D.d;
             st_f(dQ + off, (n0 + t) * D.d + c, dx[t * dp + c]);
@@ -840,7 +894,8 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_kv(Dims D, const T *__restric
             gs[j * fst + f] = g;
         }
         __syncthreads();
-        db += featurise_backward(xk, D, ws, invk, us, fk, gs, fst, dz, dx, red);
+        db += featurise_backward(xk, D, ws, invk, us, fk, gs, fst, dz, dx, red,
+                                 D.dzk ? D.dzk + (bh * D.N + n0) * D.LP : nullptr, cnt);
 #pragma unroll
         for (int k = 0; k < KOUT; ++k) {
             const int o = threadIdx.x + k * NT;
@@ -912,6 +967,19 @@ cudaError_t launch_combine(const Dims &D, const float *part, float *out, int nsp
     const int64_t E = (int64_t)D.LR * D.dv;
     dim3 grid((unsigned)std::min<int64_t>((E + 255) / 256, 64), (unsigned)D.BH);
     return launch_kernel("combine", gen::k_combine, grid, dim3(256), 0, st, part, out, E, nsplit, mode);
+}
+
+template <typename T>
+cudaError_t launch_dw(const Dims &D, const T *Q, const T *K, int nblk, float *part, float *dW, cudaStream_t st)
+{
+    const int64_t span = (((D.N + nblk - 1) / nblk + gen::DW_ROWS - 1) / gen::DW_ROWS) * gen::DW_ROWS;
+    const size_t smem = (size_t)gen::DW_ROWS * (D.d + D.LP) * sizeof(float);
+    cudaError_t e = launch_kernel("dw_partial", gen::k_dw_partial<T>, dim3((unsigned)nblk, (unsigned)D.BH),
+                                  dim3(gen::NT), smem, st, D, Q, K, span, part);
+    if (e != cudaSuccess) return e;
+    const int64_t E = (int64_t)D.LP * D.d;
+    dim3 grid((unsigned)std::min<int64_t>((E + 255) / 256, 64), (unsigned)D.BH);
+    return launch_kernel("dw_combine", gen::k_combine, grid, dim3(256), 0, st, (const float *)part, dW, E, nblk, 0);
 }
 
 cudaError_t launch_dbeta_combine(const Dims &D, const float *part, int slots, float *dbeta, cudaStream_t st)
@@ -1009,7 +1077,8 @@ cudaError_t launch_causal_bwd_kv(const Dims &D, const T *Q, const T *K, const T 
                                                 float *, cudaStream_t);                                        \
     template cudaError_t launch_causal_bwd_kv<T>(const Dims &, const T *, const T *, const T *, const T *,     \
                                                  const float2 *, const float *, const float *, int64_t, int,   \
-                                                 T *, T *, float *, cudaStream_t);
+                                                 T *, T *, float *, cudaStream_t);                      \
+    template cudaError_t launch_dw<T>(const Dims &, const T *, const T *, int, float *, float *, cudaStream_t);
 
 RACE_INSTANTIATE(float)
 RACE_INSTANTIATE(__nv_bfloat16)

@@ -48,6 +48,10 @@ cudaError_t launch_sketch(const Dims &D, const T *X, const T *Y, const float2 *a
 cudaError_t launch_combine(const Dims &D, const float *part, float *out, int nsplit, int mode, cudaStream_t st);
 // dbeta[bh] from the backward kernels' d(loss)/d(beta) partials, two [BH][slots] float arrays.
 cudaError_t launch_dbeta_combine(const Dims &D, const float *part, int slots, float *dbeta, cudaStream_t st);
+// d(loss)/d(W) per (b, h), [BH][L P][d], from the dz / |x| rows in D.dzq and D.dzk: nblk token
+// ranges per (b, h) write partials [BH][nblk][L P][d] to part, then a fixed-order sum.
+template <typename T>
+cudaError_t launch_dw(const Dims &D, const T *Q, const T *K, int nblk, float *part, float *dW, cudaStream_t st);
 template <typename T>
 cudaError_t launch_readout(const Dims &D, const T *Q, const float *W, const float *S, T *O, unsigned *err,
                            cudaStream_t st);

@@ -303,6 +303,16 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
             for (int p = 0; p < P; ++p) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dzl[p])), zl[p], zdz);
         };
+        // d(loss)/d(W): table pair pr's dz / |q| of this Q row (DB instances only: the API takes
+        // them whenever d(loss)/d(W) is asked for, and the others stay free of the code)
+        auto store_dz = [&](int pr, const float (&dz)[2 * P]) {
+            if (DB && Dm.dzq != nullptr && live) {
+                float *o = Dm.dzq + (bh * Dm.N + n0 + t) * Dm.LP + 2 * pr * P;
+#pragma unroll
+                for (int j = 0; j < 2 * P; ++j)
+                    if (2 * pr * P + j < Dm.LP) o[j] = dz[j] * inv;
+            }
+        };
         if constexpr (ROLL) {
 #pragma unroll 1
             for (int pr = h; 2 * pr < L; pr += 2) {
@@ -323,6 +333,7 @@ __global__ void __launch_bounds__(NTH, 1)
                         else dz[P + p] = dzl[p];
                     }
                 }
+                store_dz(pr, dz);
                 st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
             }
         } else {
@@ -343,6 +354,7 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
                     for (int p = 0; p < P; ++p) dz[k * P + p] = dzl[p];
                 }
+                store_dz(pr, dz);
                 st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
             }
         }
@@ -511,6 +523,7 @@ __global__ void __launch_bounds__(NTH, 1)
     for (; i < ntile; ++i) {
         const int s = i & 1;
         const int64_t n0 = n_begin + (int64_t)i * C;
+        const int cnt = (int)min((int64_t)C, n_end - n0);
         const uint32_t xs = base + Ly.x + s * Ly.stg, ys = xs + KB * BLK;
         if (wait_all(bar_load + 8 * s, (i >> 1) & 1)) {
             failed = true;
@@ -565,6 +578,15 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
             for (int p = 0; p < P; ++p) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dzl[p])), zl[p], zdz);
         };
+        // d(loss)/d(W): table pair pr's dz / |k| of this K row (DB instances only)
+        auto store_dz = [&](int pr, const float (&dz)[2 * P]) {
+            if (DB && Dm.dzk != nullptr && t < cnt) {
+                float *o = Dm.dzk + (bh * Dm.N + n0 + t) * Dm.LP + 2 * pr * P;
+#pragma unroll
+                for (int j = 0; j < 2 * P; ++j)
+                    if (2 * pr * P + j < Dm.LP) o[j] = dz[j] * inv;
+            }
+        };
         if constexpr (ROLL) {
 #pragma unroll 1
             for (int pr = h; 2 * pr < L; pr += 2) {
@@ -585,6 +607,7 @@ __global__ void __launch_bounds__(NTH, 1)
                         else dz[P + p] = dzl[p];
                     }
                 }
+                store_dz(pr, dz);
                 st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
             }
         } else {
@@ -605,6 +628,7 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
                     for (int p = 0; p < P; ++p) dz[k * P + p] = dzl[p];
                 }
+                store_dz(pr, dz);
                 st_bf16_cols<2 * P>(tlane + dzc + pr * P, dz);
             }
         }

@@ -100,13 +100,20 @@ def test_bwd_rejects_before_launch(lib):
     p = ctypes.c_void_p(4096)
     ws = lib.race_attn_workspace_bytes(s, 3, 3, 1, 1)
     bwd = lambda *a: L.race_attn_bwd(*a)
-    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, None, p, p, p, None, None, p, ws, None) == -1
-    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, None, None, p, ws - 256, None) == -3
-    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, ctypes.c_void_p(4104), p, None, None, p, ws,
-               None) == -5
-    # d(loss)/d(beta) output: float32, so 4-byte alignment is required
-    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, ctypes.c_void_p(4098), None, p, ws,
-               None) == -5
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, None, p, p, p, None, None, None, p, ws, None) == -1
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, None, None, None, p, ws - 256,
+               None) == -3
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, ctypes.c_void_p(4104), p, None, None, None, p,
+               ws, None) == -5
+    # d(loss)/d(beta) and d(loss)/d(W) outputs: float32, so 4-byte alignment is required
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, ctypes.c_void_p(4098), None, None, p,
+               ws, None) == -5
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, None, ctypes.c_void_p(4098), None, p,
+               ws, None) == -5
+    # d(loss)/d(W) needs the larger workspace (is_bwd = 2): the backward's plus the dz rows
+    ws_dw = lib.race_attn_workspace_bytes(s, 3, 3, 1, 2)
+    assert ws_dw > ws
+    assert bwd(ctypes.byref(s), p, p, p, p, 10.0, 3, 3, 1, None, p, p, p, p, None, p, None, p, ws, None) == -3
 
 
 def test_decode_rejects_before_launch(lib):

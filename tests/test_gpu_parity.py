@@ -387,6 +387,46 @@ def test_dbeta_matches_oracle(w):
     assert err <= tol, "%s dbeta error %.3e > %.1e (got %s, oracle %s)" % (w.name, err, tol, got, ref)
 
 
+DW = [
+    (W_("dw_f32", 1, 2, 100, 64, 2, 2, False, "f32"), False),
+    (W_("dw_f32_c", 1, 2, 100, 64, 2, 2, True, "f32"), False),
+    (W_("dw_f32_ph_c", 2, 3, 70, 32, 3, 2, True, "f32"), True),
+    (W_("dw_bf_nc", 1, 2, 1000, 64, 3, 3, False, "bf16"), False),
+    (W_("dw_bf_lr256", 1, 2, 300, 128, 6, 4, False, "bf16", clusters=8), False),
+    (W_("dw_bf_c5", 1, 2, 5555, 128, 3, 3, True, "bf16"), False),
+    (W_("dw_bf_c5_ph", 2, 3, 700, 128, 3, 3, True, "bf16"), True),
+    (W_("dw_bf_lr64_c", 2, 3, 257, 64, 4, 4, True, "bf16"), False),
+]
+
+
+@pytest.mark.parametrize("w,per_head", DW, ids=lambda x: x.name if hasattr(x, "name") else ("ph" if x else "shared"))
+def test_dW_matches_oracle(w, per_head):
+    """d(sum O * dO)/d(W) per (b, h), [B, H, L, P, d], against the oracle's (pinned to finite
+    differences of the brute force).  Tolerance on the relative L2 error of the whole tensor: 1e-4
+    for float32 tensors, 5e-2 for bfloat16 (the gradient tolerance).  Asking for it leaves dQ,
+    dK, dV and d(loss)/d(beta) bit for bit unchanged, and a second call gives the same bits."""
+    inp = inputs_on_gpu(w, seed=5)
+    if per_head:
+        inp["W"] = _per_head_w(w, 62)
+    args = (inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal, inp["dO"])
+    plain = race.race_attn_bwd(*args, want_dbeta=True)
+    with_dw = race.race_attn_bwd(*args, want_dbeta=True, want_dW=True)
+    again = race.race_attn_bwd(*args, want_dW=True)
+    torch.cuda.synchronize()
+    for x, y in zip(plain, with_dw[:4]):
+        assert torch.equal(x, y)
+    assert torch.equal(with_dw[4], again[3])
+    a = {k: as_oracle_array(inp[k]) for k in ("Q", "K", "V", "dO")}
+    W = inp["W"].double().cpu().numpy()
+    *_, ref = oracle.backward(a["Q"], a["K"], a["V"], a["dO"], W, w.beta, w.causal, want_dW=True)
+    got = with_dw[4].double().cpu().numpy()
+    assert got.shape == ref.shape
+    assert np.all(np.isfinite(got))
+    tol = 1e-4 if w.dtype == "f32" else 5e-2
+    err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= tol, "%s dW error %.3e > %.1e" % (w.name, err, tol)
+
+
 # One set of hyperplanes per head (W [H, L, P, d]); B = 2 so that reading W by (b, h) instead of
 # by h would fail.  One workload per kernel family.
 PER_HEAD = [
@@ -481,14 +521,14 @@ def _hard_inputs(w, seed):
 
 @pytest.mark.parametrize("w", HARD, ids=lambda w: w.name)
 def test_hard_hash(w):
-    """beta = +inf: O and dV against the oracle's hard hash (sign bits); dQ, dK and
-    d(loss)/d(beta) exactly zero."""
+    """beta = +inf: O and dV against the oracle's hard hash (sign bits); dQ, dK, d(loss)/d(beta)
+    and d(loss)/d(W) exactly zero."""
     inp = _hard_inputs(w, seed=7)
     args = (inp["Q"], inp["K"], inp["V"], inp["W"], w.beta, w.L, w.P, w.causal)
     O = race.race_attn_fwd(*args)
-    dQ, dK, dV, db = race.race_attn_bwd(*args, inp["dO"], O=O, want_dbeta=True)
+    dQ, dK, dV, db, dW = race.race_attn_bwd(*args, inp["dO"], O=O, want_dbeta=True, want_dW=True)
     torch.cuda.synchronize()
-    assert torch.all(dQ == 0) and torch.all(dK == 0) and torch.all(db == 0)
+    assert torch.all(dQ == 0) and torch.all(dK == 0) and torch.all(db == 0) and torch.all(dW == 0)
     got = (O.double().cpu().numpy(), dQ.double().cpu().numpy(), dK.double().cpu().numpy(),
            dV.double().cpu().numpy())
     ref = oracle_run(w, inp)
