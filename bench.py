@@ -316,17 +316,18 @@ def run_ours(args, w):
     Q, K, V, dO, W = inp["Q"], inp["K"], inp["V"], inp["dO"], inp["W"]
     shape = race.make_shape(w.B, w.H, w.N, w.d, w.torch_dtype)
     state = torch.empty(race.race_attn_state_bytes(shape, w.L, w.P, w.causal), dtype=torch.uint8, device=dev)
-    ws_bytes = max(race.race_attn_workspace_bytes(shape, w.L, w.P, w.causal, b) for b in (0, 1))
+    ws_bytes = max(race.race_attn_workspace_bytes(shape, w.L, w.P, w.causal, b) for b in (0, 2 if args.dW else 1))
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     O, dQ, dK, dV = (torch.empty_like(Q) for _ in range(4))
     stream = torch.cuda.current_stream(dev)
 
     dbeta = torch.empty((w.B, w.H), dtype=torch.float32, device=dev) if args.dbeta else None
+    dW = torch.empty((w.B, w.H, w.L, w.P, w.d), dtype=torch.float32, device=dev) if args.dW else None
 
     def step():
         race.race_attn_fwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, O=O, state=state, workspace=workspace)
         race.race_attn_bwd(Q, K, V, W, w.beta, w.L, w.P, w.causal, dO, O=O, dQ=dQ, dK=dK, dV=dV, state=state,
-                           workspace=workspace, dbeta=dbeta)
+                           workspace=workspace, dbeta=dbeta, dW=dW)
 
     for _ in range(args.warmup):
         step()
@@ -377,7 +378,8 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": dict(workload_config(w), dbeta=bool(args.dbeta)), "clocks": clocks, "roofline": roof,
+            "config": dict(workload_config(w), dbeta=bool(args.dbeta), dW=bool(args.dW)), "clocks": clocks,
+            "roofline": roof,
             "kernels": kernels, "gpu_launches": launches, "cpu_baseline": cpu, "e2e": e2e,
         }
         if world == 1 and not args.no_configs and not args.tokens:
@@ -414,7 +416,7 @@ def traffic_for_step(w, prof):
         return None
     total = 0.0
     for name, (nl, _) in prof.items():
-        if name in ("combine", "dbeta_combine"):
+        if name in ("combine", "dbeta_combine", "dw_combine"):
             continue
         t = traffic_for(name, w)
         if t is None:
@@ -711,6 +713,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="override N (sequence length) of the workload, e.g. for a small profiling capture")
     ap.add_argument("--dbeta", action="store_true", help="the backward also writes d(loss)/d(beta)")
+    ap.add_argument("--dW", action="store_true", help="the backward also writes d(loss)/d(W)")
     ap.add_argument("--row", choices=["step", "decode", "angular"], default="step",
                     help="decode: one causal decode step per (b, h) of --heads heads; angular: exact angular "
                          "attention at the workload's d and --tokens (default 8192) tokens")
