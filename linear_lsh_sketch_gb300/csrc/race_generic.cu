@@ -375,30 +375,34 @@ __global__ void __launch_bounds__(NT) k_sketch(Dims D, const T *__restrict__ X,
 // mode 0: out[bh][e] = sum_s part[bh][s][e]
 // mode 1: out[bh][s][e] = sum_{s' < s} part[bh][s'][e]   (exclusive prefix over segments)
 // mode 2: out[bh][s][e] = sum_{s' > s} part[bh][s'][e]   (exclusive suffix over segments)
+// The partials are read in batches of 16 independent loads before they are added (in the same
+// order as one at a time), so that the loads' latency overlaps.
 __global__ void k_combine(const float *__restrict__ part, float *__restrict__ out, int64_t E,
                           int nsplit, int mode)
 {
+    constexpr int NB = 16;
     const int64_t bh = blockIdx.y;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E;
          e += (int64_t)gridDim.x * blockDim.x) {
         const float *p = part + bh * nsplit * E + e;
-        if (mode == 0) {
-            float s = 0.f;
-            for (int i = 0; i < nsplit; ++i) s += p[i * E];
-            out[bh * E + e] = s;
-        } else if (mode == 1) {
-            float s = 0.f;
-            for (int i = 0; i < nsplit; ++i) {
-                out[(bh * nsplit + i) * E + e] = s;
-                s += p[i * E];
+        float s = 0.f;
+        for (int i0 = 0; i0 < nsplit; i0 += NB) {
+            float v[NB];
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                const int i = mode == 2 ? nsplit - 1 - (i0 + j) : i0 + j;
+                v[j] = i0 + j < nsplit ? p[(int64_t)i * E] : 0.f;
             }
-        } else {
-            float s = 0.f;
-            for (int i = nsplit - 1; i >= 0; --i) {
-                out[(bh * nsplit + i) * E + e] = s;
-                s += p[i * E];
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                if (i0 + j < nsplit) {
+                    const int i = mode == 2 ? nsplit - 1 - (i0 + j) : i0 + j;
+                    if (mode != 0) out[(bh * nsplit + i) * E + e] = s;
+                    s += v[j];
+                }
             }
         }
+        if (mode == 0) out[bh * E + e] = s;
     }
 }
 
