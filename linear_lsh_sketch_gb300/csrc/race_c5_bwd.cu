@@ -709,9 +709,11 @@ template <int D, int LRM>
 struct QCols {
     static constexpr bool TRIL_TMEM = LRM == 32;
     static constexpr uint32_t ZQ = 0;                        // projections of the Q tile, 32 columns
-    static constexpr uint32_t DV = LRM == 32 ? 64 : 32;      // dO V^T, then M1 as bf16 pairs (in place), then dxhat
-    static constexpr uint32_t G = DV + 128;                  // g (L R columns)
-    static constexpr uint32_t BT = G + LRM;                  // (tril 1) F_K
+    // g: L R <= 32 takes dO S^T with the hi and lo halves of S as one N = 64 product, so g's
+    // columns 0..31 hold the hi part (plus M1 F_K) and 32..63 the lo part; L R <= 64, L R columns
+    static constexpr uint32_t G = LRM == 32 ? 32 : 160;
+    static constexpr uint32_t DV = LRM == 32 ? 96 : 32;      // dO V^T, then M1 as bf16 pairs (in place), then dxhat
+    static constexpr uint32_t BT = DV + 128 > G + 64 ? DV + 128 : G + 64;  // (tril 1) F_K
     static constexpr uint32_t TRIL = BT + LRM;               // lower-triangular ones as bf16 pairs (A operand), 64 columns
     static constexpr uint32_t DZ = TRIL_TMEM ? TRIL + 64 : TRIL;  // dz as bf16 pairs (A operand), 16 columns
     static constexpr uint32_t ST = DZ + 16;                  // A^T (lanes = d)
@@ -897,9 +899,9 @@ __global__ void __launch_bounds__(NTHW, 1)
                     lw[j] = bfp::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
                 }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 4; ++c) {  // hi in columns 0..31, lo in 32..63 of one block
                     st_shared_v4(base + Ly.shi + sw_chunk(t, c), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
-                    st_shared_v4(base + Ly.slo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+                    st_shared_v4(base + Ly.shi + sw_chunk(t, 4 + c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
                 }
             }
             if (q4 == 0) bprev[32 * par_out + lane] = lane < LR ? uf(mv) : 0.f;
@@ -968,6 +970,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             }
             constexpr uint32_t id_dv = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t id_g1 = idesc_bf16(128, LRMAX, 0, 1);
+            constexpr uint32_t id_g64 = idesc_bf16(128, 64, 0, 1);
             constexpr uint32_t id_bt = idesc_bf16(128, LRMAX, 0, 1);
             constexpr uint32_t id_x = idesc_bf16(128, D, 0, 1);
             constexpr uint32_t id_gt = idesc_bf16(128, LRMAX, 1, 1);
@@ -1000,8 +1003,12 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint64_t ko = (uint64_t)((ks >> 2) * BLK + (ks & 3) * 32) >> 4;
                     umma(tmem + T_DV, d_do_k + ko, d_v_k + ko, id_dv, ks > 0);
-                    umma(tmem + T_G, d_do_k + ko, d_shi + (uint64_t)(ks * 128), id_g1, ks > 0);
-                    umma(tmem + T_G, d_do_k + ko, d_slo + (uint64_t)(ks * 128), id_g1, true);
+                    if constexpr (LRMAX == 32) {  // S hi and lo as one N = 64 operand
+                        umma(tmem + T_G, d_do_k + ko, d_shi + (uint64_t)(ks * 128), id_g64, ks > 0);
+                    } else {
+                        umma(tmem + T_G, d_do_k + ko, d_shi + (uint64_t)(ks * 128), id_g1, ks > 0);
+                        umma(tmem + T_G, d_do_k + ko, d_slo + (uint64_t)(ks * 128), id_g1, true);
+                    }
                 }
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks) {
@@ -1198,11 +1205,18 @@ __global__ void __launch_bounds__(NTHW, 1)
                 float rd = 0.f, cc = 0.f;
                 if constexpr (LRMAX == 32) {
                     uint32_t gr[32], br[32];
-                    ld32_nw(tlane + T_G, gr);
-                    ld32_nw(tlane + T_BT, br);
-                    wait_ld();
-                    reg_fence(gr);
-                    reg_fence(br);
+                    {
+                        uint32_t gl[32];  // g = its hi part (with M1 F_K) + its lo part
+                        ld32_nw(tlane + T_G, gr);
+                        ld32_nw(tlane + T_G + 32, gl);
+                        ld32_nw(tlane + T_BT, br);
+                        wait_ld();
+                        reg_fence(gr);
+                        reg_fence(gl);
+                        reg_fence(br);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) gr[j] = __float_as_uint(uf(gr[j]) + uf(gl[j]));
+                    }
                     float den = 0.f, pg = 0.f;
                     float phq[LT > 0 ? LRMAX : 1];  // with L compiled in: the row's bucket probabilities
 #pragma unroll
