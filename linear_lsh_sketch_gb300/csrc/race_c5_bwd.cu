@@ -38,16 +38,20 @@ using namespace race::nc5;
 constexpr int NTHW = NTH + 32;
 
 // TMEM columns (512 allocated) for sketch widths L R <= LRM (32, or 64 when d = 64).
+// With L R <= 32 (PACK) the G operand's hi and lo halves share one shared-memory block, V G^T is
+// one N = 64 product per K step (dphi_K's hi part, plus M2 F'_Q^T, in columns 0..31 of DP, its
+// lo part in 32..63), and dz takes DP's first 16 columns once the Jacobian has read them.
 template <int D, int LRM>
 struct KvCols {
+    static constexpr bool PACK = LRM == 32;
     static constexpr uint32_t SC = 0;          // F_K F'_Q^T, then P2 as bf16 pairs (in place, per half)
     static constexpr uint32_t DV = 128;        // V dO^T, then M2 as bf16 pairs (in place), then dxhat
     static constexpr uint32_t DVV = 256;       // dV (d columns)
     static constexpr uint32_t ZK = 288;        // K-row projections, 32 columns (dead before dV is written)
-    static constexpr uint32_t DP = DVV + D;    // dphi_K (LRM columns)
-    static constexpr uint32_t FK = DP + LRM;   // F_K as bf16 pairs (A operand), LRM / 2 columns
-    static constexpr uint32_t DZ = FK + LRM / 2;  // dz as bf16 pairs (A operand), 16 columns
-    static constexpr uint32_t GT = DZ + 16;    // G^T (lanes = d), LRM columns
+    static constexpr uint32_t DP = DVV + D;    // dphi_K (LRM columns; 64 with PACK)
+    static constexpr uint32_t FK = DP + (PACK ? 64 : LRM);  // F_K as bf16 pairs (A operand), LRM / 2 columns
+    static constexpr uint32_t DZ = PACK ? DP : FK + LRM / 2;  // dz as bf16 pairs (A operand), 16 columns
+    static constexpr uint32_t GT = PACK ? FK + LRM / 2 : DZ + 16;  // G^T (lanes = d), LRM columns
     static constexpr uint32_t GB = GT + LRM;   // G_B (lanes = sketch row), 16 columns (0 and 1 used)
     static_assert(GB + 16 <= 512 && ZK + 32 <= DVV + D, "key-side TMEM budget");
 };
@@ -187,7 +191,8 @@ __global__ void __launch_bounds__(NTHW, 1)
             stn<2>(tlane + T_GB, m);
         } else {
             const uint32_t zr[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            for (int c0 = 0; c0 < LRMAX / 2 + 16; c0 += 8) stn<8>(tlane + T_FK + c0, zr);  // T_FK and T_DZ
+            // T_FK (and T_DZ after it when it has columns of its own)
+            for (int c0 = 0; c0 < LRMAX / 2 + (Cols::PACK ? 0 : 16); c0 += 8) stn<8>(tlane + T_FK + c0, zr);
         }
         wait_st();
     }
@@ -222,9 +227,9 @@ __global__ void __launch_bounds__(NTHW, 1)
                     lw[j] = bfp::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
                 }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 4; ++c) {  // hi in columns 0..31, lo in 32..63 of one block
                     st_shared_v4(base + Ly.ghi + sw_chunk(t, c), hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
-                    st_shared_v4(base + Ly.glo + sw_chunk(t, c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+                    st_shared_v4(base + Ly.ghi + sw_chunk(t, 4 + c), lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
                 }
             }
             if (q4 == 0) gb[32 * par_out + lane] = lane < LR ? uf(gb0) + uf(gb1) : 0.f;  // -sum F'_Q c, c as hi + lo
@@ -297,6 +302,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             constexpr uint32_t id_sc = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t id_dvo = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t id_dp = idesc_bf16(128, LRMAX, 0, 1);
+            constexpr uint32_t id_dp64 = idesc_bf16(128, 64, 0, 1);
             constexpr uint32_t id_dv = idesc_bf16(128, D, 0, 0);
             constexpr uint32_t id_pdo = idesc_bf16(128, D, 0, 1);
             constexpr uint32_t id_mf = idesc_bf16(128, LRMAX, 0, 1);
@@ -307,7 +313,9 @@ __global__ void __launch_bounds__(NTHW, 1)
             // F'_Q (sketch rows 64..127) and for dO^T at d = 64 (rows d 64..127) that block only feeds
             // accumulator lanes nobody reads, so it points at the next whole 16 KB tile
             const uint64_t d_fq_k = desc_k(base + Ly.fq), d_fq_mn = desc_mn(base + Ly.fq, BLK);
-            const uint64_t d_ghi_k = desc_k(base + Ly.ghi), d_glo_k = desc_k(base + Ly.glo);
+            // PACK: the lo half of G starts 64 bytes into the rows of the hi half's block
+            const uint64_t d_ghi_k = desc_k(base + Ly.ghi),
+                           d_glo_k = Cols::PACK ? desc_k(base + Ly.ghi) + (64 >> 4) : desc_k(base + Ly.glo);
             const uint64_t d_ghi_mn = desc_mn(base + Ly.ghi, BLK), d_glo_mn = desc_mn(base + Ly.glo, BLK);
             const uint64_t d_v_k = desc_k(base + Ly.v), d_do_k = desc_k(base + Ly.dO);
             const uint64_t d_do_mn = desc_mn(base + Ly.dO, BLK);
@@ -338,8 +346,12 @@ __global__ void __launch_bounds__(NTHW, 1)
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint64_t ko = (uint64_t)((ks >> 2) * BLK + (ks & 3) * 32) >> 4;
                     umma(tmem + T_DV, d_v_k + ko, d_do_k + ko, id_dvo, ks > 0);
-                    umma(tmem + T_DP, d_v_k + ko, d_ghi_mn + (uint64_t)(ks * 128), id_dp, ks > 0);
-                    umma(tmem + T_DP, d_v_k + ko, d_glo_mn + (uint64_t)(ks * 128), id_dp, true);
+                    if constexpr (Cols::PACK) {  // G hi and lo as one N = 64 operand
+                        umma(tmem + T_DP, d_v_k + ko, d_ghi_mn + (uint64_t)(ks * 128), id_dp64, ks > 0);
+                    } else {
+                        umma(tmem + T_DP, d_v_k + ko, d_ghi_mn + (uint64_t)(ks * 128), id_dp, ks > 0);
+                        umma(tmem + T_DP, d_v_k + ko, d_glo_mn + (uint64_t)(ks * 128), id_dp, true);
+                    }
                 }
                 for (int ks = 0; ks < LRMAX / 16; ++ks) {
                     umma_ts(tmem + T_DVV, tmem + T_FK + 8 * ks, d_ghi_k + (uint64_t)(2 * ks), id_dv, ks > 0);
@@ -573,11 +585,14 @@ __global__ void __launch_bounds__(NTHW, 1)
                 }
                 // key-side Jacobian: dphi_K + G_B -> dz (bf16 pairs in TMEM)
                 float dph[LRMAX == 32 ? 32 : 1];
-                if constexpr (LRMAX == 32) {
+                if constexpr (LRMAX == 32) {  // dphi_K's hi part (with M2 F'_Q^T) + its lo part + G_B
                     float a[32];
                     ld32(tlane + T_DP, a);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dph[j] = a[j] + gb[LRMAX * par + j];
+                    ld32(tlane + T_DP + 32, a);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dph[j] += a[j];
                 }
                 float dz[LPP];
 #pragma unroll
