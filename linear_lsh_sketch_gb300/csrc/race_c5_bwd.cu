@@ -83,9 +83,9 @@ struct BwdLayout {
         fq = dO + kbb;  // F'_Q [t][lr], one 64-column block
         ghi = fq + BLK;
         glo = ghi + BLK;  // G operand [d rows][lr], one block each
-        whi = glo + BLK;
-        wlo = whi + (uint32_t)(D / 64) * WBLK;
-        ncm = wlo + (uint32_t)(D / 64) * WBLK;  // -c as a K-major N = 16 operand (rows 0, 1 = hi, lo)
+        whi = glo + BLK;  // W in pair layout (hi and lo blocks interleaved); wlo = its first lo block
+        wlo = whi + WBLK;
+        ncm = whi + 2 * (uint32_t)(D / 64) * WBLK;  // -c as a K-major N = 16 operand (rows 0, 1 = hi, lo)
         gb = ncm + 4096;                         // G_B fp32 [2 parities][LRM]
         cvec = gb + 8 * LRM;                     // c_t fp32 [C]
         zk = cvec + 4 * C;   // z = W x of the K rows, fp32 [lpz][C]
@@ -111,6 +111,9 @@ __global__ void __launch_bounds__(NTHW, 1)
     constexpr int LMAX = LPP / P;
     constexpr int LRMAX = LRM;  // sketch rows this instance supports
     using Cols = KvCols<D, LRM>;
+    // the K projection as one N = 64 product (hi and lo parts side by side, inside dV's columns)
+    constexpr bool MERGE_PROJ = D == 128 && LRM == 32;
+    static_assert(!MERGE_PROJ || KvCols<D, LRM>::ZK + 2 * LPP <= KvCols<D, LRM>::DVV + D, "projection inside dV");
     constexpr uint32_t T_SC = Cols::SC, T_DV = Cols::DV, T_DVV = Cols::DVV, T_ZK = Cols::ZK, T_DP = Cols::DP;
     constexpr uint32_t T_FK = Cols::FK, T_DZ = Cols::DZ, T_GT = Cols::GT, T_GB = Cols::GB;
     using Stg = KvStage<LRM>;
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         zero_region(sm + Ly.fq, BLK);
         zero_region(sm + Ly.ghi, 2 * BLK);
         init_mass_tile(sm + Ly.ncm, false);
-        load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+        load_w_pair<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi);
     }
     if (tid == NTH) {
         for (uint32_t i = 0; i < B_COUNT; ++i) {
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(NTHW, 1)
             const uint64_t d_do_mn = desc_mn(base + Ly.dO, BLK);
             const uint64_t d_do_mt = desc_mn(base + Ly.dO, BLK);
             const uint64_t d_ncm = desc_k(base + Ly.ncm);
-            const uint64_t d_whi = desc_mn(base + Ly.whi, WBLK), d_wlo = desc_mn(base + Ly.wlo, WBLK);
+            const uint64_t d_whi = desc_mn(base + Ly.whi, 2 * WBLK), d_wlo = desc_mn(base + Ly.wlo, 2 * WBLK);
             bool ok = true;
             for (int k = 0; k < nchunk && ok; ++k) {
                 const uint32_t par = k & 1;
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(NTHW, 1)
                 // the projection reuses TMEM columns of the previous chunk's dV
                 if (k >= 1 && !(ok = wait_phase(bar(B_DVR), (k - 1) & 1, abort))) break;
                 fence_after();
-                issue_projection<D>(tmem + T_ZK, base + Ly.k, base + Ly.whi, base + Ly.wlo);
+                issue_projection_pair<D, MERGE_PROJ>(tmem + T_ZK, base + Ly.k, base + Ly.whi);
                 commit(bar(B_PROJ));
                 // group A once the features and the previous chunk's G operand are in
                 if (!(ok = wait_phase(bar(B_FEAT), par, abort))) break;
@@ -517,6 +520,11 @@ __global__ void __launch_bounds__(NTHW, 1)
                     ld_cols<LPZ>(tlane + T_ZK, a);
 #pragma unroll
                     for (int j = 0; j < LPZ; ++j) z[j] = a[j];
+                    if constexpr (MERGE_PROJ) {  // + the lo hyperplanes' part
+                        ld_cols<LPZ>(tlane + T_ZK + LPP, a);
+#pragma unroll
+                        for (int j = 0; j < LPZ; ++j) z[j] += a[j];
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < LPZ; ++j) {
@@ -757,9 +765,9 @@ struct QLayout {
         fq = fk + BLK;   // F'_Q [t][lr]
         shi = fq + BLK;  // S operand [d rows][lr] (MN-major B of dO A^T)
         slo = shi + BLK;
-        whi = slo + BLK;
-        wlo = whi + (uint32_t)(D / 64) * WBLK;
-        ncm = wlo + (uint32_t)(D / 64) * WBLK;
+        whi = slo + BLK;  // W in pair layout (hi and lo blocks interleaved); wlo = its first lo block
+        wlo = whi + WBLK;
+        ncm = whi + 2 * (uint32_t)(D / 64) * WBLK;
         ones = ncm + 4096;
         tril = ones + 4096;   // LRM = 64: lower-triangular ones, K-major [t][j] in two 64-column blocks
         bprev = tril + (LRM == 64 ? 2 * BLK : 0);  // B_prev fp32 [2 parities][LRM]
@@ -786,6 +794,9 @@ __global__ void __launch_bounds__(NTHW, 1)
     constexpr int LMAX = LPP / P;
     constexpr int LRMAX = LRM;
     using Cols = QCols<D, LRM>;
+    // the Q projection as one N = 64 product: the lo part lands in g's columns, free until group A
+    constexpr bool MERGE_PROJ = LRM == 32;
+    static_assert(!MERGE_PROJ || QCols<D, LRM>::G == QCols<D, LRM>::ZQ + LPP, "lo projection in g's columns");
     constexpr uint32_t T_ZQ = Cols::ZQ, T_DV = Cols::DV, T_G = Cols::G, T_BT = Cols::BT, T_TRIL = Cols::TRIL;
     constexpr uint32_t T_DZ = Cols::DZ, T_ST = Cols::ST, T_MS = Cols::MS, T_GT = Cols::GT, T_GB = Cols::GB;
     constexpr uint32_t T_X = Cols::X;
@@ -823,7 +834,7 @@ __global__ void __launch_bounds__(NTHW, 1)
         zero_region(sm + Ly.fk, 4 * BLK);  // F_K, F'_Q, S hi, S lo
         init_mass_tile(sm + Ly.ncm, false);
         init_mass_tile(sm + Ly.ones, true);
-        load_w_tiles<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi, sm + Ly.wlo);
+        load_w_pair<D>(head_w(W, Dm, bh), Dm.LP, sm + Ly.whi);
     }
     if (tid == NTH) {
         for (uint32_t i = 0; i < B_COUNT; ++i) {
@@ -997,14 +1008,14 @@ __global__ void __launch_bounds__(NTHW, 1)
             const uint64_t d_fk_mn = desc_mn(base + Ly.fk, BLK), d_fq_mn = desc_mn(base + Ly.fq, BLK);
             const uint64_t d_shi = desc_mn(base + Ly.shi, BLK), d_slo = desc_mn(base + Ly.slo, BLK);
             const uint64_t d_ncm = desc_k(base + Ly.ncm), d_ones = desc_k(base + Ly.ones);
-            const uint64_t d_whi = desc_mn(base + Ly.whi, WBLK), d_wlo = desc_mn(base + Ly.wlo, WBLK);
+            const uint64_t d_whi = desc_mn(base + Ly.whi, 2 * WBLK), d_wlo = desc_mn(base + Ly.wlo, 2 * WBLK);
             bool ok = true;
             for (int c = 0; c < nchunk && ok; ++c) {
                 const uint32_t par = c & 1;
                 if (!(ok = wait_phase(bar(B_QK), par, abort))) break;
                 ++done[0];
                 fence_after();
-                issue_projection<D>(tmem + T_ZQ, base + Ly.q, base + Ly.whi, base + Ly.wlo);
+                issue_projection_pair<D, MERGE_PROJ>(tmem + T_ZQ, base + Ly.q, base + Ly.whi);
                 commit(bar(B_PROJ));
                 if (!(ok = wait_phase(bar(B_FEAT), par, abort))) break;
                 if (!(ok = wait_phase(bar(B_SOP), par, abort))) break;
@@ -1145,6 +1156,18 @@ __global__ void __launch_bounds__(NTHW, 1)
                     ld32(tlane + T_ZQ, a);
 #pragma unroll
                     for (int j = 0; j < LPP; ++j) z[j] = a[j];
+                    if constexpr (MERGE_PROJ) {  // + the lo hyperplanes' part (in g's columns until group A),
+                        ld32(tlane + T_ZQ + LPP, a);  // and the sum back for the Jacobian's z . dz
+#pragma unroll
+                        for (int j = 0; j < LPP; ++j) z[j] += a[j];
+#pragma unroll
+                        for (int b = 0; b < LPP / 8; ++b) {
+                            uint32_t r[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) r[j] = __float_as_uint(z[8 * b + j]);
+                            stn<8>(tlane + T_ZQ + 8 * b, r);
+                        }
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < LPP; ++j) uq[j] = j < LP ? tc::tanh_abs(z[j] * inv) : 0.f;

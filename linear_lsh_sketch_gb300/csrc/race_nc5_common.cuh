@@ -429,6 +429,50 @@ __device__ __forceinline__ void issue_projection(uint32_t tz, uint32_t xtile, ui
     }
 }
 
+// Hyperplane tiles in pair layout: per 64-column block kb, the hi rows then the lo rows,
+// [D / 64][hi 32 rows | lo 32 rows][64] (2 WBLK bytes per block), so that one K-major operand of
+// N = 64 rows holds both halves.
+template <int D>
+__device__ __forceinline__ void load_w_pair(const float *__restrict__ W, int LP, unsigned char *wp)
+{
+    for (int i = threadIdx.x; i < LPP * (D / 8); i += NTH) {
+        const int row = i / (D / 8), c = i - row * (D / 8);
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float w0 = 0.f, w1 = 0.f;
+            if (row < LP) {
+                w0 = W[row * D + 8 * c + 2 * j];
+                w1 = W[row * D + 8 * c + 2 * j + 1];
+            }
+            const bf16 h0 = __float2bfloat16_rn(w0), h1 = __float2bfloat16_rn(w1);
+            h[j] = bfp::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+            l[j] = bfp::pack_bf16(w0 - __bfloat162float(h0), w1 - __bfloat162float(h1));
+        }
+        const uint32_t off = (c >> 3) * 2 * WBLK + sw_chunk(row, c & 7);
+        st_shared_v4(smem_addr(wp) + off, h[0], h[1], h[2], h[3]);
+        st_shared_v4(smem_addr(wp) + off + WBLK, l[0], l[1], l[2], l[3]);
+    }
+}
+
+// z = X (W_hi + W_lo)^T from pair-layout tiles.  MERGED: one N = 64 product per K step that
+// leaves X W_hi^T in columns tz .. tz + 31 and X W_lo^T in tz + 32 .. tz + 63 (the reader adds
+// them); otherwise both into tz .. tz + 31.
+template <int D, bool MERGED>
+__device__ __forceinline__ void issue_projection_pair(uint32_t tz, uint32_t xtile, uint32_t wp)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t ko = (ks >> 2) * BLK + (ks & 3) * 32, kw = (ks >> 2) * 2 * WBLK + (ks & 3) * 32;
+        if constexpr (MERGED) {
+            umma(tz, desc_k(xtile + ko), desc_k(wp + kw), idesc_bf16(128, 2 * LPP, 0, 0), ks > 0);
+        } else {
+            umma(tz, desc_k(xtile + ko), desc_k(wp + kw), idesc_proj(), ks > 0);
+            umma(tz, desc_k(xtile + ko), desc_k(wp + kw + WBLK), idesc_proj(), true);
+        }
+    }
+}
+
 // The same, issued by a converged warp (one elected lane).
 template <int D>
 __device__ __forceinline__ void issue_projection_w(uint32_t tz, uint32_t xtile, uint32_t whi, uint32_t wlo)
