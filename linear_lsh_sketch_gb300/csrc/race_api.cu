@@ -213,8 +213,9 @@ int make_plan(const race_shape *s, int L, int P, int causal, Plan &pl)
     pl.off_fq = align256(pl.off_db + 2 * (size_t)D.BH * pl.db_cap * sizeof(float));
     const size_t fq_bytes = (pl.c5 && c5_bwd_supported(D)) ? c5_feature_rows_bytes(D) : 0;
     pl.ws_bwd = align256(pl.off_fq + fq_bytes);
-    pl.dw_nblk = (int)std::max<int64_t>(1, std::min(ceil_div(D.N, 32), ceil_div(2 * (int64_t)D.sms, D.BH)));
-    const size_t dz_bytes = (size_t)D.BH * D.N * D.LP * sizeof(float);
+    pl.dw_nblk = (int)std::max<int64_t>(1, std::min(ceil_div(D.N, 32), ceil_div(4 * (int64_t)D.sms, D.BH)));
+    D.dzld = (D.LP + 3) & ~3;
+    const size_t dz_bytes = (size_t)D.BH * D.N * D.dzld * sizeof(float);
     pl.off_dzq = pl.ws_bwd;
     pl.off_dzk = align256(pl.off_dzq + dz_bytes);
     pl.off_dwpart = align256(pl.off_dzk + dz_bytes);

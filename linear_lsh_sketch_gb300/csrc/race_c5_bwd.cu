@@ -640,11 +640,12 @@ __global__ void __launch_bounds__(NTHW, 1)
                     if (j < LP) zdz = fmaf(__bfloat162float(__float2bfloat16_rn(dz[j])), zk_s[j * C + t], zdz);
                 wait_st();
                 warp_signal(bar(B_JAC));
-                if (Dm.dzk != nullptr && live) {  // d(loss)/d(W): this K row's dz / |k|
-                    float *o = Dm.dzk + (bh * Dm.N + n0 + t) * LP;
+                if (Dm.dzk != nullptr && live) {  // d(loss)/d(W): this K row's dz / |k| (zeros past L P)
+                    float4 *o = reinterpret_cast<float4 *>(Dm.dzk + (bh * Dm.N + n0 + t) * Dm.dzld);
 #pragma unroll
-                    for (int j = 0; j < LMAX * P; ++j)
-                        if (j < LP) o[j] = dz[j] * inv;
+                    for (int q = 0; q < LPP / 4; ++q)
+                        if (4 * q < Dm.dzld)
+                            o[q] = make_float4(dz[4 * q] * inv, dz[4 * q + 1] * inv, dz[4 * q + 2] * inv, dz[4 * q + 3] * inv);
                 }
             } else {
                 // dV row t = F_K G_A + P2 dO, straight to global memory
@@ -1374,12 +1375,13 @@ __global__ void __launch_bounds__(NTHW, 1)
                 *reinterpret_cast<bf16 *>(mt + sw_elem(1, t & 63)) = mlo;
                 wait_st();
                 warp_signal(bar(B_JAC));
-                if (Dm.dzq != nullptr && live) {  // d(loss)/d(W): this Q row's dz / |q|
-                    float *o = Dm.dzq + (bh * Dm.N + n0 + t) * LP;
+                if (Dm.dzq != nullptr && live) {  // d(loss)/d(W): this Q row's dz / |q| (zeros past L P)
+                    float4 *o = reinterpret_cast<float4 *>(Dm.dzq + (bh * Dm.N + n0 + t) * Dm.dzld);
                     const float iq = invq_s[t];
 #pragma unroll
-                    for (int j = 0; j < LPP; ++j)
-                        if (j < LP) o[j] = dz[j] * iq;
+                    for (int q = 0; q < LPP / 4; ++q)
+                        if (4 * q < Dm.dzld)
+                            o[q] = make_float4(dz[4 * q] * iq, dz[4 * q + 1] * iq, dz[4 * q + 2] * iq, dz[4 * q + 3] * iq);
                 }
             } else {
                 // the sketch after this chunk -> bf16 operand and B_prev of the next chunk

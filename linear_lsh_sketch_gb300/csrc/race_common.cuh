@@ -26,9 +26,11 @@ struct Dims {
     int sms;         // streaming multiprocessors of the device the work is planned for
     int withhold;    // failure-path test hook: the causal tcgen05 forward skips its first tile load
     // d(loss)/d(W) (null unless asked for): every backward kernel writes each Q row's (dzq) and K
-    // row's (dzk) projection gradient dz / |x| as L P floats, [BH][N][L P]; a reduction then forms
+    // row's (dzk) projection gradient dz / |x| as L P floats, [BH][N][dzld] (dzld = L P rounded up
+    // to a multiple of 4, so that rows start on 16 bytes); a reduction then forms
     // dW = sum over rows of (dz / |x|) x^T
     float *dzq, *dzk;
+    int dzld;
 };
 
 // Bits of the device status word (the first word of a workspace): a bounded wait ran out, or a

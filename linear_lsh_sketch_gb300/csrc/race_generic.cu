@@ -148,7 +148,7 @@ __device__ float featurise_backward(const float *xs, const Dims &D, const float 
     }
     __syncthreads();
     if (dz_g)  // the tile's live rows of dz / |x| (d(loss)/d(W) is their product with the rows)
-        for (int i = threadIdx.x; i < cnt * D.LP; i += NT) dz_g[i] = dz_s[i] * inv_s[i / D.LP];
+        for (int i = threadIdx.x; i < cnt * D.LP; i += NT) dz_g[(i / D.LP) * D.dzld + i % D.LP] = dz_s[i] * inv_s[i / D.LP];
     for (int i = threadIdx.x; i < TT * D.d; i += NT) {
         const int t = i / D.d, k = i - t * D.d;
         float s = 0.f;
@@ -425,50 +425,104 @@ __global__ void __launch_bounds__(256) k_dbeta_combine(const float *__restrict__
 
 // d(loss)/d(W) of problem bh, partial over the token range [blockIdx.x * span, + span): the
 // projection z = W xhat has d(loss)/d(W) = sum over Q and K rows of dz xhat^T, and the backward
-// kernels stored dz / |x| per row, so part[bh][blockIdx.x][lp][k] = sum over the range's rows n
-// of dzq[n][lp] Q[n][k] + dzk[n][lp] K[n][k], in a fixed order (tiles of 32 rows, the Q rows then
-// the K rows of each).  Grid (blocks, BH), NT threads, 32 (d + L P) floats of shared memory.
+// kernels stored dz / |x| per row (stride dzld), so part[bh][blockIdx.x][lp][k] = sum over the
+// range's rows n of dzq[n][lp] Q[n][k] + dzk[n][lp] K[n][k].  The rows go through shared memory in
+// tiles of DW_ROWS, the Q rows then the K rows of each, copied with 16-byte loads that are issued
+// one tile ahead (held in registers while the tile before is summed).  Thread (g, k) owns column k
+// and LPB (>= dzld) accumulators over the rows of parity g, in order; half 1 adds half 0's sums
+// last, so the summation order is fixed.  Grid (blocks, BH), NT threads, dw_smem_bytes of shared
+// memory.
 constexpr int DW_ROWS = 32;
-constexpr int DW_EPT = (64 * kMaxD + NT - 1) / NT;  // (lp, k) entries per thread, L P <= 64
 
-template <typename T>
+__host__ __device__ inline size_t dw_smem_bytes(int d, int dzld, int lpb, size_t elem)
+{
+    const size_t tiles = (size_t)DW_ROWS * d * elem + (size_t)DW_ROWS * dzld * sizeof(float);
+    const size_t red = (size_t)lpb * 128 * sizeof(float);
+    return tiles > red ? tiles : red;
+}
+
+template <typename T, int LPB>
 __global__ void __launch_bounds__(NT) k_dw_partial(Dims D, const T *__restrict__ Q, const T *__restrict__ K,
                                                     int64_t span, float *__restrict__ part)
 {
-    extern __shared__ float sm[];
-    const int d = D.d, LP = D.LP, E = LP * d;
-    float *xs = sm, *zs = sm + DW_ROWS * d;
+    extern __shared__ __align__(16) unsigned char dwsm[];
+    constexpr int XC = (DW_ROWS * kMaxD * (int)sizeof(T) / 16 + NT - 1) / NT;  // 16-byte pieces per thread
+    constexpr int ZC = (DW_ROWS * 64 * 4 / 16 + NT - 1) / NT;
+    const int d = D.d, LP = D.LP, ld = D.dzld;
+    const T *xs = reinterpret_cast<const T *>(dwsm);
+    const float *zs = reinterpret_cast<const float *>(dwsm + (size_t)DW_ROWS * d * sizeof(T));
+    const int k = threadIdx.x & 127, g = threadIdx.x >> 7;
     const int64_t bh = blockIdx.y;
     const int64_t r0 = (int64_t)blockIdx.x * span, r1 = min(D.N, r0 + span);
-    float acc[DW_EPT];
+    const int ntile = r1 > r0 ? (int)((r1 - r0 + DW_ROWS - 1) / DW_ROWS) : 0;
+    float acc[LPB];
 #pragma unroll
-    for (int j = 0; j < DW_EPT; ++j) acc[j] = 0.f;
-    for (int64_t n0 = r0; n0 < r1; n0 += DW_ROWS) {
+    for (int j = 0; j < LPB; ++j) acc[j] = 0.f;
+    uint4 px[XC], pz[ZC];
+    int nx = 0, nz = 0;  // pieces of the fetched tile
+    auto fetch = [&](int it) {
+        const int64_t n0 = r0 + (int64_t)(it >> 1) * DW_ROWS;
         const int cnt = (int)min((int64_t)DW_ROWS, r1 - n0);
-        for (int side = 0; side < 2; ++side) {
-            const T *X = (side ? K : Q) + (bh * D.N + n0) * d;
-            const float *Z = (side ? D.dzk : D.dzq) + (bh * D.N + n0) * LP;
-            __syncthreads();
-            for (int i = threadIdx.x; i < cnt * d; i += NT) xs[i] = ld_f(X, i);
-            for (int i = threadIdx.x; i < cnt * LP; i += NT) zs[i] = Z[i];
-            __syncthreads();
+        const uint4 *X = reinterpret_cast<const uint4 *>(((it & 1) ? K : Q) + (bh * D.N + n0) * d);
+        const uint4 *Z = reinterpret_cast<const uint4 *>(((it & 1) ? D.dzk : D.dzq) + (bh * D.N + n0) * ld);
+        nx = (int)((size_t)cnt * d * sizeof(T) / 16);
+        nz = cnt * ld / 4;
 #pragma unroll
-            for (int j = 0; j < DW_EPT; ++j) {
-                const int e = threadIdx.x + j * NT;
-                if (e < E) {
-                    const int lp = e / d, k = e - lp * d;
-                    float a = acc[j];
-                    for (int r = 0; r < cnt; ++r) a = fmaf(zs[r * LP + lp], xs[r * d + k], a);
-                    acc[j] = a;
+        for (int c = 0; c < XC; ++c) {
+            const int i = threadIdx.x + c * NT;
+            if (i < nx) px[c] = X[i];
+        }
+#pragma unroll
+        for (int c = 0; c < ZC; ++c) {
+            const int i = threadIdx.x + c * NT;
+            if (i < nz) pz[c] = Z[i];
+        }
+    };
+    if (ntile > 0) fetch(0);
+    for (int it = 0; it < 2 * ntile; ++it) {
+        const int cnt = (int)min((int64_t)DW_ROWS, r1 - (r0 + (int64_t)(it >> 1) * DW_ROWS));
+        __syncthreads();  // the previous tile is summed
+#pragma unroll
+        for (int c = 0; c < XC; ++c) {
+            const int i = threadIdx.x + c * NT;
+            if (i < nx) reinterpret_cast<uint4 *>(dwsm)[i] = px[c];
+        }
+#pragma unroll
+        for (int c = 0; c < ZC; ++c) {
+            const int i = threadIdx.x + c * NT;
+            if (i < nz) reinterpret_cast<uint4 *>(const_cast<float *>(zs))[i] = pz[c];
+        }
+        __syncthreads();
+        if (it + 1 < 2 * ntile) fetch(it + 1);  // in flight while this tile is summed
+        if (k < d) {
+            for (int r = g; r < cnt; r += 2) {
+                const float x = ld_f(xs, (int64_t)r * d + k);
+                const float4 *zr = reinterpret_cast<const float4 *>(zs + r * ld);
+#pragma unroll
+                for (int q = 0; q < LPB / 4; ++q) {
+                    if (4 * q < ld) {
+                        const float4 z4 = zr[q];
+                        acc[4 * q] = fmaf(z4.x, x, acc[4 * q]);
+                        acc[4 * q + 1] = fmaf(z4.y, x, acc[4 * q + 1]);
+                        acc[4 * q + 2] = fmaf(z4.z, x, acc[4 * q + 2]);
+                        acc[4 * q + 3] = fmaf(z4.w, x, acc[4 * q + 3]);
+                    }
                 }
             }
         }
     }
-    float *out = part + ((int64_t)bh * gridDim.x + blockIdx.x) * E;
+    __syncthreads();
+    float *red = reinterpret_cast<float *>(dwsm);  // [LPB][128], over the tiles
+    if (g == 0) {
 #pragma unroll
-    for (int j = 0; j < DW_EPT; ++j) {
-        const int e = threadIdx.x + j * NT;
-        if (e < E) out[e] = acc[j];
+        for (int j = 0; j < LPB; ++j) red[j * 128 + k] = acc[j];
+    }
+    __syncthreads();
+    if (g == 1 && k < d) {
+        float *out = part + ((int64_t)bh * gridDim.x + blockIdx.x) * (int64_t)LP * d;
+#pragma unroll
+        for (int j = 0; j < LPB; ++j)
+            if (j < LP) out[(int64_t)j * d + k] = red[j * 128 + k] + acc[j];
     }
 }
 
@@ -580,7 +634,7 @@ __global__ void __launch_bounds__(NT) k_bwd_query(Dims D, const T *__restrict__ 
     }
     __syncthreads();
     const float db = featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red,
-                                        D.dzq ? D.dzq + (bh * D.N + n0) * D.LP : nullptr, cnt);
+                                        D.dzq ? D.dzq + (bh * D.N + n0) * D.dzld : nullptr, cnt);
     T *dQb = dQ + bh * D.N * D.d;
     for (int i = threadIdx.x; i < cnt * D.d; i += NT) {
         const int t = i / D.d, c = i - t * D.d;
@@ -641,7 +695,7 @@ __global__ void __launch_bounds__(NT) k_bwd_key(Dims D, const T *__restrict__ K,
     }
     __syncthreads();
     const float db = featurise_backward(xs, D, ws, inv, us, fs, gs, fst, dz, dx, red,
-                                        D.dzk ? D.dzk + (bh * D.N + n0) * D.LP : nullptr, cnt);
+                                        D.dzk ? D.dzk + (bh * D.N + n0) * D.dzld : nullptr, cnt);
     T *dKb = dK + bh * D.N * D.d, *dVb = dV + bh * D.N * D.d;
 #pragma unroll
     for (int k = 0; k < KOUT; ++k) {
@@ -798,7 +852,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_q(Dims D, const T *__restrict
         }
         __syncthreads();
         db += featurise_backward(xq, D, ws, invq, us, fq, gs, fst, dz, dx, red,
-                                 D.dzq ? D.dzq + (bh * D.N + n0) * D.LP : nullptr, cnt);
+                                 D.dzq ? D.dzq + (bh * D.N + n0) * D.dzld : nullptr, cnt);
         for (int i = threadIdx.x; i < cnt * D.d; i += NT) {
             const int t = i / D.d, c = i - t * D.d;
             st_f(dQ + off, (n0 + t) * D.d + c, dx[t * dp + c]);
@@ -899,7 +953,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd_kv(Dims D, const T *__restric
         }
         __syncthreads();
         db += featurise_backward(xk, D, ws, invk, us, fk, gs, fst, dz, dx, red,
-                                 D.dzk ? D.dzk + (bh * D.N + n0) * D.LP : nullptr, cnt);
+                                 D.dzk ? D.dzk + (bh * D.N + n0) * D.dzld : nullptr, cnt);
 #pragma unroll
         for (int k = 0; k < KOUT; ++k) {
             const int o = threadIdx.x + k * NT;
@@ -977,13 +1031,21 @@ template <typename T>
 cudaError_t launch_dw(const Dims &D, const T *Q, const T *K, int nblk, float *part, float *dW, cudaStream_t st)
 {
     const int64_t span = (((D.N + nblk - 1) / nblk + gen::DW_ROWS - 1) / gen::DW_ROWS) * gen::DW_ROWS;
-    const size_t smem = (size_t)gen::DW_ROWS * (D.d + D.LP) * sizeof(float);
-    cudaError_t e = launch_kernel("dw_partial", gen::k_dw_partial<T>, dim3((unsigned)nblk, (unsigned)D.BH),
-                                  dim3(gen::NT), smem, st, D, Q, K, span, part);
+    const dim3 grid((unsigned)nblk, (unsigned)D.BH);
+    const int lpb = D.dzld <= 4 ? 4 : D.dzld <= 8 ? 8 : D.dzld <= 16 ? 16 : D.dzld <= 32 ? 32 : 64;
+    const size_t smem = gen::dw_smem_bytes(D.d, D.dzld, lpb, sizeof(T));
+    cudaError_t e;
+    switch (lpb) {
+        case 4: e = launch_kernel("dw_partial", gen::k_dw_partial<T, 4>, grid, dim3(gen::NT), smem, st, D, Q, K, span, part); break;
+        case 8: e = launch_kernel("dw_partial", gen::k_dw_partial<T, 8>, grid, dim3(gen::NT), smem, st, D, Q, K, span, part); break;
+        case 16: e = launch_kernel("dw_partial", gen::k_dw_partial<T, 16>, grid, dim3(gen::NT), smem, st, D, Q, K, span, part); break;
+        case 32: e = launch_kernel("dw_partial", gen::k_dw_partial<T, 32>, grid, dim3(gen::NT), smem, st, D, Q, K, span, part); break;
+        default: e = launch_kernel("dw_partial", gen::k_dw_partial<T, 64>, grid, dim3(gen::NT), smem, st, D, Q, K, span, part); break;
+    }
     if (e != cudaSuccess) return e;
     const int64_t E = (int64_t)D.LP * D.d;
-    dim3 grid((unsigned)std::min<int64_t>((E + 255) / 256, 64), (unsigned)D.BH);
-    return launch_kernel("dw_combine", gen::k_combine, grid, dim3(256), 0, st, (const float *)part, dW, E, nblk, 0);
+    const dim3 cgrid((unsigned)std::min<int64_t>((E + 255) / 256, 64), (unsigned)D.BH);
+    return launch_kernel("dw_combine", gen::k_combine, cgrid, dim3(256), 0, st, (const float *)part, dW, E, nblk, 0);
 }
 
 cudaError_t launch_dbeta_combine(const Dims &D, const float *part, int slots, float *dbeta, cudaStream_t st)

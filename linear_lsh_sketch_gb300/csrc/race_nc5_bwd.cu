@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(NTH, 1)
         // them whenever d(loss)/d(W) is asked for, and the others stay free of the code)
         auto store_dz = [&](int pr, const float (&dz)[2 * P]) {
             if (DB && Dm.dzq != nullptr && live) {
-                float *o = Dm.dzq + (bh * Dm.N + n0 + t) * Dm.LP + 2 * pr * P;
+                float *o = Dm.dzq + (bh * Dm.N + n0 + t) * Dm.dzld + 2 * pr * P;
 #pragma unroll
                 for (int j = 0; j < 2 * P; ++j)
                     if (2 * pr * P + j < Dm.LP) o[j] = dz[j] * inv;
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(NTH, 1)
         // d(loss)/d(W): table pair pr's dz / |k| of this K row (DB instances only)
         auto store_dz = [&](int pr, const float (&dz)[2 * P]) {
             if (DB && Dm.dzk != nullptr && t < cnt) {
-                float *o = Dm.dzk + (bh * Dm.N + n0 + t) * Dm.LP + 2 * pr * P;
+                float *o = Dm.dzk + (bh * Dm.N + n0 + t) * Dm.dzld + 2 * pr * P;
 #pragma unroll
                 for (int j = 0; j < 2 * P; ++j)
                     if (2 * pr * P + j < Dm.LP) o[j] = dz[j] * inv;
