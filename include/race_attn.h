@@ -79,8 +79,8 @@ typedef struct {
 
 /*
  * Bytes of scratch memory race_attn_fwd (is_bwd = 0), race_attn_bwd (is_bwd = 1) or
- * race_attn_bwd with a dW output (is_bwd = 2: also every row's dz / |x|, 8 L P bytes per token and
- * (b, h)) needs for this problem.  Returns 0 if the arguments are invalid.  Host function: it launches nothing,
+ * race_attn_bwd with a dW output (is_bwd = 2: also every row's dz / |x|, 8 ((L P + 3) & ~3)
+ * bytes per token and (b, h)) needs for this problem.  Returns 0 if the arguments are invalid.  Host function: it launches nothing,
  * but it queries the current device's multiprocessor count (152 when there is no device).
  */
 size_t race_attn_workspace_bytes(const race_shape *shape, int L, int P, int causal, int is_bwd);

@@ -477,6 +477,8 @@ int race_attn_bwd(const race_shape *shape, const void *Q, const void *K, const v
     if (want_dw) {  // the backward kernels also write every row's dz / |x|
         pl.D.dzq = (float *)((char *)workspace + pl.off_dzq);
         pl.D.dzk = (float *)((char *)workspace + pl.off_dzk);
+        if (pl.D.LP & 3)  // the rows' padding past L P, which not every kernel family writes, reads as 0
+            RACE_TRY(cudaMemsetAsync(pl.D.dzq, 0, pl.off_dwpart - pl.off_dzq, st));
     }
     if (pl.bf16)
         rc = backward_impl<__nv_bfloat16>(pl, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,

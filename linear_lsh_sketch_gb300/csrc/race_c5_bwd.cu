@@ -82,7 +82,7 @@ struct BwdLayout {
         dO = v + kbb;
         fq = dO + kbb;  // F'_Q [t][lr], one 64-column block
         ghi = fq + BLK;
-        glo = ghi + BLK;  // G operand [d rows][lr], one block each
+        glo = ghi + BLK;  // G operand [d rows][lr], hi and lo blocks (L R <= 32: lo in ghi's columns 32..63)
         whi = glo + BLK;  // W in pair layout (hi and lo blocks interleaved); wlo = its first lo block
         wlo = whi + WBLK;
         ncm = whi + 2 * (uint32_t)(D / 64) * WBLK;  // -c as a K-major N = 16 operand (rows 0, 1 = hi, lo)
@@ -765,7 +765,7 @@ struct QLayout {
         fk = dO + kbb;   // F_K [j][lr]
         fq = fk + BLK;   // F'_Q [t][lr]
         shi = fq + BLK;  // S operand [d rows][lr] (MN-major B of dO A^T)
-        slo = shi + BLK;
+        slo = shi + BLK;  // (L R <= 32: S lo sits in shi's columns 32..63 and this block is unused)
         whi = slo + BLK;  // W in pair layout (hi and lo blocks interleaved); wlo = its first lo block
         wlo = whi + WBLK;
         ncm = whi + 2 * (uint32_t)(D / 64) * WBLK;
